@@ -1,0 +1,312 @@
+"""Pins of the fp64 oracle against facts that do not come from the oracle itself.
+
+* RoPE: closed forms (composition, relative position, norm, identity at 0) and a
+  complex-multiplication formulation.
+* RMSNorm and the whole prefill: torch library routines (rms_norm,
+  scaled_dot_product_attention, complex RoPE) in float64.
+* Link: the special cases the method reduces to (k = chunk length is full recompute;
+  a single chunk with k = 0 is a plain prefill), chunk 1 reproduces its compile,
+  compile is offset invariant, and a brute-force per-token loop agrees.
+* Metadata: a hand-worked example and closed forms.
+* Planted mistakes: each pin is shown to fail when the oracle is broken on purpose.
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import pic_inputs as pi
+from oracle import pic_oracle as po
+from oracle import bruteforce as bf
+from tests import torch_reference as tr
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _weights(spec, gains="random"):
+    return pi.gen_weights(spec, gains=gains)
+
+
+@pytest.fixture(scope="module")
+def micro():
+    w = _weights(pi.MICRO_GQA)
+    return pi.MICRO_GQA, w, po.OracleModel(pi.MICRO_GQA, w)
+
+
+@pytest.fixture(scope="module")
+def tiny():
+    w = _weights(pi.TINY)
+    return pi.TINY, w, po.OracleModel(pi.TINY, w)
+
+
+def rel_err(a, b):
+    a, b = np.asarray(a, dtype=np.float64), np.asarray(b, dtype=np.float64)
+    return float(np.max(np.abs(a - b)) / max(1e-300, np.max(np.abs(b))))
+
+
+# ----------------------------------------------------------------------------- RoPE
+
+def test_rope_composition_relative_norm():
+    rng = np.random.default_rng(0)
+    D, base = 128, 500000.0
+    x = rng.standard_normal((7, 3, D))
+    p = np.array([0, 1, 5, 100, 4096, 50000, 50239])
+    d = np.array([3, 0, 17, 511, 9, 1, 2])
+    # R(d) R(p) = R(p + d)
+    assert np.allclose(po.rope(po.rope(x, p, base), d, base), po.rope(x, p + d, base), atol=1e-9)
+    # R(0) is the identity
+    assert np.array_equal(po.rope(x, np.zeros(7, dtype=int), base), x)
+    # |R(p) x| = |x|
+    assert np.allclose(np.linalg.norm(po.rope(x, p, base), axis=-1), np.linalg.norm(x, axis=-1))
+    # <R(p) q, R(p') k> depends only on p - p'
+    q, k = rng.standard_normal((1, 1, D)), rng.standard_normal((1, 1, D))
+    def dot(a, b):
+        return float(np.sum(po.rope(q, np.array([a]), base) * po.rope(k, np.array([b]), base)))
+    assert abs(dot(10, 3) - dot(1010, 1003)) < 1e-9
+    assert abs(dot(40000, 123) - dot(39877, 0)) < 1e-8
+
+
+def test_rope_matches_complex_multiplication():
+    rng = np.random.default_rng(1)
+    for D, base in ((64, 10000.0), (128, 500000.0), (16, 10000.0)):
+        x = rng.standard_normal((9, 2, D))
+        pos = np.array([0, 1, 2, 15, 16, 511, 512, 5183, 50239])
+        ref = tr.complex_rope(torch.from_numpy(x), torch.from_numpy(pos), base).numpy()
+        # angles up to 5e4 rad carry ~pos * 1e-16 rounding in fp64
+        assert rel_err(po.rope(x, pos, base), ref) < 1e-10
+
+
+def test_rmsnorm_matches_torch():
+    rng = np.random.default_rng(2)
+    x = rng.standard_normal((5, 256)) * 3
+    g = rng.standard_normal(256)
+    ref = torch.nn.functional.rms_norm(torch.from_numpy(x), (256,), torch.from_numpy(g), 1e-5).numpy()
+    assert rel_err(po.rms_norm(x, g, 1e-5), ref) < 1e-14
+    # closed form: a constant row c maps to c/sqrt(c^2+eps) * g
+    c = np.full((1, 8), 2.0)
+    assert np.allclose(po.rms_norm(c, np.ones(8), 0.0), np.ones((1, 8)))
+
+
+def test_softmax_weights_sum_to_one():
+    rng = np.random.default_rng(3)
+    q = rng.standard_normal((6, 4, 16))
+    k = rng.standard_normal((9, 2, 16))
+    v = np.ones((9, 2, 16))
+    qp, kp = np.array([0, 2, 3, 5, 7, 8]), np.arange(9)
+    assert np.allclose(po.causal_attention(q, k, v, qp, kp), 1.0)
+    # a row that sees only itself returns that row's value
+    v2 = rng.standard_normal((9, 2, 16))
+    out = po.causal_attention(q, k, v2, qp, kp)
+    assert np.allclose(out[0, 0], v2[0, 0]) and np.allclose(out[0, 3], v2[0, 1])
+
+
+# ----------------------------------------------------------------------------- whole model vs library routines
+
+@pytest.mark.parametrize("name", ["micro", "tiny"])
+def test_prefill_matches_torch_library(name, micro, tiny):
+    spec, w, model = {"micro": micro, "tiny": tiny}[name]
+    toks = pi.gen_tokens(37 if name == "micro" else 80, spec.vocab, 99, name)
+    got = po.full_prefill(model, toks)
+    hid, logits, ks, vs = tr.prefill(spec, w, toks)
+    assert rel_err(got.hidden, hid.numpy()) < 1e-11
+    assert rel_err(model.logits(got.hidden[-1:]), logits.numpy()) < 1e-11
+    for l in range(spec.n_layers):
+        assert rel_err(got.k[l], ks[l].numpy()) < 1e-11
+        assert rel_err(got.v[l], vs[l].numpy()) < 1e-11
+
+
+# ----------------------------------------------------------------------------- link special cases
+
+def _link(spec, model, chunks, queries, k, n_dummy=0, num_blocks=256, all_logits=False):
+    st = po.OracleStore(model, num_blocks)
+    cids = st.compile_many(chunks, n_dummy)
+    out = st.link([(cids, q) for q in queries], k, all_logits=all_logits)
+    return st, cids, out
+
+
+def test_full_recompute_invariant(tiny, micro):
+    """k >= every chunk length: link equals a plain prefill of the concatenated prompt."""
+    for spec, w, model in (tiny, micro):
+        lens = [64, 64, 64, 64] if spec is pi.TINY else [5, 16, 19]
+        chunks = [pi.gen_tokens(L, spec.vocab, 7, i) for i, L in enumerate(lens)]
+        q = pi.gen_tokens(16 if spec is pi.TINY else 6, spec.vocab, 8)
+        _, _, out = _link(spec, model, chunks, [q], k=max(lens), all_logits=True)
+        fr = po.full_prefill(model, np.concatenate(chunks + [q]))
+        assert rel_err(out.hidden[0], fr.hidden[-len(q):]) < 1e-11
+        assert rel_err(out.logits[0], model.logits(fr.hidden[-len(q):])) < 1e-11
+        for l in range(spec.n_layers):
+            assert rel_err(out.k[0][l], fr.k[l]) < 1e-11
+            assert rel_err(out.v[0][l], fr.v[l]) < 1e-11
+
+
+def test_single_chunk_k0_is_plain_prefill(tiny):
+    spec, w, model = tiny
+    chunk = pi.gen_tokens(64, spec.vocab, 11)
+    q = pi.gen_tokens(16, spec.vocab, 12)
+    _, _, out = _link(spec, model, [chunk], [q], k=0)
+    fr = po.full_prefill(model, np.concatenate([chunk, q]))
+    assert rel_err(out.hidden[0], fr.hidden[-16:]) < 1e-11
+    assert rel_err(out.logits[0], model.logits(fr.hidden[-1:])) < 1e-11
+
+
+def test_chunk1_recompute_equals_compile(tiny):
+    spec, w, model = tiny
+    chunks = [pi.gen_tokens(64, spec.vocab, 13, i) for i in range(3)]
+    q = pi.gen_tokens(16, spec.vocab, 14)
+    st, cids, out = _link(spec, model, chunks, [q], k=2)
+    for l in range(spec.n_layers):
+        assert rel_err(out.k[0][l][:2], st.chunks[cids[0]].k[l][:2]) < 1e-11
+        assert rel_err(out.v[0][l][:2], st.chunks[cids[0]].v[l][:2]) < 1e-11
+        # layer 0 K/V depend on the token alone; deeper layers of later chunks change
+        # once their first rows see the prefix
+        d = rel_err(out.k[0][l][2:4], st.chunks[cids[1]].k[l][:2])
+        assert (d < 1e-12) if l == 0 else (d > 1e-6)
+
+
+def test_compile_offset_invariance(tiny):
+    """Pre-RoPE KV of an isolated chunk does not depend on where its positions start."""
+    spec, w, model = tiny
+    chunk = pi.gen_tokens(40, spec.vocab, 15)
+    ref = po.full_prefill(model, chunk)
+    for delta in (1, 517, 20000):
+        shifted = po.run_jobs(model, [po.SeqJob(chunk, np.arange(40), None, pos0=delta)])[0]
+        for l in range(spec.n_layers):
+            assert rel_err(shifted.k[l], ref.k[l]) < 1e-10
+            assert rel_err(shifted.v[l], ref.v[l]) < 1e-10
+
+
+def test_legolink0_compile_drops_dummies(tiny):
+    spec, w, model = tiny
+    chunk = pi.gen_tokens(30, spec.vocab, 16)
+    (k0, v0), = po.compile_chunks(model, [chunk], n_dummy=4)
+    fr = po.full_prefill(model, np.concatenate([np.zeros(4, dtype=np.int32), chunk]))
+    for l in range(spec.n_layers):
+        assert k0[l].shape[0] == 30
+        assert rel_err(k0[l], fr.k[l][4:]) < 1e-12
+    # the dummies matter: without them the KV differs
+    (k1, _), = po.compile_chunks(model, [chunk], n_dummy=0)
+    assert rel_err(k1[1], k0[1]) > 1e-6
+
+
+# ----------------------------------------------------------------------------- brute-force twin
+
+@pytest.mark.parametrize("k,n_dummy,lens", [(2, 0, [5, 16, 19]), (0, 4, [7, 9]), (17, 0, [18, 3, 20])])
+def test_matches_bruteforce(micro, k, n_dummy, lens):
+    spec, w, model = micro
+    chunks = [pi.gen_tokens(L, spec.vocab, 21, i) for i, L in enumerate(lens)]
+    q = pi.gen_tokens(5, spec.vocab, 22)
+    _, _, out = _link(spec, model, chunks, [q], k=k, n_dummy=n_dummy)
+    bm = bf.BruteModel(spec, w)
+    comp = [bf.brute_compile(bm, c, n_dummy) for c in chunks]
+    ref = bf.brute_link(bm, comp, chunks, q, k)
+    assert list(out.meta[0].selected) == ref["selected"]
+    assert rel_err(out.hidden[0], np.array(ref["hidden"])) < 1e-12
+    assert rel_err(out.logits[0][0], np.array(ref["logits"])) < 1e-12
+    for l in range(spec.n_layers):
+        assert rel_err(out.k[0][l], np.array(ref["k"][l])) < 1e-12
+        assert rel_err(out.v[0][l], np.array(ref["v"][l])) < 1e-12
+
+
+# ----------------------------------------------------------------------------- metadata
+
+def test_metadata_hand_example():
+    g = json.load(open(os.path.join(GOLD, "tiny_link_metadata.json")))
+    st = po.OracleStore(None, 64)
+    cids = [st._add_chunk(np.zeros(L, dtype=np.int32), [], []) for L in g["chunk_lengths"]]
+    assert [st.chunks[c].blocks for c in cids] == g["compile_blocks"]
+    m, = st.plan([(cids, g["query_length"])], g["k"])
+    assert m.private_blocks.tolist() == g["private_blocks"]
+    assert m.selected.tolist() == g["selected"]
+    assert m.slots.tolist() == g["slots"]
+    assert m.page_table.tolist() == g["page_table"]
+    assert m.page_pos.tolist() == g["page_pos"]
+    assert m.page_len.tolist() == g["page_len"]
+
+
+@pytest.mark.parametrize("k", [0, 1, 2, 15, 16, 17, 32, 512])
+def test_metadata_closed_forms(k):
+    lens = [512, 37, 16, 1, 100]
+    lq = 21
+    st = po.OracleStore(None, 1000)
+    cids = [st._add_chunk(np.zeros(L, dtype=np.int32), [], []) for L in lens]
+    m, = st.plan([(cids, lq)], k)
+    ceil = lambda a: -(-a // 16)
+    assert len(m.selected) == sum(min(k, L) for L in lens) + lq
+    assert len(m.page_table) == sum(ceil(L) for L in lens) + ceil(lq)
+    assert len(m.private_blocks) == sum(ceil(min(k, L)) for L in lens) + ceil(lq)
+    assert np.all(np.diff(m.selected) > 0)
+    assert sum(m.page_len) == sum(lens) + lq
+    # every selected row's slot lies in the page that holds its position
+    for s, slot in zip(m.selected, m.slots):
+        j = int(np.searchsorted(m.page_pos, s, side="right") - 1)
+        assert slot // 16 == m.page_table[j] and slot % 16 == s - m.page_pos[j]
+        assert slot // 16 in set(m.private_blocks.tolist())
+    # shared blocks of the chunks stay in the table past each chunk's private prefix
+    off = 0
+    for c, L in zip(cids, lens):
+        j0 = int(np.searchsorted(m.page_pos, off))
+        for j in range(ceil(min(k, L)), ceil(L)):
+            assert m.page_table[j0 + j] == st.chunks[c].blocks[j]
+        off += L
+
+
+def test_allocator_all_or_nothing_and_refcounts():
+    st = po.OracleStore(None, 10)
+    a = st._add_chunk(np.zeros(64, dtype=np.int32), [], [])      # blocks 0-3
+    b = st._add_chunk(np.zeros(40, dtype=np.int32), [], [])      # blocks 4-6
+    free_before = set(st.free)
+    with pytest.raises(po.OutOfBlocks):
+        st.plan([([a, b], 16), ([a, b], 16)], 16)                 # needs 6, only 3 free
+    assert st.free == free_before
+    m, = st.plan([([a, b], 16)], 16)
+    assert m.private_blocks.tolist() == [7, 8, 9]
+    st.requests[0] = (m.private_blocks.tolist(), [a, b])
+    st.chunks[a].refs += 1
+    st.chunks[b].refs += 1
+    st.release_chunk(a)                                            # still referenced by the request
+    assert a in st.chunks and not (set(range(4)) & st.free)
+    st.release_request(0)
+    assert a not in st.chunks and set(range(4)) <= st.free and {7, 8, 9} <= st.free
+
+
+# ----------------------------------------------------------------------------- planted mistakes
+
+def test_pins_catch_planted_mistakes(monkeypatch, micro):
+    """Each plausible slip in the oracle makes at least one pin fail."""
+    spec, w, model = micro
+    toks = pi.gen_tokens(23, spec.vocab, 31)
+    hid_ref = tr.prefill(spec, w, toks)[0].numpy()
+
+    def fails(patch_target, bad):
+        with monkeypatch.context() as m:
+            m.setattr(po, patch_target, bad)
+            got = po.full_prefill(po.OracleModel(spec, w), toks)
+        return rel_err(got.hidden, hid_ref) > 1e-6
+
+    good_rope, good_att = po.rope, po.causal_attention
+
+    def rope_wrong_sign(x, pos, base):
+        return good_rope(x, -pos, base)
+
+    def rope_interleaved(x, pos, base):
+        y = x.reshape(*x.shape[:-1], -1, 2).swapaxes(-1, -2).reshape(x.shape)
+        return good_rope(y, pos, base)
+
+    def att_strict_mask(q, k, v, qp, kp):
+        out = good_att(q, k, v, qp, kp + 0.5)  # a row no longer sees itself
+        out[0] = 0.0
+        return out
+
+    def att_wrong_group(q, k, v, qp, kp):
+        G = k.shape[1]
+        return good_att(q, k[:, ::-1].copy(), v[:, ::-1].copy(), qp, kp) if G > 1 else good_att(q, k, v, qp, kp)
+
+    assert fails("rope", rope_wrong_sign)
+    assert fails("rope", rope_interleaved)
+    assert fails("causal_attention", att_strict_mask)
+    assert fails("causal_attention", att_wrong_group)
+    with monkeypatch.context() as m:
+        m.setattr(po, "silu", lambda x: x)
+        assert rel_err(po.full_prefill(po.OracleModel(spec, w), toks).hidden, hid_ref) > 1e-6
