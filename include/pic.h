@@ -1,0 +1,226 @@
+/*
+ * pic.h — C ABI of the position-independent KV link library (GB300, sm_103a).
+ *
+ * The library implements position-independent context caching (PIC) as two steps:
+ *
+ *   compile  prefill one immutable chunk on its own, with position ids starting at 0,
+ *            and store its per-layer K (before RoPE) and V in 16-token pages.
+ *            ("EPIC: Efficient Position-Independent Caching for Serving Large Language
+ *            Models", summary page, Approach.)
+ *   link     LegoLink-k: for a prompt made of compiled chunks plus a query suffix,
+ *            recompute only the first k tokens of every chunk and all query tokens,
+ *            through every layer, attending causally to the reused KV of every
+ *            earlier chunk; RoPE is applied to each key at attention time from its
+ *            absolute position. Each chunk's first ceil(k/16) pages become
+ *            request-private copies; every other page stays shared.
+ *            (EPIC summary page, Approach; "MEPIC: Memory Efficient Position
+ *            Independent Caching for LLM Serving", abstract.)
+ *
+ * Conventions
+ *   - Every call returns pic_status; nothing throws or aborts across the ABI.
+ *     pic_last_error() gives a message for the last failure on the calling thread.
+ *   - A failing call leaves no partial state: block allocation is all-or-nothing.
+ *   - Device pointers passed in (weights, KV pools, outputs) are BORROWED: the caller
+ *     allocates them, keeps them alive while the model/store uses them, and frees them.
+ *     Handles (pic_model*, pic_store*, pic_chunk, pic_request) are OWNED by the library
+ *     and freed by the matching destroy/release call.
+ *   - GPU work is asynchronous on the caller's stream (cudaStream_t; NULL = legacy
+ *     default stream). Host-side metadata outputs are valid when the call returns.
+ *     Device-side wait timeouts are reported by pic_sync().
+ *   - Handles are not thread-safe: one thread at a time per store.
+ *   - Block size is 16 tokens. KV pool layout (per pool, K and V alike):
+ *       [n_layers][num_blocks + 1][n_kv_heads][16][head_dim] in the model dtype.
+ *     Block index num_blocks is the store's own scratch page (dummy-prefix rows
+ *     during a LegoLink-0 compile); ids 0..num_blocks-1 are allocated to chunks and
+ *     requests. K is stored without positional encoding.
+ */
+#ifndef PIC_H_
+#define PIC_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* pic_stream_t; /* identical to cudaStream_t */
+
+typedef enum {
+  PIC_OK = 0,
+  PIC_ERR_INVALID_ARG = 1,     /* bad size, pointer, handle or layout */
+  PIC_ERR_OUT_OF_BLOCKS = 2,   /* the pool cannot hold the new blocks; nothing changed */
+  PIC_ERR_CUDA = 3,            /* a CUDA runtime call failed (message in pic_last_error) */
+  PIC_ERR_DEVICE_TIMEOUT = 4,  /* a kernel gave up a bounded wait; its outputs are invalid */
+  PIC_ERR_CAPACITY = 5,        /* the call exceeds a capacity fixed at store creation */
+  PIC_ERR_UNSUPPORTED = 6      /* shape/dtype combination not built */
+} pic_status;
+
+typedef enum { PIC_F32 = 0, PIC_BF16 = 1 } pic_dtype;
+
+typedef int32_t pic_chunk;    /* > 0 when valid */
+typedef int32_t pic_request;  /* > 0 when valid */
+
+/* Llama-style pre-norm decoder: RMSNorm, rotate-half RoPE (theta_i = base^(-2i/D)),
+ * GQA (query head h reads KV head h / (n_heads / n_kv_heads)), SwiGLU MLP, final
+ * RMSNorm, untied LM head, no biases. */
+typedef struct {
+  int32_t n_layers;
+  int32_t d_model;
+  int32_t n_heads;
+  int32_t n_kv_heads;
+  int32_t head_dim;   /* 64 or 128 */
+  int32_t ffn_dim;
+  int32_t vocab;
+  double rope_base;
+  float rms_eps;
+  int32_t dtype;      /* pic_dtype of weights, KV pools and GEMM operands; accumulation is fp32 */
+  int32_t block_size; /* must be 16 */
+} pic_model_config;
+
+/* Device pointers (borrowed). Matrices are row-major [out][in] (nn.Linear layout) in
+ * the model dtype; norm gains are fp32. The per-layer arrays are HOST arrays of
+ * n_layers device pointers; the library copies the arrays at model creation. */
+typedef struct {
+  const void* embed;              /* [vocab][d_model] */
+  const void* lm_head;            /* [vocab][d_model] */
+  const float* final_norm;        /* [d_model] */
+  const float* const* attn_norm;  /* per layer [d_model] */
+  const float* const* mlp_norm;   /* per layer [d_model] */
+  const void* const* w_qkv;       /* per layer [(n_heads + 2 n_kv_heads) head_dim][d_model]: Q rows, K rows, V rows */
+  const void* const* w_o;         /* per layer [d_model][n_heads head_dim] */
+  const void* const* w_gate_up;   /* per layer [2 ffn_dim][d_model]: gate rows, then up rows */
+  const void* const* w_down;      /* per layer [d_model][ffn_dim] */
+} pic_weights;
+
+typedef struct pic_model pic_model;
+typedef struct pic_store pic_store;
+
+/* Capacities fixed at store creation (they size the library-owned device workspace). */
+typedef struct {
+  int32_t num_blocks;        /* allocatable pages; pools hold num_blocks + 1 */
+  int32_t max_rows;          /* rows computed by one compile or link call (all requests) */
+  int32_t max_requests;      /* requests (or chunks) in one call */
+  int32_t max_positions;     /* longest linked sequence, in tokens */
+  int32_t max_logit_rows;    /* rows of logits one link may produce */
+} pic_store_config;
+
+/* One request of a link batch. `chunks` and `query` are host arrays. */
+typedef struct {
+  const pic_chunk* chunks;   /* compiled chunks in prompt order (repeats allowed) */
+  int32_t n_chunks;
+  const int32_t* query;      /* query-suffix token ids */
+  int32_t query_len;         /* >= 1 */
+} pic_link_request;
+
+/* Host metadata of a linked request; arrays are owned by the store and stay valid
+ * until the request is released. All int32. */
+typedef struct {
+  int32_t n_selected;
+  const int32_t* selected;        /* absolute positions of recomputed rows, ascending */
+  const int32_t* slots;           /* block_id * 16 + row of each selected row */
+  int32_t n_pages;
+  const int32_t* page_table;      /* physical block of each page, in position order */
+  const int32_t* page_pos;        /* absolute position of row 0 of each page */
+  const int32_t* page_len;        /* valid rows of each page (ragged chunk tails) */
+  int32_t n_private;
+  const int32_t* private_blocks;  /* blocks owned by this request (chunk privates, then query) */
+} pic_request_info;
+
+const char* pic_status_string(pic_status s);
+const char* pic_last_error(void);
+/* Library version string and the CUDA arch it was built for ("sm_103a"). */
+const char* pic_version(void);
+
+/* Creates a model on the current CUDA device. Validates the config (head_dim 64/128,
+ * n_heads % n_kv_heads == 0, d_model % 64 == 0, dims multiples of 8) and, for bf16,
+ * prepares TMA descriptors over the weights. */
+pic_status pic_model_create(const pic_model_config* cfg, const pic_weights* w, pic_model** out);
+pic_status pic_model_destroy(pic_model* m);
+
+/* Creates a paged store over caller-owned K/V pools (layout in the header comment).
+ * Allocates the library-owned device workspace and the RoPE table (fp64 angles on
+ * the host, stored fp32). */
+pic_status pic_store_create(pic_model* m, const pic_store_config* cfg, void* k_pool, void* v_pool,
+                            pic_store** out);
+pic_status pic_store_destroy(pic_store* s);
+int32_t pic_store_free_blocks(const pic_store* s);
+
+/* compile: prefill `n_chunks` chunks independently (each from position 0, behind
+ * n_dummy dummy tokens of id 0 whose KV is then discarded; n_dummy in 0..16) and store
+ * each in ceil(L/16) blocks, lowest free ids first, in chunk order. tokens[i] are host
+ * arrays of lens[i] >= 1 ids. Each new chunk has refcount 1. */
+pic_status pic_compile(pic_store* s, const int32_t* const* tokens, const int32_t* lens, int32_t n_chunks,
+                       int32_t n_dummy, pic_stream_t stream, pic_chunk* out_chunks);
+
+/* Stores externally produced chunk KV as if compiled: k, v are DEVICE arrays
+ * [n_layers][n_tokens][n_kv_heads][head_dim] (pre-RoPE K) in the model dtype, copied
+ * into ceil(n_tokens/16) new blocks. tokens (host) are kept for link recomputation. */
+pic_status pic_chunk_import(pic_store* s, const int32_t* tokens, int32_t n_tokens, const void* k, const void* v,
+                            pic_stream_t stream, pic_chunk* out_chunk);
+
+/* link (LegoLink-k) over a batch of requests. Per request, in order: each chunk gets
+ * ceil(min(k, L_i)/16) private blocks (copies of its first shared blocks), then
+ * ceil(query_len/16) query blocks. Selected rows = first min(k, L_i) rows of every
+ * chunk + all query rows, at contiguous absolute positions. Recomputed pre-RoPE K/V
+ * are written into the private/query blocks of every layer.
+ * Outputs (device, caller-owned, fp32):
+ *   hidden_out [sum query_len][d_model]  final-normed hidden of every query row;
+ *   logits_out [n_reqs][vocab] (last query row per request), or
+ *              [sum query_len][vocab] when all_logits != 0.
+ * out_requests (host, n_reqs) receives the request handles. */
+pic_status pic_link(pic_store* s, const pic_link_request* reqs, int32_t n_reqs, int32_t k, int32_t all_logits,
+                    float* hidden_out, float* logits_out, pic_stream_t stream, pic_request* out_requests);
+
+pic_status pic_request_get_info(const pic_store* s, pic_request r, pic_request_info* out);
+/* Blocks of a chunk (owned by the store, valid while the chunk lives). */
+pic_status pic_chunk_get_blocks(const pic_store* s, pic_chunk c, int32_t* n_blocks, const int32_t** blocks);
+
+/* Drops the caller's reference; blocks return to the pool when no request uses the chunk. */
+pic_status pic_release_chunk(pic_store* s, pic_chunk c);
+/* Frees the request's private and query blocks and drops its chunk references. */
+pic_status pic_release_request(pic_store* s, pic_request r);
+
+/* Waits for the stream and reports PIC_ERR_DEVICE_TIMEOUT if any kernel gave up a
+ * bounded wait since the last pic_sync (the flag is then cleared). */
+pic_status pic_sync(pic_store* s, pic_stream_t stream);
+
+/* ------------------------------------------------------------------ kernel-level calls
+ * Single steps of the link path, exposed for testing and profiling. All pointers are
+ * device pointers unless stated; all work is async on `stream`.
+ */
+
+/* Bytes of scratch pic_op_gemm needs for this shape (split-K partial sums). */
+size_t pic_op_gemm_scratch_bytes(int32_t dtype, int32_t N, int32_t K, int32_t T);
+/* Y[T][N] (fp32, overwritten) = X[T][K] . W[N][K]^T, both operands in `dtype`.
+ * bf16 runs on the tcgen05 tensor-core kernel (K % 64 == 0, N % 128 == 0, 16-byte
+ * aligned rows); fp32 on the SIMT kernel. scratch: caller-owned device buffer of at
+ * least pic_op_gemm_scratch_bytes(...) bytes. */
+pic_status pic_op_gemm(int32_t dtype, const void* W, const void* X, float* Y, int32_t N, int32_t K, int32_t T,
+                       void* scratch, size_t scratch_bytes, pic_stream_t stream);
+
+/* Sparse-query paged attention with fused RoPE for ONE sequence of pages:
+ * out[t][h] = softmax_u( RoPE(q[t][h], q_pos[t]) . RoPE(K[u][g], pos(u)) / sqrt(D) ) V[u][g]
+ * over every key u of the listed pages with pos(u) <= q_pos[t], g = h / (H/G).
+ * q, out: [T][H][D]; q_pos: HOST [T] (ascending); pages: HOST arrays of n_pages
+ * (block, position of row 0, valid rows); k_layer/v_layer: one layer of the pools
+ * ([pool_blocks][G][16][D]); every page block must be < pool_blocks. rope_cs: device
+ * float2 [rope_positions][D/2] (cos, sin), e.g. from pic_op_rope_table; every position
+ * must be < rope_positions. Scratch as reported by pic_op_attention_scratch_bytes. */
+size_t pic_op_attention_scratch_bytes(int32_t T, int32_t n_heads, int32_t n_kv_heads, int32_t head_dim,
+                                      int32_t n_pages);
+pic_status pic_op_attention(int32_t dtype, int32_t T, int32_t n_heads, int32_t n_kv_heads, int32_t head_dim,
+                            const void* q, const int32_t* q_pos_host, const void* k_layer, const void* v_layer,
+                            const int32_t* page_block_host, const int32_t* page_pos_host,
+                            const int32_t* page_len_host, int32_t n_pages, int32_t pool_blocks,
+                            const void* rope_cs, int32_t rope_positions, void* out, void* scratch,
+                            size_t scratch_bytes, pic_stream_t stream);
+
+/* Fills a device float2 table [n_pos][head_dim/2] with (cos, sin)(p * base^(-2i/D)),
+ * angles formed in fp64 on the host. */
+pic_status pic_op_rope_table(int32_t n_pos, int32_t head_dim, double base, void* out, pic_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PIC_H_ */

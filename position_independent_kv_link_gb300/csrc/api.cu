@@ -1,0 +1,677 @@
+// C ABI: model and paged store, compile, link (LegoLink-k), release, kernel-level calls.
+//
+// Host-side work here is the integer bookkeeping of the method: the block allocator
+// (lowest free id first, all-or-nothing), chunk and request tables with reference
+// counts, the selected-row list, the per-request page tables and the slot mapping.
+// Every arithmetic step of the forward pass runs in the library's CUDA kernels.
+//
+// Method sources: "EPIC: Efficient Position-Independent Caching for Serving Large
+// Language Models" (summary page: summary line, Approach, Measured effects table) for
+// compile/link, LegoLink-k and LegoLink-0; "MEPIC: Memory Efficient Position
+// Independent Caching for LLM Serving" (abstract) for page-aligned chunk KV, the
+// request-specific first block, shared remaining blocks and RoPE fused in attention.
+#include <algorithm>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <memory>
+#include <set>
+
+#include "pic_internal.h"
+
+namespace pic {
+
+static thread_local std::string g_last_error;
+void set_error(const std::string& msg) { g_last_error = msg; }
+pic_status fail(pic_status s, const std::string& msg) {
+  g_last_error = msg;
+  return s;
+}
+
+}  // namespace pic
+
+using namespace pic;
+
+struct pic_model {
+  pic_model_config cfg{};
+  const void* embed = nullptr;
+  const void* lm_head = nullptr;
+  const float* final_norm = nullptr;
+  std::vector<const float*> attn_norm, mlp_norm;
+  std::vector<const void*> wqkv, wo, wgu, wdown;
+  int device = 0;
+  int num_sms = 0;
+  int qkv_dim() const { return (cfg.n_heads + 2 * cfg.n_kv_heads) * cfg.head_dim; }
+};
+
+namespace {
+
+struct Chunk {
+  std::vector<int32_t> tokens;
+  std::vector<int32_t> blocks;
+  int refs = 1;
+};
+
+struct Request {
+  std::vector<int32_t> chunk_ids;
+  std::vector<int32_t> selected, slots, page_table, page_pos, page_len, private_blocks;
+};
+
+// One forward pass over a set of rows grouped in sequences (compile: chunks; link: requests).
+struct Batch {
+  std::vector<int> tok, pos, slot, out_row, lg_row;
+  std::vector<int> pblk, ppos, plen;
+  std::vector<int> seq_row_begin, seq_row_end, seq_page_begin, seq_page_end;
+  std::vector<int> copy_pairs;
+  int n_hidden = 0, n_lg = 0;
+  bool compile = false;
+  int rows() const { return (int)tok.size(); }
+  void begin_seq() {
+    seq_row_begin.push_back(rows());
+    seq_page_begin.push_back((int)pblk.size());
+  }
+  void end_seq() {
+    seq_row_end.push_back(rows());
+    seq_page_end.push_back((int)pblk.size());
+  }
+  void row(int t, int p, int s) {
+    tok.push_back(t);
+    pos.push_back(p);
+    slot.push_back(s);
+    out_row.push_back(-1);
+    lg_row.push_back(-1);
+  }
+  void page(int b, int p, int l) {
+    pblk.push_back(b);
+    ppos.push_back(p);
+    plen.push_back(l);
+  }
+};
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace
+
+struct pic_store {
+  pic_model* m = nullptr;
+  pic_store_config cfg{};
+  void* k_pool = nullptr;
+  void* v_pool = nullptr;
+  std::set<int32_t> free;
+  std::map<int32_t, Chunk> chunks;
+  std::map<int32_t, Request> requests;
+  int32_t next_chunk = 1, next_request = 1;
+
+  // library-owned device workspace (one allocation)
+  char* ws = nullptr;
+  float* h = nullptr;
+  void* x = nullptr;
+  void* q = nullptr;
+  void* attn = nullptr;
+  void* act = nullptr;
+  void* lm_x = nullptr;
+  float* part = nullptr;
+  size_t part_floats = 0;
+  float* att_o = nullptr;
+  float* att_ml = nullptr;
+  int att_parts_cap = 0;
+  int32_t* meta_d = nullptr;
+  size_t meta_cap = 0;  // int32 elements
+  float2* rope_cs = nullptr;
+  int32_t* meta_h = nullptr;  // pinned staging
+  cudaEvent_t meta_ev = nullptr;
+  bool meta_ev_pending = false;
+
+  int scratch_block() const { return cfg.num_blocks; }
+  int blocks_total() const { return cfg.num_blocks + 1; }
+  size_t block_bytes() const {
+    const auto& c = m->cfg;
+    return (size_t)c.n_kv_heads * kBlock * c.head_dim * dtype_size(c.dtype);
+  }
+  size_t layer_bytes() const { return block_bytes() * blocks_total(); }
+  void* k_layer(int l) const { return (char*)k_pool + layer_bytes() * l; }
+  void* v_layer(int l) const { return (char*)v_pool + layer_bytes() * l; }
+  int att_blocks_cap() const { return cfg.max_rows / kBlock + cfg.max_requests + 2; }
+
+  std::vector<int32_t> take(int n) {
+    std::vector<int32_t> ids;
+    auto it = free.begin();
+    for (int i = 0; i < n; ++i) ids.push_back(*it++);
+    for (int32_t b : ids) free.erase(b);
+    return ids;
+  }
+  void give(const std::vector<int32_t>& ids) { free.insert(ids.begin(), ids.end()); }
+};
+
+namespace {
+
+int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+int gemm_splits(const pic_store* s, int N, int K, int T) {
+  if (s->m->cfg.dtype != PIC_BF16 || !tc_gemm_supported(N, K, T)) return 1;
+  const size_t cap = s->part_floats / ((size_t)T * N);
+  return tc_gemm_splits(N, K, T, s->m->num_sms, (int)std::max<size_t>(1, std::min<size_t>(cap, 16)));
+}
+
+pic_status gemm(const pic_store* s, const void* W, const void* X, float* part, int N, int K, int T, int splits,
+                cudaStream_t st) {
+  if (s->m->cfg.dtype == PIC_BF16 && tc_gemm_supported(N, K, T))
+    return tc_gemm_run(W, X, part, N, K, T, splits, st);
+  launch_gemm_simt(s->m->cfg.dtype, W, X, part, N, K, T, splits, st);
+  return PIC_OK;
+}
+
+// Uploads the batch metadata and runs embedding, every layer, and (link) the LM head.
+pic_status run_forward(pic_store* s, const Batch& b, float* hidden_out, float* logits_out, cudaStream_t st) {
+  const pic_model_config& c = s->m->cfg;
+  const int T = b.rows();
+  const int dt = c.dtype;
+  const int H = c.n_heads, G = c.n_kv_heads, D = c.head_dim, d = c.d_model, F = c.ffn_dim;
+  if (T > s->cfg.max_rows) return fail(PIC_ERR_CAPACITY, "rows exceed max_rows");
+  if (b.n_lg > s->cfg.max_logit_rows) return fail(PIC_ERR_CAPACITY, "logit rows exceed max_logit_rows");
+  if ((int)b.seq_row_begin.size() > s->cfg.max_requests + 1)
+    return fail(PIC_ERR_CAPACITY, "sequences exceed max_requests");
+
+  // attention work plan
+  AttnPlanInput pin;
+  pin.seq_row_begin = b.seq_row_begin;
+  pin.seq_row_end = b.seq_row_end;
+  pin.seq_page_begin = b.seq_page_begin;
+  pin.seq_page_end = b.seq_page_end;
+  pin.row_pos = &b.pos;
+  pin.page_pos = &b.ppos;
+  pin.G = G;
+  pin.num_sms = s->m->num_sms;
+  std::vector<AttnItem> items;
+  std::vector<AttnCombine> combs;
+  int n_parts = 0;
+  plan_attention(pin, items, combs, n_parts);
+  if (n_parts > s->att_parts_cap) return fail(PIC_ERR_CAPACITY, "attention split plan exceeds workspace");
+
+  // pack metadata: tok pos slot out lg | pblk ppos plen | copies | items | combines
+  const size_t P = b.pblk.size(), NC = b.copy_pairs.size();
+  const size_t n_int = 5 * (size_t)T + 3 * P + NC + items.size() * 6 + combs.size() * 5;
+  if (n_int > s->meta_cap) return fail(PIC_ERR_CAPACITY, "metadata exceeds workspace");
+  if (s->meta_ev_pending) {
+    PIC_CUDA(cudaEventSynchronize(s->meta_ev));
+    s->meta_ev_pending = false;
+  }
+  int32_t* hp = s->meta_h;
+  size_t o = 0;
+  auto put = [&](const void* src, size_t n) {
+    if (n) std::memcpy(hp + o, src, n * 4);
+    const size_t at = o;
+    o += n;
+    return s->meta_d + at;
+  };
+  const int* d_tok = put(b.tok.data(), T);
+  const int* d_pos = put(b.pos.data(), T);
+  const int* d_slot = put(b.slot.data(), T);
+  const int* d_out = put(b.out_row.data(), T);
+  const int* d_lg = put(b.lg_row.data(), T);
+  const int* d_pblk = put(b.pblk.data(), P);
+  const int* d_ppos = put(b.ppos.data(), P);
+  const int* d_plen = put(b.plen.data(), P);
+  const int* d_copy = put(b.copy_pairs.data(), NC);
+  const AttnItem* d_items = (const AttnItem*)put(items.data(), items.size() * 6);
+  const AttnCombine* d_combs = (const AttnCombine*)put(combs.data(), combs.size() * 5);
+  PIC_CUDA(cudaMemcpyAsync(s->meta_d, hp, o * 4, cudaMemcpyHostToDevice, st));
+  PIC_CUDA(cudaEventRecord(s->meta_ev, st));
+  s->meta_ev_pending = true;
+
+  // copy-on-write of the request-private first blocks (all layers, K and V)
+  launch_copy_blocks((int)NC / 2, d_copy, c.n_layers, s->blocks_total(), s->block_bytes(), s->k_pool, s->v_pool, st);
+
+  AttnArgs aa{};
+  aa.dtype = dt;
+  aa.H = H;
+  aa.G = G;
+  aa.D = D;
+  aa.q = s->q;
+  aa.q_pos = d_pos;
+  aa.page_block = d_pblk;
+  aa.page_pos = d_ppos;
+  aa.page_len = d_plen;
+  aa.rope_cs = s->rope_cs;
+  aa.out = s->attn;
+  aa.part_o = s->att_o;
+  aa.part_ml = s->att_ml;
+  aa.items = d_items;
+  aa.n_items = (int)items.size();
+  aa.combines = d_combs;
+  aa.n_combines = (int)combs.size();
+
+  const int qkv = s->m->qkv_dim();
+  const int sp_qkv = gemm_splits(s, qkv, d, T);
+  const int sp_o = gemm_splits(s, d, H * D, T);
+  const int sp_gu = gemm_splits(s, 2 * F, d, T);
+  const int sp_dn = gemm_splits(s, d, F, T);
+
+  launch_embed_norm(dt, T, d, s->m->embed, d_tok, s->m->attn_norm[0], c.rms_eps, s->h, s->x, st);
+  for (int l = 0; l < c.n_layers; ++l) {
+    pic_status e;
+    if ((e = gemm(s, s->m->wqkv[l], s->x, s->part, qkv, d, T, sp_qkv, st)) != PIC_OK) return e;
+    launch_qkv_epilogue(dt, T, H, G, D, s->part, sp_qkv, s->q, d_slot, s->k_layer(l), s->v_layer(l), st);
+    // compile keeps only KV: the last layer's attention and MLP feed nothing stored
+    if (b.compile && l == c.n_layers - 1) break;
+    aa.k_layer = s->k_layer(l);
+    aa.v_layer = s->v_layer(l);
+    launch_attention(aa, st);
+    if ((e = gemm(s, s->m->wo[l], s->attn, s->part, d, H * D, T, sp_o, st)) != PIC_OK) return e;
+    launch_residual_norm(dt, T, d, s->part, sp_o, s->h, s->m->mlp_norm[l], c.rms_eps, s->x, false, nullptr, nullptr,
+                         nullptr, nullptr, st);
+    if ((e = gemm(s, s->m->wgu[l], s->x, s->part, 2 * F, d, T, sp_gu, st)) != PIC_OK) return e;
+    launch_swiglu(dt, T, F, s->part, sp_gu, s->act, st);
+    if ((e = gemm(s, s->m->wdown[l], s->act, s->part, d, F, T, sp_dn, st)) != PIC_OK) return e;
+    const bool last = l == c.n_layers - 1;
+    launch_residual_norm(dt, T, d, s->part, sp_dn, s->h, last ? s->m->final_norm : s->m->attn_norm[l + 1], c.rms_eps,
+                         s->x, last, d_out, hidden_out, d_lg, s->lm_x, st);
+  }
+  if (!b.compile && b.n_lg > 0) {
+    const int sp = gemm_splits(s, c.vocab, d, b.n_lg);
+    pic_status e;
+    if (sp == 1) {
+      if ((e = gemm(s, s->m->lm_head, s->lm_x, logits_out, c.vocab, d, b.n_lg, 1, st)) != PIC_OK) return e;
+    } else {
+      if ((e = gemm(s, s->m->lm_head, s->lm_x, s->part, c.vocab, d, b.n_lg, sp, st)) != PIC_OK) return e;
+      launch_sum_partials(b.n_lg, c.vocab, s->part, sp, logits_out, st);
+    }
+  }
+  PIC_CUDA(cudaGetLastError());
+  return PIC_OK;
+}
+
+bool valid_tokens(const int32_t* t, int n, int vocab) {
+  for (int i = 0; i < n; ++i)
+    if (t[i] < 0 || t[i] >= vocab) return false;
+  return true;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* pic_status_string(pic_status s) {
+  switch (s) {
+    case PIC_OK: return "PIC_OK";
+    case PIC_ERR_INVALID_ARG: return "PIC_ERR_INVALID_ARG";
+    case PIC_ERR_OUT_OF_BLOCKS: return "PIC_ERR_OUT_OF_BLOCKS";
+    case PIC_ERR_CUDA: return "PIC_ERR_CUDA";
+    case PIC_ERR_DEVICE_TIMEOUT: return "PIC_ERR_DEVICE_TIMEOUT";
+    case PIC_ERR_CAPACITY: return "PIC_ERR_CAPACITY";
+    case PIC_ERR_UNSUPPORTED: return "PIC_ERR_UNSUPPORTED";
+  }
+  return "PIC_ERR_UNKNOWN";
+}
+
+const char* pic_last_error(void) { return g_last_error.c_str(); }
+
+const char* pic_version(void) { return "pic-link 0.1 sm_103a"; }
+
+pic_status pic_model_create(const pic_model_config* cfg, const pic_weights* w, pic_model** out) {
+  if (!cfg || !w || !out) return fail(PIC_ERR_INVALID_ARG, "null argument");
+  const auto& c = *cfg;
+  if (c.n_layers < 1 || c.d_model < 64 || c.d_model % 64 || c.n_heads < 1 || c.n_kv_heads < 1 ||
+      c.n_heads % c.n_kv_heads || (c.head_dim != 64 && c.head_dim != 128) || c.ffn_dim < 8 || c.ffn_dim % 8 ||
+      c.vocab < 1 || c.block_size != kBlock || !(c.rope_base > 1.0) || !(c.rms_eps >= 0.f) ||
+      (c.dtype != PIC_F32 && c.dtype != PIC_BF16) || (c.n_heads * c.head_dim) % 64)
+    return fail(PIC_ERR_INVALID_ARG, "invalid model config");
+  if (!w->embed || !w->lm_head || !w->final_norm || !w->attn_norm || !w->mlp_norm || !w->w_qkv || !w->w_o ||
+      !w->w_gate_up || !w->w_down)
+    return fail(PIC_ERR_INVALID_ARG, "null weight pointer");
+  std::unique_ptr<pic_model> m(new pic_model);
+  m->cfg = c;
+  m->embed = w->embed;
+  m->lm_head = w->lm_head;
+  m->final_norm = w->final_norm;
+  for (int l = 0; l < c.n_layers; ++l) {
+    if (!w->attn_norm[l] || !w->mlp_norm[l] || !w->w_qkv[l] || !w->w_o[l] || !w->w_gate_up[l] || !w->w_down[l])
+      return fail(PIC_ERR_INVALID_ARG, "null per-layer weight pointer");
+    m->attn_norm.push_back(w->attn_norm[l]);
+    m->mlp_norm.push_back(w->mlp_norm[l]);
+    m->wqkv.push_back(w->w_qkv[l]);
+    m->wo.push_back(w->w_o[l]);
+    m->wgu.push_back(w->w_gate_up[l]);
+    m->wdown.push_back(w->w_down[l]);
+  }
+  PIC_CUDA(cudaGetDevice(&m->device));
+  PIC_CUDA(cudaDeviceGetAttribute(&m->num_sms, cudaDevAttrMultiProcessorCount, m->device));
+  *out = m.release();
+  return PIC_OK;
+}
+
+pic_status pic_model_destroy(pic_model* m) {
+  delete m;
+  return PIC_OK;
+}
+
+pic_status pic_store_create(pic_model* m, const pic_store_config* cfg, void* k_pool, void* v_pool, pic_store** out) {
+  if (!m || !cfg || !k_pool || !v_pool || !out) return fail(PIC_ERR_INVALID_ARG, "null argument");
+  const auto& sc = *cfg;
+  if (sc.num_blocks < 1 || sc.max_rows < 1 || sc.max_requests < 1 || sc.max_positions < 1 || sc.max_logit_rows < 1)
+    return fail(PIC_ERR_INVALID_ARG, "invalid store config");
+  if (((uintptr_t)k_pool | (uintptr_t)v_pool) % 16) return fail(PIC_ERR_INVALID_ARG, "pools must be 16-byte aligned");
+  const auto& c = m->cfg;
+  std::unique_ptr<pic_store> s(new pic_store);
+  s->m = m;
+  s->cfg = sc;
+  s->k_pool = k_pool;
+  s->v_pool = v_pool;
+  for (int32_t i = 0; i < sc.num_blocks; ++i) s->free.insert(s->free.end(), i);
+
+  const size_t R = sc.max_rows, es = dtype_size(c.dtype);
+  const size_t d = c.d_model, HD = (size_t)c.n_heads * c.head_dim, F = c.ffn_dim;
+  const int rep = c.n_heads / c.n_kv_heads;
+  // split-K partial sums: enough for 2048 rows (or max_rows) of the widest projection
+  const size_t part_rows = std::max<size_t>(R, 2048);
+  s->part_floats = std::max({part_rows * (size_t)m->qkv_dim(), part_rows * d, part_rows * 2 * F,
+                             (size_t)sc.max_logit_rows * c.vocab, R * HD});
+  s->att_parts_cap = 4 * m->num_sms + c.n_kv_heads * s->att_blocks_cap();
+  const size_t max_pages = (size_t)sc.max_positions / kBlock + 2 * (size_t)sc.max_requests + 2;
+  const size_t max_items = (size_t)s->att_parts_cap + (size_t)c.n_kv_heads * s->att_blocks_cap();
+  s->meta_cap = 5 * R + 3 * max_pages * sc.max_requests + 2 * (size_t)sc.num_blocks + 6 * max_items +
+                5 * (size_t)s->att_parts_cap + 1024;
+
+  size_t off = 0;
+  auto carve = [&](size_t bytes) {
+    const size_t at = off;
+    off = align_up(off + bytes, 256);
+    return at;
+  };
+  const size_t o_h = carve(R * d * 4), o_x = carve(R * std::max(d, HD) * es), o_q = carve(R * HD * es),
+               o_attn = carve(R * HD * es), o_act = carve(R * F * es), o_lm = carve((size_t)sc.max_logit_rows * d * es),
+               o_part = carve(s->part_floats * 4),
+               o_atto = carve((size_t)s->att_parts_cap * kBlock * rep * c.head_dim * 4),
+               o_attml = carve((size_t)s->att_parts_cap * kBlock * rep * 2 * 4), o_meta = carve(s->meta_cap * 4),
+               o_rope = carve((size_t)sc.max_positions * (c.head_dim / 2) * sizeof(float2));
+  cudaError_t e = cudaMalloc(&s->ws, off);
+  if (e != cudaSuccess) return fail(PIC_ERR_CUDA, std::string("workspace cudaMalloc: ") + cudaGetErrorString(e));
+  s->h = (float*)(s->ws + o_h);
+  s->x = s->ws + o_x;
+  s->q = s->ws + o_q;
+  s->attn = s->ws + o_attn;
+  s->act = s->ws + o_act;
+  s->lm_x = s->ws + o_lm;
+  s->part = (float*)(s->ws + o_part);
+  s->att_o = (float*)(s->ws + o_atto);
+  s->att_ml = (float*)(s->ws + o_attml);
+  s->meta_d = (int32_t*)(s->ws + o_meta);
+  s->rope_cs = (float2*)(s->ws + o_rope);
+  e = cudaMallocHost(&s->meta_h, s->meta_cap * 4);
+  if (e != cudaSuccess) {
+    cudaFree(s->ws);
+    return fail(PIC_ERR_CUDA, std::string("cudaMallocHost: ") + cudaGetErrorString(e));
+  }
+  e = cudaEventCreateWithFlags(&s->meta_ev, cudaEventDisableTiming);
+  std::vector<float2> tab;
+  rope_table_host(sc.max_positions, c.head_dim, c.rope_base, tab);
+  if (e == cudaSuccess) e = cudaMemcpy(s->rope_cs, tab.data(), tab.size() * sizeof(float2), cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) {
+    cudaFree(s->ws);
+    cudaFreeHost(s->meta_h);
+    return fail(PIC_ERR_CUDA, std::string("store setup: ") + cudaGetErrorString(e));
+  }
+  *out = s.release();
+  return PIC_OK;
+}
+
+pic_status pic_store_destroy(pic_store* s) {
+  if (!s) return PIC_OK;
+  if (s->meta_ev) {
+    cudaEventSynchronize(s->meta_ev);
+    cudaEventDestroy(s->meta_ev);
+  }
+  cudaFree(s->ws);
+  cudaFreeHost(s->meta_h);
+  delete s;
+  return PIC_OK;
+}
+
+int32_t pic_store_free_blocks(const pic_store* s) { return s ? (int32_t)s->free.size() : -1; }
+
+pic_status pic_compile(pic_store* s, const int32_t* const* tokens, const int32_t* lens, int32_t n_chunks,
+                       int32_t n_dummy, pic_stream_t stream, pic_chunk* out_chunks) {
+  if (!s || !tokens || !lens || n_chunks < 1 || !out_chunks || n_dummy < 0 || n_dummy > kBlock)
+    return fail(PIC_ERR_INVALID_ARG, "invalid compile arguments");
+  const auto& c = s->m->cfg;
+  int need = 0;
+  long long rows = n_dummy;
+  for (int i = 0; i < n_chunks; ++i) {
+    if (!tokens[i] || lens[i] < 1) return fail(PIC_ERR_INVALID_ARG, "empty chunk");
+    if (!valid_tokens(tokens[i], lens[i], c.vocab)) return fail(PIC_ERR_INVALID_ARG, "token id out of range");
+    if (lens[i] + n_dummy > s->cfg.max_positions) return fail(PIC_ERR_CAPACITY, "chunk longer than max_positions");
+    need += ceil_div(lens[i], kBlock);
+    rows += lens[i];
+  }
+  if (n_chunks > s->cfg.max_requests) return fail(PIC_ERR_CAPACITY, "chunks exceed max_requests");
+  if (rows > s->cfg.max_rows) return fail(PIC_ERR_CAPACITY, "compile rows exceed max_rows");
+  if (need > (int)s->free.size()) return fail(PIC_ERR_OUT_OF_BLOCKS, "not enough free blocks for compile");
+
+  Batch b;
+  b.compile = true;
+  // the dummy prefix is computed once per batch into the store's scratch page
+  if (n_dummy > 0) {
+    b.begin_seq();
+    for (int j = 0; j < n_dummy; ++j) b.row(0, j, s->scratch_block() * kBlock + j);
+    b.page(s->scratch_block(), 0, n_dummy);
+    b.end_seq();
+  }
+  std::vector<std::vector<int32_t>> blocks(n_chunks);
+  for (int i = 0; i < n_chunks; ++i) {
+    blocks[i] = s->take(ceil_div(lens[i], kBlock));
+    b.begin_seq();
+    if (n_dummy > 0) b.page(s->scratch_block(), 0, n_dummy);
+    for (int j = 0; j < (int)blocks[i].size(); ++j)
+      b.page(blocks[i][j], n_dummy + kBlock * j, std::min(kBlock, lens[i] - kBlock * j));
+    for (int t = 0; t < lens[i]; ++t)
+      b.row(tokens[i][t], n_dummy + t, blocks[i][t / kBlock] * kBlock + t % kBlock);
+    b.end_seq();
+  }
+  pic_status e = run_forward(s, b, nullptr, nullptr, (cudaStream_t)stream);
+  if (e != PIC_OK) {
+    for (auto& bl : blocks) s->give(bl);
+    return e;
+  }
+  for (int i = 0; i < n_chunks; ++i) {
+    Chunk ch;
+    ch.tokens.assign(tokens[i], tokens[i] + lens[i]);
+    ch.blocks = blocks[i];
+    const int id = s->next_chunk++;
+    s->chunks[id] = std::move(ch);
+    out_chunks[i] = id;
+  }
+  return PIC_OK;
+}
+
+pic_status pic_chunk_import(pic_store* s, const int32_t* tokens, int32_t n_tokens, const void* k, const void* v,
+                            pic_stream_t stream, pic_chunk* out_chunk) {
+  if (!s || !tokens || n_tokens < 1 || !k || !v || !out_chunk) return fail(PIC_ERR_INVALID_ARG, "invalid import");
+  const auto& c = s->m->cfg;
+  if (!valid_tokens(tokens, n_tokens, c.vocab)) return fail(PIC_ERR_INVALID_ARG, "token id out of range");
+  const int nb = ceil_div(n_tokens, kBlock);
+  if (nb > (int)s->free.size()) return fail(PIC_ERR_OUT_OF_BLOCKS, "not enough free blocks for import");
+  if ((size_t)nb > s->meta_cap) return fail(PIC_ERR_CAPACITY, "chunk too long for the metadata buffer");
+  cudaStream_t st = (cudaStream_t)stream;
+  if (s->meta_ev_pending) {
+    PIC_CUDA(cudaEventSynchronize(s->meta_ev));
+    s->meta_ev_pending = false;
+  }
+  std::vector<int32_t> blocks = s->take(nb);
+  std::memcpy(s->meta_h, blocks.data(), nb * 4);
+  cudaError_t e = cudaMemcpyAsync(s->meta_d, s->meta_h, nb * 4, cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess) e = cudaEventRecord(s->meta_ev, st);
+  if (e == cudaSuccess) {
+    s->meta_ev_pending = true;
+    launch_import_kv(c.dtype, c.n_layers, n_tokens, c.n_kv_heads, c.head_dim, k, v, s->meta_d, s->blocks_total(),
+                     s->k_pool, s->v_pool, st);
+    e = cudaGetLastError();
+  }
+  if (e != cudaSuccess) {
+    s->give(blocks);
+    return fail(PIC_ERR_CUDA, std::string("import: ") + cudaGetErrorString(e));
+  }
+  Chunk ch;
+  ch.tokens.assign(tokens, tokens + n_tokens);
+  ch.blocks = blocks;
+  const int id = s->next_chunk++;
+  s->chunks[id] = std::move(ch);
+  *out_chunk = id;
+  return PIC_OK;
+}
+
+pic_status pic_link(pic_store* s, const pic_link_request* reqs, int32_t n_reqs, int32_t k, int32_t all_logits,
+                    float* hidden_out, float* logits_out, pic_stream_t stream, pic_request* out_requests) {
+  if (!s || !reqs || n_reqs < 1 || k < 0 || !hidden_out || !logits_out || !out_requests)
+    return fail(PIC_ERR_INVALID_ARG, "invalid link arguments");
+  const auto& c = s->m->cfg;
+  if (n_reqs > s->cfg.max_requests) return fail(PIC_ERR_CAPACITY, "requests exceed max_requests");
+  // validate and count blocks (nothing is allocated before every check passes)
+  int need = 0;
+  long long rows = 0, lg_rows = 0;
+  for (int r = 0; r < n_reqs; ++r) {
+    const auto& q = reqs[r];
+    if (q.n_chunks < 0 || (q.n_chunks > 0 && !q.chunks) || q.query_len < 1 || !q.query)
+      return fail(PIC_ERR_INVALID_ARG, "invalid request");
+    if (!valid_tokens(q.query, q.query_len, c.vocab)) return fail(PIC_ERR_INVALID_ARG, "query token out of range");
+    long long len = q.query_len;
+    for (int i = 0; i < q.n_chunks; ++i) {
+      auto it = s->chunks.find(q.chunks[i]);
+      if (it == s->chunks.end()) return fail(PIC_ERR_INVALID_ARG, "unknown chunk handle");
+      const int L = (int)it->second.tokens.size();
+      need += ceil_div(std::min(k, L), kBlock);
+      rows += std::min(k, L);
+      len += L;
+    }
+    if (len > s->cfg.max_positions) return fail(PIC_ERR_CAPACITY, "linked sequence exceeds max_positions");
+    need += ceil_div(q.query_len, kBlock);
+    rows += q.query_len;
+    lg_rows += all_logits ? q.query_len : 1;
+  }
+  if (rows > s->cfg.max_rows) return fail(PIC_ERR_CAPACITY, "selected rows exceed max_rows");
+  if (lg_rows > s->cfg.max_logit_rows) return fail(PIC_ERR_CAPACITY, "logit rows exceed max_logit_rows");
+  if (need > (int)s->free.size()) return fail(PIC_ERR_OUT_OF_BLOCKS, "not enough free blocks for link");
+
+  Batch b;
+  std::vector<Request> made(n_reqs);
+  for (int r = 0; r < n_reqs; ++r) {
+    const auto& q = reqs[r];
+    Request& R = made[r];
+    b.begin_seq();
+    int off = 0;
+    for (int i = 0; i < q.n_chunks; ++i) {
+      const Chunk& ch = s->chunks[q.chunks[i]];
+      const int L = (int)ch.tokens.size(), ki = std::min(k, L), mb = ceil_div(ki, kBlock);
+      std::vector<int32_t> own = s->take(mb);
+      R.private_blocks.insert(R.private_blocks.end(), own.begin(), own.end());
+      for (int j = 0; j < (int)ch.blocks.size(); ++j) {
+        const int blk = j < mb ? own[j] : ch.blocks[j];
+        R.page_table.push_back(blk);
+        R.page_pos.push_back(off + kBlock * j);
+        R.page_len.push_back(std::min(kBlock, L - kBlock * j));
+        b.page(blk, off + kBlock * j, std::min(kBlock, L - kBlock * j));
+      }
+      for (int j = 0; j < mb; ++j) {
+        b.copy_pairs.push_back(ch.blocks[j]);
+        b.copy_pairs.push_back(own[j]);
+      }
+      for (int t = 0; t < ki; ++t) {
+        const int slot = own[t / kBlock] * kBlock + t % kBlock;
+        R.selected.push_back(off + t);
+        R.slots.push_back(slot);
+        b.row(ch.tokens[t], off + t, slot);
+      }
+      R.chunk_ids.push_back(q.chunks[i]);
+      off += L;
+    }
+    std::vector<int32_t> qb = s->take(ceil_div(q.query_len, kBlock));
+    R.private_blocks.insert(R.private_blocks.end(), qb.begin(), qb.end());
+    for (int j = 0; j < (int)qb.size(); ++j) {
+      R.page_table.push_back(qb[j]);
+      R.page_pos.push_back(off + kBlock * j);
+      R.page_len.push_back(std::min(kBlock, q.query_len - kBlock * j));
+      b.page(qb[j], off + kBlock * j, std::min(kBlock, q.query_len - kBlock * j));
+    }
+    for (int t = 0; t < q.query_len; ++t) {
+      const int slot = qb[t / kBlock] * kBlock + t % kBlock;
+      R.selected.push_back(off + t);
+      R.slots.push_back(slot);
+      b.row(q.query[t], off + t, slot);
+      b.out_row.back() = b.n_hidden++;
+      if (all_logits || t == q.query_len - 1) b.lg_row.back() = b.n_lg++;
+    }
+    b.end_seq();
+  }
+  pic_status e = run_forward(s, b, hidden_out, logits_out, (cudaStream_t)stream);
+  if (e != PIC_OK) {
+    for (auto& R : made) s->give(R.private_blocks);
+    return e;
+  }
+  for (int r = 0; r < n_reqs; ++r) {
+    for (int32_t cid : made[r].chunk_ids) s->chunks[cid].refs++;
+    const int id = s->next_request++;
+    s->requests[id] = std::move(made[r]);
+    out_requests[r] = id;
+  }
+  return PIC_OK;
+}
+
+pic_status pic_request_get_info(const pic_store* s, pic_request r, pic_request_info* out) {
+  if (!s || !out) return fail(PIC_ERR_INVALID_ARG, "null argument");
+  auto it = s->requests.find(r);
+  if (it == s->requests.end()) return fail(PIC_ERR_INVALID_ARG, "unknown request handle");
+  const Request& R = it->second;
+  out->n_selected = (int32_t)R.selected.size();
+  out->selected = R.selected.data();
+  out->slots = R.slots.data();
+  out->n_pages = (int32_t)R.page_table.size();
+  out->page_table = R.page_table.data();
+  out->page_pos = R.page_pos.data();
+  out->page_len = R.page_len.data();
+  out->n_private = (int32_t)R.private_blocks.size();
+  out->private_blocks = R.private_blocks.data();
+  return PIC_OK;
+}
+
+pic_status pic_chunk_get_blocks(const pic_store* s, pic_chunk c, int32_t* n_blocks, const int32_t** blocks) {
+  if (!s || !n_blocks || !blocks) return fail(PIC_ERR_INVALID_ARG, "null argument");
+  auto it = s->chunks.find(c);
+  if (it == s->chunks.end()) return fail(PIC_ERR_INVALID_ARG, "unknown chunk handle");
+  *n_blocks = (int32_t)it->second.blocks.size();
+  *blocks = it->second.blocks.data();
+  return PIC_OK;
+}
+
+pic_status pic_release_chunk(pic_store* s, pic_chunk c) {
+  if (!s) return fail(PIC_ERR_INVALID_ARG, "null store");
+  auto it = s->chunks.find(c);
+  if (it == s->chunks.end()) return fail(PIC_ERR_INVALID_ARG, "unknown chunk handle");
+  if (--it->second.refs == 0) {
+    s->give(it->second.blocks);
+    s->chunks.erase(it);
+  }
+  return PIC_OK;
+}
+
+pic_status pic_release_request(pic_store* s, pic_request r) {
+  if (!s) return fail(PIC_ERR_INVALID_ARG, "null store");
+  auto it = s->requests.find(r);
+  if (it == s->requests.end()) return fail(PIC_ERR_INVALID_ARG, "unknown request handle");
+  s->give(it->second.private_blocks);
+  for (int32_t cid : it->second.chunk_ids) {
+    auto ci = s->chunks.find(cid);
+    if (ci != s->chunks.end() && --ci->second.refs == 0) {
+      s->give(ci->second.blocks);
+      s->chunks.erase(ci);
+    }
+  }
+  s->requests.erase(it);
+  return PIC_OK;
+}
+
+pic_status pic_sync(pic_store* s, pic_stream_t stream) {
+  (void)s;
+  PIC_CUDA(cudaStreamSynchronize((cudaStream_t)stream));
+  return tc_check_timeout();
+}
+
+}  // extern "C"

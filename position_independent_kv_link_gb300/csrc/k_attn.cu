@@ -1,0 +1,210 @@
+// Sparse-query paged attention with RoPE fused at load (MEPIC abstract: K is kept
+// without positional encoding and rotated inside the attention kernel), causal by
+// absolute position, GQA head sharing, split over page ranges with an LSE merge.
+//
+// This file holds the generic warp-per-(row, head) kernel (any dtype, D = 64 or 128),
+// the split merge and the host planner. The bf16 D=128 tensor-core kernel lives in
+// k_attn_mma.cu and takes the same work items.
+#include <algorithm>
+#include <cmath>
+
+#include "pic_internal.h"
+
+namespace pic {
+
+void launch_attention_mma(const AttnArgs& a, cudaStream_t st);  // k_attn_mma.cu
+
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <typename T, int D>
+__global__ void __launch_bounds__(128) attn_simt_kernel(AttnArgs a) {
+  constexpr int NJ = D / 32;   // dims per lane: lane + 32 j
+  const AttnItem it = a.items[blockIdx.x];
+  const int rep = a.H / a.G;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const T* Q = (const T*)a.q;
+  const T* Kl = (const T*)a.k_layer;
+  const T* Vl = (const T*)a.v_layer;
+  const float scale = rsqrtf((float)D) * kLog2e;
+  for (int pr = warp; pr < it.nrows * rep; pr += 4) {
+    const int r = pr / rep, hh = pr % rep;
+    const int t = it.row0 + r, h = it.g * rep + hh;
+    const int qp = a.q_pos[t];
+    float q[NJ], o[NJ];
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) {
+      q[j] = to_f<T>(Q[((size_t)t * a.H + h) * D + lane + 32 * j]);
+      o[j] = 0.f;
+    }
+    const float2* csq = a.rope_cs + (size_t)qp * (D / 2);
+#pragma unroll
+    for (int j = 0; j < NJ / 2; ++j) {
+      const float2 cs = csq[lane + 32 * j];
+      const float x1 = q[j], x2 = q[j + NJ / 2];
+      q[j] = (x1 * cs.x - x2 * cs.y) * scale;
+      q[j + NJ / 2] = (x2 * cs.x + x1 * cs.y) * scale;
+    }
+    float m = -INFINITY, l = 0.f;
+    bool done = false;
+    for (int p = it.page0; p < it.page1 && !done; ++p) {
+      const int blk = a.page_block[p], base = a.page_pos[p], len = a.page_len[p];
+      for (int rr = 0; rr < len; ++rr) {
+        const int kp = base + rr;
+        if (kp > qp) { done = true; break; }
+        const size_t off = (((size_t)blk * a.G + it.g) * kBlock + rr) * D;
+        const float2* csk = a.rope_cs + (size_t)kp * (D / 2);
+        float s = 0.f;
+#pragma unroll
+        for (int j = 0; j < NJ / 2; ++j) {
+          const float2 cs = csk[lane + 32 * j];
+          const float k1 = to_f<T>(Kl[off + lane + 32 * j]);
+          const float k2 = to_f<T>(Kl[off + lane + 32 * (j + NJ / 2)]);
+          s += q[j] * (k1 * cs.x - k2 * cs.y) + q[j + NJ / 2] * (k2 * cs.x + k1 * cs.y);
+        }
+#pragma unroll
+        for (int x = 16; x > 0; x >>= 1) s += __shfl_xor_sync(0xffffffffu, s, x);
+        const float mn = fmaxf(m, s);
+        const float corr = exp2f(m - mn);
+        const float pw = exp2f(s - mn);
+        l = l * corr + pw;
+#pragma unroll
+        for (int j = 0; j < NJ; ++j) o[j] = o[j] * corr + pw * to_f<T>(Vl[off + lane + 32 * j]);
+        m = mn;
+      }
+    }
+    if (it.part < 0) {
+      const float inv = 1.f / l;
+      T* out = (T*)a.out;
+#pragma unroll
+      for (int j = 0; j < NJ; ++j) out[((size_t)t * a.H + h) * D + lane + 32 * j] = from_f<T>(o[j] * inv);
+    } else {
+      const size_t pi = ((size_t)it.part * kBlock + r) * rep + hh;
+#pragma unroll
+      for (int j = 0; j < NJ; ++j) a.part_o[pi * D + lane + 32 * j] = o[j];
+      if (lane == 0) {
+        a.part_ml[pi * 2] = m;
+        a.part_ml[pi * 2 + 1] = l;
+      }
+    }
+  }
+}
+
+// Merge split results: out = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s.
+template <typename T, int D>
+__global__ void __launch_bounds__(128) attn_combine_kernel(AttnArgs a) {
+  constexpr int NJ = D / 32;
+  const AttnCombine c = a.combines[blockIdx.x];
+  const int rep = a.H / a.G;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int pr = warp; pr < c.nrows * rep; pr += 4) {
+    const int r = pr / rep, hh = pr % rep;
+    float M = -INFINITY;
+    for (int s = 0; s < c.nparts; ++s) M = fmaxf(M, a.part_ml[(((size_t)(c.part0 + s) * kBlock + r) * rep + hh) * 2]);
+    float L = 0.f, o[NJ] = {};
+    for (int s = 0; s < c.nparts; ++s) {
+      const size_t pi = ((size_t)(c.part0 + s) * kBlock + r) * rep + hh;
+      const float ls = a.part_ml[pi * 2 + 1];
+      if (ls == 0.f) continue;
+      const float w = exp2f(a.part_ml[pi * 2] - M);
+      L += w * ls;
+#pragma unroll
+      for (int j = 0; j < NJ; ++j) o[j] += w * a.part_o[pi * D + lane + 32 * j];
+    }
+    const int t = c.row0 + r, h = c.g * rep + hh;
+    const float inv = 1.f / L;
+    T* out = (T*)a.out;
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) out[((size_t)t * a.H + h) * D + lane + 32 * j] = from_f<T>(o[j] * inv);
+  }
+}
+
+template <typename T, int D>
+void launch_simt(const AttnArgs& a, cudaStream_t st) {
+  if (a.n_items > 0) attn_simt_kernel<T, D><<<a.n_items, 128, 0, st>>>(a);
+  if (a.n_combines > 0) attn_combine_kernel<T, D><<<a.n_combines, 128, 0, st>>>(a);
+}
+
+}  // namespace
+
+void launch_attention_simt(const AttnArgs& a, cudaStream_t st) {
+  if (a.dtype == PIC_BF16) {
+    if (a.D == 128) launch_simt<__nv_bfloat16, 128>(a, st);
+    else launch_simt<__nv_bfloat16, 64>(a, st);
+  } else {
+    if (a.D == 128) launch_simt<float, 128>(a, st);
+    else launch_simt<float, 64>(a, st);
+  }
+}
+
+void launch_attention(const AttnArgs& a, cudaStream_t st) {
+  if (a.dtype == PIC_BF16 && a.D == 128)
+    launch_attention_mma(a, st);
+  else
+    launch_attention_simt(a, st);
+}
+
+size_t attention_part_bytes(int n_parts, int rep, int D) {
+  return (size_t)n_parts * kBlock * rep * (D + 2) * sizeof(float);
+}
+
+// Blocks of <= 16 consecutive rows of one sequence; each block reads the prefix of the
+// sequence's pages up to its last row's position, cut into runs of P pages. P grows
+// until the work is ~4 items per SM, never finer than 4 pages.
+void plan_attention(const AttnPlanInput& in, std::vector<AttnItem>& items, std::vector<AttnCombine>& combines,
+                    int& n_parts) {
+  struct Blk { int row0, nrows, pb, pe; };
+  std::vector<Blk> blks;
+  long long total = 0;
+  const std::vector<int>& rp = *in.row_pos;
+  const std::vector<int>& pp = *in.page_pos;
+  for (size_t s = 0; s < in.seq_row_begin.size(); ++s) {
+    for (int r0 = in.seq_row_begin[s]; r0 < in.seq_row_end[s]; r0 += kBlock) {
+      const int n = std::min(kBlock, in.seq_row_end[s] - r0);
+      const int maxp = rp[r0 + n - 1];
+      int pe = in.seq_page_begin[s];
+      while (pe < in.seq_page_end[s] && pp[pe] <= maxp) ++pe;
+      blks.push_back({r0, n, in.seq_page_begin[s], pe});
+      total += (long long)(pe - in.seq_page_begin[s]);
+    }
+  }
+  const long long target = std::max<long long>(1, 4LL * in.num_sms / std::max(1, in.G));
+  int P = (int)std::max<long long>(4, (total + target - 1) / target);
+  items.clear();
+  combines.clear();
+  n_parts = 0;
+  for (const Blk& b : blks) {
+    const int np = b.pe - b.pb;
+    const int ns = std::max(1, (np + P - 1) / P);
+    for (int g = 0; g < in.G; ++g) {
+      if (ns == 1) {
+        items.push_back({b.row0, b.nrows, g, b.pb, b.pe, -1});
+        continue;
+      }
+      combines.push_back({b.row0, b.nrows, g, n_parts, ns});
+      for (int s = 0; s < ns; ++s) {
+        const int p0 = b.pb + s * P, p1 = std::min(b.pe, p0 + P);
+        items.push_back({b.row0, b.nrows, g, p0, p1, n_parts + s});
+      }
+      n_parts += ns;
+    }
+  }
+  // Heaviest items first so the long ranges start early.
+  std::stable_sort(items.begin(), items.end(),
+                   [](const AttnItem& x, const AttnItem& y) { return (x.page1 - x.page0) > (y.page1 - y.page0); });
+}
+
+void rope_table_host(int n_pos, int D, double base, std::vector<float2>& out) {
+  const int h = D / 2;
+  out.resize((size_t)n_pos * h);
+  std::vector<double> theta(h);
+  for (int i = 0; i < h; ++i) theta[i] = std::pow(base, -2.0 * i / D);
+  for (int p = 0; p < n_pos; ++p)
+    for (int i = 0; i < h; ++i) {
+      const double ang = (double)p * theta[i];
+      out[(size_t)p * h + i] = make_float2((float)std::cos(ang), (float)std::sin(ang));
+    }
+}
+
+}  // namespace pic

@@ -1,0 +1,232 @@
+// Row-wise kernels of the decoder around the GEMMs and attention: embedding gather +
+// RMSNorm, split-K reductions fused with their epilogues (QKV scatter into pages,
+// residual + RMSNorm, SwiGLU), block copies for request-private pages, KV import.
+// All are HBM/L2-bound; one CTA per row with 16-byte-friendly strided loops.
+#include "pic_internal.h"
+
+namespace pic {
+
+namespace {
+
+constexpr int kRowThreads = 256;
+
+__device__ __forceinline__ float block_sum(float v, float* red) {
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  if (l == 0) red[w] = v;
+  __syncthreads();
+  float s = 0.f;
+  if (threadIdx.x < 32) {
+    s = (l < (int)(blockDim.x >> 5)) ? red[l] : 0.f;
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if (l == 0) red[0] = s;
+  }
+  __syncthreads();
+  s = red[0];
+  __syncthreads();
+  return s;
+}
+
+// h = E[tok]; x = rmsnorm(h) * g.  Row cached in dynamic shared memory (fp32).
+template <typename T>
+__global__ void embed_norm_kernel(int d, const T* __restrict__ E, const int* __restrict__ tok,
+                                  const float* __restrict__ gain, float eps, float* __restrict__ h,
+                                  T* __restrict__ x) {
+  extern __shared__ float row[];
+  __shared__ float red[32];
+  const int t = blockIdx.x;
+  const T* e = E + (size_t)tok[t] * d;
+  float ss = 0.f;
+  for (int i = threadIdx.x; i < d; i += blockDim.x) {
+    float v = to_f<T>(e[i]);
+    row[i] = v;
+    ss += v * v;
+  }
+  ss = block_sum(ss, red);
+  const float r = rsqrtf(ss / d + eps);
+  for (int i = threadIdx.x; i < d; i += blockDim.x) {
+    h[(size_t)t * d + i] = row[i];
+    x[(size_t)t * d + i] = from_f<T>(row[i] * r * gain[i]);
+  }
+}
+
+// QKV epilogue: sum split-K slabs; q -> [T][H*D]; k, v -> page slot of this layer.
+template <typename T>
+__global__ void qkv_epilogue_kernel(int T_, int H, int G, int D, const float* __restrict__ part, int splits,
+                                    T* __restrict__ q, const int* __restrict__ slot, T* __restrict__ kl,
+                                    T* __restrict__ vl) {
+  const int t = blockIdx.x;
+  const int N = (H + 2 * G) * D;
+  const int s_ = slot[t];
+  const int blk = s_ / kBlock, r = s_ % kBlock;
+  for (int n = threadIdx.x; n < N; n += blockDim.x) {
+    float acc = 0.f;
+    for (int s = 0; s < splits; ++s) acc += part[((size_t)s * T_ + t) * N + n];
+    if (n < H * D) {
+      q[(size_t)t * H * D + n] = from_f<T>(acc);
+    } else {
+      const int m = n - H * D;
+      const int kv = m / (G * D);          // 0: K, 1: V
+      const int g = (m % (G * D)) / D, i = m % D;
+      T* dst = kv == 0 ? kl : vl;
+      dst[(((size_t)blk * G + g) * kBlock + r) * D + i] = from_f<T>(acc);
+    }
+  }
+}
+
+template <typename T>
+__global__ void residual_norm_kernel(int T_, int d, const float* __restrict__ part, int splits,
+                                     float* __restrict__ h, const float* __restrict__ gain, float eps,
+                                     T* __restrict__ x, int final_layer, const int* __restrict__ out_row,
+                                     float* __restrict__ hidden_out, const int* __restrict__ lg_row,
+                                     T* __restrict__ lm_x) {
+  extern __shared__ float row[];
+  __shared__ float red[32];
+  const int t = blockIdx.x;
+  float ss = 0.f;
+  for (int i = threadIdx.x; i < d; i += blockDim.x) {
+    float v = h[(size_t)t * d + i];
+    for (int s = 0; s < splits; ++s) v += part[((size_t)s * T_ + t) * d + i];
+    row[i] = v;
+    h[(size_t)t * d + i] = v;
+    ss += v * v;
+  }
+  ss = block_sum(ss, red);
+  const float r = rsqrtf(ss / d + eps);
+  if (!final_layer) {
+    for (int i = threadIdx.x; i < d; i += blockDim.x) x[(size_t)t * d + i] = from_f<T>(row[i] * r * gain[i]);
+    return;
+  }
+  const int o = out_row[t], lg = lg_row[t];
+  if (o >= 0)
+    for (int i = threadIdx.x; i < d; i += blockDim.x) hidden_out[(size_t)o * d + i] = row[i] * r * gain[i];
+  if (lg >= 0)
+    for (int i = threadIdx.x; i < d; i += blockDim.x) lm_x[(size_t)lg * d + i] = from_f<T>(row[i] * r * gain[i]);
+}
+
+template <typename T>
+__global__ void swiglu_kernel(int T_, int F, const float* __restrict__ part, int splits, T* __restrict__ act) {
+  const int t = blockIdx.x;
+  const size_t N = 2 * (size_t)F;
+  for (int j = threadIdx.x; j < F; j += blockDim.x) {
+    float a = 0.f, b = 0.f;
+    for (int s = 0; s < splits; ++s) {
+      const float* p = part + ((size_t)s * T_ + t) * N;
+      a += p[j];
+      b += p[F + j];
+    }
+    act[(size_t)t * F + j] = from_f<T>(a / (1.f + __expf(-a)) * b);
+  }
+}
+
+__global__ void sum_partials_kernel(int T_, int N, const float* __restrict__ part, int splits,
+                                    float* __restrict__ out) {
+  const size_t total = (size_t)T_ * N;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
+    float acc = 0.f;
+    for (int s = 0; s < splits; ++s) acc += part[(size_t)s * total + i];
+    out[i] = acc;
+  }
+}
+
+// grid: (pairs, layers, 2 pools); 16-byte copies of one block of one layer.
+__global__ void copy_blocks_kernel(const int* __restrict__ pairs, int num_blocks_total, size_t block_bytes,
+                                   char* __restrict__ kp, char* __restrict__ vp) {
+  const int i = blockIdx.x, l = blockIdx.y;
+  char* pool = blockIdx.z == 0 ? kp : vp;
+  const size_t layer_off = (size_t)l * num_blocks_total * block_bytes;
+  const int4* src = reinterpret_cast<const int4*>(pool + layer_off + (size_t)pairs[2 * i] * block_bytes);
+  int4* dst = reinterpret_cast<int4*>(pool + layer_off + (size_t)pairs[2 * i + 1] * block_bytes);
+  for (size_t j = threadIdx.x; j < block_bytes / 16; j += blockDim.x) dst[j] = src[j];
+}
+
+// grid: (n tokens, layers); copies K and V rows of one token into its page slot.
+template <typename T>
+__global__ void import_kv_kernel(int n, int G, int D, const T* __restrict__ ks, const T* __restrict__ vs,
+                                 const int* __restrict__ blocks, int num_blocks_total, T* __restrict__ kp,
+                                 T* __restrict__ vp) {
+  const int t = blockIdx.x, l = blockIdx.y;
+  const int blk = blocks[t / kBlock], r = t % kBlock;
+  const size_t src = ((size_t)l * n + t) * G * D;
+  for (int j = threadIdx.x; j < G * D; j += blockDim.x) {
+    const int g = j / D, i = j % D;
+    const size_t dst = ((((size_t)l * num_blocks_total + blk) * G + g) * kBlock + r) * D + i;
+    kp[dst] = ks[src + j];
+    vp[dst] = vs[src + j];
+  }
+}
+
+}  // namespace
+
+void launch_embed_norm(int dtype, int T, int d, const void* embed, const int* tok, const float* gain, float eps,
+                       float* h, void* x, cudaStream_t st) {
+  if (T <= 0) return;
+  const size_t sm = d * sizeof(float);
+  if (dtype == PIC_BF16)
+    embed_norm_kernel<__nv_bfloat16><<<T, kRowThreads, sm, st>>>(d, (const __nv_bfloat16*)embed, tok, gain, eps, h,
+                                                                 (__nv_bfloat16*)x);
+  else
+    embed_norm_kernel<float><<<T, kRowThreads, sm, st>>>(d, (const float*)embed, tok, gain, eps, h, (float*)x);
+}
+
+void launch_qkv_epilogue(int dtype, int T, int H, int G, int D, const float* part, int splits, void* q,
+                         const int* slot, void* k_layer, void* v_layer, cudaStream_t st) {
+  if (T <= 0) return;
+  if (dtype == PIC_BF16)
+    qkv_epilogue_kernel<__nv_bfloat16><<<T, kRowThreads, 0, st>>>(T, H, G, D, part, splits, (__nv_bfloat16*)q, slot,
+                                                                  (__nv_bfloat16*)k_layer, (__nv_bfloat16*)v_layer);
+  else
+    qkv_epilogue_kernel<float><<<T, kRowThreads, 0, st>>>(T, H, G, D, part, splits, (float*)q, slot,
+                                                          (float*)k_layer, (float*)v_layer);
+}
+
+void launch_residual_norm(int dtype, int T, int d, const float* part, int splits, float* h, const float* gain,
+                          float eps, void* x, bool final_layer, const int* out_row, float* hidden_out,
+                          const int* lg_row, void* lm_x, cudaStream_t st) {
+  if (T <= 0) return;
+  const size_t sm = d * sizeof(float);
+  if (dtype == PIC_BF16)
+    residual_norm_kernel<__nv_bfloat16><<<T, kRowThreads, sm, st>>>(T, d, part, splits, h, gain, eps,
+                                                                    (__nv_bfloat16*)x, final_layer, out_row,
+                                                                    hidden_out, lg_row, (__nv_bfloat16*)lm_x);
+  else
+    residual_norm_kernel<float><<<T, kRowThreads, sm, st>>>(T, d, part, splits, h, gain, eps, (float*)x, final_layer,
+                                                            out_row, hidden_out, lg_row, (float*)lm_x);
+}
+
+void launch_swiglu(int dtype, int T, int F, const float* part, int splits, void* act, cudaStream_t st) {
+  if (T <= 0) return;
+  if (dtype == PIC_BF16)
+    swiglu_kernel<__nv_bfloat16><<<T, kRowThreads, 0, st>>>(T, F, part, splits, (__nv_bfloat16*)act);
+  else
+    swiglu_kernel<float><<<T, kRowThreads, 0, st>>>(T, F, part, splits, (float*)act);
+}
+
+void launch_sum_partials(int T, int N, const float* part, int splits, float* out, cudaStream_t st) {
+  const size_t total = (size_t)T * N;
+  if (total == 0) return;
+  const int blocks = (int)std::min<size_t>((total + 255) / 256, 152 * 8);
+  sum_partials_kernel<<<blocks, 256, 0, st>>>(T, N, part, splits, out);
+}
+
+void launch_copy_blocks(int n_pairs, const int* pairs, int n_layers, int num_blocks_total, size_t block_bytes,
+                        void* k_pool, void* v_pool, cudaStream_t st) {
+  if (n_pairs <= 0) return;
+  dim3 grid(n_pairs, n_layers, 2);
+  copy_blocks_kernel<<<grid, 256, 0, st>>>(pairs, num_blocks_total, block_bytes, (char*)k_pool, (char*)v_pool);
+}
+
+void launch_import_kv(int dtype, int n_layers, int n, int G, int D, const void* k_src, const void* v_src,
+                      const int* blocks, int num_blocks_total, void* k_pool, void* v_pool, cudaStream_t st) {
+  if (n <= 0) return;
+  dim3 grid(n, n_layers);
+  if (dtype == PIC_BF16)
+    import_kv_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(n, G, D, (const __nv_bfloat16*)k_src,
+                                                          (const __nv_bfloat16*)v_src, blocks, num_blocks_total,
+                                                          (__nv_bfloat16*)k_pool, (__nv_bfloat16*)v_pool);
+  else
+    import_kv_kernel<float><<<grid, 256, 0, st>>>(n, G, D, (const float*)k_src, (const float*)v_src, blocks,
+                                                  num_blocks_total, (float*)k_pool, (float*)v_pool);
+}
+
+}  // namespace pic

@@ -1,0 +1,170 @@
+// Kernel-level C ABI: single steps of the link path (GEMM, paged attention, RoPE table)
+// on caller-provided device buffers, for testing and profiling the kernels in isolation.
+#include <algorithm>
+#include <cstring>
+
+#include "pic_internal.h"
+
+using namespace pic;
+
+namespace {
+
+int current_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 152;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 152;
+  return n;
+}
+
+int op_gemm_splits(int dtype, int N, int K, int T) {
+  if (dtype != PIC_BF16 || !tc_gemm_supported(N, K, T)) return 1;
+  return tc_gemm_splits(N, K, T, current_sms(), 16);
+}
+
+size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+struct AttnScratchLayout {
+  size_t ints_bytes, part_o_off, part_ml_off, total;
+  int max_parts, max_items;
+};
+
+AttnScratchLayout attn_layout(int T, int n_heads, int n_kv_heads, int head_dim, int n_pages) {
+  AttnScratchLayout L{};
+  const int n_blocks = (T + kBlock - 1) / kBlock;
+  L.max_parts = 4 * current_sms() + n_kv_heads * n_blocks;
+  L.max_items = L.max_parts + n_kv_heads * n_blocks;
+  const size_t ints = (size_t)T + 3 * (size_t)n_pages + 6 * (size_t)L.max_items + 5 * (size_t)L.max_parts;
+  L.ints_bytes = align256(ints * 4);
+  const int rep = std::max(1, n_heads / std::max(1, n_kv_heads));
+  L.part_o_off = L.ints_bytes;
+  L.part_ml_off = L.part_o_off + align256((size_t)L.max_parts * kBlock * rep * head_dim * 4);
+  L.total = L.part_ml_off + align256((size_t)L.max_parts * kBlock * rep * 2 * 4);
+  return L;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t pic_op_gemm_scratch_bytes(int32_t dtype, int32_t N, int32_t K, int32_t T) {
+  const int sp = op_gemm_splits(dtype, N, K, T);
+  return sp > 1 ? (size_t)sp * N * T * 4 : 0;
+}
+
+pic_status pic_op_gemm(int32_t dtype, const void* W, const void* X, float* Y, int32_t N, int32_t K, int32_t T,
+                       void* scratch, size_t scratch_bytes, pic_stream_t stream) {
+  if (!W || !X || !Y || N < 1 || K < 1 || T < 1 || (dtype != PIC_F32 && dtype != PIC_BF16))
+    return fail(PIC_ERR_INVALID_ARG, "invalid gemm arguments");
+  cudaStream_t st = (cudaStream_t)stream;
+  const int sp = op_gemm_splits(dtype, N, K, T);
+  float* part = Y;
+  if (sp > 1) {
+    if (!scratch || scratch_bytes < (size_t)sp * N * T * 4) return fail(PIC_ERR_INVALID_ARG, "gemm scratch too small");
+    part = (float*)scratch;
+  }
+  if (dtype == PIC_BF16 && tc_gemm_supported(N, K, T)) {
+    pic_status e = tc_gemm_run(W, X, part, N, K, T, sp, st);
+    if (e != PIC_OK) return e;
+  } else {
+    launch_gemm_simt(dtype, W, X, part, N, K, T, 1, st);
+  }
+  if (sp > 1) launch_sum_partials(T, N, part, sp, Y, st);
+  PIC_CUDA(cudaGetLastError());
+  return PIC_OK;
+}
+
+size_t pic_op_attention_scratch_bytes(int32_t T, int32_t n_heads, int32_t n_kv_heads, int32_t head_dim,
+                                      int32_t n_pages) {
+  if (T < 1 || n_heads < 1 || n_kv_heads < 1 || n_pages < 1) return 0;
+  return attn_layout(T, n_heads, n_kv_heads, head_dim, n_pages).total;
+}
+
+pic_status pic_op_attention(int32_t dtype, int32_t T, int32_t n_heads, int32_t n_kv_heads, int32_t head_dim,
+                            const void* q, const int32_t* q_pos_host, const void* k_layer, const void* v_layer,
+                            const int32_t* page_block_host, const int32_t* page_pos_host,
+                            const int32_t* page_len_host, int32_t n_pages, int32_t pool_blocks,
+                            const void* rope_cs, int32_t rope_positions, void* out, void* scratch,
+                            size_t scratch_bytes, pic_stream_t stream) {
+  if (T < 1 || n_pages < 1 || !q || !q_pos_host || !k_layer || !v_layer || !page_block_host || !page_pos_host ||
+      !page_len_host || !rope_cs || !out || !scratch || n_kv_heads < 1 || n_heads % n_kv_heads ||
+      (head_dim != 64 && head_dim != 128) || (dtype != PIC_F32 && dtype != PIC_BF16))
+    return fail(PIC_ERR_INVALID_ARG, "invalid attention arguments");
+  const AttnScratchLayout L = attn_layout(T, n_heads, n_kv_heads, head_dim, n_pages);
+  if (scratch_bytes < L.total) return fail(PIC_ERR_INVALID_ARG, "attention scratch too small");
+  for (int t = 0; t < T; ++t)
+    if (q_pos_host[t] < 0 || q_pos_host[t] >= rope_positions || (t && q_pos_host[t] <= q_pos_host[t - 1]))
+      return fail(PIC_ERR_INVALID_ARG, "query positions must be ascending and inside the RoPE table");
+  for (int p = 0; p < n_pages; ++p)
+    if (page_block_host[p] < 0 || page_block_host[p] >= pool_blocks || page_len_host[p] < 1 ||
+        page_len_host[p] > kBlock || page_pos_host[p] < 0 ||
+        page_pos_host[p] + page_len_host[p] > rope_positions ||
+        (p && page_pos_host[p] < page_pos_host[p - 1] + page_len_host[p - 1]))
+      return fail(PIC_ERR_INVALID_ARG,
+                  "pages must be in position order, inside the pool and RoPE table, with 1..16 valid rows");
+  std::vector<int> row_pos(q_pos_host, q_pos_host + T), ppos(page_pos_host, page_pos_host + n_pages);
+  AttnPlanInput in;
+  in.seq_row_begin = {0};
+  in.seq_row_end = {T};
+  in.seq_page_begin = {0};
+  in.seq_page_end = {n_pages};
+  in.row_pos = &row_pos;
+  in.page_pos = &ppos;
+  in.G = n_kv_heads;
+  in.num_sms = current_sms();
+  std::vector<AttnItem> items;
+  std::vector<AttnCombine> combs;
+  int n_parts = 0;
+  plan_attention(in, items, combs, n_parts);
+  if (n_parts > L.max_parts || (int)items.size() > L.max_items)
+    return fail(PIC_ERR_CAPACITY, "attention plan exceeds its scratch bound");
+  std::vector<int32_t> ints;
+  ints.insert(ints.end(), q_pos_host, q_pos_host + T);
+  ints.insert(ints.end(), page_block_host, page_block_host + n_pages);
+  ints.insert(ints.end(), page_pos_host, page_pos_host + n_pages);
+  ints.insert(ints.end(), page_len_host, page_len_host + n_pages);
+  const size_t o_items = ints.size();
+  ints.resize(o_items + items.size() * 6);
+  std::memcpy(ints.data() + o_items, items.data(), items.size() * sizeof(AttnItem));
+  const size_t o_combs = ints.size();
+  ints.resize(o_combs + combs.size() * 5);
+  std::memcpy(ints.data() + o_combs, combs.data(), combs.size() * sizeof(AttnCombine));
+  cudaStream_t st = (cudaStream_t)stream;
+  int32_t* di = (int32_t*)scratch;
+  PIC_CUDA(cudaMemcpyAsync(di, ints.data(), ints.size() * 4, cudaMemcpyHostToDevice, st));
+  AttnArgs a{};
+  a.dtype = dtype;
+  a.H = n_heads;
+  a.G = n_kv_heads;
+  a.D = head_dim;
+  a.q = q;
+  a.q_pos = di;
+  a.k_layer = k_layer;
+  a.v_layer = v_layer;
+  a.page_block = di + T;
+  a.page_pos = di + T + n_pages;
+  a.page_len = di + T + 2 * n_pages;
+  a.rope_cs = (const float2*)rope_cs;
+  a.out = out;
+  a.part_o = (float*)((char*)scratch + L.part_o_off);
+  a.part_ml = (float*)((char*)scratch + L.part_ml_off);
+  a.items = (const AttnItem*)(di + o_items);
+  a.n_items = (int)items.size();
+  a.combines = (const AttnCombine*)(di + o_combs);
+  a.n_combines = (int)combs.size();
+  launch_attention(a, st);
+  PIC_CUDA(cudaGetLastError());
+  return PIC_OK;
+}
+
+pic_status pic_op_rope_table(int32_t n_pos, int32_t head_dim, double base, void* out, pic_stream_t stream) {
+  if (n_pos < 1 || head_dim < 2 || head_dim % 2 || !out || !(base > 1.0))
+    return fail(PIC_ERR_INVALID_ARG, "invalid rope table arguments");
+  std::vector<float2> tab;
+  rope_table_host(n_pos, head_dim, base, tab);
+  PIC_CUDA(cudaMemcpyAsync(out, tab.data(), tab.size() * sizeof(float2), cudaMemcpyHostToDevice,
+                           (cudaStream_t)stream));
+  PIC_CUDA(cudaStreamSynchronize((cudaStream_t)stream));
+  return PIC_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,118 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <string>
+#include <vector>
+
+#include "pic.h"
+
+namespace pic {
+
+constexpr int kBlock = 16;  // tokens per KV page
+
+// ------------------------------------------------------------------ error plumbing
+void set_error(const std::string& msg);
+pic_status fail(pic_status s, const std::string& msg);
+#define PIC_CUDA(call)                                                                \
+  do {                                                                                \
+    cudaError_t e_ = (call);                                                          \
+    if (e_ != cudaSuccess)                                                            \
+      return ::pic::fail(PIC_ERR_CUDA, std::string(#call) + ": " + cudaGetErrorString(e_)); \
+  } while (0)
+
+// ------------------------------------------------------------------ element helpers
+template <typename T> __device__ __forceinline__ float to_f(T v);
+template <> __device__ __forceinline__ float to_f<float>(float v) { return v; }
+template <> __device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 v) { return __bfloat162float(v); }
+template <typename T> __device__ __forceinline__ T from_f(float v);
+template <> __device__ __forceinline__ float from_f<float>(float v) { return v; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float v) { return __float2bfloat16_rn(v); }
+
+inline size_t dtype_size(int dtype) { return dtype == PIC_BF16 ? 2 : 4; }
+
+// ------------------------------------------------------------------ row-wise kernels (k_rows.cu)
+// h[t] = E[tok[t]] (fp32); x[t] = RMSNorm(h[t]) * gain in the model dtype.
+void launch_embed_norm(int dtype, int T, int d, const void* embed, const int* tok, const float* gain, float eps,
+                       float* h, void* x, cudaStream_t st);
+// Sums `splits` partial [T][N] slabs of the fused QKV projection. Writes q [T][H*D] (dtype)
+// and the pre-RoPE k, v rows into page slots of one layer of the pools.
+void launch_qkv_epilogue(int dtype, int T, int H, int G, int D, const float* part, int splits, void* q,
+                         const int* slot, void* k_layer, void* v_layer, cudaStream_t st);
+// h[t] += sum of partials; y = RMSNorm(h[t]) * gain. Not final: x[t] = y (dtype).
+// Final: hidden_out[out_row[t]] = y (fp32) when out_row[t] >= 0 and lm_x[lg_row[t]] = y
+// (dtype) when lg_row[t] >= 0.
+void launch_residual_norm(int dtype, int T, int d, const float* part, int splits, float* h, const float* gain,
+                          float eps, void* x, bool final_layer, const int* out_row, float* hidden_out,
+                          const int* lg_row, void* lm_x, cudaStream_t st);
+// act[t][j] = silu(sum gate) * (sum up) from partial slabs [T][2F] (gate cols, then up cols).
+void launch_swiglu(int dtype, int T, int F, const float* part, int splits, void* act, cudaStream_t st);
+// out[t][n] = sum over splits of part[s][t][n].
+void launch_sum_partials(int T, int N, const float* part, int splits, float* out, cudaStream_t st);
+// For each pair i: copy block src[i] -> dst[i] in every layer of both pools.
+void launch_copy_blocks(int n_pairs, const int* pairs, int n_layers, int num_blocks_total, size_t block_bytes,
+                        void* k_pool, void* v_pool, cudaStream_t st);
+// Copies rows [n_layers][n][G][D] of a chunk's KV into its pages (row t -> blocks[t/16], t%16).
+void launch_import_kv(int dtype, int n_layers, int n, int G, int D, const void* k_src, const void* v_src,
+                      const int* blocks, int num_blocks_total, void* k_pool, void* v_pool, cudaStream_t st);
+
+// ------------------------------------------------------------------ GEMMs
+// part[s][T][N] (fp32) = X[T][k-range s] . W[N][k-range s]^T, K split evenly in `splits`.
+void launch_gemm_simt(int dtype, const void* W, const void* X, float* part, int N, int K, int T, int splits,
+                      cudaStream_t st);
+
+struct TcGemmPlan;  // tensor-map pair and schedule of one tcgen05 GEMM (k_gemm_tc.cu)
+// Shape rules of the tcgen05 kernel.
+bool tc_gemm_supported(int N, int K, int T);
+// Split-K factor chosen for a shape on a device with `num_sms` SMs (<= max_splits).
+int tc_gemm_splits(int N, int K, int T, int num_sms, int max_splits);
+pic_status tc_gemm_run(const void* W, const void* X, float* part, int N, int K, int T, int splits, cudaStream_t st);
+// Reads and clears the device flag set when a tcgen05 kernel gave up a bounded wait.
+pic_status tc_check_timeout();
+
+// ------------------------------------------------------------------ attention (k_attn.cu)
+struct AttnItem {      // one CTA's work: <=16 consecutive rows of one sequence x one KV head x a page range
+  int row0, nrows, g, page0, page1, part;  // part < 0: write normalized output directly
+};
+struct AttnCombine {   // merge `nparts` partial results of rows [row0, row0+nrows) for KV head g
+  int row0, nrows, g, part0, nparts;
+};
+struct AttnArgs {
+  int dtype, H, G, D;
+  const void* q;            // [T][H][D] pre-RoPE
+  const int* q_pos;         // [T]
+  const void* k_layer;      // [nb][G][16][D]
+  const void* v_layer;
+  const int* page_block;    // flattened pages of all sequences
+  const int* page_pos;
+  const int* page_len;
+  const float2* rope_cs;    // [max_pos][D/2]
+  void* out;                // [T][H][D]
+  float* part_o;            // [parts][16][rep][D]
+  float* part_ml;           // [parts][16][rep][2]
+  const AttnItem* items;
+  int n_items;
+  const AttnCombine* combines;
+  int n_combines;
+};
+void launch_attention(const AttnArgs& a, cudaStream_t st);
+
+// Host-side planning shared by link/compile and the kernel-level call.
+struct AttnPlanInput {
+  // per sequence: [row_begin, row_end) rows (ascending positions) and [page_begin, page_end)
+  std::vector<int> seq_row_begin, seq_row_end, seq_page_begin, seq_page_end;
+  const std::vector<int>* row_pos;
+  const std::vector<int>* page_pos;
+  int G;
+  int num_sms;
+};
+void plan_attention(const AttnPlanInput& in, std::vector<AttnItem>& items, std::vector<AttnCombine>& combines,
+                    int& n_parts);
+size_t attention_part_bytes(int n_parts, int rep, int D);
+
+void rope_table_host(int n_pos, int D, double base, std::vector<float2>& out);
+
+}  // namespace pic

@@ -1,0 +1,181 @@
+"""GPU parity of the CUDA path against the fp64 CPU oracle, through the C ABI.
+
+Element-by-element comparisons on seeded inputs: the tcgen05 and SIMT GEMMs, the
+fused-RoPE paged attention, and whole compile + link runs (tiny fp32 config at 1e-4,
+small bf16 GQA models at 2e-2), including ragged chunks, several requests, repeated
+chunks, k = 0 with the LegoLink-0 dummy prefix, k larger than a chunk, and the error
+paths of the store.
+"""
+import numpy as np
+import pytest
+import torch
+
+import pic_inputs as pi
+from oracle import pic_oracle as po
+from tests.helpers import compare_link, library_run, oracle_run, rel_err
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    torch.cuda.set_device(0)
+    from position_independent_kv_link_gb300 import load
+    load()
+
+
+# ----------------------------------------------------------------------------- GEMM
+
+@pytest.mark.parametrize("N,K,T", [(128, 64, 1), (256, 128, 5), (128, 4096, 224), (6144, 4096, 224),
+                                   (384, 512, 300), (256, 1024, 513), (4096, 14336, 64), (1024, 256, 16)])
+def test_gemm_bf16_tcgen05(N, K, T):
+    from position_independent_kv_link_gb300 import gemm
+    W = pi.randn((N, K), ("gemmW", N, K), 0.05, torch.bfloat16)
+    X = pi.randn((T, K), ("gemmX", T, K), 1.0, torch.bfloat16)
+    Y = gemm(W.cuda(), X.cuda())
+    torch.cuda.synchronize()
+    ref = X.double() @ W.double().T
+    assert rel_err(Y, ref) < 1e-5
+
+
+@pytest.mark.parametrize("N,K,T", [(96, 64, 7), (768, 256, 24), (1024, 512, 300)])
+def test_gemm_f32_simt(N, K, T):
+    from position_independent_kv_link_gb300 import gemm
+    W = pi.randn((N, K), ("gemmWf", N, K), 0.05)
+    X = pi.randn((T, K), ("gemmXf", T, K), 1.0)
+    Y = gemm(W.cuda(), X.cuda())
+    torch.cuda.synchronize()
+    assert rel_err(Y, X.double() @ W.double().T) < 1e-5
+
+
+# ----------------------------------------------------------------------------- attention
+
+def _attn_case(dtype, D, H, G, lens, qlen, k_first, seed):
+    """Pages of ragged chunks + a query, random pre-RoPE K/V, queries at selected rows."""
+    rng = np.random.default_rng(seed)
+    pblk, ppos, plen = [], [], []
+    off = 0
+    sel = []
+    for i, L in enumerate(lens + [qlen]):
+        for j in range(-(-L // 16)):
+            pblk.append(len(pblk))
+            ppos.append(off + 16 * j)
+            plen.append(min(16, L - 16 * j))
+        sel += list(range(off, off + (min(k_first, L) if i < len(lens) else L)))
+        off += L
+    sel = sorted(set(sel))
+    nb = len(pblk)
+    perm = rng.permutation(nb + 3)[:nb]               # scattered physical blocks
+    pblk = [int(perm[i]) for i in range(nb)]
+    K = pi.randn((nb + 3, G, 16, D), ("attK", seed), 1.0, dtype)
+    V = pi.randn((nb + 3, G, 16, D), ("attV", seed), 1.0, dtype)
+    q = pi.randn((len(sel), H, D), ("attQ", seed), 1.0, dtype)
+    return q, np.array(sel), K, V, (np.array(pblk), np.array(ppos), np.array(plen)), off
+
+
+@pytest.mark.parametrize("dtype,D,H,G", [(torch.float32, 64, 4, 4), (torch.float32, 128, 8, 2),
+                                         (torch.bfloat16, 128, 8, 2), (torch.bfloat16, 128, 32, 8),
+                                         (torch.bfloat16, 64, 4, 1)])
+def test_paged_attention_fused_rope(dtype, D, H, G):
+    from position_independent_kv_link_gb300 import attention, rope_table
+    base = 500000.0 if D == 128 else 10000.0
+    q, qpos, K, V, pages, n_pos = _attn_case(dtype, D, H, G, [37, 16, 5, 100, 64], 20, 3, 7)
+    rope = rope_table(n_pos + 8, D, base)
+    out = attention(q.cuda(), qpos, K.cuda(), V.cuda(), pages, rope, G)
+    torch.cuda.synchronize()
+    # oracle: assemble K/V in position order, rotate at absolute positions, causal softmax
+    blk, ppos, plen = pages
+    Ka = np.concatenate([K[b, :, :n].double().numpy().transpose(1, 0, 2) for b, n in zip(blk, plen)])
+    Va = np.concatenate([V[b, :, :n].double().numpy().transpose(1, 0, 2) for b, n in zip(blk, plen)])
+    pos = np.concatenate([np.arange(p, p + n) for p, n in zip(ppos, plen)])
+    ref = po.causal_attention(po.rope(q.double().numpy(), qpos, base), po.rope(Ka, pos, base), Va, qpos, pos)
+    tol = 1e-4 if dtype == torch.float32 else 2e-2
+    assert rel_err(out, ref) < tol
+
+
+# ----------------------------------------------------------------------------- whole link
+
+@pytest.fixture(scope="module")
+def tiny():
+    spec = pi.TINY
+    w = pi.gen_weights(spec, gains="random")
+    from position_independent_kv_link_gb300 import PicModel
+    return spec, w, PicModel(spec, w), po.OracleModel(spec, w)
+
+
+def _store(model, nb=256, rows=2048, reqs=16, pos=8192, lg=64):
+    from position_independent_kv_link_gb300 import PicStore
+    return PicStore(model, num_blocks=nb, max_rows=rows, max_requests=reqs, max_positions=pos, max_logit_rows=lg)
+
+
+def test_tiny_config_link(tiny):
+    spec, w, model, om = tiny
+    wl = pi.config_workloads()["tiny"]
+    store = _store(model)
+    _, res = library_run(store, wl)
+    _, _, out = oracle_run(om, wl, 256)
+    compare_link(store, res, out, spec)
+
+
+@pytest.mark.parametrize("k,n_dummy", [(0, 0), (0, 4), (1, 0), (2, 0), (16, 0), (17, 0), (1000, 0)])
+def test_tiny_link_variants(tiny, k, n_dummy):
+    """Ragged chunks (not multiples of 16), 3 requests with repeats, several k."""
+    spec, w, model, om = tiny
+    wl = pi.make_workload("ragged", spec, 5, [37, 64, 5, 16, 50], 19, k, n_requests=3, n_dummy=n_dummy)
+    wl.requests[1].chunk_ids = [4, 0, 0, 2]
+    wl.requests[2].chunk_ids = [3]
+    wl.requests[2].query = wl.requests[2].query[:1]
+    store = _store(model)
+    _, res = library_run(store, wl, all_logits=True)
+    _, _, out = oracle_run(om, wl, 256, all_logits=True)
+    compare_link(store, res, out, spec)
+
+
+@pytest.fixture(scope="module")
+def small_bf16():
+    spec = pi.SMALL_BF16
+    w = pi.gen_weights(spec, gains="random")
+    from position_independent_kv_link_gb300 import PicModel
+    return spec, w, PicModel(spec, w), po.OracleModel(spec, w)
+
+
+@pytest.mark.parametrize("k,n_dummy", [(16, 0), (2, 0), (0, 4), (40, 0)])
+def test_small_bf16_link(small_bf16, k, n_dummy):
+    spec, w, model, om = small_bf16
+    wl = pi.make_workload("small", spec, 6, [128, 77, 200, 16, 33, 128], 40, k, n_requests=2, n_dummy=n_dummy)
+    wl.requests[1].chunk_ids = [5, 1, 3, 0]
+    store = _store(model)
+    _, res = library_run(store, wl)
+    _, _, out = oracle_run(om, wl, 256)
+    compare_link(store, res, out, spec)
+
+
+# ----------------------------------------------------------------------------- store error paths
+
+def test_store_errors_leave_state_unchanged(tiny):
+    from position_independent_kv_link_gb300 import PicError
+    from position_independent_kv_link_gb300 import _lib as L
+    spec, w, model, om = tiny
+    store = _store(model, nb=10)
+    a, b = store.compile([np.arange(64) % spec.vocab, np.arange(40) % spec.vocab])   # 4 + 3 blocks
+    assert store.free_blocks() == 3
+    with pytest.raises(PicError) as e:
+        store.link([([a, b], np.zeros(16, dtype=np.int32))] * 2, 16)
+    assert e.value.status == L.PIC_ERR_OUT_OF_BLOCKS and store.free_blocks() == 3
+    with pytest.raises(PicError) as e:
+        store.compile([np.array([spec.vocab])])
+    assert e.value.status == L.PIC_ERR_INVALID_ARG and store.free_blocks() == 3
+    with pytest.raises(PicError) as e:
+        store.link([([a, 999], np.zeros(4, dtype=np.int32))], 2)
+    assert e.value.status == L.PIC_ERR_INVALID_ARG
+    res = store.link([([a, b], np.zeros(16, dtype=np.int32))], 16)
+    assert store.free_blocks() == 0
+    store.release_chunk(a)                    # still used by the request
+    assert store.free_blocks() == 0
+    store.release_request(res.requests[0])    # frees 3 private blocks and chunk a's 4
+    assert store.free_blocks() == 7
+    store.release_chunk(b)
+    assert store.free_blocks() == 10
+    store.sync()
