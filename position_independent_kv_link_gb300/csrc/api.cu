@@ -25,6 +25,7 @@ static thread_local std::string g_last_error;
 void set_error(const std::string& msg) { g_last_error = msg; }
 pic_status fail(pic_status s, const std::string& msg) {
   g_last_error = msg;
+  if (s == PIC_ERR_CUDA) (void)cudaGetLastError();  // do not leak a non-sticky error into later calls
   return s;
 }
 

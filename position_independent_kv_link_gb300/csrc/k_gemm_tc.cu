@@ -137,7 +137,7 @@ struct TcParams {
 __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_x,
                    const TcParams p) {
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int stage_bytes = A_STAGE_BYTES + p.BN * BK * 2;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.stages * stage_bytes);
@@ -312,7 +312,7 @@ pic_status tc_gemm_run(const void* W, const void* X, float* part, int N, int K, 
   const int real_splits = (p.nkb + p.kb_per_split - 1) / p.kb_per_split;
   if (real_splits != splits) return fail(PIC_ERR_INVALID_ARG, "tcgen05 gemm: split count leaves an empty split");
   const int stage_bytes = A_STAGE_BYTES + p.BN * BK * 2;
-  const int budget = 227 * 1024 - 1024 - 256;
+  const int budget = 227 * 1024 - 2048;  // opt-in limit minus alignment slack, barriers and static smem
   p.stages = std::max(2, std::min(8, budget / stage_bytes));
   p.tmem_cols = 32;
   while ((int)p.tmem_cols < p.BN) p.tmem_cols <<= 1;
@@ -321,13 +321,14 @@ pic_status tc_gemm_run(const void* W, const void* X, float* part, int N, int K, 
   if (!make_map(&mw, W, N, K, BM) || !make_map(&mx, X, T, K, p.BN))
     return fail(PIC_ERR_CUDA, "cuTensorMapEncodeTiled failed");
   const size_t smem = 1024 + (size_t)p.stages * stage_bytes + (2 * p.stages + 2) * 8;
+  // raise the kernel's dynamic shared-memory limit to what this launch needs (once per size, per device)
   int dev = 0;
   cudaGetDevice(&dev);
-  static bool attr_set[64] = {};
-  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+  static size_t attr_smem[64] = {};
+  if (dev < 0 || dev >= 64 || attr_smem[dev] < smem) {
+    cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return fail(PIC_ERR_CUDA, std::string("tcgen05 gemm attribute: ") + cudaGetErrorString(e));
-    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+    if (dev >= 0 && dev < 64) attr_smem[dev] = smem;
   }
   dim3 grid(N / BM, (T + p.BN - 1) / p.BN, splits);
   tc_gemm_kernel<<<grid, kThreads, smem, st>>>(mw, mx, p);
