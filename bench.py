@@ -1,0 +1,405 @@
+#!/usr/bin/env python
+"""Benchmark of the LegoLink link step (position-independent KV link) at the Llama-3-8B shape.
+
+One step = one pic_link call over one request of the workload (default: 10 compiled
+chunks x 512 tokens + a 64-token query, k = 16, bf16, random-init weights): host
+metadata, request-private block copies, 32 layers of the selected rows, final norm
+and LM head. The chunks are compiled once before timing (compile is reported
+separately). Metric: linked prompt tokens per second (chunk + query tokens / link
+latency). Inputs (15 GB of weights, 0.68 GB of KV) are far larger than L2.
+
+  python bench.py [--gpus N --steps K --warmup W] [--impl reference] [--config c2]
+
+Under torchrun each rank runs an independent replica (requests are independent, so
+the link step shards by request with no collective); value = all ranks' tokens / the
+slowest rank's time. `--impl reference` times the fp64 CPU oracle on a bounded sample
+of the same workload.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import pic_inputs as pi  # noqa: E402
+
+METRIC = "linked prompt tokens/sec (link step, 8B shape)"
+UNIT = "tokens/s"
+
+# ncu dram__bytes_read.sum + dram__bytes_write.sum per launch of the tcgen05 GEMM at the
+# gate/up shape (28672 x 4096, 224 rows), measured on the source whose sha256 prefix is
+# recorded beside it; reported as null once the kernel source changes.
+GEMM_TRAFFIC = {"src_sha256_12": None, "bytes_per_launch": None, "shape": "28672x4096x224"}
+
+
+def kernel_sha() -> str:
+    p = os.path.join(ROOT, "position_independent_kv_link_gb300", "csrc", "k_gemm_tc.cu")
+    return hashlib.sha256(open(p, "rb").read()).hexdigest()[:12]
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={','.join(self.FIELDS)}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.th = threading.Thread(target=self._read, daemon=True)
+            self.th.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.th.join(timeout=2)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx = float(f[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- setup
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def workload(name: str) -> pi.Workload:
+    return pi.config_workloads()[name]
+
+
+def roofline_link(wl: pi.Workload, pk) -> dict:
+    """Roofline of one link: max(weights + KV bytes / HBM, FLOPs / bf16 peak)."""
+    sp = wl.spec
+    H, G, D = sp.n_heads, sp.n_kv_heads, sp.head_dim
+    per_layer_w = (sp.qkv_dim * sp.d_model + sp.d_model * H * D + 3 * sp.d_model * sp.ffn_dim) * 2
+    W = sp.n_layers * per_layer_w + sp.vocab * sp.d_model * 2
+    kv = 0
+    flops_attn = 0.0
+    rows = 0
+    for r in wl.requests:
+        lens = [len(wl.chunks[c]) for c in r.chunk_ids]
+        n = sum(lens) + len(r.query)
+        kv += n * G * D * 2 * 2 * sp.n_layers
+        off = 0
+        sel = []
+        for L in lens:
+            sel += list(range(off, off + min(wl.k, L)))
+            off += L
+        sel += list(range(off, off + len(r.query)))
+        rows += len(sel)
+        flops_attn += sum(p + 1 for p in sel) * H * D * 4.0 * sp.n_layers
+    flops = 2.0 * rows * (sp.n_layers * per_layer_w / 2) + 2.0 * len(wl.requests) * sp.vocab * sp.d_model + flops_attn
+    t_mem = (W + kv) / (pk["hbm_gbs"] * 1e9)
+    t_flop = flops / (pk["bf16_tflops"] * 1e12)
+    return {"bytes": W + kv, "flops": flops, "t_mem_ms": t_mem * 1e3, "t_flop_ms": t_flop * 1e3,
+            "roofline_ms": max(t_mem, t_flop) * 1e3, "bound": "hbm" if t_mem >= t_flop else "tensor"}
+
+
+# ----------------------------------------------------------------------------- CPU oracle (baseline / reference arm)
+
+def oracle_sample(wl: pi.Workload, weights, n_layers: int):
+    """Oracle link of the workload restricted to its first n_layers layers.
+
+    Compiled chunk KV is drawn from the seeded generator (the link's cost does not
+    depend on its values). Returns (seconds, OracleStore, cids) for repeated timing.
+    """
+    from oracle import pic_oracle as po
+    spec = wl.spec.with_layers(n_layers)
+    w = {k: v for k, v in weights.items() if not k.startswith("layers.") or int(k.split(".")[1]) < n_layers}
+    model = po.OracleModel(spec, w, cache_all=True)
+    need = sum(-(-len(wl.chunks[c]) // 16) for r in wl.requests for c in r.chunk_ids) + 4 * wl.selected_rows // 16 + 64
+    st = po.OracleStore(model, need)
+    cids = {}
+    for c in sorted({c for r in wl.requests for c in r.chunk_ids}):
+        k, v = pi.gen_chunk_kv(spec, len(wl.chunks[c]), c)
+        cids[c] = st.import_chunk(wl.chunks[c], [k[l] for l in range(n_layers)], [v[l] for l in range(n_layers)])
+    for l in range(n_layers):
+        model.layer(l)          # upcast once, outside the timed calls
+    return model, st, cids
+
+
+def oracle_link_time(st, cids, wl) -> float:
+    t0 = time.perf_counter()
+    out = st.link([([cids[c] for c in r.chunk_ids], r.query) for r in wl.requests], wl.k)
+    dt = time.perf_counter() - t0
+    for rid in list(st.requests):
+        st.release_request(rid)
+    for c in cids.values():
+        st.chunks[c].refs = max(st.chunks[c].refs, 1)
+    del out
+    return dt
+
+
+def cpu_threads() -> int:
+    try:
+        import threadpoolctl
+        info = threadpoolctl.threadpool_info()
+        n = max((i.get("num_threads", 0) for i in info if i.get("user_api") == "blas"), default=0)
+        if n:
+            return n
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def run_reference(args):
+    world, rank, local = dist_env()
+    if rank != 0:
+        return 0
+    wl = workload(args.config)
+    n_layers = args.cpu_layers
+    weights = pi.gen_weights(wl.spec, layers=range(n_layers))
+    model, st, cids = oracle_sample(wl, weights, n_layers)
+    scale = wl.spec.n_layers / n_layers
+    for _ in range(args.warmup):
+        oracle_link_time(st, cids, wl)
+    ts = [oracle_link_time(st, cids, wl) for _ in range(args.steps)]
+    step_s = statistics.mean(ts) * scale
+    tokens = wl.linked_tokens
+    value = tokens / step_s
+    sample = (f"oracle link of '{wl.name}' over the first {n_layers} of {wl.spec.n_layers} layers "
+              f"(+ final norm and LM head), time scaled x{scale:g} to all layers; chunk KV from the seeded generator")
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": wl.name, "k": wl.k, "linked_tokens": tokens, "selected_rows": wl.selected_rows},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+def run_ours(args):
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    from position_independent_kv_link_gb300 import PicModel, PicStore
+
+    wl = workload(args.config)
+    spec = wl.spec
+    pk = peaks()
+    t0 = time.time()
+    weights = pi.gen_weights(spec)
+    t_gen = time.time() - t0
+    model = PicModel(spec, weights)
+    cpu_weights = weights if (rank == 0 and not args.no_cpu_baseline) else None
+    if cpu_weights is None:
+        del weights
+    n_pos = max(sum(len(wl.chunks[c]) for c in r.chunk_ids) + len(r.query) for r in wl.requests)
+    n_blocks = sum(-(-len(c) // 16) for c in wl.chunks) + 4 * (wl.selected_rows // 16 + 2 * len(wl.requests) * 10)
+    store = PicStore(model, num_blocks=n_blocks, max_rows=max(wl.selected_rows, 2048),
+                     max_requests=max(len(wl.requests), 64), max_positions=n_pos + 64,
+                     max_logit_rows=max(64, len(wl.requests)))
+    # compile every chunk once (timed separately; batches of up to 4 chunks)
+    torch.cuda.synchronize()
+    c0 = time.perf_counter()
+    cids = []
+    for i in range(0, len(wl.chunks), 4):
+        cids += store.compile(wl.chunks[i:i + 4], n_dummy=wl.n_dummy)
+    store.sync()
+    compile_s = time.perf_counter() - c0
+    compiled_tokens = sum(len(c) for c in wl.chunks)
+
+    reqs = [([cids[c] for c in r.chunk_ids], r.query) for r in wl.requests]
+    n_q = sum(len(r.query) for r in wl.requests)
+    hid = torch.empty((n_q, spec.d_model), dtype=torch.float32, device="cuda")
+    lg = torch.empty((len(wl.requests), spec.vocab), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        res = store.link(reqs, wl.k, hidden_out=hid, logits_out=lg)
+        for r in res.requests:
+            store.release_request(r)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    store.sync()
+    barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    launches0 = store.launch_count()
+    store.profile_begin()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    prof = store.profile_end()
+    launches = store.launch_count() - launches0
+    # keep the GPU busy a little longer so the clock sampler sees the loaded state
+    for _ in range(min(args.steps, 5)):
+        step()
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1)
+    store.sync()
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_step = ms / args.steps
+    tokens = wl.linked_tokens
+    value = world * tokens * args.steps / (ms / 1e3)
+
+    # end to end through the public API: host query tokens in, hidden + logits to pinned host
+    hid_h = torch.empty(hid.shape, dtype=hid.dtype, pin_memory=True)
+    lg_h = torch.empty(lg.shape, dtype=lg.dtype, pin_memory=True)
+    def e2e_step():
+        res = store.link(reqs, wl.k, hidden_out=hid, logits_out=lg)
+        hid_h.copy_(hid, non_blocking=True)
+        lg_h.copy_(lg, non_blocking=True)
+        stream.synchronize()
+        for r in res.requests:
+            store.release_request(r)
+    for _ in range(3):
+        e2e_step()
+    barrier()
+    w0 = time.perf_counter()
+    for _ in range(args.steps):
+        e2e_step()
+    w_s = time.perf_counter() - w0
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([w_s], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        w_s = float(t.item())
+    e2e_value = world * tokens * args.steps / w_s
+    h2d = sum(4 * (len(r.query) + len(r.chunk_ids)) for r in wl.requests)
+    d2h = hid.numel() * 4 + lg.numel() * 4
+
+    rl = roofline_link(wl, pk)
+    g = prof["gemm"]
+    achieved = g["bytes"] / (g["ms"] / 1e3) / 1e9 if g["ms"] > 0 else None
+    traffic = None
+    if GEMM_TRAFFIC["src_sha256_12"] == kernel_sha():
+        traffic = GEMM_TRAFFIC["bytes_per_launch"]
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded random-init weights and uniform token ids)",
+        "config": {"workload": wl.name, "k": wl.k, "linked_tokens": tokens, "selected_rows": wl.selected_rows,
+                   "l2": "inputs larger than L2 (15 GB weights + 0.68 GB KV per step)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "kernel": "tcgen05 GEMM (all projections + LM head)",
+                     "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": (achieved / pk["hbm_gbs"]) if achieved else None, "traffic": traffic,
+                     "peak_source": pk["source"]},
+        "link_roofline": {"roofline_ms": rl["roofline_ms"], "bound": rl["bound"], "measured_ms": ms_step,
+                          "frac": rl["roofline_ms"] / ms_step, "bytes": rl["bytes"], "flops": rl["flops"],
+                          "t_mem_ms": rl["t_mem_ms"], "t_flop_ms": rl["t_flop_ms"]},
+        "kernels": {k: {"ms_per_step": v["ms"] / args.steps, "launches_per_step": v["launches"] / args.steps,
+                        "GBs": v["bytes"] / (v["ms"] / 1e3) / 1e9 if v["ms"] > 0 else None,
+                        "TFs": v["flops"] / (v["ms"] / 1e3) / 1e12 if v["ms"] > 0 else None}
+                    for k, v in prof.items() if isinstance(v, dict)},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches,
+        "clocks": clk,
+        "compile": {"tokens_per_s": compiled_tokens / compile_s, "ms": compile_s * 1e3, "chunks": len(wl.chunks)},
+        "setup_s": {"weights_gen": t_gen},
+    }
+    if cpu_weights is not None:
+        n_l = args.cpu_layers
+        model_o, st_o, cids_o = oracle_sample(wl, cpu_weights, n_l)
+        t = oracle_link_time(st_o, cids_o, wl)
+        cpu_step = t * wl.spec.n_layers / n_l
+        line["cpu_baseline"] = {
+            "value": tokens / cpu_step, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
+            "sample": f"fp64 oracle link of this workload over the first {n_l} of {spec.n_layers} layers (+ LM head), "
+                      f"{t:.1f} s, scaled x{spec.n_layers / n_l:g}; chunk KV from the seeded generator"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="c2", help="tiny, c2, c3, c4, c5_k{0,2,16,32,512}")
+    ap.add_argument("--cpu-layers", type=int, default=2)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -185,6 +185,32 @@ pic_status pic_release_request(pic_store* s, pic_request r);
  * bounded wait since the last pic_sync (the flag is then cleared). */
 pic_status pic_sync(pic_store* s, pic_stream_t stream);
 
+/* ------------------------------------------------------------------ profiling
+ * Between pic_profile_begin and pic_profile_end the store brackets each of its kernel
+ * launches with CUDA events on the launch stream and records the algorithmic bytes and
+ * FLOPs of that launch (operands read once, results written once). Launch counting is
+ * always on. Classes: */
+enum {
+  PIC_PROF_GEMM = 0,       /* tcgen05 / SIMT projection GEMMs (incl. LM head) */
+  PIC_PROF_ATTENTION = 1,  /* paged attention + split merge */
+  PIC_PROF_ROWWISE = 2,    /* embedding/norm, split-K epilogues, SwiGLU */
+  PIC_PROF_COPY = 3,       /* request-private block copies, KV import */
+  PIC_PROF_CLASSES = 4
+};
+typedef struct {
+  int64_t launches[PIC_PROF_CLASSES];  /* kernel launches recorded while profiling */
+  double ms[PIC_PROF_CLASSES];         /* summed event time of those launches */
+  double bytes[PIC_PROF_CLASSES];      /* summed algorithmic bytes */
+  double flops[PIC_PROF_CLASSES];      /* summed algorithmic FLOPs */
+  int64_t total_launches;              /* all kernel launches by this store since creation */
+} pic_profile;
+
+pic_status pic_profile_begin(pic_store* s);
+/* Synchronizes the recorded streams, fills `out` and stops recording. */
+pic_status pic_profile_end(pic_store* s, pic_profile* out);
+/* Kernel launches made by this store since creation (host counter, no sync). */
+int64_t pic_store_launch_count(const pic_store* s);
+
 /* ------------------------------------------------------------------ kernel-level calls
  * Single steps of the link path, exposed for testing and profiling. All pointers are
  * device pointers unless stated; all work is async on `stream`.

@@ -313,7 +313,7 @@ class OracleStore:
 
     def import_chunk(self, tokens: np.ndarray, k_layers, v_layers) -> int:
         """Store externally produced chunk KV (per layer [L, G, D]) as if compiled."""
-        return self._add_chunk(tokens, [np.asarray(a) for a in k_layers], [np.asarray(a) for a in v_layers])
+        return self._add_chunk(tokens, [_f64(a) for a in k_layers], [_f64(a) for a in v_layers])
 
     def release_chunk(self, cid: int) -> None:
         c = self.chunks[cid]

@@ -40,6 +40,15 @@ class RequestInfo(C.Structure):
                 ("private_blocks", C.POINTER(C.c_int32))]
 
 
+PROF_CLASSES = 4
+
+
+class Profile(C.Structure):
+    _fields_ = [("launches", C.c_int64 * PROF_CLASSES), ("ms", C.c_double * PROF_CLASSES),
+                ("bytes", C.c_double * PROF_CLASSES), ("flops", C.c_double * PROF_CLASSES),
+                ("total_launches", C.c_int64)]
+
+
 P = C.c_void_p
 I32 = C.c_int32
 PI32 = C.POINTER(C.c_int32)
@@ -62,6 +71,9 @@ SIGNATURES = {
     "pic_release_chunk": (I32, [P, I32]),
     "pic_release_request": (I32, [P, I32]),
     "pic_sync": (I32, [P, P]),
+    "pic_profile_begin": (I32, [P]),
+    "pic_profile_end": (I32, [P, C.POINTER(Profile)]),
+    "pic_store_launch_count": (C.c_int64, [P]),
     "pic_op_gemm_scratch_bytes": (C.c_size_t, [I32, I32, I32, I32]),
     "pic_op_gemm": (I32, [I32, P, P, P, I32, I32, I32, P, C.c_size_t, P]),
     "pic_op_attention_scratch_bytes": (C.c_size_t, [I32, I32, I32, I32, I32]),

@@ -189,6 +189,22 @@ class PicStore:
     def free_blocks(self) -> int:
         return int(self.lib.pic_store_free_blocks(self.handle))
 
+    def profile_begin(self):
+        L.check(self.lib.pic_profile_begin(self.handle))
+
+    def profile_end(self) -> Dict[str, Dict[str, float]]:
+        """Per kernel class: launches, summed event ms, algorithmic bytes and FLOPs."""
+        p = L.Profile()
+        L.check(self.lib.pic_profile_end(self.handle, C.byref(p)))
+        names = ["gemm", "attention", "rowwise", "copy"]
+        out = {n: {"launches": int(p.launches[i]), "ms": p.ms[i], "bytes": p.bytes[i], "flops": p.flops[i]}
+               for i, n in enumerate(names)}
+        out["total_launches"] = int(p.total_launches)
+        return out
+
+    def launch_count(self) -> int:
+        return int(self.lib.pic_store_launch_count(self.handle))
+
     def sync(self, stream=None):
         L.check(self.lib.pic_sync(self.handle, _stream(stream)))
 

@@ -123,6 +123,28 @@ struct pic_store {
   cudaEvent_t meta_ev = nullptr;
   bool meta_ev_pending = false;
 
+  // profiling: event pairs around launches while enabled; launch counter always on
+  struct ProfRec {
+    int cls;
+    cudaEvent_t a, b;
+    double bytes, flops;
+    int launches;
+  };
+  bool prof_on = false;
+  std::vector<ProfRec> prof;
+  std::vector<cudaEvent_t> ev_pool;
+  size_t ev_used = 0;
+  int64_t launches = 0;
+
+  cudaEvent_t next_event() {
+    if (ev_used == ev_pool.size()) {
+      cudaEvent_t e;
+      if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+      ev_pool.push_back(e);
+    }
+    return ev_pool[ev_used++];
+  }
+
   int scratch_block() const { return cfg.num_blocks; }
   int blocks_total() const { return cfg.num_blocks + 1; }
   size_t block_bytes() const {
@@ -161,6 +183,29 @@ pic_status gemm(const pic_store* s, const void* W, const void* X, float* part, i
   launch_gemm_simt(s->m->cfg.dtype, W, X, part, N, K, T, splits, st);
   return PIC_OK;
 }
+
+// Brackets one step (one or more kernel launches) with profiling events when enabled.
+struct Rec {
+  pic_store* s;
+  cudaStream_t st;
+  pic_store::ProfRec r{};
+  Rec(pic_store* s_, cudaStream_t st_, int cls, double bytes, double flops, int n_launch) : s(s_), st(st_) {
+    s->launches += n_launch;
+    if (!s->prof_on) return;
+    r.cls = cls;
+    r.bytes = bytes;
+    r.flops = flops;
+    r.launches = n_launch;
+    r.a = s->next_event();
+    r.b = s->next_event();
+    if (r.a) cudaEventRecord(r.a, st);
+  }
+  ~Rec() {
+    if (!s->prof_on || !r.a || !r.b) return;
+    cudaEventRecord(r.b, st);
+    s->prof.push_back(r);
+  }
+};
 
 // Uploads the batch metadata and runs embedding, every layer, and (link) the LM head.
 pic_status run_forward(pic_store* s, const Batch& b, float* hidden_out, float* logits_out, cudaStream_t st) {
@@ -220,8 +265,33 @@ pic_status run_forward(pic_store* s, const Batch& b, float* hidden_out, float* l
   PIC_CUDA(cudaEventRecord(s->meta_ev, st));
   s->meta_ev_pending = true;
 
+  const size_t es = dtype_size(dt);
+  const double dT = T, dd = d, dHD = (double)H * D, dF = F, dQKV = s->m->qkv_dim();
   // copy-on-write of the request-private first blocks (all layers, K and V)
-  launch_copy_blocks((int)NC / 2, d_copy, c.n_layers, s->blocks_total(), s->block_bytes(), s->k_pool, s->v_pool, st);
+  if (NC) {
+    Rec r(s, st, PIC_PROF_COPY, (double)NC / 2 * 2 * 2 * c.n_layers * s->block_bytes(), 0, 1);
+    launch_copy_blocks((int)NC / 2, d_copy, c.n_layers, s->blocks_total(), s->block_bytes(), s->k_pool, s->v_pool, st);
+  }
+
+  // attention work per layer: KV pages read once, queries and outputs once
+  double att_kv_bytes = 0, att_pairs = 0;
+  for (size_t q = 0; q < b.seq_row_begin.size(); ++q) {
+    int last = -1;
+    for (int r = b.seq_row_begin[q]; r < b.seq_row_end[q]; ++r) last = std::max(last, b.pos[r]);
+    for (int p = b.seq_page_begin[q]; p < b.seq_page_end[q]; ++p)
+      if (b.ppos[p] <= last) att_kv_bytes += (double)b.plen[p] * G * D * 2 * es;
+    // visible keys of a row: full pages before its page + the visible part of its page
+    const int p0 = b.seq_page_begin[q], p1 = b.seq_page_end[q];
+    std::vector<double> cum(p1 - p0 + 1, 0.0);
+    for (int p = p0; p < p1; ++p) cum[p - p0 + 1] = cum[p - p0] + b.plen[p];
+    for (int r = b.seq_row_begin[q]; r < b.seq_row_end[q]; ++r) {
+      const int p = (int)(std::upper_bound(b.ppos.begin() + p0, b.ppos.begin() + p1, b.pos[r]) - b.ppos.begin()) - 1;
+      if (p >= p0) att_pairs += cum[p - p0] + std::min(b.plen[p], b.pos[r] - b.ppos[p] + 1);
+    }
+  }
+  const double att_bytes = att_kv_bytes + 2 * dT * dHD * es;
+  const double att_flops = att_pairs * H * D * 4.0;
+  const int att_launches = 1 + (combs.empty() ? 0 : 1);
 
   AttnArgs aa{};
   aa.dtype = dt;
@@ -247,34 +317,58 @@ pic_status run_forward(pic_store* s, const Batch& b, float* hidden_out, float* l
   const int sp_o = gemm_splits(s, d, H * D, T);
   const int sp_gu = gemm_splits(s, 2 * F, d, T);
   const int sp_dn = gemm_splits(s, d, F, T);
+  auto gemm_bytes = [&](double N, double K, double rows) { return N * K * es + rows * K * es + rows * N * 4; };
+  auto run_gemm = [&](const void* W, const void* X, float* part, int N, int K, int rows, int sp) {
+    Rec r(s, st, PIC_PROF_GEMM, gemm_bytes(N, K, rows), 2.0 * N * K * rows, 1);
+    return gemm(s, W, X, part, N, K, rows, sp, st);
+  };
 
-  launch_embed_norm(dt, T, d, s->m->embed, d_tok, s->m->attn_norm[0], c.rms_eps, s->h, s->x, st);
+  {
+    Rec r(s, st, PIC_PROF_ROWWISE, dT * dd * (es + 4 + es) + dT * 4, 0, 1);
+    launch_embed_norm(dt, T, d, s->m->embed, d_tok, s->m->attn_norm[0], c.rms_eps, s->h, s->x, st);
+  }
   for (int l = 0; l < c.n_layers; ++l) {
     pic_status e;
-    if ((e = gemm(s, s->m->wqkv[l], s->x, s->part, qkv, d, T, sp_qkv, st)) != PIC_OK) return e;
-    launch_qkv_epilogue(dt, T, H, G, D, s->part, sp_qkv, s->q, d_slot, s->k_layer(l), s->v_layer(l), st);
+    if ((e = run_gemm(s->m->wqkv[l], s->x, s->part, qkv, d, T, sp_qkv)) != PIC_OK) return e;
+    {
+      Rec r(s, st, PIC_PROF_ROWWISE, sp_qkv * dT * dQKV * 4 + dT * dQKV * es, 0, 1);
+      launch_qkv_epilogue(dt, T, H, G, D, s->part, sp_qkv, s->q, d_slot, s->k_layer(l), s->v_layer(l), st);
+    }
     // compile keeps only KV: the last layer's attention and MLP feed nothing stored
     if (b.compile && l == c.n_layers - 1) break;
     aa.k_layer = s->k_layer(l);
     aa.v_layer = s->v_layer(l);
-    launch_attention(aa, st);
-    if ((e = gemm(s, s->m->wo[l], s->attn, s->part, d, H * D, T, sp_o, st)) != PIC_OK) return e;
-    launch_residual_norm(dt, T, d, s->part, sp_o, s->h, s->m->mlp_norm[l], c.rms_eps, s->x, false, nullptr, nullptr,
-                         nullptr, nullptr, st);
-    if ((e = gemm(s, s->m->wgu[l], s->x, s->part, 2 * F, d, T, sp_gu, st)) != PIC_OK) return e;
-    launch_swiglu(dt, T, F, s->part, sp_gu, s->act, st);
-    if ((e = gemm(s, s->m->wdown[l], s->act, s->part, d, F, T, sp_dn, st)) != PIC_OK) return e;
+    {
+      Rec r(s, st, PIC_PROF_ATTENTION, att_bytes, att_flops, att_launches);
+      launch_attention(aa, st);
+    }
+    if ((e = run_gemm(s->m->wo[l], s->attn, s->part, d, H * D, T, sp_o)) != PIC_OK) return e;
+    {
+      Rec r(s, st, PIC_PROF_ROWWISE, sp_o * dT * dd * 4 + dT * dd * (8 + es), 0, 1);
+      launch_residual_norm(dt, T, d, s->part, sp_o, s->h, s->m->mlp_norm[l], c.rms_eps, s->x, false, nullptr,
+                           nullptr, nullptr, nullptr, st);
+    }
+    if ((e = run_gemm(s->m->wgu[l], s->x, s->part, 2 * F, d, T, sp_gu)) != PIC_OK) return e;
+    {
+      Rec r(s, st, PIC_PROF_ROWWISE, sp_gu * dT * 2 * dF * 4 + dT * dF * es, 0, 1);
+      launch_swiglu(dt, T, F, s->part, sp_gu, s->act, st);
+    }
+    if ((e = run_gemm(s->m->wdown[l], s->act, s->part, d, F, T, sp_dn)) != PIC_OK) return e;
     const bool last = l == c.n_layers - 1;
-    launch_residual_norm(dt, T, d, s->part, sp_dn, s->h, last ? s->m->final_norm : s->m->attn_norm[l + 1], c.rms_eps,
-                         s->x, last, d_out, hidden_out, d_lg, s->lm_x, st);
+    {
+      Rec r(s, st, PIC_PROF_ROWWISE, sp_dn * dT * dd * 4 + dT * dd * (8 + es), 0, 1);
+      launch_residual_norm(dt, T, d, s->part, sp_dn, s->h, last ? s->m->final_norm : s->m->attn_norm[l + 1],
+                           c.rms_eps, s->x, last, d_out, hidden_out, d_lg, s->lm_x, st);
+    }
   }
   if (!b.compile && b.n_lg > 0) {
     const int sp = gemm_splits(s, c.vocab, d, b.n_lg);
     pic_status e;
     if (sp == 1) {
-      if ((e = gemm(s, s->m->lm_head, s->lm_x, logits_out, c.vocab, d, b.n_lg, 1, st)) != PIC_OK) return e;
+      if ((e = run_gemm(s->m->lm_head, s->lm_x, logits_out, c.vocab, d, b.n_lg, 1)) != PIC_OK) return e;
     } else {
-      if ((e = gemm(s, s->m->lm_head, s->lm_x, s->part, c.vocab, d, b.n_lg, sp, st)) != PIC_OK) return e;
+      if ((e = run_gemm(s->m->lm_head, s->lm_x, s->part, c.vocab, d, b.n_lg, sp)) != PIC_OK) return e;
+      Rec r(s, st, PIC_PROF_ROWWISE, (sp + 1.0) * b.n_lg * (double)c.vocab * 4, 0, 1);
       launch_sum_partials(b.n_lg, c.vocab, s->part, sp, logits_out, st);
     }
   }
@@ -418,6 +512,7 @@ pic_status pic_store_create(pic_model* m, const pic_store_config* cfg, void* k_p
 
 pic_status pic_store_destroy(pic_store* s) {
   if (!s) return PIC_OK;
+  for (cudaEvent_t e : s->ev_pool) cudaEventDestroy(e);
   if (s->meta_ev) {
     cudaEventSynchronize(s->meta_ev);
     cudaEventDestroy(s->meta_ev);
@@ -503,6 +598,7 @@ pic_status pic_chunk_import(pic_store* s, const int32_t* tokens, int32_t n_token
   if (e == cudaSuccess) e = cudaEventRecord(s->meta_ev, st);
   if (e == cudaSuccess) {
     s->meta_ev_pending = true;
+    s->launches += 1;
     launch_import_kv(c.dtype, c.n_layers, n_tokens, c.n_kv_heads, c.head_dim, k, v, s->meta_d, s->blocks_total(),
                      s->k_pool, s->v_pool, st);
     e = cudaGetLastError();
@@ -668,6 +764,35 @@ pic_status pic_release_request(pic_store* s, pic_request r) {
   s->requests.erase(it);
   return PIC_OK;
 }
+
+pic_status pic_profile_begin(pic_store* s) {
+  if (!s) return fail(PIC_ERR_INVALID_ARG, "null store");
+  s->prof.clear();
+  s->ev_used = 0;
+  s->prof_on = true;
+  return PIC_OK;
+}
+
+pic_status pic_profile_end(pic_store* s, pic_profile* out) {
+  if (!s || !out) return fail(PIC_ERR_INVALID_ARG, "null argument");
+  std::memset(out, 0, sizeof(*out));
+  s->prof_on = false;
+  for (const auto& r : s->prof) {
+    PIC_CUDA(cudaEventSynchronize(r.b));
+    float ms = 0.f;
+    PIC_CUDA(cudaEventElapsedTime(&ms, r.a, r.b));
+    out->launches[r.cls] += r.launches;
+    out->ms[r.cls] += ms;
+    out->bytes[r.cls] += r.bytes;
+    out->flops[r.cls] += r.flops;
+  }
+  out->total_launches = s->launches;
+  s->prof.clear();
+  s->ev_used = 0;
+  return PIC_OK;
+}
+
+int64_t pic_store_launch_count(const pic_store* s) { return s ? s->launches : -1; }
 
 pic_status pic_sync(pic_store* s, pic_stream_t stream) {
   (void)s;
