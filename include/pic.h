@@ -232,7 +232,7 @@ pic_status pic_op_gemm(int32_t dtype, const void* W, const void* X, float* Y, in
  * (block, position of row 0, valid rows); k_layer/v_layer: one layer of the pools
  * ([pool_blocks][G][16][D]); every page block must be < pool_blocks. rope_cs: device
  * float2 [rope_positions][D/2] (cos, sin), e.g. from pic_op_rope_table; every position
- * must be < rope_positions. Scratch as reported by pic_op_attention_scratch_bytes. */
+ * must be < rope_positions, and rope_positions >= 16. Scratch as reported by pic_op_attention_scratch_bytes. */
 size_t pic_op_attention_scratch_bytes(int32_t T, int32_t n_heads, int32_t n_kv_heads, int32_t head_dim,
                                       int32_t n_pages);
 pic_status pic_op_attention(int32_t dtype, int32_t T, int32_t n_heads, int32_t n_kv_heads, int32_t head_dim,

@@ -478,7 +478,7 @@ pic_status pic_store_create(pic_model* m, const pic_store_config* cfg, void* k_p
                o_part = carve(s->part_floats * 4),
                o_atto = carve((size_t)s->att_parts_cap * kBlock * rep * c.head_dim * 4),
                o_attml = carve((size_t)s->att_parts_cap * kBlock * rep * 2 * 4), o_meta = carve(s->meta_cap * 4),
-               o_rope = carve((size_t)sc.max_positions * (c.head_dim / 2) * sizeof(float2));
+               o_rope = carve((size_t)std::max(16, sc.max_positions) * (c.head_dim / 2) * sizeof(float2));
   cudaError_t e = cudaMalloc(&s->ws, off);
   if (e != cudaSuccess) return fail(PIC_ERR_CUDA, std::string("workspace cudaMalloc: ") + cudaGetErrorString(e));
   s->h = (float*)(s->ws + o_h);
@@ -499,7 +499,7 @@ pic_status pic_store_create(pic_model* m, const pic_store_config* cfg, void* k_p
   }
   e = cudaEventCreateWithFlags(&s->meta_ev, cudaEventDisableTiming);
   std::vector<float2> tab;
-  rope_table_host(sc.max_positions, c.head_dim, c.rope_base, tab);
+  rope_table_host(std::max(16, sc.max_positions), c.head_dim, c.rope_base, tab);
   if (e == cudaSuccess) e = cudaMemcpy(s->rope_cs, tab.data(), tab.size() * sizeof(float2), cudaMemcpyHostToDevice);
   if (e != cudaSuccess) {
     cudaFree(s->ws);

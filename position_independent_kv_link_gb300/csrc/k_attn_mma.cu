@@ -1,7 +1,371 @@
-// Tensor-core paged attention (bf16, head_dim 128): placeholder routing to the generic kernel.
+// Tensor-core paged attention for bf16 models with head_dim 128 (mma.sync m16n8k16).
+//
+// One CTA = one work item: up to 16 consecutive query rows of one sequence x the
+// REP query heads that share KV head g (GQA) x a run of pages. Warp w owns query head
+// g*REP + w for the 16 rows (an MMA M tile). KV moves through shared memory in tiles
+// of 64 keys (4 pages), double buffered:
+//   * K: 16-byte global loads into registers, rotated by RoPE at each key's absolute
+//     position while being stored to shared memory (MEPIC abstract: K is kept without
+//     positional encoding and RoPE is fused into attention). cos/sin(p*theta) is
+//     composed from table rows 16*floor(p/16) (global, L1-resident) and p mod 16
+//     (shared), so the table read per tile is a few rows, not 64.
+//   * V: cp.async straight into shared memory.
+// S = Q K^T and O += P V run on mma.sync with fp32 accumulators; the online softmax
+// lives in registers (row max/sum by quad shuffles). Keys after the query's position,
+// padding rows of ragged pages and pages past the item's range are masked.
+// Items covering part of a row block's pages write unnormalized partials (o, m, l) that
+// the merge kernel of k_attn.cu combines.
+#include <climits>
+
 #include "pic_internal.h"
 
 namespace pic {
+
 void launch_attention_simt(const AttnArgs& a, cudaStream_t st);
-void launch_attention_mma(const AttnArgs& a, cudaStream_t st) { launch_attention_simt(a, st); }
+
+namespace {
+
+constexpr int D = 128;
+constexpr int KT = 64;                    // keys per tile
+constexpr int TILE_BYTES = KT * D * 2;    // 16 KB
+constexpr float kLog2e = 1.4426950408889634f;
+
+// byte offset of 16-byte chunk `c` (0..15) of row `r` in a [rows][128] bf16 tile, XOR-swizzled
+__device__ __forceinline__ uint32_t swz(int r, int c) { return (uint32_t)(r * 256 + ((c ^ (r & 7)) << 4)); }
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void mma16816(float* c, const uint32_t* a, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+template <int NW>
+struct KTask {  // per-thread register prefetch of K chunks for one tile
+  static constexpr int N = KT * 8 / (NW * 32);  // (key, chunk-pair) tasks per thread
+  uint4 lo[N], hi[N];
+  int pos[N];
+};
+
+template <int REP, int NW>
+__global__ void __launch_bounds__(NW * 32) attn_mma_kernel(AttnArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint8_t* sK = smem;                                  // [2][KT][D] bf16, swizzled
+  uint8_t* sV = smem + 2 * TILE_BYTES;                 // [2][KT][D]
+  uint8_t* sQ = smem + 4 * TILE_BYTES;                 // [REP][16][D]
+  float2* sLo = reinterpret_cast<float2*>(sQ + REP * 16 * D * 2);   // [16][64] cos/sin of p = 0..15
+  int* sPos = reinterpret_cast<int*>(sLo + 16 * 64);                // [2][KT] key positions (INT_MAX = masked)
+  const uint32_t sK_u = (uint32_t)__cvta_generic_to_shared(sK);
+  const uint32_t sV_u = (uint32_t)__cvta_generic_to_shared(sV);
+  const uint32_t sQ_u = (uint32_t)__cvta_generic_to_shared(sQ);
+
+  const AttnItem it = a.items[blockIdx.x];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int G = a.G;
+  const __nv_bfloat16* Kl = (const __nv_bfloat16*)a.k_layer;
+  const __nv_bfloat16* Vl = (const __nv_bfloat16*)a.v_layer;
+  const __nv_bfloat16* Q = (const __nv_bfloat16*)a.q;
+  const float qscale = rsqrtf((float)D) * kLog2e;
+
+  for (int i = tid; i < 16 * 64; i += NW * 32) sLo[i] = a.rope_cs[i];
+  __syncthreads();
+
+  // ---- Q: rotate at each row's position, scale, round to bf16, stage for ldmatrix
+  for (int i = tid; i < REP * 16 * 8; i += NW * 32) {
+    const int hh = i / 128, r = (i / 8) % 16, c = i % 8;   // dims 8c..8c+7 and 64+8c..
+    uint4 x1 = make_uint4(0, 0, 0, 0), x2 = x1;
+    if (r < it.nrows) {
+      const int t = it.row0 + r, h = it.g * REP + hh, p = a.q_pos[t];
+      const __nv_bfloat16* src = Q + ((size_t)t * a.H + h) * D;
+      const uint4 u1 = *reinterpret_cast<const uint4*>(src + 8 * c);
+      const uint4 u2 = *reinterpret_cast<const uint4*>(src + 64 + 8 * c);
+      const float2* hi = a.rope_cs + (size_t)(p & ~15) * 64 + 8 * c;
+      const float2* lo = sLo + (p & 15) * 64 + 8 * c;
+      const __nv_bfloat16* b1 = reinterpret_cast<const __nv_bfloat16*>(&u1);
+      const __nv_bfloat16* b2 = reinterpret_cast<const __nv_bfloat16*>(&u2);
+      __nv_bfloat16 o1[8], o2[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float2 H2 = hi[e], L2 = lo[e];
+        const float cs = H2.x * L2.x - H2.y * L2.y, sn = H2.y * L2.x + H2.x * L2.y;
+        const float v1 = __bfloat162float(b1[e]), v2 = __bfloat162float(b2[e]);
+        o1[e] = __float2bfloat16_rn((v1 * cs - v2 * sn) * qscale);
+        o2[e] = __float2bfloat16_rn((v2 * cs + v1 * sn) * qscale);
+      }
+      x1 = *reinterpret_cast<uint4*>(o1);
+      x2 = *reinterpret_cast<uint4*>(o2);
+    }
+    uint8_t* base = sQ + hh * 16 * D * 2;
+    *reinterpret_cast<uint4*>(base + swz(r, c)) = x1;
+    *reinterpret_cast<uint4*>(base + swz(r, c + 8)) = x2;
+  }
+
+  const int ntiles = (it.page1 - it.page0 + 3) / 4;
+  KTask<NW> kt;
+
+  auto load_k = [&](int tile) {
+#pragma unroll
+    for (int j = 0; j < KTask<NW>::N; ++j) {
+      const int task = tid + j * NW * 32;
+      const int key = task / 8, c = task % 8;
+      const int page = it.page0 + tile * 4 + key / 16, r = key % 16;
+      kt.pos[j] = INT_MAX;
+      if (page < it.page1 && r < a.page_len[page]) {
+        const int blk = a.page_block[page];
+        const __nv_bfloat16* src = Kl + (((size_t)blk * G + it.g) * kBlock + r) * D;
+        kt.lo[j] = *reinterpret_cast<const uint4*>(src + 8 * c);
+        kt.hi[j] = *reinterpret_cast<const uint4*>(src + 64 + 8 * c);
+        kt.pos[j] = a.page_pos[page] + r;
+      }
+    }
+  };
+  auto store_k = [&](int buf) {
+#pragma unroll
+    for (int j = 0; j < KTask<NW>::N; ++j) {
+      const int task = tid + j * NW * 32;
+      const int key = task / 8, c = task % 8;
+      uint4 y1 = make_uint4(0, 0, 0, 0), y2 = y1;
+      const int p = kt.pos[j];
+      if (p != INT_MAX) {
+        const float2* hi = a.rope_cs + (size_t)(p & ~15) * 64 + 8 * c;
+        const float2* lo = sLo + (p & 15) * 64 + 8 * c;
+        const __nv_bfloat16* b1 = reinterpret_cast<const __nv_bfloat16*>(&kt.lo[j]);
+        const __nv_bfloat16* b2 = reinterpret_cast<const __nv_bfloat16*>(&kt.hi[j]);
+        __nv_bfloat16 o1[8], o2[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float2 H2 = hi[e], L2 = lo[e];
+          const float cs = H2.x * L2.x - H2.y * L2.y, sn = H2.y * L2.x + H2.x * L2.y;
+          const float v1 = __bfloat162float(b1[e]), v2 = __bfloat162float(b2[e]);
+          o1[e] = __float2bfloat16_rn(v1 * cs - v2 * sn);
+          o2[e] = __float2bfloat16_rn(v2 * cs + v1 * sn);
+        }
+        y1 = *reinterpret_cast<uint4*>(o1);
+        y2 = *reinterpret_cast<uint4*>(o2);
+      }
+      uint8_t* base = sK + buf * TILE_BYTES;
+      *reinterpret_cast<uint4*>(base + swz(key, c)) = y1;
+      *reinterpret_cast<uint4*>(base + swz(key, c + 8)) = y2;
+      if (c == 0) sPos[buf * KT + key] = p;
+    }
+  };
+  auto load_v = [&](int tile, int buf) {
+    for (int task = tid; task < KT * 16; task += NW * 32) {
+      const int key = task / 16, c = task % 16;
+      const int page = it.page0 + tile * 4 + key / 16, r = key % 16;
+      const uint32_t dst = sV_u + buf * TILE_BYTES + swz(key, c);
+      if (page < it.page1 && r < a.page_len[page]) {
+        const int blk = a.page_block[page];
+        cp_async16(dst, Vl + (((size_t)blk * G + it.g) * kBlock + r) * D + 8 * c);
+      } else {
+        *reinterpret_cast<uint4*>(sV + buf * TILE_BYTES + swz(key, c)) = make_uint4(0, 0, 0, 0);
+      }
+    }
+  };
+
+  // prologue: tile 0
+  if (ntiles > 0) {
+    load_v(0, 0);
+    load_k(0);
+    store_k(0);
+  }
+  cp_async_wait_all();
+  __syncthreads();
+
+  // ---- per-warp state
+  const bool active = warp < REP;
+  const int g8 = lane >> 2, t4 = lane & 3;
+  const int qp0 = (g8 < it.nrows) ? a.q_pos[it.row0 + g8] : -1;
+  const int qp1 = (g8 + 8 < it.nrows) ? a.q_pos[it.row0 + g8 + 8] : -1;
+  uint32_t qf[8][4];
+  if (active) {
+    const uint32_t qb = sQ_u + warp * 16 * D * 2;
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      const int m = lane >> 3, row = (lane & 7) + 8 * (m & 1), c = 2 * ks + (m >> 1);
+      ldsm_x4(qb + swz(row, c), qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3]);
+    }
+  }
+  float o[16][4];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+
+  for (int tile = 0; tile < ntiles; ++tile) {
+    const int cur = tile & 1, nxt = cur ^ 1;
+    const bool has_next = tile + 1 < ntiles;
+    if (has_next) {
+      load_v(tile + 1, nxt);
+      load_k(tile + 1);
+    }
+    if (active) {
+      // S = Q K^T over 64 keys
+      float s[8][4];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
+      const uint32_t kb = sK_u + cur * TILE_BYTES;
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+#pragma unroll
+        for (int j = 0; j < 8; j += 2) {
+          const int m = lane >> 3, key = 8 * j + (lane & 7) + 8 * (m >> 1), c = 2 * ks + (m & 1);
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(kb + swz(key, c), b0, b1, b2, b3);
+          mma16816(s[j], qf[ks], b0, b1);
+          mma16816(s[j + 1], qf[ks], b2, b3);
+        }
+      }
+      // mask + online softmax (rows g8 and g8+8; this thread holds keys 8j+2t4, +1)
+      const int* kp = sPos + cur * KT;
+      float tm0 = -INFINITY, tm1 = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int p = kp[8 * j + 2 * t4 + e];
+          if (p > qp0) s[j][e] = -INFINITY;
+          if (p > qp1) s[j][2 + e] = -INFINITY;
+          tm0 = fmaxf(tm0, s[j][e]);
+          tm1 = fmaxf(tm1, s[j][2 + e]);
+        }
+      }
+      tm0 = fmaxf(tm0, __shfl_xor_sync(0xffffffffu, tm0, 1));
+      tm0 = fmaxf(tm0, __shfl_xor_sync(0xffffffffu, tm0, 2));
+      tm1 = fmaxf(tm1, __shfl_xor_sync(0xffffffffu, tm1, 1));
+      tm1 = fmaxf(tm1, __shfl_xor_sync(0xffffffffu, tm1, 2));
+      const float mn0 = fmaxf(m0, tm0), mn1 = fmaxf(m1, tm1);
+      const float ref0 = mn0 == -INFINITY ? 0.f : mn0, ref1 = mn1 == -INFINITY ? 0.f : mn1;
+      const float corr0 = exp2f(m0 - ref0), corr1 = exp2f(m1 - ref1);
+      m0 = mn0;
+      m1 = mn1;
+      float rs0 = 0.f, rs1 = 0.f;
+      uint32_t pf[4][4];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float p0 = exp2f(s[j][0] - ref0), p1 = exp2f(s[j][1] - ref0);
+        const float p2 = exp2f(s[j][2] - ref1), p3 = exp2f(s[j][3] - ref1);
+        rs0 += p0 + p1;
+        rs1 += p2 + p3;
+        pf[j >> 1][(j & 1) * 2 + 0] = pack_bf16(p0, p1);
+        pf[j >> 1][(j & 1) * 2 + 1] = pack_bf16(p2, p3);
+      }
+      l0 = l0 * corr0 + rs0;
+      l1 = l1 * corr1 + rs1;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        o[i][0] *= corr0;
+        o[i][1] *= corr0;
+        o[i][2] *= corr1;
+        o[i][3] *= corr1;
+      }
+      // O += P V
+      const uint32_t vb = sV_u + cur * TILE_BYTES;
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        // A fragment of P for keys 16kk..16kk+15: {row g8 k0-7, row g8+8 k0-7, row g8 k8-15, row g8+8 k8-15}
+        const uint32_t af[4] = {pf[kk][0], pf[kk][1], pf[kk][2], pf[kk][3]};
+#pragma unroll
+        for (int dn = 0; dn < 16; dn += 2) {
+          const int m = lane >> 3, key = 16 * kk + (lane & 7) + 8 * (m & 1), c = dn + (m >> 1);
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4_t(vb + swz(key, c), b0, b1, b2, b3);
+          mma16816(o[dn], af, b0, b1);
+          mma16816(o[dn + 1], af, b2, b3);
+        }
+      }
+    }
+    if (has_next) store_k(nxt);
+    cp_async_wait_all();
+    __syncthreads();
+  }
+
+  if (!active) return;
+  l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+  l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+  l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+  l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+  const int hh = warp, h = it.g * REP + hh;
+  if (it.part < 0) {
+    __nv_bfloat16* out = (__nv_bfloat16*)a.out;
+    const float i0 = l0 > 0.f ? 1.f / l0 : 0.f, i1 = l1 > 0.f ? 1.f / l1 : 0.f;
+#pragma unroll
+    for (int dn = 0; dn < 16; ++dn) {
+      const int dcol = 8 * dn + 2 * t4;
+      if (g8 < it.nrows)
+        *reinterpret_cast<uint32_t*>(out + ((size_t)(it.row0 + g8) * a.H + h) * D + dcol) =
+            pack_bf16(o[dn][0] * i0, o[dn][1] * i0);
+      if (g8 + 8 < it.nrows)
+        *reinterpret_cast<uint32_t*>(out + ((size_t)(it.row0 + g8 + 8) * a.H + h) * D + dcol) =
+            pack_bf16(o[dn][2] * i1, o[dn][3] * i1);
+    }
+  } else {
+    const size_t p0 = ((size_t)it.part * kBlock + g8) * REP + hh;
+    const size_t p1 = ((size_t)it.part * kBlock + g8 + 8) * REP + hh;
+#pragma unroll
+    for (int dn = 0; dn < 16; ++dn) {
+      const int dcol = 8 * dn + 2 * t4;
+      *reinterpret_cast<float2*>(a.part_o + p0 * D + dcol) = make_float2(o[dn][0], o[dn][1]);
+      *reinterpret_cast<float2*>(a.part_o + p1 * D + dcol) = make_float2(o[dn][2], o[dn][3]);
+    }
+    if (t4 == 0) {
+      a.part_ml[p0 * 2] = m0;
+      a.part_ml[p0 * 2 + 1] = l0;
+      a.part_ml[p1 * 2] = m1;
+      a.part_ml[p1 * 2 + 1] = l1;
+    }
+  }
+}
+
+template <int REP, int NW>
+void launch_rep(const AttnArgs& a, cudaStream_t st) {
+  const size_t smem = 4 * TILE_BYTES + REP * 16 * D * 2 + 16 * 64 * sizeof(float2) + 2 * KT * sizeof(int);
+  static bool attr[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64 || !attr[dev]) {
+    cudaFuncSetAttribute(attn_mma_kernel<REP, NW>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (dev >= 0 && dev < 64) attr[dev] = true;
+  }
+  attn_mma_kernel<REP, NW><<<a.n_items, NW * 32, smem, st>>>(a);
+}
+
+}  // namespace
+
+void launch_attention_mma(const AttnArgs& a, cudaStream_t st) {
+  const int rep = a.H / a.G;
+  if (a.n_items > 0) {
+    switch (rep) {
+      case 1: launch_rep<1, 4>(a, st); break;
+      case 2: launch_rep<2, 4>(a, st); break;
+      case 4: launch_rep<4, 4>(a, st); break;
+      case 8: launch_rep<8, 8>(a, st); break;
+      default: launch_attention_simt(a, st); return;
+    }
+  }
+  if (a.n_combines > 0) {
+    AttnArgs b = a;
+    b.n_items = 0;  // merge only
+    launch_attention_simt(b, st);
+  }
+}
+
 }  // namespace pic

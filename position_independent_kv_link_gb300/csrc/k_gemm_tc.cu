@@ -26,10 +26,10 @@ namespace pic {
 
 namespace {
 
-constexpr int BM = 128;          // weight rows per tile (MMA M)
+constexpr int BM = 128;          // weight rows per MMA (M); a CTA tile holds 1 or 2 of these
 constexpr int BK = 64;           // K per stage: 64 bf16 = one 128-byte swizzle row
 constexpr int UMMA_K = 16;       // K per tcgen05.mma (kind::f16)
-constexpr int A_STAGE_BYTES = BM * BK * 2;
+constexpr int A_HALF_BYTES = BM * BK * 2;
 constexpr int kThreads = 128;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
@@ -134,9 +134,13 @@ struct TcParams {
   float* part;
 };
 
+// MH = 128-row weight halves per CTA tile. Both halves share the staged activation
+// tile, so MH = 2 halves the activation bytes read from L2 per weight byte streamed.
+template <int MH>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_x,
                    const TcParams p) {
+  constexpr int A_STAGE_BYTES = MH * A_HALF_BYTES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int stage_bytes = A_STAGE_BYTES + p.BN * BK * 2;
@@ -146,7 +150,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ volatile int s_abort;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int m0 = blockIdx.x * BM, t0 = blockIdx.y * p.BN, split = blockIdx.z;
+  const int m0 = blockIdx.x * BM * MH, t0 = blockIdx.y * p.BN, split = blockIdx.z;
   const int kb0 = split * p.kb_per_split;
   const int nk = min(p.nkb - kb0, p.kb_per_split);
   const uint32_t acc_bar = smem_u32(bars + 2 * p.stages);
@@ -185,7 +189,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t b_dst = a_dst + A_STAGE_BYTES;
       mbar_expect_tx(full, stage_bytes);
       const int kx = (kb0 + kb) * BK;
-      tma_load_2d(a_dst, &map_w, kx, m0, full, pol_w);
+#pragma unroll
+      for (int hf = 0; hf < MH; ++hf) tma_load_2d(a_dst + hf * A_HALF_BYTES, &map_w, kx, m0 + hf * BM, full, pol_w);
       tma_load_2d(b_dst, &map_x, kx, t0, full, pol_x);
       issued = kb + 1;
     }
@@ -206,9 +211,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t b_base = a_base + A_STAGE_BYTES;
 #pragma unroll
       for (int k = 0; k < BK / UMMA_K; ++k) {
-        const uint64_t ad = smem_desc_sw128(a_base + k * UMMA_K * 2);
         const uint64_t bd = smem_desc_sw128(b_base + k * UMMA_K * 2);
-        umma_bf16(tmem, ad, bd, idesc, (kb | k) != 0);
+#pragma unroll
+        for (int hf = 0; hf < MH; ++hf) {
+          const uint64_t ad = smem_desc_sw128(a_base + hf * A_HALF_BYTES + k * UMMA_K * 2);
+          umma_bf16(tmem + hf * p.BN, ad, bd, idesc, (kb | k) != 0);
+        }
       }
       umma_commit(smem_u32(bars + p.stages + st));  // stage free once these MMAs retire
     }
@@ -221,17 +229,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   ok = __all_sync(0xffffffffu, ok) && !s_abort;  // warp-uniform and reconverged for .sync.aligned loads
   asm volatile("tcgen05.fence::after_thread_sync;");
   if (ok) {
-    const int n = m0 + warp * 32 + lane;
     float* out = p.part + (size_t)split * p.T * p.N;
     const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
-    for (int c = 0; c < p.BN; c += 16) {
-      float v[16];
-      tmem_ld16(lane_base + c, v);
-      if (n < p.N) {
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int t = t0 + c + j;
-          if (t < p.T) out[(size_t)t * p.N + n] = v[j];
+    for (int hf = 0; hf < MH; ++hf) {
+      const int n = m0 + hf * BM + warp * 32 + lane;
+      for (int c = 0; c < p.BN; c += 16) {
+        float v[16];
+        tmem_ld16(lane_base + hf * p.BN + c, v);
+        if (n < p.N) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int t = t0 + c + j;
+            if (t < p.T) out[(size_t)t * p.N + n] = v[j];
+          }
         }
       }
     }
@@ -276,9 +287,13 @@ int pick_bn(int T) {
 
 bool tc_gemm_supported(int N, int K, int T) { return N >= BM && N % BM == 0 && K >= BK && K % BK == 0 && T >= 1; }
 
+// Two weight halves per CTA when the shape allows (N multiple of 256, at most 256 token
+// rows per tile so both fp32 accumulators fit the 512 TMEM columns).
+int pick_mh(int N, int T) { return (N % (2 * BM) == 0) ? 2 : 1; }
+
 int tc_gemm_splits(int N, int K, int T, int num_sms, int max_splits) {
   const int BN = pick_bn(T);
-  const long long tiles = (long long)(N / BM) * ((T + BN - 1) / BN);
+  const long long tiles = (long long)(N / (BM * pick_mh(N, T))) * ((T + BN - 1) / BN);
   const int nkb = K / BK;
   const int smax = std::max(1, std::min({max_splits, nkb / 4, 16}));
   const double epi = 2.0;  // epilogue cost in k-block units
@@ -311,11 +326,12 @@ pic_status tc_gemm_run(const void* W, const void* X, float* part, int N, int K, 
   p.kb_per_split = (p.nkb + splits - 1) / splits;
   const int real_splits = (p.nkb + p.kb_per_split - 1) / p.kb_per_split;
   if (real_splits != splits) return fail(PIC_ERR_INVALID_ARG, "tcgen05 gemm: split count leaves an empty split");
-  const int stage_bytes = A_STAGE_BYTES + p.BN * BK * 2;
+  const int mh = pick_mh(N, T);
+  const int stage_bytes = mh * A_HALF_BYTES + p.BN * BK * 2;
   const int budget = 227 * 1024 - 2048;  // opt-in limit minus alignment slack, barriers and static smem
   p.stages = std::max(2, std::min(8, budget / stage_bytes));
   p.tmem_cols = 32;
-  while ((int)p.tmem_cols < p.BN) p.tmem_cols <<= 1;
+  while ((int)p.tmem_cols < mh * p.BN) p.tmem_cols <<= 1;
   p.part = part;
   CUtensorMap mw, mx;
   if (!make_map(&mw, W, N, K, BM) || !make_map(&mx, X, T, K, p.BN))
@@ -324,14 +340,15 @@ pic_status tc_gemm_run(const void* W, const void* X, float* part, int N, int K, 
   // raise the kernel's dynamic shared-memory limit to what this launch needs (once per size, per device)
   int dev = 0;
   cudaGetDevice(&dev);
-  static size_t attr_smem[64] = {};
-  if (dev < 0 || dev >= 64 || attr_smem[dev] < smem) {
-    cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  static size_t attr_smem[2][64] = {};
+  auto kern = mh == 2 ? tc_gemm_kernel<2> : tc_gemm_kernel<1>;
+  if (dev < 0 || dev >= 64 || attr_smem[mh - 1][dev] < smem) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return fail(PIC_ERR_CUDA, std::string("tcgen05 gemm attribute: ") + cudaGetErrorString(e));
-    if (dev >= 0 && dev < 64) attr_smem[dev] = smem;
+    if (dev >= 0 && dev < 64) attr_smem[mh - 1][dev] = smem;
   }
-  dim3 grid(N / BM, (T + p.BN - 1) / p.BN, splits);
-  tc_gemm_kernel<<<grid, kThreads, smem, st>>>(mw, mx, p);
+  dim3 grid(N / (BM * mh), (T + p.BN - 1) / p.BN, splits);
+  kern<<<grid, kThreads, smem, st>>>(mw, mx, p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(PIC_ERR_CUDA, std::string("tcgen05 gemm launch: ") + cudaGetErrorString(e));
   return PIC_OK;

@@ -2,6 +2,8 @@
 // RMSNorm, split-K reductions fused with their epilogues (QKV scatter into pages,
 // residual + RMSNorm, SwiGLU), block copies for request-private pages, KV import.
 // All are HBM/L2-bound; one CTA per row with 16-byte-friendly strided loops.
+#include <algorithm>
+
 #include "pic_internal.h"
 
 namespace pic {
@@ -50,30 +52,58 @@ __global__ void embed_norm_kernel(int d, const T* __restrict__ E, const int* __r
   }
 }
 
+template <typename T>
+__device__ __forceinline__ void store4(T* dst, float4 v);
+template <>
+__device__ __forceinline__ void store4<float>(float* dst, float4 v) {
+  *reinterpret_cast<float4*>(dst) = v;
+}
+template <>
+__device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16* dst, float4 v) {
+  __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
+  uint2 u;
+  u.x = *reinterpret_cast<uint32_t*>(&a);
+  u.y = *reinterpret_cast<uint32_t*>(&b);
+  *reinterpret_cast<uint2*>(dst) = u;
+}
+
+__device__ __forceinline__ float4 sum4(const float* __restrict__ part, int splits, size_t stride, size_t off) {
+  float4 acc = *reinterpret_cast<const float4*>(part + off);
+  for (int s = 1; s < splits; ++s) {
+    const float4 v = *reinterpret_cast<const float4*>(part + (size_t)s * stride + off);
+    acc.x += v.x;
+    acc.y += v.y;
+    acc.z += v.z;
+    acc.w += v.w;
+  }
+  return acc;
+}
+
 // QKV epilogue: sum split-K slabs; q -> [T][H*D]; k, v -> page slot of this layer.
+// grid (T, ceil(N / 1024)); each thread owns 4 consecutive columns (same head).
 template <typename T>
 __global__ void qkv_epilogue_kernel(int T_, int H, int G, int D, const float* __restrict__ part, int splits,
                                     T* __restrict__ q, const int* __restrict__ slot, T* __restrict__ kl,
                                     T* __restrict__ vl) {
   const int t = blockIdx.x;
   const int N = (H + 2 * G) * D;
-  const int s_ = slot[t];
-  const int blk = s_ / kBlock, r = s_ % kBlock;
-  for (int n = threadIdx.x; n < N; n += blockDim.x) {
-    float acc = 0.f;
-    for (int s = 0; s < splits; ++s) acc += part[((size_t)s * T_ + t) * N + n];
-    if (n < H * D) {
-      q[(size_t)t * H * D + n] = from_f<T>(acc);
-    } else {
-      const int m = n - H * D;
-      const int kv = m / (G * D);          // 0: K, 1: V
-      const int g = (m % (G * D)) / D, i = m % D;
-      T* dst = kv == 0 ? kl : vl;
-      dst[(((size_t)blk * G + g) * kBlock + r) * D + i] = from_f<T>(acc);
-    }
+  const int n = (blockIdx.y * blockDim.x + threadIdx.x) * 4;
+  if (n >= N) return;
+  const float4 acc = sum4(part, splits, (size_t)T_ * N, (size_t)t * N + n);
+  if (n < H * D) {
+    store4<T>(q + (size_t)t * H * D + n, acc);
+  } else {
+    const int s_ = slot[t];
+    const int blk = s_ / kBlock, r = s_ % kBlock;
+    const int m = n - H * D;
+    const int kv = m / (G * D);          // 0: K, 1: V
+    const int g = (m % (G * D)) / D, i = m % D;
+    T* dst = kv == 0 ? kl : vl;
+    store4<T>(dst + (((size_t)blk * G + g) * kBlock + r) * D + i, acc);
   }
 }
 
+// h[t] += sum of split slabs; then RMSNorm. One CTA per row, 4 columns per thread-step.
 template <typename T>
 __global__ void residual_norm_kernel(int T_, int d, const float* __restrict__ part, int splits,
                                      float* __restrict__ h, const float* __restrict__ gain, float eps,
@@ -84,39 +114,45 @@ __global__ void residual_norm_kernel(int T_, int d, const float* __restrict__ pa
   __shared__ float red[32];
   const int t = blockIdx.x;
   float ss = 0.f;
-  for (int i = threadIdx.x; i < d; i += blockDim.x) {
-    float v = h[(size_t)t * d + i];
-    for (int s = 0; s < splits; ++s) v += part[((size_t)s * T_ + t) * d + i];
-    row[i] = v;
-    h[(size_t)t * d + i] = v;
-    ss += v * v;
+  for (int i = threadIdx.x * 4; i < d; i += blockDim.x * 4) {
+    float4 v = *reinterpret_cast<const float4*>(h + (size_t)t * d + i);
+    const float4 a = sum4(part, splits, (size_t)T_ * d, (size_t)t * d + i);
+    v.x += a.x;
+    v.y += a.y;
+    v.z += a.z;
+    v.w += a.w;
+    *reinterpret_cast<float4*>(row + i) = v;
+    *reinterpret_cast<float4*>(h + (size_t)t * d + i) = v;
+    ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
   }
   ss = block_sum(ss, red);
   const float r = rsqrtf(ss / d + eps);
-  if (!final_layer) {
-    for (int i = threadIdx.x; i < d; i += blockDim.x) x[(size_t)t * d + i] = from_f<T>(row[i] * r * gain[i]);
-    return;
+  const int o = final_layer ? out_row[t] : -1, lg = final_layer ? lg_row[t] : -1;
+  for (int i = threadIdx.x * 4; i < d; i += blockDim.x * 4) {
+    const float4 v = *reinterpret_cast<const float4*>(row + i);
+    const float4 g = *reinterpret_cast<const float4*>(gain + i);
+    const float4 y = make_float4(v.x * r * g.x, v.y * r * g.y, v.z * r * g.z, v.w * r * g.w);
+    if (!final_layer) {
+      store4<T>(x + (size_t)t * d + i, y);
+    } else {
+      if (o >= 0) *reinterpret_cast<float4*>(hidden_out + (size_t)o * d + i) = y;
+      if (lg >= 0) store4<T>(lm_x + (size_t)lg * d + i, y);
+    }
   }
-  const int o = out_row[t], lg = lg_row[t];
-  if (o >= 0)
-    for (int i = threadIdx.x; i < d; i += blockDim.x) hidden_out[(size_t)o * d + i] = row[i] * r * gain[i];
-  if (lg >= 0)
-    for (int i = threadIdx.x; i < d; i += blockDim.x) lm_x[(size_t)lg * d + i] = from_f<T>(row[i] * r * gain[i]);
 }
 
+// grid (T, ceil(F / 1024)); 4 outputs per thread.
 template <typename T>
 __global__ void swiglu_kernel(int T_, int F, const float* __restrict__ part, int splits, T* __restrict__ act) {
   const int t = blockIdx.x;
+  const int j = (blockIdx.y * blockDim.x + threadIdx.x) * 4;
+  if (j >= F) return;
   const size_t N = 2 * (size_t)F;
-  for (int j = threadIdx.x; j < F; j += blockDim.x) {
-    float a = 0.f, b = 0.f;
-    for (int s = 0; s < splits; ++s) {
-      const float* p = part + ((size_t)s * T_ + t) * N;
-      a += p[j];
-      b += p[F + j];
-    }
-    act[(size_t)t * F + j] = from_f<T>(a / (1.f + __expf(-a)) * b);
-  }
+  const float4 a = sum4(part, splits, (size_t)T_ * N, (size_t)t * N + j);
+  const float4 b = sum4(part, splits, (size_t)T_ * N, (size_t)t * N + F + j);
+  const float4 y = make_float4(a.x / (1.f + __expf(-a.x)) * b.x, a.y / (1.f + __expf(-a.y)) * b.y,
+                               a.z / (1.f + __expf(-a.z)) * b.z, a.w / (1.f + __expf(-a.w)) * b.w);
+  store4<T>(act + (size_t)t * F + j, y);
 }
 
 __global__ void sum_partials_kernel(int T_, int N, const float* __restrict__ part, int splits,
@@ -172,12 +208,14 @@ void launch_embed_norm(int dtype, int T, int d, const void* embed, const int* to
 void launch_qkv_epilogue(int dtype, int T, int H, int G, int D, const float* part, int splits, void* q,
                          const int* slot, void* k_layer, void* v_layer, cudaStream_t st) {
   if (T <= 0) return;
+  const int N = (H + 2 * G) * D;
+  dim3 grid(T, (N / 4 + kRowThreads - 1) / kRowThreads);
   if (dtype == PIC_BF16)
-    qkv_epilogue_kernel<__nv_bfloat16><<<T, kRowThreads, 0, st>>>(T, H, G, D, part, splits, (__nv_bfloat16*)q, slot,
-                                                                  (__nv_bfloat16*)k_layer, (__nv_bfloat16*)v_layer);
+    qkv_epilogue_kernel<__nv_bfloat16><<<grid, kRowThreads, 0, st>>>(T, H, G, D, part, splits, (__nv_bfloat16*)q, slot,
+                                                                     (__nv_bfloat16*)k_layer, (__nv_bfloat16*)v_layer);
   else
-    qkv_epilogue_kernel<float><<<T, kRowThreads, 0, st>>>(T, H, G, D, part, splits, (float*)q, slot,
-                                                          (float*)k_layer, (float*)v_layer);
+    qkv_epilogue_kernel<float><<<grid, kRowThreads, 0, st>>>(T, H, G, D, part, splits, (float*)q, slot,
+                                                             (float*)k_layer, (float*)v_layer);
 }
 
 void launch_residual_norm(int dtype, int T, int d, const float* part, int splits, float* h, const float* gain,
@@ -185,21 +223,23 @@ void launch_residual_norm(int dtype, int T, int d, const float* part, int splits
                           const int* lg_row, void* lm_x, cudaStream_t st) {
   if (T <= 0) return;
   const size_t sm = d * sizeof(float);
+  const int thr = std::min(1024, std::max(128, (d / 4 + 31) / 32 * 32));
   if (dtype == PIC_BF16)
-    residual_norm_kernel<__nv_bfloat16><<<T, kRowThreads, sm, st>>>(T, d, part, splits, h, gain, eps,
+    residual_norm_kernel<__nv_bfloat16><<<T, thr, sm, st>>>(T, d, part, splits, h, gain, eps,
                                                                     (__nv_bfloat16*)x, final_layer, out_row,
                                                                     hidden_out, lg_row, (__nv_bfloat16*)lm_x);
   else
-    residual_norm_kernel<float><<<T, kRowThreads, sm, st>>>(T, d, part, splits, h, gain, eps, (float*)x, final_layer,
+    residual_norm_kernel<float><<<T, thr, sm, st>>>(T, d, part, splits, h, gain, eps, (float*)x, final_layer,
                                                             out_row, hidden_out, lg_row, (float*)lm_x);
 }
 
 void launch_swiglu(int dtype, int T, int F, const float* part, int splits, void* act, cudaStream_t st) {
   if (T <= 0) return;
+  dim3 grid(T, (F / 4 + kRowThreads - 1) / kRowThreads);
   if (dtype == PIC_BF16)
-    swiglu_kernel<__nv_bfloat16><<<T, kRowThreads, 0, st>>>(T, F, part, splits, (__nv_bfloat16*)act);
+    swiglu_kernel<__nv_bfloat16><<<grid, kRowThreads, 0, st>>>(T, F, part, splits, (__nv_bfloat16*)act);
   else
-    swiglu_kernel<float><<<T, kRowThreads, 0, st>>>(T, F, part, splits, (float*)act);
+    swiglu_kernel<float><<<grid, kRowThreads, 0, st>>>(T, F, part, splits, (float*)act);
 }
 
 void launch_sum_partials(int T, int N, const float* part, int splits, float* out, cudaStream_t st) {

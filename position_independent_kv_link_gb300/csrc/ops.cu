@@ -87,7 +87,7 @@ pic_status pic_op_attention(int32_t dtype, int32_t T, int32_t n_heads, int32_t n
                             size_t scratch_bytes, pic_stream_t stream) {
   if (T < 1 || n_pages < 1 || !q || !q_pos_host || !k_layer || !v_layer || !page_block_host || !page_pos_host ||
       !page_len_host || !rope_cs || !out || !scratch || n_kv_heads < 1 || n_heads % n_kv_heads ||
-      (head_dim != 64 && head_dim != 128) || (dtype != PIC_F32 && dtype != PIC_BF16))
+      (head_dim != 64 && head_dim != 128) || (dtype != PIC_F32 && dtype != PIC_BF16) || rope_positions < 16)
     return fail(PIC_ERR_INVALID_ARG, "invalid attention arguments");
   const AttnScratchLayout L = attn_layout(T, n_heads, n_kv_heads, head_dim, n_pages);
   if (scratch_bytes < L.total) return fail(PIC_ERR_INVALID_ARG, "attention scratch too small");

@@ -95,6 +95,22 @@ def test_paged_attention_fused_rope(dtype, D, H, G):
     assert rel_err(out, ref) < tol
 
 
+def test_paged_attention_config2_shape():
+    """The 8B link's attention at its full size: 10 x 512 chunks + 64 query, k = 16
+    (224 query rows, 324 pages, 32 Q / 8 KV heads), split over page runs as in the link."""
+    from position_independent_kv_link_gb300 import attention, rope_table
+    q, qpos, K, V, pages, n_pos = _attn_case(torch.bfloat16, 128, 32, 8, [512] * 10, 64, 16, 11)
+    rope = rope_table(n_pos + 16, 128, 500000.0)
+    out = attention(q.cuda(), qpos, K.cuda(), V.cuda(), pages, rope, 8)
+    torch.cuda.synchronize()
+    blk, ppos, plen = pages
+    Ka = np.concatenate([K[b, :, :n].double().numpy().transpose(1, 0, 2) for b, n in zip(blk, plen)])
+    Va = np.concatenate([V[b, :, :n].double().numpy().transpose(1, 0, 2) for b, n in zip(blk, plen)])
+    pos = np.concatenate([np.arange(p, p + n) for p, n in zip(ppos, plen)])
+    ref = po.causal_attention(po.rope(q.double().numpy(), qpos, 500000.0), po.rope(Ka, pos, 500000.0), Va, qpos, pos)
+    assert rel_err(out, ref) < 2e-2
+
+
 # ----------------------------------------------------------------------------- whole link
 
 @pytest.fixture(scope="module")
