@@ -105,7 +105,7 @@ __global__ void qkv_epilogue_kernel(int T_, int H, int G, int D, const float* __
 
 // h[t] += sum of split slabs; then RMSNorm. One CTA per row, 4 columns per thread-step.
 template <typename T>
-__global__ void residual_norm_kernel(int T_, int d, const float* __restrict__ part, int splits,
+__global__ void __launch_bounds__(512) residual_norm_kernel(int T_, int d, const float* __restrict__ part, int splits,
                                      float* __restrict__ h, const float* __restrict__ gain, float eps,
                                      T* __restrict__ x, int final_layer, const int* __restrict__ out_row,
                                      float* __restrict__ hidden_out, const int* __restrict__ lg_row,
@@ -223,7 +223,7 @@ void launch_residual_norm(int dtype, int T, int d, const float* part, int splits
                           const int* lg_row, void* lm_x, cudaStream_t st) {
   if (T <= 0) return;
   const size_t sm = d * sizeof(float);
-  const int thr = std::min(1024, std::max(128, (d / 4 + 31) / 32 * 32));
+  const int thr = std::min(512, std::max(128, (d / 4 + 31) / 32 * 32));
   if (dtype == PIC_BF16)
     residual_norm_kernel<__nv_bfloat16><<<T, thr, sm, st>>>(T, d, part, splits, h, gain, eps,
                                                                     (__nv_bfloat16*)x, final_layer, out_row,
