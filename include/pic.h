@@ -242,6 +242,29 @@ pic_status pic_op_attention(int32_t dtype, int32_t T, int32_t n_heads, int32_t n
                             const void* rope_cs, int32_t rope_positions, void* out, void* scratch,
                             size_t scratch_bytes, pic_stream_t stream);
 
+/* Allocation-free twin of pic_op_attention. The pages have no counterpart for this
+ * call: it exists for callers that cannot allocate device memory (code running inside
+ * a memory pool it does not own, plug-ins of hosts that forbid cudaMalloc after
+ * start-up, paths that must not synchronize the device). Arguments and results are
+ * those of pic_op_attention without the scratch buffer: the call uses a fixed 16 MiB
+ * area inside the library (pic_op_attention_noalloc_max_scratch() bytes), held by every
+ * GPU that loads the library until the process exits. It calls no cudaMalloc/cudaFree.
+ *  - A shape whose exact work list and partial results exceed the area is rejected
+ *    with PIC_ERR_CAPACITY before any GPU work.
+ *  - The first call on a device looks up the area's device address (with that device
+ *    current); make that first call before any stream capture.
+ *  - Every call reuses the same area and leaves its contents behind; nothing in it has
+ *    to start at zero (each word read is written earlier in the same call). Calls that
+ *    overlap on the GPU (different streams, or different host threads) race on it:
+ *    order them, e.g. by issuing them on one stream. */
+size_t pic_op_attention_noalloc_max_scratch(void);
+pic_status pic_op_attention_noalloc(int32_t dtype, int32_t T, int32_t n_heads, int32_t n_kv_heads,
+                                    int32_t head_dim, const void* q, const int32_t* q_pos_host,
+                                    const void* k_layer, const void* v_layer, const int32_t* page_block_host,
+                                    const int32_t* page_pos_host, const int32_t* page_len_host, int32_t n_pages,
+                                    int32_t pool_blocks, const void* rope_cs, int32_t rope_positions, void* out,
+                                    pic_stream_t stream);
+
 /* Fills a device float2 table [n_pos][head_dim/2] with (cos, sin)(p * base^(-2i/D)),
  * angles formed in fp64 on the host. */
 pic_status pic_op_rope_table(int32_t n_pos, int32_t head_dim, double base, void* out, pic_stream_t stream);

@@ -80,6 +80,9 @@ SIGNATURES = {
     "pic_op_attention": (I32, [I32, I32, I32, I32, I32, P, PI32, P, P, PI32, PI32, PI32, I32, I32, P, I32, P, P,
                                C.c_size_t, P]),
     "pic_op_rope_table": (I32, [I32, I32, C.c_double, P, P]),
+    "pic_op_attention_noalloc_max_scratch": (C.c_size_t, []),
+    "pic_op_attention_noalloc": (I32, [I32, I32, I32, I32, I32, P, PI32, P, P, PI32, PI32, PI32, I32, I32, P, I32, P,
+                                       P]),
 }
 
 _LIB = None

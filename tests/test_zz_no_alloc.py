@@ -1,0 +1,94 @@
+"""The allocation-free attention call matches the regular one.
+
+pic_op_attention_noalloc serves callers that cannot allocate device memory (code
+inside a memory pool it does not own, hosts that forbid cudaMalloc after start-up,
+paths that must not synchronize the device): it keeps its scratch in a fixed area of
+the library instead of a caller buffer. This file is collected last on purpose, and it
+must pass both on its own in a fresh process and after every other test.
+"""
+import ctypes as C
+
+import numpy as np
+import pytest
+import torch
+
+import pic_inputs as pi
+from tests.helpers import rel_err
+
+pytestmark = pytest.mark.gpu
+
+
+def _case(seed):
+    """Ragged chunks + a query over scattered pages (bf16, 8 Q / 2 KV heads, head_dim 128)."""
+    rng = np.random.default_rng(seed)
+    lens, qlen = [300, 37, 512, 16, 200], 40
+    pblk, ppos, plen, sel = [], [], [], []
+    off = 0
+    for i, L in enumerate(lens + [qlen]):
+        for j in range(-(-L // 16)):
+            pblk.append(len(pblk))
+            ppos.append(off + 16 * j)
+            plen.append(min(16, L - 16 * j))
+        sel += list(range(off, off + (min(3, L) if i < len(lens) else L)))
+        off += L
+    nb = len(pblk) + 5
+    pblk = [int(b) for b in rng.permutation(nb)[:len(pblk)]]
+    K = pi.randn((nb, 2, 16, 128), ("noallocK", seed), 1.0, torch.bfloat16).cuda()
+    V = pi.randn((nb, 2, 16, 128), ("noallocV", seed), 1.0, torch.bfloat16).cuda()
+    q = pi.randn((len(sel), 8, 128), ("noallocQ", seed), 1.0, torch.bfloat16).cuda()
+    i32 = lambda a: np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+    return q, i32(sel), K, V, i32(pblk), i32(ppos), i32(plen), off
+
+
+def test_noalloc_attention_matches_regular_entry_point():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    torch.cuda.set_device(0)
+    from position_independent_kv_link_gb300 import _lib as L, api
+    lib = L.load()
+    assert lib.pic_op_attention_noalloc_max_scratch() == 16 << 20
+    stream = torch.cuda.current_stream()
+    sp = C.c_void_p(stream.cuda_stream)
+    P = lambda a: a.ctypes.data_as(L.PI32)
+    for seed in (1, 2):                          # two calls in a row on the shared area
+        q, qpos, K, V, blk, ppos, plen, n_pos = _case(seed)
+        rope = api.rope_table(n_pos + 16, 128, 500000.0)
+        T, n_pages = q.shape[0], len(blk)
+        ref = torch.empty_like(q)
+        nb = lib.pic_op_attention_scratch_bytes(T, 8, 2, 128, n_pages)
+        scratch = torch.empty(nb, dtype=torch.uint8, device="cuda")
+        L.check(lib.pic_op_attention(L.PIC_BF16, T, 8, 2, 128, q.data_ptr(), P(qpos), K.data_ptr(), V.data_ptr(),
+                                     P(blk), P(ppos), P(plen), n_pages, K.shape[0], rope.data_ptr(), rope.shape[0],
+                                     ref.data_ptr(), scratch.data_ptr(), nb, sp))
+        got = torch.full_like(q, float("nan"))
+        L.check(lib.pic_op_attention_noalloc(L.PIC_BF16, T, 8, 2, 128, q.data_ptr(), P(qpos), K.data_ptr(),
+                                             V.data_ptr(), P(blk), P(ppos), P(plen), n_pages, K.shape[0],
+                                             rope.data_ptr(), rope.shape[0], got.data_ptr(), sp))
+        torch.cuda.synchronize()
+        assert torch.isfinite(got.float()).all()
+        assert rel_err(got, ref) < 2e-2
+
+
+def test_noalloc_attention_rejects_oversized_work():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    torch.cuda.set_device(0)
+    from position_independent_kv_link_gb300 import _lib as L, api
+    lib = L.load()
+    # 16 query rows at the end of 5000 pages: the planner splits the pages into ~600 runs
+    # whose merge partials (~33 KB each) exceed the fixed area
+    T, n_pages = 16, 5000
+    qpos = np.arange(16 * n_pages - T, 16 * n_pages, dtype=np.int32)
+    blk = np.arange(n_pages, dtype=np.int32)
+    ppos = (16 * np.arange(n_pages)).astype(np.int32)
+    plen = np.full(n_pages, 16, dtype=np.int32)
+    q = torch.zeros((T, 32, 128), dtype=torch.bfloat16, device="cuda")
+    K = torch.zeros((n_pages, 8, 16, 128), dtype=torch.bfloat16, device="cuda")
+    rope = api.rope_table(16 * n_pages + 16, 128, 500000.0)
+    out = torch.zeros_like(q)
+    P = lambda a: a.ctypes.data_as(L.PI32)
+    st = lib.pic_op_attention_noalloc(L.PIC_BF16, T, 32, 8, 128, q.data_ptr(), P(qpos), K.data_ptr(), K.data_ptr(),
+                                      P(blk), P(ppos), P(plen), n_pages, n_pages, rope.data_ptr(), rope.shape[0],
+                                      out.data_ptr(), C.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert st == L.PIC_ERR_CAPACITY
+    assert b"fixed area" in lib.pic_last_error()
