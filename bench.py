@@ -286,8 +286,8 @@ def run_ours(args):
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
+    # timed region: K steps, no instrumentation
     launches0 = store.launch_count()
-    store.profile_begin()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(args.steps):
@@ -295,14 +295,15 @@ def run_ours(args):
     e1.record(stream)
     torch.cuda.synchronize()
     barrier()
-    prof = store.profile_end()
     launches = store.launch_count() - launches0
-    # keep the GPU busy a little longer so the clock sampler sees the loaded state
-    for _ in range(min(args.steps, 5)):
+    ms = e0.elapsed_time(e1)
+    # the same K steps again with CUDA events around every kernel launch (per-kernel times)
+    store.profile_begin()
+    for _ in range(args.steps):
         step()
+    prof = store.profile_end()
     torch.cuda.synchronize()
     clk = clocks.stop()
-    ms = e0.elapsed_time(e1)
     store.sync()
     if world > 1:
         import torch.distributed as dist
@@ -359,6 +360,7 @@ def run_ours(args):
         "link_roofline": {"roofline_ms": rl["roofline_ms"], "bound": rl["bound"], "measured_ms": ms_step,
                           "frac": rl["roofline_ms"] / ms_step, "bytes": rl["bytes"], "flops": rl["flops"],
                           "t_mem_ms": rl["t_mem_ms"], "t_flop_ms": rl["t_flop_ms"]},
+        "kernels_note": "per-kernel times from a second, event-instrumented run of the same steps",
         "kernels": {k: {"ms_per_step": v["ms"] / args.steps, "launches_per_step": v["launches"] / args.steps,
                         "GBs": v["bytes"] / (v["ms"] / 1e3) / 1e9 if v["ms"] > 0 else None,
                         "TFs": v["flops"] / (v["ms"] / 1e3) / 1e12 if v["ms"] > 0 else None}
@@ -386,6 +388,69 @@ def run_ours(args):
     return 0
 
 
+def run_kernel(args):
+    """Times one kernel-level call at its shape in the 8B link (for ncu captures and sweeps).
+
+    gemm:      gate/up projection, 28672 x 4096 weights, 224 selected rows (tcgen05).
+    attention: the link's paged attention, 10 x 512 chunks + 64 query, k = 16
+               (224 query rows, 324 pages, 32 Q / 8 KV heads), fused RoPE.
+    """
+    import ctypes as C
+    from position_independent_kv_link_gb300 import _lib as L, api
+    torch.cuda.set_device(0)
+    lib = L.load()
+    st = torch.cuda.current_stream()
+    sp = C.c_void_p(st.cuda_stream)
+    g = torch.Generator(device="cuda").manual_seed(0)
+    if args.kernel == "gemm":
+        N, K, T = 28672, 4096, 224
+        W = (torch.randn(N, K, device="cuda", generator=g) * 0.02).to(torch.bfloat16)
+        X = torch.randn(T, K, device="cuda", generator=g).to(torch.bfloat16)
+        Y = torch.empty(T, N, device="cuda")
+        call = lambda: L.check(lib.pic_op_gemm(L.PIC_BF16, W.data_ptr(), X.data_ptr(), Y.data_ptr(), N, K, T, sp))
+        nbytes, flops = N * K * 2 + T * K * 2 + T * N * 4, 2.0 * N * K * T
+    else:
+        lens, qlen, k = [512] * 10, 64, 16
+        pblk, ppos, plen, sel, off = [], [], [], [], 0
+        for i, Ln in enumerate(lens + [qlen]):
+            for j in range(-(-Ln // 16)):
+                pblk.append(len(pblk))
+                ppos.append(off + 16 * j)
+                plen.append(min(16, Ln - 16 * j))
+            sel += list(range(off, off + (min(k, Ln) if i < len(lens) else Ln)))
+            off += Ln
+        i32 = lambda a: np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+        qpos, blk, pp, pl = i32(sel), i32(pblk), i32(ppos), i32(plen)
+        T, n_pages = len(sel), len(pblk)
+        Kp = torch.randn(n_pages, 8, 16, 128, device="cuda", generator=g).to(torch.bfloat16)
+        Vp = torch.randn(n_pages, 8, 16, 128, device="cuda", generator=g).to(torch.bfloat16)
+        q = torch.randn(T, 32, 128, device="cuda", generator=g).to(torch.bfloat16)
+        out = torch.empty_like(q)
+        rope = api.rope_table(off + 16, 128, 500000.0)
+        nb = lib.pic_op_attention_scratch_bytes(T, 32, 8, 128, n_pages)
+        scratch = torch.empty(nb, dtype=torch.uint8, device="cuda")
+        P = lambda a: a.ctypes.data_as(L.PI32)
+        call = lambda: L.check(lib.pic_op_attention(L.PIC_BF16, T, 32, 8, 128, q.data_ptr(), P(qpos), Kp.data_ptr(),
+                                                    Vp.data_ptr(), P(blk), P(pp), P(pl), n_pages, n_pages,
+                                                    rope.data_ptr(), rope.shape[0], out.data_ptr(),
+                                                    scratch.data_ptr(), nb, sp))
+        pairs = sum(p + 1 for p in sel)
+        nbytes, flops = n_pages * 16 * 8 * 128 * 2 * 2 + 2 * T * 32 * 128 * 2, pairs * 32 * 128 * 4.0
+    for _ in range(max(3, args.warmup)):
+        call()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    for _ in range(args.steps):
+        call()
+    e1.record(st)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    print(json.dumps({"kernel": args.kernel, "ms": ms, "GBs": nbytes / ms / 1e6, "TFs": flops / ms / 1e9,
+                      "steps": args.steps}), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -395,7 +460,11 @@ def main():
     ap.add_argument("--config", default="c2", help="tiny, c2, c3, c4, c5_k{0,2,16,32,512}")
     ap.add_argument("--cpu-layers", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kernel", choices=["gemm", "attention"], default=None,
+                    help="time one kernel-level call at its 8B link shape instead of the link step")
     args = ap.parse_args()
+    if args.kernel:
+        return run_kernel(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

@@ -216,14 +216,12 @@ int64_t pic_store_launch_count(const pic_store* s);
  * device pointers unless stated; all work is async on `stream`.
  */
 
-/* Bytes of scratch pic_op_gemm needs for this shape (split-K partial sums). */
-size_t pic_op_gemm_scratch_bytes(int32_t dtype, int32_t N, int32_t K, int32_t T);
 /* Y[T][N] (fp32, overwritten) = X[T][K] . W[N][K]^T, both operands in `dtype`.
- * bf16 runs on the tcgen05 tensor-core kernel (K % 64 == 0, N % 128 == 0, 16-byte
- * aligned rows); fp32 on the SIMT kernel. scratch: caller-owned device buffer of at
- * least pic_op_gemm_scratch_bytes(...) bytes. */
+ * bf16 runs on the tcgen05 tensor-core kernel when K % 64 == 0 and N % 128 == 0 (rows
+ * 16-byte aligned; split-K partial sums meet in Y through TMA bulk reduce-adds), fp32 and
+ * other shapes on the SIMT kernel. Needs no scratch. */
 pic_status pic_op_gemm(int32_t dtype, const void* W, const void* X, float* Y, int32_t N, int32_t K, int32_t T,
-                       void* scratch, size_t scratch_bytes, pic_stream_t stream);
+                       pic_stream_t stream);
 
 /* Sparse-query paged attention with fused RoPE for ONE sequence of pages:
  * out[t][h] = softmax_u( RoPE(q[t][h], q_pos[t]) . RoPE(K[u][g], pos(u)) / sqrt(D) ) V[u][g]

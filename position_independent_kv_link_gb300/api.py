@@ -236,10 +236,7 @@ def gemm(W: torch.Tensor, X: torch.Tensor, stream=None) -> torch.Tensor:
     assert X.shape[1] == K and W.dtype == X.dtype and W.is_contiguous() and X.is_contiguous()
     dt = _dtype_code(W.dtype)
     Y = torch.empty((T, N), dtype=torch.float32, device=W.device)
-    nb = lib.pic_op_gemm_scratch_bytes(dt, N, K, T)
-    scratch = torch.empty(max(nb, 1), dtype=torch.uint8, device=W.device)
-    L.check(lib.pic_op_gemm(dt, W.data_ptr(), X.data_ptr(), Y.data_ptr(), N, K, T, scratch.data_ptr(), nb,
-                            _stream(stream)))
+    L.check(lib.pic_op_gemm(dt, W.data_ptr(), X.data_ptr(), Y.data_ptr(), N, K, T, _stream(stream)))
     return Y
 
 

@@ -111,8 +111,8 @@ struct pic_store {
   void* attn = nullptr;
   void* act = nullptr;
   void* lm_x = nullptr;
-  float* part = nullptr;
-  size_t part_floats = 0;
+  float* qkv_acc = nullptr;  // [max_rows][(H+2G)D] fp32, zero between uses
+  float* gu_acc = nullptr;   // [max_rows][2F] fp32, zero between uses
   float* att_o = nullptr;
   float* att_ml = nullptr;
   int att_parts_cap = 0;
@@ -172,15 +172,14 @@ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
 int gemm_splits(const pic_store* s, int N, int K, int T) {
   if (s->m->cfg.dtype != PIC_BF16 || !tc_gemm_supported(N, K, T)) return 1;
-  const size_t cap = s->part_floats / ((size_t)T * N);
-  return tc_gemm_splits(N, K, T, s->m->num_sms, (int)std::max<size_t>(1, std::min<size_t>(cap, 16)));
+  return tc_gemm_splits(N, K, T, s->m->num_sms, 16);
 }
 
-pic_status gemm(const pic_store* s, const void* W, const void* X, float* part, int N, int K, int T, int splits,
+// Y[T][N] += X . W^T (fp32 Y accumulated in place)
+pic_status gemm(const pic_store* s, const void* W, const void* X, float* Y, int N, int K, int T, int splits,
                 cudaStream_t st) {
-  if (s->m->cfg.dtype == PIC_BF16 && tc_gemm_supported(N, K, T))
-    return tc_gemm_run(W, X, part, N, K, T, splits, st);
-  launch_gemm_simt(s->m->cfg.dtype, W, X, part, N, K, T, splits, st);
+  if (s->m->cfg.dtype == PIC_BF16 && tc_gemm_supported(N, K, T)) return tc_gemm_run(W, X, Y, N, K, T, splits, st);
+  launch_gemm_simt(s->m->cfg.dtype, W, X, Y, N, K, T, splits, st);
   return PIC_OK;
 }
 
@@ -208,7 +207,7 @@ struct Rec {
 };
 
 // Uploads the batch metadata and runs embedding, every layer, and (link) the LM head.
-pic_status run_forward(pic_store* s, const Batch& b, float* hidden_out, float* logits_out, cudaStream_t st) {
+pic_status run_forward_impl(pic_store* s, const Batch& b, float* hidden_out, float* logits_out, cudaStream_t st) {
   const pic_model_config& c = s->m->cfg;
   const int T = b.rows();
   const int dt = c.dtype;
@@ -318,21 +317,22 @@ pic_status run_forward(pic_store* s, const Batch& b, float* hidden_out, float* l
   const int sp_gu = gemm_splits(s, 2 * F, d, T);
   const int sp_dn = gemm_splits(s, d, F, T);
   auto gemm_bytes = [&](double N, double K, double rows) { return N * K * es + rows * K * es + rows * N * 4; };
-  auto run_gemm = [&](const void* W, const void* X, float* part, int N, int K, int rows, int sp) {
+  auto run_gemm = [&](const void* W, const void* X, float* Y, int N, int K, int rows, int sp) {
     Rec r(s, st, PIC_PROF_GEMM, gemm_bytes(N, K, rows), 2.0 * N * K * rows, 1);
-    return gemm(s, W, X, part, N, K, rows, sp, st);
+    return gemm(s, W, X, Y, N, K, rows, sp, st);
   };
-
+  // The QKV and gate/up GEMMs add into zeroed accumulators that their epilogues clear
+  // again; the O and down projections add straight into the residual stream h.
   {
     Rec r(s, st, PIC_PROF_ROWWISE, dT * dd * (es + 4 + es) + dT * 4, 0, 1);
     launch_embed_norm(dt, T, d, s->m->embed, d_tok, s->m->attn_norm[0], c.rms_eps, s->h, s->x, st);
   }
   for (int l = 0; l < c.n_layers; ++l) {
     pic_status e;
-    if ((e = run_gemm(s->m->wqkv[l], s->x, s->part, qkv, d, T, sp_qkv)) != PIC_OK) return e;
+    if ((e = run_gemm(s->m->wqkv[l], s->x, s->qkv_acc, qkv, d, T, sp_qkv)) != PIC_OK) return e;
     {
-      Rec r(s, st, PIC_PROF_ROWWISE, sp_qkv * dT * dQKV * 4 + dT * dQKV * es, 0, 1);
-      launch_qkv_epilogue(dt, T, H, G, D, s->part, sp_qkv, s->q, d_slot, s->k_layer(l), s->v_layer(l), st);
+      Rec r(s, st, PIC_PROF_ROWWISE, dT * dQKV * (8 + es), 0, 1);
+      launch_qkv_epilogue(dt, T, H, G, D, s->qkv_acc, s->q, d_slot, s->k_layer(l), s->v_layer(l), st);
     }
     // compile keeps only KV: the last layer's attention and MLP feed nothing stored
     if (b.compile && l == c.n_layers - 1) break;
@@ -342,38 +342,47 @@ pic_status run_forward(pic_store* s, const Batch& b, float* hidden_out, float* l
       Rec r(s, st, PIC_PROF_ATTENTION, att_bytes, att_flops, att_launches);
       launch_attention(aa, st);
     }
-    if ((e = run_gemm(s->m->wo[l], s->attn, s->part, d, H * D, T, sp_o)) != PIC_OK) return e;
+    if ((e = run_gemm(s->m->wo[l], s->attn, s->h, d, H * D, T, sp_o)) != PIC_OK) return e;
     {
-      Rec r(s, st, PIC_PROF_ROWWISE, sp_o * dT * dd * 4 + dT * dd * (8 + es), 0, 1);
-      launch_residual_norm(dt, T, d, s->part, sp_o, s->h, s->m->mlp_norm[l], c.rms_eps, s->x, false, nullptr,
-                           nullptr, nullptr, nullptr, st);
+      Rec r(s, st, PIC_PROF_ROWWISE, dT * dd * (4 + es), 0, 1);
+      launch_rmsnorm_rows(dt, T, d, s->h, s->m->mlp_norm[l], c.rms_eps, s->x, false, nullptr, nullptr, nullptr,
+                          nullptr, st);
     }
-    if ((e = run_gemm(s->m->wgu[l], s->x, s->part, 2 * F, d, T, sp_gu)) != PIC_OK) return e;
+    if ((e = run_gemm(s->m->wgu[l], s->x, s->gu_acc, 2 * F, d, T, sp_gu)) != PIC_OK) return e;
     {
-      Rec r(s, st, PIC_PROF_ROWWISE, sp_gu * dT * 2 * dF * 4 + dT * dF * es, 0, 1);
-      launch_swiglu(dt, T, F, s->part, sp_gu, s->act, st);
+      Rec r(s, st, PIC_PROF_ROWWISE, dT * 2 * dF * 8 + dT * dF * es, 0, 1);
+      launch_swiglu(dt, T, F, s->gu_acc, s->act, st);
     }
-    if ((e = run_gemm(s->m->wdown[l], s->act, s->part, d, F, T, sp_dn)) != PIC_OK) return e;
+    if ((e = run_gemm(s->m->wdown[l], s->act, s->h, d, F, T, sp_dn)) != PIC_OK) return e;
     const bool last = l == c.n_layers - 1;
     {
-      Rec r(s, st, PIC_PROF_ROWWISE, sp_dn * dT * dd * 4 + dT * dd * (8 + es), 0, 1);
-      launch_residual_norm(dt, T, d, s->part, sp_dn, s->h, last ? s->m->final_norm : s->m->attn_norm[l + 1],
-                           c.rms_eps, s->x, last, d_out, hidden_out, d_lg, s->lm_x, st);
+      Rec r(s, st, PIC_PROF_ROWWISE, dT * dd * (4 + es), 0, 1);
+      launch_rmsnorm_rows(dt, T, d, s->h, last ? s->m->final_norm : s->m->attn_norm[l + 1], c.rms_eps, s->x, last,
+                          d_out, hidden_out, d_lg, s->lm_x, st);
     }
   }
   if (!b.compile && b.n_lg > 0) {
     const int sp = gemm_splits(s, c.vocab, d, b.n_lg);
+    PIC_CUDA(cudaMemsetAsync(logits_out, 0, (size_t)b.n_lg * c.vocab * sizeof(float), st));
     pic_status e;
-    if (sp == 1) {
-      if ((e = run_gemm(s->m->lm_head, s->lm_x, logits_out, c.vocab, d, b.n_lg, 1)) != PIC_OK) return e;
-    } else {
-      if ((e = run_gemm(s->m->lm_head, s->lm_x, s->part, c.vocab, d, b.n_lg, sp)) != PIC_OK) return e;
-      Rec r(s, st, PIC_PROF_ROWWISE, (sp + 1.0) * b.n_lg * (double)c.vocab * 4, 0, 1);
-      launch_sum_partials(b.n_lg, c.vocab, s->part, sp, logits_out, st);
-    }
+    if ((e = run_gemm(s->m->lm_head, s->lm_x, logits_out, c.vocab, d, b.n_lg, sp)) != PIC_OK) return e;
   }
   PIC_CUDA(cudaGetLastError());
   return PIC_OK;
+}
+
+pic_status run_forward(pic_store* s, const Batch& b, float* hidden_out, float* logits_out, cudaStream_t st) {
+  const pic_status e = run_forward_impl(s, b, hidden_out, logits_out, st);
+  if (e != PIC_OK) {
+    // a forward stopped part-way may leave sums in the in-place accumulators: clear them
+    const std::string msg = pic_last_error();
+    const size_t R = s->cfg.max_rows;
+    cudaMemsetAsync(s->qkv_acc, 0, R * (size_t)s->m->qkv_dim() * 4, st);
+    cudaMemsetAsync(s->gu_acc, 0, R * 2 * (size_t)s->m->cfg.ffn_dim * 4, st);
+    (void)cudaGetLastError();
+    set_error(msg);
+  }
+  return e;
 }
 
 bool valid_tokens(const int32_t* t, int n, int vocab) {
@@ -457,10 +466,6 @@ pic_status pic_store_create(pic_model* m, const pic_store_config* cfg, void* k_p
   const size_t R = sc.max_rows, es = dtype_size(c.dtype);
   const size_t d = c.d_model, HD = (size_t)c.n_heads * c.head_dim, F = c.ffn_dim;
   const int rep = c.n_heads / c.n_kv_heads;
-  // split-K partial sums: enough for 2048 rows (or max_rows) of the widest projection
-  const size_t part_rows = std::max<size_t>(R, 2048);
-  s->part_floats = std::max({part_rows * (size_t)m->qkv_dim(), part_rows * d, part_rows * 2 * F,
-                             (size_t)sc.max_logit_rows * c.vocab, R * HD});
   s->att_parts_cap = 4 * m->num_sms + c.n_kv_heads * s->att_blocks_cap();
   const size_t max_pages = (size_t)sc.max_positions / kBlock + 2 * (size_t)sc.max_requests + 2;
   const size_t max_items = (size_t)s->att_parts_cap + (size_t)c.n_kv_heads * s->att_blocks_cap();
@@ -475,7 +480,7 @@ pic_status pic_store_create(pic_model* m, const pic_store_config* cfg, void* k_p
   };
   const size_t o_h = carve(R * d * 4), o_x = carve(R * std::max(d, HD) * es), o_q = carve(R * HD * es),
                o_attn = carve(R * HD * es), o_act = carve(R * F * es), o_lm = carve((size_t)sc.max_logit_rows * d * es),
-               o_part = carve(s->part_floats * 4),
+               o_qkv = carve(R * (size_t)m->qkv_dim() * 4), o_gu = carve(R * 2 * F * 4),
                o_atto = carve((size_t)s->att_parts_cap * kBlock * rep * c.head_dim * 4),
                o_attml = carve((size_t)s->att_parts_cap * kBlock * rep * 2 * 4), o_meta = carve(s->meta_cap * 4),
                o_rope = carve((size_t)std::max(16, sc.max_positions) * (c.head_dim / 2) * sizeof(float2));
@@ -487,11 +492,18 @@ pic_status pic_store_create(pic_model* m, const pic_store_config* cfg, void* k_p
   s->attn = s->ws + o_attn;
   s->act = s->ws + o_act;
   s->lm_x = s->ws + o_lm;
-  s->part = (float*)(s->ws + o_part);
+  s->qkv_acc = (float*)(s->ws + o_qkv);
+  s->gu_acc = (float*)(s->ws + o_gu);
   s->att_o = (float*)(s->ws + o_atto);
   s->att_ml = (float*)(s->ws + o_attml);
   s->meta_d = (int32_t*)(s->ws + o_meta);
   s->rope_cs = (float2*)(s->ws + o_rope);
+  // the in-place accumulators start at zero; their epilogues keep them zero between GEMMs
+  e = cudaMemset(s->ws + o_qkv, 0, o_gu + R * 2 * F * 4 - o_qkv);
+  if (e != cudaSuccess) {
+    cudaFree(s->ws);
+    return fail(PIC_ERR_CUDA, std::string("workspace memset: ") + cudaGetErrorString(e));
+  }
   e = cudaMallocHost(&s->meta_h, s->meta_cap * 4);
   if (e != cudaSuccess) {
     cudaFree(s->ws);

@@ -91,39 +91,54 @@ __global__ void __launch_bounds__(128) attn_simt_kernel(AttnArgs a) {
   }
 }
 
-// Merge split results: out = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s.
+// Merge split results: out = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s, in one pass
+// with a running maximum. grid (merges, ceil(16 * rep / 8)); one warp per (row, head),
+// D/32 consecutive dims per lane.
 template <typename T, int D>
-__global__ void __launch_bounds__(128) attn_combine_kernel(AttnArgs a) {
+__global__ void __launch_bounds__(256) attn_combine_kernel(AttnArgs a) {
   constexpr int NJ = D / 32;
   const AttnCombine c = a.combines[blockIdx.x];
   const int rep = a.H / a.G;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int pr = warp; pr < c.nrows * rep; pr += 4) {
-    const int r = pr / rep, hh = pr % rep;
-    float M = -INFINITY;
-    for (int s = 0; s < c.nparts; ++s) M = fmaxf(M, a.part_ml[(((size_t)(c.part0 + s) * kBlock + r) * rep + hh) * 2]);
-    float L = 0.f, o[NJ] = {};
-    for (int s = 0; s < c.nparts; ++s) {
-      const size_t pi = ((size_t)(c.part0 + s) * kBlock + r) * rep + hh;
-      const float ls = a.part_ml[pi * 2 + 1];
-      if (ls == 0.f) continue;
-      const float w = exp2f(a.part_ml[pi * 2] - M);
-      L += w * ls;
+  const int pr = blockIdx.y * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (pr >= c.nrows * rep) return;
+  const int r = pr / rep, hh = pr % rep;
+  float M = -INFINITY, L = 0.f, o[NJ];
 #pragma unroll
-      for (int j = 0; j < NJ; ++j) o[j] += w * a.part_o[pi * D + lane + 32 * j];
+  for (int j = 0; j < NJ; ++j) o[j] = 0.f;
+#pragma unroll 4
+  for (int s = 0; s < c.nparts; ++s) {
+    const size_t pi = ((size_t)(c.part0 + s) * kBlock + r) * rep + hh;
+    const float2 ml = *reinterpret_cast<const float2*>(a.part_ml + pi * 2);
+    float v[NJ];
+    if constexpr (NJ == 4) {
+      const float4 x = *reinterpret_cast<const float4*>(a.part_o + pi * D + lane * 4);
+      v[0] = x.x, v[1] = x.y, v[2] = x.z, v[3] = x.w;
+    } else {
+      const float2 x = *reinterpret_cast<const float2*>(a.part_o + pi * D + lane * 2);
+      v[0] = x.x, v[1] = x.y;
     }
-    const int t = c.row0 + r, h = c.g * rep + hh;
-    const float inv = 1.f / L;
-    T* out = (T*)a.out;
+    if (ml.y == 0.f) continue;  // this run saw no key at or before the row's position
+    const float Mn = fmaxf(M, ml.x);
+    const float wa = exp2f(M - Mn), wb = exp2f(ml.x - Mn);
+    L = L * wa + ml.y * wb;
 #pragma unroll
-    for (int j = 0; j < NJ; ++j) out[((size_t)t * a.H + h) * D + lane + 32 * j] = from_f<T>(o[j] * inv);
+    for (int j = 0; j < NJ; ++j) o[j] = o[j] * wa + v[j] * wb;
+    M = Mn;
   }
+  const int t = c.row0 + r, h = c.g * rep + hh;
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  T* out = (T*)a.out + ((size_t)t * a.H + h) * D + lane * NJ;
+#pragma unroll
+  for (int j = 0; j < NJ; ++j) out[j] = from_f<T>(o[j] * inv);
 }
 
 template <typename T, int D>
 void launch_simt(const AttnArgs& a, cudaStream_t st) {
   if (a.n_items > 0) attn_simt_kernel<T, D><<<a.n_items, 128, 0, st>>>(a);
-  if (a.n_combines > 0) attn_combine_kernel<T, D><<<a.n_combines, 128, 0, st>>>(a);
+  if (a.n_combines > 0) {
+    const int rep = a.H / a.G;
+    attn_combine_kernel<T, D><<<dim3(a.n_combines, (kBlock * rep + 7) / 8), 256, 0, st>>>(a);
+  }
 }
 
 }  // namespace

@@ -6,9 +6,10 @@
 // of 64 keys (4 pages), double buffered:
 //   * K: 16-byte global loads into registers, rotated by RoPE at each key's absolute
 //     position while being stored to shared memory (MEPIC abstract: K is kept without
-//     positional encoding and RoPE is fused into attention). cos/sin(p*theta) is
-//     composed from table rows 16*floor(p/16) (global, L1-resident) and p mod 16
-//     (shared), so the table read per tile is a few rows, not 64.
+//     positional encoding and RoPE is fused into attention). For a key at row r of a
+//     page starting at position P, cos/sin((P + r) theta) is composed from the table row
+//     of P (one per page, staged by cp.async) and the row of r (resident), so a tile
+//     reads 4 table rows instead of 64 and the rotation touches only shared memory.
 //   * V: cp.async straight into shared memory.
 // S = Q K^T and O += P V run on mma.sync with fp32 accumulators; the online softmax
 // lives in registers (row max/sum by quad shuffles). Keys after the query's position,
@@ -73,7 +74,9 @@ __global__ void __launch_bounds__(NW * 32) attn_mma_kernel(AttnArgs a) {
   uint8_t* sV = smem + 2 * TILE_BYTES;                 // [2][KT][D]
   uint8_t* sQ = smem + 4 * TILE_BYTES;                 // [REP][16][D]
   float2* sLo = reinterpret_cast<float2*>(sQ + REP * 16 * D * 2);   // [16][64] cos/sin of p = 0..15
-  int* sPos = reinterpret_cast<int*>(sLo + 16 * 64);                // [2][KT] key positions (INT_MAX = masked)
+  float2* sPg = sLo + 16 * 64;                                      // [2][4][64] cos/sin of each page start
+  int* sPos = reinterpret_cast<int*>(sPg + 2 * 4 * 64);             // [2][KT] key positions (INT_MAX = masked)
+  const uint32_t sPg_u = (uint32_t)__cvta_generic_to_shared(sPg);
   const uint32_t sK_u = (uint32_t)__cvta_generic_to_shared(sK);
   const uint32_t sV_u = (uint32_t)__cvta_generic_to_shared(sV);
   const uint32_t sQ_u = (uint32_t)__cvta_generic_to_shared(sQ);
@@ -146,8 +149,8 @@ __global__ void __launch_bounds__(NW * 32) attn_mma_kernel(AttnArgs a) {
       uint4 y1 = make_uint4(0, 0, 0, 0), y2 = y1;
       const int p = kt.pos[j];
       if (p != INT_MAX) {
-        const float2* hi = a.rope_cs + (size_t)(p & ~15) * 64 + 8 * c;
-        const float2* lo = sLo + (p & 15) * 64 + 8 * c;
+        const float2* hi = sPg + (buf * 4 + key / 16) * 64 + 8 * c;   // page start position
+        const float2* lo = sLo + (key % 16) * 64 + 8 * c;             // row within the page
         const __nv_bfloat16* b1 = reinterpret_cast<const __nv_bfloat16*>(&kt.lo[j]);
         const __nv_bfloat16* b2 = reinterpret_cast<const __nv_bfloat16*>(&kt.hi[j]);
         __nv_bfloat16 o1[8], o2[8];
@@ -169,6 +172,14 @@ __global__ void __launch_bounds__(NW * 32) attn_mma_kernel(AttnArgs a) {
     }
   };
   auto load_v = [&](int tile, int buf) {
+    // RoPE rows of the tile's page starts: 4 pages x 512 B
+    if (tid < 4 * 32) {
+      const int pg = tid / 32, c = tid % 32;
+      const int page = it.page0 + tile * 4 + pg;
+      if (page < it.page1)
+        cp_async16(sPg_u + (uint32_t)((buf * 4 + pg) * 64 * sizeof(float2) + c * 16),
+                   a.rope_cs + (size_t)a.page_pos[page] * 64 + c * 2);
+    }
     for (int task = tid; task < KT * 16; task += NW * 32) {
       const int key = task / 16, c = task % 16;
       const int page = it.page0 + tile * 4 + key / 16, r = key % 16;
@@ -186,9 +197,10 @@ __global__ void __launch_bounds__(NW * 32) attn_mma_kernel(AttnArgs a) {
   if (ntiles > 0) {
     load_v(0, 0);
     load_k(0);
-    store_k(0);
   }
   cp_async_wait_all();
+  __syncthreads();
+  if (ntiles > 0) store_k(0);
   __syncthreads();
 
   // ---- per-warp state
@@ -293,8 +305,9 @@ __global__ void __launch_bounds__(NW * 32) attn_mma_kernel(AttnArgs a) {
         }
       }
     }
+    cp_async_wait_all();   // V and page RoPE rows of the next tile have landed
+    __syncthreads();
     if (has_next) store_k(nxt);
-    cp_async_wait_all();
     __syncthreads();
   }
 
@@ -337,7 +350,8 @@ __global__ void __launch_bounds__(NW * 32) attn_mma_kernel(AttnArgs a) {
 
 template <int REP, int NW>
 void launch_rep(const AttnArgs& a, cudaStream_t st) {
-  const size_t smem = 4 * TILE_BYTES + REP * 16 * D * 2 + 16 * 64 * sizeof(float2) + 2 * KT * sizeof(int);
+  const size_t smem =
+      4 * TILE_BYTES + REP * 16 * D * 2 + (16 + 2 * 4) * 64 * sizeof(float2) + 2 * KT * sizeof(int);
   static bool attr[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);

@@ -1,4 +1,5 @@
-// SIMT FFMA GEMM: part[s][t][n] = sum_{k in split s} X[t][k] * W[n][k], fp32 accumulation.
+// SIMT FFMA GEMM: Y[t][n] += sum_k X[t][k] * W[n][k], fp32 accumulation; K may be split
+// over CTAs, whose sums meet in Y through atomic adds.
 // Used for fp32 models (tcgen05 has no plain-fp32 kind) and for shapes the tensor-core
 // kernel does not take. 64x64 output tile per CTA, 4x4 per thread, K in steps of 16.
 #include "pic_internal.h"
@@ -11,7 +12,7 @@ constexpr int BN = 64, BT = 64, BK = 16;
 
 template <typename TIn>
 __global__ void __launch_bounds__(256) gemm_simt_kernel(const TIn* __restrict__ W, const TIn* __restrict__ X,
-                                                        float* __restrict__ part, int N, int K, int T,
+                                                        float* __restrict__ Y, int N, int K, int T,
                                                         int k_per_split) {
   __shared__ float Ws[BK][BN + 4];
   __shared__ float Xs[BK][BT + 4];
@@ -51,24 +52,24 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(const TIn* __restrict__ 
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int n = n0 + tn + j;
-      if (n < N) part[((size_t)s * T + t) * N + n] = acc[i][j];
+      if (n < N) atomicAdd(Y + (size_t)t * N + n, acc[i][j]);
     }
   }
 }
 
 }  // namespace
 
-void launch_gemm_simt(int dtype, const void* W, const void* X, float* part, int N, int K, int T, int splits,
+void launch_gemm_simt(int dtype, const void* W, const void* X, float* Y, int N, int K, int T, int splits,
                       cudaStream_t st) {
   if (T <= 0 || N <= 0) return;
   int kps = (K + splits - 1) / splits;
   kps = (kps + BK - 1) / BK * BK;
   dim3 grid((N + BN - 1) / BN, (T + BT - 1) / BT, splits);
   if (dtype == PIC_BF16)
-    gemm_simt_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>((const __nv_bfloat16*)W, (const __nv_bfloat16*)X, part, N, K,
+    gemm_simt_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>((const __nv_bfloat16*)W, (const __nv_bfloat16*)X, Y, N, K,
                                                           T, kps);
   else
-    gemm_simt_kernel<float><<<grid, 256, 0, st>>>((const float*)W, (const float*)X, part, N, K, T, kps);
+    gemm_simt_kernel<float><<<grid, 256, 0, st>>>((const float*)W, (const float*)X, Y, N, K, T, kps);
 }
 
 }  // namespace pic

@@ -1,14 +1,16 @@
 // tcgen05 tensor-core GEMM for the projections of the selected rows (bf16 in, fp32 out).
 //
-//   part[s][t][n] = sum_{k in split s} W[n][k] * X[t][k]
+//   Y[t][n] += sum_k W[n][k] * X[t][k]        (Y fp32, accumulated in place)
 //
 // The link step multiplies a few hundred selected rows by large weight matrices, so
 // the weights take the MMA's M side (128 rows per CTA) and the token rows its N side
 // (up to 256 per tile): one weight tile is streamed from HBM exactly once per token
 // tile. Operands are staged by TMA (128-byte swizzle, K-major) through a multi-stage
 // mbarrier ring; one thread issues tcgen05.mma with the fp32 accumulator in TMEM; all
-// four warps drain TMEM with tcgen05.ld. Split-K spreads the weight stream over every
-// SM; the partial slabs are reduced by the fused epilogue kernels that follow.
+// four warps drain TMEM with tcgen05.ld into a shared-memory tile that one TMA bulk
+// reduce-add folds into Y. Split-K spreads the weight stream over every SM; the splits
+// meet in Y through those reductions, so no partial slabs are written or re-read, and a
+// projection that feeds the residual stream adds straight into it.
 //
 // Every mbarrier wait is bounded (~2 s of GPU time). On expiry the kernel raises a
 // device flag, stops issuing work, waits (bounded) for the copies and MMAs it started,
@@ -131,7 +133,6 @@ struct TcParams {
   int kb_per_split;  // k-blocks of BK per split
   int nkb;           // total k-blocks
   uint32_t tmem_cols;
-  float* part;
 };
 
 // MH = 128-row weight halves per CTA tile. Both halves share the staged activation
@@ -139,7 +140,7 @@ struct TcParams {
 template <int MH>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_x,
-                   const TcParams p) {
+                   const __grid_constant__ CUtensorMap map_y, const TcParams p) {
   constexpr int A_STAGE_BYTES = MH * A_HALF_BYTES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -224,28 +225,37 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncwarp();
 
-  // ---------------- epilogue: TMEM -> fp32 partial slab, all four warps
+  // ---------------- epilogue: TMEM -> shared tile [BN][128] fp32 -> TMA reduce-add into Y
   bool ok = mbar_wait(acc_bar, 0);
-  ok = __all_sync(0xffffffffu, ok) && !s_abort;  // warp-uniform and reconverged for .sync.aligned loads
+  ok = __syncthreads_and(ok) && !s_abort;  // block-uniform; warps reconverged for .sync.aligned loads
   asm volatile("tcgen05.fence::after_thread_sync;");
   if (ok) {
-    float* out = p.part + (size_t)split * p.T * p.N;
+    // every staged operand has been consumed by the MMAs, so the ring's memory is free
+    float* S = reinterpret_cast<float*>(smem);
     const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+    const int nl = warp * 32 + lane;
 #pragma unroll
     for (int hf = 0; hf < MH; ++hf) {
-      const int n = m0 + hf * BM + warp * 32 + lane;
       for (int c = 0; c < p.BN; c += 16) {
         float v[16];
         tmem_ld16(lane_base + hf * p.BN + c, v);
-        if (n < p.N) {
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int t = t0 + c + j;
-            if (t < p.T) out[(size_t)t * p.N + n] = v[j];
-          }
-        }
+        for (int j = 0; j < 16; ++j) S[(c + j) * BM + nl] = v[j];
       }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        asm volatile(
+            "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                reinterpret_cast<uint64_t>(&map_y)),
+            "r"(m0 + hf * BM), "r"(t0), "r"(smem_u32(S))
+            : "memory");
+        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+        asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");  // tile read out before it is reused
+      }
+      __syncthreads();
     }
+    if (threadIdx.x == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
   }
   asm volatile("tcgen05.fence::before_thread_sync;");
   __syncthreads();
@@ -263,6 +273,19 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
       fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
   });
   return fn;
+}
+
+// fp32 [rows][cols] destination of the bulk reduce-add; box = 128 columns x box_rows rows
+bool make_map_f32(CUtensorMap* m, void* base, int rows, int cols, int box_rows) {
+  auto enc = get_encode();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * 4};
+  cuuint32_t box[2] = {(cuuint32_t)BM, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
 }
 
 bool make_map(CUtensorMap* m, const void* base, int rows, int K, int box_rows) {
@@ -313,9 +336,10 @@ int tc_gemm_splits(int N, int K, int T, int num_sms, int max_splits) {
   return best;
 }
 
-pic_status tc_gemm_run(const void* W, const void* X, float* part, int N, int K, int T, int splits, cudaStream_t st) {
+pic_status tc_gemm_run(const void* W, const void* X, float* Y, int N, int K, int T, int splits, cudaStream_t st) {
   if (!tc_gemm_supported(N, K, T)) return fail(PIC_ERR_UNSUPPORTED, "tcgen05 gemm: unsupported shape");
-  if (((uintptr_t)W | (uintptr_t)X) % 16) return fail(PIC_ERR_INVALID_ARG, "tcgen05 gemm: operands not 16-byte aligned");
+  if (((uintptr_t)W | (uintptr_t)X | (uintptr_t)Y) % 16)
+    return fail(PIC_ERR_INVALID_ARG, "tcgen05 gemm: operands not 16-byte aligned");
   TcParams p{};
   p.N = N;
   p.K = K;
@@ -332,9 +356,10 @@ pic_status tc_gemm_run(const void* W, const void* X, float* part, int N, int K, 
   p.stages = std::max(2, std::min(8, budget / stage_bytes));
   p.tmem_cols = 32;
   while ((int)p.tmem_cols < mh * p.BN) p.tmem_cols <<= 1;
-  p.part = part;
-  CUtensorMap mw, mx;
-  if (!make_map(&mw, W, N, K, BM) || !make_map(&mx, X, T, K, p.BN))
+  if ((size_t)p.stages * stage_bytes < (size_t)p.BN * BM * 4)
+    return fail(PIC_ERR_UNSUPPORTED, "tcgen05 gemm: staging tile does not fit the pipeline memory");
+  CUtensorMap mw, mx, my;
+  if (!make_map(&mw, W, N, K, BM) || !make_map(&mx, X, T, K, p.BN) || !make_map_f32(&my, Y, T, N, p.BN))
     return fail(PIC_ERR_CUDA, "cuTensorMapEncodeTiled failed");
   const size_t smem = 1024 + (size_t)p.stages * stage_bytes + (2 * p.stages + 2) * 8;
   // raise the kernel's dynamic shared-memory limit to what this launch needs (once per size, per device)
@@ -348,7 +373,7 @@ pic_status tc_gemm_run(const void* W, const void* X, float* part, int N, int K, 
     if (dev >= 0 && dev < 64) attr_smem[mh - 1][dev] = smem;
   }
   dim3 grid(N / (BM * mh), (T + p.BN - 1) / p.BN, splits);
-  kern<<<grid, kThreads, smem, st>>>(mw, mx, p);
+  kern<<<grid, kThreads, smem, st>>>(mw, mx, my, p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(PIC_ERR_CUDA, std::string("tcgen05 gemm launch: ") + cudaGetErrorString(e));
   return PIC_OK;

@@ -1,7 +1,7 @@
 // Row-wise kernels of the decoder around the GEMMs and attention: embedding gather +
-// RMSNorm, split-K reductions fused with their epilogues (QKV scatter into pages,
-// residual + RMSNorm, SwiGLU), block copies for request-private pages, KV import.
-// All are HBM/L2-bound; one CTA per row with 16-byte-friendly strided loops.
+// RMSNorm, the QKV epilogue (q out, pre-RoPE K/V scattered into page slots), RMSNorm of the
+// residual stream, SwiGLU, block copies for request-private pages, KV import. All are
+// memory-bound; float4 accesses over rows.
 #include <algorithm>
 
 #include "pic_internal.h"
@@ -67,31 +67,27 @@ __device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16* dst, float4
   *reinterpret_cast<uint2*>(dst) = u;
 }
 
-__device__ __forceinline__ float4 sum4(const float* __restrict__ part, int splits, size_t stride, size_t off) {
-  float4 acc = *reinterpret_cast<const float4*>(part + off);
-  for (int s = 1; s < splits; ++s) {
-    const float4 v = *reinterpret_cast<const float4*>(part + (size_t)s * stride + off);
-    acc.x += v.x;
-    acc.y += v.y;
-    acc.z += v.z;
-    acc.w += v.w;
-  }
-  return acc;
+// Reads 4 accumulator floats and clears them for the next GEMM that adds into the buffer.
+__device__ __forceinline__ float4 take4(float* __restrict__ acc, size_t off) {
+  float4* p = reinterpret_cast<float4*>(acc + off);
+  const float4 v = *p;
+  *p = make_float4(0.f, 0.f, 0.f, 0.f);
+  return v;
 }
 
-// QKV epilogue: sum split-K slabs; q -> [T][H*D]; k, v -> page slot of this layer.
-// grid (T, ceil(N / 1024)); each thread owns 4 consecutive columns (same head).
+// QKV epilogue: q -> [T][H*D]; pre-RoPE k, v -> their page slot of this layer. The
+// accumulator [T][N] is cleared behind the read. grid (T, ceil(N / 1024)); a thread owns 4
+// consecutive columns (one head).
 template <typename T>
-__global__ void qkv_epilogue_kernel(int T_, int H, int G, int D, const float* __restrict__ part, int splits,
-                                    T* __restrict__ q, const int* __restrict__ slot, T* __restrict__ kl,
-                                    T* __restrict__ vl) {
+__global__ void qkv_epilogue_kernel(int H, int G, int D, float* __restrict__ acc, T* __restrict__ q,
+                                    const int* __restrict__ slot, T* __restrict__ kl, T* __restrict__ vl) {
   const int t = blockIdx.x;
   const int N = (H + 2 * G) * D;
   const int n = (blockIdx.y * blockDim.x + threadIdx.x) * 4;
   if (n >= N) return;
-  const float4 acc = sum4(part, splits, (size_t)T_ * N, (size_t)t * N + n);
+  const float4 v = take4(acc, (size_t)t * N + n);
   if (n < H * D) {
-    store4<T>(q + (size_t)t * H * D + n, acc);
+    store4<T>(q + (size_t)t * H * D + n, v);
   } else {
     const int s_ = slot[t];
     const int blk = s_ / kBlock, r = s_ % kBlock;
@@ -99,37 +95,34 @@ __global__ void qkv_epilogue_kernel(int T_, int H, int G, int D, const float* __
     const int kv = m / (G * D);          // 0: K, 1: V
     const int g = (m % (G * D)) / D, i = m % D;
     T* dst = kv == 0 ? kl : vl;
-    store4<T>(dst + (((size_t)blk * G + g) * kBlock + r) * D + i, acc);
+    store4<T>(dst + (((size_t)blk * G + g) * kBlock + r) * D + i, v);
   }
 }
 
-// h[t] += sum of split slabs; then RMSNorm. One CTA per row, 4 columns per thread-step.
+// y = RMSNorm(h[t]) * gain (the projection GEMMs have already added into h). Not final:
+// x[t] = y in the model dtype. Final: hidden_out[out_row[t]] = y (fp32) and
+// lm_x[lg_row[t]] = y (model dtype) where those indices are >= 0.
 template <typename T>
-__global__ void __launch_bounds__(512) residual_norm_kernel(int T_, int d, const float* __restrict__ part, int splits,
-                                     float* __restrict__ h, const float* __restrict__ gain, float eps,
-                                     T* __restrict__ x, int final_layer, const int* __restrict__ out_row,
-                                     float* __restrict__ hidden_out, const int* __restrict__ lg_row,
-                                     T* __restrict__ lm_x) {
-  extern __shared__ float row[];
+__global__ void __launch_bounds__(512) rmsnorm_rows_kernel(int d, const float* __restrict__ h,
+                                                           const float* __restrict__ gain, float eps,
+                                                           T* __restrict__ x, int final_layer,
+                                                           const int* __restrict__ out_row,
+                                                           float* __restrict__ hidden_out,
+                                                           const int* __restrict__ lg_row, T* __restrict__ lm_x) {
   __shared__ float red[32];
   const int t = blockIdx.x;
+  const float* hr = h + (size_t)t * d;
   float ss = 0.f;
   for (int i = threadIdx.x * 4; i < d; i += blockDim.x * 4) {
-    float4 v = *reinterpret_cast<const float4*>(h + (size_t)t * d + i);
-    const float4 a = sum4(part, splits, (size_t)T_ * d, (size_t)t * d + i);
-    v.x += a.x;
-    v.y += a.y;
-    v.z += a.z;
-    v.w += a.w;
-    *reinterpret_cast<float4*>(row + i) = v;
-    *reinterpret_cast<float4*>(h + (size_t)t * d + i) = v;
+    const float4 v = *reinterpret_cast<const float4*>(hr + i);
     ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
   }
   ss = block_sum(ss, red);
   const float r = rsqrtf(ss / d + eps);
   const int o = final_layer ? out_row[t] : -1, lg = final_layer ? lg_row[t] : -1;
+  if (final_layer && o < 0 && lg < 0) return;
   for (int i = threadIdx.x * 4; i < d; i += blockDim.x * 4) {
-    const float4 v = *reinterpret_cast<const float4*>(row + i);
+    const float4 v = *reinterpret_cast<const float4*>(hr + i);
     const float4 g = *reinterpret_cast<const float4*>(gain + i);
     const float4 y = make_float4(v.x * r * g.x, v.y * r * g.y, v.z * r * g.z, v.w * r * g.w);
     if (!final_layer) {
@@ -141,28 +134,19 @@ __global__ void __launch_bounds__(512) residual_norm_kernel(int T_, int d, const
   }
 }
 
-// grid (T, ceil(F / 1024)); 4 outputs per thread.
+// act = silu(gate) * up from the accumulator [T][2F] (gate columns, then up columns), which
+// is cleared behind the read. grid (T, ceil(F / 1024)); 4 outputs per thread.
 template <typename T>
-__global__ void swiglu_kernel(int T_, int F, const float* __restrict__ part, int splits, T* __restrict__ act) {
+__global__ void swiglu_kernel(int F, float* __restrict__ acc, T* __restrict__ act) {
   const int t = blockIdx.x;
   const int j = (blockIdx.y * blockDim.x + threadIdx.x) * 4;
   if (j >= F) return;
   const size_t N = 2 * (size_t)F;
-  const float4 a = sum4(part, splits, (size_t)T_ * N, (size_t)t * N + j);
-  const float4 b = sum4(part, splits, (size_t)T_ * N, (size_t)t * N + F + j);
+  const float4 a = take4(acc, (size_t)t * N + j);
+  const float4 b = take4(acc, (size_t)t * N + F + j);
   const float4 y = make_float4(a.x / (1.f + __expf(-a.x)) * b.x, a.y / (1.f + __expf(-a.y)) * b.y,
                                a.z / (1.f + __expf(-a.z)) * b.z, a.w / (1.f + __expf(-a.w)) * b.w);
   store4<T>(act + (size_t)t * F + j, y);
-}
-
-__global__ void sum_partials_kernel(int T_, int N, const float* __restrict__ part, int splits,
-                                    float* __restrict__ out) {
-  const size_t total = (size_t)T_ * N;
-  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
-    float acc = 0.f;
-    for (int s = 0; s < splits; ++s) acc += part[(size_t)s * total + i];
-    out[i] = acc;
-  }
 }
 
 // grid: (pairs, layers, 2 pools); 16-byte copies of one block of one layer.
@@ -205,48 +189,39 @@ void launch_embed_norm(int dtype, int T, int d, const void* embed, const int* to
     embed_norm_kernel<float><<<T, kRowThreads, sm, st>>>(d, (const float*)embed, tok, gain, eps, h, (float*)x);
 }
 
-void launch_qkv_epilogue(int dtype, int T, int H, int G, int D, const float* part, int splits, void* q,
-                         const int* slot, void* k_layer, void* v_layer, cudaStream_t st) {
+void launch_qkv_epilogue(int dtype, int T, int H, int G, int D, float* acc, void* q, const int* slot, void* k_layer,
+                         void* v_layer, cudaStream_t st) {
   if (T <= 0) return;
   const int N = (H + 2 * G) * D;
   dim3 grid(T, (N / 4 + kRowThreads - 1) / kRowThreads);
   if (dtype == PIC_BF16)
-    qkv_epilogue_kernel<__nv_bfloat16><<<grid, kRowThreads, 0, st>>>(T, H, G, D, part, splits, (__nv_bfloat16*)q, slot,
+    qkv_epilogue_kernel<__nv_bfloat16><<<grid, kRowThreads, 0, st>>>(H, G, D, acc, (__nv_bfloat16*)q, slot,
                                                                      (__nv_bfloat16*)k_layer, (__nv_bfloat16*)v_layer);
   else
-    qkv_epilogue_kernel<float><<<grid, kRowThreads, 0, st>>>(T, H, G, D, part, splits, (float*)q, slot,
-                                                             (float*)k_layer, (float*)v_layer);
+    qkv_epilogue_kernel<float><<<grid, kRowThreads, 0, st>>>(H, G, D, acc, (float*)q, slot, (float*)k_layer,
+                                                             (float*)v_layer);
 }
 
-void launch_residual_norm(int dtype, int T, int d, const float* part, int splits, float* h, const float* gain,
-                          float eps, void* x, bool final_layer, const int* out_row, float* hidden_out,
-                          const int* lg_row, void* lm_x, cudaStream_t st) {
+void launch_rmsnorm_rows(int dtype, int T, int d, const float* h, const float* gain, float eps, void* x,
+                         bool final_layer, const int* out_row, float* hidden_out, const int* lg_row, void* lm_x,
+                         cudaStream_t st) {
   if (T <= 0) return;
-  const size_t sm = d * sizeof(float);
   const int thr = std::min(512, std::max(128, (d / 4 + 31) / 32 * 32));
   if (dtype == PIC_BF16)
-    residual_norm_kernel<__nv_bfloat16><<<T, thr, sm, st>>>(T, d, part, splits, h, gain, eps,
-                                                                    (__nv_bfloat16*)x, final_layer, out_row,
-                                                                    hidden_out, lg_row, (__nv_bfloat16*)lm_x);
+    rmsnorm_rows_kernel<__nv_bfloat16><<<T, thr, 0, st>>>(d, h, gain, eps, (__nv_bfloat16*)x, final_layer, out_row,
+                                                          hidden_out, lg_row, (__nv_bfloat16*)lm_x);
   else
-    residual_norm_kernel<float><<<T, thr, sm, st>>>(T, d, part, splits, h, gain, eps, (float*)x, final_layer,
-                                                            out_row, hidden_out, lg_row, (float*)lm_x);
+    rmsnorm_rows_kernel<float><<<T, thr, 0, st>>>(d, h, gain, eps, (float*)x, final_layer, out_row, hidden_out,
+                                                  lg_row, (float*)lm_x);
 }
 
-void launch_swiglu(int dtype, int T, int F, const float* part, int splits, void* act, cudaStream_t st) {
+void launch_swiglu(int dtype, int T, int F, float* acc, void* act, cudaStream_t st) {
   if (T <= 0) return;
   dim3 grid(T, (F / 4 + kRowThreads - 1) / kRowThreads);
   if (dtype == PIC_BF16)
-    swiglu_kernel<__nv_bfloat16><<<grid, kRowThreads, 0, st>>>(T, F, part, splits, (__nv_bfloat16*)act);
+    swiglu_kernel<__nv_bfloat16><<<grid, kRowThreads, 0, st>>>(F, acc, (__nv_bfloat16*)act);
   else
-    swiglu_kernel<float><<<grid, kRowThreads, 0, st>>>(T, F, part, splits, (float*)act);
-}
-
-void launch_sum_partials(int T, int N, const float* part, int splits, float* out, cudaStream_t st) {
-  const size_t total = (size_t)T * N;
-  if (total == 0) return;
-  const int blocks = (int)std::min<size_t>((total + 255) / 256, 152 * 8);
-  sum_partials_kernel<<<blocks, 256, 0, st>>>(T, N, part, splits, out);
+    swiglu_kernel<float><<<grid, kRowThreads, 0, st>>>(F, acc, (float*)act);
 }
 
 void launch_copy_blocks(int n_pairs, const int* pairs, int n_layers, int num_blocks_total, size_t block_bytes,

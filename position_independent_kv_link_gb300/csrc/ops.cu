@@ -46,29 +46,19 @@ AttnScratchLayout attn_layout(int T, int n_heads, int n_kv_heads, int head_dim, 
 
 extern "C" {
 
-size_t pic_op_gemm_scratch_bytes(int32_t dtype, int32_t N, int32_t K, int32_t T) {
-  const int sp = op_gemm_splits(dtype, N, K, T);
-  return sp > 1 ? (size_t)sp * N * T * 4 : 0;
-}
-
 pic_status pic_op_gemm(int32_t dtype, const void* W, const void* X, float* Y, int32_t N, int32_t K, int32_t T,
-                       void* scratch, size_t scratch_bytes, pic_stream_t stream) {
+                       pic_stream_t stream) {
   if (!W || !X || !Y || N < 1 || K < 1 || T < 1 || (dtype != PIC_F32 && dtype != PIC_BF16))
     return fail(PIC_ERR_INVALID_ARG, "invalid gemm arguments");
   cudaStream_t st = (cudaStream_t)stream;
   const int sp = op_gemm_splits(dtype, N, K, T);
-  float* part = Y;
-  if (sp > 1) {
-    if (!scratch || scratch_bytes < (size_t)sp * N * T * 4) return fail(PIC_ERR_INVALID_ARG, "gemm scratch too small");
-    part = (float*)scratch;
-  }
+  PIC_CUDA(cudaMemsetAsync(Y, 0, (size_t)T * N * sizeof(float), st));
   if (dtype == PIC_BF16 && tc_gemm_supported(N, K, T)) {
-    pic_status e = tc_gemm_run(W, X, part, N, K, T, sp, st);
+    pic_status e = tc_gemm_run(W, X, Y, N, K, T, sp, st);
     if (e != PIC_OK) return e;
   } else {
-    launch_gemm_simt(dtype, W, X, part, N, K, T, 1, st);
+    launch_gemm_simt(dtype, W, X, Y, N, K, T, 1, st);
   }
-  if (sp > 1) launch_sum_partials(T, N, part, sp, Y, st);
   PIC_CUDA(cudaGetLastError());
   return PIC_OK;
 }

@@ -38,20 +38,17 @@ inline size_t dtype_size(int dtype) { return dtype == PIC_BF16 ? 2 : 4; }
 // h[t] = E[tok[t]] (fp32); x[t] = RMSNorm(h[t]) * gain in the model dtype.
 void launch_embed_norm(int dtype, int T, int d, const void* embed, const int* tok, const float* gain, float eps,
                        float* h, void* x, cudaStream_t st);
-// Sums `splits` partial [T][N] slabs of the fused QKV projection. Writes q [T][H*D] (dtype)
-// and the pre-RoPE k, v rows into page slots of one layer of the pools.
-void launch_qkv_epilogue(int dtype, int T, int H, int G, int D, const float* part, int splits, void* q,
-                         const int* slot, void* k_layer, void* v_layer, cudaStream_t st);
-// h[t] += sum of partials; y = RMSNorm(h[t]) * gain. Not final: x[t] = y (dtype).
-// Final: hidden_out[out_row[t]] = y (fp32) when out_row[t] >= 0 and lm_x[lg_row[t]] = y
-// (dtype) when lg_row[t] >= 0.
-void launch_residual_norm(int dtype, int T, int d, const float* part, int splits, float* h, const float* gain,
-                          float eps, void* x, bool final_layer, const int* out_row, float* hidden_out,
-                          const int* lg_row, void* lm_x, cudaStream_t st);
-// act[t][j] = silu(sum gate) * (sum up) from partial slabs [T][2F] (gate cols, then up cols).
-void launch_swiglu(int dtype, int T, int F, const float* part, int splits, void* act, cudaStream_t st);
-// out[t][n] = sum over splits of part[s][t][n].
-void launch_sum_partials(int T, int N, const float* part, int splits, float* out, cudaStream_t st);
+// QKV epilogue: reads (and clears) the fp32 accumulator [T][(H+2G)D], writes q [T][H*D]
+// (dtype) and the pre-RoPE k, v rows into their page slots of one layer of the pools.
+void launch_qkv_epilogue(int dtype, int T, int H, int G, int D, float* acc, void* q, const int* slot, void* k_layer,
+                         void* v_layer, cudaStream_t st);
+// y = RMSNorm(h[t]) * gain. Not final: x[t] = y (dtype). Final: hidden_out[out_row[t]] = y
+// (fp32) when out_row[t] >= 0 and lm_x[lg_row[t]] = y (dtype) when lg_row[t] >= 0.
+void launch_rmsnorm_rows(int dtype, int T, int d, const float* h, const float* gain, float eps, void* x,
+                         bool final_layer, const int* out_row, float* hidden_out, const int* lg_row, void* lm_x,
+                         cudaStream_t st);
+// act[t][j] = silu(gate) * up from the accumulator [T][2F] (gate cols, then up cols), cleared behind.
+void launch_swiglu(int dtype, int T, int F, float* acc, void* act, cudaStream_t st);
 // For each pair i: copy block src[i] -> dst[i] in every layer of both pools.
 void launch_copy_blocks(int n_pairs, const int* pairs, int n_layers, int num_blocks_total, size_t block_bytes,
                         void* k_pool, void* v_pool, cudaStream_t st);
@@ -60,8 +57,8 @@ void launch_import_kv(int dtype, int n_layers, int n, int G, int D, const void* 
                       const int* blocks, int num_blocks_total, void* k_pool, void* v_pool, cudaStream_t st);
 
 // ------------------------------------------------------------------ GEMMs
-// part[s][T][N] (fp32) = X[T][k-range s] . W[N][k-range s]^T, K split evenly in `splits`.
-void launch_gemm_simt(int dtype, const void* W, const void* X, float* part, int N, int K, int T, int splits,
+// Y[T][N] (fp32) += X[T][K] . W[N][K]^T; K split evenly over `splits` CTAs (atomic adds).
+void launch_gemm_simt(int dtype, const void* W, const void* X, float* Y, int N, int K, int T, int splits,
                       cudaStream_t st);
 
 struct TcGemmPlan;  // tensor-map pair and schedule of one tcgen05 GEMM (k_gemm_tc.cu)
@@ -69,7 +66,8 @@ struct TcGemmPlan;  // tensor-map pair and schedule of one tcgen05 GEMM (k_gemm_
 bool tc_gemm_supported(int N, int K, int T);
 // Split-K factor chosen for a shape on a device with `num_sms` SMs (<= max_splits).
 int tc_gemm_splits(int N, int K, int T, int num_sms, int max_splits);
-pic_status tc_gemm_run(const void* W, const void* X, float* part, int N, int K, int T, int splits, cudaStream_t st);
+// Y[T][N] (fp32, 16-byte aligned) += X[T][K] . W[N][K]^T on tcgen05, K split in `splits`.
+pic_status tc_gemm_run(const void* W, const void* X, float* Y, int N, int K, int T, int splits, cudaStream_t st);
 // Reads and clears the device flag set when a tcgen05 kernel gave up a bounded wait.
 pic_status tc_check_timeout();
 

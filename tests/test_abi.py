@@ -53,7 +53,7 @@ def test_host_only_calls(lib):
     # invalid arguments are rejected before any CUDA call
     assert lib.pic_model_create(None, None, None) == 1
     assert lib.pic_release_chunk(None, 1) == 1
-    assert lib.pic_op_gemm(0, None, None, None, 1, 1, 1, None, 0, None) == 1
+    assert lib.pic_op_gemm(0, None, None, None, 1, 1, 1, None) == 1
 
 
 def test_build_targets_sm103a():
