@@ -170,16 +170,10 @@ namespace {
 
 int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
-int gemm_splits(const pic_store* s, int N, int K, int T) {
-  if (s->m->cfg.dtype != PIC_BF16 || !tc_gemm_supported(N, K, T)) return 1;
-  return tc_gemm_splits(N, K, T, s->m->num_sms, 16);
-}
-
 // Y[T][N] += X . W^T (fp32 Y accumulated in place)
-pic_status gemm(const pic_store* s, const void* W, const void* X, float* Y, int N, int K, int T, int splits,
-                cudaStream_t st) {
-  if (s->m->cfg.dtype == PIC_BF16 && tc_gemm_supported(N, K, T)) return tc_gemm_run(W, X, Y, N, K, T, splits, st);
-  launch_gemm_simt(s->m->cfg.dtype, W, X, Y, N, K, T, splits, st);
+pic_status gemm(const pic_store* s, const void* W, const void* X, float* Y, int N, int K, int T, cudaStream_t st) {
+  if (s->m->cfg.dtype == PIC_BF16 && tc_gemm_supported(N, K, T)) return tc_gemm_run(W, X, Y, N, K, T, st);
+  launch_gemm_simt(s->m->cfg.dtype, W, X, Y, N, K, T, 1, st);
   return PIC_OK;
 }
 
@@ -312,14 +306,10 @@ pic_status run_forward_impl(pic_store* s, const Batch& b, float* hidden_out, flo
   aa.n_combines = (int)combs.size();
 
   const int qkv = s->m->qkv_dim();
-  const int sp_qkv = gemm_splits(s, qkv, d, T);
-  const int sp_o = gemm_splits(s, d, H * D, T);
-  const int sp_gu = gemm_splits(s, 2 * F, d, T);
-  const int sp_dn = gemm_splits(s, d, F, T);
   auto gemm_bytes = [&](double N, double K, double rows) { return N * K * es + rows * K * es + rows * N * 4; };
-  auto run_gemm = [&](const void* W, const void* X, float* Y, int N, int K, int rows, int sp) {
+  auto run_gemm = [&](const void* W, const void* X, float* Y, int N, int K, int rows) {
     Rec r(s, st, PIC_PROF_GEMM, gemm_bytes(N, K, rows), 2.0 * N * K * rows, 1);
-    return gemm(s, W, X, Y, N, K, rows, sp, st);
+    return gemm(s, W, X, Y, N, K, rows, st);
   };
   // The QKV and gate/up GEMMs add into zeroed accumulators that their epilogues clear
   // again; the O and down projections add straight into the residual stream h.
@@ -329,7 +319,7 @@ pic_status run_forward_impl(pic_store* s, const Batch& b, float* hidden_out, flo
   }
   for (int l = 0; l < c.n_layers; ++l) {
     pic_status e;
-    if ((e = run_gemm(s->m->wqkv[l], s->x, s->qkv_acc, qkv, d, T, sp_qkv)) != PIC_OK) return e;
+    if ((e = run_gemm(s->m->wqkv[l], s->x, s->qkv_acc, qkv, d, T)) != PIC_OK) return e;
     {
       Rec r(s, st, PIC_PROF_ROWWISE, dT * dQKV * (8 + es), 0, 1);
       launch_qkv_epilogue(dt, T, H, G, D, s->qkv_acc, s->q, d_slot, s->k_layer(l), s->v_layer(l), st);
@@ -342,18 +332,18 @@ pic_status run_forward_impl(pic_store* s, const Batch& b, float* hidden_out, flo
       Rec r(s, st, PIC_PROF_ATTENTION, att_bytes, att_flops, att_launches);
       launch_attention(aa, st);
     }
-    if ((e = run_gemm(s->m->wo[l], s->attn, s->h, d, H * D, T, sp_o)) != PIC_OK) return e;
+    if ((e = run_gemm(s->m->wo[l], s->attn, s->h, d, H * D, T)) != PIC_OK) return e;
     {
       Rec r(s, st, PIC_PROF_ROWWISE, dT * dd * (4 + es), 0, 1);
       launch_rmsnorm_rows(dt, T, d, s->h, s->m->mlp_norm[l], c.rms_eps, s->x, false, nullptr, nullptr, nullptr,
                           nullptr, st);
     }
-    if ((e = run_gemm(s->m->wgu[l], s->x, s->gu_acc, 2 * F, d, T, sp_gu)) != PIC_OK) return e;
+    if ((e = run_gemm(s->m->wgu[l], s->x, s->gu_acc, 2 * F, d, T)) != PIC_OK) return e;
     {
       Rec r(s, st, PIC_PROF_ROWWISE, dT * 2 * dF * 8 + dT * dF * es, 0, 1);
       launch_swiglu(dt, T, F, s->gu_acc, s->act, st);
     }
-    if ((e = run_gemm(s->m->wdown[l], s->act, s->h, d, F, T, sp_dn)) != PIC_OK) return e;
+    if ((e = run_gemm(s->m->wdown[l], s->act, s->h, d, F, T)) != PIC_OK) return e;
     const bool last = l == c.n_layers - 1;
     {
       Rec r(s, st, PIC_PROF_ROWWISE, dT * dd * (4 + es), 0, 1);
@@ -362,10 +352,9 @@ pic_status run_forward_impl(pic_store* s, const Batch& b, float* hidden_out, flo
     }
   }
   if (!b.compile && b.n_lg > 0) {
-    const int sp = gemm_splits(s, c.vocab, d, b.n_lg);
     PIC_CUDA(cudaMemsetAsync(logits_out, 0, (size_t)b.n_lg * c.vocab * sizeof(float), st));
     pic_status e;
-    if ((e = run_gemm(s->m->lm_head, s->lm_x, logits_out, c.vocab, d, b.n_lg, sp)) != PIC_OK) return e;
+    if ((e = run_gemm(s->m->lm_head, s->lm_x, logits_out, c.vocab, d, b.n_lg)) != PIC_OK) return e;
   }
   PIC_CUDA(cudaGetLastError());
   return PIC_OK;

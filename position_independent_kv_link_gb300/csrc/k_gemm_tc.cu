@@ -2,15 +2,22 @@
 //
 //   Y[t][n] += sum_k W[n][k] * X[t][k]        (Y fp32, accumulated in place)
 //
-// The link step multiplies a few hundred selected rows by large weight matrices, so
-// the weights take the MMA's M side (128 rows per CTA) and the token rows its N side
-// (up to 256 per tile): one weight tile is streamed from HBM exactly once per token
-// tile. Operands are staged by TMA (128-byte swizzle, K-major) through a multi-stage
-// mbarrier ring; one thread issues tcgen05.mma with the fp32 accumulator in TMEM; all
-// four warps drain TMEM with tcgen05.ld into a shared-memory tile that one TMA bulk
-// reduce-add folds into Y. Split-K spreads the weight stream over every SM; the splits
-// meet in Y through those reductions, so no partial slabs are written or re-read, and a
-// projection that feeds the residual stream adds straight into it.
+// The link step multiplies a few hundred selected rows by large weight matrices: the
+// weights take the MMA's M side (128 rows per tile) and the token rows its N side (up
+// to 256 per tile), so each weight tile is streamed from HBM once per token tile.
+//
+// Persistent, stream-K, warp-specialized. The grid has one CTA per SM; the linear space
+// of (tile, 64-wide k-block) work is cut into equal contiguous ranges, one per CTA, so
+// every SM streams the same number of weight bytes. A CTA walks its range as segments
+// (maximal runs inside one tile). Each segment accumulates in one of two TMEM buffers
+// and is folded into Y by TMA bulk reduce-adds, so segments of the same tile that land
+// on different CTAs meet in Y with no fix-up pass, and the drain of one segment
+// overlaps the MMAs of the next.
+//
+//   warp 0     TMA producer of the weight tiles (deep ring: HBM latency)
+//   warp 1     MMA issuer (one thread): tcgen05.mma kind::f16, fp32 accumulators in TMEM
+//   warp 2     TMA producer of the activation tiles (shallow ring: they sit in L2); TMEM owner
+//   warps 3-6  epilogue: tcgen05.ld -> 16-row shared tile -> cp.reduce.async.bulk add
 //
 // Every mbarrier wait is bounded (~2 s of GPU time). On expiry the kernel raises a
 // device flag, stops issuing work, waits (bounded) for the copies and MMAs it started,
@@ -28,11 +35,14 @@ namespace pic {
 
 namespace {
 
-constexpr int BM = 128;          // weight rows per MMA (M); a CTA tile holds 1 or 2 of these
+constexpr int BM = 128;          // weight rows per tile (MMA M)
 constexpr int BK = 64;           // K per stage: 64 bf16 = one 128-byte swizzle row
 constexpr int UMMA_K = 16;       // K per tcgen05.mma (kind::f16)
-constexpr int A_HALF_BYTES = BM * BK * 2;
-constexpr int kThreads = 128;
+constexpr int A_STAGE = BM * BK * 2;   // 16 KB
+constexpr int EPI_ROWS = 16;     // token rows per reduce-add tile
+constexpr int EPI_BYTES = EPI_ROWS * BM * 4;  // 8 KB, double buffered
+constexpr int kWarps = 7;
+constexpr int kThreads = kWarps * 32;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
 __device__ int g_tc_timeout = 0;
@@ -53,6 +63,10 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
 
 __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
 __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
@@ -88,10 +102,10 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
 }
 
 // Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row atoms 1024 B apart.
+// (The leading byte offset is unused for K-major tiles whose K extent fits one swizzle row.)
 __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
   uint64_t d = 0;
   d |= (uint64_t)((addr & 0x3FFFFu) >> 4);   // start address
-  // leading byte offset: unused for K-major tiles whose K extent fits one swizzle row
   d |= (uint64_t)(1024 >> 4) << 32;           // stride byte offset between 8-row atoms
   d |= (uint64_t)1 << 46;                     // descriptor version
   d |= (uint64_t)2 << 61;                     // 128-byte swizzle
@@ -126,39 +140,81 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// named barrier of the four epilogue warps
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// same barrier with an AND over the 128 epilogue threads: all of them take the same branch
+__device__ __forceinline__ bool epi_all(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 q, %1, 0;\n bar.red.and.pred p, 1, 128, q;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(r)
+      : "r"((uint32_t)v)
+      : "memory");
+  return r != 0;
+}
+
 struct TcParams {
   int N, K, T;
   int BN;            // token rows per tile (multiple of 16, <= 256)
-  int stages;
-  int kb_per_split;  // k-blocks of BK per split
-  int nkb;           // total k-blocks
+  int SA, SB;        // weight / activation ring depths
+  int nkb;           // k-blocks per tile
+  int m_tiles;       // weight-row tiles
+  long long total;   // tiles * nkb work units
   uint32_t tmem_cols;
 };
 
-// MH = 128-row weight halves per CTA tile. Both halves share the staged activation
-// tile, so MH = 2 halves the activation bytes read from L2 per weight byte streamed.
-template <int MH>
+// Segment walk shared by the MMA issuer and the epilogue: [g, end) inside one tile.
+struct Seg {
+  long long g, end;
+  int tile;
+};
+__device__ __forceinline__ bool next_seg(Seg& s, long long hi, int nkb) {
+  s.g = s.end;
+  if (s.g >= hi) return false;
+  s.tile = (int)(s.g / nkb);
+  s.end = min(hi, (long long)(s.tile + 1) * nkb);
+  return true;
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_x,
                    const __grid_constant__ CUtensorMap map_y, const TcParams p) {
-  constexpr int A_STAGE_BYTES = MH * A_HALF_BYTES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const int stage_bytes = A_STAGE_BYTES + p.BN * BK * 2;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.stages * stage_bytes);
-  // bars[0..S): full, bars[S..2S): empty, bars[2S]: accumulator ready
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * p.stages + 1);
+  const int b_stage = p.BN * BK * 2;
+  uint8_t* ringA = smem;
+  uint8_t* ringB = ringA + p.SA * A_STAGE;
+  uint8_t* epi = ringB + p.SB * b_stage;                      // [2][16][128] fp32
+  uint64_t* bars = reinterpret_cast<uint64_t*>(epi + 2 * EPI_BYTES);
+  uint64_t* a_full = bars;
+  uint64_t* a_empty = a_full + p.SA;
+  uint64_t* b_full = a_empty + p.SA;
+  uint64_t* b_empty = b_full + p.SB;
+  uint64_t* acc_full = b_empty + p.SB;     // [2]
+  uint64_t* acc_empty = acc_full + 2;      // [2]
+  uint64_t* mma_done = acc_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
   __shared__ volatile int s_abort;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int m0 = blockIdx.x * BM * MH, t0 = blockIdx.y * p.BN, split = blockIdx.z;
-  const int kb0 = split * p.kb_per_split;
-  const int nk = min(p.nkb - kb0, p.kb_per_split);
-  const uint32_t acc_bar = smem_u32(bars + 2 * p.stages);
+  const long long lo = p.total * blockIdx.x / gridDim.x, hi = p.total * (blockIdx.x + 1) / gridDim.x;
 
   if (threadIdx.x == 0) {
     s_abort = 0;
-    for (int i = 0; i < 2 * p.stages + 1; ++i) mbar_init(smem_u32(bars + i), 1);
+    for (int i = 0; i < p.SA; ++i) {
+      mbar_init(smem_u32(a_full + i), 1);
+      mbar_init(smem_u32(a_empty + i), 1);
+    }
+    for (int i = 0; i < p.SB; ++i) {
+      mbar_init(smem_u32(b_full + i), 1);
+      mbar_init(smem_u32(b_empty + i), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(acc_full + i), 1);
+      mbar_init(smem_u32(acc_empty + i), 4);   // one arrival per epilogue warp
+    }
+    mbar_init(smem_u32(mma_done), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
@@ -173,90 +229,132 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0 && lane == 0) {
-    // ---------------- TMA producer
-    uint64_t pol_w, pol_x;
-    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol_w));
-    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol_x));
-    int issued = 0;
-    for (int kb = 0; kb < nk; ++kb) {
-      const int st = kb % p.stages;
-      const uint32_t ph = (kb / p.stages) & 1;
-      if (!mbar_wait(smem_u32(bars + p.stages + st), ph ^ 1)) {
+    // ---------------- weight producer: HBM stream, evicted first from L2
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    long long issued = 0;
+    for (long long g = lo; g < hi; ++g) {
+      const long long i = g - lo;
+      const int st = (int)(i % p.SA);
+      if (s_abort || !mbar_wait(smem_u32(a_empty + st), (uint32_t)((i / p.SA) & 1) ^ 1)) {
         s_abort = 1;
         break;
       }
-      const uint32_t full = smem_u32(bars + st);
-      const uint32_t a_dst = smem_u32(smem + st * stage_bytes);
-      const uint32_t b_dst = a_dst + A_STAGE_BYTES;
-      mbar_expect_tx(full, stage_bytes);
-      const int kx = (kb0 + kb) * BK;
-#pragma unroll
-      for (int hf = 0; hf < MH; ++hf) tma_load_2d(a_dst + hf * A_HALF_BYTES, &map_w, kx, m0 + hf * BM, full, pol_w);
-      tma_load_2d(b_dst, &map_x, kx, t0, full, pol_x);
-      issued = kb + 1;
+      const int tile = (int)(g / p.nkb), kb = (int)(g % p.nkb);
+      const uint32_t full = smem_u32(a_full + st);
+      mbar_expect_tx(full, A_STAGE);
+      tma_load_2d(smem_u32(ringA + st * A_STAGE), &map_w, kb * BK, (tile % p.m_tiles) * BM, full, pol);
+      issued = i + 1;
     }
-    // copies still in flight must land before this CTA's shared memory is released
-    for (int kb = max(0, issued - p.stages); kb < issued; ++kb)
-      if (!mbar_wait(smem_u32(bars + kb % p.stages), (kb / p.stages) & 1)) break;
+    for (long long i = max(0LL, issued - p.SA); i < issued; ++i)   // land in-flight copies before exit
+      if (!mbar_wait(smem_u32(a_full + (int)(i % p.SA)), (uint32_t)((i / p.SA) & 1))) break;
+  } else if (warp == 2 && lane == 0) {
+    // ---------------- activation producer: small, reused by every weight tile, kept in L2
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    long long issued = 0;
+    for (long long g = lo; g < hi; ++g) {
+      const long long i = g - lo;
+      const int st = (int)(i % p.SB);
+      if (s_abort || !mbar_wait(smem_u32(b_empty + st), (uint32_t)((i / p.SB) & 1) ^ 1)) {
+        s_abort = 1;
+        break;
+      }
+      const int tile = (int)(g / p.nkb), kb = (int)(g % p.nkb);
+      const uint32_t full = smem_u32(b_full + st);
+      mbar_expect_tx(full, b_stage);
+      tma_load_2d(smem_u32(ringB + st * b_stage), &map_x, kb * BK, (tile / p.m_tiles) * p.BN, full, pol);
+      issued = i + 1;
+    }
+    for (long long i = max(0LL, issued - p.SB); i < issued; ++i)
+      if (!mbar_wait(smem_u32(b_full + (int)(i % p.SB)), (uint32_t)((i / p.SB) & 1))) break;
   } else if (warp == 1 && lane == 0) {
     // ---------------- MMA issuer
     const uint32_t idesc = idesc_bf16(BM, p.BN);
-    for (int kb = 0; kb < nk; ++kb) {
-      const int st = kb % p.stages;
-      if (s_abort || !mbar_wait(smem_u32(bars + st), (kb / p.stages) & 1)) {
+    Seg sg{0, lo, 0};
+    int s = 0;
+    long long i = 0;
+    bool stop = false;
+    while (!stop && next_seg(sg, hi, p.nkb)) {
+      const int ab = s & 1;
+      if (s_abort || !mbar_wait(smem_u32(acc_empty + ab), (uint32_t)((s >> 1) & 1) ^ 1)) {
         s_abort = 1;
         break;
       }
       asm volatile("tcgen05.fence::after_thread_sync;");
-      const uint32_t a_base = smem_u32(smem + st * stage_bytes);
-      const uint32_t b_base = a_base + A_STAGE_BYTES;
-#pragma unroll
-      for (int k = 0; k < BK / UMMA_K; ++k) {
-        const uint64_t bd = smem_desc_sw128(b_base + k * UMMA_K * 2);
-#pragma unroll
-        for (int hf = 0; hf < MH; ++hf) {
-          const uint64_t ad = smem_desc_sw128(a_base + hf * A_HALF_BYTES + k * UMMA_K * 2);
-          umma_bf16(tmem + hf * p.BN, ad, bd, idesc, (kb | k) != 0);
+      const uint32_t d_tmem = tmem + ab * p.BN;
+      for (long long g = sg.g; g < sg.end; ++g, ++i) {
+        const int sa = (int)(i % p.SA), sb = (int)(i % p.SB);
+        if (s_abort || !mbar_wait(smem_u32(a_full + sa), (uint32_t)((i / p.SA) & 1)) ||
+            !mbar_wait(smem_u32(b_full + sb), (uint32_t)((i / p.SB) & 1))) {
+          s_abort = 1;
+          stop = true;
+          break;
         }
+        asm volatile("tcgen05.fence::after_thread_sync;");
+        const uint32_t a_base = smem_u32(ringA + sa * A_STAGE);
+        const uint32_t b_base = smem_u32(ringB + sb * b_stage);
+#pragma unroll
+        for (int k = 0; k < BK / UMMA_K; ++k)
+          umma_bf16(d_tmem, smem_desc_sw128(a_base + k * UMMA_K * 2), smem_desc_sw128(b_base + k * UMMA_K * 2),
+                    idesc, (g != sg.g || k != 0) ? 1u : 0u);
+        umma_commit(smem_u32(a_empty + sa));  // stages free once these MMAs retire
+        umma_commit(smem_u32(b_empty + sb));
       }
-      umma_commit(smem_u32(bars + p.stages + st));  // stage free once these MMAs retire
+      if (!stop) umma_commit(smem_u32(acc_full + ab));
+      ++s;
     }
-    umma_commit(acc_bar);  // accumulator complete (or abandoned) once every MMA retires
+    umma_commit(smem_u32(mma_done));          // fires once every MMA of this CTA has retired
+    mbar_wait(smem_u32(mma_done), 0);
+  } else if (warp >= 3) {
+    // ---------------- epilogue: TMEM -> [16 tokens][128 rows] fp32 tile -> bulk reduce-add into Y
+    const int q = warp & 3;                    // TMEM lane quarter this warp may access
+    const int nl = q * 32 + lane;              // weight row within the tile
+    const bool leader = (warp == 3 && lane == 0);
+    float* stg = reinterpret_cast<float*>(epi);
+    Seg sg{0, lo, 0};
+    int s = 0, buf = 0;
+    while (next_seg(sg, hi, p.nkb)) {
+      const int ab = s & 1;
+      bool ok = !s_abort && mbar_wait(smem_u32(acc_full + ab), (uint32_t)((s >> 1) & 1));
+      ok = epi_all(ok);
+      if (!ok) {
+        s_abort = 1;
+        break;
+      }
+      asm volatile("tcgen05.fence::after_thread_sync;");
+      const int m0 = (sg.tile % p.m_tiles) * BM, t0 = (sg.tile / p.m_tiles) * p.BN;
+      const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + ab * p.BN;
+      for (int c = 0; c < p.BN; c += EPI_ROWS) {
+        float v[16];
+        tmem_ld16(taddr + c, v);
+        float* S = stg + buf * (EPI_ROWS * BM);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) S[j * BM + nl] = v[j];
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        epi_bar();
+        if (leader) {
+          if (t0 + c < p.T)
+            asm volatile(
+                "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                    reinterpret_cast<uint64_t>(&map_y)),
+                "r"(m0), "r"(t0 + c), "r"(smem_u32(S))
+                : "memory");
+          asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+          asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");  // the other buffer is free again
+        }
+        epi_bar();
+        buf ^= 1;
+      }
+      // the MMAs of the segment after next may overwrite this accumulator
+      asm volatile("tcgen05.fence::before_thread_sync;");
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(acc_empty + ab));
+      ++s;
+    }
+    if (leader) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
   }
   __syncwarp();
-
-  // ---------------- epilogue: TMEM -> shared tile [BN][128] fp32 -> TMA reduce-add into Y
-  bool ok = mbar_wait(acc_bar, 0);
-  ok = __syncthreads_and(ok) && !s_abort;  // block-uniform; warps reconverged for .sync.aligned loads
-  asm volatile("tcgen05.fence::after_thread_sync;");
-  if (ok) {
-    // every staged operand has been consumed by the MMAs, so the ring's memory is free
-    float* S = reinterpret_cast<float*>(smem);
-    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
-    const int nl = warp * 32 + lane;
-#pragma unroll
-    for (int hf = 0; hf < MH; ++hf) {
-      for (int c = 0; c < p.BN; c += 16) {
-        float v[16];
-        tmem_ld16(lane_base + hf * p.BN + c, v);
-#pragma unroll
-        for (int j = 0; j < 16; ++j) S[(c + j) * BM + nl] = v[j];
-      }
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      __syncthreads();
-      if (threadIdx.x == 0) {
-        asm volatile(
-            "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
-                reinterpret_cast<uint64_t>(&map_y)),
-            "r"(m0 + hf * BM), "r"(t0), "r"(smem_u32(S))
-            : "memory");
-        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-        asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");  // tile read out before it is reused
-      }
-      __syncthreads();
-    }
-    if (threadIdx.x == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-  }
   asm volatile("tcgen05.fence::before_thread_sync;");
   __syncthreads();
   if (warp == 2) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(p.tmem_cols));
@@ -275,19 +373,20 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
   return fn;
 }
 
-// fp32 [rows][cols] destination of the bulk reduce-add; box = 128 columns x box_rows rows
-bool make_map_f32(CUtensorMap* m, void* base, int rows, int cols, int box_rows) {
+// fp32 [rows][cols] destination of the bulk reduce-add; box = 128 columns x EPI_ROWS rows
+bool make_map_f32(CUtensorMap* m, void* base, int rows, int cols) {
   auto enc = get_encode();
   if (!enc) return false;
   cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)cols * 4};
-  cuuint32_t box[2] = {(cuuint32_t)BM, (cuuint32_t)box_rows};
+  cuuint32_t box[2] = {(cuuint32_t)BM, (cuuint32_t)EPI_ROWS};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                    CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
+// bf16 K-major operand [rows][K]; box = 64 K x box_rows rows, 128-byte swizzle
 bool make_map(CUtensorMap* m, const void* base, int rows, int K, int box_rows) {
   auto enc = get_encode();
   if (!enc) return false;
@@ -306,37 +405,23 @@ int pick_bn(int T) {
   return std::max(16, (T + 15) / 16 * 16);
 }
 
+int device_sms() {
+  static int sms[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (!sms[dev]) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    sms[dev] = n > 0 ? n : 148;
+  }
+  return sms[dev];
+}
+
 }  // namespace
 
 bool tc_gemm_supported(int N, int K, int T) { return N >= BM && N % BM == 0 && K >= BK && K % BK == 0 && T >= 1; }
 
-// Two weight halves per CTA when the shape allows (N multiple of 256, at most 256 token
-// rows per tile so both fp32 accumulators fit the 512 TMEM columns).
-int pick_mh(int N, int T) { return (N % (2 * BM) == 0) ? 2 : 1; }
-
-int tc_gemm_splits(int N, int K, int T, int num_sms, int max_splits) {
-  const int BN = pick_bn(T);
-  const long long tiles = (long long)(N / (BM * pick_mh(N, T))) * ((T + BN - 1) / BN);
-  const int nkb = K / BK;
-  const int smax = std::max(1, std::min({max_splits, nkb / 4, 16}));
-  const double epi = 2.0;  // epilogue cost in k-block units
-  int best = 1;
-  double best_t = 1e30;
-  for (int s = 1; s <= smax; ++s) {
-    const int kps = (nkb + s - 1) / s;
-    const int real_s = (nkb + kps - 1) / kps;
-    const long long ctas = tiles * real_s;
-    const long long waves = (ctas + num_sms - 1) / num_sms;
-    const double t = (double)waves * (kps + epi);
-    if (t < best_t - 1e-9) {
-      best_t = t;
-      best = real_s;
-    }
-  }
-  return best;
-}
-
-pic_status tc_gemm_run(const void* W, const void* X, float* Y, int N, int K, int T, int splits, cudaStream_t st) {
+pic_status tc_gemm_run(const void* W, const void* X, float* Y, int N, int K, int T, cudaStream_t st) {
   if (!tc_gemm_supported(N, K, T)) return fail(PIC_ERR_UNSUPPORTED, "tcgen05 gemm: unsupported shape");
   if (((uintptr_t)W | (uintptr_t)X | (uintptr_t)Y) % 16)
     return fail(PIC_ERR_INVALID_ARG, "tcgen05 gemm: operands not 16-byte aligned");
@@ -346,34 +431,33 @@ pic_status tc_gemm_run(const void* W, const void* X, float* Y, int N, int K, int
   p.T = T;
   p.BN = pick_bn(T);
   p.nkb = K / BK;
-  splits = std::max(1, std::min(splits, p.nkb));
-  p.kb_per_split = (p.nkb + splits - 1) / splits;
-  const int real_splits = (p.nkb + p.kb_per_split - 1) / p.kb_per_split;
-  if (real_splits != splits) return fail(PIC_ERR_INVALID_ARG, "tcgen05 gemm: split count leaves an empty split");
-  const int mh = pick_mh(N, T);
-  const int stage_bytes = mh * A_HALF_BYTES + p.BN * BK * 2;
-  const int budget = 227 * 1024 - 2048;  // opt-in limit minus alignment slack, barriers and static smem
-  p.stages = std::max(2, std::min(8, budget / stage_bytes));
+  p.m_tiles = N / BM;
+  const long long tiles = (long long)p.m_tiles * ((T + p.BN - 1) / p.BN);
+  p.total = tiles * p.nkb;
+  const int b_stage = p.BN * BK * 2;
+  // shared memory: the weight ring gets what the activation ring, the two epilogue tiles
+  // and the barriers leave of the opt-in limit
+  const int budget = 227 * 1024 - 1024 - 2 * EPI_BYTES - 512;
+  p.SB = b_stage <= 8192 ? 4 : (b_stage <= 16384 ? 3 : 2);
+  p.SA = std::min(12, (budget - p.SB * b_stage) / A_STAGE);
+  if (p.SA < 2) return fail(PIC_ERR_UNSUPPORTED, "tcgen05 gemm: pipeline does not fit shared memory");
   p.tmem_cols = 32;
-  while ((int)p.tmem_cols < mh * p.BN) p.tmem_cols <<= 1;
-  if ((size_t)p.stages * stage_bytes < (size_t)p.BN * BM * 4)
-    return fail(PIC_ERR_UNSUPPORTED, "tcgen05 gemm: staging tile does not fit the pipeline memory");
+  while ((int)p.tmem_cols < 2 * p.BN) p.tmem_cols <<= 1;
   CUtensorMap mw, mx, my;
-  if (!make_map(&mw, W, N, K, BM) || !make_map(&mx, X, T, K, p.BN) || !make_map_f32(&my, Y, T, N, p.BN))
+  if (!make_map(&mw, W, N, K, BM) || !make_map(&mx, X, T, K, p.BN) || !make_map_f32(&my, Y, T, N))
     return fail(PIC_ERR_CUDA, "cuTensorMapEncodeTiled failed");
-  const size_t smem = 1024 + (size_t)p.stages * stage_bytes + (2 * p.stages + 2) * 8;
-  // raise the kernel's dynamic shared-memory limit to what this launch needs (once per size, per device)
+  const size_t smem =
+      1024 + (size_t)p.SA * A_STAGE + (size_t)p.SB * b_stage + 2 * EPI_BYTES + (2 * p.SA + 2 * p.SB + 6) * 8 + 16;
   int dev = 0;
   cudaGetDevice(&dev);
-  static size_t attr_smem[2][64] = {};
-  auto kern = mh == 2 ? tc_gemm_kernel<2> : tc_gemm_kernel<1>;
-  if (dev < 0 || dev >= 64 || attr_smem[mh - 1][dev] < smem) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  static size_t attr_smem[64] = {};
+  if (dev < 0 || dev >= 64 || attr_smem[dev] < smem) {
+    cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return fail(PIC_ERR_CUDA, std::string("tcgen05 gemm attribute: ") + cudaGetErrorString(e));
-    if (dev >= 0 && dev < 64) attr_smem[mh - 1][dev] = smem;
+    if (dev >= 0 && dev < 64) attr_smem[dev] = smem;
   }
-  dim3 grid(N / (BM * mh), (T + p.BN - 1) / p.BN, splits);
-  kern<<<grid, kThreads, smem, st>>>(mw, mx, my, p);
+  const int grid = (int)std::min<long long>(device_sms(), p.total);
+  tc_gemm_kernel<<<grid, kThreads, smem, st>>>(mw, mx, my, p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(PIC_ERR_CUDA, std::string("tcgen05 gemm launch: ") + cudaGetErrorString(e));
   return PIC_OK;

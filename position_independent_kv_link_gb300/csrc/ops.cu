@@ -16,11 +16,6 @@ int current_sms() {
   return n;
 }
 
-int op_gemm_splits(int dtype, int N, int K, int T) {
-  if (dtype != PIC_BF16 || !tc_gemm_supported(N, K, T)) return 1;
-  return tc_gemm_splits(N, K, T, current_sms(), 16);
-}
-
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
 struct AttnScratchLayout {
@@ -51,10 +46,9 @@ pic_status pic_op_gemm(int32_t dtype, const void* W, const void* X, float* Y, in
   if (!W || !X || !Y || N < 1 || K < 1 || T < 1 || (dtype != PIC_F32 && dtype != PIC_BF16))
     return fail(PIC_ERR_INVALID_ARG, "invalid gemm arguments");
   cudaStream_t st = (cudaStream_t)stream;
-  const int sp = op_gemm_splits(dtype, N, K, T);
   PIC_CUDA(cudaMemsetAsync(Y, 0, (size_t)T * N * sizeof(float), st));
   if (dtype == PIC_BF16 && tc_gemm_supported(N, K, T)) {
-    pic_status e = tc_gemm_run(W, X, Y, N, K, T, sp, st);
+    pic_status e = tc_gemm_run(W, X, Y, N, K, T, st);
     if (e != PIC_OK) return e;
   } else {
     launch_gemm_simt(dtype, W, X, Y, N, K, T, 1, st);

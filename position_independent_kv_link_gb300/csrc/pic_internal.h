@@ -61,13 +61,10 @@ void launch_import_kv(int dtype, int n_layers, int n, int G, int D, const void* 
 void launch_gemm_simt(int dtype, const void* W, const void* X, float* Y, int N, int K, int T, int splits,
                       cudaStream_t st);
 
-struct TcGemmPlan;  // tensor-map pair and schedule of one tcgen05 GEMM (k_gemm_tc.cu)
-// Shape rules of the tcgen05 kernel.
+// Shape rules of the tcgen05 kernel (N % 128 == 0, K % 64 == 0).
 bool tc_gemm_supported(int N, int K, int T);
-// Split-K factor chosen for a shape on a device with `num_sms` SMs (<= max_splits).
-int tc_gemm_splits(int N, int K, int T, int num_sms, int max_splits);
-// Y[T][N] (fp32, 16-byte aligned) += X[T][K] . W[N][K]^T on tcgen05, K split in `splits`.
-pic_status tc_gemm_run(const void* W, const void* X, float* Y, int N, int K, int T, int splits, cudaStream_t st);
+// Y[T][N] (fp32, 16-byte aligned) += X[T][K] . W[N][K]^T on tcgen05 (persistent stream-K).
+pic_status tc_gemm_run(const void* W, const void* X, float* Y, int N, int K, int T, cudaStream_t st);
 // Reads and clears the device flag set when a tcgen05 kernel gave up a bounded wait.
 pic_status tc_check_timeout();
 
