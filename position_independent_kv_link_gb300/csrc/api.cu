@@ -221,6 +221,7 @@ pic_status run_forward_impl(pic_store* s, const Batch& b, float* hidden_out, flo
   pin.page_pos = &b.ppos;
   pin.G = G;
   pin.num_sms = s->m->num_sms;
+  pin.rows_per_block = attention_rows_per_block(dt, D, H / G);
   std::vector<AttnItem> items;
   std::vector<AttnCombine> combs;
   int n_parts = 0;
@@ -288,6 +289,7 @@ pic_status run_forward_impl(pic_store* s, const Batch& b, float* hidden_out, flo
 
   AttnArgs aa{};
   aa.dtype = dt;
+  aa.rb = pin.rows_per_block;
   aa.H = H;
   aa.G = G;
   aa.D = D;
@@ -470,8 +472,8 @@ pic_status pic_store_create(pic_model* m, const pic_store_config* cfg, void* k_p
   const size_t o_h = carve(R * d * 4), o_x = carve(R * std::max(d, HD) * es), o_q = carve(R * HD * es),
                o_attn = carve(R * HD * es), o_act = carve(R * F * es), o_lm = carve((size_t)sc.max_logit_rows * d * es),
                o_qkv = carve(R * (size_t)m->qkv_dim() * 4), o_gu = carve(R * 2 * F * 4),
-               o_atto = carve((size_t)s->att_parts_cap * kBlock * rep * c.head_dim * 4),
-               o_attml = carve((size_t)s->att_parts_cap * kBlock * rep * 2 * 4), o_meta = carve(s->meta_cap * 4),
+               o_atto = carve((size_t)s->att_parts_cap * kAttnPartRows * rep * c.head_dim * 4),
+               o_attml = carve((size_t)s->att_parts_cap * kAttnPartRows * rep * 2 * 4), o_meta = carve(s->meta_cap * 4),
                o_rope = carve((size_t)std::max(16, sc.max_positions) * (c.head_dim / 2) * sizeof(float2));
   cudaError_t e = cudaMalloc(&s->ws, off);
   if (e != cudaSuccess) return fail(PIC_ERR_CUDA, std::string("workspace cudaMalloc: ") + cudaGetErrorString(e));

@@ -80,7 +80,7 @@ __global__ void __launch_bounds__(128) attn_simt_kernel(AttnArgs a) {
 #pragma unroll
       for (int j = 0; j < NJ; ++j) out[((size_t)t * a.H + h) * D + lane + 32 * j] = from_f<T>(o[j] * inv);
     } else {
-      const size_t pi = ((size_t)it.part * kBlock + r) * rep + hh;
+      const size_t pi = ((size_t)it.part * kAttnPartRows + r) * rep + hh;
 #pragma unroll
       for (int j = 0; j < NJ; ++j) a.part_o[pi * D + lane + 32 * j] = o[j];
       if (lane == 0) {
@@ -107,7 +107,7 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(AttnArgs a) {
   for (int j = 0; j < NJ; ++j) o[j] = 0.f;
 #pragma unroll 4
   for (int s = 0; s < c.nparts; ++s) {
-    const size_t pi = ((size_t)(c.part0 + s) * kBlock + r) * rep + hh;
+    const size_t pi = ((size_t)(c.part0 + s) * kAttnPartRows + r) * rep + hh;
     const float2 ml = *reinterpret_cast<const float2*>(a.part_ml + pi * 2);
     float v[NJ];
     if constexpr (NJ == 4) {
@@ -137,7 +137,7 @@ void launch_simt(const AttnArgs& a, cudaStream_t st) {
   if (a.n_items > 0) attn_simt_kernel<T, D><<<a.n_items, 128, 0, st>>>(a);
   if (a.n_combines > 0) {
     const int rep = a.H / a.G;
-    attn_combine_kernel<T, D><<<dim3(a.n_combines, (kBlock * rep + 7) / 8), 256, 0, st>>>(a);
+    attn_combine_kernel<T, D><<<dim3(a.n_combines, (a.rb * rep + 7) / 8), 256, 0, st>>>(a);
   }
 }
 
@@ -153,18 +153,22 @@ void launch_attention_simt(const AttnArgs& a, cudaStream_t st) {
   }
 }
 
+bool use_mma(int dtype, int D, int rep) { return dtype == PIC_BF16 && D == 128 && (rep == 1 || rep == 2 || rep == 4 || rep == 8); }
+
+int attention_rows_per_block(int dtype, int D, int rep) { return (use_mma(dtype, D, rep) && rep <= 4) ? 32 : 16; }
+
 void launch_attention(const AttnArgs& a, cudaStream_t st) {
-  if (a.dtype == PIC_BF16 && a.D == 128)
+  if (use_mma(a.dtype, a.D, a.H / a.G))
     launch_attention_mma(a, st);
   else
     launch_attention_simt(a, st);
 }
 
 size_t attention_part_bytes(int n_parts, int rep, int D) {
-  return (size_t)n_parts * kBlock * rep * (D + 2) * sizeof(float);
+  return (size_t)n_parts * kAttnPartRows * rep * (D + 2) * sizeof(float);
 }
 
-// Blocks of <= 16 consecutive rows of one sequence; each block reads the prefix of the
+// Blocks of <= rows_per_block consecutive rows of one sequence; each block reads the prefix of the
 // sequence's pages up to its last row's position, cut into runs of P pages. P grows
 // until the work is ~4 items per SM, never finer than 4 pages.
 void plan_attention(const AttnPlanInput& in, std::vector<AttnItem>& items, std::vector<AttnCombine>& combines,
@@ -175,8 +179,9 @@ void plan_attention(const AttnPlanInput& in, std::vector<AttnItem>& items, std::
   const std::vector<int>& rp = *in.row_pos;
   const std::vector<int>& pp = *in.page_pos;
   for (size_t s = 0; s < in.seq_row_begin.size(); ++s) {
-    for (int r0 = in.seq_row_begin[s]; r0 < in.seq_row_end[s]; r0 += kBlock) {
-      const int n = std::min(kBlock, in.seq_row_end[s] - r0);
+    const int rb = in.rows_per_block > 0 ? in.rows_per_block : kBlock;
+    for (int r0 = in.seq_row_begin[s]; r0 < in.seq_row_end[s]; r0 += rb) {
+      const int n = std::min(rb, in.seq_row_end[s] - r0);
       const int maxp = rp[r0 + n - 1];
       int pe = in.seq_page_begin[s];
       while (pe < in.seq_page_end[s] && pp[pe] <= maxp) ++pe;

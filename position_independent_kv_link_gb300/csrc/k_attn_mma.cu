@@ -1,21 +1,23 @@
 // Tensor-core paged attention for bf16 models with head_dim 128 (mma.sync m16n8k16).
 //
-// One CTA = one work item: up to 16 consecutive query rows of one sequence x the
-// REP query heads that share KV head g (GQA) x a run of pages. Warp w owns query head
-// g*REP + w for the 16 rows (an MMA M tile). KV moves through shared memory in tiles
-// of 64 keys (4 pages), double buffered:
-//   * K: 16-byte global loads into registers, rotated by RoPE at each key's absolute
-//     position while being stored to shared memory (MEPIC abstract: K is kept without
-//     positional encoding and RoPE is fused into attention). For a key at row r of a
-//     page starting at position P, cos/sin((P + r) theta) is composed from the table row
-//     of P (one per page, staged by cp.async) and the row of r (resident), so a tile
-//     reads 4 table rows instead of 64 and the rotation touches only shared memory.
-//   * V: cp.async straight into shared memory.
+// One CTA = one work item: up to 16*RG consecutive query rows of one sequence x the REP
+// query heads that share KV head g (GQA) x a run of pages. Warp w owns query head
+// g*REP + (w % REP) for the 16 rows of row group w / REP (one MMA M tile), so every K/V
+// tile staged in shared memory feeds RG*REP warps. KV moves in tiles of 64 keys (4 pages):
+//   * K: cp.async into a raw buffer one tile ahead, then rotated by RoPE at each key's
+//     absolute position, shared -> shared, into the double-buffered operand tile (MEPIC
+//     abstract: K is kept without positional encoding and RoPE is fused into attention).
+//     For a key at row r of a page that starts at position P, cos/sin((P + r) theta) is
+//     composed from the table row of P (one per page, staged by cp.async) and the row of
+//     r (resident), so a tile reads 4 table rows instead of 64.
+//   * V: cp.async straight into the double-buffered operand tile.
+//   * page metadata (block, start, length) is cached in shared memory in windows of 512
+//     pages, so no global load sits in front of the KV loads.
 // S = Q K^T and O += P V run on mma.sync with fp32 accumulators; the online softmax
 // lives in registers (row max/sum by quad shuffles). Keys after the query's position,
-// padding rows of ragged pages and pages past the item's range are masked.
-// Items covering part of a row block's pages write unnormalized partials (o, m, l) that
-// the merge kernel of k_attn.cu combines.
+// padding rows of ragged pages and pages past the item's range are masked. Items that
+// cover part of a row block's pages write unnormalized partials (o, m, l) that the merge
+// kernel of k_attn.cu combines.
 #include <climits>
 
 #include "pic_internal.h"
@@ -29,6 +31,7 @@ namespace {
 constexpr int D = 128;
 constexpr int KT = 64;                    // keys per tile
 constexpr int TILE_BYTES = KT * D * 2;    // 16 KB
+constexpr int WIN = 512;                  // pages of metadata cached at once
 constexpr float kLog2e = 1.4426950408889634f;
 
 // byte offset of 16-byte chunk `c` (0..15) of row `r` in a [rows][128] bf16 tile, XOR-swizzled
@@ -60,26 +63,41 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
-template <int NW>
-struct KTask {  // per-thread register prefetch of K chunks for one tile
-  static constexpr int N = KT * 8 / (NW * 32);  // (key, chunk-pair) tasks per thread
-  uint4 lo[N], hi[N];
-  int pos[N];
-};
+// rotate 8 dims (i) and their partners (i + 64) by the composed angle, times `scale`
+__device__ __forceinline__ void rope8(const uint4& x1, const uint4& x2, const float2* hi, const float2* lo,
+                                      float scale, uint4& y1, uint4& y2) {
+  const __nv_bfloat16* b1 = reinterpret_cast<const __nv_bfloat16*>(&x1);
+  const __nv_bfloat16* b2 = reinterpret_cast<const __nv_bfloat16*>(&x2);
+  __nv_bfloat16 o1[8], o2[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const float2 H2 = hi[e], L2 = lo[e];
+    const float cs = H2.x * L2.x - H2.y * L2.y, sn = H2.y * L2.x + H2.x * L2.y;
+    const float v1 = __bfloat162float(b1[e]), v2 = __bfloat162float(b2[e]);
+    o1[e] = __float2bfloat16_rn((v1 * cs - v2 * sn) * scale);
+    o2[e] = __float2bfloat16_rn((v2 * cs + v1 * sn) * scale);
+  }
+  y1 = *reinterpret_cast<uint4*>(o1);
+  y2 = *reinterpret_cast<uint4*>(o2);
+}
 
-template <int REP, int NW>
-__global__ void __launch_bounds__(NW * 32) attn_mma_kernel(AttnArgs a) {
+template <int REP, int RG>
+__global__ void __launch_bounds__(REP * RG * 32) attn_mma_kernel(AttnArgs a) {
+  constexpr int NW = REP * RG, NT = NW * 32;
   extern __shared__ __align__(128) uint8_t smem[];
-  uint8_t* sK = smem;                                  // [2][KT][D] bf16, swizzled
-  uint8_t* sV = smem + 2 * TILE_BYTES;                 // [2][KT][D]
-  uint8_t* sQ = smem + 4 * TILE_BYTES;                 // [REP][16][D]
-  float2* sLo = reinterpret_cast<float2*>(sQ + REP * 16 * D * 2);   // [16][64] cos/sin of p = 0..15
-  float2* sPg = sLo + 16 * 64;                                      // [2][4][64] cos/sin of each page start
-  int* sPos = reinterpret_cast<int*>(sPg + 2 * 4 * 64);             // [2][KT] key positions (INT_MAX = masked)
-  const uint32_t sPg_u = (uint32_t)__cvta_generic_to_shared(sPg);
+  uint8_t* sK = smem;                                   // [2][KT][D] rotated K (Q staging at start)
+  uint8_t* sKr = sK + 2 * TILE_BYTES;                   // [KT][D] raw K of the next tile
+  uint8_t* sV = sKr + TILE_BYTES;                       // [2][KT][D]
+  float2* sLo = reinterpret_cast<float2*>(sV + 2 * TILE_BYTES);   // [16][64] cos/sin of p = 0..15
+  float2* sPg = sLo + 16 * 64;                                     // [2][4][64] cos/sin of page starts
+  int* sBlk = reinterpret_cast<int*>(sPg + 2 * 4 * 64);            // [WIN] page metadata window
+  int* sPp = sBlk + WIN;
+  int* sPl = sPp + WIN;
+  int* sPos = sPl + WIN;                                           // [2][KT] key positions (INT_MAX = masked)
   const uint32_t sK_u = (uint32_t)__cvta_generic_to_shared(sK);
+  const uint32_t sKr_u = (uint32_t)__cvta_generic_to_shared(sKr);
   const uint32_t sV_u = (uint32_t)__cvta_generic_to_shared(sV);
-  const uint32_t sQ_u = (uint32_t)__cvta_generic_to_shared(sQ);
+  const uint32_t sPg_u = (uint32_t)__cvta_generic_to_shared(sPg);
 
   const AttnItem it = a.items[blockIdx.x];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -87,136 +105,104 @@ __global__ void __launch_bounds__(NW * 32) attn_mma_kernel(AttnArgs a) {
   const __nv_bfloat16* Kl = (const __nv_bfloat16*)a.k_layer;
   const __nv_bfloat16* Vl = (const __nv_bfloat16*)a.v_layer;
   const __nv_bfloat16* Q = (const __nv_bfloat16*)a.q;
+  const int npages = it.page1 - it.page0;
+  const int ntiles = (npages + 3) / 4;
+
+  auto load_meta = [&](int win0) {
+    for (int i = tid; i < WIN; i += NT) {
+      const int pg = it.page0 + win0 + i;
+      if (pg < it.page1) {
+        sBlk[i] = a.page_block[pg];
+        sPp[i] = a.page_pos[pg];
+        sPl[i] = a.page_len[pg];
+      }
+    }
+  };
+  for (int i = tid; i < 16 * 64; i += NT) sLo[i] = a.rope_cs[i];
+  int win = 0;
+  load_meta(0);
+  __syncthreads();
+
+  // ---- Q: rotate at each row's position, scale into log2 units, stage for ldmatrix
   const float qscale = rsqrtf((float)D) * kLog2e;
-
-  for (int i = tid; i < 16 * 64; i += NW * 32) sLo[i] = a.rope_cs[i];
-  __syncthreads();
-
-  // ---- Q: rotate at each row's position, scale, round to bf16, stage for ldmatrix
-  for (int i = tid; i < REP * 16 * 8; i += NW * 32) {
-    const int hh = i / 128, r = (i / 8) % 16, c = i % 8;   // dims 8c..8c+7 and 64+8c..
-    uint4 x1 = make_uint4(0, 0, 0, 0), x2 = x1;
+  for (int i = tid; i < NW * 16 * 8; i += NT) {
+    const int w = i / 128, r16 = (i / 8) % 16, c = i % 8;
+    const int r = (w / REP) * 16 + r16, qh = w % REP;
+    uint4 y1 = make_uint4(0, 0, 0, 0), y2 = y1;
     if (r < it.nrows) {
-      const int t = it.row0 + r, h = it.g * REP + hh, p = a.q_pos[t];
+      const int t = it.row0 + r, h = it.g * REP + qh, p = a.q_pos[t];
       const __nv_bfloat16* src = Q + ((size_t)t * a.H + h) * D;
-      const uint4 u1 = *reinterpret_cast<const uint4*>(src + 8 * c);
-      const uint4 u2 = *reinterpret_cast<const uint4*>(src + 64 + 8 * c);
-      const float2* hi = a.rope_cs + (size_t)(p & ~15) * 64 + 8 * c;
-      const float2* lo = sLo + (p & 15) * 64 + 8 * c;
-      const __nv_bfloat16* b1 = reinterpret_cast<const __nv_bfloat16*>(&u1);
-      const __nv_bfloat16* b2 = reinterpret_cast<const __nv_bfloat16*>(&u2);
-      __nv_bfloat16 o1[8], o2[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const float2 H2 = hi[e], L2 = lo[e];
-        const float cs = H2.x * L2.x - H2.y * L2.y, sn = H2.y * L2.x + H2.x * L2.y;
-        const float v1 = __bfloat162float(b1[e]), v2 = __bfloat162float(b2[e]);
-        o1[e] = __float2bfloat16_rn((v1 * cs - v2 * sn) * qscale);
-        o2[e] = __float2bfloat16_rn((v2 * cs + v1 * sn) * qscale);
-      }
-      x1 = *reinterpret_cast<uint4*>(o1);
-      x2 = *reinterpret_cast<uint4*>(o2);
+      rope8(*reinterpret_cast<const uint4*>(src + 8 * c), *reinterpret_cast<const uint4*>(src + 64 + 8 * c),
+            a.rope_cs + (size_t)(p & ~15) * 64 + 8 * c, sLo + (p & 15) * 64 + 8 * c, qscale, y1, y2);
     }
-    uint8_t* base = sQ + hh * 16 * D * 2;
-    *reinterpret_cast<uint4*>(base + swz(r, c)) = x1;
-    *reinterpret_cast<uint4*>(base + swz(r, c + 8)) = x2;
+    uint8_t* base = sK + w * 16 * D * 2;
+    *reinterpret_cast<uint4*>(base + swz(r16, c)) = y1;
+    *reinterpret_cast<uint4*>(base + swz(r16, c + 8)) = y2;
   }
-
-  const int ntiles = (it.page1 - it.page0 + 3) / 4;
-  KTask<NW> kt;
-
-  auto load_k = [&](int tile) {
-#pragma unroll
-    for (int j = 0; j < KTask<NW>::N; ++j) {
-      const int task = tid + j * NW * 32;
-      const int key = task / 8, c = task % 8;
-      const int page = it.page0 + tile * 4 + key / 16, r = key % 16;
-      kt.pos[j] = INT_MAX;
-      if (page < it.page1 && r < a.page_len[page]) {
-        const int blk = a.page_block[page];
-        const __nv_bfloat16* src = Kl + (((size_t)blk * G + it.g) * kBlock + r) * D;
-        kt.lo[j] = *reinterpret_cast<const uint4*>(src + 8 * c);
-        kt.hi[j] = *reinterpret_cast<const uint4*>(src + 64 + 8 * c);
-        kt.pos[j] = a.page_pos[page] + r;
-      }
-    }
-  };
-  auto store_k = [&](int buf) {
-#pragma unroll
-    for (int j = 0; j < KTask<NW>::N; ++j) {
-      const int task = tid + j * NW * 32;
-      const int key = task / 8, c = task % 8;
-      uint4 y1 = make_uint4(0, 0, 0, 0), y2 = y1;
-      const int p = kt.pos[j];
-      if (p != INT_MAX) {
-        const float2* hi = sPg + (buf * 4 + key / 16) * 64 + 8 * c;   // page start position
-        const float2* lo = sLo + (key % 16) * 64 + 8 * c;             // row within the page
-        const __nv_bfloat16* b1 = reinterpret_cast<const __nv_bfloat16*>(&kt.lo[j]);
-        const __nv_bfloat16* b2 = reinterpret_cast<const __nv_bfloat16*>(&kt.hi[j]);
-        __nv_bfloat16 o1[8], o2[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float2 H2 = hi[e], L2 = lo[e];
-          const float cs = H2.x * L2.x - H2.y * L2.y, sn = H2.y * L2.x + H2.x * L2.y;
-          const float v1 = __bfloat162float(b1[e]), v2 = __bfloat162float(b2[e]);
-          o1[e] = __float2bfloat16_rn(v1 * cs - v2 * sn);
-          o2[e] = __float2bfloat16_rn(v2 * cs + v1 * sn);
-        }
-        y1 = *reinterpret_cast<uint4*>(o1);
-        y2 = *reinterpret_cast<uint4*>(o2);
-      }
-      uint8_t* base = sK + buf * TILE_BYTES;
-      *reinterpret_cast<uint4*>(base + swz(key, c)) = y1;
-      *reinterpret_cast<uint4*>(base + swz(key, c + 8)) = y2;
-      if (c == 0) sPos[buf * KT + key] = p;
-    }
-  };
-  auto load_v = [&](int tile, int buf) {
-    // RoPE rows of the tile's page starts: 4 pages x 512 B
-    if (tid < 4 * 32) {
-      const int pg = tid / 32, c = tid % 32;
-      const int page = it.page0 + tile * 4 + pg;
-      if (page < it.page1)
-        cp_async16(sPg_u + (uint32_t)((buf * 4 + pg) * 64 * sizeof(float2) + c * 16),
-                   a.rope_cs + (size_t)a.page_pos[page] * 64 + c * 2);
-    }
-    for (int task = tid; task < KT * 16; task += NW * 32) {
-      const int key = task / 16, c = task % 16;
-      const int page = it.page0 + tile * 4 + key / 16, r = key % 16;
-      const uint32_t dst = sV_u + buf * TILE_BYTES + swz(key, c);
-      if (page < it.page1 && r < a.page_len[page]) {
-        const int blk = a.page_block[page];
-        cp_async16(dst, Vl + (((size_t)blk * G + it.g) * kBlock + r) * D + 8 * c);
-      } else {
-        *reinterpret_cast<uint4*>(sV + buf * TILE_BYTES + swz(key, c)) = make_uint4(0, 0, 0, 0);
-      }
-    }
-  };
-
-  // prologue: tile 0
-  if (ntiles > 0) {
-    load_v(0, 0);
-    load_k(0);
-  }
-  cp_async_wait_all();
   __syncthreads();
-  if (ntiles > 0) store_k(0);
-  __syncthreads();
-
-  // ---- per-warp state
-  const bool active = warp < REP;
+  const int rg = warp / REP, hh = warp % REP;
+  const bool active = rg * 16 < it.nrows;
   const int g8 = lane >> 2, t4 = lane & 3;
-  const int qp0 = (g8 < it.nrows) ? a.q_pos[it.row0 + g8] : -1;
-  const int qp1 = (g8 + 8 < it.nrows) ? a.q_pos[it.row0 + g8 + 8] : -1;
+  const int row0 = rg * 16 + g8, row1 = row0 + 8;
+  const int qp0 = row0 < it.nrows ? a.q_pos[it.row0 + row0] : -1;
+  const int qp1 = row1 < it.nrows ? a.q_pos[it.row0 + row1] : -1;
   uint32_t qf[8][4];
-  if (active) {
-    const uint32_t qb = sQ_u + warp * 16 * D * 2;
+  {
+    const uint32_t qb = sK_u + warp * 16 * D * 2;
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks) {
       const int m = lane >> 3, row = (lane & 7) + 8 * (m & 1), c = 2 * ks + (m >> 1);
       ldsm_x4(qb + swz(row, c), qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3]);
     }
   }
+  __syncthreads();  // the Q staging area becomes the K operand buffers
+
+  // ---- tile loaders (page metadata relative to the current window)
+  auto issue_loads = [&](int tile, int buf) {
+    const int pbase = tile * 4 - win;  // window index of the tile's first page
+    for (int task = tid; task < KT * 16; task += NT) {
+      const int key = task / 16, c = task % 16;
+      const int pi = pbase + key / 16, r = key % 16;
+      const bool valid = tile * 4 + key / 16 < npages && r < sPl[pi];
+      const uint32_t off = swz(key, c);
+      if (valid) {
+        const size_t src = (((size_t)sBlk[pi] * G + it.g) * kBlock + r) * D + 8 * c;
+        cp_async16(sKr_u + off, Kl + src);
+        cp_async16(sV_u + buf * TILE_BYTES + off, Vl + src);
+      } else {
+        *reinterpret_cast<uint4*>(sV + buf * TILE_BYTES + off) = make_uint4(0, 0, 0, 0);
+      }
+    }
+    for (int i = tid; i < 4 * 32; i += NT) {   // 4 page-start RoPE rows of 512 B
+      const int pg = i / 32, c = i % 32;
+      if (tile * 4 + pg < npages)
+        cp_async16(sPg_u + (uint32_t)((buf * 4 + pg) * 64 * sizeof(float2) + c * 16),
+                   a.rope_cs + (size_t)sPp[pbase + pg] * 64 + c * 2);
+    }
+  };
+  auto rotate_k = [&](int tile, int buf) {
+    const int pbase = tile * 4 - win;
+    for (int task = tid; task < KT * 8; task += NT) {
+      const int key = task / 8, c = task % 8;
+      const int pi = pbase + key / 16, r = key % 16;
+      const bool valid = tile * 4 + key / 16 < npages && r < sPl[pi];
+      uint4 y1 = make_uint4(0, 0, 0, 0), y2 = y1;
+      if (valid)
+        rope8(*reinterpret_cast<const uint4*>(sKr + swz(key, c)), *reinterpret_cast<const uint4*>(sKr + swz(key, c + 8)),
+              sPg + (buf * 4 + key / 16) * 64 + 8 * c, sLo + r * 64 + 8 * c, 1.f, y1, y2);
+      uint8_t* base = sK + buf * TILE_BYTES;
+      *reinterpret_cast<uint4*>(base + swz(key, c)) = y1;
+      *reinterpret_cast<uint4*>(base + swz(key, c + 8)) = y2;
+      if (c == 0) sPos[buf * KT + key] = valid ? sPp[pi] + r : INT_MAX;
+    }
+  };
+
+  if (ntiles > 0) issue_loads(0, 0);
+  cp_async_wait_all();
+  __syncthreads();
+  if (ntiles > 0) rotate_k(0, 0);
+  __syncthreads();
+
   float o[16][4];
 #pragma unroll
   for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
@@ -226,8 +212,14 @@ __global__ void __launch_bounds__(NW * 32) attn_mma_kernel(AttnArgs a) {
     const int cur = tile & 1, nxt = cur ^ 1;
     const bool has_next = tile + 1 < ntiles;
     if (has_next) {
-      load_v(tile + 1, nxt);
-      load_k(tile + 1);
+      const int w1 = ((tile + 1) * 4 / WIN) * WIN;
+      if (w1 != win) {  // the next tile starts a new metadata window (same for every thread)
+        __syncthreads();
+        win = w1;
+        load_meta(win);
+        __syncthreads();
+      }
+      issue_loads(tile + 1, nxt);
     }
     if (active) {
       // S = Q K^T over 64 keys
@@ -246,7 +238,7 @@ __global__ void __launch_bounds__(NW * 32) attn_mma_kernel(AttnArgs a) {
           mma16816(s[j + 1], qf[ks], b2, b3);
         }
       }
-      // mask + online softmax (rows g8 and g8+8; this thread holds keys 8j+2t4, +1)
+      // mask + online softmax (rows row0 and row1; this thread holds keys 8j+2t4, +1)
       const int* kp = sPos + cur * KT;
       float tm0 = -INFINITY, tm1 = -INFINITY;
 #pragma unroll
@@ -293,7 +285,7 @@ __global__ void __launch_bounds__(NW * 32) attn_mma_kernel(AttnArgs a) {
       const uint32_t vb = sV_u + cur * TILE_BYTES;
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
-        // A fragment of P for keys 16kk..16kk+15: {row g8 k0-7, row g8+8 k0-7, row g8 k8-15, row g8+8 k8-15}
+        // A fragment of P for keys 16kk..16kk+15: {row0 k0-7, row1 k0-7, row0 k8-15, row1 k8-15}
         const uint32_t af[4] = {pf[kk][0], pf[kk][1], pf[kk][2], pf[kk][3]};
 #pragma unroll
         for (int dn = 0; dn < 16; dn += 2) {
@@ -305,9 +297,9 @@ __global__ void __launch_bounds__(NW * 32) attn_mma_kernel(AttnArgs a) {
         }
       }
     }
-    cp_async_wait_all();   // V and page RoPE rows of the next tile have landed
+    cp_async_wait_all();   // raw K, V and page RoPE rows of the next tile have landed
     __syncthreads();
-    if (has_next) store_k(nxt);
+    if (has_next) rotate_k(tile + 1, nxt);
     __syncthreads();
   }
 
@@ -316,23 +308,23 @@ __global__ void __launch_bounds__(NW * 32) attn_mma_kernel(AttnArgs a) {
   l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
   l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
   l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-  const int hh = warp, h = it.g * REP + hh;
+  const int h = it.g * REP + hh;
   if (it.part < 0) {
     __nv_bfloat16* out = (__nv_bfloat16*)a.out;
     const float i0 = l0 > 0.f ? 1.f / l0 : 0.f, i1 = l1 > 0.f ? 1.f / l1 : 0.f;
 #pragma unroll
     for (int dn = 0; dn < 16; ++dn) {
       const int dcol = 8 * dn + 2 * t4;
-      if (g8 < it.nrows)
-        *reinterpret_cast<uint32_t*>(out + ((size_t)(it.row0 + g8) * a.H + h) * D + dcol) =
+      if (row0 < it.nrows)
+        *reinterpret_cast<uint32_t*>(out + ((size_t)(it.row0 + row0) * a.H + h) * D + dcol) =
             pack_bf16(o[dn][0] * i0, o[dn][1] * i0);
-      if (g8 + 8 < it.nrows)
-        *reinterpret_cast<uint32_t*>(out + ((size_t)(it.row0 + g8 + 8) * a.H + h) * D + dcol) =
+      if (row1 < it.nrows)
+        *reinterpret_cast<uint32_t*>(out + ((size_t)(it.row0 + row1) * a.H + h) * D + dcol) =
             pack_bf16(o[dn][2] * i1, o[dn][3] * i1);
     }
   } else {
-    const size_t p0 = ((size_t)it.part * kBlock + g8) * REP + hh;
-    const size_t p1 = ((size_t)it.part * kBlock + g8 + 8) * REP + hh;
+    const size_t p0 = ((size_t)it.part * kAttnPartRows + row0) * REP + hh;
+    const size_t p1 = ((size_t)it.part * kAttnPartRows + row1) * REP + hh;
 #pragma unroll
     for (int dn = 0; dn < 16; ++dn) {
       const int dcol = 8 * dn + 2 * t4;
@@ -348,18 +340,19 @@ __global__ void __launch_bounds__(NW * 32) attn_mma_kernel(AttnArgs a) {
   }
 }
 
-template <int REP, int NW>
+template <int REP, int RG>
 void launch_rep(const AttnArgs& a, cudaStream_t st) {
-  const size_t smem =
-      4 * TILE_BYTES + REP * 16 * D * 2 + (16 + 2 * 4) * 64 * sizeof(float2) + 2 * KT * sizeof(int);
+  constexpr int NW = REP * RG;
+  static_assert(NW * 16 * D * 2 <= 2 * TILE_BYTES, "Q staging must fit the K operand buffers");
+  const size_t smem = 5 * TILE_BYTES + (16 + 2 * 4) * 64 * sizeof(float2) + (3 * WIN + 2 * KT) * sizeof(int);
   static bool attr[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64 || !attr[dev]) {
-    cudaFuncSetAttribute(attn_mma_kernel<REP, NW>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaFuncSetAttribute(attn_mma_kernel<REP, RG>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (dev >= 0 && dev < 64) attr[dev] = true;
   }
-  attn_mma_kernel<REP, NW><<<a.n_items, NW * 32, smem, st>>>(a);
+  attn_mma_kernel<REP, RG><<<a.n_items, NW * 32, smem, st>>>(a);
 }
 
 }  // namespace
@@ -367,11 +360,11 @@ void launch_rep(const AttnArgs& a, cudaStream_t st) {
 void launch_attention_mma(const AttnArgs& a, cudaStream_t st) {
   const int rep = a.H / a.G;
   if (a.n_items > 0) {
-    switch (rep) {
-      case 1: launch_rep<1, 4>(a, st); break;
-      case 2: launch_rep<2, 4>(a, st); break;
-      case 4: launch_rep<4, 4>(a, st); break;
-      case 8: launch_rep<8, 8>(a, st); break;
+    switch (rep) {   // rows per item: 32 (two row groups) for rep <= 4, 16 for rep 8
+      case 1: launch_rep<1, 2>(a, st); break;
+      case 2: launch_rep<2, 2>(a, st); break;
+      case 4: launch_rep<4, 2>(a, st); break;
+      case 8: launch_rep<8, 1>(a, st); break;
       default: launch_attention_simt(a, st); return;
     }
   }

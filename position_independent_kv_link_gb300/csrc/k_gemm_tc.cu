@@ -438,7 +438,10 @@ pic_status tc_gemm_run(const void* W, const void* X, float* Y, int N, int K, int
   // shared memory: the weight ring gets what the activation ring, the two epilogue tiles
   // and the barriers leave of the opt-in limit
   const int budget = 227 * 1024 - 1024 - 2 * EPI_BYTES - 512;
-  p.SB = b_stage <= 8192 ? 4 : (b_stage <= 16384 ? 3 : 2);
+  // ~96 KB of activation stages hide the L2 latency of the next activation tile (one
+  // tile is consumed every k-block); the weight ring keeps the rest for HBM latency.
+  p.SB = std::max(2, std::min(8, (96 * 1024 + b_stage - 1) / b_stage));
+  while (p.SB > 2 && (budget - p.SB * b_stage) / A_STAGE < 5) --p.SB;
   p.SA = std::min(12, (budget - p.SB * b_stage) / A_STAGE);
   if (p.SA < 2) return fail(PIC_ERR_UNSUPPORTED, "tcgen05 gemm: pipeline does not fit shared memory");
   p.tmem_cols = 32;

@@ -87,6 +87,7 @@ pic_status pic_op_attention_noalloc(int32_t dtype, int32_t T, int32_t n_heads, i
   in.row_pos = &row_pos;
   in.page_pos = &ppos;
   in.G = n_kv_heads;
+  in.rows_per_block = attention_rows_per_block(dtype, head_dim, n_heads / n_kv_heads);
   in.num_sms = device_sms();
   std::vector<AttnItem> items;
   std::vector<AttnCombine> combs;
@@ -97,8 +98,8 @@ pic_status pic_op_attention_noalloc(int32_t dtype, int32_t T, int32_t n_heads, i
   const int rep = n_heads / n_kv_heads;
   const size_t n_ints = (size_t)T + 3 * (size_t)n_pages + 6 * items.size() + 5 * combs.size();
   const size_t o_part = align256(n_ints * 4);
-  const size_t o_ml = o_part + align256((size_t)n_parts * kBlock * rep * head_dim * 4);
-  const size_t need = o_ml + align256((size_t)n_parts * kBlock * rep * 2 * 4);
+  const size_t o_ml = o_part + align256((size_t)n_parts * kAttnPartRows * rep * head_dim * 4);
+  const size_t need = o_ml + align256((size_t)n_parts * kAttnPartRows * rep * 2 * 4);
   if (need > kNoAllocScratchBytes)
     return fail(PIC_ERR_CAPACITY, "attention needs " + std::to_string(need) + " bytes of scratch; the fixed area holds " +
                                       std::to_string(kNoAllocScratchBytes) + " (use pic_op_attention with a caller buffer)");
@@ -126,6 +127,7 @@ pic_status pic_op_attention_noalloc(int32_t dtype, int32_t T, int32_t n_heads, i
   PIC_CUDA(cudaMemcpyAsync(di, ints.data(), ints.size() * 4, cudaMemcpyHostToDevice, st));
   AttnArgs a{};
   a.dtype = dtype;
+  a.rb = in.rows_per_block;
   a.H = n_heads;
   a.G = n_kv_heads;
   a.D = head_dim;

@@ -32,8 +32,8 @@ AttnScratchLayout attn_layout(int T, int n_heads, int n_kv_heads, int head_dim, 
   L.ints_bytes = align256(ints * 4);
   const int rep = std::max(1, n_heads / std::max(1, n_kv_heads));
   L.part_o_off = L.ints_bytes;
-  L.part_ml_off = L.part_o_off + align256((size_t)L.max_parts * kBlock * rep * head_dim * 4);
-  L.total = L.part_ml_off + align256((size_t)L.max_parts * kBlock * rep * 2 * 4);
+  L.part_ml_off = L.part_o_off + align256((size_t)L.max_parts * kAttnPartRows * rep * head_dim * 4);
+  L.total = L.part_ml_off + align256((size_t)L.max_parts * kAttnPartRows * rep * 2 * 4);
   return L;
 }
 
@@ -94,6 +94,7 @@ pic_status pic_op_attention(int32_t dtype, int32_t T, int32_t n_heads, int32_t n
   in.row_pos = &row_pos;
   in.page_pos = &ppos;
   in.G = n_kv_heads;
+  in.rows_per_block = attention_rows_per_block(dtype, head_dim, n_heads / n_kv_heads);
   in.num_sms = current_sms();
   std::vector<AttnItem> items;
   std::vector<AttnCombine> combs;
@@ -117,6 +118,7 @@ pic_status pic_op_attention(int32_t dtype, int32_t T, int32_t n_heads, int32_t n
   PIC_CUDA(cudaMemcpyAsync(di, ints.data(), ints.size() * 4, cudaMemcpyHostToDevice, st));
   AttnArgs a{};
   a.dtype = dtype;
+  a.rb = in.rows_per_block;
   a.H = n_heads;
   a.G = n_kv_heads;
   a.D = head_dim;

@@ -69,7 +69,9 @@ pic_status tc_gemm_run(const void* W, const void* X, float* Y, int N, int K, int
 pic_status tc_check_timeout();
 
 // ------------------------------------------------------------------ attention (k_attn.cu)
-struct AttnItem {      // one CTA's work: <=16 consecutive rows of one sequence x one KV head x a page range
+constexpr int kAttnPartRows = 32;          // row slots of one split-partial slab
+
+struct AttnItem {      // one CTA's work: <= rb consecutive rows of one sequence x one KV head x a page range
   int row0, nrows, g, page0, page1, part;  // part < 0: write normalized output directly
 };
 struct AttnCombine {   // merge `nparts` partial results of rows [row0, row0+nrows) for KV head g
@@ -77,6 +79,7 @@ struct AttnCombine {   // merge `nparts` partial results of rows [row0, row0+nro
 };
 struct AttnArgs {
   int dtype, H, G, D;
+  int rb;                   // rows per work item of this plan (16 or 32)
   const void* q;            // [T][H][D] pre-RoPE
   const int* q_pos;         // [T]
   const void* k_layer;      // [nb][G][16][D]
@@ -86,8 +89,8 @@ struct AttnArgs {
   const int* page_len;
   const float2* rope_cs;    // [max_pos][D/2]
   void* out;                // [T][H][D]
-  float* part_o;            // [parts][16][rep][D]
-  float* part_ml;           // [parts][16][rep][2]
+  float* part_o;            // [parts][kAttnPartRows][rep][D]
+  float* part_ml;           // [parts][kAttnPartRows][rep][2]
   const AttnItem* items;
   int n_items;
   const AttnCombine* combines;
@@ -103,7 +106,10 @@ struct AttnPlanInput {
   const std::vector<int>* page_pos;
   int G;
   int num_sms;
+  int rows_per_block;       // from attention_rows_per_block()
 };
+// Rows per work item the attention kernels take for this model shape (16 or 32).
+int attention_rows_per_block(int dtype, int D, int rep);
 void plan_attention(const AttnPlanInput& in, std::vector<AttnItem>& items, std::vector<AttnCombine>& combines,
                     int& n_parts);
 size_t attention_part_bytes(int n_parts, int rep, int D);
