@@ -403,11 +403,16 @@ def run_kernel(args):
     sp = C.c_void_p(st.cuda_stream)
     g = torch.Generator(device="cuda").manual_seed(0)
     if args.kernel == "gemm":
-        N, K, T = 28672, 4096, 224
+        N, K, T = (int(x) for x in args.shape.split(",")) if args.shape else (28672, 4096, 224)
         W = (torch.randn(N, K, device="cuda", generator=g) * 0.02).to(torch.bfloat16)
         X = torch.randn(T, K, device="cuda", generator=g).to(torch.bfloat16)
         Y = torch.empty(T, N, device="cuda")
-        call = lambda: L.check(lib.pic_op_gemm(L.PIC_BF16, W.data_ptr(), X.data_ptr(), Y.data_ptr(), N, K, T, sp))
+        if args.unpacked:
+            call = lambda: L.check(lib.pic_op_gemm(L.PIC_BF16, W.data_ptr(), X.data_ptr(), Y.data_ptr(), N, K, T, sp))
+        else:   # the tile layout the model repacks its matrices into
+            Wp = api.pack_weight(W)
+            del W
+            call = lambda: L.check(lib.pic_op_gemm_packed(Wp.data_ptr(), X.data_ptr(), Y.data_ptr(), N, K, T, sp))
         nbytes, flops = N * K * 2 + T * K * 2 + T * N * 4, 2.0 * N * K * T
     else:
         lens, qlen, k = [512] * 10, 64, 16
@@ -446,7 +451,7 @@ def run_kernel(args):
     e1.record(st)
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / args.steps
-    print(json.dumps({"kernel": args.kernel, "ms": ms, "GBs": nbytes / ms / 1e6, "TFs": flops / ms / 1e9,
+    print(json.dumps({"kernel": args.kernel, "shape": args.shape, "ms": ms, "GBs": nbytes / ms / 1e6, "TFs": flops / ms / 1e9,
                       "steps": args.steps}), flush=True)
     return 0
 
@@ -462,6 +467,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--kernel", choices=["gemm", "attention"], default=None,
                     help="time one kernel-level call at its 8B link shape instead of the link step")
+    ap.add_argument("--shape", default=None, help="gemm N,K,T for --kernel gemm (default 28672,4096,224)")
+    ap.add_argument("--unpacked", action="store_true", help="--kernel gemm on the plain [N][K] layout")
     args = ap.parse_args()
     if args.kernel:
         return run_kernel(args)

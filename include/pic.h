@@ -134,7 +134,9 @@ const char* pic_version(void);
 
 /* Creates a model on the current CUDA device. Validates the config (head_dim 64/128,
  * n_heads % n_kv_heads == 0, d_model % 64 == 0, dims multiples of 8) and, for bf16,
- * prepares TMA descriptors over the weights. */
+ * repacks the bf16 projection matrices into a library-owned tensor-core tile copy
+ * (pic_op_pack_weight layout; the originals stay borrowed and are still read for the
+ * embedding gather). */
 pic_status pic_model_create(const pic_model_config* cfg, const pic_weights* w, pic_model** out);
 pic_status pic_model_destroy(pic_model* m);
 
@@ -222,6 +224,16 @@ int64_t pic_store_launch_count(const pic_store* s);
  * other shapes on the SIMT kernel. Needs no scratch. */
 pic_status pic_op_gemm(int32_t dtype, const void* W, const void* X, float* Y, int32_t N, int32_t K, int32_t T,
                        pic_stream_t stream);
+
+/* Repacks a bf16 [N][K] matrix (N % 128 == 0, K % 64 == 0) into N*K*2 bytes of 16 KB
+ * tiles of 128 rows x 64 columns, tile (n/128, k/64) at byte ((n/128)*(K/64) + k/64)*16384,
+ * each stored as the 128-byte-swizzled K-major image the tensor cores read from shared
+ * memory. pic_model_create does this for every bf16 projection matrix (one library-owned
+ * copy) so each weight tile streams from HBM as one sequential bulk copy. */
+pic_status pic_op_pack_weight(const void* W, void* out, int32_t N, int32_t K, pic_stream_t stream);
+/* pic_op_gemm (bf16) with W given in the pic_op_pack_weight layout. */
+pic_status pic_op_gemm_packed(const void* W_packed, const void* X, float* Y, int32_t N, int32_t K, int32_t T,
+                              pic_stream_t stream);
 
 /* Sparse-query paged attention with fused RoPE for ONE sequence of pages:
  * out[t][h] = softmax_u( RoPE(q[t][h], q_pos[t]) . RoPE(K[u][g], pos(u)) / sqrt(D) ) V[u][g]

@@ -75,6 +75,8 @@ SIGNATURES = {
     "pic_profile_end": (I32, [P, C.POINTER(Profile)]),
     "pic_store_launch_count": (C.c_int64, [P]),
     "pic_op_gemm": (I32, [I32, P, P, P, I32, I32, I32, P]),
+    "pic_op_pack_weight": (I32, [P, P, I32, I32, P]),
+    "pic_op_gemm_packed": (I32, [P, P, P, I32, I32, I32, P]),
     "pic_op_attention_scratch_bytes": (C.c_size_t, [I32, I32, I32, I32, I32]),
     "pic_op_attention": (I32, [I32, I32, I32, I32, I32, P, PI32, P, P, PI32, PI32, PI32, I32, I32, P, I32, P, P,
                                C.c_size_t, P]),

@@ -240,6 +240,24 @@ def gemm(W: torch.Tensor, X: torch.Tensor, stream=None) -> torch.Tensor:
     return Y
 
 
+def pack_weight(W: torch.Tensor, stream=None) -> torch.Tensor:
+    """bf16 [N][K] -> the tensor-core tile layout (pic_op_pack_weight), as a flat bf16 tensor."""
+    lib = L.load()
+    N, K = W.shape
+    out = torch.empty(N * K, dtype=torch.bfloat16, device=W.device)
+    L.check(lib.pic_op_pack_weight(W.contiguous().data_ptr(), out.data_ptr(), N, K, _stream(stream)))
+    return out
+
+
+def gemm_packed(Wp: torch.Tensor, N: int, K: int, X: torch.Tensor, stream=None) -> torch.Tensor:
+    """Y[T][N] = X @ W^T with W in the pic_op_pack_weight layout."""
+    lib = L.load()
+    T = X.shape[0]
+    Y = torch.empty((T, N), dtype=torch.float32, device=X.device)
+    L.check(lib.pic_op_gemm_packed(Wp.data_ptr(), X.contiguous().data_ptr(), Y.data_ptr(), N, K, T, _stream(stream)))
+    return Y
+
+
 def rope_table(n_pos: int, head_dim: int, base: float, device="cuda") -> torch.Tensor:
     lib = L.load()
     out = torch.empty((n_pos, head_dim // 2, 2), dtype=torch.float32, device=device)

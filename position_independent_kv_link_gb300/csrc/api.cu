@@ -42,7 +42,12 @@ struct pic_model {
   std::vector<const void*> wqkv, wo, wgu, wdown;
   int device = 0;
   int num_sms = 0;
+  // bf16: projection matrices repacked once into the tcgen05 tile layout (library-owned)
+  void* packed = nullptr;
+  std::vector<const void*> pqkv, po, pgu, pdown;
+  const void* plm = nullptr;
   int qkv_dim() const { return (cfg.n_heads + 2 * cfg.n_kv_heads) * cfg.head_dim; }
+  ~pic_model() { cudaFree(packed); }
 };
 
 namespace {
@@ -170,8 +175,10 @@ namespace {
 
 int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
-// Y[T][N] += X . W^T (fp32 Y accumulated in place)
-pic_status gemm(const pic_store* s, const void* W, const void* X, float* Y, int N, int K, int T, cudaStream_t st) {
+// Y[T][N] += X . W^T (fp32 Y accumulated in place); Wp: the packed copy of W, if any
+pic_status gemm(const pic_store* s, const void* W, const void* Wp, const void* X, float* Y, int N, int K, int T,
+                cudaStream_t st) {
+  if (Wp) return tc_gemm_run_packed(Wp, X, Y, N, K, T, st);
   if (s->m->cfg.dtype == PIC_BF16 && tc_gemm_supported(N, K, T)) return tc_gemm_run(W, X, Y, N, K, T, st);
   launch_gemm_simt(s->m->cfg.dtype, W, X, Y, N, K, T, 1, st);
   return PIC_OK;
@@ -309,10 +316,11 @@ pic_status run_forward_impl(pic_store* s, const Batch& b, float* hidden_out, flo
 
   const int qkv = s->m->qkv_dim();
   auto gemm_bytes = [&](double N, double K, double rows) { return N * K * es + rows * K * es + rows * N * 4; };
-  auto run_gemm = [&](const void* W, const void* X, float* Y, int N, int K, int rows) {
+  auto run_gemm = [&](const void* W, const void* Wp, const void* X, float* Y, int N, int K, int rows) {
     Rec r(s, st, PIC_PROF_GEMM, gemm_bytes(N, K, rows), 2.0 * N * K * rows, 1);
-    return gemm(s, W, X, Y, N, K, rows, st);
+    return gemm(s, W, Wp, X, Y, N, K, rows, st);
   };
+  auto pk = [&](const std::vector<const void*>& v, int l) -> const void* { return v.empty() ? nullptr : v[l]; };
   // The QKV and gate/up GEMMs add into zeroed accumulators that their epilogues clear
   // again; the O and down projections add straight into the residual stream h.
   {
@@ -321,7 +329,7 @@ pic_status run_forward_impl(pic_store* s, const Batch& b, float* hidden_out, flo
   }
   for (int l = 0; l < c.n_layers; ++l) {
     pic_status e;
-    if ((e = run_gemm(s->m->wqkv[l], s->x, s->qkv_acc, qkv, d, T)) != PIC_OK) return e;
+    if ((e = run_gemm(s->m->wqkv[l], pk(s->m->pqkv, l), s->x, s->qkv_acc, qkv, d, T)) != PIC_OK) return e;
     {
       Rec r(s, st, PIC_PROF_ROWWISE, dT * dQKV * (8 + es), 0, 1);
       launch_qkv_epilogue(dt, T, H, G, D, s->qkv_acc, s->q, d_slot, s->k_layer(l), s->v_layer(l), st);
@@ -334,18 +342,18 @@ pic_status run_forward_impl(pic_store* s, const Batch& b, float* hidden_out, flo
       Rec r(s, st, PIC_PROF_ATTENTION, att_bytes, att_flops, att_launches);
       launch_attention(aa, st);
     }
-    if ((e = run_gemm(s->m->wo[l], s->attn, s->h, d, H * D, T)) != PIC_OK) return e;
+    if ((e = run_gemm(s->m->wo[l], pk(s->m->po, l), s->attn, s->h, d, H * D, T)) != PIC_OK) return e;
     {
       Rec r(s, st, PIC_PROF_ROWWISE, dT * dd * (4 + es), 0, 1);
       launch_rmsnorm_rows(dt, T, d, s->h, s->m->mlp_norm[l], c.rms_eps, s->x, false, nullptr, nullptr, nullptr,
                           nullptr, st);
     }
-    if ((e = run_gemm(s->m->wgu[l], s->x, s->gu_acc, 2 * F, d, T)) != PIC_OK) return e;
+    if ((e = run_gemm(s->m->wgu[l], pk(s->m->pgu, l), s->x, s->gu_acc, 2 * F, d, T)) != PIC_OK) return e;
     {
       Rec r(s, st, PIC_PROF_ROWWISE, dT * 2 * dF * 8 + dT * dF * es, 0, 1);
       launch_swiglu(dt, T, F, s->gu_acc, s->act, st);
     }
-    if ((e = run_gemm(s->m->wdown[l], s->act, s->h, d, F, T)) != PIC_OK) return e;
+    if ((e = run_gemm(s->m->wdown[l], pk(s->m->pdown, l), s->act, s->h, d, F, T)) != PIC_OK) return e;
     const bool last = l == c.n_layers - 1;
     {
       Rec r(s, st, PIC_PROF_ROWWISE, dT * dd * (4 + es), 0, 1);
@@ -356,7 +364,7 @@ pic_status run_forward_impl(pic_store* s, const Batch& b, float* hidden_out, flo
   if (!b.compile && b.n_lg > 0) {
     PIC_CUDA(cudaMemsetAsync(logits_out, 0, (size_t)b.n_lg * c.vocab * sizeof(float), st));
     pic_status e;
-    if ((e = run_gemm(s->m->lm_head, s->lm_x, logits_out, c.vocab, d, b.n_lg)) != PIC_OK) return e;
+    if ((e = run_gemm(s->m->lm_head, s->m->plm, s->lm_x, logits_out, c.vocab, d, b.n_lg)) != PIC_OK) return e;
   }
   PIC_CUDA(cudaGetLastError());
   return PIC_OK;
@@ -431,6 +439,42 @@ pic_status pic_model_create(const pic_model_config* cfg, const pic_weights* w, p
   }
   PIC_CUDA(cudaGetDevice(&m->device));
   PIC_CUDA(cudaDeviceGetAttribute(&m->num_sms, cudaDevAttrMultiProcessorCount, m->device));
+  if (c.dtype == PIC_BF16) {
+    // repack every projection matrix the tensor-core GEMM takes into contiguous 16 KB
+    // tiles in their shared-memory image: each weight tile then streams from HBM as one
+    // sequential bulk copy
+    const int d = c.d_model, HD = c.n_heads * c.head_dim, F = c.ffn_dim, Q = m->qkv_dim();
+    struct Job { const void* src; int N, K; const void** dst; };
+    std::vector<Job> jobs;
+    m->pqkv.assign(c.n_layers, nullptr);
+    m->po.assign(c.n_layers, nullptr);
+    m->pgu.assign(c.n_layers, nullptr);
+    m->pdown.assign(c.n_layers, nullptr);
+    for (int l = 0; l < c.n_layers; ++l) {
+      jobs.push_back({m->wqkv[l], Q, d, &m->pqkv[l]});
+      jobs.push_back({m->wo[l], d, HD, &m->po[l]});
+      jobs.push_back({m->wgu[l], 2 * F, d, &m->pgu[l]});
+      jobs.push_back({m->wdown[l], d, F, &m->pdown[l]});
+    }
+    jobs.push_back({m->lm_head, c.vocab, d, &m->plm});
+    size_t total = 0;
+    for (const Job& j : jobs)
+      if (tc_gemm_supported(j.N, j.K, 1)) total += (size_t)j.N * j.K * 2;
+    if (total) {
+      cudaError_t e = cudaMalloc(&m->packed, total);
+      if (e != cudaSuccess) return fail(PIC_ERR_CUDA, std::string("packed weights cudaMalloc: ") + cudaGetErrorString(e));
+      size_t off = 0;
+      for (const Job& j : jobs) {
+        if (!tc_gemm_supported(j.N, j.K, 1)) continue;
+        void* dst = (char*)m->packed + off;
+        pic_status ps = tc_pack_weight(j.src, dst, j.N, j.K, 0);
+        if (ps != PIC_OK) return ps;
+        *j.dst = dst;
+        off += (size_t)j.N * j.K * 2;
+      }
+      PIC_CUDA(cudaDeviceSynchronize());
+    }
+  }
   *out = m.release();
   return PIC_OK;
 }

@@ -101,6 +101,16 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// 1-D bulk copy of a contiguous global range into shared memory, completing on `bar`
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
+                                          uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar), "l"(policy)
+      : "memory");
+}
+
 // Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row atoms 1024 B apart.
 // (The leading byte offset is unused for K-major tiles whose K extent fits one swizzle row.)
 __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
@@ -155,6 +165,7 @@ __device__ __forceinline__ bool epi_all(bool v) {
 }
 
 struct TcParams {
+  const uint8_t* w_packed;  // PACKED: [N/128][K/64] tiles of 16 KB in their shared-memory image
   int N, K, T;
   int BN;            // token rows per tile (multiple of 16, <= 256)
   int SA, SB;        // weight / activation ring depths
@@ -177,6 +188,9 @@ __device__ __forceinline__ bool next_seg(Seg& s, long long hi, int nkb) {
   return true;
 }
 
+// PACKED: weight tiles come from the pre-swizzled tile copy by one contiguous 16 KB bulk
+// copy each (sequential DRAM pages); otherwise by a 2-D tensor copy of the [N][K] matrix.
+template <bool PACKED>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_x,
                    const __grid_constant__ CUtensorMap map_y, const TcParams p) {
@@ -243,7 +257,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int tile = (int)(g / p.nkb), kb = (int)(g % p.nkb);
       const uint32_t full = smem_u32(a_full + st);
       mbar_expect_tx(full, A_STAGE);
-      tma_load_2d(smem_u32(ringA + st * A_STAGE), &map_w, kb * BK, (tile % p.m_tiles) * BM, full, pol);
+      if (PACKED)
+        bulk_load(smem_u32(ringA + st * A_STAGE),
+                  p.w_packed + ((size_t)(tile % p.m_tiles) * p.nkb + kb) * A_STAGE, A_STAGE, full, pol);
+      else
+        tma_load_2d(smem_u32(ringA + st * A_STAGE), &map_w, kb * BK, (tile % p.m_tiles) * BM, full, pol);
       issued = i + 1;
     }
     for (long long i = max(0LL, issued - p.SA); i < issued; ++i)   // land in-flight copies before exit
@@ -360,6 +378,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 2) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(p.tmem_cols));
 }
 
+// [N][K] bf16 -> [N/128][K/64] tiles of 128 rows x 64 k, each stored exactly as a
+// 128-byte-swizzled K-major shared-memory tile (16-byte chunk j of row r at slot j ^ (r % 8)).
+__global__ void pack_sw128_kernel(const uint4* __restrict__ W, uint4* __restrict__ P, int K, int nkb) {
+  const int tile = blockIdx.x;            // mt * nkb + kb
+  const int mt = tile / nkb, kb = tile % nkb;
+  for (int i = threadIdx.x; i < BM * 8; i += blockDim.x) {
+    const int r = i / 8, j = i % 8;
+    const uint4 v = W[((size_t)(mt * BM + r) * K + kb * BK) / 8 + j];
+    P[(size_t)tile * (A_STAGE / 16) + r * 8 + (j ^ (r & 7))] = v;
+  }
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
@@ -421,11 +451,14 @@ int device_sms() {
 
 bool tc_gemm_supported(int N, int K, int T) { return N >= BM && N % BM == 0 && K >= BK && K % BK == 0 && T >= 1; }
 
-pic_status tc_gemm_run(const void* W, const void* X, float* Y, int N, int K, int T, cudaStream_t st) {
+namespace {
+
+pic_status tc_gemm_launch(const void* W, bool packed, const void* X, float* Y, int N, int K, int T, cudaStream_t st) {
   if (!tc_gemm_supported(N, K, T)) return fail(PIC_ERR_UNSUPPORTED, "tcgen05 gemm: unsupported shape");
   if (((uintptr_t)W | (uintptr_t)X | (uintptr_t)Y) % 16)
     return fail(PIC_ERR_INVALID_ARG, "tcgen05 gemm: operands not 16-byte aligned");
   TcParams p{};
+  p.w_packed = packed ? static_cast<const uint8_t*>(W) : nullptr;
   p.N = N;
   p.K = K;
   p.T = T;
@@ -447,22 +480,44 @@ pic_status tc_gemm_run(const void* W, const void* X, float* Y, int N, int K, int
   p.tmem_cols = 32;
   while ((int)p.tmem_cols < 2 * p.BN) p.tmem_cols <<= 1;
   CUtensorMap mw, mx, my;
-  if (!make_map(&mw, W, N, K, BM) || !make_map(&mx, X, T, K, p.BN) || !make_map_f32(&my, Y, T, N))
+  std::memset(&mw, 0, sizeof(mw));
+  if ((!packed && !make_map(&mw, W, N, K, BM)) || !make_map(&mx, X, T, K, p.BN) || !make_map_f32(&my, Y, T, N))
     return fail(PIC_ERR_CUDA, "cuTensorMapEncodeTiled failed");
   const size_t smem =
       1024 + (size_t)p.SA * A_STAGE + (size_t)p.SB * b_stage + 2 * EPI_BYTES + (2 * p.SA + 2 * p.SB + 6) * 8 + 16;
   int dev = 0;
   cudaGetDevice(&dev);
-  static size_t attr_smem[64] = {};
-  if (dev < 0 || dev >= 64 || attr_smem[dev] < smem) {
-    cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  static size_t attr_smem[2][64] = {};
+  auto kern = packed ? tc_gemm_kernel<true> : tc_gemm_kernel<false>;
+  if (dev < 0 || dev >= 64 || attr_smem[packed][dev] < smem) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return fail(PIC_ERR_CUDA, std::string("tcgen05 gemm attribute: ") + cudaGetErrorString(e));
-    if (dev >= 0 && dev < 64) attr_smem[dev] = smem;
+    if (dev >= 0 && dev < 64) attr_smem[packed][dev] = smem;
   }
   const int grid = (int)std::min<long long>(device_sms(), p.total);
-  tc_gemm_kernel<<<grid, kThreads, smem, st>>>(mw, mx, my, p);
+  kern<<<grid, kThreads, smem, st>>>(mw, mx, my, p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(PIC_ERR_CUDA, std::string("tcgen05 gemm launch: ") + cudaGetErrorString(e));
+  return PIC_OK;
+}
+
+}  // namespace
+
+pic_status tc_gemm_run(const void* W, const void* X, float* Y, int N, int K, int T, cudaStream_t st) {
+  return tc_gemm_launch(W, false, X, Y, N, K, T, st);
+}
+
+pic_status tc_gemm_run_packed(const void* Wp, const void* X, float* Y, int N, int K, int T, cudaStream_t st) {
+  return tc_gemm_launch(Wp, true, X, Y, N, K, T, st);
+}
+
+pic_status tc_pack_weight(const void* W, void* out, int N, int K, cudaStream_t st) {
+  if (!tc_gemm_supported(N, K, 1)) return fail(PIC_ERR_UNSUPPORTED, "pack: N % 128 and K % 64 must be 0");
+  if (((uintptr_t)W | (uintptr_t)out) % 16) return fail(PIC_ERR_INVALID_ARG, "pack: pointers not 16-byte aligned");
+  const int nkb = K / BK;
+  pack_sw128_kernel<<<(N / BM) * nkb, 256, 0, st>>>((const uint4*)W, (uint4*)out, K, nkb);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(PIC_ERR_CUDA, std::string("pack launch: ") + cudaGetErrorString(e));
   return PIC_OK;
 }
 

@@ -57,6 +57,20 @@ pic_status pic_op_gemm(int32_t dtype, const void* W, const void* X, float* Y, in
   return PIC_OK;
 }
 
+pic_status pic_op_pack_weight(const void* W, void* out, int32_t N, int32_t K, pic_stream_t stream) {
+  if (!W || !out || N < 1 || K < 1) return fail(PIC_ERR_INVALID_ARG, "invalid pack arguments");
+  return tc_pack_weight(W, out, N, K, (cudaStream_t)stream);
+}
+
+pic_status pic_op_gemm_packed(const void* W_packed, const void* X, float* Y, int32_t N, int32_t K, int32_t T,
+                              pic_stream_t stream) {
+  if (!W_packed || !X || !Y || N < 1 || K < 1 || T < 1) return fail(PIC_ERR_INVALID_ARG, "invalid gemm arguments");
+  if (!tc_gemm_supported(N, K, T)) return fail(PIC_ERR_UNSUPPORTED, "packed gemm: N % 128 and K % 64 must be 0");
+  cudaStream_t st = (cudaStream_t)stream;
+  PIC_CUDA(cudaMemsetAsync(Y, 0, (size_t)T * N * sizeof(float), st));
+  return tc_gemm_run_packed(W_packed, X, Y, N, K, T, st);
+}
+
 size_t pic_op_attention_scratch_bytes(int32_t T, int32_t n_heads, int32_t n_kv_heads, int32_t head_dim,
                                       int32_t n_pages) {
   if (T < 1 || n_heads < 1 || n_kv_heads < 1 || n_pages < 1) return 0;

@@ -65,6 +65,11 @@ void launch_gemm_simt(int dtype, const void* W, const void* X, float* Y, int N, 
 bool tc_gemm_supported(int N, int K, int T);
 // Y[T][N] (fp32, 16-byte aligned) += X[T][K] . W[N][K]^T on tcgen05 (persistent stream-K).
 pic_status tc_gemm_run(const void* W, const void* X, float* Y, int N, int K, int T, cudaStream_t st);
+// Same with the weights in the tile layout written by tc_pack_weight.
+pic_status tc_gemm_run_packed(const void* Wp, const void* X, float* Y, int N, int K, int T, cudaStream_t st);
+// [N][K] bf16 -> N*K*2 bytes of 16 KB tiles (128 rows x 64 k, 128-byte swizzled image), tile (mt, kb) at
+// (mt * K/64 + kb) * 16 KB.
+pic_status tc_pack_weight(const void* W, void* out, int N, int K, cudaStream_t st);
 // Reads and clears the device flag set when a tcgen05 kernel gave up a bounded wait.
 pic_status tc_check_timeout();
 

@@ -40,6 +40,18 @@ def test_gemm_bf16_tcgen05(N, K, T):
     assert rel_err(Y, ref) < 1e-5
 
 
+@pytest.mark.parametrize("N,K,T", [(128, 64, 1), (6144, 4096, 224), (384, 512, 300), (4096, 14336, 64),
+                                   (1024, 256, 513)])
+def test_gemm_bf16_packed_weights(N, K, T):
+    """The layout the model repacks its matrices into, through the packed tcgen05 path."""
+    from position_independent_kv_link_gb300 import gemm_packed, pack_weight
+    W = pi.randn((N, K), ("gemmWp", N, K), 0.05, torch.bfloat16)
+    X = pi.randn((T, K), ("gemmXp", T, K), 1.0, torch.bfloat16)
+    Y = gemm_packed(pack_weight(W.cuda()), N, K, X.cuda())
+    torch.cuda.synchronize()
+    assert rel_err(Y, X.double() @ W.double().T) < 1e-5
+
+
 @pytest.mark.parametrize("N,K,T", [(96, 64, 7), (768, 256, 24), (1024, 512, 300)])
 def test_gemm_f32_simt(N, K, T):
     from position_independent_kv_link_gb300 import gemm
