@@ -14,9 +14,10 @@
 // on different CTAs meet in Y with no fix-up pass, and the drain of one segment
 // overlaps the MMAs of the next.
 //
-//   warp 0     TMA producer of the weight tiles (deep ring: HBM latency)
-//   warp 1     MMA issuer (one thread): tcgen05.mma kind::f16, fp32 accumulators in TMEM
-//   warp 2     TMA producer of the activation tiles (shallow ring: they sit in L2); TMEM owner
+//   warp 0     TMA producer: weight tile + activation tile of each k-block into one stage
+//   warp 1     MMA issuer (one thread): tcgen05.mma kind::f16, fp32 accumulators in TMEM,
+//              one tcgen05.commit per k-block to free its stage
+//   warp 2     TMEM owner (alloc/dealloc)
 //   warps 3-6  epilogue: tcgen05.ld -> 16-row shared tile -> cp.reduce.async.bulk add
 //
 // Every mbarrier wait is bounded (~2 s of GPU time). On expiry the kernel raises a
@@ -168,23 +169,23 @@ struct TcParams {
   const uint8_t* w_packed;  // PACKED: [N/128][K/64] tiles of 16 KB in their shared-memory image
   int N, K, T;
   int BN;            // token rows per tile (multiple of 16, <= 256)
-  int SA, SB;        // weight / activation ring depths
+  int S;             // pipeline stages (one k-block of weights + activations each)
   int nkb;           // k-blocks per tile
   int m_tiles;       // weight-row tiles
-  long long total;   // tiles * nkb work units
+  int total;         // tiles * nkb work units (< 2^31, checked on the host)
   uint32_t tmem_cols;
 };
 
 // Segment walk shared by the MMA issuer and the epilogue: [g, end) inside one tile.
 struct Seg {
-  long long g, end;
+  int g, end;
   int tile;
 };
-__device__ __forceinline__ bool next_seg(Seg& s, long long hi, int nkb) {
+__device__ __forceinline__ bool next_seg(Seg& s, int hi, int nkb) {
   s.g = s.end;
   if (s.g >= hi) return false;
-  s.tile = (int)(s.g / nkb);
-  s.end = min(hi, (long long)(s.tile + 1) * nkb);
+  s.tile = s.g / nkb;
+  s.end = min(hi, (s.tile + 1) * nkb);
   return true;
 }
 
@@ -197,32 +198,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int b_stage = p.BN * BK * 2;
-  uint8_t* ringA = smem;
-  uint8_t* ringB = ringA + p.SA * A_STAGE;
-  uint8_t* epi = ringB + p.SB * b_stage;                      // [2][16][128] fp32
+  const int stage = A_STAGE + b_stage;                        // one k-block: weight tile, then activation tile
+  uint8_t* ring = smem;
+  uint8_t* epi = ring + p.S * stage;                          // [2][16][128] fp32
   uint64_t* bars = reinterpret_cast<uint64_t*>(epi + 2 * EPI_BYTES);
-  uint64_t* a_full = bars;
-  uint64_t* a_empty = a_full + p.SA;
-  uint64_t* b_full = a_empty + p.SA;
-  uint64_t* b_empty = b_full + p.SB;
-  uint64_t* acc_full = b_empty + p.SB;     // [2]
+  uint64_t* full = bars;
+  uint64_t* empty = full + p.S;
+  uint64_t* acc_full = empty + p.S;        // [2]
   uint64_t* acc_empty = acc_full + 2;      // [2]
   uint64_t* mma_done = acc_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
   __shared__ volatile int s_abort;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const long long lo = p.total * blockIdx.x / gridDim.x, hi = p.total * (blockIdx.x + 1) / gridDim.x;
+  const int lo = (int)((long long)p.total * blockIdx.x / gridDim.x);
+  const int hi = (int)((long long)p.total * (blockIdx.x + 1) / gridDim.x);
 
   if (threadIdx.x == 0) {
     s_abort = 0;
-    for (int i = 0; i < p.SA; ++i) {
-      mbar_init(smem_u32(a_full + i), 1);
-      mbar_init(smem_u32(a_empty + i), 1);
-    }
-    for (int i = 0; i < p.SB; ++i) {
-      mbar_init(smem_u32(b_full + i), 1);
-      mbar_init(smem_u32(b_empty + i), 1);
+    for (int i = 0; i < p.S; ++i) {
+      mbar_init(smem_u32(full + i), 1);
+      mbar_init(smem_u32(empty + i), 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(acc_full + i), 1);
@@ -243,55 +239,50 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0 && lane == 0) {
-    // ---------------- weight producer: HBM stream, evicted first from L2
-    uint64_t pol;
-    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
-    long long issued = 0;
-    for (long long g = lo; g < hi; ++g) {
-      const long long i = g - lo;
-      const int st = (int)(i % p.SA);
-      if (s_abort || !mbar_wait(smem_u32(a_empty + st), (uint32_t)((i / p.SA) & 1) ^ 1)) {
+    // ---------------- TMA producer: weight tile (HBM stream, evicted first from L2) and
+    // activation tile (small, reused by every weight tile, kept in L2) of each k-block.
+    // Stage, phase and (tile, k-block) advance incrementally: no division in the loop.
+    uint64_t pol_w, pol_x;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol_w));
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol_x));
+    int st = 0, issued = 0;
+    uint32_t ph = 0;
+    int tile = lo / p.nkb, kb = lo % p.nkb;
+    int mt = tile % p.m_tiles, tt = tile / p.m_tiles;
+    for (int g = lo; g < hi; ++g) {
+      if (s_abort || !mbar_wait(smem_u32(empty + st), ph ^ 1)) {
         s_abort = 1;
         break;
       }
-      const int tile = (int)(g / p.nkb), kb = (int)(g % p.nkb);
-      const uint32_t full = smem_u32(a_full + st);
-      mbar_expect_tx(full, A_STAGE);
+      const uint32_t fb = smem_u32(full + st);
+      const uint32_t dst = smem_u32(ring + st * stage);
+      mbar_expect_tx(fb, stage);
       if (PACKED)
-        bulk_load(smem_u32(ringA + st * A_STAGE),
-                  p.w_packed + ((size_t)(tile % p.m_tiles) * p.nkb + kb) * A_STAGE, A_STAGE, full, pol);
+        bulk_load(dst, p.w_packed + ((size_t)mt * p.nkb + kb) * A_STAGE, A_STAGE, fb, pol_w);
       else
-        tma_load_2d(smem_u32(ringA + st * A_STAGE), &map_w, kb * BK, (tile % p.m_tiles) * BM, full, pol);
-      issued = i + 1;
-    }
-    for (long long i = max(0LL, issued - p.SA); i < issued; ++i)   // land in-flight copies before exit
-      if (!mbar_wait(smem_u32(a_full + (int)(i % p.SA)), (uint32_t)((i / p.SA) & 1))) break;
-  } else if (warp == 2 && lane == 0) {
-    // ---------------- activation producer: small, reused by every weight tile, kept in L2
-    uint64_t pol;
-    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
-    long long issued = 0;
-    for (long long g = lo; g < hi; ++g) {
-      const long long i = g - lo;
-      const int st = (int)(i % p.SB);
-      if (s_abort || !mbar_wait(smem_u32(b_empty + st), (uint32_t)((i / p.SB) & 1) ^ 1)) {
-        s_abort = 1;
-        break;
+        tma_load_2d(dst, &map_w, kb * BK, mt * BM, fb, pol_w);
+      tma_load_2d(dst + A_STAGE, &map_x, kb * BK, tt * p.BN, fb, pol_x);
+      ++issued;
+      if (++st == p.S) {
+        st = 0;
+        ph ^= 1;
       }
-      const int tile = (int)(g / p.nkb), kb = (int)(g % p.nkb);
-      const uint32_t full = smem_u32(b_full + st);
-      mbar_expect_tx(full, b_stage);
-      tma_load_2d(smem_u32(ringB + st * b_stage), &map_x, kb * BK, (tile / p.m_tiles) * p.BN, full, pol);
-      issued = i + 1;
+      if (++kb == p.nkb) {
+        kb = 0;
+        if (++mt == p.m_tiles) {
+          mt = 0;
+          ++tt;
+        }
+      }
     }
-    for (long long i = max(0LL, issued - p.SB); i < issued; ++i)
-      if (!mbar_wait(smem_u32(b_full + (int)(i % p.SB)), (uint32_t)((i / p.SB) & 1))) break;
+    for (int j = max(0, issued - p.S); j < issued; ++j)   // land in-flight copies before exit
+      if (!mbar_wait(smem_u32(full + j % p.S), (uint32_t)((j / p.S) & 1))) break;
   } else if (warp == 1 && lane == 0) {
-    // ---------------- MMA issuer
+    // ---------------- MMA issuer: one commit per k-block releases its stage
     const uint32_t idesc = idesc_bf16(BM, p.BN);
     Seg sg{0, lo, 0};
-    int s = 0;
-    long long i = 0;
+    int s = 0, st = 0;
+    uint32_t ph = 0;
     bool stop = false;
     while (!stop && next_seg(sg, hi, p.nkb)) {
       const int ab = s & 1;
@@ -301,23 +292,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       asm volatile("tcgen05.fence::after_thread_sync;");
       const uint32_t d_tmem = tmem + ab * p.BN;
-      for (long long g = sg.g; g < sg.end; ++g, ++i) {
-        const int sa = (int)(i % p.SA), sb = (int)(i % p.SB);
-        if (s_abort || !mbar_wait(smem_u32(a_full + sa), (uint32_t)((i / p.SA) & 1)) ||
-            !mbar_wait(smem_u32(b_full + sb), (uint32_t)((i / p.SB) & 1))) {
+      for (int g = sg.g; g < sg.end; ++g) {
+        if (s_abort || !mbar_wait(smem_u32(full + st), ph)) {
           s_abort = 1;
           stop = true;
           break;
         }
         asm volatile("tcgen05.fence::after_thread_sync;");
-        const uint32_t a_base = smem_u32(ringA + sa * A_STAGE);
-        const uint32_t b_base = smem_u32(ringB + sb * b_stage);
+        const uint32_t a_base = smem_u32(ring + st * stage);
+        const uint32_t b_base = a_base + A_STAGE;
 #pragma unroll
         for (int k = 0; k < BK / UMMA_K; ++k)
           umma_bf16(d_tmem, smem_desc_sw128(a_base + k * UMMA_K * 2), smem_desc_sw128(b_base + k * UMMA_K * 2),
                     idesc, (g != sg.g || k != 0) ? 1u : 0u);
-        umma_commit(smem_u32(a_empty + sa));  // stages free once these MMAs retire
-        umma_commit(smem_u32(b_empty + sb));
+        umma_commit(smem_u32(empty + st));  // the stage is free once these MMAs retire
+        if (++st == p.S) {
+          st = 0;
+          ph ^= 1;
+        }
       }
       if (!stop) umma_commit(smem_u32(acc_full + ab));
       ++s;
@@ -466,17 +458,13 @@ pic_status tc_gemm_launch(const void* W, bool packed, const void* X, float* Y, i
   p.nkb = K / BK;
   p.m_tiles = N / BM;
   const long long tiles = (long long)p.m_tiles * ((T + p.BN - 1) / p.BN);
-  p.total = tiles * p.nkb;
+  if (tiles * p.nkb >= (1LL << 31)) return fail(PIC_ERR_UNSUPPORTED, "tcgen05 gemm: shape too large");
+  p.total = (int)(tiles * p.nkb);
   const int b_stage = p.BN * BK * 2;
-  // shared memory: the weight ring gets what the activation ring, the two epilogue tiles
-  // and the barriers leave of the opt-in limit
+  // shared memory: as many stages as fit next to the two epilogue tiles and the barriers
   const int budget = 227 * 1024 - 1024 - 2 * EPI_BYTES - 512;
-  // ~96 KB of activation stages hide the L2 latency of the next activation tile (one
-  // tile is consumed every k-block); the weight ring keeps the rest for HBM latency.
-  p.SB = std::max(2, std::min(8, (96 * 1024 + b_stage - 1) / b_stage));
-  while (p.SB > 2 && (budget - p.SB * b_stage) / A_STAGE < 5) --p.SB;
-  p.SA = std::min(12, (budget - p.SB * b_stage) / A_STAGE);
-  if (p.SA < 2) return fail(PIC_ERR_UNSUPPORTED, "tcgen05 gemm: pipeline does not fit shared memory");
+  p.S = std::min(12, budget / (A_STAGE + b_stage));
+  if (p.S < 2) return fail(PIC_ERR_UNSUPPORTED, "tcgen05 gemm: pipeline does not fit shared memory");
   p.tmem_cols = 32;
   while ((int)p.tmem_cols < 2 * p.BN) p.tmem_cols <<= 1;
   CUtensorMap mw, mx, my;
@@ -484,7 +472,7 @@ pic_status tc_gemm_launch(const void* W, bool packed, const void* X, float* Y, i
   if ((!packed && !make_map(&mw, W, N, K, BM)) || !make_map(&mx, X, T, K, p.BN) || !make_map_f32(&my, Y, T, N))
     return fail(PIC_ERR_CUDA, "cuTensorMapEncodeTiled failed");
   const size_t smem =
-      1024 + (size_t)p.SA * A_STAGE + (size_t)p.SB * b_stage + 2 * EPI_BYTES + (2 * p.SA + 2 * p.SB + 6) * 8 + 16;
+      1024 + (size_t)p.S * (A_STAGE + b_stage) + 2 * EPI_BYTES + (2 * p.S + 6) * 8 + 16;
   int dev = 0;
   cudaGetDevice(&dev);
   static size_t attr_smem[2][64] = {};
@@ -494,7 +482,7 @@ pic_status tc_gemm_launch(const void* W, bool packed, const void* X, float* Y, i
     if (e != cudaSuccess) return fail(PIC_ERR_CUDA, std::string("tcgen05 gemm attribute: ") + cudaGetErrorString(e));
     if (dev >= 0 && dev < 64) attr_smem[packed][dev] = smem;
   }
-  const int grid = (int)std::min<long long>(device_sms(), p.total);
+  const int grid = std::min(device_sms(), p.total);
   kern<<<grid, kThreads, smem, st>>>(mw, mx, my, p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(PIC_ERR_CUDA, std::string("tcgen05 gemm launch: ") + cudaGetErrorString(e));
