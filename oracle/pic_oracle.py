@@ -312,8 +312,12 @@ class OracleStore:
         return [self._add_chunk(c, k, v) for c, (k, v) in zip(chunks, kv)]
 
     def import_chunk(self, tokens: np.ndarray, k_layers, v_layers) -> int:
-        """Store externally produced chunk KV (per layer [L, G, D]) as if compiled."""
-        return self._add_chunk(tokens, [_f64(a) for a in k_layers], [_f64(a) for a in v_layers])
+        """Store externally produced chunk KV (per layer [L, G, D]) as if compiled.
+
+        Values are kept as given (bf16/fp32 are exact in fp64) and upcast layer by layer
+        when the link reads them.
+        """
+        return self._add_chunk(tokens, list(k_layers), list(v_layers))
 
     def release_chunk(self, cid: int) -> None:
         c = self.chunks[cid]
