@@ -407,6 +407,8 @@ def run_kernel(args):
         W = (torch.randn(N, K, device="cuda", generator=g) * 0.02).to(torch.bfloat16)
         X = torch.randn(T, K, device="cuda", generator=g).to(torch.bfloat16)
         Y = torch.empty(T, N, device="cuda")
+        if not args.unpacked:
+            X = X.to(torch.float16)   # the packed (model) path runs fp16 operands
         if args.unpacked:
             call = lambda: L.check(lib.pic_op_gemm(L.PIC_BF16, W.data_ptr(), X.data_ptr(), Y.data_ptr(), N, K, T, sp))
         else:   # the tile layout the model repacks its matrices into
@@ -429,8 +431,8 @@ def run_kernel(args):
         T, n_pages = len(sel), len(pblk)
         Kp = torch.randn(n_pages, 8, 16, 128, device="cuda", generator=g).to(torch.bfloat16)
         Vp = torch.randn(n_pages, 8, 16, 128, device="cuda", generator=g).to(torch.bfloat16)
-        q = torch.randn(T, 32, 128, device="cuda", generator=g).to(torch.bfloat16)
-        out = torch.empty_like(q)
+        q = torch.randn(T, 32, 128, device="cuda", generator=g)
+        out = torch.empty(q.shape, dtype=torch.float16, device="cuda")
         rope = api.rope_table(off + 16, 128, 500000.0)
         nb = lib.pic_op_attention_scratch_bytes(T, 32, 8, 128, n_pages)
         scratch = torch.empty(nb, dtype=torch.uint8, device="cuda")

@@ -225,24 +225,29 @@ int64_t pic_store_launch_count(const pic_store* s);
 pic_status pic_op_gemm(int32_t dtype, const void* W, const void* X, float* Y, int32_t N, int32_t K, int32_t T,
                        pic_stream_t stream);
 
-/* Repacks a bf16 [N][K] matrix (N % 128 == 0, K % 64 == 0) into N*K*2 bytes of 16 KB
- * tiles of 128 rows x 64 columns, tile (n/128, k/64) at byte ((n/128)*(K/64) + k/64)*16384,
- * each stored as the 128-byte-swizzled K-major image the tensor cores read from shared
- * memory. pic_model_create does this for every bf16 projection matrix (one library-owned
- * copy) so each weight tile streams from HBM as one sequential bulk copy. */
+/* Repacks a bf16 [N][K] matrix (N % 128 == 0, K % 64 == 0) into N*K*2 bytes of fp16
+ * 16 KB tiles of 128 rows x 64 columns, tile (n/128, k/64) at byte
+ * ((n/128)*(K/64) + k/64)*16384, each stored as the 128-byte-swizzled K-major image the
+ * tensor cores read from shared memory (bf16 values are exact in fp16 down to 2^-14 in
+ * magnitude; smaller ones keep 2^-24 absolute precision). pic_model_create does this for
+ * every bf16 projection matrix (one library-owned copy) so each weight tile streams from
+ * HBM as one sequential bulk copy and the activations can be fp16. */
 pic_status pic_op_pack_weight(const void* W, void* out, int32_t N, int32_t K, pic_stream_t stream);
-/* pic_op_gemm (bf16) with W given in the pic_op_pack_weight layout. */
+/* Y[T][N] (fp32, overwritten) = X[T][K] . W^T with W in the pic_op_pack_weight layout and
+ * X fp16, on the tcgen05 kernel. */
 pic_status pic_op_gemm_packed(const void* W_packed, const void* X, float* Y, int32_t N, int32_t K, int32_t T,
                               pic_stream_t stream);
 
 /* Sparse-query paged attention with fused RoPE for ONE sequence of pages:
  * out[t][h] = softmax_u( RoPE(q[t][h], q_pos[t]) . RoPE(K[u][g], pos(u)) / sqrt(D) ) V[u][g]
  * over every key u of the listed pages with pos(u) <= q_pos[t], g = h / (H/G).
- * q, out: [T][H][D]; q_pos: HOST [T] (ascending); pages: HOST arrays of n_pages
- * (block, position of row 0, valid rows); k_layer/v_layer: one layer of the pools
- * ([pool_blocks][G][16][D]); every page block must be < pool_blocks. rope_cs: device
- * float2 [rope_positions][D/2] (cos, sin), e.g. from pic_op_rope_table; every position
- * must be < rope_positions, and rope_positions >= 16. Scratch as reported by pic_op_attention_scratch_bytes. */
+ * dtype: type of the K/V pools. q: fp32 [T][H][D] (pre-RoPE); out: [T][H][D] fp16 when
+ * dtype is PIC_BF16 (the operand type of the projection that follows), fp32 when PIC_F32.
+ * q_pos: HOST [T] (ascending); pages: HOST arrays of n_pages (block, position of row 0,
+ * valid rows); k_layer/v_layer: one layer of the pools ([pool_blocks][G][16][D]); every
+ * page block must be < pool_blocks. rope_cs: device float2 [rope_positions][D/2] (cos,
+ * sin), e.g. from pic_op_rope_table; every position must be < rope_positions, and
+ * rope_positions >= 16. Scratch as reported by pic_op_attention_scratch_bytes. */
 size_t pic_op_attention_scratch_bytes(int32_t T, int32_t n_heads, int32_t n_kv_heads, int32_t head_dim,
                                       int32_t n_pages);
 pic_status pic_op_attention(int32_t dtype, int32_t T, int32_t n_heads, int32_t n_kv_heads, int32_t head_dim,

@@ -241,18 +241,19 @@ def gemm(W: torch.Tensor, X: torch.Tensor, stream=None) -> torch.Tensor:
 
 
 def pack_weight(W: torch.Tensor, stream=None) -> torch.Tensor:
-    """bf16 [N][K] -> the tensor-core tile layout (pic_op_pack_weight), as a flat bf16 tensor."""
+    """bf16 [N][K] -> the fp16 tensor-core tile layout (pic_op_pack_weight), as a flat tensor."""
     lib = L.load()
     N, K = W.shape
-    out = torch.empty(N * K, dtype=torch.bfloat16, device=W.device)
+    out = torch.empty(N * K, dtype=torch.float16, device=W.device)
     L.check(lib.pic_op_pack_weight(W.contiguous().data_ptr(), out.data_ptr(), N, K, _stream(stream)))
     return out
 
 
 def gemm_packed(Wp: torch.Tensor, N: int, K: int, X: torch.Tensor, stream=None) -> torch.Tensor:
-    """Y[T][N] = X @ W^T with W in the pic_op_pack_weight layout."""
+    """Y[T][N] = X @ W^T with W in the pic_op_pack_weight layout (fp16 tiles) and X fp16."""
     lib = L.load()
     T = X.shape[0]
+    assert X.dtype == torch.float16
     Y = torch.empty((T, N), dtype=torch.float32, device=X.device)
     L.check(lib.pic_op_gemm_packed(Wp.data_ptr(), X.contiguous().data_ptr(), Y.data_ptr(), N, K, T, _stream(stream)))
     return Y
@@ -268,16 +269,22 @@ def rope_table(n_pos: int, head_dim: int, base: float, device="cuda") -> torch.T
 def attention(q: torch.Tensor, q_pos: np.ndarray, k_layer: torch.Tensor, v_layer: torch.Tensor,
               pages: Tuple[np.ndarray, np.ndarray, np.ndarray], rope: torch.Tensor, n_kv_heads: int,
               stream=None) -> torch.Tensor:
-    """Paged attention of one sequence through pic_op_attention. q [T, H, D]."""
+    """Paged attention of one sequence through pic_op_attention.
+
+    q: fp32 [T, H, D] (pre-RoPE); k_layer/v_layer: one layer of the pools. Returns fp16
+    [T, H, D] for bf16 pools, fp32 for fp32 pools.
+    """
     lib = L.load()
     T, H, D = q.shape
+    assert q.dtype == torch.float32
     blk, ppos, plen = (_i32(a) for a in pages)
     qp = _i32(q_pos)
-    out = torch.empty_like(q)
+    out = torch.empty(q.shape, dtype=torch.float16 if k_layer.dtype == torch.bfloat16 else torch.float32,
+                      device=q.device)
     nb = lib.pic_op_attention_scratch_bytes(T, H, n_kv_heads, D, len(blk))
     scratch = torch.empty(max(nb, 1), dtype=torch.uint8, device=q.device)
-    L.check(lib.pic_op_attention(_dtype_code(q.dtype), T, H, n_kv_heads, D, q.contiguous().data_ptr(), _ptr_i32(qp),
-                                 k_layer.data_ptr(), v_layer.data_ptr(), _ptr_i32(blk), _ptr_i32(ppos),
+    L.check(lib.pic_op_attention(_dtype_code(k_layer.dtype), T, H, n_kv_heads, D, q.contiguous().data_ptr(),
+                                 _ptr_i32(qp), k_layer.data_ptr(), v_layer.data_ptr(), _ptr_i32(blk), _ptr_i32(ppos),
                                  _ptr_i32(plen), len(blk), k_layer.shape[0], rope.data_ptr(), rope.shape[0],
                                  out.data_ptr(), scratch.data_ptr(), nb, _stream(stream)))
     return out

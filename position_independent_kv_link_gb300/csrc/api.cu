@@ -112,7 +112,7 @@ struct pic_store {
   char* ws = nullptr;
   float* h = nullptr;
   void* x = nullptr;
-  void* q = nullptr;
+  float* q = nullptr;        // [max_rows][H*D] fp32, pre-RoPE
   void* attn = nullptr;
   void* act = nullptr;
   void* lm_x = nullptr;
@@ -179,8 +179,7 @@ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 pic_status gemm(const pic_store* s, const void* W, const void* Wp, const void* X, float* Y, int N, int K, int T,
                 cudaStream_t st) {
   if (Wp) return tc_gemm_run_packed(Wp, X, Y, N, K, T, st);
-  if (s->m->cfg.dtype == PIC_BF16 && tc_gemm_supported(N, K, T)) return tc_gemm_run(W, X, Y, N, K, T, st);
-  launch_gemm_simt(s->m->cfg.dtype, W, X, Y, N, K, T, 1, st);
+  launch_gemm_simt(s->m->cfg.dtype, s->m->cfg.dtype == PIC_BF16, W, X, Y, N, K, T, 1, st);
   return PIC_OK;
 }
 
@@ -513,8 +512,9 @@ pic_status pic_store_create(pic_model* m, const pic_store_config* cfg, void* k_p
     off = align_up(off + bytes, 256);
     return at;
   };
-  const size_t o_h = carve(R * d * 4), o_x = carve(R * std::max(d, HD) * es), o_q = carve(R * HD * es),
-               o_attn = carve(R * HD * es), o_act = carve(R * F * es), o_lm = carve((size_t)sc.max_logit_rows * d * es),
+  const size_t as = act_size(c.dtype);
+  const size_t o_h = carve(R * d * 4), o_x = carve(R * std::max(d, HD) * as), o_q = carve(R * HD * 4),
+               o_attn = carve(R * HD * as), o_act = carve(R * F * as), o_lm = carve((size_t)sc.max_logit_rows * d * as),
                o_qkv = carve(R * (size_t)m->qkv_dim() * 4), o_gu = carve(R * 2 * F * 4),
                o_atto = carve((size_t)s->att_parts_cap * kAttnPartRows * rep * c.head_dim * 4),
                o_attml = carve((size_t)s->att_parts_cap * kAttnPartRows * rep * 2 * 4), o_meta = carve(s->meta_cap * 4),
@@ -523,7 +523,7 @@ pic_status pic_store_create(pic_model* m, const pic_store_config* cfg, void* k_p
   if (e != cudaSuccess) return fail(PIC_ERR_CUDA, std::string("workspace cudaMalloc: ") + cudaGetErrorString(e));
   s->h = (float*)(s->ws + o_h);
   s->x = s->ws + o_x;
-  s->q = s->ws + o_q;
+  s->q = (float*)(s->ws + o_q);
   s->attn = s->ws + o_attn;
   s->act = s->ws + o_act;
   s->lm_x = s->ws + o_lm;

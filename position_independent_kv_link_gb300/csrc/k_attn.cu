@@ -18,13 +18,14 @@ namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
 
-template <typename T, int D>
+// T: KV storage type; O: output type (fp16 for bf16 KV, fp32 for fp32 KV); q is fp32.
+template <typename T, typename O, int D>
 __global__ void __launch_bounds__(128) attn_simt_kernel(AttnArgs a) {
   constexpr int NJ = D / 32;   // dims per lane: lane + 32 j
   const AttnItem it = a.items[blockIdx.x];
   const int rep = a.H / a.G;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const T* Q = (const T*)a.q;
+  const float* Q = a.q;
   const T* Kl = (const T*)a.k_layer;
   const T* Vl = (const T*)a.v_layer;
   const float scale = rsqrtf((float)D) * kLog2e;
@@ -35,7 +36,7 @@ __global__ void __launch_bounds__(128) attn_simt_kernel(AttnArgs a) {
     float q[NJ], o[NJ];
 #pragma unroll
     for (int j = 0; j < NJ; ++j) {
-      q[j] = to_f<T>(Q[((size_t)t * a.H + h) * D + lane + 32 * j]);
+      q[j] = Q[((size_t)t * a.H + h) * D + lane + 32 * j];
       o[j] = 0.f;
     }
     const float2* csq = a.rope_cs + (size_t)qp * (D / 2);
@@ -76,9 +77,9 @@ __global__ void __launch_bounds__(128) attn_simt_kernel(AttnArgs a) {
     }
     if (it.part < 0) {
       const float inv = 1.f / l;
-      T* out = (T*)a.out;
+      O* out = (O*)a.out;
 #pragma unroll
-      for (int j = 0; j < NJ; ++j) out[((size_t)t * a.H + h) * D + lane + 32 * j] = from_f<T>(o[j] * inv);
+      for (int j = 0; j < NJ; ++j) out[((size_t)t * a.H + h) * D + lane + 32 * j] = from_f<O>(o[j] * inv);
     } else {
       const size_t pi = ((size_t)it.part * kAttnPartRows + r) * rep + hh;
 #pragma unroll
@@ -94,7 +95,7 @@ __global__ void __launch_bounds__(128) attn_simt_kernel(AttnArgs a) {
 // Merge split results: out = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s, in one pass
 // with a running maximum. grid (merges, ceil(16 * rep / 8)); one warp per (row, head),
 // D/32 consecutive dims per lane.
-template <typename T, int D>
+template <typename O, int D>
 __global__ void __launch_bounds__(256) attn_combine_kernel(AttnArgs a) {
   constexpr int NJ = D / 32;
   const AttnCombine c = a.combines[blockIdx.x];
@@ -127,17 +128,17 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(AttnArgs a) {
   }
   const int t = c.row0 + r, h = c.g * rep + hh;
   const float inv = L > 0.f ? 1.f / L : 0.f;
-  T* out = (T*)a.out + ((size_t)t * a.H + h) * D + lane * NJ;
+  O* out = (O*)a.out + ((size_t)t * a.H + h) * D + lane * NJ;
 #pragma unroll
-  for (int j = 0; j < NJ; ++j) out[j] = from_f<T>(o[j] * inv);
+  for (int j = 0; j < NJ; ++j) out[j] = from_f<O>(o[j] * inv);
 }
 
-template <typename T, int D>
+template <typename T, typename O, int D>
 void launch_simt(const AttnArgs& a, cudaStream_t st) {
-  if (a.n_items > 0) attn_simt_kernel<T, D><<<a.n_items, 128, 0, st>>>(a);
+  if (a.n_items > 0) attn_simt_kernel<T, O, D><<<a.n_items, 128, 0, st>>>(a);
   if (a.n_combines > 0) {
     const int rep = a.H / a.G;
-    attn_combine_kernel<T, D><<<dim3(a.n_combines, (a.rb * rep + 7) / 8), 256, 0, st>>>(a);
+    attn_combine_kernel<O, D><<<dim3(a.n_combines, (a.rb * rep + 7) / 8), 256, 0, st>>>(a);
   }
 }
 
@@ -145,11 +146,11 @@ void launch_simt(const AttnArgs& a, cudaStream_t st) {
 
 void launch_attention_simt(const AttnArgs& a, cudaStream_t st) {
   if (a.dtype == PIC_BF16) {
-    if (a.D == 128) launch_simt<__nv_bfloat16, 128>(a, st);
-    else launch_simt<__nv_bfloat16, 64>(a, st);
+    if (a.D == 128) launch_simt<__nv_bfloat16, __half, 128>(a, st);
+    else launch_simt<__nv_bfloat16, __half, 64>(a, st);
   } else {
-    if (a.D == 128) launch_simt<float, 128>(a, st);
-    else launch_simt<float, 64>(a, st);
+    if (a.D == 128) launch_simt<float, float, 128>(a, st);
+    else launch_simt<float, float, 64>(a, st);
   }
 }
 

@@ -1,4 +1,4 @@
-// Tensor-core paged attention for bf16 models with head_dim 128 (mma.sync m16n8k16).
+// Tensor-core paged attention for bf16 KV with head_dim 128 (mma.sync m16n8k16, fp16 operands).
 //
 // One CTA = one work item: up to 16*RG consecutive query rows of one sequence x the REP
 // query heads that share KV head g (GQA) x a run of pages. Warp w owns query head
@@ -10,7 +10,9 @@
 //     For a key at row r of a page that starts at position P, cos/sin((P + r) theta) is
 //     composed from the table row of P (one per page, staged by cp.async) and the row of
 //     r (resident), so a tile reads 4 table rows instead of 64.
-//   * V: cp.async straight into the double-buffered operand tile.
+//   * V: cp.async into a raw buffer, converted to fp16 in the same pass.
+//   Operands are fp16 (bf16 K/V values are exact in fp16; q arrives in fp32 and is rounded
+//   once, after RoPE); S, the softmax and O are fp32; the output is fp16.
 //   * page metadata (block, start, length) is cached in shared memory in windows of 512
 //     pages, so no global load sits in front of the KV loads.
 // S = Q K^T and O += P V run on mma.sync with fp32 accumulators; the online softmax
@@ -49,13 +51,13 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t&
 }
 __device__ __forceinline__ void mma16816(float* c, const uint32_t* a, uint32_t b0, uint32_t b1) {
   asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
       "{%0,%1,%2,%3};"
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+__device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
 }
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
@@ -63,22 +65,29 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
-// rotate 8 dims (i) and their partners (i + 64) by the composed angle, times `scale`
-__device__ __forceinline__ void rope8(const uint4& x1, const uint4& x2, const float2* hi, const float2* lo,
-                                      float scale, uint4& y1, uint4& y2) {
-  const __nv_bfloat16* b1 = reinterpret_cast<const __nv_bfloat16*>(&x1);
-  const __nv_bfloat16* b2 = reinterpret_cast<const __nv_bfloat16*>(&x2);
-  __nv_bfloat16 o1[8], o2[8];
+// rotate 8 dims (i) and their partners (i + 64) by the composed angle, times `scale`, to fp16
+__device__ __forceinline__ void rope8(const float* v1, const float* v2, const float2* hi, const float2* lo, float scale,
+                                      uint4& y1, uint4& y2) {
+  __half o1[8], o2[8];
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
     const float2 H2 = hi[e], L2 = lo[e];
     const float cs = H2.x * L2.x - H2.y * L2.y, sn = H2.y * L2.x + H2.x * L2.y;
-    const float v1 = __bfloat162float(b1[e]), v2 = __bfloat162float(b2[e]);
-    o1[e] = __float2bfloat16_rn((v1 * cs - v2 * sn) * scale);
-    o2[e] = __float2bfloat16_rn((v2 * cs + v1 * sn) * scale);
+    o1[e] = __float2half_rn((v1[e] * cs - v2[e] * sn) * scale);
+    o2[e] = __float2half_rn((v2[e] * cs + v1[e] * sn) * scale);
   }
   y1 = *reinterpret_cast<uint4*>(o1);
   y2 = *reinterpret_cast<uint4*>(o2);
+}
+
+__device__ __forceinline__ void bf16x8_to_f32(const uint4& u, float* f) {
+  const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float2 x = __bfloat1622float2(b[e]);
+    f[2 * e] = x.x;
+    f[2 * e + 1] = x.y;
+  }
 }
 
 template <int REP, int RG>
@@ -86,8 +95,9 @@ __global__ void __launch_bounds__(REP * RG * 32) attn_mma_kernel(AttnArgs a) {
   constexpr int NW = REP * RG, NT = NW * 32;
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* sK = smem;                                   // [2][KT][D] rotated K (Q staging at start)
-  uint8_t* sKr = sK + 2 * TILE_BYTES;                   // [KT][D] raw K of the next tile
-  uint8_t* sV = sKr + TILE_BYTES;                       // [2][KT][D]
+  uint8_t* sKr = sK + 2 * TILE_BYTES;                   // [KT][D] raw (bf16) K of the next tile
+  uint8_t* sVr = sKr + TILE_BYTES;                      // [KT][D] raw (bf16) V of the next tile
+  uint8_t* sV = sVr + TILE_BYTES;                       // [2][KT][D] fp16 V operand
   float2* sLo = reinterpret_cast<float2*>(sV + 2 * TILE_BYTES);   // [16][64] cos/sin of p = 0..15
   float2* sPg = sLo + 16 * 64;                                     // [2][4][64] cos/sin of page starts
   int* sBlk = reinterpret_cast<int*>(sPg + 2 * 4 * 64);            // [WIN] page metadata window
@@ -96,7 +106,7 @@ __global__ void __launch_bounds__(REP * RG * 32) attn_mma_kernel(AttnArgs a) {
   int* sPos = sPl + WIN;                                           // [2][KT] key positions (INT_MAX = masked)
   const uint32_t sK_u = (uint32_t)__cvta_generic_to_shared(sK);
   const uint32_t sKr_u = (uint32_t)__cvta_generic_to_shared(sKr);
-  const uint32_t sV_u = (uint32_t)__cvta_generic_to_shared(sV);
+  const uint32_t sVr_u = (uint32_t)__cvta_generic_to_shared(sVr);
   const uint32_t sPg_u = (uint32_t)__cvta_generic_to_shared(sPg);
 
   const AttnItem it = a.items[blockIdx.x];
@@ -104,7 +114,7 @@ __global__ void __launch_bounds__(REP * RG * 32) attn_mma_kernel(AttnArgs a) {
   const int G = a.G;
   const __nv_bfloat16* Kl = (const __nv_bfloat16*)a.k_layer;
   const __nv_bfloat16* Vl = (const __nv_bfloat16*)a.v_layer;
-  const __nv_bfloat16* Q = (const __nv_bfloat16*)a.q;
+  const float* Q = a.q;
   const int npages = it.page1 - it.page0;
   const int ntiles = (npages + 3) / 4;
 
@@ -131,9 +141,13 @@ __global__ void __launch_bounds__(REP * RG * 32) attn_mma_kernel(AttnArgs a) {
     uint4 y1 = make_uint4(0, 0, 0, 0), y2 = y1;
     if (r < it.nrows) {
       const int t = it.row0 + r, h = it.g * REP + qh, p = a.q_pos[t];
-      const __nv_bfloat16* src = Q + ((size_t)t * a.H + h) * D;
-      rope8(*reinterpret_cast<const uint4*>(src + 8 * c), *reinterpret_cast<const uint4*>(src + 64 + 8 * c),
-            a.rope_cs + (size_t)(p & ~15) * 64 + 8 * c, sLo + (p & 15) * 64 + 8 * c, qscale, y1, y2);
+      const float* src = Q + ((size_t)t * a.H + h) * D;
+      float v1[8], v2[8];
+      *reinterpret_cast<float4*>(v1) = *reinterpret_cast<const float4*>(src + 8 * c);
+      *reinterpret_cast<float4*>(v1 + 4) = *reinterpret_cast<const float4*>(src + 8 * c + 4);
+      *reinterpret_cast<float4*>(v2) = *reinterpret_cast<const float4*>(src + 64 + 8 * c);
+      *reinterpret_cast<float4*>(v2 + 4) = *reinterpret_cast<const float4*>(src + 64 + 8 * c + 4);
+      rope8(v1, v2, a.rope_cs + (size_t)(p & ~15) * 64 + 8 * c, sLo + (p & 15) * 64 + 8 * c, qscale, y1, y2);
     }
     uint8_t* base = sK + w * 16 * D * 2;
     *reinterpret_cast<uint4*>(base + swz(r16, c)) = y1;
@@ -168,9 +182,7 @@ __global__ void __launch_bounds__(REP * RG * 32) attn_mma_kernel(AttnArgs a) {
       if (valid) {
         const size_t src = (((size_t)sBlk[pi] * G + it.g) * kBlock + r) * D + 8 * c;
         cp_async16(sKr_u + off, Kl + src);
-        cp_async16(sV_u + buf * TILE_BYTES + off, Vl + src);
-      } else {
-        *reinterpret_cast<uint4*>(sV + buf * TILE_BYTES + off) = make_uint4(0, 0, 0, 0);
+        cp_async16(sVr_u + off, Vl + src);
       }
     }
     for (int i = tid; i < 4 * 32; i += NT) {   // 4 page-start RoPE rows of 512 B
@@ -180,19 +192,38 @@ __global__ void __launch_bounds__(REP * RG * 32) attn_mma_kernel(AttnArgs a) {
                    a.rope_cs + (size_t)sPp[pbase + pg] * 64 + c * 2);
     }
   };
-  auto rotate_k = [&](int tile, int buf) {
+  // raw bf16 K and V of a tile -> fp16 operands: K rotated at each key's position, V converted;
+  // padding and out-of-range keys become zeros with position INT_MAX (masked)
+  auto prepare_kv = [&](int tile, int buf) {
     const int pbase = tile * 4 - win;
     for (int task = tid; task < KT * 8; task += NT) {
       const int key = task / 8, c = task % 8;
       const int pi = pbase + key / 16, r = key % 16;
       const bool valid = tile * 4 + key / 16 < npages && r < sPl[pi];
-      uint4 y1 = make_uint4(0, 0, 0, 0), y2 = y1;
-      if (valid)
-        rope8(*reinterpret_cast<const uint4*>(sKr + swz(key, c)), *reinterpret_cast<const uint4*>(sKr + swz(key, c + 8)),
-              sPg + (buf * 4 + key / 16) * 64 + 8 * c, sLo + r * 64 + 8 * c, 1.f, y1, y2);
-      uint8_t* base = sK + buf * TILE_BYTES;
-      *reinterpret_cast<uint4*>(base + swz(key, c)) = y1;
-      *reinterpret_cast<uint4*>(base + swz(key, c + 8)) = y2;
+      uint4 k1 = make_uint4(0, 0, 0, 0), k2 = k1, v1 = k1, v2 = k1;
+      if (valid) {
+        float a1[8], a2[8];
+        bf16x8_to_f32(*reinterpret_cast<const uint4*>(sKr + swz(key, c)), a1);
+        bf16x8_to_f32(*reinterpret_cast<const uint4*>(sKr + swz(key, c + 8)), a2);
+        rope8(a1, a2, sPg + (buf * 4 + key / 16) * 64 + 8 * c, sLo + r * 64 + 8 * c, 1.f, k1, k2);
+        float b1[8], b2[8];
+        bf16x8_to_f32(*reinterpret_cast<const uint4*>(sVr + swz(key, c)), b1);
+        bf16x8_to_f32(*reinterpret_cast<const uint4*>(sVr + swz(key, c + 8)), b2);
+        __half h1[8], h2[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          h1[e] = __float2half_rn(b1[e]);
+          h2[e] = __float2half_rn(b2[e]);
+        }
+        v1 = *reinterpret_cast<uint4*>(h1);
+        v2 = *reinterpret_cast<uint4*>(h2);
+      }
+      uint8_t* kb_ = sK + buf * TILE_BYTES;
+      uint8_t* vb_ = sV + buf * TILE_BYTES;
+      *reinterpret_cast<uint4*>(kb_ + swz(key, c)) = k1;
+      *reinterpret_cast<uint4*>(kb_ + swz(key, c + 8)) = k2;
+      *reinterpret_cast<uint4*>(vb_ + swz(key, c)) = v1;
+      *reinterpret_cast<uint4*>(vb_ + swz(key, c + 8)) = v2;
       if (c == 0) sPos[buf * KT + key] = valid ? sPp[pi] + r : INT_MAX;
     }
   };
@@ -200,7 +231,7 @@ __global__ void __launch_bounds__(REP * RG * 32) attn_mma_kernel(AttnArgs a) {
   if (ntiles > 0) issue_loads(0, 0);
   cp_async_wait_all();
   __syncthreads();
-  if (ntiles > 0) rotate_k(0, 0);
+  if (ntiles > 0) prepare_kv(0, 0);
   __syncthreads();
 
   float o[16][4];
@@ -269,8 +300,8 @@ __global__ void __launch_bounds__(REP * RG * 32) attn_mma_kernel(AttnArgs a) {
         const float p2 = exp2f(s[j][2] - ref1), p3 = exp2f(s[j][3] - ref1);
         rs0 += p0 + p1;
         rs1 += p2 + p3;
-        pf[j >> 1][(j & 1) * 2 + 0] = pack_bf16(p0, p1);
-        pf[j >> 1][(j & 1) * 2 + 1] = pack_bf16(p2, p3);
+        pf[j >> 1][(j & 1) * 2 + 0] = pack_h2(p0, p1);
+        pf[j >> 1][(j & 1) * 2 + 1] = pack_h2(p2, p3);
       }
       l0 = l0 * corr0 + rs0;
       l1 = l1 * corr1 + rs1;
@@ -282,7 +313,7 @@ __global__ void __launch_bounds__(REP * RG * 32) attn_mma_kernel(AttnArgs a) {
         o[i][3] *= corr1;
       }
       // O += P V
-      const uint32_t vb = sV_u + cur * TILE_BYTES;
+      const uint32_t vb = (uint32_t)__cvta_generic_to_shared(sV) + cur * TILE_BYTES;
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
         // A fragment of P for keys 16kk..16kk+15: {row0 k0-7, row1 k0-7, row0 k8-15, row1 k8-15}
@@ -297,9 +328,9 @@ __global__ void __launch_bounds__(REP * RG * 32) attn_mma_kernel(AttnArgs a) {
         }
       }
     }
-    cp_async_wait_all();   // raw K, V and page RoPE rows of the next tile have landed
+    cp_async_wait_all();   // raw K and V and the page RoPE rows of the next tile have landed
     __syncthreads();
-    if (has_next) rotate_k(tile + 1, nxt);
+    if (has_next) prepare_kv(tile + 1, nxt);
     __syncthreads();
   }
 
@@ -310,17 +341,17 @@ __global__ void __launch_bounds__(REP * RG * 32) attn_mma_kernel(AttnArgs a) {
   l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
   const int h = it.g * REP + hh;
   if (it.part < 0) {
-    __nv_bfloat16* out = (__nv_bfloat16*)a.out;
+    __half* out = (__half*)a.out;
     const float i0 = l0 > 0.f ? 1.f / l0 : 0.f, i1 = l1 > 0.f ? 1.f / l1 : 0.f;
 #pragma unroll
     for (int dn = 0; dn < 16; ++dn) {
       const int dcol = 8 * dn + 2 * t4;
       if (row0 < it.nrows)
         *reinterpret_cast<uint32_t*>(out + ((size_t)(it.row0 + row0) * a.H + h) * D + dcol) =
-            pack_bf16(o[dn][0] * i0, o[dn][1] * i0);
+            pack_h2(o[dn][0] * i0, o[dn][1] * i0);
       if (row1 < it.nrows)
         *reinterpret_cast<uint32_t*>(out + ((size_t)(it.row0 + row1) * a.H + h) * D + dcol) =
-            pack_bf16(o[dn][2] * i1, o[dn][3] * i1);
+            pack_h2(o[dn][2] * i1, o[dn][3] * i1);
     }
   } else {
     const size_t p0 = ((size_t)it.part * kAttnPartRows + row0) * REP + hh;
@@ -344,7 +375,7 @@ template <int REP, int RG>
 void launch_rep(const AttnArgs& a, cudaStream_t st) {
   constexpr int NW = REP * RG;
   static_assert(NW * 16 * D * 2 <= 2 * TILE_BYTES, "Q staging must fit the K operand buffers");
-  const size_t smem = 5 * TILE_BYTES + (16 + 2 * 4) * 64 * sizeof(float2) + (3 * WIN + 2 * KT) * sizeof(int);
+  const size_t smem = 6 * TILE_BYTES + (16 + 2 * 4) * 64 * sizeof(float2) + (3 * WIN + 2 * KT) * sizeof(int);
   static bool attr[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);

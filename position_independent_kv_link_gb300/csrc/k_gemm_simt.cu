@@ -10,8 +10,8 @@ namespace {
 
 constexpr int BN = 64, BT = 64, BK = 16;
 
-template <typename TIn>
-__global__ void __launch_bounds__(256) gemm_simt_kernel(const TIn* __restrict__ W, const TIn* __restrict__ X,
+template <typename TW, typename TX>
+__global__ void __launch_bounds__(256) gemm_simt_kernel(const TW* __restrict__ W, const TX* __restrict__ X,
                                                         float* __restrict__ Y, int N, int K, int T,
                                                         int k_per_split) {
   __shared__ float Ws[BK][BN + 4];
@@ -25,9 +25,9 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(const TIn* __restrict__ 
     for (int i = tid; i < BN * BK; i += 256) {
       const int r = i / BK, c = i % BK;
       const int n = n0 + r, k = k0 + c;
-      Ws[c][r] = (n < N && k < ke) ? to_f<TIn>(W[(size_t)n * K + k]) : 0.f;
+      Ws[c][r] = (n < N && k < ke) ? to_f<TW>(W[(size_t)n * K + k]) : 0.f;
       const int t = t0 + r;
-      Xs[c][r] = (t < T && k < ke) ? to_f<TIn>(X[(size_t)t * K + k]) : 0.f;
+      Xs[c][r] = (t < T && k < ke) ? to_f<TX>(X[(size_t)t * K + k]) : 0.f;
     }
     __syncthreads();
 #pragma unroll
@@ -59,17 +59,20 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(const TIn* __restrict__ 
 
 }  // namespace
 
-void launch_gemm_simt(int dtype, const void* W, const void* X, float* Y, int N, int K, int T, int splits,
-                      cudaStream_t st) {
+void launch_gemm_simt(int w_dtype, bool x_half, const void* W, const void* X, float* Y, int N, int K, int T,
+                      int splits, cudaStream_t st) {
   if (T <= 0 || N <= 0) return;
   int kps = (K + splits - 1) / splits;
   kps = (kps + BK - 1) / BK * BK;
   dim3 grid((N + BN - 1) / BN, (T + BT - 1) / BT, splits);
-  if (dtype == PIC_BF16)
-    gemm_simt_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>((const __nv_bfloat16*)W, (const __nv_bfloat16*)X, Y, N, K,
-                                                          T, kps);
+  if (w_dtype == PIC_BF16 && x_half)
+    gemm_simt_kernel<__nv_bfloat16, __half><<<grid, 256, 0, st>>>((const __nv_bfloat16*)W, (const __half*)X, Y, N, K,
+                                                                  T, kps);
+  else if (w_dtype == PIC_BF16)
+    gemm_simt_kernel<__nv_bfloat16, __nv_bfloat16><<<grid, 256, 0, st>>>((const __nv_bfloat16*)W,
+                                                                         (const __nv_bfloat16*)X, Y, N, K, T, kps);
   else
-    gemm_simt_kernel<float><<<grid, 256, 0, st>>>((const float*)W, (const float*)X, Y, N, K, T, kps);
+    gemm_simt_kernel<float, float><<<grid, 256, 0, st>>>((const float*)W, (const float*)X, Y, N, K, T, kps);
 }
 
 }  // namespace pic

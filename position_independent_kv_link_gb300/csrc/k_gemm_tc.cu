@@ -123,9 +123,10 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
   return d;
 }
 
-// Instruction descriptor of kind::f16: bf16 A and B (both K-major), fp32 D, M x N.
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+// Instruction descriptor of kind::f16: A and B both bf16 (fmt 1) or both fp16 (fmt 0),
+// both K-major, fp32 D, M x N.
+__host__ __device__ constexpr uint32_t idesc_f16kind(int M, int N, uint32_t fmt) {
+  return (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
 __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
@@ -173,6 +174,7 @@ struct TcParams {
   int nkb;           // k-blocks per tile
   int m_tiles;       // weight-row tiles
   int total;         // tiles * nkb work units (< 2^31, checked on the host)
+  uint32_t ab_fmt;   // operand format of both A and B: 1 = bf16, 0 = fp16
   uint32_t tmem_cols;
 };
 
@@ -279,7 +281,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait(smem_u32(full + j % p.S), (uint32_t)((j / p.S) & 1))) break;
   } else if (warp == 1 && lane == 0) {
     // ---------------- MMA issuer: one commit per k-block releases its stage
-    const uint32_t idesc = idesc_bf16(BM, p.BN);
+    const uint32_t idesc = idesc_f16kind(BM, p.BN, p.ab_fmt);
     Seg sg{0, lo, 0};
     int s = 0, st = 0;
     uint32_t ph = 0;
@@ -370,7 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 2) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(p.tmem_cols));
 }
 
-// [N][K] bf16 -> [N/128][K/64] tiles of 128 rows x 64 k, each stored exactly as a
+// [N][K] bf16 -> [N/128][K/64] fp16 tiles of 128 rows x 64 k, each stored exactly as a
 // 128-byte-swizzled K-major shared-memory tile (16-byte chunk j of row r at slot j ^ (r % 8)).
 __global__ void pack_sw128_kernel(const uint4* __restrict__ W, uint4* __restrict__ P, int K, int nkb) {
   const int tile = blockIdx.x;            // mt * nkb + kb
@@ -378,7 +380,12 @@ __global__ void pack_sw128_kernel(const uint4* __restrict__ W, uint4* __restrict
   for (int i = threadIdx.x; i < BM * 8; i += blockDim.x) {
     const int r = i / 8, j = i % 8;
     const uint4 v = W[((size_t)(mt * BM + r) * K + kb * BK) / 8 + j];
-    P[(size_t)tile * (A_STAGE / 16) + r * 8 + (j ^ (r & 7))] = v;
+    const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&v);
+    uint4 o;
+    __half2* h = reinterpret_cast<__half2*>(&o);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) h[e] = __float22half2_rn(__bfloat1622float2(b[e]));
+    P[(size_t)tile * (A_STAGE / 16) + r * 8 + (j ^ (r & 7))] = o;
   }
 }
 
@@ -408,15 +415,16 @@ bool make_map_f32(CUtensorMap* m, void* base, int rows, int cols) {
   return r == CUDA_SUCCESS;
 }
 
-// bf16 K-major operand [rows][K]; box = 64 K x box_rows rows, 128-byte swizzle
-bool make_map(CUtensorMap* m, const void* base, int rows, int K, int box_rows) {
+// 16-bit K-major operand [rows][K] (bf16 or fp16); box = 64 K x box_rows rows, 128-byte swizzle
+bool make_map(CUtensorMap* m, const void* base, int rows, int K, int box_rows, bool f16 = false) {
   auto enc = get_encode();
   if (!enc) return false;
   cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)K * 2};
   cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+  CUresult r = enc(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                   const_cast<void*>(base), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
@@ -451,6 +459,7 @@ pic_status tc_gemm_launch(const void* W, bool packed, const void* X, float* Y, i
     return fail(PIC_ERR_INVALID_ARG, "tcgen05 gemm: operands not 16-byte aligned");
   TcParams p{};
   p.w_packed = packed ? static_cast<const uint8_t*>(W) : nullptr;
+  p.ab_fmt = packed ? 0u : 1u;   // the packed copy is fp16 (X too); the plain layout is bf16
   p.N = N;
   p.K = K;
   p.T = T;
@@ -469,7 +478,8 @@ pic_status tc_gemm_launch(const void* W, bool packed, const void* X, float* Y, i
   while ((int)p.tmem_cols < 2 * p.BN) p.tmem_cols <<= 1;
   CUtensorMap mw, mx, my;
   std::memset(&mw, 0, sizeof(mw));
-  if ((!packed && !make_map(&mw, W, N, K, BM)) || !make_map(&mx, X, T, K, p.BN) || !make_map_f32(&my, Y, T, N))
+  if ((!packed && !make_map(&mw, W, N, K, BM)) || !make_map(&mx, X, T, K, p.BN, packed) ||
+      !make_map_f32(&my, Y, T, N))
     return fail(PIC_ERR_CUDA, "cuTensorMapEncodeTiled failed");
   const size_t smem =
       1024 + (size_t)p.S * (A_STAGE + b_stage) + 2 * EPI_BYTES + (2 * p.S + 6) * 8 + 16;

@@ -30,10 +30,10 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
 }
 
 // h = E[tok]; x = rmsnorm(h) * g.  Row cached in dynamic shared memory (fp32).
-template <typename T>
+template <typename T, typename A>
 __global__ void embed_norm_kernel(int d, const T* __restrict__ E, const int* __restrict__ tok,
                                   const float* __restrict__ gain, float eps, float* __restrict__ h,
-                                  T* __restrict__ x) {
+                                  A* __restrict__ x) {
   extern __shared__ float row[];
   __shared__ float red[32];
   const int t = blockIdx.x;
@@ -48,7 +48,7 @@ __global__ void embed_norm_kernel(int d, const T* __restrict__ E, const int* __r
   const float r = rsqrtf(ss / d + eps);
   for (int i = threadIdx.x; i < d; i += blockDim.x) {
     h[(size_t)t * d + i] = row[i];
-    x[(size_t)t * d + i] = from_f<T>(row[i] * r * gain[i]);
+    x[(size_t)t * d + i] = from_f<A>(row[i] * r * gain[i]);
   }
 }
 
@@ -68,6 +68,15 @@ __device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16* dst, float4
 }
 
 // Reads 4 accumulator floats and clears them for the next GEMM that adds into the buffer.
+template <>
+__device__ __forceinline__ void store4<__half>(__half* dst, float4 v) {
+  __half2 a = __floats2half2_rn(v.x, v.y), b = __floats2half2_rn(v.z, v.w);
+  uint2 u;
+  u.x = *reinterpret_cast<uint32_t*>(&a);
+  u.y = *reinterpret_cast<uint32_t*>(&b);
+  *reinterpret_cast<uint2*>(dst) = u;
+}
+
 __device__ __forceinline__ float4 take4(float* __restrict__ acc, size_t off) {
   float4* p = reinterpret_cast<float4*>(acc + off);
   const float4 v = *p;
@@ -75,11 +84,11 @@ __device__ __forceinline__ float4 take4(float* __restrict__ acc, size_t off) {
   return v;
 }
 
-// QKV epilogue: q -> [T][H*D]; pre-RoPE k, v -> their page slot of this layer. The
+// QKV epilogue: q -> [T][H*D] fp32; pre-RoPE k, v -> their page slot of this layer. The
 // accumulator [T][N] is cleared behind the read. grid (T, ceil(N / 1024)); a thread owns 4
 // consecutive columns (one head).
 template <typename T>
-__global__ void qkv_epilogue_kernel(int H, int G, int D, float* __restrict__ acc, T* __restrict__ q,
+__global__ void qkv_epilogue_kernel(int H, int G, int D, float* __restrict__ acc, float* __restrict__ q,
                                     const int* __restrict__ slot, T* __restrict__ kl, T* __restrict__ vl) {
   const int t = blockIdx.x;
   const int N = (H + 2 * G) * D;
@@ -87,7 +96,7 @@ __global__ void qkv_epilogue_kernel(int H, int G, int D, float* __restrict__ acc
   if (n >= N) return;
   const float4 v = take4(acc, (size_t)t * N + n);
   if (n < H * D) {
-    store4<T>(q + (size_t)t * H * D + n, v);
+    store4<float>(q + (size_t)t * H * D + n, v);
   } else {
     const int s_ = slot[t];
     const int blk = s_ / kBlock, r = s_ % kBlock;
@@ -183,22 +192,23 @@ void launch_embed_norm(int dtype, int T, int d, const void* embed, const int* to
   if (T <= 0) return;
   const size_t sm = d * sizeof(float);
   if (dtype == PIC_BF16)
-    embed_norm_kernel<__nv_bfloat16><<<T, kRowThreads, sm, st>>>(d, (const __nv_bfloat16*)embed, tok, gain, eps, h,
-                                                                 (__nv_bfloat16*)x);
+    embed_norm_kernel<__nv_bfloat16, __half><<<T, kRowThreads, sm, st>>>(d, (const __nv_bfloat16*)embed, tok, gain,
+                                                                         eps, h, (__half*)x);
   else
-    embed_norm_kernel<float><<<T, kRowThreads, sm, st>>>(d, (const float*)embed, tok, gain, eps, h, (float*)x);
+    embed_norm_kernel<float, float><<<T, kRowThreads, sm, st>>>(d, (const float*)embed, tok, gain, eps, h,
+                                                                (float*)x);
 }
 
-void launch_qkv_epilogue(int dtype, int T, int H, int G, int D, float* acc, void* q, const int* slot, void* k_layer,
+void launch_qkv_epilogue(int dtype, int T, int H, int G, int D, float* acc, float* q, const int* slot, void* k_layer,
                          void* v_layer, cudaStream_t st) {
   if (T <= 0) return;
   const int N = (H + 2 * G) * D;
   dim3 grid(T, (N / 4 + kRowThreads - 1) / kRowThreads);
   if (dtype == PIC_BF16)
-    qkv_epilogue_kernel<__nv_bfloat16><<<grid, kRowThreads, 0, st>>>(H, G, D, acc, (__nv_bfloat16*)q, slot,
+    qkv_epilogue_kernel<__nv_bfloat16><<<grid, kRowThreads, 0, st>>>(H, G, D, acc, q, slot,
                                                                      (__nv_bfloat16*)k_layer, (__nv_bfloat16*)v_layer);
   else
-    qkv_epilogue_kernel<float><<<grid, kRowThreads, 0, st>>>(H, G, D, acc, (float*)q, slot, (float*)k_layer,
+    qkv_epilogue_kernel<float><<<grid, kRowThreads, 0, st>>>(H, G, D, acc, q, slot, (float*)k_layer,
                                                              (float*)v_layer);
 }
 
@@ -208,8 +218,8 @@ void launch_rmsnorm_rows(int dtype, int T, int d, const float* h, const float* g
   if (T <= 0) return;
   const int thr = std::min(512, std::max(128, (d / 4 + 31) / 32 * 32));
   if (dtype == PIC_BF16)
-    rmsnorm_rows_kernel<__nv_bfloat16><<<T, thr, 0, st>>>(d, h, gain, eps, (__nv_bfloat16*)x, final_layer, out_row,
-                                                          hidden_out, lg_row, (__nv_bfloat16*)lm_x);
+    rmsnorm_rows_kernel<__half><<<T, thr, 0, st>>>(d, h, gain, eps, (__half*)x, final_layer, out_row, hidden_out,
+                                                   lg_row, (__half*)lm_x);
   else
     rmsnorm_rows_kernel<float><<<T, thr, 0, st>>>(d, h, gain, eps, (float*)x, final_layer, out_row, hidden_out,
                                                   lg_row, (float*)lm_x);
@@ -219,7 +229,7 @@ void launch_swiglu(int dtype, int T, int F, float* acc, void* act, cudaStream_t 
   if (T <= 0) return;
   dim3 grid(T, (F / 4 + kRowThreads - 1) / kRowThreads);
   if (dtype == PIC_BF16)
-    swiglu_kernel<__nv_bfloat16><<<grid, kRowThreads, 0, st>>>(F, acc, (__nv_bfloat16*)act);
+    swiglu_kernel<__half><<<grid, kRowThreads, 0, st>>>(F, acc, (__half*)act);
   else
     swiglu_kernel<float><<<grid, kRowThreads, 0, st>>>(F, acc, (float*)act);
 }

@@ -131,7 +131,7 @@ pic_status pic_op_attention_noalloc(int32_t dtype, int32_t T, int32_t n_heads, i
   a.H = n_heads;
   a.G = n_kv_heads;
   a.D = head_dim;
-  a.q = q;
+  a.q = (const float*)q;
   a.q_pos = di;
   a.k_layer = k_layer;
   a.v_layer = v_layer;

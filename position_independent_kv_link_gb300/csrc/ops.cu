@@ -51,7 +51,7 @@ pic_status pic_op_gemm(int32_t dtype, const void* W, const void* X, float* Y, in
     pic_status e = tc_gemm_run(W, X, Y, N, K, T, st);
     if (e != PIC_OK) return e;
   } else {
-    launch_gemm_simt(dtype, W, X, Y, N, K, T, 1, st);
+    launch_gemm_simt(dtype, false, W, X, Y, N, K, T, 1, st);
   }
   PIC_CUDA(cudaGetLastError());
   return PIC_OK;
@@ -136,7 +136,7 @@ pic_status pic_op_attention(int32_t dtype, int32_t T, int32_t n_heads, int32_t n
   a.H = n_heads;
   a.G = n_kv_heads;
   a.D = head_dim;
-  a.q = q;
+  a.q = (const float*)q;
   a.q_pos = di;
   a.k_layer = k_layer;
   a.v_layer = v_layer;

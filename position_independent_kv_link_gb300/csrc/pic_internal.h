@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -31,23 +32,32 @@ template <> __device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 v
 template <typename T> __device__ __forceinline__ T from_f(float v);
 template <> __device__ __forceinline__ float from_f<float>(float v) { return v; }
 template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float v) { return __float2bfloat16_rn(v); }
+template <> __device__ __forceinline__ float to_f<__half>(__half v) { return __half2float(v); }
+template <> __device__ __forceinline__ __half from_f<__half>(float v) { return __float2half_rn(v); }
 
+// Storage of weights and KV follows the model dtype. For bf16 models the activations fed
+// to the tensor cores (normed hidden rows, attention output, SwiGLU output) are fp16 and
+// the packed weight copy is fp16 too (every bf16 weight above 2^-14 in magnitude is exact
+// in fp16): 3 more mantissa bits per rounding at the same tensor-core rate. Accumulators,
+// norms, softmax and the residual stream are fp32 throughout; q stays fp32 until RoPE.
 inline size_t dtype_size(int dtype) { return dtype == PIC_BF16 ? 2 : 4; }
+inline size_t act_size(int dtype) { return dtype == PIC_BF16 ? 2 : 4; }
 
 // ------------------------------------------------------------------ row-wise kernels (k_rows.cu)
-// h[t] = E[tok[t]] (fp32); x[t] = RMSNorm(h[t]) * gain in the model dtype.
+// h[t] = E[tok[t]] (fp32); x[t] = RMSNorm(h[t]) * gain in the activation type.
 void launch_embed_norm(int dtype, int T, int d, const void* embed, const int* tok, const float* gain, float eps,
                        float* h, void* x, cudaStream_t st);
 // QKV epilogue: reads (and clears) the fp32 accumulator [T][(H+2G)D], writes q [T][H*D]
-// (dtype) and the pre-RoPE k, v rows into their page slots of one layer of the pools.
-void launch_qkv_epilogue(int dtype, int T, int H, int G, int D, float* acc, void* q, const int* slot, void* k_layer,
+// (fp32) and the pre-RoPE k, v rows (model dtype) into their page slots of one layer.
+void launch_qkv_epilogue(int dtype, int T, int H, int G, int D, float* acc, float* q, const int* slot, void* k_layer,
                          void* v_layer, cudaStream_t st);
-// y = RMSNorm(h[t]) * gain. Not final: x[t] = y (dtype). Final: hidden_out[out_row[t]] = y
-// (fp32) when out_row[t] >= 0 and lm_x[lg_row[t]] = y (dtype) when lg_row[t] >= 0.
+// y = RMSNorm(h[t]) * gain. Not final: x[t] = y (activation type). Final: hidden_out[out_row[t]]
+// = y (fp32) when out_row[t] >= 0 and lm_x[lg_row[t]] = y (activation type) when lg_row[t] >= 0.
 void launch_rmsnorm_rows(int dtype, int T, int d, const float* h, const float* gain, float eps, void* x,
                          bool final_layer, const int* out_row, float* hidden_out, const int* lg_row, void* lm_x,
                          cudaStream_t st);
-// act[t][j] = silu(gate) * up from the accumulator [T][2F] (gate cols, then up cols), cleared behind.
+// act[t][j] = silu(gate) * up (activation type) from the accumulator [T][2F] (gate cols, then
+// up cols), cleared behind.
 void launch_swiglu(int dtype, int T, int F, float* acc, void* act, cudaStream_t st);
 // For each pair i: copy block src[i] -> dst[i] in every layer of both pools.
 void launch_copy_blocks(int n_pairs, const int* pairs, int n_layers, int num_blocks_total, size_t block_bytes,
@@ -58,17 +68,19 @@ void launch_import_kv(int dtype, int n_layers, int n, int G, int D, const void* 
 
 // ------------------------------------------------------------------ GEMMs
 // Y[T][N] (fp32) += X[T][K] . W[N][K]^T; K split evenly over `splits` CTAs (atomic adds).
-void launch_gemm_simt(int dtype, const void* W, const void* X, float* Y, int N, int K, int T, int splits,
-                      cudaStream_t st);
+// W in `w_dtype` (PIC_F32 / PIC_BF16); X in `x_half` ? fp16 : the same type as W.
+void launch_gemm_simt(int w_dtype, bool x_half, const void* W, const void* X, float* Y, int N, int K, int T,
+                      int splits, cudaStream_t st);
 
 // Shape rules of the tcgen05 kernel (N % 128 == 0, K % 64 == 0).
 bool tc_gemm_supported(int N, int K, int T);
-// Y[T][N] (fp32, 16-byte aligned) += X[T][K] . W[N][K]^T on tcgen05 (persistent stream-K).
+// Y[T][N] (fp32, 16-byte aligned) += X[T][K] . W[N][K]^T on tcgen05 (persistent stream-K),
+// W and X bf16.
 pic_status tc_gemm_run(const void* W, const void* X, float* Y, int N, int K, int T, cudaStream_t st);
-// Same with the weights in the tile layout written by tc_pack_weight.
+// Same with fp16 weights in the tile layout written by tc_pack_weight and fp16 X.
 pic_status tc_gemm_run_packed(const void* Wp, const void* X, float* Y, int N, int K, int T, cudaStream_t st);
-// [N][K] bf16 -> N*K*2 bytes of 16 KB tiles (128 rows x 64 k, 128-byte swizzled image), tile (mt, kb) at
-// (mt * K/64 + kb) * 16 KB.
+// [N][K] bf16 -> N*K*2 bytes of fp16 16 KB tiles (128 rows x 64 k, 128-byte swizzled image),
+// tile (mt, kb) at (mt * K/64 + kb) * 16 KB.
 pic_status tc_pack_weight(const void* W, void* out, int N, int K, cudaStream_t st);
 // Reads and clears the device flag set when a tcgen05 kernel gave up a bounded wait.
 pic_status tc_check_timeout();
@@ -85,7 +97,7 @@ struct AttnCombine {   // merge `nparts` partial results of rows [row0, row0+nro
 struct AttnArgs {
   int dtype, H, G, D;
   int rb;                   // rows per work item of this plan (16 or 32)
-  const void* q;            // [T][H][D] pre-RoPE
+  const float* q;           // [T][H][D] pre-RoPE, fp32
   const int* q_pos;         // [T]
   const void* k_layer;      // [nb][G][16][D]
   const void* v_layer;
@@ -93,7 +105,7 @@ struct AttnArgs {
   const int* page_pos;
   const int* page_len;
   const float2* rope_cs;    // [max_pos][D/2]
-  void* out;                // [T][H][D]
+  void* out;                // [T][H][D] activation type (fp16 for bf16 KV, fp32 for fp32 KV)
   float* part_o;            // [parts][kAttnPartRows][rep][D]
   float* part_ml;           // [parts][kAttnPartRows][rep][2]
   const AttnItem* items;

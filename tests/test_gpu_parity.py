@@ -46,7 +46,7 @@ def test_gemm_bf16_packed_weights(N, K, T):
     """The layout the model repacks its matrices into, through the packed tcgen05 path."""
     from position_independent_kv_link_gb300 import gemm_packed, pack_weight
     W = pi.randn((N, K), ("gemmWp", N, K), 0.05, torch.bfloat16)
-    X = pi.randn((T, K), ("gemmXp", T, K), 1.0, torch.bfloat16)
+    X = pi.randn((T, K), ("gemmXp", T, K), 1.0, torch.float16)
     Y = gemm_packed(pack_weight(W.cuda()), N, K, X.cuda())
     torch.cuda.synchronize()
     assert rel_err(Y, X.double() @ W.double().T) < 1e-5
@@ -83,7 +83,7 @@ def _attn_case(dtype, D, H, G, lens, qlen, k_first, seed):
     pblk = [int(perm[i]) for i in range(nb)]
     K = pi.randn((nb + 3, G, 16, D), ("attK", seed), 1.0, dtype)
     V = pi.randn((nb + 3, G, 16, D), ("attV", seed), 1.0, dtype)
-    q = pi.randn((len(sel), H, D), ("attQ", seed), 1.0, dtype)
+    q = pi.randn((len(sel), H, D), ("attQ", seed), 1.0, torch.float32)
     return q, np.array(sel), K, V, (np.array(pblk), np.array(ppos), np.array(plen)), off
 
 

@@ -19,7 +19,7 @@ pytestmark = pytest.mark.gpu
 
 
 def _case(seed):
-    """Ragged chunks + a query over scattered pages (bf16, 8 Q / 2 KV heads, head_dim 128)."""
+    """Ragged chunks + a query over scattered pages (bf16 KV, 8 Q / 2 KV heads, head_dim 128; fp32 q)."""
     rng = np.random.default_rng(seed)
     lens, qlen = [300, 37, 512, 16, 200], 40
     pblk, ppos, plen, sel = [], [], [], []
@@ -35,7 +35,7 @@ def _case(seed):
     pblk = [int(b) for b in rng.permutation(nb)[:len(pblk)]]
     K = pi.randn((nb, 2, 16, 128), ("noallocK", seed), 1.0, torch.bfloat16).cuda()
     V = pi.randn((nb, 2, 16, 128), ("noallocV", seed), 1.0, torch.bfloat16).cuda()
-    q = pi.randn((len(sel), 8, 128), ("noallocQ", seed), 1.0, torch.bfloat16).cuda()
+    q = pi.randn((len(sel), 8, 128), ("noallocQ", seed), 1.0, torch.float32).cuda()
     i32 = lambda a: np.ascontiguousarray(np.asarray(a, dtype=np.int32))
     return q, i32(sel), K, V, i32(pblk), i32(ppos), i32(plen), off
 
@@ -54,13 +54,13 @@ def test_noalloc_attention_matches_regular_entry_point():
         q, qpos, K, V, blk, ppos, plen, n_pos = _case(seed)
         rope = api.rope_table(n_pos + 16, 128, 500000.0)
         T, n_pages = q.shape[0], len(blk)
-        ref = torch.empty_like(q)
+        ref = torch.empty(q.shape, dtype=torch.float16, device="cuda")
         nb = lib.pic_op_attention_scratch_bytes(T, 8, 2, 128, n_pages)
         scratch = torch.empty(nb, dtype=torch.uint8, device="cuda")
         L.check(lib.pic_op_attention(L.PIC_BF16, T, 8, 2, 128, q.data_ptr(), P(qpos), K.data_ptr(), V.data_ptr(),
                                      P(blk), P(ppos), P(plen), n_pages, K.shape[0], rope.data_ptr(), rope.shape[0],
                                      ref.data_ptr(), scratch.data_ptr(), nb, sp))
-        got = torch.full_like(q, float("nan"))
+        got = torch.full(q.shape, float("nan"), dtype=torch.float16, device="cuda")
         L.check(lib.pic_op_attention_noalloc(L.PIC_BF16, T, 8, 2, 128, q.data_ptr(), P(qpos), K.data_ptr(),
                                              V.data_ptr(), P(blk), P(ppos), P(plen), n_pages, K.shape[0],
                                              rope.data_ptr(), rope.shape[0], got.data_ptr(), sp))
@@ -82,10 +82,10 @@ def test_noalloc_attention_rejects_oversized_work():
     blk = np.arange(n_pages, dtype=np.int32)
     ppos = (16 * np.arange(n_pages)).astype(np.int32)
     plen = np.full(n_pages, 16, dtype=np.int32)
-    q = torch.zeros((T, 32, 128), dtype=torch.bfloat16, device="cuda")
+    q = torch.zeros((T, 32, 128), dtype=torch.float32, device="cuda")
     K = torch.zeros((n_pages, 8, 16, 128), dtype=torch.bfloat16, device="cuda")
     rope = api.rope_table(16 * n_pages + 16, 128, 500000.0)
-    out = torch.zeros_like(q)
+    out = torch.zeros((T, 32, 128), dtype=torch.float16, device="cuda")
     P = lambda a: a.ctypes.data_as(L.PI32)
     st = lib.pic_op_attention_noalloc(L.PIC_BF16, T, 32, 8, 128, q.data_ptr(), P(qpos), K.data_ptr(), K.data_ptr(),
                                       P(blk), P(ppos), P(plen), n_pages, n_pages, rope.data_ptr(), rope.shape[0],
