@@ -844,7 +844,9 @@ int64_t pic_store_launch_count(const pic_store* s) { return s ? s->launches : -1
 pic_status pic_sync(pic_store* s, pic_stream_t stream) {
   (void)s;
   PIC_CUDA(cudaStreamSynchronize((cudaStream_t)stream));
-  return tc_check_timeout();
+  const pic_status a = attn_check_timeout();
+  const pic_status g = tc_check_timeout();
+  return a != PIC_OK ? a : g;
 }
 
 }  // extern "C"

@@ -3,8 +3,9 @@
 // absolute position, GQA head sharing, split over page ranges with an LSE merge.
 //
 // This file holds the generic warp-per-(row, head) kernel (any dtype, D = 64 or 128),
-// the split merge and the host planner. The bf16 D=128 tensor-core kernel lives in
-// k_attn_mma.cu and takes the same work items.
+// the split merge and the host planner. The bf16 D=128 kernels take the same work
+// items: k_attn_tc.cu (tcgen05, 4 query heads per KV head) and k_attn_mma.cu
+// (mma.sync, 1, 2 or 8 query heads per KV head).
 #include <algorithm>
 #include <cmath>
 
@@ -13,6 +14,8 @@
 namespace pic {
 
 void launch_attention_mma(const AttnArgs& a, cudaStream_t st);  // k_attn_mma.cu
+bool tc_attention_supported(int dtype, int D, int rep);          // k_attn_tc.cu
+void launch_attention_tc(const AttnArgs& a, cudaStream_t st);
 
 namespace {
 
@@ -159,7 +162,14 @@ bool use_mma(int dtype, int D, int rep) { return dtype == PIC_BF16 && D == 128 &
 int attention_rows_per_block(int dtype, int D, int rep) { return (use_mma(dtype, D, rep) && rep <= 4) ? 32 : 16; }
 
 void launch_attention(const AttnArgs& a, cudaStream_t st) {
-  if (use_mma(a.dtype, a.D, a.H / a.G))
+  if (tc_attention_supported(a.dtype, a.D, a.H / a.G)) {
+    launch_attention_tc(a, st);
+    if (a.n_combines > 0) {
+      AttnArgs b = a;
+      b.n_items = 0;  // merge only
+      launch_attention_simt(b, st);
+    }
+  } else if (use_mma(a.dtype, a.D, a.H / a.G))
     launch_attention_mma(a, st);
   else
     launch_attention_simt(a, st);

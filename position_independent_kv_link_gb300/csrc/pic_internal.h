@@ -82,8 +82,10 @@ pic_status tc_gemm_run_packed(const void* Wp, const void* X, float* Y, int N, in
 // [N][K] bf16 -> N*K*2 bytes of fp16 16 KB tiles (128 rows x 64 k, 128-byte swizzled image),
 // tile (mt, kb) at (mt * K/64 + kb) * 16 KB.
 pic_status tc_pack_weight(const void* W, void* out, int N, int K, cudaStream_t st);
-// Reads and clears the device flag set when a tcgen05 kernel gave up a bounded wait.
+// Reads and clears the device flag set when a tcgen05 GEMM gave up a bounded wait.
 pic_status tc_check_timeout();
+// Same for the tcgen05 attention kernel (k_attn_tc.cu).
+pic_status attn_check_timeout();
 
 // ------------------------------------------------------------------ attention (k_attn.cu)
 constexpr int kAttnPartRows = 32;          // row slots of one split-partial slab

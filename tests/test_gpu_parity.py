@@ -89,7 +89,8 @@ def _attn_case(dtype, D, H, G, lens, qlen, k_first, seed):
 
 @pytest.mark.parametrize("dtype,D,H,G", [(torch.float32, 64, 4, 4), (torch.float32, 128, 8, 2),
                                          (torch.bfloat16, 128, 8, 2), (torch.bfloat16, 128, 32, 8),
-                                         (torch.bfloat16, 64, 4, 1)])
+                                         (torch.bfloat16, 64, 4, 1), (torch.bfloat16, 128, 8, 8),
+                                         (torch.bfloat16, 128, 8, 4), (torch.bfloat16, 128, 16, 2)])
 def test_paged_attention_fused_rope(dtype, D, H, G):
     from position_independent_kv_link_gb300 import attention, rope_table
     base = 500000.0 if D == 128 else 10000.0
