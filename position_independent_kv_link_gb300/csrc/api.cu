@@ -112,7 +112,7 @@ struct pic_store {
   char* ws = nullptr;
   float* h = nullptr;
   void* x = nullptr;
-  float* q = nullptr;        // [max_rows][H*D] fp32, pre-RoPE
+  float* q = nullptr;        // [max_rows][H*D] fp32 pre-RoPE, or fp16 rotated (tensor-core attention)
   void* attn = nullptr;
   void* act = nullptr;
   void* lm_x = nullptr;
@@ -124,6 +124,7 @@ struct pic_store {
   int32_t* meta_d = nullptr;
   size_t meta_cap = 0;  // int32 elements
   float2* rope_cs = nullptr;
+  std::vector<CUtensorMap> kv_maps;  // per layer: K map, V map (tensor-core attention), built on first use
   int32_t* meta_h = nullptr;  // pinned staging
   cudaEvent_t meta_ev = nullptr;
   bool meta_ev_pending = false;
@@ -228,6 +229,7 @@ pic_status run_forward_impl(pic_store* s, const Batch& b, float* hidden_out, flo
   pin.G = G;
   pin.num_sms = s->m->num_sms;
   pin.rows_per_block = attention_rows_per_block(dt, D, H / G);
+  pin.persistent = attention_persistent(dt, D, H / G);
   std::vector<AttnItem> items;
   std::vector<AttnCombine> combs;
   int n_parts = 0;
@@ -294,6 +296,19 @@ pic_status run_forward_impl(pic_store* s, const Batch& b, float* hidden_out, flo
   const int att_launches = 1 + (combs.empty() ? 0 : 1);
 
   AttnArgs aa{};
+  const bool att_tc = attention_persistent(dt, D, H / G);
+  if (att_tc) {
+    if (s->kv_maps.empty()) {
+      s->kv_maps.resize(2 * (size_t)c.n_layers);
+      for (int l = 0; l < c.n_layers; ++l)
+        if (!attn_kv_map(&s->kv_maps[2 * l], s->k_layer(l), s->blocks_total(), G) ||
+            !attn_kv_map(&s->kv_maps[2 * l + 1], s->v_layer(l), s->blocks_total(), G)) {
+          s->kv_maps.clear();
+          return fail(PIC_ERR_CUDA, "cuTensorMapEncodeTiled failed for the KV pools");
+        }
+    }
+    if (!attn_q_map(&aa.qmap, s->q, T, H)) return fail(PIC_ERR_CUDA, "cuTensorMapEncodeTiled failed for q");
+  }
   aa.dtype = dt;
   aa.rb = pin.rows_per_block;
   aa.H = H;
@@ -331,12 +346,17 @@ pic_status run_forward_impl(pic_store* s, const Batch& b, float* hidden_out, flo
     if ((e = run_gemm(s->m->wqkv[l], pk(s->m->pqkv, l), s->x, s->qkv_acc, qkv, d, T)) != PIC_OK) return e;
     {
       Rec r(s, st, PIC_PROF_ROWWISE, dT * dQKV * (8 + es), 0, 1);
-      launch_qkv_epilogue(dt, T, H, G, D, s->qkv_acc, s->q, d_slot, s->k_layer(l), s->v_layer(l), st);
+      launch_qkv_epilogue(dt, T, H, G, D, s->qkv_acc, s->q, d_slot, s->k_layer(l), s->v_layer(l), d_pos, s->rope_cs,
+                          att_tc ? (__half*)s->q : nullptr, st);
     }
     // compile keeps only KV: the last layer's attention and MLP feed nothing stored
     if (b.compile && l == c.n_layers - 1) break;
     aa.k_layer = s->k_layer(l);
     aa.v_layer = s->v_layer(l);
+    if (att_tc) {
+      aa.kmap = s->kv_maps[2 * l];
+      aa.vmap = s->kv_maps[2 * l + 1];
+    }
     {
       Rec r(s, st, PIC_PROF_ATTENTION, att_bytes, att_flops, att_launches);
       launch_attention(aa, st);

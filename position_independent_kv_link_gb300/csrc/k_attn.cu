@@ -161,6 +161,16 @@ bool use_mma(int dtype, int D, int rep) { return dtype == PIC_BF16 && D == 128 &
 
 int attention_rows_per_block(int dtype, int D, int rep) { return (use_mma(dtype, D, rep) && rep <= 4) ? 32 : 16; }
 
+bool attention_persistent(int dtype, int D, int rep) { return tc_attention_supported(dtype, D, rep); }
+
+pic_status attention_prepare_tc(AttnArgs& a, int T, int pool_blocks, __half* q16, cudaStream_t st) {
+  launch_rope_q16(T, a.H, a.q, a.q_pos, a.rope_cs, q16, st);
+  if (!attn_q_map(&a.qmap, q16, T, a.H) || !attn_kv_map(&a.kmap, a.k_layer, pool_blocks, a.G) ||
+      !attn_kv_map(&a.vmap, a.v_layer, pool_blocks, a.G))
+    return fail(PIC_ERR_CUDA, "cuTensorMapEncodeTiled failed for the attention operands");
+  return PIC_OK;
+}
+
 void launch_attention(const AttnArgs& a, cudaStream_t st) {
   if (tc_attention_supported(a.dtype, a.D, a.H / a.G)) {
     launch_attention_tc(a, st);
@@ -200,8 +210,18 @@ void plan_attention(const AttnPlanInput& in, std::vector<AttnItem>& items, std::
       total += (long long)(pe - in.seq_page_begin[s]);
     }
   }
-  const long long target = std::max<long long>(1, 4LL * in.num_sms / std::max(1, in.G));
-  int P = (int)std::max<long long>(4, (total + target - 1) / target);
+  // Pages per split part. One CTA per item: about four items per SM. Persistent kernel: about
+  // two items per CTA, in whole 64-key tiles (4 pages), so fewer partial results are merged.
+  const int G = std::max(1, in.G);
+  int P;
+  if (in.persistent) {
+    const long long want = 2LL * std::max(1, in.num_sms);
+    P = (int)std::max<long long>(8, (total * G + want - 1) / want);
+    P = (P + 3) / 4 * 4;
+  } else {
+    const long long target = std::max<long long>(1, 4LL * in.num_sms / G);
+    P = (int)std::max<long long>(4, (total + target - 1) / target);
+  }
   items.clear();
   combines.clear();
   n_parts = 0;
@@ -224,6 +244,17 @@ void plan_attention(const AttnPlanInput& in, std::vector<AttnItem>& items, std::
   // Heaviest items first so the long ranges start early.
   std::stable_sort(items.begin(), items.end(),
                    [](const AttnItem& x, const AttnItem& y) { return (x.page1 - x.page0) > (y.page1 - y.page0); });
+  if (in.persistent && !items.empty()) {
+    // CTA c takes items c, c + n, c + 2n, ...: deal the sorted items in snake order
+    // (round k runs over the CTAs backwards when k is odd) so the loads even out.
+    const int n = std::min<int>((int)items.size(), std::max(1, in.num_sms));
+    std::vector<AttnItem> dealt(items.size());
+    for (size_t k = 0; k * n < items.size(); ++k) {
+      const int m = (int)std::min<size_t>(n, items.size() - k * n);
+      for (int c = 0; c < m; ++c) dealt[k * n + c] = items[k * n + ((k & 1) ? m - 1 - c : c)];
+    }
+    items.swap(dealt);
+  }
 }
 
 void rope_table_host(int n_pos, int D, double base, std::vector<float2>& out) {

@@ -1,27 +1,36 @@
 // tcgen05 paged attention with fused RoPE for bf16 KV, head_dim 128, 4 query heads per KV head.
 //
-// One CTA = one work item: up to 32 consecutive query rows of one sequence x the 4 query
-// heads that share KV head g x a run of pages. The 32 rows x 4 heads are exactly one
-// M = 128 MMA tile (row m = head * 32 + row), so each 64-key tile of K and V is staged
-// once and read by the tensor cores once for all of them.
+// Persistent: CTA b walks the work items b, b + grid, b + 2 grid, ... (the planner deals them
+// in that order). An item is up to 32 consecutive query rows of one sequence x the 4 query
+// heads sharing KV head g x a run of pages. The 32 rows x 4 heads form one M = 128 MMA tile
+// (row m = head * 32 + row), so each 64-key tile (4 pages) of K and V is staged once for all.
 //
-//   warps 0-3  softmax: thread = one MMA row = one TMEM lane. Reads its row of S from
-//              TMEM, masks keys after its position (and padding), keeps a running
-//              reference maximum, writes P = 2^(S - ref) as fp16 into shared memory and
-//              sums it. O in TMEM is rescaled only when the maximum grows by more than
-//              2^8 (P stays <= 256, safe in fp16); the same reference is used for the
-//              sum, so the final O / l is exact softmax.
-//   warps 4-7  transform: cp.async of the raw bf16 K/V pages one tile ahead, then K is
-//              rotated by RoPE at each key's absolute position (MEPIC abstract: K is kept
-//              without positional encoding and RoPE is fused into attention) and V is
-//              transposed, both to fp16 in the 128-byte-swizzled K-major layout of the MMA
-//              operands. cos/sin(p theta) is composed from the table row of the page start
-//              and the row of the offset inside the page.
-//   warp 8     TMEM owner; one thread issues S = Q K^T (M128 N64 K128, into one of two
-//              TMEM buffers) and O += P V (M128 N128 K64) with tcgen05.mma kind::f16.
-// Page metadata is cached in shared memory in windows of 512 pages. Every mbarrier wait is
-// bounded; on expiry the CTA raises the device timeout flag and winds down.
+//   warp 9     loads: TMA boxes of each page's pre-RoPE K and V (16 rows x 64 dims, 128-byte
+//              swizzled, three tiles in flight), the cos/sin table rows of the page starts
+//              (bulk copies) and, per item, the Q tile (rotated and scaled fp16 rows written by
+//              the QKV epilogue).
+//   warps 4-7  transform: K rotated by RoPE at each key's absolute position (MEPIC abstract:
+//              K is kept without positional encoding and RoPE is fused into attention) into
+//              the fp16 K-major operand; V converted to fp16 in place (it stays [key][dim],
+//              the MN-major operand of O += P V). cos/sin(p theta) is composed from the table
+//              row of the page start and that of the offset inside the page (the latter held
+//              in registers: each thread always rotates the same row offset and dims).
+//   warp 8     TMEM owner; one thread issues S = Q K^T (M128 N64 K128) into one of two TMEM
+//              buffers and O += P V (M128 N128 K64) with tcgen05.mma kind::f16.
+//   warps 0-3  softmax: thread = one MMA row = one TMEM lane. Reads its row of S, masks keys
+//              after its position (only on tiles that need it), keeps a running reference
+//              maximum, writes P = 2^(S - ref) as the fp16 operand and sums it. O in TMEM is
+//              rescaled only when the maximum grows by more than 2^8 (P stays <= 256, safe in
+//              fp16); the sum uses the same reference, so O / l is exact softmax. At the end
+//              of an item it drains O (normalized output, or the unnormalized partial with
+//              its reference maximum and sum for the merge).
+// Barrier phases run over the CTA's whole tile sequence, so the next item's loads overlap the
+// current item's tail. Every wait is bounded; on expiry the CTA raises the device timeout flag
+// and winds down.
 #include <climits>
+#include <mutex>
+
+#include <cudaTypedefs.h>
 
 #include "pic_internal.h"
 
@@ -35,27 +44,31 @@ namespace {
 constexpr int D = 128;
 constexpr int REP = 4;
 constexpr int RB = 32;                    // query rows per item
-constexpr int KT = 64;                    // keys per tile
-constexpr int WIN = 512;
-constexpr int kThreads = 9 * 32;
-constexpr float kLog2e = 1.4426950408889634f;
+constexpr int KT = 64;                    // keys per tile (4 pages)
+constexpr int NSLOT = 3;                  // raw K/V tiles in flight
+constexpr int kThreads = 10 * 32;
 constexpr float kRescale = 8.f;           // rescale O when the row max grows by more than 2^8
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
 // shared memory map (bytes from a 1024-aligned base)
-constexpr int OFF_Q = 0;                       // 2 halves x [128 rows][128 B]        32 KB
-constexpr int OFF_K = OFF_Q + 32768;           // [2 buf][2 halves][64 rows][128 B]    32 KB
-constexpr int OFF_VT = OFF_K + 32768;          // [2 buf][128 dims][128 B = 64 keys]   32 KB
-constexpr int OFF_P = OFF_VT + 32768;          // [2 buf][128 rows][128 B = 64 keys]   32 KB
-constexpr int OFF_RAW = OFF_P + 32768;         // [2 buf][K 16 KB | V 16 KB] bf16      64 KB
-constexpr int OFF_LO = OFF_RAW + 65536;        // float2 [16][64]                       8 KB
-constexpr int OFF_PG = OFF_LO + 8192;          // float2 [2][4][64]                     4 KB
-constexpr int OFF_META = OFF_PG + 4096;        // int [3][WIN]                          6 KB
-constexpr int OFF_TM = OFF_META + 3 * WIN * 4; // int [2][4][2] (page start, valid rows)
-constexpr int OFF_POS = OFF_TM + 64;           // int [2][KT]
-constexpr int OFF_BAR = OFF_POS + 2 * KT * 4;  // mbarriers
-constexpr int N_BARS = 12;
+constexpr int OFF_Q = 0;                          // 2 halves x [128 rows][128 B] fp16      32 KB
+constexpr int OFF_KOP = OFF_Q + 32768;            // [2][2 halves][64 keys][128 B] fp16     32 KB
+constexpr int OFF_P = OFF_KOP + 32768;            // [2][128 rows][128 B] fp16              32 KB
+constexpr int OFF_KRAW = OFF_P + 32768;           // [3][2 halves][64 keys][128 B] bf16     48 KB
+constexpr int OFF_V = OFF_KRAW + NSLOT * 16384;   // [3][2 halves][64 keys][128 B] bf16->fp16 48 KB
+constexpr int OFF_CS = OFF_V + NSLOT * 16384;     // [3][4 pages][512 B] cos/sin rows         6 KB
+constexpr int OFF_TM = OFF_CS + NSLOT * 2048;     // int [3][4][2] page start, valid rows
+constexpr int OFF_POS = OFF_TM + 128;             // int [2][KT] key positions (INT_MAX = none)
+constexpr int OFF_TILE = OFF_POS + 2 * KT * 4;    // int [2] last key position, INT_MAX if ragged
+constexpr int OFF_BAR = OFF_TILE + 16;
+constexpr int N_BARS = 24;
 constexpr int SMEM_BYTES = OFF_BAR + N_BARS * 8 + 16;
+static_assert(OFF_BAR % 8 == 0, "mbarrier alignment");
+static_assert(SMEM_BYTES + 1024 <= 227 * 1024, "shared memory budget");
+
+// barrier slots
+constexpr int B_KVFULL = 0, B_SFULL = 2, B_SFREE = 4, B_PFULL = 6, B_PVDONE = 8, B_RAWFULL = 10, B_KRFREE = 13,
+              B_VFREE = 16, B_QFULL = 19, B_QFREE = 20, B_OFREE = 21, B_MMADONE = 22;
 
 __device__ int g_attn_timeout = 0;
 
@@ -70,6 +83,9 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
 }
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
 __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
   uint32_t ok;
@@ -91,27 +107,31 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
     }
   }
 }
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-// named barrier of the four transform warps, with an AND so that all take the same branch
-__device__ __forceinline__ bool tr_all(bool v) {
-  uint32_t r;
+__device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
   asm volatile(
-      "{\n .reg .pred p, q;\n setp.ne.u32 q, %1, 0;\n bar.red.and.pred p, 2, 128, q;\n selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(r)
-      : "r"((uint32_t)v)
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
       : "memory");
-  return r != 0;
 }
-__device__ __forceinline__ void tr_bar() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
+__device__ __forceinline__ void tma_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+      "[%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_1d(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+               : "memory");
+}
 
-// 16-byte chunk c (0..7) of row r of a [rows][128 B] tile, 128-byte swizzle (UMMA K-major)
+// 16-byte chunk c (0..7) of row r of a [rows][128 B] tile, 128-byte swizzle (the TMA and UMMA layout)
 __device__ __forceinline__ uint32_t sw128(int r, int c) { return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4)); }
-// 16-byte chunk c (0..15) of row r of a [rows][256 B] raw tile, XOR-swizzled
-__device__ __forceinline__ uint32_t swz256(int r, int c) { return (uint32_t)(r * 256 + ((c ^ (r & 7)) << 4)); }
 
-__device__ __forceinline__ uint64_t desc_sw128(uint32_t addr) {
+// K-major operand: 8-row atoms 1024 B apart, 128-byte swizzle
+__device__ __forceinline__ uint64_t desc_kmajor(uint32_t addr) {
   uint64_t d = 0;
   d |= (uint64_t)((addr & 0x3FFFFu) >> 4);
   d |= (uint64_t)(1024 >> 4) << 32;
@@ -119,9 +139,20 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t addr) {
   d |= (uint64_t)2 << 61;
   return d;
 }
-// kind::f16, A and B fp16 K-major, D fp32, M x N
-__device__ __forceinline__ constexpr uint32_t idesc_f16(int M, int N) {
-  return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+// MN-major operand [k rows][n] (n contiguous, 64 n per 128-byte row): blocks of 64 n are
+// `lbo` bytes apart, groups of 8 k rows 1024 B apart, 128-byte swizzle
+__device__ __forceinline__ uint64_t desc_mnmajor(uint32_t addr, uint32_t lbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((addr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)(1024 >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+// kind::f16, A and B fp16, D fp32, M x N; A K-major; B K-major or MN-major
+__device__ __forceinline__ constexpr uint32_t idesc_f16(int M, int N, bool b_mn_major) {
+  return (1u << 4) | ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 __device__ __forceinline__ void umma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
   asm volatile(
@@ -159,63 +190,62 @@ __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.
 __device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
-
-// rotate dims (8c..8c+7) and (64+8c..) by the composed angle, times `scale`, to fp16
-__device__ __forceinline__ void rope8(const float* v1, const float* v2, const float2* hi, const float2* lo, float scale,
-                                      uint4& y1, uint4& y2) {
-  __half o1[8], o2[8];
-#pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    const float2 H2 = hi[e], L2 = lo[e];
-    const float cs = H2.x * L2.x - H2.y * L2.y, sn = H2.y * L2.x + H2.x * L2.y;
-    o1[e] = __float2half_rn((v1[e] * cs - v2[e] * sn) * scale);
-    o2[e] = __float2half_rn((v2[e] * cs + v1[e] * sn) * scale);
-  }
-  y1 = *reinterpret_cast<uint4*>(o1);
-  y2 = *reinterpret_cast<uint4*>(o2);
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// bf16 pair -> fp16 pair (exact widening, one rounding)
+__device__ __forceinline__ uint32_t bf2_to_h2(uint32_t w) {
+  return pack_f16x2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
 }
 __device__ __forceinline__ void bf8_to_f32(const uint4& u, float* f) {
-  const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&u);
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
-    const float2 x = __bfloat1622float2(b[e]);
-    f[2 * e] = x.x;
-    f[2 * e + 1] = x.y;
+    f[2 * e] = __uint_as_float(w[e] << 16);
+    f[2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
   }
 }
 
-__global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnArgs a) {
+__device__ __forceinline__ int item_tiles(const AttnItem& it) { return (it.page1 - it.page0 + 3) >> 2; }
+
+__global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_constant__ AttnArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  float2* sLo = reinterpret_cast<float2*>(sm + OFF_LO);
-  float2* sPg = reinterpret_cast<float2*>(sm + OFF_PG);
-  int* sBlk = reinterpret_cast<int*>(sm + OFF_META);
-  int* sPp = sBlk + WIN;
-  int* sPl = sPp + WIN;
-  int* sTm = reinterpret_cast<int*>(sm + OFF_TM);   // [buf][page][start, valid rows]
+  int* sTm = reinterpret_cast<int*>(sm + OFF_TM);   // [slot][page][start, valid rows]
   int* sPos = reinterpret_cast<int*>(sm + OFF_POS);
+  int* sTile = reinterpret_cast<int*>(sm + OFF_TILE);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
-  // [0,2) kv_full  [2,4) s_full  [4,6) s_free  [6,8) p_full  [8,10) pv_done  [10] mma_done
-  const uint32_t b_kvfull = smem_u32(bars), b_sfull = smem_u32(bars + 2), b_sfree = smem_u32(bars + 4),
-                 b_pfull = smem_u32(bars + 6), b_pvdone = smem_u32(bars + 8), b_mmadone = smem_u32(bars + 10);
+  auto bar = [&](int i) { return smem_u32(bars + i); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + N_BARS);
   __shared__ volatile int s_abort;
 
-  const AttnItem it = a.items[blockIdx.x];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int npages = it.page1 - it.page0;
-  const int ntiles = (npages + 3) / 4;
 
   if (tid == 0) {
     s_abort = 0;
     for (int i = 0; i < 2; ++i) {
-      mbar_init(b_kvfull + 8 * i, 4);
-      mbar_init(b_sfull + 8 * i, 1);
-      mbar_init(b_sfree + 8 * i, 4);
-      mbar_init(b_pfull + 8 * i, 4);
-      mbar_init(b_pvdone + 8 * i, 1);
+      mbar_init(bar(B_KVFULL + i), 4);
+      mbar_init(bar(B_SFULL + i), 1);
+      mbar_init(bar(B_SFREE + i), 4);
+      mbar_init(bar(B_PFULL + i), 4);
+      mbar_init(bar(B_PVDONE + i), 1);
     }
-    mbar_init(b_mmadone, 1);
+    for (int i = 0; i < NSLOT; ++i) {
+      mbar_init(bar(B_RAWFULL + i), 1);
+      mbar_init(bar(B_KRFREE + i), 4);
+      mbar_init(bar(B_VFREE + i), 1);
+    }
+    mbar_init(bar(B_QFULL), 1);
+    mbar_init(bar(B_QFREE), 1);
+    mbar_init(bar(B_OFREE), 4);
+    mbar_init(bar(B_MMADONE), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 8) {
@@ -223,28 +253,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnArgs a) {
                  "r"(256));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
-  for (int i = tid; i < 16 * 64; i += kThreads) sLo[i] = a.rope_cs[i];
-  __syncthreads();
-
-  // ---- Q tile: row m = head * 32 + row, rotated at the row's position, scaled into log2 units
-  const float qscale = rsqrtf((float)D) * kLog2e;
-  for (int i = tid; i < 128 * 8; i += kThreads) {
-    const int m = i / 8, c = i % 8, hh = m / RB, r = m % RB;
-    uint4 y1 = make_uint4(0, 0, 0, 0), y2 = y1;
-    if (r < it.nrows) {
-      const int t = it.row0 + r, h = it.g * REP + hh, p = a.q_pos[t];
-      const float* src = a.q + ((size_t)t * a.H + h) * D;
-      float v1[8], v2[8];
-      *reinterpret_cast<float4*>(v1) = *reinterpret_cast<const float4*>(src + 8 * c);
-      *reinterpret_cast<float4*>(v1 + 4) = *reinterpret_cast<const float4*>(src + 8 * c + 4);
-      *reinterpret_cast<float4*>(v2) = *reinterpret_cast<const float4*>(src + 64 + 8 * c);
-      *reinterpret_cast<float4*>(v2 + 4) = *reinterpret_cast<const float4*>(src + 64 + 8 * c + 4);
-      rope8(v1, v2, a.rope_cs + (size_t)(p & ~15) * 64 + 8 * c, sLo + (p & 15) * 64 + 8 * c, qscale, y1, y2);
-    }
-    *reinterpret_cast<uint4*>(sm + OFF_Q + sw128(m, c)) = y1;
-    *reinterpret_cast<uint4*>(sm + OFF_Q + 16384 + sw128(m, c)) = y2;
-  }
-  fence_async_smem();
   fence_before();
   __syncthreads();
   fence_after();
@@ -253,92 +261,107 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnArgs a) {
   if (warp < 4) {
     // =============================== softmax warps
     const int hh = warp, r = lane, m = hh * RB + r;
-    const int qp = r < it.nrows ? a.q_pos[it.row0 + r] : -1;
     const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
-    float mref = -INFINITY, l = 0.f;
+    uint32_t gt = 0;
     bool ok = true;
-    for (int j = 0; j < ntiles && ok; ++j) {
-      const int b = j & 1, u = j >> 1;
-      // kv_full of the same tile also orders this thread after the transform's key positions
-      ok = __all_sync(0xffffffffu,
-                      !s_abort && mbar_wait(b_sfull + 8 * b, u & 1) && mbar_wait(b_kvfull + 8 * b, u & 1));
-      if (!ok) break;
-      fence_after();
-      float s[64];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld16(trow + 128 + 64 * b + 16 * c, s + 16 * c);
-      tmem_wait_ld();
-      fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(b_sfree + 8 * b);
-      const int* kp = sPos + b * KT;
-      float mx = -INFINITY;
-#pragma unroll
-      for (int i = 0; i < 64; ++i) {
-        if (kp[i] > qp) s[i] = -INFINITY;
-        mx = fmaxf(mx, s[i]);
-      }
-      // new reference when the maximum grows by more than 2^8 (or for the first keys seen)
-      const bool grow = mx > mref + kRescale || (mref == -INFINITY && mx > -INFINITY);
-      const float mnew = grow ? mx : mref;
-      const float scale = (grow && mref != -INFINITY) ? exp2f(mref - mnew) : 1.f;
-      if (__any_sync(0xffffffffu, scale != 1.f)) {
-        // O holds the sums of the tiles before: rescale it once PV of the previous tile is done
-        if (!mbar_wait(b_pvdone + 8 * ((j - 1) & 1), ((j - 1) >> 1) & 1)) {
-          s_abort = 1;
-          ok = false;
-        }
-        if (!__all_sync(0xffffffffu, ok)) break;
+    for (int ii = blockIdx.x; ii < a.n_items && ok; ii += gridDim.x) {
+      const AttnItem it = a.items[ii];
+      const int nt = item_tiles(it);
+      const int qp = r < it.nrows ? a.q_pos[it.row0 + r] : -1;
+      float mref = -INFINITY, l = 0.f;
+      for (int j = 0; j < nt; ++j, ++gt) {
+        const int b = gt & 1;
+        const uint32_t u = gt >> 1;
+        // kv_full of the same tile also orders this thread after the transform's key positions
+        ok = __all_sync(0xffffffffu, !s_abort && mbar_wait(bar(B_SFULL + b), u & 1) &&
+                                         mbar_wait(bar(B_KVFULL + b), u & 1));
+        if (!ok) break;
         fence_after();
-        for (int c = 0; c < 128; c += 16) {
-          float o[16];
-          tmem_ld16(trow + c, o);
-          tmem_wait_ld();
+        float s[64];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) o[e] *= scale;
-          tmem_st16(trow + c, o);
-        }
-        tmem_wait_st();
+        for (int c = 0; c < 4; ++c) tmem_ld16(trow + 128 + 64 * b + 16 * c, s + 16 * c);
+        tmem_wait_ld();
         fence_before();
-      }
-      l *= scale;
-      mref = mnew;
-      // P = 2^(S - ref) in fp16 into the operand tile; P of tile j - 2 must have been consumed
-      if (j >= 2 && !mbar_wait(b_pvdone + 8 * b, (u - 1) & 1)) {
-        s_abort = 1;
-        ok = false;
-      }
-      if (!__all_sync(0xffffffffu, ok)) break;
-      uint8_t* prow = sm + OFF_P + b * 16384;
-      float rs = 0.f;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_SFREE + b));
+        if (__any_sync(0xffffffffu, sTile[b] > qp)) {
+          const int4* kp = reinterpret_cast<const int4*>(sPos + b * KT);
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        __half hv[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float p = mref == -INFINITY ? 0.f : exp2f(s[8 * c + e] - mref);
-          rs += p;
-          hv[e] = __float2half_rn(p);
+          for (int i = 0; i < 16; ++i) {
+            const int4 k4 = kp[i];
+            if (k4.x > qp) s[4 * i] = -INFINITY;
+            if (k4.y > qp) s[4 * i + 1] = -INFINITY;
+            if (k4.z > qp) s[4 * i + 2] = -INFINITY;
+            if (k4.w > qp) s[4 * i + 3] = -INFINITY;
+          }
         }
-        *reinterpret_cast<uint4*>(prow + sw128(m, c)) = *reinterpret_cast<uint4*>(hv);
+        float mx = s[0];
+#pragma unroll
+        for (int i = 1; i < 64; ++i) mx = fmaxf(mx, s[i]);
+        // new reference when the maximum grows by more than 2^8 (or for the first keys seen)
+        const bool grow = mx > mref + kRescale;
+        const float mnew = grow ? mx : mref;
+        const float scale = (grow && mref != -INFINITY) ? ex2(mref - mnew) : 1.f;
+        if (__any_sync(0xffffffffu, scale != 1.f)) {
+          // O holds the sums of this item's earlier tiles: rescale once PV of the previous tile is done
+          if (!mbar_wait(bar(B_PVDONE + ((gt - 1) & 1)), ((gt - 1) >> 1) & 1)) ok = false;
+          if (!__all_sync(0xffffffffu, ok)) {
+            ok = false;
+            break;
+          }
+          fence_after();
+#pragma unroll 1
+          for (int c = 0; c < 128; c += 16) {
+            float o[16];
+            tmem_ld16(trow + c, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 16; ++e) o[e] *= scale;
+            tmem_st16(trow + c, o);
+          }
+          tmem_wait_st();
+          fence_before();
+        }
+        l *= scale;
+        mref = mnew;
+        // P = 2^(S - ref) as the fp16 operand; P of tile gt - 2 must have been consumed
+        if (gt >= 2 && !mbar_wait(bar(B_PVDONE + b), (u - 1) & 1)) ok = false;
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+        uint8_t* prow = sm + OFF_P + b * 16384;
+        const float mz = mref == -INFINITY ? 0.f : mref;   // fully masked so far: every s is -inf, p = 0
+        float rs = 0.f;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          uint32_t hv[4];
+#pragma unroll
+          for (int e = 0; e < 8; e += 2) {
+            const float p0 = ex2(s[8 * c + e] - mz), p1 = ex2(s[8 * c + e + 1] - mz);
+            rs += p0 + p1;
+            hv[e / 2] = pack_f16x2(p0, p1);
+          }
+          *reinterpret_cast<uint4*>(prow + sw128(m, c)) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+        }
+        l += rs;
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_PFULL + b));
       }
-      l += rs;
-      fence_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(b_pfull + 8 * b);
-    }
-    // ---- output: O / l (or the unnormalized partial with its reference max and sum)
-    if (ok && ntiles > 0) {
-      ok = __all_sync(0xffffffffu, mbar_wait(b_pvdone + 8 * ((ntiles - 1) & 1), ((ntiles - 1) >> 1) & 1));
-      if (!ok) s_abort = 1;
-    }
-    if (ok) {
-      fence_after();
+      if (!ok) break;
+      // ---- drain O: normalized output, or the unnormalized partial with its reference max and sum
+      if (nt > 0) {
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(B_PVDONE + ((gt - 1) & 1)), ((gt - 1) >> 1) & 1));
+        if (!ok) break;
+        fence_after();
+      }
       const int h = it.g * REP + hh;
       const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll 1
       for (int c = 0; c < 128; c += 16) {
         float o[16];
-        if (ntiles > 0) {
+        if (nt > 0) {
           tmem_ld16(trow + c, o);
           tmem_wait_ld();
         } else {
@@ -347,166 +370,250 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnArgs a) {
         }
         if (it.part < 0) {
           if (r < it.nrows) {
-            __half hv[16];
+            uint32_t hv[8];
 #pragma unroll
-            for (int e = 0; e < 16; ++e) hv[e] = __float2half_rn(o[e] * inv);
-            __half* dst = (__half*)a.out + ((size_t)(it.row0 + r) * a.H + h) * D + c;
-            *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<uint4*>(hv);
-            *reinterpret_cast<uint4*>(dst + 8) = *reinterpret_cast<uint4*>(hv + 8);
+            for (int e = 0; e < 16; e += 2) hv[e / 2] = pack_f16x2(o[e] * inv, o[e + 1] * inv);
+            uint4* dst = reinterpret_cast<uint4*>((__half*)a.out + ((size_t)(it.row0 + r) * a.H + h) * D + c);
+            dst[0] = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+            dst[1] = make_uint4(hv[4], hv[5], hv[6], hv[7]);
           }
         } else {
-          float* dst = a.part_o + (((size_t)it.part * kAttnPartRows + r) * REP + hh) * D + c;
+          float4* dst = reinterpret_cast<float4*>(a.part_o + (((size_t)it.part * kAttnPartRows + r) * REP + hh) * D + c);
 #pragma unroll
-          for (int e = 0; e < 16; e += 4) *reinterpret_cast<float4*>(dst + e) = make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
+          for (int e = 0; e < 4; ++e) dst[e] = make_float4(o[4 * e], o[4 * e + 1], o[4 * e + 2], o[4 * e + 3]);
         }
+      }
+      if (nt > 0) {
+        fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_OFREE));
       }
       if (it.part >= 0) {
         const size_t pi = ((size_t)it.part * kAttnPartRows + r) * REP + hh;
-        a.part_ml[pi * 2] = mref;
-        a.part_ml[pi * 2 + 1] = l;
+        *reinterpret_cast<float2*>(a.part_ml + pi * 2) = make_float2(mref, l);
       }
-    }
-  } else if (warp < 8) {
-    // =============================== transform warps: raw pages -> fp16 K (rotated) and V^T
-    const int tt = tid - 128;
-    const __nv_bfloat16* Kl = (const __nv_bfloat16*)a.k_layer;
-    const __nv_bfloat16* Vl = (const __nv_bfloat16*)a.v_layer;
-    int win = -1;
-    auto issue = [&](int tile) {
-      const int b = tile & 1;
-      const int w1 = (tile * 4 / WIN) * WIN;
-      if (w1 != win) {   // same decision in every transform thread
-        tr_bar();
-        win = w1;
-        for (int i = tt; i < WIN; i += 128) {
-          const int pg = it.page0 + win + i;
-          if (pg < it.page1) {
-            sBlk[i] = a.page_block[pg];
-            sPp[i] = a.page_pos[pg];
-            sPl[i] = a.page_len[pg];
-          }
-        }
-        tr_bar();
-      }
-      const int pbase = tile * 4 - win;
-      if (tt < 4) {
-        const bool in = tile * 4 + tt < npages;
-        sTm[(b * 4 + tt) * 2] = in ? sPp[pbase + tt] : 0;
-        sTm[(b * 4 + tt) * 2 + 1] = in ? sPl[pbase + tt] : 0;
-      }
-      uint8_t* raw = sm + OFF_RAW + b * 32768;
-      for (int task = tt; task < KT * 16; task += 128) {
-        const int key = task / 16, c = task % 16, pg = key / 16, rr = key % 16;
-        if (tile * 4 + pg < npages && rr < sPl[pbase + pg]) {
-          const size_t src = (((size_t)sBlk[pbase + pg] * a.G + it.g) * kBlock + rr) * D + 8 * c;
-          cp_async16(smem_u32(raw + swz256(key, c)), Kl + src);
-          cp_async16(smem_u32(raw + 16384 + swz256(key, c)), Vl + src);
-        }
-      }
-      {  // RoPE rows of the tile's four page starts
-        const int pg = tt / 32, c = tt % 32;
-        if (tile * 4 + pg < npages)
-          cp_async16(smem_u32(sPg + (b * 4 + pg) * 64) + c * 16, a.rope_cs + (size_t)sPp[pbase + pg] * 64 + c * 2);
-      }
-      asm volatile("cp.async.commit_group;" ::: "memory");
-    };
-    bool ok = true;
-    if (ntiles > 0) issue(0);
-    for (int j = 0; j < ntiles; ++j) {
-      const int b = j & 1, u = j >> 1;
-      tr_bar();   // every thread is done reading the raw buffer the next issue overwrites
-      if (j + 1 < ntiles) {
-        issue(j + 1);
-        asm volatile("cp.async.wait_group 1;" ::: "memory");
-      } else {
-        asm volatile("cp.async.wait_group 0;" ::: "memory");
-      }
-      // operand buffer b is free once PV of tile j - 2 has retired
-      ok = tr_all(!s_abort && (j < 2 || mbar_wait(b_pvdone + 8 * b, (u - 1) & 1)));
-      if (!ok) {
-        s_abort = 1;
-        break;
-      }
-      const uint8_t* raw = sm + OFF_RAW + b * 32768;
-      uint8_t* kt = sm + OFF_K + b * 16384;
-      uint8_t* vt = sm + OFF_VT + b * 16384;
-      // K: rotate (dims c and c + 64 together)
-      for (int task = tt; task < KT * 8; task += 128) {
-        const int key = task / 8, c = task % 8, pg = key / 16, rr = key % 16;
-        const bool valid = rr < sTm[(b * 4 + pg) * 2 + 1];
-        uint4 y1 = make_uint4(0, 0, 0, 0), y2 = y1;
-        if (valid) {
-          float v1[8], v2[8];
-          bf8_to_f32(*reinterpret_cast<const uint4*>(raw + swz256(key, c)), v1);
-          bf8_to_f32(*reinterpret_cast<const uint4*>(raw + swz256(key, c + 8)), v2);
-          rope8(v1, v2, sPg + (b * 4 + pg) * 64 + 8 * c, sLo + rr * 64 + 8 * c, 1.f, y1, y2);
-        }
-        *reinterpret_cast<uint4*>(kt + sw128(key, c)) = y1;
-        *reinterpret_cast<uint4*>(kt + 8192 + sw128(key, c)) = y2;
-        if (c == 0) sPos[b * KT + key] = valid ? sTm[(b * 4 + pg) * 2] + rr : INT_MAX;
-      }
-      // V: transpose to [dim][key] fp16 (the K-major operand of O += P V)
-      for (int task = tt; task < KT * 16; task += 128) {
-        const int key = task % KT, c = task / KT, pg = key / 16, rr = key % 16;
-        const bool valid = rr < sTm[(b * 4 + pg) * 2 + 1];
-        float v[8];
-        if (valid) {
-          bf8_to_f32(*reinterpret_cast<const uint4*>(raw + 16384 + swz256(key, c)), v);
-        } else {
-#pragma unroll
-          for (int e = 0; e < 8; ++e) v[e] = 0.f;
-        }
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int d = 8 * c + e;
-          *reinterpret_cast<__half*>(vt + sw128(d, key / 8) + (key % 8) * 2) = __float2half_rn(v[e]);
-        }
-      }
-      fence_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(b_kvfull + 8 * b);
-    }
-    asm volatile("cp.async.wait_all;" ::: "memory");
-  } else if (lane == 0) {
-    // =============================== MMA issuer
-    const uint32_t id_s = idesc_f16(128, KT), id_pv = idesc_f16(128, D);
-    const uint32_t qa = smem_u32(sm + OFF_Q);
-    auto issue_s = [&](int j) -> bool {
-      const int b = j & 1, u = j >> 1;
-      if (s_abort || !mbar_wait(b_kvfull + 8 * b, u & 1)) return false;
-      if (j >= 2 && !mbar_wait(b_sfree + 8 * b, (u - 1) & 1)) return false;
-      fence_after();
-      const uint32_t kb = smem_u32(sm + OFF_K + b * 16384);
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {   // K dimension 128 = 2 halves x 4 steps of 16
-        const uint32_t off = (k & 3) * 32;
-        umma(tmem + 128 + 64 * b, desc_sw128(qa + (k >> 2) * 16384 + off), desc_sw128(kb + (k >> 2) * 8192 + off),
-             id_s, k != 0);
-      }
-      umma_commit(b_sfull + 8 * b);
-      return true;
-    };
-    bool ok = ntiles == 0 || issue_s(0);
-    for (int j = 0; j < ntiles && ok; ++j) {
-      if (j + 1 < ntiles && !issue_s(j + 1)) {
-        ok = false;
-        break;
-      }
-      const int b = j & 1, u = j >> 1;
-      if (s_abort || !mbar_wait(b_pfull + 8 * b, u & 1)) {
-        ok = false;
-        break;
-      }
-      fence_after();
-      const uint32_t pa = smem_u32(sm + OFF_P + b * 16384), vb = smem_u32(sm + OFF_VT + b * 16384);
-#pragma unroll
-      for (int k = 0; k < 4; ++k)   // K dimension 64 keys = 4 steps of 16
-        umma(tmem, desc_sw128(pa + k * 32), desc_sw128(vb + k * 32), id_pv, (j | k) != 0);
-      umma_commit(b_pvdone + 8 * b);
     }
     if (!ok) s_abort = 1;
-    umma_commit(b_mmadone);   // fires once every MMA of this CTA has retired
-    mbar_wait(b_mmadone, 0);
+  } else if (warp < 8) {
+    // =============================== transform warps
+    const int tt = tid - 128, tw = warp - 4;
+    const int rr = lane & 15, cq = 2 * tw + (lane >> 4);   // K: row offset in page, dims 8cq.. and 64 + 8cq..
+    float2 lo[8];   // (cos, sin)(rr theta_i) for this thread's 8 frequencies
+#pragma unroll
+    for (int e = 0; e < 8; ++e) lo[e] = a.rope_cs[rr * 64 + 8 * cq + e];
+    uint32_t gt = 0;
+    bool ok = true;
+    for (int ii = blockIdx.x; ii < a.n_items && ok; ii += gridDim.x) {
+      const int nt = item_tiles(a.items[ii]);
+      for (int j = 0; j < nt; ++j, ++gt) {
+        const int b = gt & 1, s = gt % NSLOT;
+        const uint32_t u = gt >> 1, k = gt / NSLOT;
+        // raw tile landed; K operand buffer b and its key positions free once PV of tile gt - 2 retired
+        ok = __all_sync(0xffffffffu, !s_abort && mbar_wait(bar(B_RAWFULL + s), k & 1) &&
+                                         (gt < 2 || mbar_wait(bar(B_PVDONE + b), (u - 1) & 1)));
+        if (!ok) break;
+        const int* tm = sTm + s * 8;
+        const uint8_t* kraw = sm + OFF_KRAW + s * 16384;
+        uint8_t* kop = sm + OFF_KOP + b * 16384;
+        // K: rotate row offset rr of each of the four pages
+#pragma unroll 1
+        for (int pg = 0; pg < 4; ++pg) {
+          const int key = pg * 16 + rr, start = tm[2 * pg], len = tm[2 * pg + 1];
+          uint4 y1 = make_uint4(0, 0, 0, 0), y2 = y1;
+          if (rr < len) {
+            float v1[8], v2[8];
+            bf8_to_f32(*reinterpret_cast<const uint4*>(kraw + sw128(key, cq)), v1);
+            bf8_to_f32(*reinterpret_cast<const uint4*>(kraw + 8192 + sw128(key, cq)), v2);
+            const float4* hrow = reinterpret_cast<const float4*>(sm + OFF_CS + (s * 4 + pg) * 512) + 4 * cq;
+            uint32_t o1[4], o2[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const float4 h4 = hrow[q];   // (cos, sin) of the page start for frequencies 8cq + 2q, + 1
+              const float2 hi[2] = {make_float2(h4.x, h4.y), make_float2(h4.z, h4.w)};
+              float y1e[2], y2e[2];
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                const int f = 2 * q + e;
+                const float cs = hi[e].x * lo[f].x - hi[e].y * lo[f].y;
+                const float sn = hi[e].y * lo[f].x + hi[e].x * lo[f].y;
+                y1e[e] = v1[f] * cs - v2[f] * sn;
+                y2e[e] = v2[f] * cs + v1[f] * sn;
+              }
+              o1[q] = pack_f16x2(y1e[0], y1e[1]);
+              o2[q] = pack_f16x2(y2e[0], y2e[1]);
+            }
+            y1 = make_uint4(o1[0], o1[1], o1[2], o1[3]);
+            y2 = make_uint4(o2[0], o2[1], o2[2], o2[3]);
+          }
+          *reinterpret_cast<uint4*>(kop + sw128(key, cq)) = y1;
+          *reinterpret_cast<uint4*>(kop + 8192 + sw128(key, cq)) = y2;
+          if (cq == 0) sPos[b * KT + key] = rr < len ? start + rr : INT_MAX;
+        }
+        if (tt == 0) {   // last key position of the tile; INT_MAX when some slot holds no key
+          int kmax = -1;
+          bool full = true;
+          for (int pg = 0; pg < 4; ++pg) {
+            const int len = tm[2 * pg + 1];
+            if (len > 0) kmax = tm[2 * pg] + len - 1;
+            if (len < kBlock) full = false;
+          }
+          sTile[b] = full ? kmax : INT_MAX;
+        }
+        // V: bf16 -> fp16 in place; rows without a key become 0 (P is 0 there, V must be finite)
+        uint8_t* vt = sm + OFF_V + s * 16384;
+#pragma unroll 4
+        for (int i = 0; i < 8; ++i) {
+          const int ch = tt + 128 * i, key = (ch >> 3) & 63;
+          uint4* p = reinterpret_cast<uint4*>(vt + ch * 16);
+          if ((key & 15) < tm[2 * (key >> 4) + 1]) {
+            const uint4 w = *p;
+            *p = make_uint4(bf2_to_h2(w.x), bf2_to_h2(w.y), bf2_to_h2(w.z), bf2_to_h2(w.w));
+          } else {
+            *p = make_uint4(0, 0, 0, 0);
+          }
+        }
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(bar(B_KRFREE + s));
+          mbar_arrive(bar(B_KVFULL + b));
+        }
+      }
+    }
+    if (!ok) s_abort = 1;
+  } else if (warp == 8) {
+    // =============================== MMA issuer
+    if (lane == 0) {
+      const uint32_t id_s = idesc_f16(128, KT, false), id_pv = idesc_f16(128, D, true);
+      const uint32_t qa = smem_u32(sm + OFF_Q);
+      auto issue_s = [&](uint32_t g_tile) -> bool {
+        const int b = g_tile & 1;
+        const uint32_t u = g_tile >> 1;
+        if (s_abort || !mbar_wait(bar(B_KVFULL + b), u & 1)) return false;
+        if (g_tile >= 2 && !mbar_wait(bar(B_SFREE + b), (u - 1) & 1)) return false;
+        fence_after();
+        const uint32_t kb = smem_u32(sm + OFF_KOP + b * 16384);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {   // K dimension 128 = 2 halves x 4 steps of 16
+          const uint32_t off = (k & 3) * 32;
+          umma(tmem + 128 + 64 * b, desc_kmajor(qa + (k >> 2) * 16384 + off),
+               desc_kmajor(kb + (k >> 2) * 8192 + off), id_s, k != 0);
+        }
+        umma_commit(bar(B_SFULL + b));
+        return true;
+      };
+      uint32_t gt = 0, ai = 0;
+      bool ok = true;
+      for (int ii = blockIdx.x; ii < a.n_items && ok; ii += gridDim.x) {
+        const int nt = item_tiles(a.items[ii]);
+        if (nt == 0) continue;
+        if (s_abort || !mbar_wait(bar(B_QFULL), ai & 1)) {
+          ok = false;
+          break;
+        }
+        ok = issue_s(gt);
+        if (ok && nt == 1) umma_commit(bar(B_QFREE));
+        for (int j = 0; j < nt && ok; ++j) {
+          const uint32_t g = gt + j;
+          if (j + 1 < nt) {
+            if (!issue_s(g + 1)) {
+              ok = false;
+              break;
+            }
+            if (j + 2 == nt) umma_commit(bar(B_QFREE));   // every S of this item issued
+          }
+          const int b = g & 1, s = g % NSLOT;
+          if (s_abort || !mbar_wait(bar(B_PFULL + b), (g >> 1) & 1)) {
+            ok = false;
+            break;
+          }
+          if (j == 0 && ai > 0 && !mbar_wait(bar(B_OFREE), (ai - 1) & 1)) {   // previous item's O drained
+            ok = false;
+            break;
+          }
+          fence_after();
+          const uint32_t pa = smem_u32(sm + OFF_P + b * 16384), vb = smem_u32(sm + OFF_V + s * 16384);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)   // K dimension 64 keys = 4 steps of 16 (2 groups of 8 key rows)
+            umma(tmem, desc_kmajor(pa + k * 32), desc_mnmajor(vb + k * 2048, 8192), id_pv, (j | k) != 0);
+          umma_commit(bar(B_PVDONE + b));
+          umma_commit(bar(B_VFREE + s));
+        }
+        gt += nt;
+        ++ai;
+      }
+      if (!ok) s_abort = 1;
+      umma_commit(bar(B_MMADONE));   // fires once every MMA of this CTA has retired
+      mbar_wait(bar(B_MMADONE), 0);
+    }
+  } else {
+    // =============================== loads (lane 0 issues; the warp reads page metadata)
+    uint32_t gt = 0, ai = 0;
+    bool ok = true;
+    int w0 = 0, wblk = 0, wpos = 0, wlen = 0;   // lane i: metadata of page w0 + i
+    for (int ii = blockIdx.x; ii < a.n_items && ok; ii += gridDim.x) {
+      const AttnItem it = a.items[ii];
+      const int nt = item_tiles(it);
+      for (int j = 0; j < nt; ++j, ++gt) {
+        const int s = gt % NSLOT;
+        const uint32_t k = gt / NSLOT;
+        const int p0 = it.page0 + 4 * j, np = min(4, it.page1 - p0);
+        if (j == 0 || p0 + 4 > w0 + 32) {
+          w0 = p0;
+          const int pg = w0 + lane;
+          if (pg < it.page1) {
+            wblk = a.page_block[pg];
+            wpos = a.page_pos[pg];
+            wlen = a.page_len[pg];
+          }
+        }
+        int blk[4], pos[4], len[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          blk[q] = __shfl_sync(0xffffffffu, wblk, p0 - w0 + q);
+          pos[q] = __shfl_sync(0xffffffffu, wpos, p0 - w0 + q);
+          len[q] = q < np ? __shfl_sync(0xffffffffu, wlen, p0 - w0 + q) : 0;
+        }
+        // slot s free: its K consumed by the transform and its V by PV of tile gt - 3
+        if (lane == 0)
+          ok = !s_abort && (k == 0 || (mbar_wait(bar(B_KRFREE + s), (k - 1) & 1) &&
+                                       mbar_wait(bar(B_VFREE + s), (k - 1) & 1)));
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        if (lane == 0) {
+          int* tm = sTm + s * 8;
+          for (int q = 0; q < 4; ++q) {
+            tm[2 * q] = pos[q];
+            tm[2 * q + 1] = len[q];
+          }
+          const uint32_t fb = bar(B_RAWFULL + s);
+          mbar_expect_tx(fb, (uint32_t)np * (4 * 2048 + 512));
+          const uint32_t kd = smem_u32(sm + OFF_KRAW + s * 16384), vd = smem_u32(sm + OFF_V + s * 16384);
+          for (int q = 0; q < np; ++q) {
+            const int y = (blk[q] * a.G + it.g) * kBlock;
+            tma_2d(kd + q * 2048, &a.kmap, 0, y, fb);
+            tma_2d(kd + 8192 + q * 2048, &a.kmap, 64, y, fb);
+            tma_2d(vd + q * 2048, &a.vmap, 0, y, fb);
+            tma_2d(vd + 8192 + q * 2048, &a.vmap, 64, y, fb);
+            bulk_1d(smem_u32(sm + OFF_CS + (s * 4 + q) * 512), a.rope_cs + (size_t)pos[q] * 64, 512, fb);
+          }
+        }
+        if (j == 0) {   // this item's Q, once every S of the previous item has completed
+          if (lane == 0) ok = !s_abort && (ai == 0 || mbar_wait(bar(B_QFREE), (ai - 1) & 1));
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) break;
+          if (lane == 0) {
+            const uint32_t qb = bar(B_QFULL);
+            mbar_expect_tx(qb, 32768);
+            for (int q = 0; q < 8; ++q)   // (head, half): 32 rows x 64 dims
+              tma_3d(smem_u32(sm + OFF_Q + (q & 1) * 16384 + (q >> 1) * 4096), &a.qmap, 64 * (q & 1),
+                     it.g * REP + (q >> 1), it.row0, qb);
+          }
+          ++ai;
+        }
+      }
+    }
+    if (!ok) s_abort = 1;
   }
   __syncwarp();
   fence_before();
@@ -514,10 +621,58 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(AttnArgs a) {
   if (warp == 8) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(256));
 }
 
+int sm_count() {
+  static int n[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return 152;
+  if (!n[dev] && (cudaDeviceGetAttribute(&n[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n[dev] <= 0))
+    n[dev] = 152;
+  return n[dev];
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
 }  // namespace
 
 bool tc_attention_supported(int dtype, int D_, int rep) { return dtype == PIC_BF16 && D_ == D && rep == REP; }
 
+bool attn_q_map(CUtensorMap* m, const void* q16, int T, int H) {
+  auto enc = encode_fn();
+  if (!enc || T < 1 || H < 1) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)T};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2};
+  cuuint32_t box[3] = {64, 1, RB};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(q16), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool attn_kv_map(CUtensorMap* m, const void* layer, int pool_blocks, int G) {
+  auto enc = encode_fn();
+  if (!enc || pool_blocks < 1 || G < 1) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)pool_blocks * G * kBlock};
+  cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+  cuuint32_t box[2] = {64, kBlock};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(layer), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Grid = min(items, SMs): the planner deals items for exactly this walk.
 void launch_attention_tc(const AttnArgs& a, cudaStream_t st) {
   static bool attr[64] = {};
   int dev = 0;
@@ -527,7 +682,7 @@ void launch_attention_tc(const AttnArgs& a, cudaStream_t st) {
     cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (dev >= 0 && dev < 64) attr[dev] = true;
   }
-  if (a.n_items > 0) attn_tc_kernel<<<a.n_items, kThreads, smem, st>>>(a);
+  if (a.n_items > 0) attn_tc_kernel<<<std::min(a.n_items, sm_count()), kThreads, smem, st>>>(a);
 }
 
 pic_status attn_check_timeout() {

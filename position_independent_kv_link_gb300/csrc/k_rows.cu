@@ -87,13 +87,41 @@ __device__ __forceinline__ float4 take4(float* __restrict__ acc, size_t off) {
 // QKV epilogue: q -> [T][H*D] fp32; pre-RoPE k, v -> their page slot of this layer. The
 // accumulator [T][N] is cleared behind the read. grid (T, ceil(N / 1024)); a thread owns 4
 // consecutive columns (one head).
+// Dims i..i+3 and i+64..i+67 (i < 64) of one 128-dim q head: rotate-half RoPE at the angles of
+// one table row, times `scale`, rounded once to fp16.
+__device__ __forceinline__ void rope_q16_store(float4 a, float4 b, const float2* __restrict__ cs_row, int i, float scale,
+                                               __half* __restrict__ dst) {
+  const float x1[4] = {a.x, a.y, a.z, a.w}, x2[4] = {b.x, b.y, b.z, b.w};
+  float y1[4], y2[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float2 c = cs_row[i + e];
+    y1[e] = (x1[e] * c.x - x2[e] * c.y) * scale;
+    y2[e] = (x2[e] * c.x + x1[e] * c.y) * scale;
+  }
+  store4<__half>(dst + i, make_float4(y1[0], y1[1], y1[2], y1[3]));
+  store4<__half>(dst + 64 + i, make_float4(y2[0], y2[1], y2[2], y2[3]));
+}
+
+constexpr float kQ16Scale = 1.4426950408889634f * 0.08838834764831845f;   // log2(e) / sqrt(128)
+
 template <typename T>
 __global__ void qkv_epilogue_kernel(int H, int G, int D, float* __restrict__ acc, float* __restrict__ q,
-                                    const int* __restrict__ slot, T* __restrict__ kl, T* __restrict__ vl) {
+                                    const int* __restrict__ slot, T* __restrict__ kl, T* __restrict__ vl,
+                                    const int* __restrict__ pos, const float2* __restrict__ rope_cs,
+                                    __half* __restrict__ q16) {
   const int t = blockIdx.x;
   const int N = (H + 2 * G) * D;
   const int n = (blockIdx.y * blockDim.x + threadIdx.x) * 4;
   if (n >= N) return;
+  if (q16 && n < H * D) {   // rotated fp16 q: the thread of dims i < 64 also takes dims i + 64
+    const int i = n % D;
+    if (i >= 64) return;
+    const size_t base = (size_t)t * N + n;
+    const float4 a = take4(acc, base), b = take4(acc, base + 64);
+    rope_q16_store(a, b, rope_cs + (size_t)pos[t] * 64, i, kQ16Scale, q16 + (size_t)t * H * D + (n - i));
+    return;
+  }
   const float4 v = take4(acc, (size_t)t * N + n);
   if (n < H * D) {
     store4<float>(q + (size_t)t * H * D + n, v);
@@ -200,16 +228,35 @@ void launch_embed_norm(int dtype, int T, int d, const void* embed, const int* to
 }
 
 void launch_qkv_epilogue(int dtype, int T, int H, int G, int D, float* acc, float* q, const int* slot, void* k_layer,
-                         void* v_layer, cudaStream_t st) {
+                         void* v_layer, const int* pos, const float2* rope_cs, __half* q16, cudaStream_t st) {
   if (T <= 0) return;
   const int N = (H + 2 * G) * D;
   dim3 grid(T, (N / 4 + kRowThreads - 1) / kRowThreads);
   if (dtype == PIC_BF16)
-    qkv_epilogue_kernel<__nv_bfloat16><<<grid, kRowThreads, 0, st>>>(H, G, D, acc, q, slot,
-                                                                     (__nv_bfloat16*)k_layer, (__nv_bfloat16*)v_layer);
+    qkv_epilogue_kernel<__nv_bfloat16><<<grid, kRowThreads, 0, st>>>(
+        H, G, D, acc, q, slot, (__nv_bfloat16*)k_layer, (__nv_bfloat16*)v_layer, pos, rope_cs, q16);
   else
     qkv_epilogue_kernel<float><<<grid, kRowThreads, 0, st>>>(H, G, D, acc, q, slot, (float*)k_layer,
-                                                             (float*)v_layer);
+                                                             (float*)v_layer, pos, rope_cs, nullptr);
+}
+
+namespace {
+__global__ void rope_q16_kernel(int H, const float* __restrict__ q, const int* __restrict__ pos,
+                                const float2* __restrict__ rope_cs, __half* __restrict__ q16) {
+  const int t = blockIdx.x;
+  const int j = blockIdx.y * blockDim.x + threadIdx.x;   // (head, i / 4) with i < 64
+  if (j >= H * 16) return;
+  const int h = j / 16, i = (j % 16) * 4;
+  const float* src = q + ((size_t)t * H + h) * 128;
+  rope_q16_store(*reinterpret_cast<const float4*>(src + i), *reinterpret_cast<const float4*>(src + 64 + i),
+                 rope_cs + (size_t)pos[t] * 64, i, kQ16Scale, q16 + ((size_t)t * H + h) * 128);
+}
+}  // namespace
+
+void launch_rope_q16(int T, int H, const float* q, const int* pos, const float2* rope_cs, __half* q16,
+                     cudaStream_t st) {
+  if (T <= 0) return;
+  rope_q16_kernel<<<dim3(T, (H * 16 + 255) / 256), 256, 0, st>>>(H, q, pos, rope_cs, q16);
 }
 
 void launch_rmsnorm_rows(int dtype, int T, int d, const float* h, const float* gain, float eps, void* x,

@@ -88,18 +88,21 @@ pic_status pic_op_attention_noalloc(int32_t dtype, int32_t T, int32_t n_heads, i
   in.page_pos = &ppos;
   in.G = n_kv_heads;
   in.rows_per_block = attention_rows_per_block(dtype, head_dim, n_heads / n_kv_heads);
+  in.persistent = attention_persistent(dtype, head_dim, n_heads / n_kv_heads);
   in.num_sms = device_sms();
   std::vector<AttnItem> items;
   std::vector<AttnCombine> combs;
   int n_parts = 0;
   plan_attention(in, items, combs, n_parts);
 
-  // exact footprint of this call: metadata ints, then partial outputs and (max, sum) pairs
+  // exact footprint of this call: metadata ints, partial outputs and (max, sum) pairs, then
+  // the rotated fp16 q of the tensor-core path
   const int rep = n_heads / n_kv_heads;
   const size_t n_ints = (size_t)T + 3 * (size_t)n_pages + 6 * items.size() + 5 * combs.size();
   const size_t o_part = align256(n_ints * 4);
   const size_t o_ml = o_part + align256((size_t)n_parts * kAttnPartRows * rep * head_dim * 4);
-  const size_t need = o_ml + align256((size_t)n_parts * kAttnPartRows * rep * 2 * 4);
+  const size_t o_q16 = o_ml + align256((size_t)n_parts * kAttnPartRows * rep * 2 * 4);
+  const size_t need = o_q16 + (in.persistent ? align256((size_t)T * n_heads * head_dim * 2) : 0);
   if (need > kNoAllocScratchBytes)
     return fail(PIC_ERR_CAPACITY, "attention needs " + std::to_string(need) + " bytes of scratch; the fixed area holds " +
                                       std::to_string(kNoAllocScratchBytes) + " (use pic_op_attention with a caller buffer)");
@@ -146,6 +149,10 @@ pic_status pic_op_attention_noalloc(int32_t dtype, int32_t T, int32_t n_heads, i
   a.n_items = (int)items.size();
   a.combines = (const AttnCombine*)(di + o_combs);
   a.n_combines = (int)combs.size();
+  if (in.persistent) {
+    s = attention_prepare_tc(a, T, pool_blocks, (__half*)((char*)scratch + o_q16), st);
+    if (s != PIC_OK) return s;
+  }
   launch_attention(a, st);
   PIC_CUDA(cudaGetLastError());
   return PIC_OK;

@@ -19,7 +19,7 @@ int current_sms() {
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
 struct AttnScratchLayout {
-  size_t ints_bytes, part_o_off, part_ml_off, total;
+  size_t ints_bytes, part_o_off, part_ml_off, q16_off, total;
   int max_parts, max_items;
 };
 
@@ -33,7 +33,8 @@ AttnScratchLayout attn_layout(int T, int n_heads, int n_kv_heads, int head_dim, 
   const int rep = std::max(1, n_heads / std::max(1, n_kv_heads));
   L.part_o_off = L.ints_bytes;
   L.part_ml_off = L.part_o_off + align256((size_t)L.max_parts * kAttnPartRows * rep * head_dim * 4);
-  L.total = L.part_ml_off + align256((size_t)L.max_parts * kAttnPartRows * rep * 2 * 4);
+  L.q16_off = L.part_ml_off + align256((size_t)L.max_parts * kAttnPartRows * rep * 2 * 4);
+  L.total = L.q16_off + align256((size_t)T * n_heads * head_dim * 2);   // rotated fp16 q (tensor-core path)
   return L;
 }
 
@@ -109,6 +110,7 @@ pic_status pic_op_attention(int32_t dtype, int32_t T, int32_t n_heads, int32_t n
   in.page_pos = &ppos;
   in.G = n_kv_heads;
   in.rows_per_block = attention_rows_per_block(dtype, head_dim, n_heads / n_kv_heads);
+  in.persistent = attention_persistent(dtype, head_dim, n_heads / n_kv_heads);
   in.num_sms = current_sms();
   std::vector<AttnItem> items;
   std::vector<AttnCombine> combs;
@@ -151,6 +153,10 @@ pic_status pic_op_attention(int32_t dtype, int32_t T, int32_t n_heads, int32_t n
   a.n_items = (int)items.size();
   a.combines = (const AttnCombine*)(di + o_combs);
   a.n_combines = (int)combs.size();
+  if (in.persistent) {
+    pic_status e = attention_prepare_tc(a, T, pool_blocks, (__half*)((char*)scratch + L.q16_off), st);
+    if (e != PIC_OK) return e;
+  }
   launch_attention(a, st);
   PIC_CUDA(cudaGetLastError());
   return PIC_OK;

@@ -1,6 +1,7 @@
 // Internal declarations shared by the library's translation units.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -47,10 +48,16 @@ inline size_t act_size(int dtype) { return dtype == PIC_BF16 ? 2 : 4; }
 // h[t] = E[tok[t]] (fp32); x[t] = RMSNorm(h[t]) * gain in the activation type.
 void launch_embed_norm(int dtype, int T, int d, const void* embed, const int* tok, const float* gain, float eps,
                        float* h, void* x, cudaStream_t st);
-// QKV epilogue: reads (and clears) the fp32 accumulator [T][(H+2G)D], writes q [T][H*D]
-// (fp32) and the pre-RoPE k, v rows (model dtype) into their page slots of one layer.
+// QKV epilogue: reads (and clears) the fp32 accumulator [T][(H+2G)D], writes the pre-RoPE
+// k, v rows (model dtype) into their page slots of one layer, and q [T][H][D]: fp32 pre-RoPE
+// when q16 is null, else (q16 non-null, D = 128) rotated at pos[t] with the cos/sin table,
+// times log2(e)/sqrt(D), in fp16 into q16 -- the operand of the tensor-core attention.
 void launch_qkv_epilogue(int dtype, int T, int H, int G, int D, float* acc, float* q, const int* slot, void* k_layer,
-                         void* v_layer, cudaStream_t st);
+                         void* v_layer, const int* pos, const float2* rope_cs, __half* q16, cudaStream_t st);
+// q16[t][h] = fp16(RoPE(q[t][h], pos[t]) * log2(e)/sqrt(D)) for D = 128 (same arithmetic as the
+// epilogue's q16 output), for callers that hold fp32 pre-RoPE q.
+void launch_rope_q16(int T, int H, const float* q, const int* pos, const float2* rope_cs, __half* q16,
+                     cudaStream_t st);
 // y = RMSNorm(h[t]) * gain. Not final: x[t] = y (activation type). Final: hidden_out[out_row[t]]
 // = y (fp32) when out_row[t] >= 0 and lm_x[lg_row[t]] = y (activation type) when lg_row[t] >= 0.
 void launch_rmsnorm_rows(int dtype, int T, int d, const float* h, const float* gain, float eps, void* x,
@@ -97,6 +104,9 @@ struct AttnCombine {   // merge `nparts` partial results of rows [row0, row0+nro
   int row0, nrows, g, part0, nparts;
 };
 struct AttnArgs {
+  // tensor-core kernel only (attention_persistent shapes): Q as fp16 [T][H][D] rotated and
+  // scaled (attn_q_map), K and V pools of the layer as [rows][D] bf16 (attn_kv_map)
+  CUtensorMap qmap, kmap, vmap;
   int dtype, H, G, D;
   int rb;                   // rows per work item of this plan (16 or 32)
   const float* q;           // [T][H][D] pre-RoPE, fp32
@@ -126,9 +136,22 @@ struct AttnPlanInput {
   int G;
   int num_sms;
   int rows_per_block;       // from attention_rows_per_block()
+  bool persistent = false;  // from attention_persistent(): one CTA per SM walks a strided item list
 };
 // Rows per work item the attention kernels take for this model shape (16 or 32).
 int attention_rows_per_block(int dtype, int D, int rep);
+// True when the shape runs the persistent tensor-core kernel: its CTA b takes items b, b + grid,
+// b + 2 grid, ... with grid = min(items, SMs), so the planner orders items for that walk.
+bool attention_persistent(int dtype, int D, int rep);
+// Tensor maps of the tensor-core attention: Q fp16 [T][H][128] (3-D, boxes of 64 dims x 1
+// head x 32 rows) and one layer of a KV pool, [pool_blocks * G * 16 rows][128] bf16 (boxes of
+// 64 dims x 16 rows). Both 128-byte swizzled. False when encoding fails.
+bool attn_q_map(CUtensorMap* m, const void* q16, int T, int H);
+bool attn_kv_map(CUtensorMap* m, const void* layer, int pool_blocks, int G);
+// For callers holding fp32 pre-RoPE a.q (kernel-level calls): writes the rotated fp16 copy
+// into q16 ([T][H][128], 16-byte aligned) and sets a.qmap / a.kmap / a.vmap from it and from
+// a.k_layer / a.v_layer (pools of pool_blocks blocks).
+pic_status attention_prepare_tc(AttnArgs& a, int T, int pool_blocks, __half* q16, cudaStream_t st);
 void plan_attention(const AttnPlanInput& in, std::vector<AttnItem>& items, std::vector<AttnCombine>& combines,
                     int& n_parts);
 size_t attention_part_bytes(int n_parts, int rep, int D);

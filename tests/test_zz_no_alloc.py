@@ -75,8 +75,8 @@ def test_noalloc_attention_rejects_oversized_work():
     torch.cuda.set_device(0)
     from position_independent_kv_link_gb300 import _lib as L, api
     lib = L.load()
-    # 16 query rows at the end of 5000 pages: the planner splits the pages into ~600 runs
-    # whose merge partials (~33 KB each) exceed the fixed area
+    # 16 query rows at the end of 5000 pages: the planner splits the pages into ~300 runs
+    # whose merge partials (~65 KB each) exceed the fixed area
     T, n_pages = 16, 5000
     qpos = np.arange(16 * n_pages - T, 16 * n_pages, dtype=np.int32)
     blk = np.arange(n_pages, dtype=np.int32)
