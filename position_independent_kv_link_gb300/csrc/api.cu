@@ -116,8 +116,8 @@ struct pic_store {
   void* attn = nullptr;
   void* act = nullptr;
   void* lm_x = nullptr;
-  float* qkv_acc = nullptr;  // [max_rows][(H+2G)D] fp32, zero between uses
-  float* gu_acc = nullptr;   // [max_rows][2F] fp32, zero between uses
+  float* qkv_acc = nullptr;  // [max_rows][(H+2G)D] fp32, zeroed before each QKV GEMM
+  float* gu_acc = nullptr;   // [max_rows][2F] fp32, zeroed before each gate/up GEMM
   float* att_o = nullptr;
   float* att_ml = nullptr;
   int att_parts_cap = 0;
@@ -334,18 +334,25 @@ pic_status run_forward_impl(pic_store* s, const Batch& b, float* hidden_out, flo
     Rec r(s, st, PIC_PROF_GEMM, gemm_bytes(N, K, rows), 2.0 * N * K * rows, 1);
     return gemm(s, W, Wp, X, Y, N, K, rows, st);
   };
+  // The QKV and gate/up GEMMs reduce into fp32 accumulators zeroed by a memset just before
+  // (cheaper than clearing them behind the read: the epilogues only read them).
+  auto zero_acc = [&](float* acc, size_t n) -> pic_status {
+    Rec r(s, st, PIC_PROF_COPY, (double)n * 4, 0, 0);   // a runtime memset, not a library kernel
+    PIC_CUDA(cudaMemsetAsync(acc, 0, n * 4, st));
+    return PIC_OK;
+  };
   auto pk = [&](const std::vector<const void*>& v, int l) -> const void* { return v.empty() ? nullptr : v[l]; };
-  // The QKV and gate/up GEMMs add into zeroed accumulators that their epilogues clear
-  // again; the O and down projections add straight into the residual stream h.
+  // The O and down projections add straight into the residual stream h.
   {
     Rec r(s, st, PIC_PROF_ROWWISE, dT * dd * (es + 4 + es) + dT * 4, 0, 1);
     launch_embed_norm(dt, T, d, s->m->embed, d_tok, s->m->attn_norm[0], c.rms_eps, s->h, s->x, st);
   }
   for (int l = 0; l < c.n_layers; ++l) {
     pic_status e;
+    if ((e = zero_acc(s->qkv_acc, (size_t)T * qkv)) != PIC_OK) return e;
     if ((e = run_gemm(s->m->wqkv[l], pk(s->m->pqkv, l), s->x, s->qkv_acc, qkv, d, T)) != PIC_OK) return e;
     {
-      Rec r(s, st, PIC_PROF_ROWWISE, dT * dQKV * (8 + es), 0, 1);
+      Rec r(s, st, PIC_PROF_ROWWISE, dT * dQKV * (4 + es), 0, 1);
       launch_qkv_epilogue(dt, T, H, G, D, s->qkv_acc, s->q, d_slot, s->k_layer(l), s->v_layer(l), d_pos, s->rope_cs,
                           att_tc ? (__half*)s->q : nullptr, st);
     }
@@ -367,9 +374,10 @@ pic_status run_forward_impl(pic_store* s, const Batch& b, float* hidden_out, flo
       launch_rmsnorm_rows(dt, T, d, s->h, s->m->mlp_norm[l], c.rms_eps, s->x, false, nullptr, nullptr, nullptr,
                           nullptr, st);
     }
+    if ((e = zero_acc(s->gu_acc, (size_t)T * 2 * F)) != PIC_OK) return e;
     if ((e = run_gemm(s->m->wgu[l], pk(s->m->pgu, l), s->x, s->gu_acc, 2 * F, d, T)) != PIC_OK) return e;
     {
-      Rec r(s, st, PIC_PROF_ROWWISE, dT * 2 * dF * 8 + dT * dF * es, 0, 1);
+      Rec r(s, st, PIC_PROF_ROWWISE, dT * 2 * dF * 4 + dT * dF * es, 0, 1);
       launch_swiglu(dt, T, F, s->gu_acc, s->act, st);
     }
     if ((e = run_gemm(s->m->wdown[l], pk(s->m->pdown, l), s->act, s->h, d, F, T)) != PIC_OK) return e;
@@ -553,7 +561,7 @@ pic_status pic_store_create(pic_model* m, const pic_store_config* cfg, void* k_p
   s->att_ml = (float*)(s->ws + o_attml);
   s->meta_d = (int32_t*)(s->ws + o_meta);
   s->rope_cs = (float2*)(s->ws + o_rope);
-  // the in-place accumulators start at zero; their epilogues keep them zero between GEMMs
+  // the accumulators start at zero (each forward also zeroes them before their GEMM)
   e = cudaMemset(s->ws + o_qkv, 0, o_gu + R * 2 * F * 4 - o_qkv);
   if (e != cudaSuccess) {
     cudaFree(s->ws);

@@ -5,17 +5,18 @@
 // heads sharing KV head g x a run of pages. The 32 rows x 4 heads form one M = 128 MMA tile
 // (row m = head * 32 + row), so each 64-key tile (4 pages) of K and V is staged once for all.
 //
-//   warp 9     loads: TMA boxes of each page's pre-RoPE K and V (16 rows x 64 dims, 128-byte
-//              swizzled, three tiles in flight), the cos/sin table rows of the page starts
+//   warp 13    loads: TMA boxes of each page's pre-RoPE K and V (16 rows x 64 dims, 128-byte
+//              swizzled; raw K is held until rotated, three tiles deep, V until its PV, four
+//              deep), the cos/sin table rows of the page starts
 //              (bulk copies) and, per item, the Q tile (rotated and scaled fp16 rows written by
 //              the QKV epilogue).
-//   warps 4-7  transform: K rotated by RoPE at each key's absolute position (MEPIC abstract:
+//   warps 4-11 transform: K rotated by RoPE at each key's absolute position (MEPIC abstract:
 //              K is kept without positional encoding and RoPE is fused into attention) into
 //              the fp16 K-major operand; V converted to fp16 in place (it stays [key][dim],
 //              the MN-major operand of O += P V). cos/sin(p theta) is composed from the table
 //              row of the page start and that of the offset inside the page (the latter held
 //              in registers: each thread always rotates the same row offset and dims).
-//   warp 8     TMEM owner; one thread issues S = Q K^T (M128 N64 K128) into one of two TMEM
+//   warp 12    TMEM owner; one thread issues S = Q K^T (M128 N64 K128) into one of two TMEM
 //              buffers and O += P V (M128 N128 K64) with tcgen05.mma kind::f16.
 //   warps 0-3  softmax: thread = one MMA row = one TMEM lane. Reads its row of S, masks keys
 //              after its position (only on tiles that need it), keeps a running reference
@@ -45,8 +46,12 @@ constexpr int D = 128;
 constexpr int REP = 4;
 constexpr int RB = 32;                    // query rows per item
 constexpr int KT = 64;                    // keys per tile (4 pages)
-constexpr int NSLOT = 3;                  // raw K/V tiles in flight
-constexpr int kThreads = 10 * 32;
+constexpr int NKS = 3;                    // raw K tiles (freed once rotated)
+constexpr int NVS = 4;                    // V tiles (freed once their PV retired); also indexes the
+                                          // page metadata, cos/sin rows and key positions of a tile
+constexpr int kTransformWarps = 8;
+constexpr int kThreads = (4 + kTransformWarps + 2) * 32;
+constexpr int W_MMA = 4 + kTransformWarps, W_LOAD = W_MMA + 1;
 constexpr float kRescale = 8.f;           // rescale O when the row max grows by more than 2^8
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
@@ -55,20 +60,20 @@ constexpr int OFF_Q = 0;                          // 2 halves x [128 rows][128 B
 constexpr int OFF_KOP = OFF_Q + 32768;            // [2][2 halves][64 keys][128 B] fp16     32 KB
 constexpr int OFF_P = OFF_KOP + 32768;            // [2][128 rows][128 B] fp16              32 KB
 constexpr int OFF_KRAW = OFF_P + 32768;           // [3][2 halves][64 keys][128 B] bf16     48 KB
-constexpr int OFF_V = OFF_KRAW + NSLOT * 16384;   // [3][2 halves][64 keys][128 B] bf16->fp16 48 KB
-constexpr int OFF_CS = OFF_V + NSLOT * 16384;     // [3][4 pages][512 B] cos/sin rows         6 KB
-constexpr int OFF_TM = OFF_CS + NSLOT * 2048;     // int [3][4][2] page start, valid rows
-constexpr int OFF_POS = OFF_TM + 128;             // int [2][KT] key positions (INT_MAX = none)
-constexpr int OFF_TILE = OFF_POS + 2 * KT * 4;    // int [2] last key position, INT_MAX if ragged
+constexpr int OFF_V = OFF_KRAW + NKS * 16384;     // [4][2 halves][64 keys][128 B] bf16->fp16 64 KB
+constexpr int OFF_CS = OFF_V + NVS * 16384;       // [4][4 pages][512 B] cos/sin rows         8 KB
+constexpr int OFF_TM = OFF_CS + NVS * 2048;       // int [4][4][2] page start, valid rows
+constexpr int OFF_POS = OFF_TM + NVS * 32;        // int [4][KT] key positions (INT_MAX = none)
+constexpr int OFF_TILE = OFF_POS + NVS * KT * 4;  // int [4] last key position, INT_MAX if ragged
 constexpr int OFF_BAR = OFF_TILE + 16;
-constexpr int N_BARS = 24;
+constexpr int N_BARS = 28;
 constexpr int SMEM_BYTES = OFF_BAR + N_BARS * 8 + 16;
 static_assert(OFF_BAR % 8 == 0, "mbarrier alignment");
 static_assert(SMEM_BYTES + 1024 <= 227 * 1024, "shared memory budget");
 
 // barrier slots
-constexpr int B_KVFULL = 0, B_SFULL = 2, B_SFREE = 4, B_PFULL = 6, B_PVDONE = 8, B_RAWFULL = 10, B_KRFREE = 13,
-              B_VFREE = 16, B_QFULL = 19, B_QFREE = 20, B_OFREE = 21, B_MMADONE = 22;
+constexpr int B_KVFULL = 0, B_SFULL = 2, B_SFREE = 4, B_PFULL = 6, B_PVDONE = 8, B_RAWFULL = 10, B_KRFREE = 14,
+              B_VFREE = 17, B_QFULL = 21, B_QFREE = 22, B_OFREE = 23, B_MMADONE = 24;
 
 __device__ int g_attn_timeout = 0;
 
@@ -231,24 +236,24 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
   if (tid == 0) {
     s_abort = 0;
     for (int i = 0; i < 2; ++i) {
-      mbar_init(bar(B_KVFULL + i), 4);
+      mbar_init(bar(B_KVFULL + i), kTransformWarps);
       mbar_init(bar(B_SFULL + i), 1);
       mbar_init(bar(B_SFREE + i), 4);
       mbar_init(bar(B_PFULL + i), 4);
       mbar_init(bar(B_PVDONE + i), 1);
     }
-    for (int i = 0; i < NSLOT; ++i) {
+    for (int i = 0; i < NVS; ++i) {
       mbar_init(bar(B_RAWFULL + i), 1);
-      mbar_init(bar(B_KRFREE + i), 4);
       mbar_init(bar(B_VFREE + i), 1);
     }
+    for (int i = 0; i < NKS; ++i) mbar_init(bar(B_KRFREE + i), kTransformWarps);
     mbar_init(bar(B_QFULL), 1);
     mbar_init(bar(B_QFREE), 1);
     mbar_init(bar(B_OFREE), 4);
     mbar_init(bar(B_MMADONE), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp == 8) {
+  if (warp == W_MMA) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
                  "r"(256));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
@@ -270,7 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       const int qp = r < it.nrows ? a.q_pos[it.row0 + r] : -1;
       float mref = -INFINITY, l = 0.f;
       for (int j = 0; j < nt; ++j, ++gt) {
-        const int b = gt & 1;
+        const int b = gt & 1, sl = gt % NVS;
         const uint32_t u = gt >> 1;
         // kv_full of the same tile also orders this thread after the transform's key positions
         ok = __all_sync(0xffffffffu, !s_abort && mbar_wait(bar(B_SFULL + b), u & 1) &&
@@ -284,8 +289,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(B_SFREE + b));
-        if (__any_sync(0xffffffffu, sTile[b] > qp)) {
-          const int4* kp = reinterpret_cast<const int4*>(sPos + b * KT);
+        if (__any_sync(0xffffffffu, sTile[sl] > qp)) {
+          const int4* kp = reinterpret_cast<const int4*>(sPos + sl * KT);
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const int4 k4 = kp[i];
@@ -359,28 +364,31 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       const int h = it.g * REP + hh;
       const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll 1
-      for (int c = 0; c < 128; c += 16) {
-        float o[16];
+      for (int c0 = 0; c0 < 128; c0 += 64) {   // 64 columns per TMEM round trip
+        float o[64];
         if (nt > 0) {
-          tmem_ld16(trow + c, o);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) tmem_ld16(trow + c0 + 16 * c, o + 16 * c);
           tmem_wait_ld();
         } else {
 #pragma unroll
-          for (int e = 0; e < 16; ++e) o[e] = 0.f;
+          for (int e = 0; e < 64; ++e) o[e] = 0.f;
         }
         if (it.part < 0) {
           if (r < it.nrows) {
-            uint32_t hv[8];
+            uint4* dst = reinterpret_cast<uint4*>((__half*)a.out + ((size_t)(it.row0 + r) * a.H + h) * D + c0);
 #pragma unroll
-            for (int e = 0; e < 16; e += 2) hv[e / 2] = pack_f16x2(o[e] * inv, o[e + 1] * inv);
-            uint4* dst = reinterpret_cast<uint4*>((__half*)a.out + ((size_t)(it.row0 + r) * a.H + h) * D + c);
-            dst[0] = make_uint4(hv[0], hv[1], hv[2], hv[3]);
-            dst[1] = make_uint4(hv[4], hv[5], hv[6], hv[7]);
+            for (int c = 0; c < 8; ++c)
+              dst[c] = make_uint4(pack_f16x2(o[8 * c] * inv, o[8 * c + 1] * inv),
+                                  pack_f16x2(o[8 * c + 2] * inv, o[8 * c + 3] * inv),
+                                  pack_f16x2(o[8 * c + 4] * inv, o[8 * c + 5] * inv),
+                                  pack_f16x2(o[8 * c + 6] * inv, o[8 * c + 7] * inv));
           }
         } else {
-          float4* dst = reinterpret_cast<float4*>(a.part_o + (((size_t)it.part * kAttnPartRows + r) * REP + hh) * D + c);
+          float4* dst =
+              reinterpret_cast<float4*>(a.part_o + (((size_t)it.part * kAttnPartRows + r) * REP + hh) * D + c0);
 #pragma unroll
-          for (int e = 0; e < 4; ++e) dst[e] = make_float4(o[4 * e], o[4 * e + 1], o[4 * e + 2], o[4 * e + 3]);
+          for (int e = 0; e < 16; ++e) dst[e] = make_float4(o[4 * e], o[4 * e + 1], o[4 * e + 2], o[4 * e + 3]);
         }
       }
       if (nt > 0) {
@@ -394,10 +402,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       }
     }
     if (!ok) s_abort = 1;
-  } else if (warp < 8) {
+  } else if (warp < W_MMA) {
     // =============================== transform warps
     const int tt = tid - 128, tw = warp - 4;
-    const int rr = lane & 15, cq = 2 * tw + (lane >> 4);   // K: row offset in page, dims 8cq.. and 64 + 8cq..
+    // K: row offset rr of pages pg0, pg0 + 1; dims 8cq..8cq+7 and 64 + 8cq..
+    const int rr = lane & 15, cq = 2 * (tw & 3) + (lane >> 4), pg0 = 2 * (tw >> 2);
     float2 lo[8];   // (cos, sin)(rr theta_i) for this thread's 8 frequencies
 #pragma unroll
     for (int e = 0; e < 8; ++e) lo[e] = a.rope_cs[rr * 64 + 8 * cq + e];
@@ -406,18 +415,20 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     for (int ii = blockIdx.x; ii < a.n_items && ok; ii += gridDim.x) {
       const int nt = item_tiles(a.items[ii]);
       for (int j = 0; j < nt; ++j, ++gt) {
-        const int b = gt & 1, s = gt % NSLOT;
-        const uint32_t u = gt >> 1, k = gt / NSLOT;
-        // raw tile landed; K operand buffer b and its key positions free once PV of tile gt - 2 retired
-        ok = __all_sync(0xffffffffu, !s_abort && mbar_wait(bar(B_RAWFULL + s), k & 1) &&
-                                         (gt < 2 || mbar_wait(bar(B_PVDONE + b), (u - 1) & 1)));
+        const int b = gt & 1, s = gt % NVS, ks = gt % NKS;
+        const uint32_t u = gt >> 1;
+        // raw tile landed; K operand buffer b free once S of tile gt - 2 has completed (the
+        // key positions live per V slot: their next writer waits on this slot's loads, which
+        // wait for PV of this tile)
+        ok = __all_sync(0xffffffffu, !s_abort && mbar_wait(bar(B_RAWFULL + s), (gt / NVS) & 1) &&
+                                         (gt < 2 || mbar_wait(bar(B_SFULL + b), (u - 1) & 1)));
         if (!ok) break;
         const int* tm = sTm + s * 8;
-        const uint8_t* kraw = sm + OFF_KRAW + s * 16384;
+        const uint8_t* kraw = sm + OFF_KRAW + ks * 16384;
         uint8_t* kop = sm + OFF_KOP + b * 16384;
-        // K: rotate row offset rr of each of the four pages
+        // K: rotate row offset rr of pages pg0 and pg0 + 1
 #pragma unroll 1
-        for (int pg = 0; pg < 4; ++pg) {
+        for (int pg = pg0; pg < pg0 + 2; ++pg) {
           const int key = pg * 16 + rr, start = tm[2 * pg], len = tm[2 * pg + 1];
           uint4 y1 = make_uint4(0, 0, 0, 0), y2 = y1;
           if (rr < len) {
@@ -447,7 +458,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
           }
           *reinterpret_cast<uint4*>(kop + sw128(key, cq)) = y1;
           *reinterpret_cast<uint4*>(kop + 8192 + sw128(key, cq)) = y2;
-          if (cq == 0) sPos[b * KT + key] = rr < len ? start + rr : INT_MAX;
+          if (cq == 0) sPos[s * KT + key] = rr < len ? start + rr : INT_MAX;
         }
         if (tt == 0) {   // last key position of the tile; INT_MAX when some slot holds no key
           int kmax = -1;
@@ -457,13 +468,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
             if (len > 0) kmax = tm[2 * pg] + len - 1;
             if (len < kBlock) full = false;
           }
-          sTile[b] = full ? kmax : INT_MAX;
+          sTile[s] = full ? kmax : INT_MAX;
         }
         // V: bf16 -> fp16 in place; rows without a key become 0 (P is 0 there, V must be finite)
         uint8_t* vt = sm + OFF_V + s * 16384;
-#pragma unroll 4
-        for (int i = 0; i < 8; ++i) {
-          const int ch = tt + 128 * i, key = (ch >> 3) & 63;
+#pragma unroll
+        for (int i = 0; i < 1024 / (32 * kTransformWarps); ++i) {
+          const int ch = tt + 32 * kTransformWarps * i, key = (ch >> 3) & 63;
           uint4* p = reinterpret_cast<uint4*>(vt + ch * 16);
           if ((key & 15) < tm[2 * (key >> 4) + 1]) {
             const uint4 w = *p;
@@ -475,13 +486,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         fence_async_smem();
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive(bar(B_KRFREE + s));
+          mbar_arrive(bar(B_KRFREE + ks));
           mbar_arrive(bar(B_KVFULL + b));
         }
       }
     }
     if (!ok) s_abort = 1;
-  } else if (warp == 8) {
+  } else if (warp == W_MMA) {
     // =============================== MMA issuer
     if (lane == 0) {
       const uint32_t id_s = idesc_f16(128, KT, false), id_pv = idesc_f16(128, D, true);
@@ -522,7 +533,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
             }
             if (j + 2 == nt) umma_commit(bar(B_QFREE));   // every S of this item issued
           }
-          const int b = g & 1, s = g % NSLOT;
+          const int b = g & 1, s = g % NVS;
           if (s_abort || !mbar_wait(bar(B_PFULL + b), (g >> 1) & 1)) {
             ok = false;
             break;
@@ -555,8 +566,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       const AttnItem it = a.items[ii];
       const int nt = item_tiles(it);
       for (int j = 0; j < nt; ++j, ++gt) {
-        const int s = gt % NSLOT;
-        const uint32_t k = gt / NSLOT;
+        const int s = gt % NVS, ks = gt % NKS;
+        const uint32_t kv = gt / NVS, kk = gt / NKS;
         const int p0 = it.page0 + 4 * j, np = min(4, it.page1 - p0);
         if (j == 0 || p0 + 4 > w0 + 32) {
           w0 = p0;
@@ -574,10 +585,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
           pos[q] = __shfl_sync(0xffffffffu, wpos, p0 - w0 + q);
           len[q] = q < np ? __shfl_sync(0xffffffffu, wlen, p0 - w0 + q) : 0;
         }
-        // slot s free: its K consumed by the transform and its V by PV of tile gt - 3
+        // K slot ks free once tile gt - 3 was rotated, V slot s once PV of tile gt - 4 retired
         if (lane == 0)
-          ok = !s_abort && (k == 0 || (mbar_wait(bar(B_KRFREE + s), (k - 1) & 1) &&
-                                       mbar_wait(bar(B_VFREE + s), (k - 1) & 1)));
+          ok = !s_abort && (kk == 0 || mbar_wait(bar(B_KRFREE + ks), (kk - 1) & 1)) &&
+               (kv == 0 || mbar_wait(bar(B_VFREE + s), (kv - 1) & 1));
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
         if (lane == 0) {
@@ -588,7 +599,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
           }
           const uint32_t fb = bar(B_RAWFULL + s);
           mbar_expect_tx(fb, (uint32_t)np * (4 * 2048 + 512));
-          const uint32_t kd = smem_u32(sm + OFF_KRAW + s * 16384), vd = smem_u32(sm + OFF_V + s * 16384);
+          const uint32_t kd = smem_u32(sm + OFF_KRAW + ks * 16384), vd = smem_u32(sm + OFF_V + s * 16384);
           for (int q = 0; q < np; ++q) {
             const int y = (blk[q] * a.G + it.g) * kBlock;
             tma_2d(kd + q * 2048, &a.kmap, 0, y, fb);
@@ -618,7 +629,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
   __syncwarp();
   fence_before();
   __syncthreads();
-  if (warp == 8) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(256));
+  if (warp == W_MMA) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(256));
 }
 
 int sm_count() {

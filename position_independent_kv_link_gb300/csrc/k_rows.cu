@@ -67,7 +67,6 @@ __device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16* dst, float4
   *reinterpret_cast<uint2*>(dst) = u;
 }
 
-// Reads 4 accumulator floats and clears them for the next GEMM that adds into the buffer.
 template <>
 __device__ __forceinline__ void store4<__half>(__half* dst, float4 v) {
   __half2 a = __floats2half2_rn(v.x, v.y), b = __floats2half2_rn(v.z, v.w);
@@ -77,15 +76,14 @@ __device__ __forceinline__ void store4<__half>(__half* dst, float4 v) {
   *reinterpret_cast<uint2*>(dst) = u;
 }
 
-__device__ __forceinline__ float4 take4(float* __restrict__ acc, size_t off) {
-  float4* p = reinterpret_cast<float4*>(acc + off);
-  const float4 v = *p;
-  *p = make_float4(0.f, 0.f, 0.f, 0.f);
-  return v;
+// 4 accumulator floats (the accumulators are zeroed before their GEMM, not cleared here:
+// clearing behind the read costs about as much again as the read)
+__device__ __forceinline__ float4 take4(const float* __restrict__ acc, size_t off) {
+  return *reinterpret_cast<const float4*>(acc + off);
 }
 
 // QKV epilogue: q -> [T][H*D] fp32; pre-RoPE k, v -> their page slot of this layer. The
-// accumulator [T][N] is cleared behind the read. grid (T, ceil(N / 1024)); a thread owns 4
+// accumulator [T][N] is only read. grid (T, ceil(N / 1024)); a thread owns 4
 // consecutive columns (one head).
 // Dims i..i+3 and i+64..i+67 (i < 64) of one 128-dim q head: rotate-half RoPE at the angles of
 // one table row, times `scale`, rounded once to fp16.
@@ -103,10 +101,8 @@ __device__ __forceinline__ void rope_q16_store(float4 a, float4 b, const float2*
   store4<__half>(dst + 64 + i, make_float4(y2[0], y2[1], y2[2], y2[3]));
 }
 
-constexpr float kQ16Scale = 1.4426950408889634f * 0.08838834764831845f;   // log2(e) / sqrt(128)
-
 template <typename T>
-__global__ void qkv_epilogue_kernel(int H, int G, int D, float* __restrict__ acc, float* __restrict__ q,
+__global__ void qkv_epilogue_kernel(int H, int G, int D, const float* __restrict__ acc, float* __restrict__ q,
                                     const int* __restrict__ slot, T* __restrict__ kl, T* __restrict__ vl,
                                     const int* __restrict__ pos, const float2* __restrict__ rope_cs,
                                     __half* __restrict__ q16) {
@@ -172,9 +168,9 @@ __global__ void __launch_bounds__(512) rmsnorm_rows_kernel(int d, const float* _
 }
 
 // act = silu(gate) * up from the accumulator [T][2F] (gate columns, then up columns), which
-// is cleared behind the read. grid (T, ceil(F / 1024)); 4 outputs per thread.
+// is only read. grid (T, ceil(F / 1024)); 4 outputs per thread.
 template <typename T>
-__global__ void swiglu_kernel(int F, float* __restrict__ acc, T* __restrict__ act) {
+__global__ void swiglu_kernel(int F, const float* __restrict__ acc, T* __restrict__ act) {
   const int t = blockIdx.x;
   const int j = (blockIdx.y * blockDim.x + threadIdx.x) * 4;
   if (j >= F) return;

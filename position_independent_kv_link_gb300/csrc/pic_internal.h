@@ -48,7 +48,7 @@ inline size_t act_size(int dtype) { return dtype == PIC_BF16 ? 2 : 4; }
 // h[t] = E[tok[t]] (fp32); x[t] = RMSNorm(h[t]) * gain in the activation type.
 void launch_embed_norm(int dtype, int T, int d, const void* embed, const int* tok, const float* gain, float eps,
                        float* h, void* x, cudaStream_t st);
-// QKV epilogue: reads (and clears) the fp32 accumulator [T][(H+2G)D], writes the pre-RoPE
+// QKV epilogue: reads the fp32 accumulator [T][(H+2G)D], writes the pre-RoPE
 // k, v rows (model dtype) into their page slots of one layer, and q [T][H][D]: fp32 pre-RoPE
 // when q16 is null, else (q16 non-null, D = 128) rotated at pos[t] with the cos/sin table,
 // times log2(e)/sqrt(D), in fp16 into q16 -- the operand of the tensor-core attention.
@@ -64,7 +64,7 @@ void launch_rmsnorm_rows(int dtype, int T, int d, const float* h, const float* g
                          bool final_layer, const int* out_row, float* hidden_out, const int* lg_row, void* lm_x,
                          cudaStream_t st);
 // act[t][j] = silu(gate) * up (activation type) from the accumulator [T][2F] (gate cols, then
-// up cols), cleared behind.
+// up cols).
 void launch_swiglu(int dtype, int T, int F, float* acc, void* act, cudaStream_t st);
 // For each pair i: copy block src[i] -> dst[i] in every layer of both pools.
 void launch_copy_blocks(int n_pairs, const int* pairs, int n_layers, int num_blocks_total, size_t block_bytes,
@@ -84,6 +84,9 @@ bool tc_gemm_supported(int N, int K, int T);
 // Y[T][N] (fp32, 16-byte aligned) += X[T][K] . W[N][K]^T on tcgen05 (persistent stream-K),
 // W and X bf16.
 pic_status tc_gemm_run(const void* W, const void* X, float* Y, int N, int K, int T, cudaStream_t st);
+// Scale folded into the fp16 q operand of the tensor-core attention: log2(e) / sqrt(128).
+constexpr float kQ16Scale = 1.4426950408889634f * 0.08838834764831845f;
+
 // Same with fp16 weights in the tile layout written by tc_pack_weight and fp16 X.
 pic_status tc_gemm_run_packed(const void* Wp, const void* X, float* Y, int N, int K, int T, cudaStream_t st);
 // [N][K] bf16 -> N*K*2 bytes of fp16 16 KB tiles (128 rows x 64 k, 128-byte swizzled image),
