@@ -193,11 +193,12 @@ pic_status pic_sync(pic_store* s, pic_stream_t stream);
  * FLOPs of that launch (operands read once, results written once). Launch counting is
  * always on. Classes: */
 enum {
-  PIC_PROF_GEMM = 0,       /* tcgen05 / SIMT projection GEMMs (incl. LM head) */
+  PIC_PROF_GEMM = 0,       /* tcgen05 / SIMT projection GEMMs (incl. LM head) except gate/up */
   PIC_PROF_ATTENTION = 1,  /* paged attention + split merge */
   PIC_PROF_ROWWISE = 2,    /* embedding/norm, split-K epilogues, SwiGLU */
-  PIC_PROF_COPY = 3,       /* request-private block copies, KV import */
-  PIC_PROF_CLASSES = 4
+  PIC_PROF_COPY = 3,       /* request-private block copies, KV import, accumulator zeroing */
+  PIC_PROF_GEMM_GATE_UP = 4, /* the MLP gate/up projection GEMM (the largest weight stream) */
+  PIC_PROF_CLASSES = 5
 };
 typedef struct {
   int64_t launches[PIC_PROF_CLASSES];  /* kernel launches recorded while profiling */

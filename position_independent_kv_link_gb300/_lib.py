@@ -40,7 +40,7 @@ class RequestInfo(C.Structure):
                 ("private_blocks", C.POINTER(C.c_int32))]
 
 
-PROF_CLASSES = 4
+PROF_CLASSES = 5
 
 
 class Profile(C.Structure):

@@ -196,7 +196,7 @@ class PicStore:
         """Per kernel class: launches, summed event ms, algorithmic bytes and FLOPs."""
         p = L.Profile()
         L.check(self.lib.pic_profile_end(self.handle, C.byref(p)))
-        names = ["gemm", "attention", "rowwise", "copy"]
+        names = ["gemm", "attention", "rowwise", "copy", "gemm_gate_up"]
         out = {n: {"launches": int(p.launches[i]), "ms": p.ms[i], "bytes": p.bytes[i], "flops": p.flops[i]}
                for i, n in enumerate(names)}
         out["total_launches"] = int(p.total_launches)

@@ -330,8 +330,9 @@ pic_status run_forward_impl(pic_store* s, const Batch& b, float* hidden_out, flo
 
   const int qkv = s->m->qkv_dim();
   auto gemm_bytes = [&](double N, double K, double rows) { return N * K * es + rows * K * es + rows * N * 4; };
-  auto run_gemm = [&](const void* W, const void* Wp, const void* X, float* Y, int N, int K, int rows) {
-    Rec r(s, st, PIC_PROF_GEMM, gemm_bytes(N, K, rows), 2.0 * N * K * rows, 1);
+  auto run_gemm = [&](const void* W, const void* Wp, const void* X, float* Y, int N, int K, int rows,
+                      int cls = PIC_PROF_GEMM) {
+    Rec r(s, st, cls, gemm_bytes(N, K, rows), 2.0 * N * K * rows, 1);
     return gemm(s, W, Wp, X, Y, N, K, rows, st);
   };
   // The QKV and gate/up GEMMs reduce into fp32 accumulators zeroed by a memset just before
@@ -375,7 +376,8 @@ pic_status run_forward_impl(pic_store* s, const Batch& b, float* hidden_out, flo
                           nullptr, st);
     }
     if ((e = zero_acc(s->gu_acc, (size_t)T * 2 * F)) != PIC_OK) return e;
-    if ((e = run_gemm(s->m->wgu[l], pk(s->m->pgu, l), s->x, s->gu_acc, 2 * F, d, T)) != PIC_OK) return e;
+    if ((e = run_gemm(s->m->wgu[l], pk(s->m->pgu, l), s->x, s->gu_acc, 2 * F, d, T, PIC_PROF_GEMM_GATE_UP)) != PIC_OK)
+      return e;
     {
       Rec r(s, st, PIC_PROF_ROWWISE, dT * 2 * dF * 4 + dT * dF * es, 0, 1);
       launch_swiglu(dt, T, F, s->gu_acc, s->act, st);
