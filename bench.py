@@ -122,6 +122,21 @@ def dist_env():
     return world, rank, local
 
 
+def slowest_rank(x: float, world: int, device: str = "cuda") -> float:
+    """Max over ranks of a per-rank elapsed time: the whole job's time in a weak-scaled run."""
+    if world <= 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank: float, world: int, seconds: float) -> float:
+    """Whole-job rate: every rank processed units_per_rank; seconds is the slowest rank's time."""
+    return world * units_per_rank / seconds
+
+
 def workload(name: str) -> pi.Workload:
     return pi.config_workloads()[name]
 
@@ -306,14 +321,10 @@ def run_ours(args):
     torch.cuda.synchronize()
     clk = clocks.stop()
     store.sync()
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = slowest_rank(ms, world)
     ms_step = ms / args.steps
     tokens = wl.linked_tokens
-    value = world * tokens * args.steps / (ms / 1e3)
+    value = job_throughput(tokens * args.steps, world, ms / 1e3)
 
     # end to end through the public API: host query tokens in, hidden + logits to pinned host
     hid_h = torch.empty(hid.shape, dtype=hid.dtype, pin_memory=True)
@@ -331,13 +342,8 @@ def run_ours(args):
     w0 = time.perf_counter()
     for _ in range(args.steps):
         e2e_step()
-    w_s = time.perf_counter() - w0
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([w_s], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        w_s = float(t.item())
-    e2e_value = world * tokens * args.steps / w_s
+    w_s = slowest_rank(time.perf_counter() - w0, world)
+    e2e_value = job_throughput(tokens * args.steps, world, w_s)
     h2d = sum(4 * (len(r.query) + len(r.chunk_ids)) for r in wl.requests)
     d2h = hid.numel() * 4 + lg.numel() * 4
 
