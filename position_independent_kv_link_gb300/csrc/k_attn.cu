@@ -95,9 +95,11 @@ __global__ void __launch_bounds__(128) attn_simt_kernel(AttnArgs a) {
   }
 }
 
-// Merge split results: out = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s, in one pass
-// with a running maximum. grid (merges, ceil(16 * rep / 8)); one warp per (row, head),
-// D/32 consecutive dims per lane.
+// Merge split results: out = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s with M = max_s m_s
+// over the parts that saw a key (l_s > 0). grid (merges, ceil(rows * rep / 8)); one warp per
+// (row, head). The lanes first read the parts' (m, l) side by side (32 parts per pass) and
+// reduce M and the denominator across the warp; then each lane sums its D/32 dims over the
+// parts with the weights broadcast, the parts' loads independent of each other.
 template <typename O, int D>
 __global__ void __launch_bounds__(256) attn_combine_kernel(AttnArgs a) {
   constexpr int NJ = D / 32;
@@ -106,29 +108,46 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(AttnArgs a) {
   const int pr = blockIdx.y * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   if (pr >= c.nrows * rep) return;
   const int r = pr / rep, hh = pr % rep;
-  float M = -INFINITY, L = 0.f, o[NJ];
+  auto part = [&](int s) { return ((size_t)(c.part0 + s) * kAttnPartRows + r) * rep + hh; };
+  float M = -INFINITY;
+  for (int s0 = 0; s0 < c.nparts; s0 += 32) {
+    const int s = s0 + lane;
+    if (s < c.nparts) {
+      const float2 ml = *reinterpret_cast<const float2*>(a.part_ml + part(s) * 2);
+      if (ml.y > 0.f) M = fmaxf(M, ml.x);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  float o[NJ], L = 0.f;
 #pragma unroll
   for (int j = 0; j < NJ; ++j) o[j] = 0.f;
-#pragma unroll 4
-  for (int s = 0; s < c.nparts; ++s) {
-    const size_t pi = ((size_t)(c.part0 + s) * kAttnPartRows + r) * rep + hh;
-    const float2 ml = *reinterpret_cast<const float2*>(a.part_ml + pi * 2);
-    float v[NJ];
-    if constexpr (NJ == 4) {
-      const float4 x = *reinterpret_cast<const float4*>(a.part_o + pi * D + lane * 4);
-      v[0] = x.x, v[1] = x.y, v[2] = x.z, v[3] = x.w;
-    } else {
-      const float2 x = *reinterpret_cast<const float2*>(a.part_o + pi * D + lane * 2);
-      v[0] = x.x, v[1] = x.y;
+  for (int s0 = 0; s0 < c.nparts; s0 += 32) {
+    const int s = s0 + lane;
+    float w = 0.f;   // this lane's part weight
+    if (s < c.nparts) {
+      const float2 ml = *reinterpret_cast<const float2*>(a.part_ml + part(s) * 2);
+      if (ml.y > 0.f) {
+        w = exp2f(ml.x - M);
+        L += w * ml.y;
+      }
     }
-    if (ml.y == 0.f) continue;  // this run saw no key at or before the row's position
-    const float Mn = fmaxf(M, ml.x);
-    const float wa = exp2f(M - Mn), wb = exp2f(ml.x - Mn);
-    L = L * wa + ml.y * wb;
-#pragma unroll
-    for (int j = 0; j < NJ; ++j) o[j] = o[j] * wa + v[j] * wb;
-    M = Mn;
+    const int n = min(32, c.nparts - s0);
+#pragma unroll 4
+    for (int k = 0; k < n; ++k) {
+      const float wk = __shfl_sync(0xffffffffu, w, k);
+      const float* src = a.part_o + part(s0 + k) * D + lane * NJ;
+      if constexpr (NJ == 4) {
+        const float4 x = *reinterpret_cast<const float4*>(src);
+        o[0] += wk * x.x, o[1] += wk * x.y, o[2] += wk * x.z, o[3] += wk * x.w;
+      } else {
+        const float2 x = *reinterpret_cast<const float2*>(src);
+        o[0] += wk * x.x, o[1] += wk * x.y;
+      }
+    }
   }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
   const int t = c.row0 + r, h = c.g * rep + hh;
   const float inv = L > 0.f ? 1.f / L : 0.f;
   O* out = (O*)a.out + ((size_t)t * a.H + h) * D + lane * NJ;

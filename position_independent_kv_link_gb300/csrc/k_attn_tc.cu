@@ -5,17 +5,17 @@
 // heads sharing KV head g x a run of pages. The 32 rows x 4 heads form one M = 128 MMA tile
 // (row m = head * 32 + row), so each 64-key tile (4 pages) of K and V is staged once for all.
 //
-//   warp 13    loads: TMA boxes of each page's pre-RoPE K and V (16 rows x 64 dims, 128-byte
-//              swizzled; raw K is held until rotated, three tiles deep, V until its PV, four
-//              deep), the cos/sin table rows of the page starts
-//              (bulk copies) and, per item, the Q tile (rotated and scaled fp16 rows written by
-//              the QKV epilogue).
+//   warp 13    loads: one TMA box per page for its pre-RoPE K and one for its V (16 rows x both
+//              64-dim halves, 4 KB, 128-byte swizzled; two tiles in flight), the cos/sin table
+//              rows of the page starts (plain loads by the warp's lanes) and, per item, the Q
+//              tile (rotated and scaled fp16 rows written by the QKV epilogue).
 //   warps 4-11 transform: K rotated by RoPE at each key's absolute position (MEPIC abstract:
 //              K is kept without positional encoding and RoPE is fused into attention) into
-//              the fp16 K-major operand; V converted to fp16 in place (it stays [key][dim],
-//              the MN-major operand of O += P V). cos/sin(p theta) is composed from the table
-//              row of the page start and that of the offset inside the page (the latter held
-//              in registers: each thread always rotates the same row offset and dims).
+//              the fp16 K-major operand; V converted to fp16 into the MN-major operand of
+//              O += P V ([key][dim], three tiles held until their PV). cos/sin(p theta) is
+//              composed from the table row of the page start and that of the offset inside the
+//              page (the latter held in registers: each thread always rotates the same row
+//              offset and dims).
 //   warp 12    TMEM owner; one thread issues S = Q K^T (M128 N64 K128) into one of two TMEM
 //              buffers and O += P V (M128 N128 K64) with tcgen05.mma kind::f16.
 //   warps 0-3  softmax: thread = one MMA row = one TMEM lane. Reads its row of S, masks keys
@@ -46,9 +46,10 @@ constexpr int D = 128;
 constexpr int REP = 4;
 constexpr int RB = 32;                    // query rows per item
 constexpr int KT = 64;                    // keys per tile (4 pages)
-constexpr int NKS = 3;                    // raw K tiles (freed once rotated)
-constexpr int NVS = 4;                    // V tiles (freed once their PV retired); also indexes the
-                                          // page metadata, cos/sin rows and key positions of a tile
+constexpr int NRS = 2;                    // raw K/V tiles in flight (freed once transformed); also
+                                          // indexes the page metadata and cos/sin rows of a tile
+constexpr int NVS = 3;                    // fp16 V operand tiles (freed once their PV retired); also
+                                          // indexes the key positions of a tile
 constexpr int kTransformWarps = 8;
 constexpr int kThreads = (4 + kTransformWarps + 2) * 32;
 constexpr int W_MMA = 4 + kTransformWarps, W_LOAD = W_MMA + 1;
@@ -59,21 +60,23 @@ constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 constexpr int OFF_Q = 0;                          // 2 halves x [128 rows][128 B] fp16      32 KB
 constexpr int OFF_KOP = OFF_Q + 32768;            // [2][2 halves][64 keys][128 B] fp16     32 KB
 constexpr int OFF_P = OFF_KOP + 32768;            // [2][128 rows][128 B] fp16              32 KB
-constexpr int OFF_KRAW = OFF_P + 32768;           // [3][2 halves][64 keys][128 B] bf16     48 KB
-constexpr int OFF_V = OFF_KRAW + NKS * 16384;     // [4][2 halves][64 keys][128 B] bf16->fp16 64 KB
-constexpr int OFF_CS = OFF_V + NVS * 16384;       // [4][4 pages][512 B] cos/sin rows         8 KB
-constexpr int OFF_TM = OFF_CS + NVS * 2048;       // int [4][4][2] page start, valid rows
-constexpr int OFF_POS = OFF_TM + NVS * 32;        // int [4][KT] key positions (INT_MAX = none)
-constexpr int OFF_TILE = OFF_POS + NVS * KT * 4;  // int [4] last key position, INT_MAX if ragged
+// raw pages as TMA writes them: [page][16 rows][2 halves][128 B], the 128-byte rows swizzled
+constexpr int OFF_KRAW = OFF_P + 32768;           // [2][4 pages][4 KB] bf16                  32 KB
+constexpr int OFF_VRAW = OFF_KRAW + NRS * 16384;  // [2][4 pages][4 KB] bf16                  32 KB
+constexpr int OFF_V = OFF_VRAW + NRS * 16384;     // [3][2 halves][64 keys][128 B] fp16       48 KB
+constexpr int OFF_CS = OFF_V + NVS * 16384;       // [2][4 pages][512 B] cos/sin rows          4 KB
+constexpr int OFF_TM = OFF_CS + NRS * 2048;       // int [2][4][2] page start, valid rows
+constexpr int OFF_POS = OFF_TM + 128;             // int [3][KT] key positions (INT_MAX = none)
+constexpr int OFF_TILE = OFF_POS + NVS * KT * 4;  // int [3] last key position, INT_MAX if ragged
 constexpr int OFF_BAR = OFF_TILE + 16;
-constexpr int N_BARS = 28;
+constexpr int N_BARS = 24;
 constexpr int SMEM_BYTES = OFF_BAR + N_BARS * 8 + 16;
 static_assert(OFF_BAR % 8 == 0, "mbarrier alignment");
 static_assert(SMEM_BYTES + 1024 <= 227 * 1024, "shared memory budget");
 
 // barrier slots
-constexpr int B_KVFULL = 0, B_SFULL = 2, B_SFREE = 4, B_PFULL = 6, B_PVDONE = 8, B_RAWFULL = 10, B_KRFREE = 14,
-              B_VFREE = 17, B_QFULL = 21, B_QFREE = 22, B_OFREE = 23, B_MMADONE = 24;
+constexpr int B_KVFULL = 0, B_SFULL = 2, B_SFREE = 4, B_PFULL = 6, B_PVDONE = 8, B_RAWFULL = 10, B_RAWFREE = 12,
+              B_VFREE = 14, B_QFULL = 17, B_QFREE = 18, B_OFREE = 19, B_MMADONE = 20;
 
 __device__ int g_attn_timeout = 0;
 
@@ -91,6 +94,10 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
 }
 __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+// expected transaction bytes without an arrival (the arrival follows separately)
+__device__ __forceinline__ void mbar_add_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
 __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
   uint32_t ok;
@@ -112,13 +119,6 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
     }
   }
 }
-__device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
-          dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
-      : "memory");
-}
 __device__ __forceinline__ void tma_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z, uint32_t bar) {
   asm volatile(
       "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
@@ -126,12 +126,6 @@ __device__ __forceinline__ void tma_3d(uint32_t dst, const CUtensorMap* map, int
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
       : "memory");
 }
-__device__ __forceinline__ void bulk_1d(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
-               : "memory");
-}
-
 // 16-byte chunk c (0..7) of row r of a [rows][128 B] tile, 128-byte swizzle (the TMA and UMMA layout)
 __device__ __forceinline__ uint32_t sw128(int r, int c) { return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4)); }
 
@@ -242,11 +236,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       mbar_init(bar(B_PFULL + i), 4);
       mbar_init(bar(B_PVDONE + i), 1);
     }
-    for (int i = 0; i < NVS; ++i) {
+    for (int i = 0; i < NRS; ++i) {
       mbar_init(bar(B_RAWFULL + i), 1);
-      mbar_init(bar(B_VFREE + i), 1);
+      mbar_init(bar(B_RAWFREE + i), kTransformWarps);
     }
-    for (int i = 0; i < NKS; ++i) mbar_init(bar(B_KRFREE + i), kTransformWarps);
+    for (int i = 0; i < NVS; ++i) mbar_init(bar(B_VFREE + i), 1);
     mbar_init(bar(B_QFULL), 1);
     mbar_init(bar(B_QFREE), 1);
     mbar_init(bar(B_OFREE), 4);
@@ -415,27 +409,28 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     for (int ii = blockIdx.x; ii < a.n_items && ok; ii += gridDim.x) {
       const int nt = item_tiles(a.items[ii]);
       for (int j = 0; j < nt; ++j, ++gt) {
-        const int b = gt & 1, s = gt % NVS, ks = gt % NKS;
+        const int b = gt & 1, rs = gt % NRS, s = gt % NVS;
         const uint32_t u = gt >> 1;
-        // raw tile landed; K operand buffer b free once S of tile gt - 2 has completed (the
-        // key positions live per V slot: their next writer waits on this slot's loads, which
-        // wait for PV of this tile)
-        ok = __all_sync(0xffffffffu, !s_abort && mbar_wait(bar(B_RAWFULL + s), (gt / NVS) & 1) &&
-                                         (gt < 2 || mbar_wait(bar(B_SFULL + b), (u - 1) & 1)));
+        // raw tile landed; K operand buffer b free once S of tile gt - 2 has completed; V
+        // operand slot s (and its key positions) once PV of tile gt - 3 has retired
+        ok = __all_sync(0xffffffffu, !s_abort && mbar_wait(bar(B_RAWFULL + rs), (gt / NRS) & 1) &&
+                                         (gt < 2 || mbar_wait(bar(B_SFULL + b), (u - 1) & 1)) &&
+                                         (gt < NVS || mbar_wait(bar(B_VFREE + s), (gt / NVS - 1) & 1)));
         if (!ok) break;
-        const int* tm = sTm + s * 8;
-        const uint8_t* kraw = sm + OFF_KRAW + ks * 16384;
+        const int* tm = sTm + rs * 8;
+        const uint8_t* kraw = sm + OFF_KRAW + rs * 16384;
         uint8_t* kop = sm + OFF_KOP + b * 16384;
-        // K: rotate row offset rr of pages pg0 and pg0 + 1
-#pragma unroll 1
+        // K: rotate row offset rr of pages pg0 and pg0 + 1 (two independent chains)
+#pragma unroll
         for (int pg = pg0; pg < pg0 + 2; ++pg) {
           const int key = pg * 16 + rr, start = tm[2 * pg], len = tm[2 * pg + 1];
           uint4 y1 = make_uint4(0, 0, 0, 0), y2 = y1;
           if (rr < len) {
             float v1[8], v2[8];
-            bf8_to_f32(*reinterpret_cast<const uint4*>(kraw + sw128(key, cq)), v1);
-            bf8_to_f32(*reinterpret_cast<const uint4*>(kraw + 8192 + sw128(key, cq)), v2);
-            const float4* hrow = reinterpret_cast<const float4*>(sm + OFF_CS + (s * 4 + pg) * 512) + 4 * cq;
+            const uint8_t* kp = kraw + pg * 4096;   // 128-byte rows 2 rr (dims 0..63) and 2 rr + 1
+            bf8_to_f32(*reinterpret_cast<const uint4*>(kp + sw128(2 * rr, cq)), v1);
+            bf8_to_f32(*reinterpret_cast<const uint4*>(kp + sw128(2 * rr + 1, cq)), v2);
+            const float4* hrow = reinterpret_cast<const float4*>(sm + OFF_CS + (rs * 4 + pg) * 512) + 4 * cq;
             uint32_t o1[4], o2[4];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
@@ -470,23 +465,26 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
           }
           sTile[s] = full ? kmax : INT_MAX;
         }
-        // V: bf16 -> fp16 in place; rows without a key become 0 (P is 0 there, V must be finite)
+        // V: raw [page][row][half] bf16 -> fp16 [half][key][128 B], the MN-major operand; rows
+        // without a key become 0 (P is 0 there, V must be finite)
+        const uint8_t* vraw = sm + OFF_VRAW + rs * 16384;
         uint8_t* vt = sm + OFF_V + s * 16384;
 #pragma unroll
         for (int i = 0; i < 1024 / (32 * kTransformWarps); ++i) {
-          const int ch = tt + 32 * kTransformWarps * i, key = (ch >> 3) & 63;
-          uint4* p = reinterpret_cast<uint4*>(vt + ch * 16);
-          if ((key & 15) < tm[2 * (key >> 4) + 1]) {
-            const uint4 w = *p;
-            *p = make_uint4(bf2_to_h2(w.x), bf2_to_h2(w.y), bf2_to_h2(w.z), bf2_to_h2(w.w));
-          } else {
-            *p = make_uint4(0, 0, 0, 0);
+          const int ch = tt + 32 * kTransformWarps * i;   // 16-byte chunk of the raw tile
+          const int pg = ch >> 8, rp = (ch >> 3) & 31, r = rp >> 1, h = rp & 1, c = (ch & 7) ^ (rp & 7);
+          const int key = pg * 16 + r;
+          uint4 o = make_uint4(0, 0, 0, 0);
+          if (r < tm[2 * pg + 1]) {
+            const uint4 w = *reinterpret_cast<const uint4*>(vraw + ch * 16);
+            o = make_uint4(bf2_to_h2(w.x), bf2_to_h2(w.y), bf2_to_h2(w.z), bf2_to_h2(w.w));
           }
+          *reinterpret_cast<uint4*>(vt + h * 8192 + sw128(key, c)) = o;
         }
         fence_async_smem();
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive(bar(B_KRFREE + ks));
+          mbar_arrive(bar(B_RAWFREE + rs));
           mbar_arrive(bar(B_KVFULL + b));
         }
       }
@@ -557,7 +555,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       umma_commit(bar(B_MMADONE));   // fires once every MMA of this CTA has retired
       mbar_wait(bar(B_MMADONE), 0);
     }
-  } else {
+  } else if (warp == W_LOAD) {
     // =============================== loads (lane 0 issues; the warp reads page metadata)
     uint32_t gt = 0, ai = 0;
     bool ok = true;
@@ -566,8 +564,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       const AttnItem it = a.items[ii];
       const int nt = item_tiles(it);
       for (int j = 0; j < nt; ++j, ++gt) {
-        const int s = gt % NVS, ks = gt % NKS;
-        const uint32_t kv = gt / NVS, kk = gt / NKS;
+        const int rs = gt % NRS;
+        const uint32_t kr = gt / NRS;
         const int p0 = it.page0 + 4 * j, np = min(4, it.page1 - p0);
         if (j == 0 || p0 + 4 > w0 + 32) {
           w0 = p0;
@@ -585,30 +583,39 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
           pos[q] = __shfl_sync(0xffffffffu, wpos, p0 - w0 + q);
           len[q] = q < np ? __shfl_sync(0xffffffffu, wlen, p0 - w0 + q) : 0;
         }
-        // K slot ks free once tile gt - 3 was rotated, V slot s once PV of tile gt - 4 retired
-        if (lane == 0)
-          ok = !s_abort && (kk == 0 || mbar_wait(bar(B_KRFREE + ks), (kk - 1) & 1)) &&
-               (kv == 0 || mbar_wait(bar(B_VFREE + s), (kv - 1) & 1));
+        // raw slot rs free once the transform is done with tile gt - 2
+        if (lane == 0) ok = !s_abort && (kr == 0 || mbar_wait(bar(B_RAWFREE + rs), (kr - 1) & 1));
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
+        // cos/sin rows of the page starts: 4 x 512 B, one 16-byte chunk per lane and page,
+        // loaded before the TMA issue so that their latency overlaps it
+        float4 cs4[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if (q < np) cs4[q] = reinterpret_cast<const float4*>(a.rope_cs + (size_t)pos[q] * 64)[lane];
+        const uint32_t fb = bar(B_RAWFULL + rs);
         if (lane == 0) {
-          int* tm = sTm + s * 8;
+          int* tm = sTm + rs * 8;
           for (int q = 0; q < 4; ++q) {
             tm[2 * q] = pos[q];
             tm[2 * q + 1] = len[q];
           }
-          const uint32_t fb = bar(B_RAWFULL + s);
-          mbar_expect_tx(fb, (uint32_t)np * (4 * 2048 + 512));
-          const uint32_t kd = smem_u32(sm + OFF_KRAW + ks * 16384), vd = smem_u32(sm + OFF_V + s * 16384);
-          for (int q = 0; q < np; ++q) {
-            const int y = (blk[q] * a.G + it.g) * kBlock;
-            tma_2d(kd + q * 2048, &a.kmap, 0, y, fb);
-            tma_2d(kd + 8192 + q * 2048, &a.kmap, 64, y, fb);
-            tma_2d(vd + q * 2048, &a.vmap, 0, y, fb);
-            tma_2d(vd + 8192 + q * 2048, &a.vmap, 64, y, fb);
-            bulk_1d(smem_u32(sm + OFF_CS + (s * 4 + q) * 512), a.rope_cs + (size_t)pos[q] * 64, 512, fb);
-          }
+          mbar_add_tx(fb, (uint32_t)np * 8192);
         }
+        __syncwarp();
+        if (lane < np) {   // one lane per page issues that page's K and V boxes
+          const uint32_t kd = smem_u32(sm + OFF_KRAW + rs * 16384) + lane * 4096,
+                         vd = smem_u32(sm + OFF_VRAW + rs * 16384) + lane * 4096;
+          const int bq = lane == 0 ? blk[0] : lane == 1 ? blk[1] : lane == 2 ? blk[2] : blk[3];
+          const int y = (bq * a.G + it.g) * kBlock;
+          tma_3d(kd, &a.kmap, 0, 0, y, fb);
+          tma_3d(vd, &a.vmap, 0, 0, y, fb);
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if (q < np) reinterpret_cast<float4*>(sm + OFF_CS + (rs * 4 + q) * 512)[lane] = cs4[q];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(fb);   // releases the metadata and cos/sin rows with the boxes
         if (j == 0) {   // this item's Q, once every S of the previous item has completed
           if (lane == 0) ok = !s_abort && (ai == 0 || mbar_wait(bar(B_QFREE), (ai - 1) & 1));
           ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -671,14 +678,15 @@ bool attn_q_map(CUtensorMap* m, const void* q16, int T, int H) {
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// [rows][128] bf16 viewed as [rows][2 halves][64]: one box = one page (16 rows x both halves)
 bool attn_kv_map(CUtensorMap* m, const void* layer, int pool_blocks, int G) {
   auto enc = encode_fn();
   if (!enc || pool_blocks < 1 || G < 1) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)pool_blocks * G * kBlock};
-  cuuint64_t strides[1] = {(cuuint64_t)D * 2};
-  cuuint32_t box[2] = {64, kBlock};
-  cuuint32_t estr[2] = {1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(layer), dims, strides, box, estr,
+  cuuint64_t dims[3] = {64, 2, (cuuint64_t)pool_blocks * G * kBlock};
+  cuuint64_t strides[2] = {128, (cuuint64_t)D * 2};
+  cuuint32_t box[3] = {64, 2, kBlock};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(layer), dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
