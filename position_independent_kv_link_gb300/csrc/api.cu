@@ -179,7 +179,7 @@ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 // Y[T][N] += X . W^T (fp32 Y accumulated in place); Wp: the packed copy of W, if any
 pic_status gemm(const pic_store* s, const void* W, const void* Wp, const void* X, float* Y, int N, int K, int T,
                 cudaStream_t st) {
-  if (Wp) return tc_gemm_run_packed(Wp, X, Y, N, K, T, st);
+  if (Wp) return tc_gemm_run_packed(Wp, X, Y, N, K, T, st, true);   // model weights: fixed since creation
   launch_gemm_simt(s->m->cfg.dtype, s->m->cfg.dtype == PIC_BF16, W, X, Y, N, K, T, 1, st);
   return PIC_OK;
 }
@@ -335,8 +335,11 @@ pic_status run_forward_impl(pic_store* s, const Batch& b, float* hidden_out, flo
     Rec r(s, st, cls, gemm_bytes(N, K, rows), 2.0 * N * K * rows, 1);
     return gemm(s, W, Wp, X, Y, N, K, rows, st);
   };
-  // The QKV and gate/up GEMMs reduce into fp32 accumulators zeroed by a memset just before
-  // (cheaper than clearing them behind the read: the epilogues only read them).
+  // The QKV and gate/up GEMMs reduce into fp32 accumulators zeroed by memsets (cheaper than
+  // clearing them behind the read: the epilogues only read them). The memsets sit where no
+  // GEMM follows directly, so each GEMM can start its weight stream while the kernel before
+  // it finishes (programmatic dependent launch): both at the start, then qkv_acc again after
+  // each QKV epilogue and gu_acc after the next layer's (the last SwiGLU read it).
   auto zero_acc = [&](float* acc, size_t n) -> pic_status {
     Rec r(s, st, PIC_PROF_COPY, (double)n * 4, 0, 0);   // a runtime memset, not a library kernel
     PIC_CUDA(cudaMemsetAsync(acc, 0, n * 4, st));
@@ -345,18 +348,25 @@ pic_status run_forward_impl(pic_store* s, const Batch& b, float* hidden_out, flo
   auto pk = [&](const std::vector<const void*>& v, int l) -> const void* { return v.empty() ? nullptr : v[l]; };
   // The O and down projections add straight into the residual stream h.
   {
+    pic_status e;
+    if ((e = zero_acc(s->qkv_acc, (size_t)T * qkv)) != PIC_OK) return e;
+    if ((e = zero_acc(s->gu_acc, (size_t)T * 2 * F)) != PIC_OK) return e;
+    if (!b.compile && b.n_lg > 0) PIC_CUDA(cudaMemsetAsync(logits_out, 0, (size_t)b.n_lg * c.vocab * sizeof(float), st));
+  }
+  {
     Rec r(s, st, PIC_PROF_ROWWISE, dT * dd * (es + 4 + es) + dT * 4, 0, 1);
     launch_embed_norm(dt, T, d, s->m->embed, d_tok, s->m->attn_norm[0], c.rms_eps, s->h, s->x, st);
   }
   for (int l = 0; l < c.n_layers; ++l) {
     pic_status e;
-    if ((e = zero_acc(s->qkv_acc, (size_t)T * qkv)) != PIC_OK) return e;
     if ((e = run_gemm(s->m->wqkv[l], pk(s->m->pqkv, l), s->x, s->qkv_acc, qkv, d, T)) != PIC_OK) return e;
     {
       Rec r(s, st, PIC_PROF_ROWWISE, dT * dQKV * (4 + es), 0, 1);
       launch_qkv_epilogue(dt, T, H, G, D, s->qkv_acc, s->q, d_slot, s->k_layer(l), s->v_layer(l), d_pos, s->rope_cs,
                           att_tc ? (__half*)s->q : nullptr, st);
     }
+    if ((e = zero_acc(s->qkv_acc, (size_t)T * qkv)) != PIC_OK) return e;
+    if (l > 0 && (e = zero_acc(s->gu_acc, (size_t)T * 2 * F)) != PIC_OK) return e;
     // compile keeps only KV: the last layer's attention and MLP feed nothing stored
     if (b.compile && l == c.n_layers - 1) break;
     aa.k_layer = s->k_layer(l);
@@ -375,7 +385,6 @@ pic_status run_forward_impl(pic_store* s, const Batch& b, float* hidden_out, flo
       launch_rmsnorm_rows(dt, T, d, s->h, s->m->mlp_norm[l], c.rms_eps, s->x, false, nullptr, nullptr, nullptr,
                           nullptr, st);
     }
-    if ((e = zero_acc(s->gu_acc, (size_t)T * 2 * F)) != PIC_OK) return e;
     if ((e = run_gemm(s->m->wgu[l], pk(s->m->pgu, l), s->x, s->gu_acc, 2 * F, d, T, PIC_PROF_GEMM_GATE_UP)) != PIC_OK)
       return e;
     {
@@ -390,8 +399,7 @@ pic_status run_forward_impl(pic_store* s, const Batch& b, float* hidden_out, flo
                           d_out, hidden_out, d_lg, s->lm_x, st);
     }
   }
-  if (!b.compile && b.n_lg > 0) {
-    PIC_CUDA(cudaMemsetAsync(logits_out, 0, (size_t)b.n_lg * c.vocab * sizeof(float), st));
+  if (!b.compile && b.n_lg > 0) {   // logits were zeroed at the start
     pic_status e;
     if ((e = run_gemm(s->m->lm_head, s->m->plm, s->lm_x, logits_out, c.vocab, d, b.n_lg)) != PIC_OK) return e;
   }

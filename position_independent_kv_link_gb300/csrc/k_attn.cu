@@ -102,6 +102,7 @@ __global__ void __launch_bounds__(128) attn_simt_kernel(AttnArgs a) {
 // parts with the weights broadcast, the parts' loads independent of each other.
 template <typename O, int D>
 __global__ void __launch_bounds__(256) attn_combine_kernel(AttnArgs a) {
+  asm volatile("griddepcontrol.launch_dependents;");   // the O projection may start its weight loads
   constexpr int NJ = D / 32;
   const AttnCombine c = a.combines[blockIdx.x];
   const int rep = a.H / a.G;

@@ -20,6 +20,12 @@
 //   warp 2     TMEM owner (alloc/dealloc)
 //   warps 3-6  epilogue: tcgen05.ld -> 16-row shared tile -> cp.reduce.async.bulk add
 //
+// For the model's fixed weights it is launched as a programmatic dependent of the previous
+// kernel in the stream: the producer fills the first pipeline stages with weight tiles (which
+// no kernel of the forward writes) while that kernel finishes, then waits for it
+// (griddepcontrol.wait) before the first activation load; the epilogue waits the same way
+// before its first reduce-add. Without that launch attribute the waits return at once.
+//
 // Every mbarrier wait is bounded (~2 s of GPU time). On expiry the kernel raises a
 // device flag, stops issuing work, waits (bounded) for the copies and MMAs it started,
 // frees its TMEM and returns; the host reports PIC_ERR_DEVICE_TIMEOUT.
@@ -251,7 +257,40 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t ph = 0;
     int tile = lo / p.nkb, kb = lo % p.nkb;
     int mt = tile % p.m_tiles, tt = tile / p.m_tiles;
-    for (int g = lo; g < hi; ++g) {
+    // weights of the first stages before the previous kernel has finished, then its outputs
+    const int pre = min(p.S, hi - lo);
+    {
+      int k2 = kb, m2 = mt;
+      for (int i = 0; i < pre; ++i) {
+        const uint32_t fb = smem_u32(full + i), dst = smem_u32(ring + i * stage);
+        mbar_expect_tx(fb, stage);
+        if (PACKED)
+          bulk_load(dst, p.w_packed + ((size_t)m2 * p.nkb + k2) * A_STAGE, A_STAGE, fb, pol_w);
+        else
+          tma_load_2d(dst, &map_w, k2 * BK, m2 * BM, fb, pol_w);
+        if (++k2 == p.nkb) {
+          k2 = 0;
+          if (++m2 == p.m_tiles) m2 = 0;
+        }
+      }
+    }
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    for (int i = 0; i < pre; ++i) {
+      tma_load_2d(smem_u32(ring + i * stage) + A_STAGE, &map_x, kb * BK, tt * p.BN, smem_u32(full + i), pol_x);
+      ++issued;
+      if (++st == p.S) {
+        st = 0;
+        ph ^= 1;
+      }
+      if (++kb == p.nkb) {
+        kb = 0;
+        if (++mt == p.m_tiles) {
+          mt = 0;
+          ++tt;
+        }
+      }
+    }
+    for (int g = lo + pre; g < hi; ++g) {
       if (s_abort || !mbar_wait(smem_u32(empty + st), ph ^ 1)) {
         s_abort = 1;
         break;
@@ -324,6 +363,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nl = q * 32 + lane;              // weight row within the tile
     const bool leader = (warp == 3 && lane == 0);
     float* stg = reinterpret_cast<float*>(epi);
+    asm volatile("griddepcontrol.wait;" ::: "memory");   // Y is written by earlier kernels
     Seg sg{0, lo, 0};
     int s = 0, buf = 0;
     while (next_seg(sg, hi, p.nkb)) {
@@ -453,7 +493,8 @@ bool tc_gemm_supported(int N, int K, int T) { return N >= BM && N % BM == 0 && K
 
 namespace {
 
-pic_status tc_gemm_launch(const void* W, bool packed, const void* X, float* Y, int N, int K, int T, cudaStream_t st) {
+pic_status tc_gemm_launch(const void* W, bool packed, const void* X, float* Y, int N, int K, int T, cudaStream_t st,
+                          bool early_weights) {
   if (!tc_gemm_supported(N, K, T)) return fail(PIC_ERR_UNSUPPORTED, "tcgen05 gemm: unsupported shape");
   if (((uintptr_t)W | (uintptr_t)X | (uintptr_t)Y) % 16)
     return fail(PIC_ERR_INVALID_ARG, "tcgen05 gemm: operands not 16-byte aligned");
@@ -493,7 +534,17 @@ pic_status tc_gemm_launch(const void* W, bool packed, const void* X, float* Y, i
     if (dev >= 0 && dev < 64) attr_smem[packed][dev] = smem;
   }
   const int grid = std::min(device_sms(), p.total);
-  kern<<<grid, kThreads, smem, st>>>(mw, mx, my, p);
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = early_weights ? 1 : 0;
+  cudaLaunchKernelEx(&cfg, kern, mw, mx, my, p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(PIC_ERR_CUDA, std::string("tcgen05 gemm launch: ") + cudaGetErrorString(e));
   return PIC_OK;
@@ -502,11 +553,12 @@ pic_status tc_gemm_launch(const void* W, bool packed, const void* X, float* Y, i
 }  // namespace
 
 pic_status tc_gemm_run(const void* W, const void* X, float* Y, int N, int K, int T, cudaStream_t st) {
-  return tc_gemm_launch(W, false, X, Y, N, K, T, st);
+  return tc_gemm_launch(W, false, X, Y, N, K, T, st, false);
 }
 
-pic_status tc_gemm_run_packed(const void* Wp, const void* X, float* Y, int N, int K, int T, cudaStream_t st) {
-  return tc_gemm_launch(Wp, true, X, Y, N, K, T, st);
+pic_status tc_gemm_run_packed(const void* Wp, const void* X, float* Y, int N, int K, int T, cudaStream_t st,
+                              bool early_weights) {
+  return tc_gemm_launch(Wp, true, X, Y, N, K, T, st, early_weights);
 }
 
 pic_status tc_pack_weight(const void* W, void* out, int N, int K, cudaStream_t st) {

@@ -34,6 +34,7 @@ template <typename T, typename A>
 __global__ void embed_norm_kernel(int d, const T* __restrict__ E, const int* __restrict__ tok,
                                   const float* __restrict__ gain, float eps, float* __restrict__ h,
                                   A* __restrict__ x) {
+  asm volatile("griddepcontrol.launch_dependents;");   // the next GEMM may start its weight loads
   extern __shared__ float row[];
   __shared__ float red[32];
   const int t = blockIdx.x;
@@ -142,6 +143,7 @@ __global__ void __launch_bounds__(512) rmsnorm_rows_kernel(int d, const float* _
                                                            const int* __restrict__ out_row,
                                                            float* __restrict__ hidden_out,
                                                            const int* __restrict__ lg_row, T* __restrict__ lm_x) {
+  asm volatile("griddepcontrol.launch_dependents;");   // the next GEMM may start its weight loads
   __shared__ float red[32];
   const int t = blockIdx.x;
   const float* hr = h + (size_t)t * d;
@@ -171,6 +173,7 @@ __global__ void __launch_bounds__(512) rmsnorm_rows_kernel(int d, const float* _
 // is only read. grid (T, ceil(F / 1024)); 4 outputs per thread.
 template <typename T>
 __global__ void swiglu_kernel(int F, const float* __restrict__ acc, T* __restrict__ act) {
+  asm volatile("griddepcontrol.launch_dependents;");   // the next GEMM may start its weight loads
   const int t = blockIdx.x;
   const int j = (blockIdx.y * blockDim.x + threadIdx.x) * 4;
   if (j >= F) return;
