@@ -335,14 +335,14 @@ pic_status run_forward_impl(pic_store* s, const Batch& b, float* hidden_out, flo
     Rec r(s, st, cls, gemm_bytes(N, K, rows), 2.0 * N * K * rows, 1);
     return gemm(s, W, Wp, X, Y, N, K, rows, st);
   };
-  // The QKV and gate/up GEMMs reduce into fp32 accumulators zeroed by memsets (cheaper than
-  // clearing them behind the read: the epilogues only read them). The memsets sit where no
-  // GEMM follows directly, so each GEMM can start its weight stream while the kernel before
-  // it finishes (programmatic dependent launch): both at the start, then qkv_acc again after
-  // each QKV epilogue and gu_acc after the next layer's (the last SwiGLU read it).
+  // The QKV and gate/up GEMMs reduce into fp32 accumulators zeroed ahead of them (cheaper than
+  // clearing them behind the read: the epilogues only read them): both at the start, then
+  // qkv_acc again after each QKV epilogue and gu_acc after the next layer's (the last SwiGLU
+  // read it), where their traffic does not delay a GEMM. Every kernel of the forward is a
+  // programmatic dependent launch of the one before it.
   auto zero_acc = [&](float* acc, size_t n) -> pic_status {
-    Rec r(s, st, PIC_PROF_COPY, (double)n * 4, 0, 0);   // a runtime memset, not a library kernel
-    PIC_CUDA(cudaMemsetAsync(acc, 0, n * 4, st));
+    Rec r(s, st, PIC_PROF_COPY, (double)n * 4, 0, 1);
+    launch_zero(acc, n, st);
     return PIC_OK;
   };
   auto pk = [&](const std::vector<const void*>& v, int l) -> const void* { return v.empty() ? nullptr : v[l]; };
@@ -351,7 +351,7 @@ pic_status run_forward_impl(pic_store* s, const Batch& b, float* hidden_out, flo
     pic_status e;
     if ((e = zero_acc(s->qkv_acc, (size_t)T * qkv)) != PIC_OK) return e;
     if ((e = zero_acc(s->gu_acc, (size_t)T * 2 * F)) != PIC_OK) return e;
-    if (!b.compile && b.n_lg > 0) PIC_CUDA(cudaMemsetAsync(logits_out, 0, (size_t)b.n_lg * c.vocab * sizeof(float), st));
+    if (!b.compile && b.n_lg > 0 && (e = zero_acc(logits_out, (size_t)b.n_lg * c.vocab)) != PIC_OK) return e;
   }
   {
     Rec r(s, st, PIC_PROF_ROWWISE, dT * dd * (es + 4 + es) + dT * 4, 0, 1);

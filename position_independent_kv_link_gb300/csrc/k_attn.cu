@@ -102,7 +102,7 @@ __global__ void __launch_bounds__(128) attn_simt_kernel(AttnArgs a) {
 // parts with the weights broadcast, the parts' loads independent of each other.
 template <typename O, int D>
 __global__ void __launch_bounds__(256) attn_combine_kernel(AttnArgs a) {
-  asm volatile("griddepcontrol.launch_dependents;");   // the O projection may start its weight loads
+  pdl_enter();
   constexpr int NJ = D / 32;
   const AttnCombine c = a.combines[blockIdx.x];
   const int rep = a.H / a.G;
@@ -161,7 +161,7 @@ void launch_simt(const AttnArgs& a, cudaStream_t st) {
   if (a.n_items > 0) attn_simt_kernel<T, O, D><<<a.n_items, 128, 0, st>>>(a);
   if (a.n_combines > 0) {
     const int rep = a.H / a.G;
-    attn_combine_kernel<O, D><<<dim3(a.n_combines, (a.rb * rep + 7) / 8), 256, 0, st>>>(a);
+    launch_dependent(attn_combine_kernel<O, D>, dim3(a.n_combines, (a.rb * rep + 7) / 8), dim3(256), 0, st, a);
   }
 }
 

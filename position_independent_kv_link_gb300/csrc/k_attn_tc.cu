@@ -255,6 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
   fence_before();
   __syncthreads();
   fence_after();
+  pdl_enter();   // the setup above overlaps the previous kernel; everything below reads its outputs
   const uint32_t tmem = *tmem_slot;   // O: columns [0,128); S buffer b: [128 + 64 b, 192 + 64 b)
 
   if (warp < 4) {
@@ -701,7 +702,7 @@ void launch_attention_tc(const AttnArgs& a, cudaStream_t st) {
     cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (dev >= 0 && dev < 64) attr[dev] = true;
   }
-  if (a.n_items > 0) attn_tc_kernel<<<std::min(a.n_items, sm_count()), kThreads, smem, st>>>(a);
+  if (a.n_items > 0) launch_dependent(attn_tc_kernel, dim3(std::min(a.n_items, sm_count())), dim3(kThreads), smem, st, a);
 }
 
 pic_status attn_check_timeout() {

@@ -275,6 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;");   // the next kernel may launch and wait for us
     for (int i = 0; i < pre; ++i) {
       tma_load_2d(smem_u32(ring + i * stage) + A_STAGE, &map_x, kb * BK, tt * p.BN, smem_u32(full + i), pol_x);
       ++issued;

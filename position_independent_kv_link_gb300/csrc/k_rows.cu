@@ -34,7 +34,7 @@ template <typename T, typename A>
 __global__ void embed_norm_kernel(int d, const T* __restrict__ E, const int* __restrict__ tok,
                                   const float* __restrict__ gain, float eps, float* __restrict__ h,
                                   A* __restrict__ x) {
-  asm volatile("griddepcontrol.launch_dependents;");   // the next GEMM may start its weight loads
+  pdl_enter();
   extern __shared__ float row[];
   __shared__ float red[32];
   const int t = blockIdx.x;
@@ -107,6 +107,7 @@ __global__ void qkv_epilogue_kernel(int H, int G, int D, const float* __restrict
                                     const int* __restrict__ slot, T* __restrict__ kl, T* __restrict__ vl,
                                     const int* __restrict__ pos, const float2* __restrict__ rope_cs,
                                     __half* __restrict__ q16) {
+  pdl_enter();
   const int t = blockIdx.x;
   const int N = (H + 2 * G) * D;
   const int n = (blockIdx.y * blockDim.x + threadIdx.x) * 4;
@@ -143,7 +144,7 @@ __global__ void __launch_bounds__(512) rmsnorm_rows_kernel(int d, const float* _
                                                            const int* __restrict__ out_row,
                                                            float* __restrict__ hidden_out,
                                                            const int* __restrict__ lg_row, T* __restrict__ lm_x) {
-  asm volatile("griddepcontrol.launch_dependents;");   // the next GEMM may start its weight loads
+  pdl_enter();
   __shared__ float red[32];
   const int t = blockIdx.x;
   const float* hr = h + (size_t)t * d;
@@ -173,7 +174,7 @@ __global__ void __launch_bounds__(512) rmsnorm_rows_kernel(int d, const float* _
 // is only read. grid (T, ceil(F / 1024)); 4 outputs per thread.
 template <typename T>
 __global__ void swiglu_kernel(int F, const float* __restrict__ acc, T* __restrict__ act) {
-  asm volatile("griddepcontrol.launch_dependents;");   // the next GEMM may start its weight loads
+  pdl_enter();
   const int t = blockIdx.x;
   const int j = (blockIdx.y * blockDim.x + threadIdx.x) * 4;
   if (j >= F) return;
@@ -185,9 +186,19 @@ __global__ void swiglu_kernel(int F, const float* __restrict__ acc, T* __restric
   store4<T>(act + (size_t)t * F + j, y);
 }
 
+// p[0..n) = 0: 16-byte stores where p is 16-byte aligned, the rest one float at a time
+__global__ void zero_kernel(float* __restrict__ p, size_t n) {
+  pdl_enter();
+  const size_t n4 = ((uintptr_t)p % 16 == 0) ? n / 4 : 0;
+  const size_t i0 = blockIdx.x * (size_t)blockDim.x + threadIdx.x, step = (size_t)gridDim.x * blockDim.x;
+  for (size_t i = i0; i < n4; i += step) reinterpret_cast<float4*>(p)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (size_t i = 4 * n4 + i0; i < n; i += step) p[i] = 0.f;
+}
+
 // grid: (pairs, layers, 2 pools); 16-byte copies of one block of one layer.
 __global__ void copy_blocks_kernel(const int* __restrict__ pairs, int num_blocks_total, size_t block_bytes,
                                    char* __restrict__ kp, char* __restrict__ vp) {
+  pdl_enter();
   const int i = blockIdx.x, l = blockIdx.y;
   char* pool = blockIdx.z == 0 ? kp : vp;
   const size_t layer_off = (size_t)l * num_blocks_total * block_bytes;
@@ -219,10 +230,10 @@ void launch_embed_norm(int dtype, int T, int d, const void* embed, const int* to
   if (T <= 0) return;
   const size_t sm = d * sizeof(float);
   if (dtype == PIC_BF16)
-    embed_norm_kernel<__nv_bfloat16, __half><<<T, kRowThreads, sm, st>>>(d, (const __nv_bfloat16*)embed, tok, gain,
+    launch_dependent(embed_norm_kernel<__nv_bfloat16, __half>, dim3(T), dim3(kRowThreads), sm, st, d, (const __nv_bfloat16*)embed, tok, gain,
                                                                          eps, h, (__half*)x);
   else
-    embed_norm_kernel<float, float><<<T, kRowThreads, sm, st>>>(d, (const float*)embed, tok, gain, eps, h,
+    launch_dependent(embed_norm_kernel<float, float>, dim3(T), dim3(kRowThreads), sm, st, d, (const float*)embed, tok, gain, eps, h,
                                                                 (float*)x);
 }
 
@@ -232,10 +243,10 @@ void launch_qkv_epilogue(int dtype, int T, int H, int G, int D, float* acc, floa
   const int N = (H + 2 * G) * D;
   dim3 grid(T, (N / 4 + kRowThreads - 1) / kRowThreads);
   if (dtype == PIC_BF16)
-    qkv_epilogue_kernel<__nv_bfloat16><<<grid, kRowThreads, 0, st>>>(
+    launch_dependent(qkv_epilogue_kernel<__nv_bfloat16>, grid, dim3(kRowThreads), 0, st,
         H, G, D, acc, q, slot, (__nv_bfloat16*)k_layer, (__nv_bfloat16*)v_layer, pos, rope_cs, q16);
   else
-    qkv_epilogue_kernel<float><<<grid, kRowThreads, 0, st>>>(H, G, D, acc, q, slot, (float*)k_layer,
+    launch_dependent(qkv_epilogue_kernel<float>, grid, dim3(kRowThreads), 0, st, H, G, D, acc, q, slot, (float*)k_layer,
                                                              (float*)v_layer, pos, rope_cs, nullptr);
 }
 
@@ -264,10 +275,10 @@ void launch_rmsnorm_rows(int dtype, int T, int d, const float* h, const float* g
   if (T <= 0) return;
   const int thr = std::min(512, std::max(128, (d / 4 + 31) / 32 * 32));
   if (dtype == PIC_BF16)
-    rmsnorm_rows_kernel<__half><<<T, thr, 0, st>>>(d, h, gain, eps, (__half*)x, final_layer, out_row, hidden_out,
+    launch_dependent(rmsnorm_rows_kernel<__half>, dim3(T), dim3(thr), 0, st, d, h, gain, eps, (__half*)x, (int)final_layer, out_row, hidden_out,
                                                    lg_row, (__half*)lm_x);
   else
-    rmsnorm_rows_kernel<float><<<T, thr, 0, st>>>(d, h, gain, eps, (float*)x, final_layer, out_row, hidden_out,
+    launch_dependent(rmsnorm_rows_kernel<float>, dim3(T), dim3(thr), 0, st, d, h, gain, eps, (float*)x, (int)final_layer, out_row, hidden_out,
                                                   lg_row, (float*)lm_x);
 }
 
@@ -275,16 +286,23 @@ void launch_swiglu(int dtype, int T, int F, float* acc, void* act, cudaStream_t 
   if (T <= 0) return;
   dim3 grid(T, (F / 4 + kRowThreads - 1) / kRowThreads);
   if (dtype == PIC_BF16)
-    swiglu_kernel<__half><<<grid, kRowThreads, 0, st>>>(F, acc, (__half*)act);
+    launch_dependent(swiglu_kernel<__half>, grid, dim3(kRowThreads), 0, st, F, (const float*)acc, (__half*)act);
   else
-    swiglu_kernel<float><<<grid, kRowThreads, 0, st>>>(F, acc, (float*)act);
+    launch_dependent(swiglu_kernel<float>, grid, dim3(kRowThreads), 0, st, F, (const float*)acc, (float*)act);
+}
+
+void launch_zero(float* p, size_t n, cudaStream_t st) {
+  if (n == 0) return;
+  const unsigned blocks = (unsigned)std::min<size_t>(4096, (n / 4 + 255) / 256 + 1);
+  launch_dependent(zero_kernel, dim3(blocks), dim3(256), 0, st, p, n);
 }
 
 void launch_copy_blocks(int n_pairs, const int* pairs, int n_layers, int num_blocks_total, size_t block_bytes,
                         void* k_pool, void* v_pool, cudaStream_t st) {
   if (n_pairs <= 0) return;
   dim3 grid(n_pairs, n_layers, 2);
-  copy_blocks_kernel<<<grid, 256, 0, st>>>(pairs, num_blocks_total, block_bytes, (char*)k_pool, (char*)v_pool);
+  launch_dependent(copy_blocks_kernel, grid, dim3(256), 0, st, pairs, num_blocks_total, block_bytes, (char*)k_pool,
+                   (char*)v_pool);
 }
 
 void launch_import_kv(int dtype, int n_layers, int n, int G, int D, const void* k_src, const void* v_src,

@@ -26,6 +26,31 @@ pic_status fail(pic_status s, const std::string& msg);
       return ::pic::fail(PIC_ERR_CUDA, std::string(#call) + ": " + cudaGetErrorString(e_)); \
   } while (0)
 
+// ------------------------------------------------------------------ programmatic dependent launch
+// The forward's kernels are launched as programmatic dependents of the kernel before them in
+// the stream, so a kernel's launch and prologue overlap the previous kernel's tail. Such a
+// kernel calls pdl_enter() before its first global-memory access: it waits until the
+// previous kernel has completed and its writes are visible, then lets the next kernel launch.
+__device__ __forceinline__ void pdl_enter() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");
+}
+template <typename... P, typename... A>
+inline cudaError_t launch_dependent(void (*k)(P...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                                    A... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k, static_cast<P>(args)...);
+}
+
 // ------------------------------------------------------------------ element helpers
 template <typename T> __device__ __forceinline__ float to_f(T v);
 template <> __device__ __forceinline__ float to_f<float>(float v) { return v; }
@@ -66,6 +91,8 @@ void launch_rmsnorm_rows(int dtype, int T, int d, const float* h, const float* g
 // act[t][j] = silu(gate) * up (activation type) from the accumulator [T][2F] (gate cols, then
 // up cols).
 void launch_swiglu(int dtype, int T, int F, float* acc, void* act, cudaStream_t st);
+// n floats set to zero (a forward kernel: programmatic dependent launch).
+void launch_zero(float* p, size_t n, cudaStream_t st);
 // For each pair i: copy block src[i] -> dst[i] in every layer of both pools.
 void launch_copy_blocks(int n_pairs, const int* pairs, int n_layers, int num_blocks_total, size_t block_bytes,
                         void* k_pool, void* v_pool, cudaStream_t st);
