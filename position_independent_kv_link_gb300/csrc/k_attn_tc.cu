@@ -76,7 +76,12 @@ static_assert(SMEM_BYTES + 1024 <= 227 * 1024, "shared memory budget");
 
 // barrier slots
 constexpr int B_KVFULL = 0, B_SFULL = 2, B_SFREE = 4, B_PFULL = 6, B_PVDONE = 8, B_RAWFULL = 10, B_RAWFREE = 12,
-              B_VFREE = 14, B_QFULL = 17, B_QFREE = 18, B_OFREE = 19, B_MMADONE = 20;
+              B_VFREE = 14, B_QFULL = 17, B_QFREE = 18, B_OFREE = 19, B_MMADONE = 20, B_POSFULL = 21;
+// Every waiter must observe each phase of a barrier before the barrier can complete the next
+// one (a parity wait cannot tell phase n from n + 2). KVFULL therefore has only the MMA as a
+// waiter (the transform cannot re-arm buffer b before S of the tile has run); the softmax
+// takes the key positions from POSFULL, per V slot, which the transform re-arms only after
+// PV of the slot's tile, i.e. after the softmax has consumed it.
 
 __device__ int g_attn_timeout = 0;
 
@@ -240,7 +245,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       mbar_init(bar(B_RAWFULL + i), 1);
       mbar_init(bar(B_RAWFREE + i), kTransformWarps);
     }
-    for (int i = 0; i < NVS; ++i) mbar_init(bar(B_VFREE + i), 1);
+    for (int i = 0; i < NVS; ++i) {
+      mbar_init(bar(B_VFREE + i), 1);
+      mbar_init(bar(B_POSFULL + i), kTransformWarps);
+    }
     mbar_init(bar(B_QFULL), 1);
     mbar_init(bar(B_QFREE), 1);
     mbar_init(bar(B_OFREE), 4);
@@ -272,9 +280,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       for (int j = 0; j < nt; ++j, ++gt) {
         const int b = gt & 1, sl = gt % NVS;
         const uint32_t u = gt >> 1;
-        // kv_full of the same tile also orders this thread after the transform's key positions
+        // S of the tile, and the transform's key positions of it
         ok = __all_sync(0xffffffffu, !s_abort && mbar_wait(bar(B_SFULL + b), u & 1) &&
-                                         mbar_wait(bar(B_KVFULL + b), u & 1));
+                                         mbar_wait(bar(B_POSFULL + sl), (gt / NVS) & 1));
         if (!ok) break;
         fence_after();
         float s[64];
@@ -487,6 +495,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         if (lane == 0) {
           mbar_arrive(bar(B_RAWFREE + rs));
           mbar_arrive(bar(B_KVFULL + b));
+          mbar_arrive(bar(B_POSFULL + s));
         }
       }
     }
