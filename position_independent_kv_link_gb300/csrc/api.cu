@@ -340,17 +340,16 @@ pic_status run_forward_impl(pic_store* s, const Batch& b, float* hidden_out, flo
   // qkv_acc again after each QKV epilogue and gu_acc after the next layer's (the last SwiGLU
   // read it), where their traffic does not delay a GEMM. Every kernel of the forward is a
   // programmatic dependent launch of the one before it.
-  auto zero_acc = [&](float* acc, size_t n) -> pic_status {
-    Rec r(s, st, PIC_PROF_COPY, (double)n * 4, 0, 1);
-    launch_zero(acc, n, st);
+  auto zero_acc = [&](float* acc, size_t n, float* acc2 = nullptr, size_t n2 = 0) -> pic_status {
+    Rec r(s, st, PIC_PROF_COPY, (double)(n + n2) * 4, 0, 1);
+    launch_zero(acc, n, st, acc2, n2);
     return PIC_OK;
   };
   auto pk = [&](const std::vector<const void*>& v, int l) -> const void* { return v.empty() ? nullptr : v[l]; };
   // The O and down projections add straight into the residual stream h.
   {
     pic_status e;
-    if ((e = zero_acc(s->qkv_acc, (size_t)T * qkv)) != PIC_OK) return e;
-    if ((e = zero_acc(s->gu_acc, (size_t)T * 2 * F)) != PIC_OK) return e;
+    if ((e = zero_acc(s->qkv_acc, (size_t)T * qkv, s->gu_acc, (size_t)T * 2 * F)) != PIC_OK) return e;
     if (!b.compile && b.n_lg > 0 && (e = zero_acc(logits_out, (size_t)b.n_lg * c.vocab)) != PIC_OK) return e;
   }
   {
@@ -365,8 +364,9 @@ pic_status run_forward_impl(pic_store* s, const Batch& b, float* hidden_out, flo
       launch_qkv_epilogue(dt, T, H, G, D, s->qkv_acc, s->q, d_slot, s->k_layer(l), s->v_layer(l), d_pos, s->rope_cs,
                           att_tc ? (__half*)s->q : nullptr, st);
     }
-    if ((e = zero_acc(s->qkv_acc, (size_t)T * qkv)) != PIC_OK) return e;
-    if (l > 0 && (e = zero_acc(s->gu_acc, (size_t)T * 2 * F)) != PIC_OK) return e;
+    if ((e = zero_acc(s->qkv_acc, (size_t)T * qkv, l > 0 ? s->gu_acc : nullptr, l > 0 ? (size_t)T * 2 * F : 0)) !=
+        PIC_OK)
+      return e;
     // compile keeps only KV: the last layer's attention and MLP feed nothing stored
     if (b.compile && l == c.n_layers - 1) break;
     aa.k_layer = s->k_layer(l);

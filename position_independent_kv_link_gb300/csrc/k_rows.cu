@@ -187,12 +187,16 @@ __global__ void swiglu_kernel(int F, const float* __restrict__ acc, T* __restric
 }
 
 // p[0..n) = 0: 16-byte stores where p is 16-byte aligned, the rest one float at a time
-__global__ void zero_kernel(float* __restrict__ p, size_t n) {
-  pdl_enter();
+__device__ __forceinline__ void zero_range(float* __restrict__ p, size_t n, size_t i0, size_t step) {
   const size_t n4 = ((uintptr_t)p % 16 == 0) ? n / 4 : 0;
-  const size_t i0 = blockIdx.x * (size_t)blockDim.x + threadIdx.x, step = (size_t)gridDim.x * blockDim.x;
   for (size_t i = i0; i < n4; i += step) reinterpret_cast<float4*>(p)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   for (size_t i = 4 * n4 + i0; i < n; i += step) p[i] = 0.f;
+}
+__global__ void zero_kernel(float* __restrict__ p, size_t n, float* __restrict__ p2, size_t n2) {
+  pdl_enter();
+  const size_t i0 = blockIdx.x * (size_t)blockDim.x + threadIdx.x, step = (size_t)gridDim.x * blockDim.x;
+  zero_range(p, n, i0, step);
+  if (p2) zero_range(p2, n2, i0, step);
 }
 
 // grid: (pairs, layers, 2 pools); 16-byte copies of one block of one layer.
@@ -291,10 +295,10 @@ void launch_swiglu(int dtype, int T, int F, float* acc, void* act, cudaStream_t 
     launch_dependent(swiglu_kernel<float>, grid, dim3(kRowThreads), 0, st, F, (const float*)acc, (float*)act);
 }
 
-void launch_zero(float* p, size_t n, cudaStream_t st) {
-  if (n == 0) return;
-  const unsigned blocks = (unsigned)std::min<size_t>(4096, (n / 4 + 255) / 256 + 1);
-  launch_dependent(zero_kernel, dim3(blocks), dim3(256), 0, st, p, n);
+void launch_zero(float* p, size_t n, cudaStream_t st, float* p2, size_t n2) {
+  if (n == 0 && n2 == 0) return;
+  const unsigned blocks = (unsigned)std::min<size_t>(4096, (std::max(n, n2) / 4 + 255) / 256 + 1);
+  launch_dependent(zero_kernel, dim3(blocks), dim3(256), 0, st, p, n, p2, n2);
 }
 
 void launch_copy_blocks(int n_pairs, const int* pairs, int n_layers, int num_blocks_total, size_t block_bytes,

@@ -91,8 +91,9 @@ void launch_rmsnorm_rows(int dtype, int T, int d, const float* h, const float* g
 // act[t][j] = silu(gate) * up (activation type) from the accumulator [T][2F] (gate cols, then
 // up cols).
 void launch_swiglu(int dtype, int T, int F, float* acc, void* act, cudaStream_t st);
-// n floats set to zero (a forward kernel: programmatic dependent launch).
-void launch_zero(float* p, size_t n, cudaStream_t st);
+// n floats at p (and n2 at p2, when given) set to zero, in one launch (a forward kernel:
+// programmatic dependent launch).
+void launch_zero(float* p, size_t n, cudaStream_t st, float* p2 = nullptr, size_t n2 = 0);
 // For each pair i: copy block src[i] -> dst[i] in every layer of both pools.
 void launch_copy_blocks(int n_pairs, const int* pairs, int n_layers, int num_blocks_total, size_t block_bytes,
                         void* k_pool, void* v_pool, cudaStream_t st);
