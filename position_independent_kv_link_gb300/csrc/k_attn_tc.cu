@@ -208,27 +208,15 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
 __device__ __forceinline__ uint32_t bf2_to_h2(uint32_t w) {
   return pack_f16x2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
 }
-// packed fp32 pairs (sm_100+ f32x2 arithmetic): one instruction per two lanes of work
-__device__ __forceinline__ uint64_t pk2(float a, float b) {
-  uint64_t r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
-  return r;
+__device__ __forceinline__ void bf8_to_f32(const uint4& u, float* f) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    f[2 * e] = __uint_as_float(w[e] << 16);
+    f[2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
+  }
 }
-__device__ __forceinline__ void upk2(uint64_t v, float& a, float& b) { asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v)); }
-__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
-  uint64_t d;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
-__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
-  uint64_t d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-  return d;
-}
-// the two bf16 of a 32-bit word as an fp32 pair (exact widening)
-__device__ __forceinline__ uint64_t bf2_pk(uint32_t w) {
-  return pk2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
-}
+
 __device__ __forceinline__ int item_tiles(const AttnItem& it) { return (it.page1 - it.page0 + 3) >> 2; }
 
 __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_constant__ AttnArgs a) {
@@ -422,17 +410,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     const int tt = tid - 128, tw = warp - 4;
     // K: row offset rr of pages pg0, pg0 + 1; dims 8cq..8cq+7 and 64 + 8cq..
     const int rr = lane & 15, cq = 2 * (tw & 3) + (lane >> 4), pg0 = 2 * (tw >> 2);
-    // (cos, sin)(rr theta_i) of this thread's 8 frequencies, as packed pairs of consecutive
-    // frequencies: cos, sin, -sin, -cos
-    uint64_t lc[4], ls[4], nls[4], nlc[4];
+    float2 lo[8];   // (cos, sin)(rr theta_i) for this thread's 8 frequencies
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const float2 a0 = a.rope_cs[rr * 64 + 8 * cq + 2 * q], a1 = a.rope_cs[rr * 64 + 8 * cq + 2 * q + 1];
-      lc[q] = pk2(a0.x, a1.x);
-      ls[q] = pk2(a0.y, a1.y);
-      nls[q] = pk2(-a0.y, -a1.y);
-      nlc[q] = pk2(-a0.x, -a1.x);
-    }
+    for (int e = 0; e < 8; ++e) lo[e] = a.rope_cs[rr * 64 + 8 * cq + e];
     uint32_t gt = 0;
     bool ok = true;
     for (int ii = blockIdx.x; ii < a.n_items && ok; ii += gridDim.x) {
@@ -455,26 +435,27 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
           const int key = pg * 16 + rr, start = tm[2 * pg], len = tm[2 * pg + 1];
           uint4 y1 = make_uint4(0, 0, 0, 0), y2 = y1;
           if (rr < len) {
+            float v1[8], v2[8];
             const uint8_t* kp = kraw + pg * 4096;   // 128-byte rows 2 rr (dims 0..63) and 2 rr + 1
-            const uint4 w1 = *reinterpret_cast<const uint4*>(kp + sw128(2 * rr, cq));
-            const uint4 w2 = *reinterpret_cast<const uint4*>(kp + sw128(2 * rr + 1, cq));
-            const uint32_t a1[4] = {w1.x, w1.y, w1.z, w1.w}, a2[4] = {w2.x, w2.y, w2.z, w2.w};
+            bf8_to_f32(*reinterpret_cast<const uint4*>(kp + sw128(2 * rr, cq)), v1);
+            bf8_to_f32(*reinterpret_cast<const uint4*>(kp + sw128(2 * rr + 1, cq)), v2);
             const float4* hrow = reinterpret_cast<const float4*>(sm + OFF_CS + (rs * 4 + pg) * 512) + 4 * cq;
             uint32_t o1[4], o2[4];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {   // frequencies 8cq + 2q and 8cq + 2q + 1 side by side
-              const float4 h4 = hrow[q];   // (cos, sin) of the page start for both
-              const uint64_t hc = pk2(h4.x, h4.z), hs = pk2(h4.y, h4.w);
-              // angle composition: cos(a+b), sin(a+b) and -sin(a+b)
-              const uint64_t cs = fma2(hc, lc[q], mul2(hs, nls[q]));
-              const uint64_t sn = fma2(hs, lc[q], mul2(hc, ls[q]));
-              const uint64_t nsn = fma2(hs, nlc[q], mul2(hc, nls[q]));
-              const uint64_t v1 = bf2_pk(a1[q]), v2 = bf2_pk(a2[q]);
-              float y1a, y1b, y2a, y2b;
-              upk2(fma2(v1, cs, mul2(v2, nsn)), y1a, y1b);   // v1 cos - v2 sin
-              upk2(fma2(v2, cs, mul2(v1, sn)), y2a, y2b);    // v2 cos + v1 sin
-              o1[q] = pack_f16x2(y1a, y1b);
-              o2[q] = pack_f16x2(y2a, y2b);
+            for (int q = 0; q < 4; ++q) {
+              const float4 h4 = hrow[q];   // (cos, sin) of the page start for frequencies 8cq + 2q, + 1
+              const float2 hi[2] = {make_float2(h4.x, h4.y), make_float2(h4.z, h4.w)};
+              float y1e[2], y2e[2];
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                const int f = 2 * q + e;
+                const float cs = hi[e].x * lo[f].x - hi[e].y * lo[f].y;
+                const float sn = hi[e].y * lo[f].x + hi[e].x * lo[f].y;
+                y1e[e] = v1[f] * cs - v2[f] * sn;
+                y2e[e] = v2[f] * cs + v1[f] * sn;
+              }
+              o1[q] = pack_f16x2(y1e[0], y1e[1]);
+              o2[q] = pack_f16x2(y2e[0], y2e[1]);
             }
             y1 = make_uint4(o1[0], o1[1], o1[2], o1[3]);
             y2 = make_uint4(o2[0], o2[1], o2[2], o2[3]);
