@@ -266,7 +266,7 @@ def run_ours(args):
     n_pos = max(sum(len(wl.chunks[c]) for c in r.chunk_ids) + len(r.query) for r in wl.requests)
     n_blocks = sum(-(-len(c) // 16) for c in wl.chunks) + 4 * (wl.selected_rows // 16 + 2 * len(wl.requests) * 10)
     store = PicStore(model, num_blocks=n_blocks, max_rows=max(wl.selected_rows, 2048),
-                     max_requests=max(len(wl.requests), 64), max_positions=n_pos + 64,
+                     max_requests=max(len(wl.requests), 64), max_positions=n_pos + 80 + args.steps,
                      max_logit_rows=max(64, len(wl.requests)))
     # compile every chunk once (timed separately; batches of up to 4 chunks)
     torch.cuda.synchronize()
@@ -347,7 +347,31 @@ def run_ours(args):
     h2d = sum(4 * (len(r.query) + len(r.chunk_ids)) for r in wl.requests)
     d2h = hid.numel() * 4 + lg.numel() * 4
 
+    # decode after the link: one generated token per request per step (pic_decode), each
+    # attending to its request's whole linked KV; timed with events over K steps
+    res = store.link(reqs, wl.k, hidden_out=hid, logits_out=lg)
+    n_r = len(res.requests)
+    dh = torch.empty((n_r, spec.d_model), dtype=torch.float32, device="cuda")
+    dl = torch.empty((n_r, spec.vocab), dtype=torch.float32, device="cuda")
+    dtok = pi.gen_tokens((3 + args.steps) * n_r, spec.vocab, 7, "decode").reshape(-1, n_r)
+    for i in range(3):
+        store.decode(res.requests, dtok[i], hidden_out=dh, logits_out=dl)
+    store.sync()
+    barrier()
+    d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    d0.record(stream)
+    for i in range(args.steps):
+        store.decode(res.requests, dtok[3 + i], hidden_out=dh, logits_out=dl)
+    d1.record(stream)
+    torch.cuda.synchronize()
+    store.sync()
+    barrier()
+    dec_ms = slowest_rank(d0.elapsed_time(d1), world)
+    for r in res.requests:
+        store.release_request(r)
+
     rl = roofline_link(wl, pk)
+    dec_roof_ms = rl["bytes"] / (pk["hbm_gbs"] * 1e9) * 1e3   # weights + the requests' KV, read once
     # dominant kernel: the gate/up projection GEMM (largest weight stream of the step);
     # achieved = its algorithmic bytes per launch / its mean event-timed launch duration
     g = prof["gemm_gate_up"]
@@ -378,6 +402,12 @@ def run_ours(args):
         "gpu_launches": launches,
         "clocks": clk,
         "compile": {"tokens_per_s": compiled_tokens / compile_s, "ms": compile_s * 1e3, "chunks": len(wl.chunks)},
+        "decode": {"what": "pic_decode after the link: one generated token per request per step, attending to "
+                           "the request's linked KV (RoPE at load)",
+                   "requests": n_r, "steps": args.steps, "ms_per_step": dec_ms / args.steps,
+                   "tokens_per_s": job_throughput(n_r * args.steps, world, dec_ms / 1e3),
+                   "roofline_ms": dec_roof_ms, "frac": dec_roof_ms / (dec_ms / args.steps),
+                   "bound": "hbm: every weight and the requests' KV read once per step"},
         "setup_s": {"weights_gen": t_gen},
     }
     if cpu_weights is not None:

@@ -174,6 +174,28 @@ pic_status pic_chunk_import(pic_store* s, const int32_t* tokens, int32_t n_token
 pic_status pic_link(pic_store* s, const pic_link_request* reqs, int32_t n_reqs, int32_t k, int32_t all_logits,
                     float* hidden_out, float* logits_out, pic_stream_t stream, pic_request* out_requests);
 
+/* decode: one generated token per linked request, after its link -- the step that turns the
+ * linked prompt into output tokens (time to first token ends at the link's logits; EPIC
+ * summary page, Measured effects table). For each i, host token tokens[i] is appended to
+ * request reqs[i] at the position after the request's last one (its last query row or last
+ * decoded token) and runs through every layer: its pre-RoPE K and V go into the next row of
+ * the request's last page, or, when that page is full, into row 0 of a new block (lowest
+ * free id, requests in call order; the block joins the request's private blocks and page
+ * table); its query attends causally to every row of the request's pages -- the reused and
+ * recomputed chunk rows, the query rows, earlier decoded rows -- and to itself, with RoPE
+ * applied at load from each key's absolute position, as in link.
+ * Requests must be distinct and alive. n_reqs <= max_requests, max_rows and max_logit_rows;
+ * each request's new length <= max_positions (else PIC_ERR_CAPACITY). PIC_ERR_OUT_OF_BLOCKS
+ * when the pool cannot give every request that needs one a new block; then nothing changes.
+ * Outputs (device, caller-owned, fp32): hidden_out [n_reqs][d_model] final-normed hidden of
+ * each new row; logits_out [n_reqs][vocab]. out_positions, out_slots (host int32 [n_reqs],
+ * either may be NULL): the new rows' absolute positions and slots (block_id * 16 + row).
+ * pic_request_get_info reports the grown page table afterwards; its selected/slots lists
+ * stay those of the link. */
+pic_status pic_decode(pic_store* s, const pic_request* reqs, const int32_t* tokens, int32_t n_reqs,
+                      float* hidden_out, float* logits_out, pic_stream_t stream, int32_t* out_positions,
+                      int32_t* out_slots);
+
 pic_status pic_request_get_info(const pic_store* s, pic_request r, pic_request_info* out);
 /* Blocks of a chunk (owned by the store, valid while the chunk lives). */
 pic_status pic_chunk_get_blocks(const pic_store* s, pic_chunk c, int32_t* n_blocks, const int32_t** blocks);

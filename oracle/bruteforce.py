@@ -14,6 +14,8 @@ Method (cited by page title and section):
            layer, every other row reuses its compiled KV; RoPE is applied to each key
            at attention time from its absolute position ("MEPIC: Memory Efficient
            Position Independent Caching for LLM Serving", abstract).
+  decode:  after the link, each further token takes the next position and runs through
+           every layer against the linked caches, which it extends.
 """
 from __future__ import annotations
 
@@ -127,11 +129,13 @@ def brute_compile(m: BruteModel, chunk: Sequence[int], n_dummy: int = 0, dummy: 
 
 
 def brute_link(m: BruteModel, compiled: List[Tuple], chunks: Sequence[Sequence[int]], query: Sequence[int],
-               k: int) -> Dict[str, object]:
+               k: int, decode: Sequence[int] = ()) -> Dict[str, object]:
     """LegoLink-k for one request, one token at a time in position order.
 
     compiled[i] = (K rows per layer, V rows per layer) of chunk i as brute_compile returns.
-    Returns hidden of the query rows, last-row logits and per-layer recomputed K/V rows.
+    Returns hidden of the query rows, last-row logits and per-layer recomputed K/V rows;
+    then the tokens of `decode` are generated one after another from the linked caches
+    (their hidden states, logits and per-layer K/V rows under "decode_*").
     """
     nl = m.spec.n_layers
     seq: List[int] = []
@@ -159,4 +163,16 @@ def brute_link(m: BruteModel, compiled: List[Tuple], chunks: Sequence[Sequence[i
     logits = _mv(m.Wlm, hq[-1])
     rk = [[Kc[l][p] for p in selected] for l in range(nl)]
     rv = [[Vc[l][p] for p in selected] for l in range(nl)]
-    return {"selected": selected, "hidden": hq, "logits": logits, "k": rk, "v": rv}
+    dh, dl, dk, dv = [], [], [], []
+    for tok in decode:
+        p = len(seq)
+        seq.append(int(tok))
+        for l in range(nl):
+            Kc[l].append(None)
+            Vc[l].append(None)
+        dh.append(_step(m, seq[p], p, Kc, Vc))
+        dl.append(_mv(m.Wlm, dh[-1]))
+        dk.append([Kc[l][p] for l in range(nl)])
+        dv.append([Vc[l][p] for l in range(nl)])
+    return {"selected": selected, "hidden": hq, "logits": logits, "k": rk, "v": rv,
+            "decode_hidden": dh, "decode_logits": dl, "decode_k": dk, "decode_v": dv}

@@ -41,6 +41,11 @@ What the pages leave open and this oracle reads plainly (each reading is one lin
     replaced by the recomputed rows.
   * outputs: final-normed hidden states of all query rows, logits of the last query
     row of each request (or of all query rows).
+  * decode after link: one new token per request at the next position, run through
+    every layer while attending to the request's whole linked KV (compiled rows, the
+    recomputed rows that replaced them, the query rows and earlier decoded rows) and
+    to itself; its pre-RoPE K/V go into the request's last page, or into a new block
+    (lowest free id) when that page is full.
 
 Everything is numpy float64. Weights and stored KV arrive as bf16/fp32 values and are
 upcast exactly.
@@ -262,12 +267,38 @@ class LinkMeta:
 
 
 @dataclasses.dataclass
+class DecodeOut:
+    """One decode step over a batch of linked requests."""
+    positions: np.ndarray         # int32 [n]: absolute position of each new token
+    slots: np.ndarray             # int32 [n]: block_id * 16 + row of each new token
+    hidden: np.ndarray            # [n, d] final-normed hidden of the new rows
+    logits: np.ndarray            # [n, vocab]
+    k: List[List[np.ndarray]]     # per request, per layer pre-RoPE K of the new row [G, D]
+    v: List[List[np.ndarray]]
+
+
+@dataclasses.dataclass
+class _LinkedKV:
+    """What a decode step needs of a linked request: every token, and where each
+    position's KV comes from (compiled chunk rows, overridden by the recomputed rows)."""
+    chunk_ids: List[int]
+    tokens: np.ndarray            # positions 0..N-1: chunks, query, decoded tokens
+    selected: np.ndarray          # recomputed positions of the link
+    k_sel: List[np.ndarray]       # per layer [n_sel, G, D]
+    v_sel: List[np.ndarray]
+    k_dec: List[List[np.ndarray]]  # per layer, the decoded rows' [G, D] in order
+    v_dec: List[List[np.ndarray]]
+    meta: LinkMeta                # page table of the request, grown by decode
+
+
+@dataclasses.dataclass
 class LinkOut:
     meta: List[LinkMeta]
     hidden: List[np.ndarray]      # per request final-normed hidden of the query rows [Lq, d]
     logits: List[np.ndarray]      # per request logits [1 or Lq, vocab]
     k: List[List[np.ndarray]]     # per request, per layer recomputed pre-RoPE K [n_sel, G, D]
     v: List[List[np.ndarray]]
+    rids: List[int] = dataclasses.field(default_factory=list)   # request handles, for decode
 
 
 class OracleStore:
@@ -279,6 +310,7 @@ class OracleStore:
         self.free = set(range(num_blocks))
         self.chunks: Dict[int, OracleChunk] = {}
         self.requests: Dict[int, Tuple[List[int], List[int]]] = {}
+        self.linked: Dict[int, _LinkedKV] = {}
         self._next_chunk = 0
         self._next_req = 0
 
@@ -328,6 +360,7 @@ class OracleStore:
 
     def release_request(self, rid: int) -> None:
         blocks, cids = self.requests.pop(rid)
+        self.linked.pop(rid, None)
         self.free.update(blocks)
         for cid in cids:
             self.release_chunk(cid)
@@ -380,12 +413,14 @@ class OracleStore:
              all_logits: bool = False) -> LinkOut:
         """LegoLink-k over a batch of requests (steps a1-a10), returning outputs and metadata."""
         metas = self.plan([(cids, len(q)) for cids, q in requests], k)
+        rids = []
         for (cids, _), meta in zip(requests, metas):
             rid = self._next_req
             self._next_req += 1
             for c in cids:
                 self.chunks[c].refs += 1
             self.requests[rid] = (list(meta.private_blocks), list(cids))
+            rids.append(rid)
         jobs = []
         for (cids, q), meta in zip(requests, metas):
             chs = [self.chunks[c] for c in cids]
@@ -400,8 +435,85 @@ class OracleStore:
             jobs.append(SeqJob(seq, meta.selected.astype(np.int64), base_kv))
         res = run_jobs(self.model, jobs)
         hidden, logits = [], []
-        for (cids, q), r in zip(requests, res):
+        for (cids, q), r, job, meta, rid in zip(requests, res, jobs, metas, rids):
             hq = r.hidden[-len(q):]
             hidden.append(hq)
             logits.append(self.model.logits(hq if all_logits else hq[-1:]))
-        return LinkOut(metas, hidden, logits, [r.k for r in res], [r.v for r in res])
+            nl = self.model.spec.n_layers
+            own = LinkMeta(*(np.array(getattr(meta, f.name)) for f in dataclasses.fields(LinkMeta)))
+            self.linked[rid] = _LinkedKV(list(cids), np.asarray(job.tokens), job.sel, r.k, r.v,
+                                         [[] for _ in range(nl)], [[] for _ in range(nl)], own)
+        return LinkOut(metas, hidden, logits, [r.k for r in res], [r.v for r in res], rids)
+
+    def request_meta(self, rid: int) -> LinkMeta:
+        """Current page table of a linked request (grows with every decoded token)."""
+        return self.linked[rid].meta
+
+    def _request_kv(self, rid: int, l: int) -> Tuple[np.ndarray, np.ndarray]:
+        """Pre-RoPE K, V [N, G, D] of every position of a linked request at layer l: the
+        compiled chunk rows, the link's recomputed rows in their place, then the query rows
+        and the decoded rows."""
+        st = self.linked[rid]
+        G, D = self.model.spec.n_kv_heads, self.model.spec.head_dim
+        N = len(st.tokens)
+        K, V = np.zeros((N, G, D)), np.zeros((N, G, D))
+        off = 0
+        for c in st.chunk_ids:
+            ch = self.chunks[c]
+            L = len(ch.tokens)
+            K[off:off + L] = _f64(ch.k[l])
+            V[off:off + L] = _f64(ch.v[l])
+            off += L
+        K[st.selected] = st.k_sel[l]
+        V[st.selected] = st.v_sel[l]
+        n_dec = len(st.k_dec[l])
+        if n_dec:
+            K[N - n_dec:] = np.stack(st.k_dec[l])
+            V[N - n_dec:] = np.stack(st.v_dec[l])
+        return K, V
+
+    def decode(self, rids: Sequence[int], tokens: Sequence[int]) -> DecodeOut:
+        """One decode step: token tokens[i] is appended to linked request rids[i] at the
+        position after its last one and run through every layer; it attends to all of the
+        request's KV and to itself. A request whose last page is full first takes the
+        lowest free block (all requests' blocks or none). Requests must be distinct."""
+        rids = list(rids)
+        if len(set(rids)) != len(rids) or len(tokens) != len(rids):
+            raise ValueError("decode: one token per distinct request")
+        need = sum(1 for rid in rids if self.linked[rid].meta.page_len[-1] == BLOCK)
+        if need > len(self.free):
+            raise OutOfBlocks("decode")
+        positions, slots, jobs = [], [], []
+        for rid, tok in zip(rids, tokens):
+            st = self.linked[rid]
+            m = st.meta
+            pos = int(m.page_pos[-1]) + int(m.page_len[-1])
+            if m.page_len[-1] == BLOCK:
+                b, = self._take(1)
+                self.requests[rid][0].append(b)
+                m.page_table = np.append(m.page_table, np.int32(b))
+                m.page_pos = np.append(m.page_pos, np.int32(pos))
+                m.page_len = np.append(m.page_len, np.int32(1))
+                m.private_blocks = np.append(m.private_blocks, np.int32(b))
+            else:
+                m.page_len[-1] += 1
+            positions.append(pos)
+            slots.append(int(m.page_table[-1]) * BLOCK + int(m.page_len[-1]) - 1)
+
+            def base_kv(l, rid=rid):
+                K, V = self._request_kv(rid, l)    # positions 0..pos-1; the new row is appended
+                G, D = K.shape[1], K.shape[2]
+                return np.concatenate([K, np.zeros((1, G, D))]), np.concatenate([V, np.zeros((1, G, D))])
+            jobs.append(SeqJob(np.append(st.tokens, np.int64(tok)), np.array([pos]), base_kv))
+        # every job reads its base KV before any new row is stored
+        res = run_jobs(self.model, jobs)
+        for rid, tok, r in zip(rids, tokens, res):
+            st = self.linked[rid]
+            st.tokens = np.append(st.tokens, np.int64(tok))
+            for l in range(self.model.spec.n_layers):
+                st.k_dec[l].append(r.k[l][0])
+                st.v_dec[l].append(r.v[l][0])
+        hidden = np.concatenate([r.hidden for r in res])
+        i32 = lambda a: np.asarray(a, dtype=np.int32)
+        return DecodeOut(i32(positions), i32(slots), hidden, self.model.logits(hidden),
+                         [[k[0] for k in r.k] for r in res], [[v[0] for v in r.v] for r in res])

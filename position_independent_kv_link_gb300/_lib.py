@@ -66,6 +66,7 @@ SIGNATURES = {
     "pic_compile": (I32, [P, C.POINTER(PI32), PI32, I32, I32, P, PI32]),
     "pic_chunk_import": (I32, [P, PI32, I32, P, P, P, PI32]),
     "pic_link": (I32, [P, C.POINTER(LinkRequest), I32, I32, I32, P, P, P, PI32]),
+    "pic_decode": (I32, [P, PI32, PI32, I32, P, P, P, PI32, PI32]),
     "pic_request_get_info": (I32, [P, I32, C.POINTER(RequestInfo)]),
     "pic_chunk_get_blocks": (I32, [P, I32, PI32, C.POINTER(PI32)]),
     "pic_release_chunk": (I32, [P, I32]),

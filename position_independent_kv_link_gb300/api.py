@@ -99,6 +99,14 @@ class LinkResult:
         self.requests = requests      # request handles
 
 
+class DecodeResult:
+    def __init__(self, hidden, logits, positions, slots):
+        self.hidden = hidden          # [n, d] fp32 (device)
+        self.logits = logits          # [n, vocab] fp32 (device)
+        self.positions = positions    # int32 [n]: absolute position of each new token
+        self.slots = slots            # int32 [n]: block_id * 16 + row of each new token
+
+
 class PicStore:
     """Paged chunk-KV store: caller-owned pools (torch) + library-owned workspace."""
 
@@ -163,6 +171,27 @@ class PicStore:
         L.check(self.lib.pic_link(self.handle, reqs, len(requests), k, int(all_logits), hidden_out.data_ptr(),
                                   logits_out.data_ptr(), _stream(stream), _ptr_i32(out)))
         return LinkResult(hidden_out, logits_out, out.tolist())
+
+    def decode(self, requests: Sequence[int], tokens: Sequence[int], stream=None,
+               hidden_out: Optional[torch.Tensor] = None,
+               logits_out: Optional[torch.Tensor] = None) -> DecodeResult:
+        """One generated token per linked request (pic_decode): hidden [n, d_model] and logits
+        [n, vocab] of the new rows, with their positions and slots."""
+        cfg = self.model.cfg
+        ra, ta = _i32(requests), _i32(tokens)
+        n = len(ra)
+        assert len(ta) == n
+        dev = self.k_pool.device
+        if hidden_out is None:
+            hidden_out = torch.empty((n, cfg.d_model), dtype=torch.float32, device=dev)
+        if logits_out is None:
+            logits_out = torch.empty((n, cfg.vocab), dtype=torch.float32, device=dev)
+        assert hidden_out.shape == (n, cfg.d_model) and hidden_out.dtype == torch.float32
+        assert logits_out.shape == (n, cfg.vocab) and logits_out.dtype == torch.float32
+        positions, slots = np.zeros(n, dtype=np.int32), np.zeros(n, dtype=np.int32)
+        L.check(self.lib.pic_decode(self.handle, _ptr_i32(ra), _ptr_i32(ta), n, hidden_out.data_ptr(),
+                                    logits_out.data_ptr(), _stream(stream), _ptr_i32(positions), _ptr_i32(slots)))
+        return DecodeResult(hidden_out, logits_out, positions, slots)
 
     # -- metadata / lifetime
     def request_info(self, r: int) -> Dict[str, np.ndarray]:

@@ -307,7 +307,10 @@ pic_status run_forward_impl(pic_store* s, const Batch& b, float* hidden_out, flo
           return fail(PIC_ERR_CUDA, "cuTensorMapEncodeTiled failed for the KV pools");
         }
     }
-    if (!attn_q_map(&aa.qmap, s->q, T, H)) return fail(PIC_ERR_CUDA, "cuTensorMapEncodeTiled failed for q");
+    // q is read in boxes of 32 rows: a batch of fewer rows (decode) still maps 32 (the q
+    // workspace holds them); rows past a work item's own are fully masked and never stored
+    if (!attn_q_map(&aa.qmap, s->q, std::max(T, 32), H))
+      return fail(PIC_ERR_CUDA, "cuTensorMapEncodeTiled failed for q");
   }
   aa.dtype = dt;
   aa.rb = pin.rows_per_block;
@@ -551,7 +554,8 @@ pic_status pic_store_create(pic_model* m, const pic_store_config* cfg, void* k_p
     return at;
   };
   const size_t as = act_size(c.dtype);
-  const size_t o_h = carve(R * d * 4), o_x = carve(R * std::max(d, HD) * as), o_q = carve(R * HD * 4),
+  const size_t o_h = carve(R * d * 4), o_x = carve(R * std::max(d, HD) * as),
+               o_q = carve(std::max<size_t>(R, 16) * HD * 4),   // fp32 q, or >= 32 rows of fp16 q
                o_attn = carve(R * HD * as), o_act = carve(R * F * as), o_lm = carve((size_t)sc.max_logit_rows * d * as),
                o_qkv = carve(R * (size_t)m->qkv_dim() * 4), o_gu = carve(R * 2 * F * 4),
                o_atto = carve((size_t)s->att_parts_cap * kAttnPartRows * rep * c.head_dim * 4),
@@ -571,8 +575,10 @@ pic_status pic_store_create(pic_model* m, const pic_store_config* cfg, void* k_p
   s->att_ml = (float*)(s->ws + o_attml);
   s->meta_d = (int32_t*)(s->ws + o_meta);
   s->rope_cs = (float2*)(s->ws + o_rope);
-  // the accumulators start at zero (each forward also zeroes them before their GEMM)
+  // the accumulators start at zero (each forward also zeroes them before their GEMM), and so
+  // do the q rows that no forward has written yet
   e = cudaMemset(s->ws + o_qkv, 0, o_gu + R * 2 * F * 4 - o_qkv);
+  if (e == cudaSuccess) e = cudaMemset(s->ws + o_q, 0, o_attn - o_q);
   if (e != cudaSuccess) {
     cudaFree(s->ws);
     return fail(PIC_ERR_CUDA, std::string("workspace memset: ") + cudaGetErrorString(e));
@@ -793,6 +799,75 @@ pic_status pic_link(pic_store* s, const pic_link_request* reqs, int32_t n_reqs, 
     const int id = s->next_request++;
     s->requests[id] = std::move(made[r]);
     out_requests[r] = id;
+  }
+  return PIC_OK;
+}
+
+pic_status pic_decode(pic_store* s, const pic_request* reqs, const int32_t* tokens, int32_t n_reqs,
+                      float* hidden_out, float* logits_out, pic_stream_t stream, int32_t* out_positions,
+                      int32_t* out_slots) {
+  if (!s || !reqs || !tokens || n_reqs < 1 || !hidden_out || !logits_out)
+    return fail(PIC_ERR_INVALID_ARG, "invalid decode arguments");
+  const auto& c = s->m->cfg;
+  if (n_reqs > s->cfg.max_requests) return fail(PIC_ERR_CAPACITY, "requests exceed max_requests");
+  if (n_reqs > s->cfg.max_rows) return fail(PIC_ERR_CAPACITY, "decode rows exceed max_rows");
+  if (n_reqs > s->cfg.max_logit_rows) return fail(PIC_ERR_CAPACITY, "logit rows exceed max_logit_rows");
+  if (!valid_tokens(tokens, n_reqs, c.vocab)) return fail(PIC_ERR_INVALID_ARG, "token id out of range");
+  // validate and count new blocks (nothing is allocated before every check passes)
+  std::set<int32_t> seen;
+  int need = 0;
+  for (int i = 0; i < n_reqs; ++i) {
+    auto it = s->requests.find(reqs[i]);
+    if (it == s->requests.end()) return fail(PIC_ERR_INVALID_ARG, "unknown request handle");
+    if (!seen.insert(reqs[i]).second) return fail(PIC_ERR_INVALID_ARG, "a request appears twice in one decode");
+    const Request& R = it->second;
+    if (R.page_pos.back() + R.page_len.back() >= s->cfg.max_positions)
+      return fail(PIC_ERR_CAPACITY, "decoded sequence exceeds max_positions");
+    if (R.page_len.back() == kBlock) ++need;
+  }
+  if (need > (int)s->free.size()) return fail(PIC_ERR_OUT_OF_BLOCKS, "not enough free blocks for decode");
+
+  // one sequence per request: its whole page table, the last page one row longer (or a new
+  // page), and the new row at the next position
+  Batch b;
+  std::vector<int32_t> fresh(n_reqs, -1), pos(n_reqs), slot(n_reqs);
+  for (int i = 0; i < n_reqs; ++i) {
+    const Request& R = s->requests[reqs[i]];
+    const int np = (int)R.page_table.size(), last_len = R.page_len.back();
+    pos[i] = R.page_pos.back() + last_len;
+    b.begin_seq();
+    for (int j = 0; j < np; ++j)
+      b.page(R.page_table[j], R.page_pos[j], R.page_len[j] + (j == np - 1 && last_len < kBlock ? 1 : 0));
+    if (last_len == kBlock) {
+      fresh[i] = s->take(1)[0];
+      b.page(fresh[i], pos[i], 1);
+      slot[i] = fresh[i] * kBlock;
+    } else {
+      slot[i] = R.page_table.back() * kBlock + last_len;
+    }
+    b.row(tokens[i], pos[i], slot[i]);
+    b.out_row.back() = b.n_hidden++;
+    b.lg_row.back() = b.n_lg++;
+    b.end_seq();
+  }
+  pic_status e = run_forward(s, b, hidden_out, logits_out, (cudaStream_t)stream);
+  if (e != PIC_OK) {
+    for (int32_t f : fresh)
+      if (f >= 0) s->give({f});
+    return e;
+  }
+  for (int i = 0; i < n_reqs; ++i) {
+    Request& R = s->requests[reqs[i]];
+    if (fresh[i] >= 0) {
+      R.page_table.push_back(fresh[i]);
+      R.page_pos.push_back(pos[i]);
+      R.page_len.push_back(1);
+      R.private_blocks.push_back(fresh[i]);
+    } else {
+      R.page_len.back() += 1;
+    }
+    if (out_positions) out_positions[i] = pos[i];
+    if (out_slots) out_slots[i] = slot[i];
   }
   return PIC_OK;
 }

@@ -6,7 +6,8 @@ bounded time. Compiled chunk KV is a seeded stand-in imported into both stores (
 link's arithmetic does not depend on how the chunk KV was produced; compile itself is
 checked at the same width with fewer layers).
 
-  c2 / c5 (10 x 512 + 64 query, k in {0, 2, 16, 32}): every output, 32 layers.
+  c2 / c5 (10 x 512 + 64 query, k in {0, 2, 16, 32}): every output, 32 layers; at k = 16
+      also one decode step after the link (hidden, logits, the new K/V row of every layer).
   c5 k = 512 (full recompute): recomputed K/V of chunks 1-2 at every layer (they depend
       only on those chunks), compared with a plain prefill of chunks 1-2.
   c3 (98 x 512 + 64, k = 16): recomputed K/V of the first 4 chunks' rows at every layer
@@ -108,6 +109,16 @@ def test_c2_c5_full_outputs(m8b, k):
     assert rel_err(res.hidden, out.hidden[0]) <= TOL
     assert rel_err(res.logits, out.logits[0]) <= TOL
     _check_kv(store, res.requests[0], out.k[0], out.v[0], range(spec.n_layers))
+    if k == 16:   # one decode step after the link, at the size the benchmark times it
+        tok = [int(pi.gen_tokens(1, spec.vocab, 63)[0])]
+        d = store.decode(res.requests, tok)
+        store.sync()
+        od = ost.decode(out.rids, tok)
+        assert d.positions.tolist() == od.positions.tolist() and d.slots.tolist() == od.slots.tolist()
+        assert rel_err(d.hidden, od.hidden) <= TOL and rel_err(d.logits, od.logits) <= TOL
+        for l in range(spec.n_layers):
+            kk, vv = store.kv_rows(l, d.slots)
+            assert rel_err(kk, od.k[0][l][None]) <= TOL and rel_err(vv, od.v[0][l][None]) <= TOL
     store.close()
 
 

@@ -3,8 +3,8 @@
 Element-by-element comparisons on seeded inputs: the tcgen05 and SIMT GEMMs, the
 fused-RoPE paged attention, and whole compile + link runs (tiny fp32 config at 1e-4,
 small bf16 GQA models at 2e-2), including ragged chunks, several requests, repeated
-chunks, k = 0 with the LegoLink-0 dummy prefix, k larger than a chunk, and the error
-paths of the store.
+chunks, k = 0 with the LegoLink-0 dummy prefix, k larger than a chunk, decode steps after
+the link (page growth across block boundaries), and the error paths of the store.
 """
 import numpy as np
 import pytest
@@ -12,7 +12,7 @@ import torch
 
 import pic_inputs as pi
 from oracle import pic_oracle as po
-from tests.helpers import compare_link, library_run, oracle_run, rel_err
+from tests.helpers import compare_link, library_run, oracle_run, rel_err, tol_for
 
 pytestmark = pytest.mark.gpu
 
@@ -179,6 +179,87 @@ def test_small_bf16_link(small_bf16, k, n_dummy):
     _, res = library_run(store, wl)
     _, _, out = oracle_run(om, wl, 256)
     compare_link(store, res, out, spec)
+
+
+# ----------------------------------------------------------------------------- decode after link
+
+def _decode_parity(store, om, wl, steps, seed, nb=256):
+    """Links the workload in the library and in the oracle, then runs `steps` decode steps over
+    every request (in reverse request order). Each step: positions, slots and page tables
+    bit-exact; hidden, logits and the new K/V rows of every layer within tolerance."""
+    spec = wl.spec
+    _, res = library_run(store, wl)
+    ost, _, out = oracle_run(om, wl, nb)
+    compare_link(store, res, out, spec, check_kv=False)
+    lib_r, orc_r = res.requests[::-1], out.rids[::-1]
+    worst_all = 0.0
+    for step in range(steps):
+        toks = [int(t) for t in pi.gen_tokens(len(lib_r), spec.vocab, seed, step)]
+        d = store.decode(lib_r, toks)
+        store.sync()
+        o = ost.decode(orc_r, toks)
+        assert np.array_equal(d.positions, o.positions) and np.array_equal(d.slots, o.slots), step
+        for lr, orid in zip(lib_r, orc_r):
+            info, m = store.request_info(lr), ost.request_meta(orid)
+            for key in ("page_table", "page_pos", "page_len", "private_blocks"):
+                assert np.array_equal(info[key], getattr(m, key)), (step, key, info[key], getattr(m, key))
+        errs = {"hidden": rel_err(d.hidden, o.hidden), "logits": rel_err(d.logits, o.logits)}
+        for l in range(spec.n_layers):
+            k, v = store.kv_rows(l, d.slots)
+            errs[f"k{l}"] = rel_err(k, np.stack([kk[l] for kk in o.k]))
+            errs[f"v{l}"] = rel_err(v, np.stack([vv[l] for vv in o.v]))
+        worst = max(errs, key=errs.get)
+        assert errs[worst] <= tol_for(spec), (step, worst, errs[worst])
+        worst_all = max(worst_all, errs[worst])
+    return worst_all
+
+
+def test_tiny_decode_after_link(tiny):
+    """3 requests over ragged chunks with 16, 19 and 16 query rows: steps 1 and 17 open a new
+    block for two requests at once (the call order decides the ids), step 14 for one."""
+    spec, w, model, om = tiny
+    wl = pi.make_workload("ragged decode", spec, 5, [37, 64, 5, 16, 50], 16, 2, n_requests=3)
+    wl.requests[1].chunk_ids = [4, 0, 0, 2]
+    wl.requests[1].query = pi.gen_tokens(19, spec.vocab, 60)
+    wl.requests[2].chunk_ids = [3]
+    _decode_parity(_store(model), om, wl, 18, 61)
+
+
+@pytest.mark.parametrize("k,n_dummy", [(16, 0), (0, 4)])
+def test_small_bf16_decode_after_link(small_bf16, k, n_dummy):
+    """bf16 GQA (4 query heads per KV head, D = 128: the tensor-core attention) with 2 decode
+    rows per step, far fewer than one 32-row work item."""
+    spec, w, model, om = small_bf16
+    wl = pi.make_workload("small decode", spec, 6, [128, 77, 200, 16, 33, 128], 40, k, n_requests=2,
+                          n_dummy=n_dummy)
+    wl.requests[1].chunk_ids = [5, 1, 3, 0]
+    _decode_parity(_store(model), om, wl, 10, 62)
+
+
+def test_decode_errors_leave_state_unchanged(tiny):
+    from position_independent_kv_link_gb300 import PicError
+    from position_independent_kv_link_gb300 import _lib as L
+    spec, w, model, om = tiny
+    store = _store(model, nb=6)
+    a, = store.compile([np.arange(32) % spec.vocab])                 # 2 blocks
+    q = np.arange(16, dtype=np.int32)
+    res = store.link([([a], q), ([a], q)], 2)                        # 2 x (1 private + 1 query): pool full
+    r0, r1 = res.requests
+    info = [store.request_info(r) for r in (r0, r1)]
+    for bad, status in ((([r0, r1], [1, 2]), L.PIC_ERR_OUT_OF_BLOCKS), ((([r0, r0], [1, 2])), L.PIC_ERR_INVALID_ARG),
+                        ((([r0, 999], [1, 2])), L.PIC_ERR_INVALID_ARG), ((([r0], [spec.vocab])), L.PIC_ERR_INVALID_ARG)):
+        with pytest.raises(PicError) as e:
+            store.decode(*bad)
+        assert e.value.status == status
+        assert store.free_blocks() == 0
+        for r, before in zip((r0, r1), info):
+            after = store.request_info(r)
+            assert all(np.array_equal(after[k], before[k]) for k in before)
+    store.release_request(r1)
+    d = store.decode([r0], [5])                                      # takes the lowest freed block
+    store.sync()
+    assert d.slots.tolist() == [int(min(info[1]["private_blocks"])) * 16]
+    assert d.positions.tolist() == [48]
 
 
 # ----------------------------------------------------------------------------- store error paths

@@ -7,6 +7,9 @@
 * Link: the special cases the method reduces to (k = chunk length is full recompute;
   a single chunk with k = 0 is a plain prefill), chunk 1 reproduces its compile,
   compile is offset invariant, and a brute-force per-token loop agrees.
+* Decode after link: with k = chunk length (and for one chunk with k = 0) each decoded
+  token continues a plain prefill; otherwise it agrees with the brute-force twin, which
+  generates from its own link's caches; page growth follows a hand-worked example.
 * Metadata: a hand-worked example and closed forms.
 * Planted mistakes: each pin is shown to fail when the oracle is broken on purpose.
 """
@@ -269,6 +272,125 @@ def test_allocator_all_or_nothing_and_refcounts():
     assert a in st.chunks and not (set(range(4)) & st.free)
     st.release_request(0)
     assert a not in st.chunks and set(range(4)) <= st.free and {7, 8, 9} <= st.free
+
+
+# ----------------------------------------------------------------------------- decode after link
+
+def test_decode_after_full_recompute_is_prefill(tiny, micro):
+    """k >= every chunk length: each decoded token equals the last row of a plain prefill of
+    prompt + query + the tokens decoded so far (hidden state, logits and its K/V)."""
+    for spec, w, model in (tiny, micro):
+        lens = [64, 40, 64] if spec is pi.TINY else [5, 16, 19]
+        chunks = [pi.gen_tokens(L, spec.vocab, 41, i) for i, L in enumerate(lens)]
+        q = pi.gen_tokens(16 if spec is pi.TINY else 6, spec.vocab, 42)   # tiny: the first token opens a block
+        st, _, out = _link(spec, model, chunks, [q], k=max(lens))
+        seq = np.concatenate(chunks + [q])
+        for t in pi.gen_tokens(3, spec.vocab, 43):
+            d = st.decode(out.rids, [int(t)])
+            seq = np.append(seq, t)
+            fr = po.full_prefill(model, seq)
+            assert d.positions.tolist() == [len(seq) - 1]
+            assert rel_err(d.hidden[0], fr.hidden[-1]) < 1e-11
+            assert rel_err(d.logits[0], model.logits(fr.hidden[-1:])[0]) < 1e-11
+            for l in range(spec.n_layers):
+                assert rel_err(d.k[0][l], fr.k[l][-1]) < 1e-11
+                assert rel_err(d.v[0][l], fr.v[l][-1]) < 1e-11
+
+
+def test_decode_single_chunk_k0_is_prefill(tiny):
+    """One chunk, k = 0: the linked KV is the chunk's own prefill, so decoding continues a
+    plain prefill of chunk + query."""
+    spec, w, model = tiny
+    chunk, q = pi.gen_tokens(50, spec.vocab, 44), pi.gen_tokens(9, spec.vocab, 45)
+    st, _, out = _link(spec, model, [chunk], [q], k=0)
+    seq = np.concatenate([chunk, q])
+    for t in pi.gen_tokens(2, spec.vocab, 46):
+        d = st.decode(out.rids, [int(t)])
+        seq = np.append(seq, t)
+        fr = po.full_prefill(model, seq)
+        assert rel_err(d.hidden[0], fr.hidden[-1]) < 1e-11
+        assert rel_err(d.logits[0], model.logits(fr.hidden[-1:])[0]) < 1e-11
+
+
+@pytest.mark.parametrize("k,n_dummy,lens", [(2, 0, [5, 16, 19]), (0, 4, [7, 9]), (17, 0, [18, 3, 20])])
+def test_decode_matches_bruteforce(micro, k, n_dummy, lens):
+    """Between the special cases: decoding after LegoLink-k agrees with the per-token twin,
+    which generates from the caches its own link left behind."""
+    spec, w, model = micro
+    chunks = [pi.gen_tokens(L, spec.vocab, 47, i) for i, L in enumerate(lens)]
+    q = pi.gen_tokens(5, spec.vocab, 48)
+    gen = [int(t) for t in pi.gen_tokens(3, spec.vocab, 49)]
+    st, _, out = _link(spec, model, chunks, [q], k=k, n_dummy=n_dummy)
+    ds = [st.decode(out.rids, [t]) for t in gen]
+    bm = bf.BruteModel(spec, w)
+    comp = [bf.brute_compile(bm, c, n_dummy) for c in chunks]
+    ref = bf.brute_link(bm, comp, chunks, q, k, decode=gen)
+    for i, d in enumerate(ds):
+        assert d.positions.tolist() == [sum(lens) + len(q) + i]
+        assert rel_err(d.hidden[0], np.array(ref["decode_hidden"][i])) < 1e-12
+        assert rel_err(d.logits[0], np.array(ref["decode_logits"][i])) < 1e-12
+        for l in range(spec.n_layers):
+            assert rel_err(d.k[0][l], np.array(ref["decode_k"][i][l])) < 1e-12
+            assert rel_err(d.v[0][l], np.array(ref["decode_v"][i][l])) < 1e-12
+
+
+def test_decode_metadata_hand_example(tiny):
+    spec, w, model = tiny
+    g = json.load(open(os.path.join(GOLD, "tiny_decode_metadata.json")))
+    st = po.OracleStore(model, 64)
+    chunks = [pi.gen_tokens(L, spec.vocab, 50, i) for i, L in enumerate(g["chunk_lengths"])]
+    cids = st.compile_many(chunks)
+    assert [st.chunks[c].blocks for c in cids] == g["compile_blocks"]
+    reqs = [([cids[c] for c in r["chunks"]], pi.gen_tokens(r["query_length"], spec.vocab, 51, i))
+            for i, r in enumerate(g["requests"])]
+    out = st.link(reqs, 2)
+    for m, r in zip(out.meta, g["requests"]):
+        assert m.private_blocks.tolist() == r["link_private_blocks"]
+        assert m.page_table.tolist() == r["link_page_table"]
+        assert m.page_pos.tolist() == r["link_page_pos"]
+        assert m.page_len.tolist() == r["link_page_len"]
+    order = [out.rids[i] for i in g["decode_order"]]
+    for i, step in enumerate(g["decode_steps"]):
+        d = st.decode(order, [i + 1] * len(order))
+        assert d.positions.tolist() == step["positions"] and d.slots.tolist() == step["slots"]
+    for rid, f in zip(out.rids, g["final"]):
+        m = st.request_meta(rid)
+        for key in ("page_table", "page_pos", "page_len", "private_blocks"):
+            assert getattr(m, key).tolist() == f[key], key
+    # the link's own returned metadata is not changed by decoding
+    assert out.meta[0].page_table.tolist() == g["requests"][0]["link_page_table"]
+
+
+def test_decode_requests_are_independent(tiny):
+    """Decoding several requests in one call gives each the result it gets alone."""
+    spec, w, model = tiny
+    chunks = [pi.gen_tokens(L, spec.vocab, 52, i) for i, L in enumerate([64, 23, 40])]
+    queries = [pi.gen_tokens(Lq, spec.vocab, 53, i) for i, Lq in enumerate([16, 7])]
+    st, cids, out = _link(spec, model, chunks, queries, k=3)
+    both = st.decode(out.rids[::-1], [5, 6])
+    for i, (q, tok) in enumerate(zip(queries, [6, 5])):
+        st1, _, o1 = _link(spec, model, chunks, [q], k=3)
+        d1 = st1.decode(o1.rids, [tok])
+        j = 1 - i
+        assert both.positions[j] == d1.positions[0]
+        assert rel_err(both.hidden[j], d1.hidden[0]) < 1e-13
+        assert rel_err(both.logits[j], d1.logits[0]) < 1e-13
+
+
+def test_decode_allocation_all_or_nothing(tiny):
+    spec, w, model = tiny
+    chunk = pi.gen_tokens(32, spec.vocab, 54)
+    st, cids, out = _link(spec, model, [chunk], [pi.gen_tokens(16, spec.vocab, 55)] * 2, k=2, num_blocks=6)
+    assert len(st.free) == 0                          # 2 chunk blocks + 2 x (1 private + 1 query)
+    before = [st.request_meta(r).page_len.tolist() for r in out.rids]
+    with pytest.raises(po.OutOfBlocks):
+        st.decode(out.rids, [1, 2])                   # both last pages are full
+    assert [st.request_meta(r).page_len.tolist() for r in out.rids] == before
+    with pytest.raises(ValueError):
+        st.decode([out.rids[0]] * 2, [1, 2])
+    st.release_request(out.rids[1])
+    d = st.decode(out.rids[:1], [3])                  # the released blocks serve the next page
+    assert d.slots.tolist() == [min(out.meta[1].private_blocks) * 16]
 
 
 # ----------------------------------------------------------------------------- planted mistakes
