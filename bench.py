@@ -266,7 +266,7 @@ def run_ours(args):
     n_pos = max(sum(len(wl.chunks[c]) for c in r.chunk_ids) + len(r.query) for r in wl.requests)
     n_blocks = sum(-(-len(c) // 16) for c in wl.chunks) + 4 * (wl.selected_rows // 16 + 2 * len(wl.requests) * 10)
     store = PicStore(model, num_blocks=n_blocks, max_rows=max(wl.selected_rows, 2048),
-                     max_requests=max(len(wl.requests), 64), max_positions=n_pos + 80 + args.steps,
+                     max_requests=max(len(wl.requests), 64), max_positions=n_pos + 80 + 2 * args.steps,
                      max_logit_rows=max(64, len(wl.requests)))
     # compile every chunk once (timed separately; batches of up to 4 chunks)
     torch.cuda.synchronize()
@@ -347,31 +347,12 @@ def run_ours(args):
     h2d = sum(4 * (len(r.query) + len(r.chunk_ids)) for r in wl.requests)
     d2h = hid.numel() * 4 + lg.numel() * 4
 
-    # decode after the link: one generated token per request per step (pic_decode), each
-    # attending to its request's whole linked KV; timed with events over K steps
-    res = store.link(reqs, wl.k, hidden_out=hid, logits_out=lg)
-    n_r = len(res.requests)
-    dh = torch.empty((n_r, spec.d_model), dtype=torch.float32, device="cuda")
-    dl = torch.empty((n_r, spec.vocab), dtype=torch.float32, device="cuda")
-    dtok = pi.gen_tokens((3 + args.steps) * n_r, spec.vocab, 7, "decode").reshape(-1, n_r)
-    for i in range(3):
-        store.decode(res.requests, dtok[i], hidden_out=dh, logits_out=dl)
-    store.sync()
-    barrier()
-    d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    d0.record(stream)
-    for i in range(args.steps):
-        store.decode(res.requests, dtok[3 + i], hidden_out=dh, logits_out=dl)
-    d1.record(stream)
-    torch.cuda.synchronize()
-    store.sync()
-    barrier()
-    dec_ms = slowest_rank(d0.elapsed_time(d1), world)
-    for r in res.requests:
-        store.release_request(r)
+    dec = time_decode(store, reqs, wl, 3, args.steps, stream, world, barrier)
 
     rl = roofline_link(wl, pk)
     dec_roof_ms = rl["bytes"] / (pk["hbm_gbs"] * 1e9) * 1e3   # weights + the requests' KV, read once
+    dec_ms = dec["ms"]
+    n_r = dec["requests"]
     # dominant kernel: the gate/up projection GEMM (largest weight stream of the step);
     # achieved = its algorithmic bytes per launch / its mean event-timed launch duration
     g = prof["gemm_gate_up"]
@@ -407,7 +388,8 @@ def run_ours(args):
                    "requests": n_r, "steps": args.steps, "ms_per_step": dec_ms / args.steps,
                    "tokens_per_s": job_throughput(n_r * args.steps, world, dec_ms / 1e3),
                    "roofline_ms": dec_roof_ms, "frac": dec_roof_ms / (dec_ms / args.steps),
-                   "bound": "hbm: every weight and the requests' KV read once per step"},
+                   "bound": "hbm: every weight and the requests' KV read once per step",
+                   "gpu_launches_per_step": dec["launches"] / args.steps, "kernels": dec["kernels"]},
         "setup_s": {"weights_gen": t_gen},
     }
     if cpu_weights is not None:
@@ -424,6 +406,68 @@ def run_ours(args):
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+    return 0
+
+
+def time_decode(store, reqs, wl, warmup, steps, stream, world, barrier):
+    """Links the workload's requests once, then times `steps` decode steps (one generated token
+    per request each, pic_decode over the linked KV) with CUDA events after `warmup` steps, and
+    the same number again under the store's per-launch profiling. Releases the requests."""
+    spec = wl.spec
+    res = store.link(reqs, wl.k)
+    n_r = len(res.requests)
+    dh = torch.empty((n_r, spec.d_model), dtype=torch.float32, device="cuda")
+    dl = torch.empty((n_r, spec.vocab), dtype=torch.float32, device="cuda")
+    dtok = pi.gen_tokens((warmup + 2 * steps) * n_r, spec.vocab, 7, "decode").reshape(-1, n_r)
+    for i in range(warmup):
+        store.decode(res.requests, dtok[i], hidden_out=dh, logits_out=dl)
+    store.sync()
+    barrier()
+    n0 = store.launch_count()
+    d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    d0.record(stream)
+    for i in range(steps):
+        store.decode(res.requests, dtok[warmup + i], hidden_out=dh, logits_out=dl)
+    d1.record(stream)
+    torch.cuda.synchronize()
+    store.sync()
+    barrier()
+    ms = slowest_rank(d0.elapsed_time(d1), world)
+    launches = store.launch_count() - n0
+    store.profile_begin()
+    for i in range(steps):
+        store.decode(res.requests, dtok[warmup + steps + i], hidden_out=dh, logits_out=dl)
+    prof = store.profile_end()
+    store.sync()
+    for r in res.requests:
+        store.release_request(r)
+    kernels = {k: {"ms_per_step": v["ms"] / steps, "launches_per_step": v["launches"] / steps,
+                   "GBs": v["bytes"] / (v["ms"] / 1e3) / 1e9 if v["ms"] > 0 else None}
+               for k, v in prof.items() if isinstance(v, dict)}
+    return {"ms": ms, "requests": n_r, "launches": launches, "kernels": kernels}
+
+
+def run_decode(args):
+    """Decode steps only (for launch lists): compile and link the workload once, then W + K
+    decode steps; prints the event-timed step and the library's launches per step."""
+    from position_independent_kv_link_gb300 import PicModel, PicStore
+    torch.cuda.set_device(0)
+    wl = workload(args.config)
+    spec = wl.spec
+    model = PicModel(spec, pi.gen_weights(spec))
+    n_pos = max(sum(len(wl.chunks[c]) for c in r.chunk_ids) + len(r.query) for r in wl.requests)
+    n_blocks = sum(-(-len(c) // 16) for c in wl.chunks) + 4 * (wl.selected_rows // 16 + 2 * len(wl.requests) * 10)
+    store = PicStore(model, num_blocks=n_blocks, max_rows=max(wl.selected_rows, 2048),
+                     max_requests=max(len(wl.requests), 64), max_positions=n_pos + 80 + 2 * args.steps + args.warmup,
+                     max_logit_rows=max(64, len(wl.requests)))
+    cids = []
+    for i in range(0, len(wl.chunks), 4):
+        cids += store.compile(wl.chunks[i:i + 4], n_dummy=wl.n_dummy)
+    reqs = [([cids[c] for c in r.chunk_ids], r.query) for r in wl.requests]
+    d = time_decode(store, reqs, wl, args.warmup, args.steps, torch.cuda.current_stream(), 1, lambda: None)
+    print(json.dumps({"kernel": "decode", "workload": wl.name, "requests": d["requests"],
+                      "ms_per_step": d["ms"] / args.steps, "launches_per_step": d["launches"] / args.steps,
+                      "steps": args.steps, "warmup": args.warmup, "kernels": d["kernels"]}), flush=True)
     return 0
 
 
@@ -506,11 +550,14 @@ def main():
     ap.add_argument("--config", default="c2", help="tiny, c2, c3, c4, c5_k{0,2,16,32,512}")
     ap.add_argument("--cpu-layers", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--kernel", choices=["gemm", "attention"], default=None,
-                    help="time one kernel-level call at its 8B link shape instead of the link step")
+    ap.add_argument("--kernel", choices=["gemm", "attention", "decode"], default=None,
+                    help="time one kernel-level call at its 8B link shape instead of the link step "
+                         "(decode: decode steps after one link of --config)")
     ap.add_argument("--shape", default=None, help="gemm N,K,T for --kernel gemm (default 28672,4096,224)")
     ap.add_argument("--unpacked", action="store_true", help="--kernel gemm on the plain [N][K] layout")
     args = ap.parse_args()
+    if args.kernel == "decode":
+        return run_decode(args)
     if args.kernel:
         return run_kernel(args)
     if args.impl == "reference":
