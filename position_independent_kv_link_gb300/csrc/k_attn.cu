@@ -210,8 +210,7 @@ size_t attention_part_bytes(int n_parts, int rep, int D) {
 }
 
 // Blocks of <= rows_per_block consecutive rows of one sequence; each block reads the prefix of the
-// sequence's pages up to its last row's position, cut into runs of P pages. P grows
-// until the work is ~4 items per SM, never finer than 4 pages.
+// sequence's pages up to its last row's position, cut into runs of P pages (P chosen below).
 void plan_attention(const AttnPlanInput& in, std::vector<AttnItem>& items, std::vector<AttnCombine>& combines,
                     int& n_parts) {
   struct Blk { int row0, nrows, pb, pe; };
@@ -230,50 +229,75 @@ void plan_attention(const AttnPlanInput& in, std::vector<AttnItem>& items, std::
       total += (long long)(pe - in.seq_page_begin[s]);
     }
   }
-  // Pages per split part. One CTA per item: about four items per SM. Persistent kernel: about
-  // two items per CTA, in whole 64-key tiles (4 pages), so fewer partial results are merged.
   const int G = std::max(1, in.G);
-  int P;
-  if (in.persistent) {
-    const long long want = 2LL * std::max(1, in.num_sms);
-    P = (int)std::max<long long>(8, (total * G + want - 1) / want);
-    P = (P + 3) / 4 * 4;
-  } else {
+  auto build = [&](int P, std::vector<AttnItem>& its, std::vector<AttnCombine>& cbs, int& nparts) {
+    its.clear();
+    cbs.clear();
+    nparts = 0;
+    for (const Blk& b : blks) {
+      const int np = b.pe - b.pb;
+      const int ns = std::max(1, (np + P - 1) / P);
+      for (int g = 0; g < in.G; ++g) {
+        if (ns == 1) {
+          its.push_back({b.row0, b.nrows, g, b.pb, b.pe, -1});
+          continue;
+        }
+        cbs.push_back({b.row0, b.nrows, g, nparts, ns});
+        for (int s = 0; s < ns; ++s) {
+          const int p0 = b.pb + s * P, p1 = std::min(b.pe, p0 + P);
+          its.push_back({b.row0, b.nrows, g, p0, p1, nparts + s});
+        }
+        nparts += ns;
+      }
+    }
+    // Heaviest items first so the long ranges start early.
+    std::stable_sort(its.begin(), its.end(),
+                     [](const AttnItem& x, const AttnItem& y) { return (x.page1 - x.page0) > (y.page1 - y.page0); });
+  };
+  if (!in.persistent) {
+    // Pages per split part: one CTA per item, about four items per SM, never finer than 4 pages.
     const long long target = std::max<long long>(1, 4LL * in.num_sms / G);
-    P = (int)std::max<long long>(4, (total + target - 1) / target);
+    build((int)std::max<long long>(4, (total + target - 1) / target), items, combines, n_parts);
+    return;
   }
-  items.clear();
-  combines.clear();
-  n_parts = 0;
-  for (const Blk& b : blks) {
-    const int np = b.pe - b.pb;
-    const int ns = std::max(1, (np + P - 1) / P);
-    for (int g = 0; g < in.G; ++g) {
-      if (ns == 1) {
-        items.push_back({b.row0, b.nrows, g, b.pb, b.pe, -1});
-        continue;
+  // Persistent kernel: CTA c of n = min(items, SMs) takes items c, c + n, c + 2n, ...; the sorted
+  // items are dealt in snake order (round k runs over the CTAs backwards when k is odd). Parts are
+  // whole 64-key tiles (4 pages). The part size is the one, among those giving about 1, 1.5, 2,
+  // 3 or 4 items per SM, whose deal has the smallest estimated makespan -- per CTA the sum of its
+  // items' tiles plus two tiles of fixed cost per item (Q load, O drain) -- then the fewest items.
+  auto deal = [&](std::vector<AttnItem>& its) -> long long {
+    const int n = std::min<int>((int)its.size(), std::max(1, in.num_sms));
+    std::vector<AttnItem> dealt(its.size());
+    std::vector<long long> load(std::max(1, n), 0);
+    for (size_t k = 0; k * n < its.size(); ++k) {
+      const int m = (int)std::min<size_t>(n, its.size() - k * n);
+      for (int c = 0; c < m; ++c) {
+        const AttnItem& it = its[k * n + ((k & 1) ? m - 1 - c : c)];
+        dealt[k * n + c] = it;
+        load[c] += (it.page1 - it.page0 + 3) / 4 + 2;
       }
-      combines.push_back({b.row0, b.nrows, g, n_parts, ns});
-      for (int s = 0; s < ns; ++s) {
-        const int p0 = b.pb + s * P, p1 = std::min(b.pe, p0 + P);
-        items.push_back({b.row0, b.nrows, g, p0, p1, n_parts + s});
-      }
-      n_parts += ns;
     }
-  }
-  // Heaviest items first so the long ranges start early.
-  std::stable_sort(items.begin(), items.end(),
-                   [](const AttnItem& x, const AttnItem& y) { return (x.page1 - x.page0) > (y.page1 - y.page0); });
-  if (in.persistent && !items.empty()) {
-    // CTA c takes items c, c + n, c + 2n, ...: deal the sorted items in snake order
-    // (round k runs over the CTAs backwards when k is odd) so the loads even out.
-    const int n = std::min<int>((int)items.size(), std::max(1, in.num_sms));
-    std::vector<AttnItem> dealt(items.size());
-    for (size_t k = 0; k * n < items.size(); ++k) {
-      const int m = (int)std::min<size_t>(n, items.size() - k * n);
-      for (int c = 0; c < m; ++c) dealt[k * n + c] = items[k * n + ((k & 1) ? m - 1 - c : c)];
+    its.swap(dealt);
+    return *std::max_element(load.begin(), load.end());
+  };
+  long long best = -1;
+  int best_P = 0;
+  for (const int twice_per_sm : {2, 3, 4, 6, 8}) {
+    const long long want = std::max<long long>(1, (long long)twice_per_sm * std::max(1, in.num_sms) / 2);
+    const int P = (int)((std::max<long long>(8, (total * G + want - 1) / want) + 3) / 4 * 4);
+    if (P == best_P) continue;
+    std::vector<AttnItem> its;
+    std::vector<AttnCombine> cbs;
+    int nparts = 0;
+    build(P, its, cbs, nparts);
+    const long long span = deal(its);
+    if (best < 0 || span < best || (span == best && its.size() < items.size())) {
+      best = span;
+      best_P = P;
+      items.swap(its);
+      combines.swap(cbs);
+      n_parts = nparts;
     }
-    items.swap(dealt);
   }
 }
 

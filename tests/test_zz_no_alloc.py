@@ -75,10 +75,12 @@ def test_noalloc_attention_rejects_oversized_work():
     torch.cuda.set_device(0)
     from position_independent_kv_link_gb300 import _lib as L, api
     lib = L.load()
-    # 16 query rows at the end of 5000 pages: the planner splits the pages into ~300 runs
-    # whose merge partials (~65 KB each) exceed the fixed area
-    T, n_pages = 16, 5000
-    qpos = np.arange(16 * n_pages - T, 16 * n_pages, dtype=np.int32)
+    # T rows whose rotated fp16 q (the tensor-core path's operand: T x 32 heads x 128 dims x 2
+    # bytes) alone fills the fixed area; the metadata and merge partials come on top of it,
+    # whatever the work plan
+    T = int(lib.pic_op_attention_noalloc_max_scratch()) // (32 * 128 * 2)
+    n_pages = T // 16
+    qpos = np.arange(T, dtype=np.int32)
     blk = np.arange(n_pages, dtype=np.int32)
     ppos = (16 * np.arange(n_pages)).astype(np.int32)
     plen = np.full(n_pages, 16, dtype=np.int32)
