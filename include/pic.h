@@ -303,6 +303,25 @@ pic_status pic_op_attention_noalloc(int32_t dtype, int32_t T, int32_t n_heads, i
                                     int32_t pool_blocks, const void* rope_cs, int32_t rope_positions, void* out,
                                     pic_stream_t stream);
 
+/* Host only (no GPU work, no device needed): the attention work plan the library launches
+ * for a batch of sequences, e.g. the requests of a link or a decode step, each with its
+ * selected rows and its pages. Rows are grouped in blocks of up to 32 (tensor-core and
+ * mma.sync shapes) or 16 consecutive rows of one sequence; a block reads its sequence's pages
+ * up to the page holding its last row's position, split into runs ("parts") whose partial
+ * results are merged per (block, KV head).
+ * seq_rows, seq_pages: [n_seqs + 1] non-decreasing offsets into row_pos [seq_rows[n_seqs]]
+ * and page_pos [seq_pages[n_seqs]] (positions ascending within each sequence); num_sms >= 1.
+ * Outputs (host): items [max_items][6] = (row0, nrows, kv_head, page0, page1, part), part -1
+ * when the block's pages are not split, in the order the kernels take them (the persistent
+ * kernel's CTA c of n = min(items, num_sms) takes items c, c + n, ...); combines
+ * [max_combines][5] = (row0, nrows, kv_head, part0, nparts); counts [3] = (items, combines,
+ * parts). PIC_ERR_CAPACITY when an output array is too small (counts are still set);
+ * PIC_ERR_INVALID_ARG for inconsistent offsets or unordered positions. */
+pic_status pic_op_attention_plan(int32_t dtype, int32_t n_heads, int32_t n_kv_heads, int32_t head_dim,
+                                 int32_t n_seqs, const int32_t* seq_rows, const int32_t* seq_pages,
+                                 const int32_t* row_pos, const int32_t* page_pos, int32_t num_sms, int32_t* items,
+                                 int32_t max_items, int32_t* combines, int32_t max_combines, int32_t* counts);
+
 /* Fills a device float2 table [n_pos][head_dim/2] with (cos, sin)(p * base^(-2i/D)),
  * angles formed in fp64 on the host. */
 pic_status pic_op_rope_table(int32_t n_pos, int32_t head_dim, double base, void* out, pic_stream_t stream);

@@ -8,11 +8,12 @@ loudly if it has not been built.
 from ._lib import LIB_PATH, PicError, load  # noqa: F401
 
 __all__ = ["LIB_PATH", "PicError", "load", "PicModel", "PicStore", "gemm", "gemm_packed", "pack_weight", "attention",
-           "rope_table"]
+           "attention_plan", "rope_table"]
 
 
 def __getattr__(name):
-    if name in ("PicModel", "PicStore", "gemm", "gemm_packed", "pack_weight", "attention", "rope_table", "LinkResult"):
+    if name in ("PicModel", "PicStore", "gemm", "gemm_packed", "pack_weight", "attention", "attention_plan",
+                "rope_table", "LinkResult", "DecodeResult"):
         from . import api
         return getattr(api, name)
     raise AttributeError(name)

@@ -83,6 +83,7 @@ SIGNATURES = {
                                C.c_size_t, P]),
     "pic_op_rope_table": (I32, [I32, I32, C.c_double, P, P]),
     "pic_op_attention_noalloc_max_scratch": (C.c_size_t, []),
+    "pic_op_attention_plan": (I32, [I32, I32, I32, I32, I32, PI32, PI32, PI32, PI32, I32, PI32, I32, PI32, I32, PI32]),
     "pic_op_attention_noalloc": (I32, [I32, I32, I32, I32, I32, P, PI32, P, P, PI32, PI32, PI32, I32, I32, P, I32, P,
                                        P]),
 }

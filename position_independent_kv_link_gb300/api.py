@@ -317,3 +317,34 @@ def attention(q: torch.Tensor, q_pos: np.ndarray, k_layer: torch.Tensor, v_layer
                                  _ptr_i32(plen), len(blk), k_layer.shape[0], rope.data_ptr(), rope.shape[0],
                                  out.data_ptr(), scratch.data_ptr(), nb, _stream(stream)))
     return out
+
+
+def attention_plan(dtype: torch.dtype, n_heads: int, n_kv_heads: int, head_dim: int,
+                   seqs: Sequence[Tuple[Sequence[int], Sequence[int]]], num_sms: int):
+    """The attention work plan the library launches (pic_op_attention_plan; host only).
+
+    seqs: per sequence (row positions, page start positions), both ascending. Returns
+    (items int32 [n, 6] = row0, nrows, kv_head, page0, page1, part; combines int32 [m, 5] =
+    row0, nrows, kv_head, part0, nparts; number of parts), rows and pages indexed over the
+    concatenation of the sequences.
+    """
+    lib = L.load()
+    rows = [_i32(r) for r, _ in seqs]
+    pages = [_i32(p) for _, p in seqs]
+    seq_rows = _i32(np.concatenate([[0], np.cumsum([len(r) for r in rows])]))
+    seq_pages = _i32(np.concatenate([[0], np.cumsum([len(p) for p in pages])]))
+    rp = _i32(np.concatenate(rows)) if rows else _i32([])
+    pp = _i32(np.concatenate(pages)) if pages else _i32([])
+    counts = np.zeros(3, dtype=np.int32)
+    cap_i, cap_c = 1024, 256
+    while True:
+        items = np.zeros((cap_i, 6), dtype=np.int32)
+        combs = np.zeros((cap_c, 5), dtype=np.int32)
+        st = lib.pic_op_attention_plan(_dtype_code(dtype), n_heads, n_kv_heads, head_dim, len(seqs), _ptr_i32(seq_rows),
+                                       _ptr_i32(seq_pages), _ptr_i32(rp), _ptr_i32(pp), num_sms, _ptr_i32(items),
+                                       cap_i, _ptr_i32(combs), cap_c, _ptr_i32(counts))
+        if st == L.PIC_ERR_CAPACITY and (counts[0] > cap_i or counts[1] > cap_c):
+            cap_i, cap_c = max(cap_i, int(counts[0])), max(cap_c, int(counts[1]))
+            continue
+        L.check(st)
+        return items[:counts[0]].copy(), combs[:counts[1]].copy(), int(counts[2])

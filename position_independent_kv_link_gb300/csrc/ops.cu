@@ -162,6 +162,53 @@ pic_status pic_op_attention(int32_t dtype, int32_t T, int32_t n_heads, int32_t n
   return PIC_OK;
 }
 
+pic_status pic_op_attention_plan(int32_t dtype, int32_t n_heads, int32_t n_kv_heads, int32_t head_dim,
+                                 int32_t n_seqs, const int32_t* seq_rows, const int32_t* seq_pages,
+                                 const int32_t* row_pos, const int32_t* page_pos, int32_t num_sms, int32_t* items,
+                                 int32_t max_items, int32_t* combines, int32_t max_combines, int32_t* counts) {
+  if (n_seqs < 1 || !seq_rows || !seq_pages || !counts || num_sms < 1 || n_kv_heads < 1 || n_heads < 1 ||
+      n_heads % n_kv_heads || (head_dim != 64 && head_dim != 128) || (dtype != PIC_F32 && dtype != PIC_BF16) ||
+      max_items < 0 || max_combines < 0 || (max_items > 0 && !items) || (max_combines > 0 && !combines) ||
+      seq_rows[0] != 0 || seq_pages[0] != 0)
+    return fail(PIC_ERR_INVALID_ARG, "invalid plan arguments");
+  for (int s = 0; s < n_seqs; ++s) {
+    if (seq_rows[s + 1] < seq_rows[s] || seq_pages[s + 1] < seq_pages[s])
+      return fail(PIC_ERR_INVALID_ARG, "sequence offsets must not decrease");
+    for (int r = seq_rows[s] + 1; r < seq_rows[s + 1]; ++r)
+      if (row_pos[r] <= row_pos[r - 1]) return fail(PIC_ERR_INVALID_ARG, "row positions must ascend per sequence");
+    for (int p = seq_pages[s] + 1; p < seq_pages[s + 1]; ++p)
+      if (page_pos[p] <= page_pos[p - 1]) return fail(PIC_ERR_INVALID_ARG, "page positions must ascend per sequence");
+  }
+  if ((seq_rows[n_seqs] > 0 && !row_pos) || (seq_pages[n_seqs] > 0 && !page_pos))
+    return fail(PIC_ERR_INVALID_ARG, "invalid plan arguments");
+  std::vector<int> rp(row_pos, row_pos + seq_rows[n_seqs]), pp(page_pos, page_pos + seq_pages[n_seqs]);
+  AttnPlanInput in;
+  for (int s = 0; s < n_seqs; ++s) {
+    in.seq_row_begin.push_back(seq_rows[s]);
+    in.seq_row_end.push_back(seq_rows[s + 1]);
+    in.seq_page_begin.push_back(seq_pages[s]);
+    in.seq_page_end.push_back(seq_pages[s + 1]);
+  }
+  in.row_pos = &rp;
+  in.page_pos = &pp;
+  in.G = n_kv_heads;
+  in.num_sms = num_sms;
+  in.rows_per_block = attention_rows_per_block(dtype, head_dim, n_heads / n_kv_heads);
+  in.persistent = attention_persistent(dtype, head_dim, n_heads / n_kv_heads);
+  std::vector<AttnItem> its;
+  std::vector<AttnCombine> cbs;
+  int n_parts = 0;
+  plan_attention(in, its, cbs, n_parts);
+  counts[0] = (int32_t)its.size();
+  counts[1] = (int32_t)cbs.size();
+  counts[2] = n_parts;
+  if ((int)its.size() > max_items || (int)cbs.size() > max_combines)
+    return fail(PIC_ERR_CAPACITY, "plan output arrays too small");
+  if (!its.empty()) std::memcpy(items, its.data(), its.size() * sizeof(AttnItem));
+  if (!cbs.empty()) std::memcpy(combines, cbs.data(), cbs.size() * sizeof(AttnCombine));
+  return PIC_OK;
+}
+
 pic_status pic_op_rope_table(int32_t n_pos, int32_t head_dim, double base, void* out, pic_stream_t stream) {
   if (n_pos < 1 || head_dim < 2 || head_dim % 2 || !out || !(base > 1.0))
     return fail(PIC_ERR_INVALID_ARG, "invalid rope table arguments");
