@@ -348,6 +348,7 @@ def run_ours(args):
     d2h = hid.numel() * 4 + lg.numel() * 4
 
     dec = time_decode(store, reqs, wl, 3, args.steps, stream, world, barrier)
+    cpool = time_compile_pool(model, spec, pk, world, barrier) if spec.n_layers == 32 else None
 
     rl = roofline_link(wl, pk)
     dec_roof_ms = rl["bytes"] / (pk["hbm_gbs"] * 1e9) * 1e3   # weights + the requests' KV, read once
@@ -383,6 +384,7 @@ def run_ours(args):
         "gpu_launches": launches,
         "clocks": clk,
         "compile": {"tokens_per_s": compiled_tokens / compile_s, "ms": compile_s * 1e3, "chunks": len(wl.chunks)},
+        "compile_pool": cpool,
         "decode": {"what": "pic_decode after the link: one generated token per request per step, attending to "
                            "the request's linked KV (RoPE at load)",
                    "requests": n_r, "steps": args.steps, "ms_per_step": dec_ms / args.steps,
@@ -445,6 +447,55 @@ def time_decode(store, reqs, wl, warmup, steps, stream, world, barrier):
                    "GBs": v["bytes"] / (v["ms"] / 1e3) / 1e9 if v["ms"] > 0 else None}
                for k, v in prof.items() if isinstance(v, dict)}
     return {"ms": ms, "requests": n_r, "launches": launches, "kernels": kernels}
+
+
+def compile_flops_per_token(spec, L: int) -> float:
+    """FLOPs of pic_compile per token of an L-token chunk: every projection of all layers but
+    the last, whose QKV alone is needed (its K/V are the last stored rows), plus causal
+    attention within the chunk (QK and PV, 4 FLOPs per head dim and visible key)."""
+    H, D, d, F = spec.n_heads, spec.head_dim, spec.d_model, spec.ffn_dim
+    per_layer = spec.qkv_dim * d + H * D * d + 3 * d * F
+    gemm = 2.0 * ((spec.n_layers - 1) * per_layer + spec.qkv_dim * d)
+    attn = (L + 1) / 2 * H * D * 4.0 * (spec.n_layers - 1)
+    return gemm + attn
+
+
+def time_compile_pool(model, spec, pk, world, barrier):
+    """Batched compile throughput over the chunk pool of the batched workload (64 chunks x 512
+    tokens), 4 chunks (2048 rows) per pic_compile call after one warm-up call; every chunk's KV
+    stays resident until the end. CUDA events around the 16 timed calls."""
+    from position_independent_kv_link_gb300 import PicStore
+    pool = pi.config_workloads(spec)["c4"].chunks
+    L = len(pool[0])
+    per_call = 4
+    st = PicStore(model, num_blocks=sum(-(-len(c) // 16) for c in pool) + 8 * per_call, max_rows=per_call * L,
+                  max_requests=per_call, max_positions=L + 16)
+    warm = st.compile(pool[:per_call])
+    st.sync()
+    for c in warm:
+        st.release_chunk(c)
+    barrier()
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    ids = []
+    for i in range(0, len(pool), per_call):
+        ids += st.compile(pool[i:i + per_call])
+    e1.record(stream)
+    torch.cuda.synchronize()
+    st.sync()
+    barrier()
+    ms = slowest_rank(e0.elapsed_time(e1), world)
+    st.close()
+    tokens = sum(len(c) for c in pool)
+    tf = tokens * compile_flops_per_token(spec, L) / (ms / 1e3) / 1e12
+    peak = pk["bf16_tflops_sustained"]
+    return {"what": "pic_compile of the batched workload's chunk pool, 4 chunks (2048 rows) per call",
+            "chunks": len(pool), "tokens": tokens, "ms": ms, "ms_per_call": ms / (len(pool) // per_call),
+            "tokens_per_s": job_throughput(tokens, world, ms / 1e3),
+            "roofline": {"bound": "tensor", "achieved": tf, "peak": peak, "unit": "TFLOP/s", "frac": tf / peak,
+                         "peak_kind": "bf16 dense, sustained (a ~0.4 s run of back-to-back GEMMs)",
+                         "flops_per_token": compile_flops_per_token(spec, L)}}
 
 
 def run_decode(args):
