@@ -498,6 +498,39 @@ def time_compile_pool(model, spec, pk, world, barrier):
                          "flops_per_token": compile_flops_per_token(spec, L)}}
 
 
+def run_compile(args):
+    """Compile calls only (for launch lists): the batched workload's chunk pool, 4 chunks (2048
+    rows) per pic_compile call; W warm-up calls, then K timed calls. Prints the event-timed call
+    and the library's launches per call."""
+    from position_independent_kv_link_gb300 import PicModel, PicStore
+    torch.cuda.set_device(0)
+    spec = workload(args.config).spec
+    model = PicModel(spec, pi.gen_weights(spec))
+    pool = pi.config_workloads(spec)["c4"].chunks
+    per_call, n_calls = 4, max(1, args.warmup) + args.steps
+    batch = lambda i: [pool[(per_call * i + j) % len(pool)] for j in range(per_call)]
+    st = PicStore(model, num_blocks=n_calls * sum(-(-len(c) // 16) for c in batch(0)) + 8,
+                  max_rows=per_call * len(pool[0]), max_requests=per_call, max_positions=len(pool[0]) + 16)
+    for i in range(max(1, args.warmup)):
+        st.compile(batch(i))
+    st.sync()
+    n0 = st.launch_count()
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        st.compile(batch(max(1, args.warmup) + i))
+    e1.record(stream)
+    torch.cuda.synchronize()
+    st.sync()
+    ms = e0.elapsed_time(e1) / args.steps
+    tokens = per_call * len(pool[0])
+    print(json.dumps({"kernel": "compile", "chunks_per_call": per_call, "tokens_per_call": tokens, "ms_per_call": ms,
+                      "tokens_per_s": tokens / (ms / 1e3), "launches_per_call": (st.launch_count() - n0) / args.steps,
+                      "steps": args.steps, "warmup": max(1, args.warmup)}), flush=True)
+    return 0
+
+
 def run_decode(args):
     """Decode steps only (for launch lists): compile and link the workload once, then W + K
     decode steps; prints the event-timed step and the library's launches per step."""
@@ -601,14 +634,17 @@ def main():
     ap.add_argument("--config", default="c2", help="tiny, c2, c3, c4, c5_k{0,2,16,32,512}")
     ap.add_argument("--cpu-layers", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--kernel", choices=["gemm", "attention", "decode"], default=None,
+    ap.add_argument("--kernel", choices=["gemm", "attention", "decode", "compile"], default=None,
                     help="time one kernel-level call at its 8B link shape instead of the link step "
-                         "(decode: decode steps after one link of --config)")
+                         "(decode: decode steps after one link of --config; compile: calls of 4 x 512-token "
+                         "chunks)")
     ap.add_argument("--shape", default=None, help="gemm N,K,T for --kernel gemm (default 28672,4096,224)")
     ap.add_argument("--unpacked", action="store_true", help="--kernel gemm on the plain [N][K] layout")
     args = ap.parse_args()
     if args.kernel == "decode":
         return run_decode(args)
+    if args.kernel == "compile":
+        return run_compile(args)
     if args.kernel:
         return run_kernel(args)
     if args.impl == "reference":
