@@ -432,3 +432,66 @@ def test_pins_catch_planted_mistakes(monkeypatch, micro):
     with monkeypatch.context() as m:
         m.setattr(po, "silu", lambda x: x)
         assert rel_err(po.full_prefill(po.OracleModel(spec, w), toks).hidden, hid_ref) > 1e-6
+
+
+def test_decode_pins_catch_planted_mistakes(monkeypatch, tiny):
+    """Slips in the oracle's decode bookkeeping make the decode pins fail: reading the
+    compiled KV where the link recomputed rows, an off-by-one position, and forgetting the
+    rows decoded earlier."""
+    spec, w, model = tiny
+    lens = [64, 40, 64]
+    chunks = [pi.gen_tokens(L, spec.vocab, 41, i) for i, L in enumerate(lens)]
+    q = pi.gen_tokens(16, spec.vocab, 42)
+    gen = [int(t) for t in pi.gen_tokens(3, spec.vocab, 43)]
+
+    def worst_error():
+        st, _, out = _link(spec, model, chunks, [q], k=max(lens))
+        seq, worst = np.concatenate(chunks + [q]), 0.0
+        for t in gen:
+            d = st.decode(out.rids, [t])
+            seq = np.append(seq, t)
+            worst = max(worst, rel_err(d.hidden[0], po.full_prefill(model, seq).hidden[-1]))
+        return worst
+
+    assert worst_error() < 1e-11
+    good_kv = po.OracleStore._request_kv
+
+    def compiled_rows_only(self, rid, l):
+        K, V = good_kv(self, rid, l)
+        st, off = self.linked[rid], 0
+        for c in st.chunk_ids:             # undo the link's recomputed rows
+            ch = self.chunks[c]
+            K[off:off + len(ch.tokens)] = po._f64(ch.k[l])
+            V[off:off + len(ch.tokens)] = po._f64(ch.v[l])
+            off += len(ch.tokens)
+        return K, V
+
+    def no_decoded_rows(self, rid, l):
+        K, V = good_kv(self, rid, l)
+        n_dec = len(self.linked[rid].k_dec[l])
+        if n_dec:
+            K[-n_dec:] = 0.0
+            V[-n_dec:] = 0.0
+        return K, V
+
+    for bad in (compiled_rows_only, no_decoded_rows):
+        with monkeypatch.context() as m:
+            m.setattr(po.OracleStore, "_request_kv", bad)
+            assert worst_error() > 1e-6, bad.__name__
+    good_jobs = po.run_jobs
+
+    def reuses_last_position(model_, jobs):
+        """The new token takes the request's last used position instead of the next one."""
+        out = []
+        for j in jobs:
+            if len(j.sel) == 1 and j.base_kv is not None:
+                n = int(j.sel[0])
+                toks = np.concatenate([j.tokens[:n - 1], j.tokens[n:n + 1]])
+                out.append(po.SeqJob(toks, np.array([n - 1]), lambda l, f=j.base_kv: tuple(a[:-1] for a in f(l))))
+            else:
+                out.append(j)
+        return good_jobs(model_, out)
+
+    with monkeypatch.context() as m:
+        m.setattr(po, "run_jobs", reuses_last_position)
+        assert worst_error() > 1e-6
