@@ -197,6 +197,41 @@ pic_status pic_decode(pic_store* s, const pic_request* reqs, const int32_t* toke
                       int32_t* out_slots);
 
 pic_status pic_request_get_info(const pic_store* s, pic_request r, pic_request_info* out);
+
+/* compile with content-addressed reuse. PIC compiles each chunk once and links it into any
+ * prompt (EPIC summary page, Approach); MEPIC keeps one shared copy of a chunk's KV in HBM for
+ * every request that uses it (abstract). For each chunk, a resident chunk that an earlier
+ * pic_compile_cached made from the same tokens and n_dummy is returned instead of compiling
+ * again (one more
+ * reference; out_hits[i] = 1), and identical chunks within the call are compiled once; the
+ * others are compiled in one batch, as pic_compile does (out_hits[i] = 0). out_hits (host
+ * [n_chunks]) may be NULL. Chunks made by this call are "cached": when their last reference
+ * (handles and requests) is released they stay resident, their handles no longer valid,
+ * until reused by a later pic_compile_cached or evicted. Every call that needs blocks
+ * (compile, import, link, decode) and finds too few free ones first evicts unreferenced
+ * cached chunks, least recently released first -- only if that frees enough; otherwise it
+ * fails with PIC_ERR_OUT_OF_BLOCKS and evicts nothing. Evictions are not undone if the call
+ * then fails for another reason. Chunks from pic_compile and pic_chunk_import are never
+ * cached: their blocks return to the pool at their last release, as before. */
+pic_status pic_compile_cached(pic_store* s, const int32_t* const* tokens, const int32_t* lens, int32_t n_chunks,
+                              int32_t n_dummy, pic_stream_t stream, pic_chunk* out_chunks, int32_t* out_hits);
+
+/* Counters of the content-addressed reuse and the pool's occupancy (HBM in use by KV pages =
+ * blocks_in_use x block_bytes). */
+typedef struct {
+  int64_t hits;                 /* pic_compile_cached chunks served without compiling */
+  int64_t misses;               /* chunks it compiled */
+  int64_t evictions;            /* unreferenced cached chunks evicted to free blocks */
+  int32_t cached_chunks;        /* resident cached chunks, referenced or not */
+  int32_t unreferenced_chunks;  /* of those, the evictable ones */
+  int32_t unreferenced_blocks;  /* blocks held by the evictable ones */
+  int32_t blocks_in_use;        /* allocated blocks: num_blocks - free */
+  int64_t block_bytes;          /* bytes of one block id in both pools over all layers */
+} pic_cache_stats;
+pic_status pic_store_get_cache_stats(const pic_store* s, pic_cache_stats* out);
+/* Evicts up to max_chunks (all when < 0) unreferenced cached chunks, least recently released
+ * first; n_evicted (may be NULL) receives the count. */
+pic_status pic_store_evict(pic_store* s, int32_t max_chunks, int32_t* n_evicted);
 /* Blocks of a chunk (owned by the store, valid while the chunk lives). */
 pic_status pic_chunk_get_blocks(const pic_store* s, pic_chunk c, int32_t* n_blocks, const int32_t** blocks);
 

@@ -43,6 +43,12 @@ class RequestInfo(C.Structure):
 PROF_CLASSES = 5
 
 
+class CacheStats(C.Structure):
+    _fields_ = [("hits", C.c_int64), ("misses", C.c_int64), ("evictions", C.c_int64),
+                ("cached_chunks", C.c_int32), ("unreferenced_chunks", C.c_int32),
+                ("unreferenced_blocks", C.c_int32), ("blocks_in_use", C.c_int32), ("block_bytes", C.c_int64)]
+
+
 class Profile(C.Structure):
     _fields_ = [("launches", C.c_int64 * PROF_CLASSES), ("ms", C.c_double * PROF_CLASSES),
                 ("bytes", C.c_double * PROF_CLASSES), ("flops", C.c_double * PROF_CLASSES),
@@ -64,6 +70,9 @@ SIGNATURES = {
     "pic_store_destroy": (I32, [P]),
     "pic_store_free_blocks": (I32, [P]),
     "pic_compile": (I32, [P, C.POINTER(PI32), PI32, I32, I32, P, PI32]),
+    "pic_compile_cached": (I32, [P, C.POINTER(PI32), PI32, I32, I32, P, PI32, PI32]),
+    "pic_store_get_cache_stats": (I32, [P, C.POINTER(CacheStats)]),
+    "pic_store_evict": (I32, [P, I32, PI32]),
     "pic_chunk_import": (I32, [P, PI32, I32, P, P, P, PI32]),
     "pic_link": (I32, [P, C.POINTER(LinkRequest), I32, I32, I32, P, P, P, PI32]),
     "pic_decode": (I32, [P, PI32, PI32, I32, P, P, P, PI32, PI32]),

@@ -172,6 +172,29 @@ class PicStore:
                                   logits_out.data_ptr(), _stream(stream), _ptr_i32(out)))
         return LinkResult(hidden_out, logits_out, out.tolist())
 
+    def compile_cached(self, chunks: Sequence[np.ndarray], n_dummy: int = 0, stream=None):
+        """pic_compile_cached: (chunk handles, hit flags) -- a chunk whose content an earlier
+        compile_cached already made resident is reused instead of compiled."""
+        toks = [_i32(c) for c in chunks]
+        ptrs = (L.PI32 * len(toks))(*[_ptr_i32(t) for t in toks])
+        lens = _i32([len(t) for t in toks])
+        out = np.zeros(len(toks), dtype=np.int32)
+        hits = np.zeros(len(toks), dtype=np.int32)
+        L.check(self.lib.pic_compile_cached(self.handle, ptrs, _ptr_i32(lens), len(toks), n_dummy, _stream(stream),
+                                            _ptr_i32(out), _ptr_i32(hits)))
+        return out.tolist(), hits.astype(bool).tolist()
+
+    def cache_stats(self) -> Dict[str, int]:
+        st = L.CacheStats()
+        L.check(self.lib.pic_store_get_cache_stats(self.handle, C.byref(st)))
+        return {name: int(getattr(st, name)) for name, _ in L.CacheStats._fields_}
+
+    def evict(self, max_chunks: int = -1) -> int:
+        """Evicts up to max_chunks (all when < 0) unreferenced cached chunks; returns how many."""
+        n = C.c_int32()
+        L.check(self.lib.pic_store_evict(self.handle, max_chunks, C.byref(n)))
+        return n.value
+
     def decode(self, requests: Sequence[int], tokens: Sequence[int], stream=None,
                hidden_out: Optional[torch.Tensor] = None,
                logits_out: Optional[torch.Tensor] = None) -> DecodeResult:

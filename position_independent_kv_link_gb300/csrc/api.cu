@@ -13,6 +13,7 @@
 #include <algorithm>
 #include <cstdio>
 #include <cstring>
+#include <list>
 #include <map>
 #include <memory>
 #include <set>
@@ -56,7 +57,26 @@ struct Chunk {
   std::vector<int32_t> tokens;
   std::vector<int32_t> blocks;
   int refs = 1;
+  int n_dummy = 0;
+  bool cached = false;   // from pic_compile_cached: indexed by content, kept resident at refs 0
+  uint64_t key = 0;      // content hash (cached chunks)
 };
+
+// FNV-1a over (n_dummy, length, token ids): the bucket of a chunk's content in the store's
+// index (a hit is confirmed by comparing the tokens themselves).
+uint64_t content_key(const int32_t* tokens, int n, int n_dummy) {
+  uint64_t h = 1469598103934665603ull;
+  auto mix = [&](uint32_t v) {
+    for (int b = 0; b < 4; ++b) {
+      h ^= (v >> (8 * b)) & 0xffu;
+      h *= 1099511628211ull;
+    }
+  };
+  mix((uint32_t)n_dummy);
+  mix((uint32_t)n);
+  for (int i = 0; i < n; ++i) mix((uint32_t)tokens[i]);
+  return h;
+}
 
 struct Request {
   std::vector<int32_t> chunk_ids;
@@ -105,6 +125,11 @@ struct pic_store {
   void* v_pool = nullptr;
   std::set<int32_t> free;
   std::map<int32_t, Chunk> chunks;
+  // content-addressed reuse (pic_compile_cached): content hash -> chunk id, and the cached
+  // chunks nothing references, least recently released first (evicted in that order)
+  std::multimap<uint64_t, int32_t> cache_index;
+  std::list<int32_t> lru;
+  int64_t cache_hits = 0, cache_misses = 0, cache_evictions = 0;
   std::map<int32_t, Request> requests;
   int32_t next_chunk = 1, next_request = 1;
 
@@ -170,6 +195,64 @@ struct pic_store {
     return ids;
   }
   void give(const std::vector<int32_t>& ids) { free.insert(ids.begin(), ids.end()); }
+
+  // A chunk handle the caller may use: alive and referenced (a released cached chunk stays
+  // resident for reuse but its old handle is gone).
+  Chunk* live_chunk(int32_t id) {
+    auto it = chunks.find(id);
+    return it == chunks.end() || it->second.refs < 1 ? nullptr : &it->second;
+  }
+  // The chunk's last reference is gone: a cached chunk stays resident (evictable), any other
+  // returns its blocks.
+  void retire(int32_t id) {
+    auto it = chunks.find(id);
+    if (it == chunks.end()) return;
+    if (it->second.cached) {
+      lru.push_back(id);
+      return;
+    }
+    give(it->second.blocks);
+    chunks.erase(it);
+  }
+  void evict_front() {
+    const int32_t id = lru.front();
+    lru.pop_front();
+    auto it = chunks.find(id);
+    auto range = cache_index.equal_range(it->second.key);
+    for (auto i = range.first; i != range.second; ++i)
+      if (i->second == id) {
+        cache_index.erase(i);
+        break;
+      }
+    give(it->second.blocks);
+    chunks.erase(it);
+    ++cache_evictions;
+  }
+  // Makes `need` blocks free, evicting unreferenced cached chunks least recently released
+  // first; evicts nothing and returns false when even evicting all of them is not enough.
+  bool reserve(int need) {
+    size_t avail = free.size();
+    for (int32_t id : lru) avail += chunks[id].blocks.size();
+    if ((size_t)std::max(0, need) > avail) return false;
+    while ((int)free.size() < need) evict_front();
+    return true;
+  }
+  // A cached chunk with the same content and dummy prefix (0 when none).
+  int32_t find_cached(uint64_t key, const int32_t* tokens, int n, int n_dummy) {
+    auto range = cache_index.equal_range(key);
+    for (auto i = range.first; i != range.second; ++i) {
+      const Chunk& c = chunks[i->second];
+      if (c.n_dummy == n_dummy && (int)c.tokens.size() == n && std::equal(c.tokens.begin(), c.tokens.end(), tokens))
+        return i->second;
+    }
+    return 0;
+  }
+  // One more reference to a chunk (taking it off the eviction list if it was there).
+  void ref(int32_t id) {
+    Chunk& c = chunks[id];
+    if (c.refs == 0) lru.remove(id);
+    ++c.refs;
+  }
 };
 
 namespace {
@@ -616,24 +699,34 @@ pic_status pic_store_destroy(pic_store* s) {
 
 int32_t pic_store_free_blocks(const pic_store* s) { return s ? (int32_t)s->free.size() : -1; }
 
-pic_status pic_compile(pic_store* s, const int32_t* const* tokens, const int32_t* lens, int32_t n_chunks,
-                       int32_t n_dummy, pic_stream_t stream, pic_chunk* out_chunks) {
-  if (!s || !tokens || !lens || n_chunks < 1 || !out_chunks || n_dummy < 0 || n_dummy > kBlock)
+namespace {
+
+pic_status check_compile_args(const pic_store* s, const int32_t* const* tokens, const int32_t* lens,
+                              int32_t n_chunks, int32_t n_dummy, const void* out) {
+  if (!s || !tokens || !lens || n_chunks < 1 || !out || n_dummy < 0 || n_dummy > kBlock)
     return fail(PIC_ERR_INVALID_ARG, "invalid compile arguments");
-  const auto& c = s->m->cfg;
-  int need = 0;
-  long long rows = n_dummy;
   for (int i = 0; i < n_chunks; ++i) {
     if (!tokens[i] || lens[i] < 1) return fail(PIC_ERR_INVALID_ARG, "empty chunk");
-    if (!valid_tokens(tokens[i], lens[i], c.vocab)) return fail(PIC_ERR_INVALID_ARG, "token id out of range");
+    if (!valid_tokens(tokens[i], lens[i], s->m->cfg.vocab)) return fail(PIC_ERR_INVALID_ARG, "token id out of range");
     if (lens[i] + n_dummy > s->cfg.max_positions) return fail(PIC_ERR_CAPACITY, "chunk longer than max_positions");
-    need += ceil_div(lens[i], kBlock);
-    rows += lens[i];
   }
-  if (n_chunks > s->cfg.max_requests) return fail(PIC_ERR_CAPACITY, "chunks exceed max_requests");
-  if (rows > s->cfg.max_rows) return fail(PIC_ERR_CAPACITY, "compile rows exceed max_rows");
-  if (need > (int)s->free.size()) return fail(PIC_ERR_OUT_OF_BLOCKS, "not enough free blocks for compile");
+  return PIC_OK;
+}
 
+// Compiles chunks `idx` of the call in one forward into newly taken blocks (the caller has
+// made the blocks free); on success out_ids[j] is the new chunk of idx[j] (refcount 1).
+pic_status compile_batch(pic_store* s, const int32_t* const* tokens, const int32_t* lens, const std::vector<int>& idx,
+                         int32_t n_dummy, cudaStream_t st, std::vector<int32_t>& out_ids) {
+  long long rows = n_dummy;
+  int need = 0;
+  for (int i : idx) {
+    rows += lens[i];
+    need += ceil_div(lens[i], kBlock);
+  }
+  if ((int)idx.size() > s->cfg.max_requests) return fail(PIC_ERR_CAPACITY, "chunks exceed max_requests");
+  if (rows > s->cfg.max_rows) return fail(PIC_ERR_CAPACITY, "compile rows exceed max_rows");
+  if (!s->reserve(need)) return fail(PIC_ERR_OUT_OF_BLOCKS, "not enough free blocks for compile");
+  const int n_chunks = (int)idx.size();
   Batch b;
   b.compile = true;
   // the dummy prefix is computed once per batch into the store's scratch page
@@ -644,29 +737,100 @@ pic_status pic_compile(pic_store* s, const int32_t* const* tokens, const int32_t
     b.end_seq();
   }
   std::vector<std::vector<int32_t>> blocks(n_chunks);
-  for (int i = 0; i < n_chunks; ++i) {
-    blocks[i] = s->take(ceil_div(lens[i], kBlock));
+  for (int j0 = 0; j0 < n_chunks; ++j0) {
+    const int i = idx[j0];
+    blocks[j0] = s->take(ceil_div(lens[i], kBlock));
     b.begin_seq();
     if (n_dummy > 0) b.page(s->scratch_block(), 0, n_dummy);
-    for (int j = 0; j < (int)blocks[i].size(); ++j)
-      b.page(blocks[i][j], n_dummy + kBlock * j, std::min(kBlock, lens[i] - kBlock * j));
+    for (int j = 0; j < (int)blocks[j0].size(); ++j)
+      b.page(blocks[j0][j], n_dummy + kBlock * j, std::min(kBlock, lens[i] - kBlock * j));
     for (int t = 0; t < lens[i]; ++t)
-      b.row(tokens[i][t], n_dummy + t, blocks[i][t / kBlock] * kBlock + t % kBlock);
+      b.row(tokens[i][t], n_dummy + t, blocks[j0][t / kBlock] * kBlock + t % kBlock);
     b.end_seq();
   }
-  pic_status e = run_forward(s, b, nullptr, nullptr, (cudaStream_t)stream);
+  pic_status e = run_forward(s, b, nullptr, nullptr, st);
   if (e != PIC_OK) {
     for (auto& bl : blocks) s->give(bl);
     return e;
   }
-  for (int i = 0; i < n_chunks; ++i) {
+  out_ids.assign(n_chunks, 0);
+  for (int j0 = 0; j0 < n_chunks; ++j0) {
+    const int i = idx[j0];
     Chunk ch;
     ch.tokens.assign(tokens[i], tokens[i] + lens[i]);
-    ch.blocks = blocks[i];
+    ch.blocks = blocks[j0];
+    ch.n_dummy = n_dummy;
     const int id = s->next_chunk++;
     s->chunks[id] = std::move(ch);
-    out_chunks[i] = id;
+    out_ids[j0] = id;
   }
+  return PIC_OK;
+}
+
+}  // namespace
+
+pic_status pic_compile(pic_store* s, const int32_t* const* tokens, const int32_t* lens, int32_t n_chunks,
+                       int32_t n_dummy, pic_stream_t stream, pic_chunk* out_chunks) {
+  pic_status e = check_compile_args(s, tokens, lens, n_chunks, n_dummy, out_chunks);
+  if (e != PIC_OK) return e;
+  std::vector<int> idx(n_chunks);
+  for (int i = 0; i < n_chunks; ++i) idx[i] = i;
+  std::vector<int32_t> ids;
+  if ((e = compile_batch(s, tokens, lens, idx, n_dummy, (cudaStream_t)stream, ids)) != PIC_OK) return e;
+  std::copy(ids.begin(), ids.end(), out_chunks);
+  return PIC_OK;
+}
+
+pic_status pic_compile_cached(pic_store* s, const int32_t* const* tokens, const int32_t* lens, int32_t n_chunks,
+                              int32_t n_dummy, pic_stream_t stream, pic_chunk* out_chunks, int32_t* out_hits) {
+  pic_status e = check_compile_args(s, tokens, lens, n_chunks, n_dummy, out_chunks);
+  if (e != PIC_OK) return e;
+  // each chunk: a resident cached chunk of the same content, an earlier chunk of this call, or
+  // a miss to compile
+  std::vector<int32_t> hit(n_chunks, 0);
+  std::vector<int> same_as(n_chunks, -1), miss;
+  std::vector<uint64_t> key(n_chunks);
+  for (int i = 0; i < n_chunks; ++i) {
+    key[i] = content_key(tokens[i], lens[i], n_dummy);
+    if ((hit[i] = s->find_cached(key[i], tokens[i], lens[i], n_dummy)) != 0) continue;
+    for (int j : miss)
+      if (key[j] == key[i] && lens[j] == lens[i] && std::equal(tokens[i], tokens[i] + lens[i], tokens[j])) {
+        same_as[i] = j;
+        break;
+      }
+    if (same_as[i] < 0) miss.push_back(i);
+  }
+  // hold the hits first so that making room for the misses cannot evict them
+  for (int i = 0; i < n_chunks; ++i)
+    if (hit[i]) s->ref(hit[i]);
+  std::vector<int32_t> ids;
+  if (!miss.empty() && (e = compile_batch(s, tokens, lens, miss, n_dummy, (cudaStream_t)stream, ids)) != PIC_OK) {
+    for (int i = 0; i < n_chunks; ++i)
+      if (hit[i] && --s->chunks[hit[i]].refs == 0) s->retire(hit[i]);
+    return e;
+  }
+  std::vector<int32_t> new_id(n_chunks, 0);
+  for (size_t j = 0; j < miss.size(); ++j) {
+    Chunk& c = s->chunks[ids[j]];
+    c.cached = true;
+    c.key = key[miss[j]];
+    s->cache_index.emplace(c.key, ids[j]);
+    new_id[miss[j]] = ids[j];
+  }
+  for (int i = 0; i < n_chunks; ++i) {
+    if (hit[i]) {
+      out_chunks[i] = hit[i];
+    } else if (same_as[i] >= 0) {
+      out_chunks[i] = new_id[same_as[i]];
+      s->chunks[out_chunks[i]].refs++;
+    } else {
+      out_chunks[i] = new_id[i];
+    }
+    const bool reused = hit[i] || same_as[i] >= 0;
+    if (out_hits) out_hits[i] = reused ? 1 : 0;
+    if (reused) ++s->cache_hits;
+  }
+  s->cache_misses += (int64_t)miss.size();
   return PIC_OK;
 }
 
@@ -676,8 +840,8 @@ pic_status pic_chunk_import(pic_store* s, const int32_t* tokens, int32_t n_token
   const auto& c = s->m->cfg;
   if (!valid_tokens(tokens, n_tokens, c.vocab)) return fail(PIC_ERR_INVALID_ARG, "token id out of range");
   const int nb = ceil_div(n_tokens, kBlock);
-  if (nb > (int)s->free.size()) return fail(PIC_ERR_OUT_OF_BLOCKS, "not enough free blocks for import");
   if ((size_t)nb > s->meta_cap) return fail(PIC_ERR_CAPACITY, "chunk too long for the metadata buffer");
+  if (!s->reserve(nb)) return fail(PIC_ERR_OUT_OF_BLOCKS, "not enough free blocks for import");
   cudaStream_t st = (cudaStream_t)stream;
   if (s->meta_ev_pending) {
     PIC_CUDA(cudaEventSynchronize(s->meta_ev));
@@ -723,9 +887,9 @@ pic_status pic_link(pic_store* s, const pic_link_request* reqs, int32_t n_reqs, 
     if (!valid_tokens(q.query, q.query_len, c.vocab)) return fail(PIC_ERR_INVALID_ARG, "query token out of range");
     long long len = q.query_len;
     for (int i = 0; i < q.n_chunks; ++i) {
-      auto it = s->chunks.find(q.chunks[i]);
-      if (it == s->chunks.end()) return fail(PIC_ERR_INVALID_ARG, "unknown chunk handle");
-      const int L = (int)it->second.tokens.size();
+      const Chunk* ch = s->live_chunk(q.chunks[i]);
+      if (!ch) return fail(PIC_ERR_INVALID_ARG, "unknown chunk handle");
+      const int L = (int)ch->tokens.size();
       need += ceil_div(std::min(k, L), kBlock);
       rows += std::min(k, L);
       len += L;
@@ -737,7 +901,7 @@ pic_status pic_link(pic_store* s, const pic_link_request* reqs, int32_t n_reqs, 
   }
   if (rows > s->cfg.max_rows) return fail(PIC_ERR_CAPACITY, "selected rows exceed max_rows");
   if (lg_rows > s->cfg.max_logit_rows) return fail(PIC_ERR_CAPACITY, "logit rows exceed max_logit_rows");
-  if (need > (int)s->free.size()) return fail(PIC_ERR_OUT_OF_BLOCKS, "not enough free blocks for link");
+  if (!s->reserve(need)) return fail(PIC_ERR_OUT_OF_BLOCKS, "not enough free blocks for link");
 
   Batch b;
   std::vector<Request> made(n_reqs);
@@ -825,7 +989,7 @@ pic_status pic_decode(pic_store* s, const pic_request* reqs, const int32_t* toke
       return fail(PIC_ERR_CAPACITY, "decoded sequence exceeds max_positions");
     if (R.page_len.back() == kBlock) ++need;
   }
-  if (need > (int)s->free.size()) return fail(PIC_ERR_OUT_OF_BLOCKS, "not enough free blocks for decode");
+  if (!s->reserve(need)) return fail(PIC_ERR_OUT_OF_BLOCKS, "not enough free blocks for decode");
 
   // one sequence per request: its whole page table, the last page one row longer (or a new
   // page), and the new row at the next position
@@ -892,7 +1056,7 @@ pic_status pic_request_get_info(const pic_store* s, pic_request r, pic_request_i
 pic_status pic_chunk_get_blocks(const pic_store* s, pic_chunk c, int32_t* n_blocks, const int32_t** blocks) {
   if (!s || !n_blocks || !blocks) return fail(PIC_ERR_INVALID_ARG, "null argument");
   auto it = s->chunks.find(c);
-  if (it == s->chunks.end()) return fail(PIC_ERR_INVALID_ARG, "unknown chunk handle");
+  if (it == s->chunks.end() || it->second.refs < 1) return fail(PIC_ERR_INVALID_ARG, "unknown chunk handle");
   *n_blocks = (int32_t)it->second.blocks.size();
   *blocks = it->second.blocks.data();
   return PIC_OK;
@@ -900,12 +1064,9 @@ pic_status pic_chunk_get_blocks(const pic_store* s, pic_chunk c, int32_t* n_bloc
 
 pic_status pic_release_chunk(pic_store* s, pic_chunk c) {
   if (!s) return fail(PIC_ERR_INVALID_ARG, "null store");
-  auto it = s->chunks.find(c);
-  if (it == s->chunks.end()) return fail(PIC_ERR_INVALID_ARG, "unknown chunk handle");
-  if (--it->second.refs == 0) {
-    s->give(it->second.blocks);
-    s->chunks.erase(it);
-  }
+  Chunk* ch = s->live_chunk(c);
+  if (!ch) return fail(PIC_ERR_INVALID_ARG, "unknown chunk handle");
+  if (--ch->refs == 0) s->retire(c);
   return PIC_OK;
 }
 
@@ -916,12 +1077,39 @@ pic_status pic_release_request(pic_store* s, pic_request r) {
   s->give(it->second.private_blocks);
   for (int32_t cid : it->second.chunk_ids) {
     auto ci = s->chunks.find(cid);
-    if (ci != s->chunks.end() && --ci->second.refs == 0) {
-      s->give(ci->second.blocks);
-      s->chunks.erase(ci);
-    }
+    if (ci != s->chunks.end() && ci->second.refs > 0 && --ci->second.refs == 0) s->retire(cid);
   }
   s->requests.erase(it);
+  return PIC_OK;
+}
+
+pic_status pic_store_get_cache_stats(const pic_store* s, pic_cache_stats* out) {
+  if (!s || !out) return fail(PIC_ERR_INVALID_ARG, "null argument");
+  std::memset(out, 0, sizeof(*out));
+  out->hits = s->cache_hits;
+  out->misses = s->cache_misses;
+  out->evictions = s->cache_evictions;
+  for (const auto& kv : s->chunks)
+    if (kv.second.cached) {
+      ++out->cached_chunks;
+      if (kv.second.refs == 0) {
+        ++out->unreferenced_chunks;
+        out->unreferenced_blocks += (int32_t)kv.second.blocks.size();
+      }
+    }
+  out->blocks_in_use = s->cfg.num_blocks - (int32_t)s->free.size();
+  out->block_bytes = (int64_t)s->block_bytes() * 2 * s->m->cfg.n_layers;
+  return PIC_OK;
+}
+
+pic_status pic_store_evict(pic_store* s, int32_t max_chunks, int32_t* n_evicted) {
+  if (!s) return fail(PIC_ERR_INVALID_ARG, "null store");
+  int32_t n = 0;
+  while (!s->lru.empty() && (max_chunks < 0 || n < max_chunks)) {
+    s->evict_front();
+    ++n;
+  }
+  if (n_evicted) *n_evicted = n;
   return PIC_OK;
 }
 

@@ -46,6 +46,25 @@ def test_binding_covers_every_declared_symbol():
     assert set(declared_functions()) <= set(_lib.SIGNATURES)
 
 
+def declared_arities():
+    """name -> number of parameters, from the prototypes in include/*.h."""
+    out = {}
+    for h in HEADERS:
+        src = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        for m in re.finditer(r"\b(pic_\w+)\s*\(([^;{}]*?)\)\s*;", src, flags=re.S):
+            params = m.group(2).strip()
+            out[m.group(1)] = 0 if params in ("", "void") else params.count(",") + 1
+    return out
+
+
+def test_binding_arities_match_the_header():
+    from position_independent_kv_link_gb300 import _lib
+    ar = declared_arities()
+    assert set(ar) == set(declared_functions())
+    wrong = {n: (k, len(_lib.SIGNATURES[n][1])) for n, k in ar.items() if len(_lib.SIGNATURES[n][1]) != k}
+    assert not wrong, wrong
+
+
 def test_host_only_calls(lib):
     assert lib.pic_status_string(0) == b"PIC_OK"
     assert lib.pic_status_string(2) == b"PIC_ERR_OUT_OF_BLOCKS"
@@ -54,6 +73,10 @@ def test_host_only_calls(lib):
     assert lib.pic_model_create(None, None, None) == 1
     assert lib.pic_release_chunk(None, 1) == 1
     assert lib.pic_op_gemm(0, None, None, None, 1, 1, 1, None) == 1
+    assert lib.pic_compile_cached(None, None, None, 1, 0, None, None, None) == 1
+    assert lib.pic_store_get_cache_stats(None, None) == 1
+    assert lib.pic_store_evict(None, -1, None) == 1
+    assert lib.pic_decode(None, None, None, 1, None, None, None, None, None) == 1
 
 
 def test_build_targets_sm103a():
