@@ -713,8 +713,9 @@ pic_status check_compile_args(const pic_store* s, const int32_t* const* tokens, 
   return PIC_OK;
 }
 
-// Compiles chunks `idx` of the call in one forward into newly taken blocks (the caller has
-// made the blocks free); on success out_ids[j] is the new chunk of idx[j] (refcount 1).
+// Compiles chunks `idx` of the call in one forward into newly taken blocks (evicting
+// unreferenced cached chunks first if too few are free); on success out_ids[j] is the new
+// chunk of idx[j] (refcount 1).
 pic_status compile_batch(pic_store* s, const int32_t* const* tokens, const int32_t* lens, const std::vector<int>& idx,
                          int32_t n_dummy, cudaStream_t st, std::vector<int32_t>& out_ids) {
   long long rows = n_dummy;
