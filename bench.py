@@ -395,20 +395,23 @@ def run_ours(args):
         "setup_s": {"weights_gen": t_gen},
     }
     if cpu_weights is not None:
-        # the oracle as it stands, on this host's cores: the same sample of the link (its first
-        # --cpu-layers layers) repeated until about 10 s of CPU work, the mean scaled to all layers
-        n_l = args.cpu_layers
-        model_o, st_o, cids_o = oracle_sample(wl, cpu_weights, n_l)
-        ts = []
-        while sum(ts) < 10.0 and len(ts) < 30:
-            ts.append(oracle_link_time(st_o, cids_o, wl))
-        t = statistics.mean(ts)
-        cpu_step = t * wl.spec.n_layers / n_l
-        line["cpu_baseline"] = {
-            "value": tokens / cpu_step, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
-            "sample": f"fp64 oracle link of this workload over the first {n_l} of {spec.n_layers} layers (+ LM head), "
-                      f"mean of {len(ts)} runs ({sum(ts):.1f} s of CPU work), {t:.2f} s each, scaled "
-                      f"x{spec.n_layers / n_l:g}; chunk KV from the seeded generator"}
+        try:
+            # the oracle as it stands, on this host's cores: the same sample of the link (its first
+            # --cpu-layers layers) repeated until about 10 s of CPU work, the mean scaled to all layers
+            n_l = args.cpu_layers
+            model_o, st_o, cids_o = oracle_sample(wl, cpu_weights, n_l)
+            ts = []
+            while sum(ts) < 10.0 and len(ts) < 30:
+                ts.append(oracle_link_time(st_o, cids_o, wl))
+            t = statistics.mean(ts)
+            cpu_step = t * wl.spec.n_layers / n_l
+            line["cpu_baseline"] = {
+                "value": tokens / cpu_step, "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
+                "sample": f"fp64 oracle link of this workload over the first {n_l} of {spec.n_layers} layers (+ LM head), "
+                          f"mean of {len(ts)} runs ({sum(ts):.1f} s of CPU work), {t:.2f} s each, scaled "
+                          f"x{spec.n_layers / n_l:g}; chunk KV from the seeded generator"}
+        except Exception as e:   # reported in the line, never fatal to it
+            line["cpu_baseline"] = {"error": repr(e)[:200], "kind": "oracle"}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
