@@ -495,3 +495,22 @@ def test_decode_pins_catch_planted_mistakes(monkeypatch, tiny):
     with monkeypatch.context() as m:
         m.setattr(po, "run_jobs", reuses_last_position)
         assert worst_error() > 1e-6
+
+
+def test_decode_opens_blocks_in_call_order(tiny):
+    """Two requests whose last pages are full decode in one call: the new blocks are taken in
+    the call's request order (hand-worked fixture)."""
+    spec, w, model = tiny
+    g = json.load(open(os.path.join(GOLD, "tiny_decode_two_new_blocks.json")))
+    st = po.OracleStore(model, 64)
+    cids = st.compile_many([pi.gen_tokens(L, spec.vocab, 56, i) for i, L in enumerate(g["chunk_lengths"])])
+    assert [st.chunks[c].blocks for c in cids] == g["compile_blocks"]
+    out = st.link([([cids[c] for c in r["chunks"]], pi.gen_tokens(r["query_length"], spec.vocab, 57, i))
+                   for i, r in enumerate(g["requests"])], 2)
+    assert [m.private_blocks.tolist() for m in out.meta] == [r["link_private_blocks"] for r in g["requests"]]
+    for i, step in enumerate(g["steps"]):
+        d = st.decode([out.rids[j] for j in step["order"]], [i + 3] * len(step["order"]))
+        assert d.positions.tolist() == step["positions"] and d.slots.tolist() == step["slots"]
+    for rid, f in zip(out.rids, g["final"]):
+        m = st.request_meta(rid)
+        assert {k: getattr(m, k).tolist() for k in f} == f
