@@ -164,9 +164,10 @@ def roofline_link(wl: pi.Workload, pk) -> dict:
         flops_attn += sum(p + 1 for p in sel) * H * D * 4.0 * sp.n_layers
     flops = 2.0 * rows * (sp.n_layers * per_layer_w / 2) + 2.0 * len(wl.requests) * sp.vocab * sp.d_model + flops_attn
     t_mem = (W + kv) / (pk["hbm_gbs"] * 1e9)
-    t_flop = flops / (pk["bf16_tflops"] * 1e12)
+    t_flop = flops / (pk["bf16_tflops_sustained"] * 1e12)   # a link step is a long run of back-to-back GEMMs
     return {"bytes": W + kv, "flops": flops, "t_mem_ms": t_mem * 1e3, "t_flop_ms": t_flop * 1e3,
-            "roofline_ms": max(t_mem, t_flop) * 1e3, "bound": "hbm" if t_mem >= t_flop else "tensor"}
+            "roofline_ms": max(t_mem, t_flop) * 1e3, "bound": "hbm" if t_mem >= t_flop else "tensor",
+            "peaks": "HBM copy and sustained dense bf16, measured"}
 
 
 # ----------------------------------------------------------------------------- CPU oracle (baseline / reference arm)
@@ -245,6 +246,93 @@ def run_reference(args):
 
 # ----------------------------------------------------------------------------- GPU arm
 
+def make_store(model, wl, extra_positions=0):
+    """A store sized for the workload: its chunks, one private block per chunk per request and
+    the query pages (with slack), every request's positions."""
+    from position_independent_kv_link_gb300 import PicStore
+    n_pos = max(sum(len(wl.chunks[c]) for c in r.chunk_ids) + len(r.query) for r in wl.requests)
+    n_blocks = sum(-(-len(c) // 16) for c in wl.chunks) + 4 * (wl.selected_rows // 16 + 2 * len(wl.requests) * 10)
+    return PicStore(model, num_blocks=n_blocks, max_rows=max(wl.selected_rows, 2048),
+                    max_requests=max(len(wl.requests), 64), max_positions=n_pos + 80 + extra_positions,
+                    max_logit_rows=max(64, len(wl.requests)))
+
+
+def compile_all(store, wl):
+    """Every chunk of the workload compiled, 4 per call (LegoLink-0 dummies when the workload has them)."""
+    cids = []
+    for i in range(0, len(wl.chunks), 4):
+        cids += store.compile(wl.chunks[i:i + 4], n_dummy=wl.n_dummy)
+    store.sync()
+    return cids
+
+
+def kernel_classes(prof, steps):
+    """Per-class event times of an instrumented run, per step."""
+    return {k: {"ms_per_step": v["ms"] / steps, "launches_per_step": v["launches"] / steps,
+                "GBs": v["bytes"] / (v["ms"] / 1e3) / 1e9 if v["ms"] > 0 else None,
+                "TFs": v["flops"] / (v["ms"] / 1e3) / 1e12 if v["ms"] > 0 else None}
+            for k, v in prof.items() if isinstance(v, dict)}
+
+
+def attention_roofline(prof, n_layers, pk):
+    """The fused-RoPE paged attention (kernel + split merge) against its own floor: the slower of
+    its FLOPs (4 per head dim and visible query-key pair) at the sustained bf16 tensor peak (it
+    runs inside a long step) and its KV + q + output bytes at the HBM peak."""
+    a = prof.get("attention")
+    if not a or a["ms"] <= 0:
+        return None
+    t_flop = a["flops"] / (pk["bf16_tflops_sustained"] * 1e12) * 1e3
+    t_mem = a["bytes"] / (pk["hbm_gbs"] * 1e9) * 1e3
+    floor = max(t_flop, t_mem)
+    return {"bound": "tensor" if t_flop >= t_mem else "hbm", "ms": a["ms"], "floor_ms": floor,
+            "frac": floor / a["ms"], "us_per_layer": a["ms"] * 1e3 / n_layers,
+            "achieved_tflops": a["flops"] / (a["ms"] / 1e3) / 1e12, "achieved_gbs": a["bytes"] / (a["ms"] / 1e3) / 1e9,
+            "peak_tflops": pk["bf16_tflops_sustained"], "peak_gbs": pk["hbm_gbs"],
+            "peak_kind": "bf16 dense sustained / HBM copy, measured"}
+
+
+def measure_config(model, name, pk, steps, warmup):
+    """One evaluated configuration: compile its chunks, time `steps` link steps (all requests in
+    one pic_link call) after `warmup`, then the same steps under per-launch profiling."""
+    wl = workload(name)
+    store = make_store(model, wl)
+    try:
+        cids = compile_all(store, wl)
+        reqs = [([cids[c] for c in r.chunk_ids], r.query) for r in wl.requests]
+
+        def step():
+            res = store.link(reqs, wl.k)
+            for r in res.requests:
+                store.release_request(r)
+        for _ in range(max(3, warmup)):
+            step()
+        store.sync()
+        stream = torch.cuda.current_stream()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        store.sync()
+        ms = e0.elapsed_time(e1) / steps
+        store.profile_begin()
+        for _ in range(steps):
+            step()
+        prof = store.profile_end()
+        store.sync()
+    finally:
+        store.close()
+    rl = roofline_link(wl, pk)
+    return {"workload": wl.name, "k": wl.k, "requests": len(wl.requests), "linked_tokens": wl.linked_tokens,
+            "selected_rows": wl.selected_rows, "steps": steps, "ms_per_step": ms,
+            "tokens_per_s": wl.linked_tokens / (ms / 1e3),
+            "link_roofline": {"bound": rl["bound"], "roofline_ms": rl["roofline_ms"], "frac": rl["roofline_ms"] / ms,
+                              "t_mem_ms": rl["t_mem_ms"], "t_flop_ms": rl["t_flop_ms"]},
+            "attention_roofline": attention_roofline(prof, wl.spec.n_layers, pk),
+            "kernels": kernel_classes(prof, steps)}
+
+
 def run_ours(args):
     world, rank, local = dist_env()
     torch.cuda.set_device(local)
@@ -263,18 +351,11 @@ def run_ours(args):
     cpu_weights = weights if (rank == 0 and not args.no_cpu_baseline) else None
     if cpu_weights is None:
         del weights
-    n_pos = max(sum(len(wl.chunks[c]) for c in r.chunk_ids) + len(r.query) for r in wl.requests)
-    n_blocks = sum(-(-len(c) // 16) for c in wl.chunks) + 4 * (wl.selected_rows // 16 + 2 * len(wl.requests) * 10)
-    store = PicStore(model, num_blocks=n_blocks, max_rows=max(wl.selected_rows, 2048),
-                     max_requests=max(len(wl.requests), 64), max_positions=n_pos + 80 + 2 * args.steps,
-                     max_logit_rows=max(64, len(wl.requests)))
+    store = make_store(model, wl, extra_positions=2 * args.steps)
     # compile every chunk once (timed separately; batches of up to 4 chunks)
     torch.cuda.synchronize()
     c0 = time.perf_counter()
-    cids = []
-    for i in range(0, len(wl.chunks), 4):
-        cids += store.compile(wl.chunks[i:i + 4], n_dummy=wl.n_dummy)
-    store.sync()
+    cids = compile_all(store, wl)
     compile_s = time.perf_counter() - c0
     compiled_tokens = sum(len(c) for c in wl.chunks)
 
@@ -354,12 +435,14 @@ def run_ours(args):
     dec_roof_ms = rl["bytes"] / (pk["hbm_gbs"] * 1e9) * 1e3   # weights + the requests' KV, read once
     dec_ms = dec["ms"]
     n_r = dec["requests"]
-    # dominant kernel: the gate/up projection GEMM (largest weight stream of the step);
-    # achieved = its algorithmic bytes per launch / its mean event-timed launch duration
-    g = prof["gemm_gate_up"]
-    achieved = g["bytes"] / (g["ms"] / 1e3) / 1e9 if g["ms"] > 0 else None
+    # dominant kernel: the tcgen05 GEMM over ALL its launches of the step (QKV, O, gate/up, down,
+    # LM head); achieved = their algorithmic bytes (weights + activations read once, fp32 result
+    # written once) / their summed event-timed launch durations
+    gl = [prof[k] for k in ("gemm", "gemm_gate_up") if k in prof]
+    g_ms, g_bytes, g_n = sum(v["ms"] for v in gl), sum(v["bytes"] for v in gl), sum(v["launches"] for v in gl)
+    achieved = g_bytes / (g_ms / 1e3) / 1e9 if g_ms > 0 else None
     traffic = None
-    if GEMM_TRAFFIC["src_sha256_12"] == kernel_sha():
+    if GEMM_TRAFFIC["src_sha256_12"] == kernel_sha() and GEMM_TRAFFIC.get("shape") == "all launches of a c2 step":
         traffic = GEMM_TRAFFIC["bytes_per_launch"]
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -368,10 +451,13 @@ def run_ours(args):
         "config": {"workload": wl.name, "k": wl.k, "linked_tokens": tokens, "selected_rows": wl.selected_rows,
                    "l2": "inputs larger than L2 (15 GB weights + 0.68 GB KV per step)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-        "roofline": {"bound": "hbm", "kernel": "tcgen05 GEMM, MLP gate/up projection (28672 x 4096 weights)",
+        "roofline": {"bound": "hbm", "kernel": "tc_gemm_kernel (tcgen05), all launches of the step: QKV, O, gate/up, "
+                                                 "down projections and the LM head",
                      "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
                      "frac": (achieved / pk["hbm_gbs"]) if achieved else None, "traffic": traffic,
-                     "peak_source": pk["source"]},
+                     "algorithmic_bytes_per_launch": g_bytes / g_n if g_n else None,
+                     "launches_per_step": g_n / args.steps, "peak_source": pk["source"]},
+        "attention_roofline": attention_roofline(prof, spec.n_layers, pk),
         "link_roofline": {"roofline_ms": rl["roofline_ms"], "bound": rl["bound"], "measured_ms": ms_step,
                           "frac": rl["roofline_ms"] / ms_step, "bytes": rl["bytes"], "flops": rl["flops"],
                           "t_mem_ms": rl["t_mem_ms"], "t_flop_ms": rl["t_flop_ms"]},
@@ -394,6 +480,17 @@ def run_ours(args):
                    "gpu_launches_per_step": dec["launches"] / args.steps, "kernels": dec["kernels"]},
         "setup_s": {"weights_gen": t_gen},
     }
+    # the other evaluated configurations on the same model (the 8B shape): link throughput, the
+    # link roofline and per-class kernel times; c5 at k = 16 is the headline workload itself
+    if not args.no_configs and spec.n_layers == 32:
+        cfgs = {}
+        for name, n in (("c3", 5), ("c4", 5), ("c5_k0", 10), ("c5_k2", 10), ("c5_k32", 10), ("c5_k512", 5)):
+            try:
+                cfgs[name] = measure_config(model, name, pk, min(n, args.steps), 3)
+            except Exception as e:   # reported in the line, never fatal to it
+                cfgs[name] = {"error": repr(e)[:300]}
+        cfgs["c5_k16"] = {"same_as": "the headline workload (c2)"}
+        line["configs"] = cfgs
     if cpu_weights is not None:
         try:
             # the oracle as it stands, on this host's cores: the same sample of the link (its first
@@ -592,7 +689,8 @@ def run_kernel(args):
 
     gemm:      gate/up projection, 28672 x 4096 weights, 224 selected rows (tcgen05).
     attention: the link's paged attention, 10 x 512 chunks + 64 query, k = 16
-               (224 query rows, 324 pages, 32 Q / 8 KV heads), fused RoPE.
+               (224 query rows, 324 pages, 32 Q / 8 KV heads), fused RoPE; --shape
+               n_chunks,k,query_len for other prompts of 512-token chunks.
     """
     import ctypes as C
     from position_independent_kv_link_gb300 import _lib as L, api
@@ -616,7 +714,8 @@ def run_kernel(args):
             call = lambda: L.check(lib.pic_op_gemm_packed(Wp.data_ptr(), X.data_ptr(), Y.data_ptr(), N, K, T, sp))
         nbytes, flops = N * K * 2 + T * K * 2 + T * N * 4, 2.0 * N * K * T
     else:
-        lens, qlen, k = [512] * 10, 64, 16
+        n_chunks, k, qlen = (int(x) for x in args.shape.split(",")) if args.shape else (10, 16, 64)
+        lens = [512] * n_chunks
         pblk, ppos, plen, sel, off = [], [], [], [], 0
         for i, Ln in enumerate(lens + [qlen]):
             for j in range(-(-Ln // 16)):
@@ -666,11 +765,13 @@ def main():
     ap.add_argument("--config", default="c2", help="tiny, c2, c3, c4, c5_k{0,2,16,32,512}")
     ap.add_argument("--cpu-layers", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true", help="skip the other configurations' link measurements")
     ap.add_argument("--kernel", choices=["gemm", "attention", "decode", "compile"], default=None,
                     help="time one kernel-level call at its 8B link shape instead of the link step "
                          "(decode: decode steps after one link of --config; compile: calls of 4 x 512-token "
                          "chunks)")
-    ap.add_argument("--shape", default=None, help="gemm N,K,T for --kernel gemm (default 28672,4096,224)")
+    ap.add_argument("--shape", default=None, help="gemm N,K,T for --kernel gemm (default 28672,4096,224); "
+                                                  "attention n_chunks,k,query_len of 512-token chunks (default 10,16,64)")
     ap.add_argument("--unpacked", action="store_true", help="--kernel gemm on the plain [N][K] layout")
     args = ap.parse_args()
     if args.kernel == "decode":

@@ -53,7 +53,9 @@ typedef enum {
   PIC_ERR_CUDA = 3,            /* a CUDA runtime call failed (message in pic_last_error) */
   PIC_ERR_DEVICE_TIMEOUT = 4,  /* a kernel gave up a bounded wait; its outputs are invalid */
   PIC_ERR_CAPACITY = 5,        /* the call exceeds a capacity fixed at store creation */
-  PIC_ERR_UNSUPPORTED = 6      /* shape/dtype combination not built */
+  PIC_ERR_UNSUPPORTED = 6,     /* shape/dtype combination not built */
+  PIC_ERR_RANGE = 7            /* a value bound for an fp16 tensor-core operand was outside fp16's
+                                  range; the outputs since the last pic_sync are invalid */
 } pic_status;
 
 typedef enum { PIC_F32 = 0, PIC_BF16 = 1 } pic_dtype;
@@ -240,9 +242,21 @@ pic_status pic_release_chunk(pic_store* s, pic_chunk c);
 /* Frees the request's private and query blocks and drops its chunk references. */
 pic_status pic_release_request(pic_store* s, pic_request r);
 
-/* Waits for the stream and reports PIC_ERR_DEVICE_TIMEOUT if any kernel gave up a
- * bounded wait since the last pic_sync (the flag is then cleared). */
+/* Waits for the stream and reports what the kernels flagged since the last pic_sync (the
+ * flags are then cleared): PIC_ERR_DEVICE_TIMEOUT if a kernel gave up a bounded wait, else
+ * PIC_ERR_RANGE if a value bound for an fp16 tensor-core operand of a bf16 model was outside
+ * fp16's finite range or NaN -- a normed or SwiGLU activation or a rotated, scaled q above
+ * 65504 in magnitude, a stored V above 65504 or a stored K above 46000 (RoPE can grow a K
+ * component by up to sqrt 2). The pages fix no precision beyond bf16 storage; the fp16
+ * operands are this library's reading, and this check is where a model outside it shows.
+ * s may be NULL. */
 pic_status pic_sync(pic_store* s, pic_stream_t stream);
+
+/* Sets one of the device flags that pic_sync reports, from the host, without running a
+ * kernel: 1 = the tensor-core attention's bounded-wait timeout, 2 = the tensor-core GEMM's,
+ * 3 = the fp16 range flag. Lets a caller (and the tests) exercise its handling of those
+ * statuses without making a kernel wait or overflow. PIC_ERR_INVALID_ARG for other values. */
+pic_status pic_debug_raise_device_flag(int32_t which);
 
 /* ------------------------------------------------------------------ profiling
  * Between pic_profile_begin and pic_profile_end the store brackets each of its kernel
@@ -325,7 +339,8 @@ pic_status pic_op_attention(int32_t dtype, int32_t T, int32_t n_heads, int32_t n
  *  - A shape whose exact work list and partial results exceed the area is rejected
  *    with PIC_ERR_CAPACITY before any GPU work.
  *  - The first call on a device looks up the area's device address (with that device
- *    current); make that first call before any stream capture.
+ *    current); make that first call before any stream capture. That look-up is guarded
+ *    by a lock, so first calls from several host threads are safe.
  *  - Every call reuses the same area and leaves its contents behind; nothing in it has
  *    to start at zero (each word read is written earlier in the same call). Calls that
  *    overlap on the GPU (different streams, or different host threads) race on it:
@@ -340,14 +355,17 @@ pic_status pic_op_attention_noalloc(int32_t dtype, int32_t T, int32_t n_heads, i
 
 /* Host only (no GPU work, no device needed): the attention work plan the library launches
  * for a batch of sequences, e.g. the requests of a link or a decode step, each with its
- * selected rows and its pages. Rows are grouped in blocks of up to 32 (tensor-core and
- * mma.sync shapes) or 16 consecutive rows of one sequence; a block reads its sequence's pages
- * up to the page holding its last row's position, split into runs ("parts") whose partial
- * results are merged per (block, KV head).
+ * selected rows and its pages. Rows are grouped in blocks of up to 64 (tensor-core shape:
+ * bf16, head_dim 128, 4 query heads per KV head), 32 (mma.sync shapes with up to 4 query
+ * heads per KV head) or 16 consecutive rows of one sequence; a block reads its sequence's
+ * pages up to the page holding its last row's position, split into runs ("parts") whose
+ * partial results are merged per (block, KV head).
  * seq_rows, seq_pages: [n_seqs + 1] non-decreasing offsets into row_pos [seq_rows[n_seqs]]
  * and page_pos [seq_pages[n_seqs]] (positions ascending within each sequence); num_sms >= 1.
- * Outputs (host): items [max_items][6] = (row0, nrows, kv_head, page0, page1, part), part -1
- * when the block's pages are not split, in the order the kernels take them (the persistent
+ * Outputs (host): items [max_items][7] = (row0, nrows, kv_head, page0, page1, part,
+ * page_mid), part -1 when the block's pages are not split, page_mid the end of the pages of
+ * [page0, page1) that the item's first 32 rows can see (page1 for items of <= 32 rows), in
+ * the order the kernels take them (the persistent
  * kernel's CTA c of n = min(items, num_sms) takes items c, c + n, ...); combines
  * [max_combines][5] = (row0, nrows, kv_head, part0, nparts); counts [3] = (items, combines,
  * parts). PIC_ERR_CAPACITY when an output array is too small (counts are still set);

@@ -5,7 +5,7 @@ import os
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libpiclink.so")
 
 PIC_OK, PIC_ERR_INVALID_ARG, PIC_ERR_OUT_OF_BLOCKS, PIC_ERR_CUDA, PIC_ERR_DEVICE_TIMEOUT, PIC_ERR_CAPACITY, \
-    PIC_ERR_UNSUPPORTED = range(7)
+    PIC_ERR_UNSUPPORTED, PIC_ERR_RANGE = range(8)
 PIC_F32, PIC_BF16 = 0, 1
 
 
@@ -81,6 +81,7 @@ SIGNATURES = {
     "pic_release_chunk": (I32, [P, I32]),
     "pic_release_request": (I32, [P, I32]),
     "pic_sync": (I32, [P, P]),
+    "pic_debug_raise_device_flag": (I32, [I32]),
     "pic_profile_begin": (I32, [P]),
     "pic_profile_end": (I32, [P, C.POINTER(Profile)]),
     "pic_store_launch_count": (C.c_int64, [P]),
@@ -108,7 +109,7 @@ class PicError(RuntimeError):
 
 def status_name(s):
     names = ["PIC_OK", "PIC_ERR_INVALID_ARG", "PIC_ERR_OUT_OF_BLOCKS", "PIC_ERR_CUDA", "PIC_ERR_DEVICE_TIMEOUT",
-             "PIC_ERR_CAPACITY", "PIC_ERR_UNSUPPORTED"]
+             "PIC_ERR_CAPACITY", "PIC_ERR_UNSUPPORTED", "PIC_ERR_RANGE"]
     return names[s] if 0 <= s < len(names) else f"status {s}"
 
 

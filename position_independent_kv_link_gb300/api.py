@@ -347,7 +347,7 @@ def attention_plan(dtype: torch.dtype, n_heads: int, n_kv_heads: int, head_dim: 
     """The attention work plan the library launches (pic_op_attention_plan; host only).
 
     seqs: per sequence (row positions, page start positions), both ascending. Returns
-    (items int32 [n, 6] = row0, nrows, kv_head, page0, page1, part; combines int32 [m, 5] =
+    (items int32 [n, 7] = row0, nrows, kv_head, page0, page1, part, page_mid; combines int32 [m, 5] =
     row0, nrows, kv_head, part0, nparts; number of parts), rows and pages indexed over the
     concatenation of the sequences.
     """
@@ -361,7 +361,7 @@ def attention_plan(dtype: torch.dtype, n_heads: int, n_kv_heads: int, head_dim: 
     counts = np.zeros(3, dtype=np.int32)
     cap_i, cap_c = 1024, 256
     while True:
-        items = np.zeros((cap_i, 6), dtype=np.int32)
+        items = np.zeros((cap_i, 7), dtype=np.int32)
         combs = np.zeros((cap_c, 5), dtype=np.int32)
         st = lib.pic_op_attention_plan(_dtype_code(dtype), n_heads, n_kv_heads, head_dim, len(seqs), _ptr_i32(seq_rows),
                                        _ptr_i32(seq_pages), _ptr_i32(rp), _ptr_i32(pp), num_sms, _ptr_i32(items),

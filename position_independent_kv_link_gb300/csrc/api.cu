@@ -321,7 +321,7 @@ pic_status run_forward_impl(pic_store* s, const Batch& b, float* hidden_out, flo
 
   // pack metadata: tok pos slot out lg | pblk ppos plen | copies | items | combines
   const size_t P = b.pblk.size(), NC = b.copy_pairs.size();
-  const size_t n_int = 5 * (size_t)T + 3 * P + NC + items.size() * 6 + combs.size() * 5;
+  const size_t n_int = 5 * (size_t)T + 3 * P + NC + items.size() * kAttnItemInts + combs.size() * 5;
   if (n_int > s->meta_cap) return fail(PIC_ERR_CAPACITY, "metadata exceeds workspace");
   if (s->meta_ev_pending) {
     PIC_CUDA(cudaEventSynchronize(s->meta_ev));
@@ -344,7 +344,7 @@ pic_status run_forward_impl(pic_store* s, const Batch& b, float* hidden_out, flo
   const int* d_ppos = put(b.ppos.data(), P);
   const int* d_plen = put(b.plen.data(), P);
   const int* d_copy = put(b.copy_pairs.data(), NC);
-  const AttnItem* d_items = (const AttnItem*)put(items.data(), items.size() * 6);
+  const AttnItem* d_items = (const AttnItem*)put(items.data(), items.size() * kAttnItemInts);
   const AttnCombine* d_combs = (const AttnCombine*)put(combs.data(), combs.size() * 5);
   PIC_CUDA(cudaMemcpyAsync(s->meta_d, hp, o * 4, cudaMemcpyHostToDevice, st));
   PIC_CUDA(cudaEventRecord(s->meta_ev, st));
@@ -526,6 +526,7 @@ const char* pic_status_string(pic_status s) {
     case PIC_ERR_DEVICE_TIMEOUT: return "PIC_ERR_DEVICE_TIMEOUT";
     case PIC_ERR_CAPACITY: return "PIC_ERR_CAPACITY";
     case PIC_ERR_UNSUPPORTED: return "PIC_ERR_UNSUPPORTED";
+    case PIC_ERR_RANGE: return "PIC_ERR_RANGE";
   }
   return "PIC_ERR_UNKNOWN";
 }
@@ -596,6 +597,8 @@ pic_status pic_model_create(const pic_model_config* cfg, const pic_weights* w, p
         off += (size_t)j.N * j.K * 2;
       }
       PIC_CUDA(cudaDeviceSynchronize());
+      const pic_status pr = tc_check_pack_range();
+      if (pr != PIC_OK) return pr;
     }
   }
   *out = m.release();
@@ -627,7 +630,7 @@ pic_status pic_store_create(pic_model* m, const pic_store_config* cfg, void* k_p
   s->att_parts_cap = 4 * m->num_sms + c.n_kv_heads * s->att_blocks_cap();
   const size_t max_pages = (size_t)sc.max_positions / kBlock + 2 * (size_t)sc.max_requests + 2;
   const size_t max_items = (size_t)s->att_parts_cap + (size_t)c.n_kv_heads * s->att_blocks_cap();
-  s->meta_cap = 5 * R + 3 * max_pages * sc.max_requests + 2 * (size_t)sc.num_blocks + 6 * max_items +
+  s->meta_cap = 5 * R + 3 * max_pages * sc.max_requests + 2 * (size_t)sc.num_blocks + kAttnItemInts * max_items +
                 5 * (size_t)s->att_parts_cap + 1024;
 
   size_t off = 0;
@@ -1146,9 +1149,22 @@ int64_t pic_store_launch_count(const pic_store* s) { return s ? s->launches : -1
 pic_status pic_sync(pic_store* s, pic_stream_t stream) {
   (void)s;
   PIC_CUDA(cudaStreamSynchronize((cudaStream_t)stream));
+  // every flag is read (and cleared) even when an earlier one is set
   const pic_status a = attn_check_timeout();
   const pic_status g = tc_check_timeout();
-  return a != PIC_OK ? a : g;
+  const pic_status r = rows_check_range();
+  return a != PIC_OK ? a : g != PIC_OK ? g : r;
+}
+
+pic_status pic_debug_raise_device_flag(int32_t which) {
+  switch (which) {
+    case 1: attn_raise_timeout(); break;
+    case 2: tc_raise_timeout(); break;
+    case 3: rows_raise_range(); break;
+    default: return fail(PIC_ERR_INVALID_ARG, "device flag must be 1, 2 or 3");
+  }
+  PIC_CUDA(cudaGetLastError());
+  return PIC_OK;
 }
 
 }  // extern "C"

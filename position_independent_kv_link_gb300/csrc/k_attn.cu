@@ -179,7 +179,10 @@ void launch_attention_simt(const AttnArgs& a, cudaStream_t st) {
 
 bool use_mma(int dtype, int D, int rep) { return dtype == PIC_BF16 && D == 128 && (rep == 1 || rep == 2 || rep == 4 || rep == 8); }
 
-int attention_rows_per_block(int dtype, int D, int rep) { return (use_mma(dtype, D, rep) && rep <= 4) ? 32 : 16; }
+int attention_rows_per_block(int dtype, int D, int rep) {
+  if (tc_attention_supported(dtype, D, rep)) return attention_tc_rows_per_item();
+  return (use_mma(dtype, D, rep) && rep <= 4) ? 32 : 16;
+}
 
 bool attention_persistent(int dtype, int D, int rep) { return tc_attention_supported(dtype, D, rep); }
 
@@ -211,9 +214,11 @@ size_t attention_part_bytes(int n_parts, int rep, int D) {
 
 // Blocks of <= rows_per_block consecutive rows of one sequence; each block reads the prefix of the
 // sequence's pages up to its last row's position, cut into runs of P pages (P chosen below).
+// For blocks of more than 32 rows, the pages its first 32 rows see end earlier (pe0): every
+// item records where, clipped to its own run (page_mid).
 void plan_attention(const AttnPlanInput& in, std::vector<AttnItem>& items, std::vector<AttnCombine>& combines,
                     int& n_parts) {
-  struct Blk { int row0, nrows, pb, pe; };
+  struct Blk { int row0, nrows, pb, pe, pe0; };
   std::vector<Blk> blks;
   long long total = 0;
   const std::vector<int>& rp = *in.row_pos;
@@ -222,10 +227,14 @@ void plan_attention(const AttnPlanInput& in, std::vector<AttnItem>& items, std::
     const int rb = in.rows_per_block > 0 ? in.rows_per_block : kBlock;
     for (int r0 = in.seq_row_begin[s]; r0 < in.seq_row_end[s]; r0 += rb) {
       const int n = std::min(rb, in.seq_row_end[s] - r0);
-      const int maxp = rp[r0 + n - 1];
-      int pe = in.seq_page_begin[s];
-      while (pe < in.seq_page_end[s] && pp[pe] <= maxp) ++pe;
-      blks.push_back({r0, n, in.seq_page_begin[s], pe});
+      auto visible_end = [&](int last_row) {
+        int pe = in.seq_page_begin[s];
+        while (pe < in.seq_page_end[s] && pp[pe] <= rp[last_row]) ++pe;
+        return pe;
+      };
+      const int pe = visible_end(r0 + n - 1);
+      const int pe0 = n > 32 ? visible_end(r0 + 31) : pe;
+      blks.push_back({r0, n, in.seq_page_begin[s], pe, pe0});
       total += (long long)(pe - in.seq_page_begin[s]);
     }
   }
@@ -239,13 +248,13 @@ void plan_attention(const AttnPlanInput& in, std::vector<AttnItem>& items, std::
       const int ns = std::max(1, (np + P - 1) / P);
       for (int g = 0; g < in.G; ++g) {
         if (ns == 1) {
-          its.push_back({b.row0, b.nrows, g, b.pb, b.pe, -1});
+          its.push_back({b.row0, b.nrows, g, b.pb, b.pe, -1, b.pe0});
           continue;
         }
         cbs.push_back({b.row0, b.nrows, g, nparts, ns});
         for (int s = 0; s < ns; ++s) {
           const int p0 = b.pb + s * P, p1 = std::min(b.pe, p0 + P);
-          its.push_back({b.row0, b.nrows, g, p0, p1, nparts + s});
+          its.push_back({b.row0, b.nrows, g, p0, p1, nparts + s, std::min(p1, std::max(p0, b.pe0))});
         }
         nparts += ns;
       }
@@ -263,8 +272,15 @@ void plan_attention(const AttnPlanInput& in, std::vector<AttnItem>& items, std::
   // Persistent kernel: CTA c of n = min(items, SMs) takes items c, c + n, c + 2n, ...; the sorted
   // items are dealt in snake order (round k runs over the CTAs backwards when k is odd). Parts are
   // whole 64-key tiles (4 pages). The part size is the one, among those giving about 1, 1.5, 2,
-  // 3 or 4 items per SM, whose deal has the smallest estimated makespan -- per CTA the sum of its
-  // items' tiles plus two tiles of fixed cost per item (Q load, O drain) -- then the fewest items.
+  // 3 or 4 items per SM, whose deal has the smallest estimated makespan, then the fewest items.
+  // Estimated cost of an item: per 64-key tile one unit for loading and transforming it plus one
+  // per MMA tile that takes part (rows 0-31 up to page_mid, rows 32-63 throughout), and four
+  // units of fixed cost (Q load, O drain).
+  auto cost = [](const AttnItem& it) -> long long {
+    const int nt = (it.page1 - it.page0 + 3) / 4;
+    const int n0 = std::max(0, (it.page_mid - it.page0 + 3) / 4), n1 = it.nrows > 32 ? nt : 0;
+    return nt + n0 + n1 + 4;
+  };
   auto deal = [&](std::vector<AttnItem>& its) -> long long {
     const int n = std::min<int>((int)its.size(), std::max(1, in.num_sms));
     std::vector<AttnItem> dealt(its.size());
@@ -274,7 +290,7 @@ void plan_attention(const AttnPlanInput& in, std::vector<AttnItem>& items, std::
       for (int c = 0; c < m; ++c) {
         const AttnItem& it = its[k * n + ((k & 1) ? m - 1 - c : c)];
         dealt[k * n + c] = it;
-        load[c] += (it.page1 - it.page0 + 3) / 4 + 2;
+        load[c] += cost(it);
       }
     }
     its.swap(dealt);

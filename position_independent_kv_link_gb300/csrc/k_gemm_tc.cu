@@ -53,6 +53,7 @@ constexpr int kThreads = kWarps * 32;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
 __device__ int g_tc_timeout = 0;
+__device__ int g_pack_range = 0;   // a packed weight was outside fp16's finite range (or NaN)
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -424,8 +425,14 @@ __global__ void pack_sw128_kernel(const uint4* __restrict__ W, uint4* __restrict
     const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&v);
     uint4 o;
     __half2* h = reinterpret_cast<__half2*>(&o);
+    bool bad = false;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) h[e] = __float22half2_rn(__bfloat1622float2(b[e]));
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = __bfloat1622float2(b[e]);
+      bad |= !(fabsf(f.x) <= 65504.f) | !(fabsf(f.y) <= 65504.f);
+      h[e] = __float22half2_rn(f);
+    }
+    if (bad) atomicExch(&g_pack_range, 1);
     P[(size_t)tile * (A_STAGE / 16) + r * 8 + (j ^ (r & 7))] = o;
   }
 }
@@ -570,6 +577,23 @@ pic_status tc_pack_weight(const void* W, void* out, int N, int K, cudaStream_t s
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(PIC_ERR_CUDA, std::string("pack launch: ") + cudaGetErrorString(e));
   return PIC_OK;
+}
+
+pic_status tc_check_pack_range() {
+  int v = 0, zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_pack_range, sizeof(int));
+  if (e != cudaSuccess) return fail(PIC_ERR_CUDA, std::string("pack range flag: ") + cudaGetErrorString(e));
+  if (v) {
+    cudaMemcpyToSymbol(g_pack_range, &zero, sizeof(int));
+    return fail(PIC_ERR_RANGE, "a projection weight is outside fp16's range (|w| > 65504 or NaN): it cannot be packed "
+                               "as an fp16 tensor-core operand");
+  }
+  return PIC_OK;
+}
+
+void tc_raise_timeout() {
+  const int one = 1;
+  cudaMemcpyToSymbol(g_tc_timeout, &one, sizeof(int));
 }
 
 pic_status tc_check_timeout() {

@@ -3,6 +3,7 @@
 // residual stream, SwiGLU, block copies for request-private pages, KV import. All are
 // memory-bound; float4 accesses over rows.
 #include <algorithm>
+#include <type_traits>
 
 #include "pic_internal.h"
 
@@ -11,6 +12,23 @@ namespace pic {
 namespace {
 
 constexpr int kRowThreads = 256;
+
+// fp16 range guard. For bf16 models the tensor cores take fp16 operands: the activations these
+// kernels write (normed rows, SwiGLU output, the rotated and scaled q) and, inside attention, K
+// rotated by RoPE and V. A value outside fp16's finite range (|x| > 65504, or NaN) would become
+// inf there without notice, so the kernels that write those values set this word instead;
+// pic_sync reports it as PIC_ERR_RANGE. Stored K is checked against 46000: a rotation mixes two
+// components and can grow one by up to sqrt(2) (65504 / sqrt(2) = 46319).
+__device__ unsigned int g_range_flag = 0;
+constexpr float kF16Max = 65504.f;
+constexpr float kKRotMax = 46000.f;
+__device__ __forceinline__ bool outside(float x, float lim) { return !(fabsf(x) <= lim); }
+__device__ __forceinline__ bool outside4(float4 v, float lim) {
+  return outside(v.x, lim) | outside(v.y, lim) | outside(v.z, lim) | outside(v.w, lim);
+}
+__device__ __forceinline__ void flag_range(bool bad) {
+  if (bad) atomicOr(&g_range_flag, 1u);
+}
 
 __device__ __forceinline__ float block_sum(float v, float* red) {
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -47,10 +65,14 @@ __global__ void embed_norm_kernel(int d, const T* __restrict__ E, const int* __r
   }
   ss = block_sum(ss, red);
   const float r = rsqrtf(ss / d + eps);
+  bool bad = false;
   for (int i = threadIdx.x; i < d; i += blockDim.x) {
     h[(size_t)t * d + i] = row[i];
-    x[(size_t)t * d + i] = from_f<A>(row[i] * r * gain[i]);
+    const float y = row[i] * r * gain[i];
+    if constexpr (std::is_same<A, __half>::value) bad |= outside(y, kF16Max);
+    x[(size_t)t * d + i] = from_f<A>(y);
   }
+  flag_range(bad);
 }
 
 template <typename T>
@@ -70,6 +92,7 @@ __device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16* dst, float4
 
 template <>
 __device__ __forceinline__ void store4<__half>(__half* dst, float4 v) {
+  flag_range(outside4(v, kF16Max));
   __half2 a = __floats2half2_rn(v.x, v.y), b = __floats2half2_rn(v.z, v.w);
   uint2 u;
   u.x = *reinterpret_cast<uint32_t*>(&a);
@@ -130,6 +153,7 @@ __global__ void qkv_epilogue_kernel(int H, int G, int D, const float* __restrict
     const int kv = m / (G * D);          // 0: K, 1: V
     const int g = (m % (G * D)) / D, i = m % D;
     T* dst = kv == 0 ? kl : vl;
+    if constexpr (std::is_same<T, __nv_bfloat16>::value) flag_range(outside4(v, kv == 0 ? kKRotMax : kF16Max));
     store4<T>(dst + (((size_t)blk * G + g) * kBlock + r) * D + i, v);
   }
 }
@@ -222,12 +246,32 @@ __global__ void import_kv_kernel(int n, int G, int D, const T* __restrict__ ks, 
   for (int j = threadIdx.x; j < G * D; j += blockDim.x) {
     const int g = j / D, i = j % D;
     const size_t dst = ((((size_t)l * num_blocks_total + blk) * G + g) * kBlock + r) * D + i;
-    kp[dst] = ks[src + j];
-    vp[dst] = vs[src + j];
+    const T k = ks[src + j], v = vs[src + j];
+    if constexpr (std::is_same<T, __nv_bfloat16>::value)
+      flag_range(outside(to_f<T>(k), kKRotMax) | outside(to_f<T>(v), kF16Max));
+    kp[dst] = k;
+    vp[dst] = v;
   }
 }
 
 }  // namespace
+
+pic_status rows_check_range() {
+  unsigned v = 0, zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_range_flag, sizeof(v));
+  if (e != cudaSuccess) return fail(PIC_ERR_CUDA, std::string("range flag: ") + cudaGetErrorString(e));
+  if (v) {
+    cudaMemcpyToSymbol(g_range_flag, &zero, sizeof(zero));
+    return fail(PIC_ERR_RANGE, "a value bound for an fp16 tensor-core operand was outside fp16's range (|x| > 65504, "
+                               "or > 46000 for stored K, or NaN); the outputs since the last pic_sync are invalid");
+  }
+  return PIC_OK;
+}
+
+void rows_raise_range() {
+  const unsigned one = 1;
+  cudaMemcpyToSymbol(g_range_flag, &one, sizeof(one));
+}
 
 void launch_embed_norm(int dtype, int T, int d, const void* embed, const int* tok, const float* gain, float eps,
                        float* h, void* x, cudaStream_t st) {

@@ -9,6 +9,7 @@
 // planner and kernels on it. The area is a file-scope device array, so every GPU that
 // loads the library holds it until the process exits.
 #include <cstring>
+#include <mutex>
 #include <vector>
 
 #include "pic_internal.h"
@@ -24,13 +25,16 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratch
 constexpr int kMaxDevices = 64;
 
 // The array's name in host code is only a host-side stand-in; the kernels need the
-// device address, fetched once per device with that device current.
+// device address, fetched once per device with that device current. The per-device cache is
+// filled under a mutex, so first calls from several host threads are safe.
 pic_status scratch_address(void** out) {
+  static std::mutex mu;
   static void* addr[kMaxDevices] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return fail(PIC_ERR_CUDA, std::string("cudaGetDevice: ") + cudaGetErrorString(e));
   if (dev < 0 || dev >= kMaxDevices) return fail(PIC_ERR_UNSUPPORTED, "device index beyond the supported range");
+  std::lock_guard<std::mutex> lock(mu);
   if (!addr[dev]) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
@@ -98,7 +102,7 @@ pic_status pic_op_attention_noalloc(int32_t dtype, int32_t T, int32_t n_heads, i
   // exact footprint of this call: metadata ints, partial outputs and (max, sum) pairs, then
   // the rotated fp16 q of the tensor-core path
   const int rep = n_heads / n_kv_heads;
-  const size_t n_ints = (size_t)T + 3 * (size_t)n_pages + 6 * items.size() + 5 * combs.size();
+  const size_t n_ints = (size_t)T + 3 * (size_t)n_pages + kAttnItemInts * items.size() + 5 * combs.size();
   const size_t o_part = align256(n_ints * 4);
   const size_t o_ml = o_part + align256((size_t)n_parts * kAttnPartRows * rep * head_dim * 4);
   const size_t o_q16 = o_ml + align256((size_t)n_parts * kAttnPartRows * rep * 2 * 4);
@@ -118,7 +122,7 @@ pic_status pic_op_attention_noalloc(int32_t dtype, int32_t T, int32_t n_heads, i
   ints.insert(ints.end(), page_pos_host, page_pos_host + n_pages);
   ints.insert(ints.end(), page_len_host, page_len_host + n_pages);
   const size_t o_items = ints.size();
-  ints.resize(o_items + items.size() * 6);
+  ints.resize(o_items + items.size() * kAttnItemInts);
   std::memcpy(ints.data() + o_items, items.data(), items.size() * sizeof(AttnItem));
   const size_t o_combs = ints.size();
   ints.resize(o_combs + combs.size() * 5);

@@ -28,7 +28,7 @@ AttnScratchLayout attn_layout(int T, int n_heads, int n_kv_heads, int head_dim, 
   const int n_blocks = (T + kBlock - 1) / kBlock;
   L.max_parts = 4 * current_sms() + n_kv_heads * n_blocks;
   L.max_items = L.max_parts + n_kv_heads * n_blocks;
-  const size_t ints = (size_t)T + 3 * (size_t)n_pages + 6 * (size_t)L.max_items + 5 * (size_t)L.max_parts;
+  const size_t ints = (size_t)T + 3 * (size_t)n_pages + kAttnItemInts * (size_t)L.max_items + 5 * (size_t)L.max_parts;
   L.ints_bytes = align256(ints * 4);
   const int rep = std::max(1, n_heads / std::max(1, n_kv_heads));
   L.part_o_off = L.ints_bytes;
@@ -124,7 +124,7 @@ pic_status pic_op_attention(int32_t dtype, int32_t T, int32_t n_heads, int32_t n
   ints.insert(ints.end(), page_pos_host, page_pos_host + n_pages);
   ints.insert(ints.end(), page_len_host, page_len_host + n_pages);
   const size_t o_items = ints.size();
-  ints.resize(o_items + items.size() * 6);
+  ints.resize(o_items + items.size() * kAttnItemInts);
   std::memcpy(ints.data() + o_items, items.data(), items.size() * sizeof(AttnItem));
   const size_t o_combs = ints.size();
   ints.resize(o_combs + combs.size() * 5);

@@ -127,13 +127,27 @@ pic_status tc_pack_weight(const void* W, void* out, int N, int K, cudaStream_t s
 pic_status tc_check_timeout();
 // Same for the tcgen05 attention kernel (k_attn_tc.cu).
 pic_status attn_check_timeout();
+// Reads and clears the device word the row-wise kernels set when a value bound for an fp16
+// tensor-core operand is outside fp16's range (k_rows.cu): PIC_ERR_RANGE.
+pic_status rows_check_range();
+// Reads and clears the flag tc_pack_weight sets for a weight outside fp16's range: PIC_ERR_RANGE.
+pic_status tc_check_pack_range();
+// Set those device flags from the host, as the kernels would (pic_debug_raise_device_flag).
+void attn_raise_timeout();
+void tc_raise_timeout();
+void rows_raise_range();
 
 // ------------------------------------------------------------------ attention (k_attn.cu)
-constexpr int kAttnPartRows = 32;          // row slots of one split-partial slab
+constexpr int kAttnPartRows = 64;          // row slots of one split-partial slab (rows of the largest item)
 
-struct AttnItem {      // one CTA's work: <= rb consecutive rows of one sequence x one KV head x a page range
-  int row0, nrows, g, page0, page1, part;  // part < 0: write normalized output directly
+// One CTA's work: <= rb consecutive rows of one sequence x one KV head x the page range
+// [page0, page1). part < 0: write the normalized output directly, else a split partial.
+// page_mid: the first 32 rows of the item see no key at or after page page_mid of the range
+// (the tensor-core kernel stops their MMA tile there); page1 when the item has <= 32 rows.
+struct AttnItem {
+  int row0, nrows, g, page0, page1, part, page_mid;
 };
+constexpr int kAttnItemInts = sizeof(AttnItem) / sizeof(int);
 struct AttnCombine {   // merge `nparts` partial results of rows [row0, row0+nrows) for KV head g
   int row0, nrows, g, part0, nparts;
 };
@@ -142,7 +156,7 @@ struct AttnArgs {
   // scaled (attn_q_map), K and V pools of the layer as [rows][D] bf16 (attn_kv_map)
   CUtensorMap qmap, kmap, vmap;
   int dtype, H, G, D;
-  int rb;                   // rows per work item of this plan (16 or 32)
+  int rb;                   // rows per work item of this plan (16, 32 or 64)
   const float* q;           // [T][H][D] pre-RoPE, fp32
   const int* q_pos;         // [T]
   const void* k_layer;      // [nb][G][16][D]
@@ -172,8 +186,10 @@ struct AttnPlanInput {
   int rows_per_block;       // from attention_rows_per_block()
   bool persistent = false;  // from attention_persistent(): one CTA per SM walks a strided item list
 };
-// Rows per work item the attention kernels take for this model shape (16 or 32).
+// Rows per work item the attention kernels take for this model shape (16, 32, or 64 for the
+// tensor-core kernel, whose items are two MMA tiles of 32 rows).
 int attention_rows_per_block(int dtype, int D, int rep);
+int attention_tc_rows_per_item();   // k_attn_tc.cu
 // True when the shape runs the persistent tensor-core kernel: its CTA b takes items b, b + grid,
 // b + 2 grid, ... with grid = min(items, SMs), so the planner orders items for that walk.
 bool attention_persistent(int dtype, int D, int rep);

@@ -12,10 +12,15 @@ checked at the same width with fewer layers).
       only on those chunks), compared with a plain prefill of chunks 1-2.
   c3 (98 x 512 + 64, k = 16): recomputed K/V of the first 4 chunks' rows at every layer
       (prefix sample), plus a 2-layer model over the whole 50k-token prompt, every output.
-  c4 (32 requests x 8 Zipf chunks + 32 query): requests 1 and 2 in full, out of the
-      batch of 32.
+  c3 also against stored fp64 oracle outputs of the whole 32-layer link (the 64 query rows'
+      hidden states, the last row's logits, sampled recomputed K/V rows at sampled layers),
+      written by tests/golden/make_c3_golden.py.
+  c4 (32 requests x 8 Zipf chunks + 32 query): requests 1, 2, 16 and 32 (the last) in full,
+      out of the batch of 32.
 Page tables, slots and selected lists are compared bit-exactly for every request.
 """
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -140,7 +145,15 @@ def test_c5_full_recompute_prefix(m8b):
 
 # ----------------------------------------------------------------------------- c3 (long context)
 
-def test_c3_prefix_rows_all_layers(m8b):
+C3_GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "c3_link_outputs.npz")
+
+
+def test_c3_all_layers(m8b):
+    """The 98-chunk, 50k-token link through all 32 layers. (1) The 64 query rows' final hidden
+    states, the last row's logits and sampled recomputed K/V rows against the fp64 oracle's
+    outputs, computed once by tests/golden/make_c3_golden.py from the same seeded weights and
+    chunk KV. (2) The recomputed K/V of the first 4 chunks' rows at every layer against an
+    oracle link of those chunks (they depend on nothing later)."""
     spec, w, model, om = m8b
     wl = pi.config_workloads()["c3"]
     store = _store(model, wl)
@@ -150,6 +163,15 @@ def test_c3_prefix_rows_all_layers(m8b):
     res = store.link([([g[c] for c in r.chunk_ids], r.query)], wl.k)
     store.sync()
     _check_meta(store, res.requests, _meta_oracle(wl, order, wl.requests))
+    gold = np.load(C3_GOLDEN)
+    info = store.request_info(res.requests[0])
+    assert np.array_equal(info["selected"], gold["selected"])
+    assert rel_err(res.hidden, gold["hidden"]) <= TOL
+    assert rel_err(res.logits, gold["logits"]) <= TOL
+    slots = info["slots"][gold["kv_rows"]]
+    for i, l in enumerate(gold["kv_layers"]):
+        k, v = store.kv_rows(int(l), slots)
+        assert rel_err(k, gold["k"][i]) <= TOL and rel_err(v, gold["v"][i]) <= TOL, int(l)
     # rows of chunks 1-4 depend on those chunks only: an oracle link over them gives their KV
     ost = po.OracleStore(om, 1 << 12)
     _, o = _import(_NullStore(), spec, wl, range(4), ost)
@@ -198,7 +220,7 @@ def test_c4_batched_sampled_requests(m8b):
     res = store.link([([g[c] for c in r.chunk_ids], r.query) for r in wl.requests], wl.k)
     store.sync()
     _check_meta(store, res.requests, _meta_oracle(wl, order, wl.requests))
-    sample = [0, 1]
+    sample = [0, 1, 15, 31]
     need = sorted({c for i in sample for c in wl.requests[i].chunk_ids})
     ost = po.OracleStore(om, 1 << 13)
     _, o = _import(_NullStore(), spec, wl, need, ost)

@@ -181,6 +181,25 @@ def test_small_bf16_link(small_bf16, k, n_dummy):
     compare_link(store, res, out, spec)
 
 
+def test_small_bf16_link_batch_of_four(small_bf16):
+    """Four requests in one tensor-core batch (ragged queries, shared and repeated chunks, the
+    same chunk at different offsets): every request's hidden states, logits and recomputed K/V
+    rows of every layer are compared, so a row offset or work-item boundary that only goes wrong
+    for a later request of the batch shows."""
+    spec, w, model, om = small_bf16
+    wl = pi.make_workload("small batch", spec, 8, [128, 77, 200, 16, 33, 128, 300, 64], 40, 16, n_requests=4)
+    wl.requests[1].chunk_ids = [5, 1, 3, 0]
+    wl.requests[2].chunk_ids = [7, 6, 2]
+    wl.requests[2].query = wl.requests[2].query[:23]
+    wl.requests[3].chunk_ids = [4, 0, 6, 1, 5, 3, 2, 7]
+    wl.requests[3].query = wl.requests[3].query[:1]
+    store = _store(model, lg=128)
+    _, res = library_run(store, wl, all_logits=True)
+    _, _, out = oracle_run(om, wl, 256, all_logits=True)
+    errs = compare_link(store, res, out, spec)
+    assert all(f"k{i}.1" in errs for i in range(4))
+
+
 # ----------------------------------------------------------------------------- decode after link
 
 def _decode_parity(store, om, wl, steps, seed, nb=256):

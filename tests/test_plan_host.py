@@ -69,20 +69,21 @@ SHAPES = {   # name: (dtype, H, G, D) -> the kernel family that runs it
     "mma_rep8": (torch.bfloat16, 16, 2, 128),
     "simt": (torch.float32, 4, 4, 64),
 }
-ROWS_PER_BLOCK = {"tcgen05": 32, "mma_rep1": 32, "mma_rep8": 16, "simt": 16}
+ROWS_PER_BLOCK = {"tcgen05": 64, "mma_rep1": 32, "mma_rep8": 16, "simt": 16}
 
 
 # ----------------------------------------------------------------------------- invariants
 
 def expected_blocks(seqs, rb):
-    """(row0, nrows, page_begin, page_end) per row block, indices over the concatenated batch."""
+    """(row0, nrows, page_begin, page_end, page_end of the first 32 rows) per row block,
+    indices over the concatenated batch."""
     out, r_off, p_off = [], 0, 0
     for rows, pages in seqs:
         for b0 in range(0, len(rows), rb):
             n = min(rb, len(rows) - b0)
-            last = rows[b0 + n - 1]
-            pe = sum(1 for p in pages if p <= last)
-            out.append((r_off + b0, n, p_off, p_off + pe))
+            pe = sum(1 for p in pages if p <= rows[b0 + n - 1])
+            pe0 = sum(1 for p in pages if p <= rows[b0 + min(n, 32) - 1])
+            out.append((r_off + b0, n, p_off, p_off + pe, p_off + pe0))
         r_off += len(rows)
         p_off += len(pages)
     return out
@@ -90,10 +91,13 @@ def expected_blocks(seqs, rb):
 
 def check_plan(items, combs, n_parts, seqs, G, rb, num_sms, persistent):
     blocks = expected_blocks(seqs, rb)
+    pe0_of = {(row0, nrows): pe0 for row0, nrows, _, _, pe0 in blocks}
     by_key = {}
     for it in items.tolist():
-        row0, nrows, g, p0, p1, part = it
+        row0, nrows, g, p0, p1, part, pmid = it
         assert 0 <= g < G and 1 <= nrows <= rb and p0 <= p1
+        # the first 32 rows see the run's pages up to page_mid, none after it
+        assert pmid == min(p1, max(p0, pe0_of[(row0, nrows)]))
         by_key.setdefault((row0, nrows, g), []).append((p0, p1, part))
     assert len(by_key) == len(blocks) * G, "every (row block, KV head) has items, and nothing else does"
     comb_by_key = {}
@@ -102,7 +106,7 @@ def check_plan(items, combs, n_parts, seqs, G, rb, num_sms, persistent):
         assert (row0, nrows, g) not in comb_by_key
         comb_by_key[(row0, nrows, g)] = (part0, nparts)
     seen_parts = []
-    for row0, nrows, pb, pe in blocks:
+    for row0, nrows, pb, pe, _ in blocks:
         for g in range(G):
             runs = sorted(by_key[(row0, nrows, g)])
             # the runs tile [pb, pe) exactly: each page read once
@@ -164,19 +168,29 @@ def test_plan_invariants_random_batches(lib, kind, seed):
 def model_plan(seqs, G, rb, num_sms, persistent):
     """Independent restatement of the planner's rule (same item fields and order)."""
     blocks = expected_blocks(seqs, rb)
-    total = sum(pe - pb for _, _, pb, pe in blocks)
+    total = sum(pe - pb for _, _, pb, pe, _ in blocks)
 
     def build(P):
         items, parts = [], 0
-        for row0, n, pb, pe in blocks:
+        for row0, n, pb, pe, pe0 in blocks:
             ns = max(1, -(-(pe - pb) // P))
             for g in range(G):
                 if ns == 1:
-                    items.append((row0, n, g, pb, pe, -1))
+                    items.append((row0, n, g, pb, pe, -1, pe0))
                     continue
-                items += [(row0, n, g, pb + s * P, min(pe, pb + (s + 1) * P), parts + s) for s in range(ns)]
+                for s in range(ns):
+                    p0, p1 = pb + s * P, min(pe, pb + (s + 1) * P)
+                    items.append((row0, n, g, p0, p1, parts + s, min(p1, max(p0, pe0))))
                 parts += ns
         return sorted(items, key=lambda it: -(it[4] - it[3]))   # stable: heaviest first
+
+    def cost(it):
+        """Per 64-key tile: 1 + the MMA tiles taking part (rows 0-31 up to page_mid, rows 32-63
+        throughout), plus 4 per item."""
+        nt = (it[4] - it[3] + 3) // 4
+        n0 = max(0, (it[6] - it[3] + 3) // 4)
+        n1 = nt if it[1] > 32 else 0
+        return nt + n0 + n1 + 4
 
     if not persistent:
         target = max(1, (4 * num_sms) // G)
@@ -190,7 +204,7 @@ def model_plan(seqs, G, rb, num_sms, persistent):
             for c in range(m):
                 it = items[k0 + (m - 1 - c if (k0 // n) & 1 else c)]
                 dealt[k0 + c] = it
-                load[c] += (it[4] - it[3] + 3) // 4 + 2
+                load[c] += cost(it)
         return dealt, max(load)
 
     best = None
@@ -237,7 +251,7 @@ def test_plan_rejects_bad_input_and_reports_sizes(lib):
         return lib.pic_op_attention_plan(L.PIC_BF16, 32, 8, 128, 1, P(sr), P(sp), P(r), P(p), num_sms,
                                          None, 0, None, 0, P(counts))
     # output arrays too small: the sizes are reported for a second call
-    assert call(seq_rows, seq_pages, rp, pp) == L.PIC_ERR_CAPACITY and counts.tolist() == [328, 48, 320]
+    assert call(seq_rows, seq_pages, rp, pp) == L.PIC_ERR_CAPACITY and counts.tolist() == [296, 32, 296]
     bad = rp.copy()
     bad[5] = bad[4]                                            # row positions must ascend
     assert call(seq_rows, seq_pages, bad, pp) == L.PIC_ERR_INVALID_ARG
