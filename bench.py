@@ -274,18 +274,19 @@ def kernel_classes(prof, steps):
             for k, v in prof.items() if isinstance(v, dict)}
 
 
-def attention_roofline(prof, n_layers, pk):
+def attention_roofline(prof, n_layers, pk, steps):
     """The fused-RoPE paged attention (kernel + split merge) against its own floor: the slower of
     its FLOPs (4 per head dim and visible query-key pair) at the sustained bf16 tensor peak (it
-    runs inside a long step) and its KV + q + output bytes at the HBM peak."""
+    runs inside a long step) and its KV + q + output bytes at the HBM peak. Per step."""
     a = prof.get("attention")
     if not a or a["ms"] <= 0:
         return None
-    t_flop = a["flops"] / (pk["bf16_tflops_sustained"] * 1e12) * 1e3
-    t_mem = a["bytes"] / (pk["hbm_gbs"] * 1e9) * 1e3
+    ms = a["ms"] / steps
+    t_flop = a["flops"] / steps / (pk["bf16_tflops_sustained"] * 1e12) * 1e3
+    t_mem = a["bytes"] / steps / (pk["hbm_gbs"] * 1e9) * 1e3
     floor = max(t_flop, t_mem)
-    return {"bound": "tensor" if t_flop >= t_mem else "hbm", "ms": a["ms"], "floor_ms": floor,
-            "frac": floor / a["ms"], "us_per_layer": a["ms"] * 1e3 / n_layers,
+    return {"bound": "tensor" if t_flop >= t_mem else "hbm", "ms_per_step": ms, "floor_ms": floor,
+            "frac": floor / ms, "us_per_layer": ms * 1e3 / n_layers,
             "achieved_tflops": a["flops"] / (a["ms"] / 1e3) / 1e12, "achieved_gbs": a["bytes"] / (a["ms"] / 1e3) / 1e9,
             "peak_tflops": pk["bf16_tflops_sustained"], "peak_gbs": pk["hbm_gbs"],
             "peak_kind": "bf16 dense sustained / HBM copy, measured"}
@@ -329,7 +330,7 @@ def measure_config(model, name, pk, steps, warmup):
             "tokens_per_s": wl.linked_tokens / (ms / 1e3),
             "link_roofline": {"bound": rl["bound"], "roofline_ms": rl["roofline_ms"], "frac": rl["roofline_ms"] / ms,
                               "t_mem_ms": rl["t_mem_ms"], "t_flop_ms": rl["t_flop_ms"]},
-            "attention_roofline": attention_roofline(prof, wl.spec.n_layers, pk),
+            "attention_roofline": attention_roofline(prof, wl.spec.n_layers, pk, steps),
             "kernels": kernel_classes(prof, steps)}
 
 
@@ -457,7 +458,7 @@ def run_ours(args):
                      "frac": (achieved / pk["hbm_gbs"]) if achieved else None, "traffic": traffic,
                      "algorithmic_bytes_per_launch": g_bytes / g_n if g_n else None,
                      "launches_per_step": g_n / args.steps, "peak_source": pk["source"]},
-        "attention_roofline": attention_roofline(prof, spec.n_layers, pk),
+        "attention_roofline": attention_roofline(prof, spec.n_layers, pk, args.steps),
         "link_roofline": {"roofline_ms": rl["roofline_ms"], "bound": rl["bound"], "measured_ms": ms_step,
                           "frac": rl["roofline_ms"] / ms_step, "bytes": rl["bytes"], "flops": rl["flops"],
                           "t_mem_ms": rl["t_mem_ms"], "t_flop_ms": rl["t_flop_ms"]},

@@ -149,7 +149,8 @@ struct pic_store {
   int32_t* meta_d = nullptr;
   size_t meta_cap = 0;  // int32 elements
   float2* rope_cs = nullptr;
-  std::vector<CUtensorMap> kv_maps;  // per layer: K map, V map (tensor-core attention), built on first use
+  std::vector<CUtensorMap> kv_maps;  // per layer: K, V (4-block boxes), K, V (1-page boxes); built on first use
+  CUtensorMap cs_map;                // rows of the cos/sin table (with kv_maps)
   int32_t* meta_h = nullptr;  // pinned staging
   cudaEvent_t meta_ev = nullptr;
   bool meta_ev_pending = false;
@@ -382,18 +383,20 @@ pic_status run_forward_impl(pic_store* s, const Batch& b, float* hidden_out, flo
   const bool att_tc = attention_persistent(dt, D, H / G);
   if (att_tc) {
     if (s->kv_maps.empty()) {
-      s->kv_maps.resize(2 * (size_t)c.n_layers);
+      s->kv_maps.resize(4 * (size_t)c.n_layers);
       for (int l = 0; l < c.n_layers; ++l)
-        if (!attn_kv_map(&s->kv_maps[2 * l], s->k_layer(l), s->blocks_total(), G) ||
-            !attn_kv_map(&s->kv_maps[2 * l + 1], s->v_layer(l), s->blocks_total(), G)) {
+        if (!attn_kv_map(&s->kv_maps[4 * l], &s->kv_maps[4 * l + 2], s->k_layer(l), s->blocks_total(), G) ||
+            !attn_kv_map(&s->kv_maps[4 * l + 1], &s->kv_maps[4 * l + 3], s->v_layer(l), s->blocks_total(), G)) {
           s->kv_maps.clear();
           return fail(PIC_ERR_CUDA, "cuTensorMapEncodeTiled failed for the KV pools");
         }
+      if (!attn_cs_map(&s->cs_map, s->rope_cs, std::max(16, s->cfg.max_positions))) {
+        s->kv_maps.clear();
+        return fail(PIC_ERR_CUDA, "cuTensorMapEncodeTiled failed for the cos/sin table");
+      }
     }
-    // q is read in boxes of 32 rows: a batch of fewer rows (decode) still maps 32 (the q
-    // workspace holds them); rows past a work item's own are fully masked and never stored
-    if (!attn_q_map(&aa.qmap, s->q, std::max(T, 32), H))
-      return fail(PIC_ERR_CUDA, "cuTensorMapEncodeTiled failed for q");
+    aa.csmap = s->cs_map;
+    aa.q16 = (const __half*)s->q;   // written rotated and scaled by the QKV epilogue
   }
   aa.dtype = dt;
   aa.rb = pin.rows_per_block;
@@ -458,8 +461,10 @@ pic_status run_forward_impl(pic_store* s, const Batch& b, float* hidden_out, flo
     aa.k_layer = s->k_layer(l);
     aa.v_layer = s->v_layer(l);
     if (att_tc) {
-      aa.kmap = s->kv_maps[2 * l];
-      aa.vmap = s->kv_maps[2 * l + 1];
+      aa.kmap = s->kv_maps[4 * l];
+      aa.vmap = s->kv_maps[4 * l + 1];
+      aa.kmap1 = s->kv_maps[4 * l + 2];
+      aa.vmap1 = s->kv_maps[4 * l + 3];
     }
     {
       Rec r(s, st, PIC_PROF_ATTENTION, att_bytes, att_flops, att_launches);

@@ -10,29 +10,36 @@
 // key tiles holding pages [page0, page_mid) and the item's later key tiles run for tile 1
 // alone.
 //
-//   warp 17     loads: one TMA box per page for its pre-RoPE K and one for its V (16 rows x both
-//               64-dim halves, 4 KB, 128-byte swizzled; two key tiles in flight), the cos/sin
-//               table rows of the page starts (plain loads by the warp's lanes) and, per item,
-//               the Q tiles (rotated and scaled fp16 rows written by the QKV epilogue).
-//   warps 8-15  transform: K rotated by RoPE at each key's absolute position (MEPIC abstract:
-//               K is kept without positional encoding and RoPE is fused into attention) into
-//               the fp16 K-major operand; V converted to fp16 into the MN-major operand of
-//               O += P V ([key][dim], three key tiles held until their PV). cos/sin(p theta) is
-//               composed from the table row of the page start and that of the offset inside
-//               the page (the latter held in registers: each thread always rotates the same
-//               row offset and dims).
-//   warp 16     TMEM owner (all 512 columns: O of tile t at [128t, 128t + 128), two S buffers
-//               of tile t at 256 + 128t + {0, 64}); one thread issues S_t = Q_t K^T (M128 N64
-//               K128) and O_t += P_t V (M128 N128 K64, P_t read from TMEM) with tcgen05.mma
-//               kind::f16.
-//   warps 0-7   softmax: warpgroup t serves MMA tile t, thread = one MMA row = one TMEM lane.
-//               Reads its row of S, masks keys after its position (only on key tiles that need
-//               it), keeps a running reference maximum and writes P = 2^(S - ref) as fp16
-//               pairs over the same S buffer in TMEM, the A operand of the PV product. O in
-//               TMEM is rescaled only when the maximum grows by more than 2^8 (P stays <= 256,
-//               safe in fp16); the sum uses the same reference, so O / l is exact softmax. At
-//               the end of an item it drains O_t (normalized output, or the unnormalized
-//               partial with its reference maximum and sum for the merge).
+// Key tiles stream through a ring of 4 shared-memory stages. A stage holds K and V of 64 keys
+// exactly in the layout the MMAs read ([64-dim half][key][128 B], 128-byte swizzled): the load
+// warp fills each half with one TMA box over 4 consecutive pool blocks (pages of a chunk or a
+// query are allocated consecutively), or one box per page when they are not, plus the cos/sin
+// table rows of the page starts. The transform then rotates K and converts V to fp16 in place,
+// and the stage is free again once the PV products of its key tile have retired.
+//
+//   warp 17     loads: K and V boxes and the cos/sin rows of each key tile (TMA), the page
+//               metadata (the warp's lanes hold a window of 32 pages, the next one prefetched).
+//   warps 8-15  transform, in place: K rotated by RoPE at each key's absolute position (MEPIC
+//               abstract: K is kept without positional encoding and RoPE is fused into
+//               attention) into fp16, V converted to fp16; rows without a key zeroed.
+//               cos/sin(p theta) is composed from the table row of the page start and that of
+//               the offset inside the page (the latter held in registers: each thread always
+//               rotates the same row offset and dims).
+//   warp 16     TMEM owner (all 512 columns: O_t at [128t, 128t + 128), two S buffers of tile t
+//               at 256 + 128t + {0, 64}); one thread issues the S products S_t = Q_t K^T (M128
+//               N64 K128) of both MMA tiles, each as soon as its key tile is transformed and its
+//               S buffer free -- a key tile ahead of the softmax.
+//   warps 0-7   MMA tile t = warpgroup t, thread = one MMA row = one TMEM lane. The warpgroup
+//               writes the tile's Q rows into shared memory at the start of an item (the A
+//               operand of its S products); per key tile each thread reads its row of S, masks
+//               keys after its position (only on key tiles that need it), keeps a running
+//               reference maximum and writes P = 2^(S - ref) as fp16 pairs over the S columns,
+//               and the warpgroup's first thread then issues O_t += P_t V (M128 N128 K64, P_t
+//               from TMEM) at once. O in TMEM is rescaled only when the maximum grows by more
+//               than 2^8 (P stays <= 256, safe in fp16); the sum uses the same reference, so
+//               O / l is exact softmax. At the end of an item the warpgroup drains O_t
+//               (normalized output, or the unnormalized partial with its reference maximum and
+//               sum for the merge).
 // Barrier phases run over the CTA's whole key-tile sequence (and per MMA tile over that tile's
 // own sequence), so the next item's loads overlap the current item's tail. Every wait is
 // bounded; on expiry the CTA raises the device timeout flag, stops issuing work, waits
@@ -56,10 +63,7 @@ constexpr int REP = 4;
 constexpr int RB = 32;                    // query rows per MMA tile
 constexpr int MT = 2;                     // MMA tiles per item (items of up to 64 rows)
 constexpr int KT = 64;                    // keys per tile (4 pages)
-constexpr int NRS = 2;                    // raw K/V tiles in flight (freed once transformed); also
-                                          // indexes the page metadata and cos/sin rows of a tile
-constexpr int NVS = 3;                    // fp16 V operand tiles (freed once their PVs retired);
-                                          // also indexes the key positions of a tile
+constexpr int NST = 4;                    // key-tile stages
 constexpr int kSoftmaxWarps = 4 * MT;
 constexpr int kTransformWarps = 8;
 constexpr int W_XF = kSoftmaxWarps;                 // first transform warp
@@ -68,47 +72,39 @@ constexpr int kThreads = (W_LOAD + 1) * 32;
 constexpr float kRescale = 8.f;           // rescale O when the row max grows by more than 2^8
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t TM_O = 0, TM_S = 256;  // TMEM columns of O_t (+ 128t) and S buffer b of tile t (+ 128t + 64b)
 
 // shared memory map (bytes from a 1024-aligned base)
 constexpr int Q_TILE = 32768;                     // one MMA tile of Q: 2 halves x [128 rows][128 B] fp16
+constexpr int ST_BYTES = 32768;                   // one key tile: K then V, each [2 halves][64 keys][128 B]
 constexpr int OFF_Q = 0;                          // [MT] Q tiles                              64 KB
-constexpr int OFF_KOP = OFF_Q + MT * Q_TILE;      // [2][2 halves][64 keys][128 B] fp16        32 KB
-// raw pages as TMA writes them: [page][16 rows][2 halves][128 B], the 128-byte rows swizzled
-constexpr int OFF_KRAW = OFF_KOP + 32768;         // [2][4 pages][4 KB] bf16                   32 KB
-constexpr int OFF_VRAW = OFF_KRAW + NRS * 16384;  // [2][4 pages][4 KB] bf16                   32 KB
-constexpr int OFF_V = OFF_VRAW + NRS * 16384;     // [3][2 halves][64 keys][128 B] fp16        48 KB
-constexpr int OFF_CS = OFF_V + NVS * 16384;       // [2][4 pages][512 B] cos/sin rows           4 KB
-constexpr int OFF_TM = OFF_CS + NRS * 2048;       // int [2][4][2] page start, valid rows
-constexpr int OFF_POS = OFF_TM + 128;             // int [3][KT] key positions (INT_MAX = none)
-constexpr int OFF_TILE = OFF_POS + NVS * KT * 4;  // int [3] last key position, INT_MAX if ragged
-constexpr int OFF_BAR = OFF_TILE + 16;
+constexpr int OFF_ST = OFF_Q + MT * Q_TILE;       // [NST] key-tile stages                    128 KB
+constexpr int OFF_CS = OFF_ST + NST * ST_BYTES;   // [NST][4 pages][512 B] cos/sin rows         8 KB
+constexpr int OFF_TM = OFF_CS + NST * 2048;       // int [NST][4][2] page start, valid rows
+constexpr int OFF_POS = OFF_TM + NST * 32;        // int [NST][KT] key positions (INT_MAX = none)
+constexpr int OFF_TILE = OFF_POS + NST * KT * 4;  // int [NST] last key position, INT_MAX if ragged
+constexpr int OFF_BAR = (OFF_TILE + NST * 4 + 7) / 8 * 8;
 constexpr int N_BARS = 32;
 constexpr int SMEM_BYTES = OFF_BAR + N_BARS * 8 + 16;
-static_assert(OFF_BAR % 8 == 0, "mbarrier alignment");
 static_assert(SMEM_BYTES + 1024 <= 227 * 1024, "shared memory budget");
 
 // barrier slots ([t][b]: MMA tile t, S buffer b)
-constexpr int B_KVFULL = 0;                       // [2]   K operand buffer ready (transform)
-constexpr int B_SFULL = 2;                        // [2][2] S_t in buffer b computed (MMA commit)
-constexpr int B_PFULL = 6;                        // [2][2] P_t in buffer b written (softmax t)
-constexpr int B_PVDONE = 10;                      // [2][2] O_t += P_t V of buffer b retired (commit)
-constexpr int B_RAWFULL = 14;                     // [2]   raw K/V tile landed (TMA)
-constexpr int B_RAWFREE = 16;                     // [2]   raw K/V tile consumed (transform)
-constexpr int B_VFREE = 18;                       // [3]   V operand slot's PVs retired (commit)
-constexpr int B_POSFULL = 21;                     // [3]   key positions of a V slot (transform)
-constexpr int B_QFULL = 24, B_QFREE = 25;         // item's Q tiles landed / every S of the item done
-constexpr int B_OFREE = 26;                       // [2]   O_t drained (softmax t)
-constexpr int B_MMADONE = 28;
-constexpr int B_KFREE = 29;                       // [2]   every S of the K operand buffer's tile done (commit)
-static_assert(B_KFREE + 2 <= N_BARS, "barrier slots");
+constexpr int B_FULL = 0;                         // [NST] stage landed (TMA bytes + loader arrival)
+constexpr int B_XF = B_FULL + NST;                // [NST] stage transformed (transform warps)
+constexpr int B_EMPTY = B_XF + NST;               // [NST] both MMA tiles' PVs of the stage's key tile retired
+constexpr int B_SFULL = B_EMPTY + NST;            // [2][2] S_t in buffer b computed (commit)
+constexpr int B_PVDONE = B_SFULL + 2 * MT;        // [2][2] O_t += P_t V of buffer b retired (commit)
+constexpr int B_QREADY = B_PVDONE + 2 * MT;       // [2] Q_t of the item written (warpgroup t)
+constexpr int B_DONE = B_QREADY + MT;             // [3] every MMA of an issuing thread retired
+static_assert(B_DONE + MT + 1 <= N_BARS, "barrier slots");
 // Every waiter must observe each phase of a barrier before the barrier can complete the next
-// one (a parity wait cannot tell phase n from n + 2). KVFULL therefore has only the MMA as a
-// waiter, and KFREE only the transform (the MMA cannot commit buffer b's next S before the
-// transform re-armed KVFULL); the
-// softmax takes the key positions from POSFULL, per V slot, which the transform re-arms only
-// after every PV of the slot's key tile, i.e. after both softmax warpgroups consumed it. The
-// S/P/PV barriers of MMA tile t count that tile's own key tiles, so a warpgroup that skips
-// key tiles (tile 0 past page_mid) never waits on phases it did not take part in.
+// one (a parity wait cannot tell phase n from n + 2). FULL has only the transform as waiter;
+// XF is waited on by the S issuer and both warpgroups, but a stage can only be refilled after
+// both warpgroups released it, i.e. after each has used that phase (a warpgroup releases a key
+// tile it takes no part in only after waiting for it, so its release never counts toward the
+// stage's previous use); EMPTY has only the loader. The S/PV/Q barriers of MMA tile t count
+// that tile's own key tiles and items: S_t into buffer b is issued only after the PV that read
+// buffer b's previous P retired, and the next item's first S_t only after Q_t was rewritten.
 
 __device__ int g_attn_timeout = 0;
 
@@ -127,9 +123,14 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
 __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
-// expected transaction bytes without an arrival (the arrival follows separately)
-__device__ __forceinline__ void mbar_add_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
 }
 __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
   uint32_t ok;
@@ -151,11 +152,19 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
     }
   }
 }
-__device__ __forceinline__ void tma_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z, uint32_t bar) {
+__device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
   asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
-      "[%5];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tma_5d(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2, int c3, int c4,
+                                       uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5, "
+      "%6}], [%7];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(bar)
       : "memory");
 }
 // 16-byte chunk c (0..7) of row r of a [rows][128 B] tile, 128-byte swizzle (the TMA and UMMA layout)
@@ -265,7 +274,7 @@ __device__ __forceinline__ int item_tiles_of(const AttnItem& it, int t) {
 __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_constant__ AttnArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  int* sTm = reinterpret_cast<int*>(sm + OFF_TM);   // [slot][page][start, valid rows]
+  int* sTm = reinterpret_cast<int*>(sm + OFF_TM);   // [stage][page][start, valid rows]
   int* sPos = reinterpret_cast<int*>(sm + OFF_POS);
   int* sTile = reinterpret_cast<int*>(sm + OFF_TILE);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
@@ -277,27 +286,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
 
   if (tid == 0) {
     s_abort = 0;
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(bar(B_KVFULL + i), kTransformWarps);
-      mbar_init(bar(B_KFREE + i), 1);
+    for (int i = 0; i < NST; ++i) {
+      mbar_init(bar(B_FULL + i), 1);
+      mbar_init(bar(B_XF + i), kTransformWarps);
+      mbar_init(bar(B_EMPTY + i), MT);   // one release per MMA tile
     }
     for (int i = 0; i < 2 * MT; ++i) {
       mbar_init(bar(B_SFULL + i), 1);
-      mbar_init(bar(B_PFULL + i), 4);
       mbar_init(bar(B_PVDONE + i), 1);
     }
-    for (int i = 0; i < NRS; ++i) {
-      mbar_init(bar(B_RAWFULL + i), 1);
-      mbar_init(bar(B_RAWFREE + i), kTransformWarps);
-    }
-    for (int i = 0; i < NVS; ++i) {
-      mbar_init(bar(B_VFREE + i), 1);
-      mbar_init(bar(B_POSFULL + i), kTransformWarps);
-    }
-    mbar_init(bar(B_QFULL), 1);
-    mbar_init(bar(B_QFREE), 1);
-    for (int t = 0; t < MT; ++t) mbar_init(bar(B_OFREE + t), 4);
-    mbar_init(bar(B_MMADONE), 1);
+    for (int t = 0; t < MT; ++t) mbar_init(bar(B_QREADY + t), 1);
+    for (int i = 0; i <= MT; ++i) mbar_init(bar(B_DONE + i), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == W_MMA) {
@@ -312,161 +311,278 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
   const uint32_t tmem = *tmem_slot;
 
   if (warp < kSoftmaxWarps) {
-    // =============================== softmax warps: warpgroup t, head hh, row r of MMA tile t
+    // =============================== MMA tile t: softmax warps (head hh, row r); the warpgroup's
+    // first thread issues the tile's PV products
     const int t = warp >> 2, hh = warp & 3, r = lane;   // MMA row hh * 32 + r = TMEM lane
+    const bool issuer = hh == 0 && lane == 0;
     const uint32_t trow = tmem + ((uint32_t)(hh * 32) << 16);   // this warp's TMEM lane quarter
-    const uint32_t t_o = trow + 128 * t, t_s = trow + 256 + 128 * t;
+    const uint32_t t_o = trow + TM_O + 128 * t, t_sb = trow + TM_S + 128 * t;
+    const uint32_t id_pv = idesc_f16(128, D, true);
+    uint8_t* qs = sm + OFF_Q + t * Q_TILE;
+    // every thread of the warpgroup takes part, so all of them take the same branch after it
+    auto wg_all = [&](bool v) -> bool {
+      uint32_t res;
+      asm volatile(
+          "{\n .reg .pred p, q;\n setp.ne.u32 q, %1, 0;\n bar.red.and.pred p, %2, 128, q;\n selp.u32 %0, 1, 0, p;\n}\n"
+          : "=r"(res)
+          : "r"((uint32_t)v), "r"(1 + t)
+          : "memory");
+      return res != 0;
+    };
     uint32_t gt = 0, ct = 0;   // key tiles of the CTA; key tiles of this MMA tile
     bool ok = true;
-    for (int ii = blockIdx.x; ii < a.n_items && ok; ii += gridDim.x) {
+    for (int ii = blockIdx.x; ii < a.n_items; ii += gridDim.x) {
       const AttnItem it = a.items[ii];
       const int nt = item_tiles(it), na = item_tiles_of(it, t);
       const int row = RB * t + r;
-      if (RB * t >= it.nrows) {   // no rows of this MMA tile in the item (then na == 0)
-        gt += nt;
-        continue;
-      }
-      const int qp = row < it.nrows ? a.q_pos[it.row0 + row] : -1;
-      float mref = -INFINITY, l = 0.f;
-      for (int j = 0; j < na; ++j, ++ct) {
-        const uint32_t g = gt + j;
-        const int b = ct & 1, sl = g % NVS;
-        // S of the key tile, and the transform's key positions of it
-        ok = __all_sync(0xffffffffu, !s_abort && mbar_wait(bar(B_SFULL + 2 * t + b), (ct >> 1) & 1) &&
-                                         mbar_wait(bar(B_POSFULL + sl), (g / NVS) & 1));
-        if (!ok) break;
-        fence_after();
-        // Two halves of 32 keys keep the register footprint low: the low half is read for the
-        // maximum and again for P; P (64 fp16 = 32 columns) goes over the high half's columns,
-        // high keys first (their S is in registers by then), then the low keys.
-        const uint32_t sb = t_s + 64 * b;
-        const bool need_mask = __any_sync(0xffffffffu, sTile[sl] > qp);
-        const int* kpos = sPos + sl * KT;
-        auto load_half = [&](int h, float* v) {   // S of keys 32h..32h+31, masked by position
-          tmem_ld16(sb + 32 * h, v);
-          tmem_ld16(sb + 32 * h + 16, v + 16);
-          tmem_wait_ld();
-          if (need_mask) {
-            const int4* kp = reinterpret_cast<const int4*>(kpos + 32 * h);
+      const bool mine = row < it.nrows;
+      const int qp = mine ? a.q_pos[it.row0 + row] : -1;
+      if (na > 0) {
+        // this row's q (128 fp16, rotated and scaled) into the K-major, 128-byte-swizzled A
+        // operand of the S products: MMA row m = hh * 32 + r, dims 8c..8c+7 of half h at
+        // [h][m][chunk c]. Every S product of this tile's previous item has retired (this
+        // warpgroup consumed them), and the next is issued only after QREADY.
+        const uint4* src =
+            reinterpret_cast<const uint4*>(a.q16 + ((size_t)(it.row0 + (mine ? row : 0)) * a.H + it.g * REP + hh) * D);
+        const int m = hh * RB + r;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const int4 k4 = kp[i];
-              if (k4.x > qp) v[4 * i] = -INFINITY;
-              if (k4.y > qp) v[4 * i + 1] = -INFINITY;
-              if (k4.z > qp) v[4 * i + 2] = -INFINITY;
-              if (k4.w > qp) v[4 * i + 3] = -INFINITY;
+        for (int c = 0; c < 16; ++c) {
+          const uint4 x = mine ? src[c] : make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4*>(qs + (c >> 3) * 16384 + sw128(m, c & 7)) = x;
+        }
+        fence_async_smem();
+      }
+      ok = wg_all(ok && !s_abort);
+      if (!ok) break;
+      if (na > 0 && issuer) mbar_arrive(bar(B_QREADY + t));
+      float mref = -INFINITY, l = 0.f;
+      for (int j = 0; j < nt; ++j) {
+        const uint32_t g = gt + j;
+        const int sl = g % NST;
+        if (j >= na) {
+          // this MMA tile takes no part in the key tile: release its share of the stage once the
+          // stage holds the tile (the release must not count toward the stage's previous use)
+          if (issuer) {
+            if (!s_abort && mbar_wait(bar(B_XF + sl), (g / NST) & 1))
+              umma_commit(bar(B_EMPTY + sl));
+            else
+              s_abort = 1;
+          }
+          continue;
+        }
+        const int b = ct & 1;
+        const uint32_t t_s = t_sb + 64 * b;
+        bool okw = !s_abort && mbar_wait(bar(B_SFULL + 2 * t + b), (ct >> 1) & 1) &&
+                   mbar_wait(bar(B_XF + sl), (g / NST) & 1);
+        okw = __all_sync(0xffffffffu, okw);
+        if (okw) {
+          fence_after();
+          // Two halves of 32 keys keep the register footprint low: the low half is read for the
+          // maximum and again for P; P (64 fp16 = 32 columns) goes over the high half's columns,
+          // high keys first (their S is in registers by then), then the low keys.
+          const bool need_mask = __any_sync(0xffffffffu, sTile[sl] > qp);
+          const int* kpos = sPos + sl * KT;
+          auto load_half = [&](int h, float* v) {   // S of keys 32h..32h+31, masked by position
+            tmem_ld16(t_s + 32 * h, v);
+            tmem_ld16(t_s + 32 * h + 16, v + 16);
+            tmem_wait_ld();
+            if (need_mask) {
+              const int4* kp = reinterpret_cast<const int4*>(kpos + 32 * h);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                const int4 k4 = kp[i];
+                if (k4.x > qp) v[4 * i] = -INFINITY;
+                if (k4.y > qp) v[4 * i + 1] = -INFINITY;
+                if (k4.z > qp) v[4 * i + 2] = -INFINITY;
+                if (k4.w > qp) v[4 * i + 3] = -INFINITY;
+              }
+            }
+          };
+          float s[32];
+          load_half(0, s);
+          float mx = s[0];
+#pragma unroll
+          for (int i = 1; i < 32; ++i) mx = fmaxf(mx, s[i]);
+          load_half(1, s);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) mx = fmaxf(mx, s[i]);
+          // new reference when the maximum grows by more than 2^8 (or for the first keys seen)
+          const bool grow = mx > mref + kRescale;
+          const float mnew = grow ? mx : mref;
+          const float scale = (grow && mref != -INFINITY) ? ex2(mref - mnew) : 1.f;
+          l *= scale;
+          mref = mnew;
+          // P = 2^(S - ref) as fp16 pairs: keys 2c, 2c + 1 in column 32 + c of the S buffer
+          const float mz = mref == -INFINITY ? 0.f : mref;   // fully masked so far: every s is -inf, p = 0
+          float rs = 0.f;
+          auto store_p = [&](int h) {
+            uint32_t pv[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const float p0 = ex2(s[2 * e] - mz), p1 = ex2(s[2 * e + 1] - mz);
+              rs += p0 + p1;
+              pv[e] = pack_f16x2(p0, p1);
+            }
+            tmem_st16(t_s + 32 + 16 * h, pv);
+          };
+          store_p(1);
+          load_half(0, s);
+          store_p(0);
+          l += rs;
+          if (__any_sync(0xffffffffu, scale != 1.f)) {
+            // O holds the sums of this item's earlier key tiles: rescale it before this P is
+            // added, once the PV of the previous key tile has retired (a rescale needs a finite
+            // earlier maximum, so j > 0)
+            if (__all_sync(0xffffffffu, mbar_wait(bar(B_PVDONE + 2 * t + ((ct - 1) & 1)), ((ct - 1) >> 1) & 1))) {
+              fence_after();
+#pragma unroll 1
+              for (int c = 0; c < 128; c += 16) {
+                float o[16];
+                tmem_ld16(t_o + c, o);
+                tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 16; ++e) o[e] *= scale;
+                tmem_st16f(t_o + c, o);
+              }
+            } else {
+              okw = false;
             }
           }
-        };
-        float s[32];
-        load_half(0, s);
-        float mx = s[0];
-#pragma unroll
-        for (int i = 1; i < 32; ++i) mx = fmaxf(mx, s[i]);
-        load_half(1, s);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) mx = fmaxf(mx, s[i]);
-        // new reference when the maximum grows by more than 2^8 (or for the first keys seen)
-        const bool grow = mx > mref + kRescale;
-        const float mnew = grow ? mx : mref;
-        const float scale = (grow && mref != -INFINITY) ? ex2(mref - mnew) : 1.f;
-        l *= scale;
-        mref = mnew;
-        // P = 2^(S - ref) as fp16 pairs: keys 2c, 2c + 1 in column 32 + c of the S buffer
-        const float mz = mref == -INFINITY ? 0.f : mref;   // fully masked so far: every s is -inf, p = 0
-        float rs = 0.f;
-        auto store_p = [&](int h) {
-          uint32_t pv[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const float p0 = ex2(s[2 * e] - mz), p1 = ex2(s[2 * e + 1] - mz);
-            rs += p0 + p1;
-            pv[e] = pack_f16x2(p0, p1);
-          }
-          tmem_st16(sb + 32 + 16 * h, pv);
-        };
-        store_p(1);
-        load_half(0, s);
-        store_p(0);
-        if (__any_sync(0xffffffffu, scale != 1.f)) {
-          // O holds the sums of this item's earlier key tiles: rescale it before this P is added,
-          // once the PV of the previous key tile has retired (a rescale needs a finite earlier
-          // maximum, so j > 0)
-          const uint32_t pc = ct - 1;
-          if (!mbar_wait(bar(B_PVDONE + 2 * t + (pc & 1)), (pc >> 1) & 1)) ok = false;
-          if (!__all_sync(0xffffffffu, ok)) {
-            ok = false;
-            break;
-          }
-          fence_after();
-#pragma unroll 1
-          for (int c = 0; c < 128; c += 16) {
-            float o[16];
-            tmem_ld16(t_o + c, o);
-            tmem_wait_ld();
-#pragma unroll
-            for (int e = 0; e < 16; ++e) o[e] *= scale;
-            tmem_st16f(t_o + c, o);
-          }
+          tmem_wait_st();
+          fence_before();
         }
-        l += rs;
-        tmem_wait_st();
-        fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(B_PFULL + 2 * t + b));
+        ok = wg_all(okw);   // P_t (and the rescaled O_t) of the whole tile written
+        if (!ok) break;
+        // ---- O_t += P_t V at once; the stage's share is released when it retires
+        if (issuer) {
+          fence_after();
+          const uint32_t vb = smem_u32(sm + OFF_ST + sl * ST_BYTES + 16384);
+          const uint32_t pa = tmem + TM_S + 128 * t + 64 * b + 32;   // P over the S buffer's high half
+#pragma unroll
+          for (int k = 0; k < 4; ++k)   // K dimension 64 keys = 4 steps of 16 (8 TMEM columns of P each)
+            umma_ts(tmem + TM_O + 128 * t, pa + 8 * k, desc_mnmajor(vb + k * 2048, 8192), id_pv, (j | k) != 0);
+          umma_commit(bar(B_PVDONE + 2 * t + b));
+          umma_commit(bar(B_EMPTY + sl));
+        }
+        ++ct;
       }
       if (!ok) break;
       // ---- drain O_t: normalized output, or the unnormalized partial with its reference max and sum
+      bool okd = true;
       if (na > 0) {
-        const uint32_t pc = ct - 1;
-        ok = __all_sync(0xffffffffu, mbar_wait(bar(B_PVDONE + 2 * t + (pc & 1)), (pc >> 1) & 1));
-        if (!ok) break;
+        okd = __all_sync(0xffffffffu, mbar_wait(bar(B_PVDONE + 2 * t + ((ct - 1) & 1)), ((ct - 1) >> 1) & 1));
         fence_after();
       }
-      const int h = it.g * REP + hh;
-      const float inv = l > 0.f ? 1.f / l : 0.f;
+      if (okd && RB * t < it.nrows) {
+        const int h = it.g * REP + hh;
+        const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll 1
-      for (int c0 = 0; c0 < 128; c0 += 64) {   // 64 columns per TMEM round trip
-        float o[64];
-        if (na > 0) {
+        for (int c0 = 0; c0 < 128; c0 += 64) {   // 64 columns per TMEM round trip
+          float o[64];
+          if (na > 0) {
 #pragma unroll
-          for (int c = 0; c < 4; ++c) tmem_ld16(t_o + c0 + 16 * c, o + 16 * c);
-          tmem_wait_ld();
-        } else {
+            for (int c = 0; c < 4; ++c) tmem_ld16(t_o + c0 + 16 * c, o + 16 * c);
+            tmem_wait_ld();
+          } else {
 #pragma unroll
-          for (int e = 0; e < 64; ++e) o[e] = 0.f;
-        }
-        if (it.part < 0) {
-          if (row < it.nrows) {
-            uint4* dst = reinterpret_cast<uint4*>((__half*)a.out + ((size_t)(it.row0 + row) * a.H + h) * D + c0);
-#pragma unroll
-            for (int c = 0; c < 8; ++c)
-              dst[c] = make_uint4(pack_f16x2(o[8 * c] * inv, o[8 * c + 1] * inv),
-                                  pack_f16x2(o[8 * c + 2] * inv, o[8 * c + 3] * inv),
-                                  pack_f16x2(o[8 * c + 4] * inv, o[8 * c + 5] * inv),
-                                  pack_f16x2(o[8 * c + 6] * inv, o[8 * c + 7] * inv));
+            for (int e = 0; e < 64; ++e) o[e] = 0.f;
           }
-        } else if (row < it.nrows) {
-          float4* dst =
-              reinterpret_cast<float4*>(a.part_o + (((size_t)it.part * kAttnPartRows + row) * REP + hh) * D + c0);
+          if (it.part < 0) {
+            if (mine) {
+              uint4* dst = reinterpret_cast<uint4*>((__half*)a.out + ((size_t)(it.row0 + row) * a.H + h) * D + c0);
 #pragma unroll
-          for (int e = 0; e < 16; ++e) dst[e] = make_float4(o[4 * e], o[4 * e + 1], o[4 * e + 2], o[4 * e + 3]);
+              for (int c = 0; c < 8; ++c)
+                dst[c] = make_uint4(pack_f16x2(o[8 * c] * inv, o[8 * c + 1] * inv),
+                                    pack_f16x2(o[8 * c + 2] * inv, o[8 * c + 3] * inv),
+                                    pack_f16x2(o[8 * c + 4] * inv, o[8 * c + 5] * inv),
+                                    pack_f16x2(o[8 * c + 6] * inv, o[8 * c + 7] * inv));
+            }
+          } else if (mine) {
+            float4* dst =
+                reinterpret_cast<float4*>(a.part_o + (((size_t)it.part * kAttnPartRows + row) * REP + hh) * D + c0);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) dst[e] = make_float4(o[4 * e], o[4 * e + 1], o[4 * e + 2], o[4 * e + 3]);
+          }
         }
+        if (it.part >= 0 && mine) {
+          const size_t pi = ((size_t)it.part * kAttnPartRows + row) * REP + hh;
+          *reinterpret_cast<float2*>(a.part_ml + pi * 2) = make_float2(mref, l);
+        }
+        fence_before();   // the next item's first PV overwrites O_t after the barrier at its start
       }
-      if (na > 0) {
-        fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(B_OFREE + t));
-      }
-      if (it.part >= 0 && row < it.nrows) {
-        const size_t pi = ((size_t)it.part * kAttnPartRows + row) * REP + hh;
-        *reinterpret_cast<float2*>(a.part_ml + pi * 2) = make_float2(mref, l);
-      }
+      if (!okd) s_abort = 1;
       gt += nt;
     }
     if (!ok) s_abort = 1;
+    // every MMA this thread issued has retired before the TMEM is given up
+    if (issuer) {
+      umma_commit(bar(B_DONE + t));
+      mbar_wait(bar(B_DONE + t), 0);
+    }
+  } else if (warp == W_MMA) {
+    // =============================== S products of both MMA tiles, each as soon as its key tile
+    // is transformed, its S buffer free (the PV that read it retired) and, for an item's first,
+    // its Q tile written
+    if (lane == 0) {
+      const uint32_t id_s = idesc_f16(128, KT, false);
+      uint32_t gt = 0;
+      uint32_t ct[MT] = {0, 0}, ci[MT] = {0, 0};   // per MMA tile: key tiles and items taken part in
+      bool ok = true;
+      for (int ii = blockIdx.x; ii < a.n_items && ok; ii += gridDim.x) {
+        const AttnItem it = a.items[ii];
+        const int nt = item_tiles(it);
+        const int na[MT] = {item_tiles_of(it, 0), item_tiles_of(it, 1)};
+        int js[MT] = {0, 0};
+        uint32_t idle = 0;
+        unsigned long long t_idle = 0;
+        while (js[0] < na[0] || js[1] < na[1]) {
+          bool prog = false;
+#pragma unroll
+          for (int t = 0; t < MT; ++t) {
+            if (js[t] >= na[t]) continue;
+            const uint32_t g = gt + js[t], c = ct[t] + js[t];
+            const int b = c & 1, st = g % NST;
+            if (mbar_test(bar(B_XF + st), (g / NST) & 1) &&
+                (js[t] > 0 || mbar_test(bar(B_QREADY + t), ci[t] & 1)) &&
+                (c < 2 || mbar_test(bar(B_PVDONE + 2 * t + b), ((c - 2) >> 1) & 1))) {
+              fence_after();
+              const uint32_t qa = smem_u32(sm + OFF_Q + t * Q_TILE), kb = smem_u32(sm + OFF_ST + st * ST_BYTES);
+#pragma unroll
+              for (int k = 0; k < 8; ++k) {   // K dimension 128 = 2 halves x 4 steps of 16
+                const uint32_t off = (k & 3) * 32;
+                umma_ss(tmem + TM_S + 128 * t + 64 * b, desc_kmajor(qa + (k >> 2) * 16384 + off),
+                        desc_kmajor(kb + (k >> 2) * 8192 + off), id_s, k != 0);
+              }
+              umma_commit(bar(B_SFULL + 2 * t + b));
+              ++js[t];
+              prog = true;
+            }
+          }
+          if (prog) {
+            idle = 0;
+            continue;
+          }
+          if (idle++ == 0) {
+            t_idle = gtimer();
+          } else if ((idle & 255) == 0 && (s_abort || gtimer() - t_idle > kWaitLimitNs)) {
+            if (!s_abort) atomicExch(&g_attn_timeout, 1);
+            ok = false;
+            break;
+          }
+        }
+        for (int t = 0; t < MT; ++t)
+          if (na[t] > 0) {
+            ct[t] += na[t];
+            ++ci[t];
+          }
+        gt += nt;
+      }
+      if (!ok) s_abort = 1;
+      umma_commit(bar(B_DONE + MT));   // fires once every MMA of this thread has retired
+      mbar_wait(bar(B_DONE + MT), 0);
+    }
   } else if (warp < W_MMA) {
-    // =============================== transform warps
+    // =============================== transform warps, in place in the stage
     const int tt = tid - W_XF * 32, tw = warp - W_XF;
     // K: row offset rr of pages pg0, pg0 + 1; dims 8cq..8cq+7 and 64 + 8cq..
     const int rr = lane & 15, cq = 2 * (tw & 3) + (lane >> 4), pg0 = 2 * (tw >> 2);
@@ -478,29 +594,42 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     for (int ii = blockIdx.x; ii < a.n_items && ok; ii += gridDim.x) {
       const int nt = item_tiles(a.items[ii]);
       for (int j = 0; j < nt; ++j, ++gt) {
-        const int b = gt & 1, rs = gt % NRS, s = gt % NVS;
-        const uint32_t u = gt >> 1;
-        // raw tile landed; K operand buffer b free once every S of key tile gt - 2 has completed
-        // (KVFULL's next phase is taken by the MMA only after those S); V operand slot s (and
-        // its key positions) once every PV of key tile gt - 3 has retired
-        ok = __all_sync(0xffffffffu, !s_abort && mbar_wait(bar(B_RAWFULL + rs), (gt / NRS) & 1) &&
-                                         (gt < 2 || mbar_wait(bar(B_KFREE + b), (u - 1) & 1)) &&
-                                         (gt < NVS || mbar_wait(bar(B_VFREE + s), (gt / NVS - 1) & 1)));
+        const int s = gt % NST;
+        ok = __all_sync(0xffffffffu, !s_abort && mbar_wait(bar(B_FULL + s), (gt / NST) & 1));
         if (!ok) break;
-        const int* tm = sTm + rs * 8;
-        const uint8_t* kraw = sm + OFF_KRAW + rs * 16384;
-        uint8_t* kop = sm + OFF_KOP + b * 16384;
-        // K: rotate row offset rr of pages pg0 and pg0 + 1 (two independent chains)
+        // Every shared-memory input of the tile is read before the first store (the stores go
+        // to the same stage, so a load placed after them could not be moved ahead of them).
+        const int4 tmA = reinterpret_cast<const int4*>(sTm + s * 8)[0], tmB = reinterpret_cast<const int4*>(sTm + s * 8)[1];
+        const int st0 = pg0 ? tmB.x : tmA.x, ln0 = pg0 ? tmB.y : tmA.y, st1 = pg0 ? tmB.z : tmA.z,
+                  ln1 = pg0 ? tmB.w : tmA.w;
+        uint8_t* kst = sm + OFF_ST + s * ST_BYTES;
+        uint8_t* vst = kst + 16384;
+        // K, rows rr of pages pg0 and pg0 + 1: dims 8cq..8cq+7 (half 0) and 64 + 8cq.. (half 1)
+        uint4* kp[2][2];
+        uint4 kr[2][2];
 #pragma unroll
-        for (int pg = pg0; pg < pg0 + 2; ++pg) {
-          const int key = pg * 16 + rr, start = tm[2 * pg], len = tm[2 * pg + 1];
-          uint4 y1 = make_uint4(0, 0, 0, 0), y2 = y1;
+        for (int u = 0; u < 2; ++u) {
+          const int key = (pg0 + u) * 16 + rr;
+          kp[u][0] = reinterpret_cast<uint4*>(kst + sw128(key, cq));
+          kp[u][1] = reinterpret_cast<uint4*>(kst + 8192 + sw128(key, cq));
+          kr[u][0] = *kp[u][0];
+          kr[u][1] = *kp[u][1];
+        }
+        // V: 4 chunks of 16 bytes of [half][key][8]
+        uint4 vr[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) vr[i] = reinterpret_cast<const uint4*>(vst)[tt + 32 * kTransformWarps * i];
+        // K rotated by RoPE at start + rr; rows without a key (ragged or missing pages) become 0
+        uint4 ky[2][2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int len = u ? ln1 : ln0;
+          ky[u][0] = ky[u][1] = make_uint4(0, 0, 0, 0);
           if (rr < len) {
             float v1[8], v2[8];
-            const uint8_t* kp = kraw + pg * 4096;   // 128-byte rows 2 rr (dims 0..63) and 2 rr + 1
-            bf8_to_f32(*reinterpret_cast<const uint4*>(kp + sw128(2 * rr, cq)), v1);
-            bf8_to_f32(*reinterpret_cast<const uint4*>(kp + sw128(2 * rr + 1, cq)), v2);
-            const float4* hrow = reinterpret_cast<const float4*>(sm + OFF_CS + (rs * 4 + pg) * 512) + 4 * cq;
+            bf8_to_f32(kr[u][0], v1);
+            bf8_to_f32(kr[u][1], v2);
+            const float4* hrow = reinterpret_cast<const float4*>(sm + OFF_CS + (s * 4 + pg0 + u) * 512) + 4 * cq;
             uint32_t o1[4], o2[4];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
@@ -518,225 +647,131 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
               o1[q] = pack_f16x2(y1e[0], y1e[1]);
               o2[q] = pack_f16x2(y2e[0], y2e[1]);
             }
-            y1 = make_uint4(o1[0], o1[1], o1[2], o1[3]);
-            y2 = make_uint4(o2[0], o2[1], o2[2], o2[3]);
+            ky[u][0] = make_uint4(o1[0], o1[1], o1[2], o1[3]);
+            ky[u][1] = make_uint4(o2[0], o2[1], o2[2], o2[3]);
           }
-          *reinterpret_cast<uint4*>(kop + sw128(key, cq)) = y1;
-          *reinterpret_cast<uint4*>(kop + 8192 + sw128(key, cq)) = y2;
-          if (cq == 0) sPos[s * KT + key] = rr < len ? start + rr : INT_MAX;
+        }
+        // V bf16 -> fp16 in place ([half][key][128 B] is already the MN-major operand of
+        // O += P V); rows without a key become 0 (P is 0 there, V must be finite)
+        uint4 vy[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int key = ((tt + 32 * kTransformWarps * i) >> 3) & 63;
+          const uint4 w = vr[i];
+          const int pg = key >> 4, ln = pg == 0 ? tmA.y : pg == 1 ? tmA.w : pg == 2 ? tmB.y : tmB.w;
+          vy[i] = (key & 15) < ln
+                      ? make_uint4(bf2_to_h2(w.x), bf2_to_h2(w.y), bf2_to_h2(w.z), bf2_to_h2(w.w))
+                      : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          *kp[u][0] = ky[u][0];
+          *kp[u][1] = ky[u][1];
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) reinterpret_cast<uint4*>(vst)[tt + 32 * kTransformWarps * i] = vy[i];
+        if (cq == 0) {
+          sPos[s * KT + pg0 * 16 + rr] = rr < ln0 ? st0 + rr : INT_MAX;
+          sPos[s * KT + (pg0 + 1) * 16 + rr] = rr < ln1 ? st1 + rr : INT_MAX;
         }
         if (tt == 0) {   // last key position of the tile; INT_MAX when some slot holds no key
+          const int sts[4] = {tmA.x, tmA.z, tmB.x, tmB.z}, lns[4] = {tmA.y, tmA.w, tmB.y, tmB.w};
           int kmax = -1;
           bool full = true;
+#pragma unroll
           for (int pg = 0; pg < 4; ++pg) {
-            const int len = tm[2 * pg + 1];
-            if (len > 0) kmax = tm[2 * pg] + len - 1;
-            if (len < kBlock) full = false;
+            if (lns[pg] > 0) kmax = sts[pg] + lns[pg] - 1;
+            if (lns[pg] < kBlock) full = false;
           }
           sTile[s] = full ? kmax : INT_MAX;
         }
-        // V: raw [page][row][half] bf16 -> fp16 [half][key][128 B], the MN-major operand; rows
-        // without a key become 0 (P is 0 there, V must be finite)
-        const uint8_t* vraw = sm + OFF_VRAW + rs * 16384;
-        uint8_t* vt = sm + OFF_V + s * 16384;
-#pragma unroll
-        for (int i = 0; i < 1024 / (32 * kTransformWarps); ++i) {
-          const int ch = tt + 32 * kTransformWarps * i;   // 16-byte chunk of the raw tile
-          const int pg = ch >> 8, rp = (ch >> 3) & 31, r = rp >> 1, h = rp & 1, c = (ch & 7) ^ (rp & 7);
-          const int key = pg * 16 + r;
-          uint4 o = make_uint4(0, 0, 0, 0);
-          if (r < tm[2 * pg + 1]) {
-            const uint4 w = *reinterpret_cast<const uint4*>(vraw + ch * 16);
-            o = make_uint4(bf2_to_h2(w.x), bf2_to_h2(w.y), bf2_to_h2(w.z), bf2_to_h2(w.w));
-          }
-          *reinterpret_cast<uint4*>(vt + h * 8192 + sw128(key, c)) = o;
-        }
         fence_async_smem();
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(bar(B_RAWFREE + rs));
-          mbar_arrive(bar(B_KVFULL + b));
-          mbar_arrive(bar(B_POSFULL + s));
-        }
+        if (lane == 0) mbar_arrive(bar(B_XF + s));
       }
     }
     if (!ok) s_abort = 1;
-  } else if (warp == W_MMA) {
-    // =============================== MMA issuer
-    if (lane == 0) {
-      const uint32_t id_s = idesc_f16(128, KT, false), id_pv = idesc_f16(128, D, true);
-      uint32_t gt = 0, ai = 0;
-      uint32_t ct[MT] = {0, 0}, ci[MT] = {0, 0};   // per MMA tile: key tiles and items taken part in
-      // S_t of the MMA tile's c-th key tile into S buffer c & 1, from the K operand at kaddr
-      auto issue_s = [&](int t, uint32_t c, uint32_t kaddr) -> bool {
-        const int b = c & 1;
-        // the buffer's previous contents (P of key tile c - 2) must have been read by its PV
-        if (c >= 2 && !mbar_wait(bar(B_PVDONE + 2 * t + b), ((c - 2) >> 1) & 1)) return false;
-        fence_after();
-        const uint32_t qa = smem_u32(sm + OFF_Q + t * Q_TILE);
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {   // K dimension 128 = 2 halves x 4 steps of 16
-          const uint32_t off = (k & 3) * 32;
-          umma_ss(tmem + 256 + 128 * t + 64 * b, desc_kmajor(qa + (k >> 2) * 16384 + off),
-                  desc_kmajor(kaddr + (k >> 2) * 8192 + off), id_s, k != 0);
-        }
-        umma_commit(bar(B_SFULL + 2 * t + b));
-        return true;
-      };
-      // every S of key tile g (the item's j-th): its K operand ready, then each MMA tile taking part
-      auto issue_tile_s = [&](uint32_t g, int j, const int* na) -> bool {
-        const int kb = g & 1;
-        if (s_abort || !mbar_wait(bar(B_KVFULL + kb), (g >> 1) & 1)) return false;
-        fence_after();
-        const uint32_t kaddr = smem_u32(sm + OFF_KOP + kb * 16384);
-        for (int t = 0; t < MT; ++t)
-          if (j < na[t] && !issue_s(t, ct[t] + j, kaddr)) return false;
-        umma_commit(bar(B_KFREE + kb));   // the K operand buffer is free once these S complete
-        return true;
-      };
-      bool ok = true;
-      for (int ii = blockIdx.x; ii < a.n_items && ok; ii += gridDim.x) {
-        const AttnItem it = a.items[ii];
-        const int nt = item_tiles(it);
-        const int na[MT] = {item_tiles_of(it, 0), item_tiles_of(it, 1)};
-        if (nt == 0) continue;
-        if (s_abort || !mbar_wait(bar(B_QFULL), ai & 1)) {
-          ok = false;
-          break;
-        }
-        ok = issue_tile_s(gt, 0, na);
-        if (ok && nt == 1) umma_commit(bar(B_QFREE));
-        for (int j = 0; j < nt && ok; ++j) {
-          const uint32_t g = gt + j;
-          if (j + 1 < nt) {   // next key tile's S first: the softmax finds it ready after this P
-            if (!issue_tile_s(g + 1, j + 1, na)) {
-              ok = false;
-              break;
-            }
-            if (j + 2 == nt) umma_commit(bar(B_QFREE));   // every S of this item issued
-          }
-          const int s = g % NVS;
-          const uint32_t vb = smem_u32(sm + OFF_V + s * 16384);
-          for (int t = 0; t < MT; ++t) {
-            if (j >= na[t]) continue;
-            const uint32_t c = ct[t] + j;
-            const int b = c & 1;
-            if (s_abort || !mbar_wait(bar(B_PFULL + 2 * t + b), (c >> 1) & 1) ||
-                (j == 0 && ci[t] > 0 && !mbar_wait(bar(B_OFREE + t), (ci[t] - 1) & 1))) {   // previous O_t drained
-              ok = false;
-              break;
-            }
-            fence_after();
-            const uint32_t pa = tmem + 256 + 128 * t + 64 * b + 32;   // P over the S buffer's high half
-#pragma unroll
-            for (int k = 0; k < 4; ++k)   // K dimension 64 keys = 4 steps of 16 (8 TMEM columns of P each)
-              umma_ts(tmem + 128 * t, pa + 8 * k, desc_mnmajor(vb + k * 2048, 8192), id_pv, (j | k) != 0);
-            umma_commit(bar(B_PVDONE + 2 * t + b));
-          }
-          if (ok) umma_commit(bar(B_VFREE + s));
-        }
-        for (int t = 0; t < MT; ++t)
-          if (na[t] > 0) {
-            ct[t] += na[t];
-            ++ci[t];
-          }
-        gt += nt;
-        ++ai;
-      }
-      if (!ok) s_abort = 1;
-      umma_commit(bar(B_MMADONE));   // fires once every MMA of this CTA has retired
-      mbar_wait(bar(B_MMADONE), 0);
-    }
   } else if (warp == W_LOAD) {
-    // =============================== loads (lane 0 issues; the warp reads page metadata)
-    uint32_t n_raw = 0, n_q = 0;   // raw key tiles and Q loads issued
+    // =============================== loads (lanes issue the boxes; the warp holds page metadata)
+    uint32_t n_ld = 0;   // key tiles issued
     bool ok = true;
-    int w0 = 0, wblk = 0, wpos = 0, wlen = 0;   // lane i: metadata of page w0 + i
+    // lane i: metadata of page w0 + i (cur) and of page w0 + 32 + i (nxt, loaded one window ahead)
+    int w0 = 0, cblk = 0, cpos = 0, clen = 0, nblk = 0, npos = 0, nlen = 0;
     for (int ii = blockIdx.x; ii < a.n_items && ok; ii += gridDim.x) {
       const AttnItem it = a.items[ii];
       const int nt = item_tiles(it);
+      auto fetch = [&](int w, int& b, int& p, int& l) {
+        const int pg = w + lane;
+        if (pg < it.page1) {
+          b = a.page_block[pg];
+          p = a.page_pos[pg];
+          l = a.page_len[pg];
+        }
+      };
       for (int j = 0; j < nt; ++j) {
-        const uint32_t gt = n_raw;
-        const int rs = gt % NRS;
-        const uint32_t kr = gt / NRS;
+        const uint32_t gt = n_ld;
+        const int s = gt % NST;
+        const uint32_t kr = gt / NST;
         const int p0 = it.page0 + 4 * j, np = min(4, it.page1 - p0);
-        if (j == 0 || p0 + 4 > w0 + 32) {
+        if (j == 0) {
           w0 = p0;
-          const int pg = w0 + lane;
-          if (pg < it.page1) {
-            wblk = a.page_block[pg];
-            wpos = a.page_pos[pg];
-            wlen = a.page_len[pg];
-          }
+          fetch(w0, cblk, cpos, clen);
+          fetch(w0 + 32, nblk, npos, nlen);
+        } else if (p0 == w0 + 32) {   // windows are 8 key tiles: a tile never straddles two
+          w0 = p0;
+          cblk = nblk, cpos = npos, clen = nlen;
+          fetch(w0 + 32, nblk, npos, nlen);
         }
         int blk[4], pos[4], len[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          blk[q] = __shfl_sync(0xffffffffu, wblk, p0 - w0 + q);
-          pos[q] = __shfl_sync(0xffffffffu, wpos, p0 - w0 + q);
-          len[q] = q < np ? __shfl_sync(0xffffffffu, wlen, p0 - w0 + q) : 0;
+          blk[q] = __shfl_sync(0xffffffffu, cblk, p0 - w0 + q);
+          pos[q] = __shfl_sync(0xffffffffu, cpos, p0 - w0 + q);
+          len[q] = q < np ? __shfl_sync(0xffffffffu, clen, p0 - w0 + q) : 0;
         }
-        // raw slot rs free once the transform is done with key tile gt - 2
-        if (lane == 0) ok = !s_abort && (kr == 0 || mbar_wait(bar(B_RAWFREE + rs), (kr - 1) & 1));
+        // stage s free once every PV of key tile gt - NST has retired
+        if (lane == 0) ok = !s_abort && (kr == 0 || mbar_wait(bar(B_EMPTY + s), (kr - 1) & 1));
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
-        // cos/sin rows of the page starts: 4 x 512 B, one 16-byte chunk per lane and page,
-        // loaded before the TMA issue so that their latency overlaps it
-        float4 cs4[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-          if (q < np) cs4[q] = reinterpret_cast<const float4*>(a.rope_cs + (size_t)pos[q] * 64)[lane];
-        const uint32_t fb = bar(B_RAWFULL + rs);
+        const uint32_t fb = bar(B_FULL + s);
         if (lane == 0) {
-          int* tm = sTm + rs * 8;
+          int* tm = sTm + s * 8;
           for (int q = 0; q < 4; ++q) {
             tm[2 * q] = pos[q];
             tm[2 * q + 1] = len[q];
           }
-          mbar_add_tx(fb, (uint32_t)np * 8192);
+          mbar_expect_tx(fb, (uint32_t)np * (8192 + 512));   // arrives too: the boxes complete the phase
         }
         __syncwarp();
-        if (lane < np) {   // one lane per page issues that page's K and V boxes
-          const uint32_t kd = smem_u32(sm + OFF_KRAW + rs * 16384) + lane * 4096,
-                         vd = smem_u32(sm + OFF_VRAW + rs * 16384) + lane * 4096;
-          const int bq = lane == 0 ? blk[0] : lane == 1 ? blk[1] : lane == 2 ? blk[2] : blk[3];
-          const int y = (bq * a.G + it.g) * kBlock;
-          tma_3d(kd, &a.kmap, 0, 0, y, fb);
-          tma_3d(vd, &a.vmap, 0, 0, y, fb);
-        }
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-          if (q < np) reinterpret_cast<float4*>(sm + OFF_CS + (rs * 4 + q) * 512)[lane] = cs4[q];
-        __syncwarp();
-        if (lane == 0) mbar_arrive(fb);   // releases the metadata and cos/sin rows with the boxes
-        ++n_raw;
-        if (j == 0) {   // this item's Q tiles, once every S of the previous item has completed
-          if (lane == 0) ok = !s_abort && (n_q == 0 || mbar_wait(bar(B_QFREE), (n_q - 1) & 1));
-          ok = __shfl_sync(0xffffffffu, ok, 0);
-          if (!ok) break;
-          if (lane == 0) {
-            const int nq = it.nrows > RB ? 2 : 1;
-            const uint32_t qb = bar(B_QFULL);
-            mbar_expect_tx(qb, (uint32_t)nq * Q_TILE);
-            for (int t = 0; t < nq; ++t)
-              for (int q = 0; q < 8; ++q)   // (head, half): 32 rows x 64 dims
-                tma_3d(smem_u32(sm + OFF_Q + t * Q_TILE + (q & 1) * 16384 + (q >> 1) * 4096), &a.qmap, 64 * (q & 1),
-                       it.g * REP + (q >> 1), it.row0 + RB * t, qb);
+        const uint32_t kd = smem_u32(sm + OFF_ST + s * ST_BYTES), vd = kd + 16384;
+        const uint32_t csd = smem_u32(sm + OFF_CS + s * 2048);
+        const bool run = np == 4 && blk[1] == blk[0] + 1 && blk[2] == blk[0] + 2 && blk[3] == blk[0] + 3;
+        if (run) {   // 4 consecutive blocks: one box per (K or V, half), 8 KB each
+          if (lane < 4) {
+            const int h = lane & 1;
+            tma_5d((lane < 2 ? kd : vd) + h * 8192, lane < 2 ? &a.kmap : &a.vmap, 0, h, 0, it.g, blk[0], fb);
           }
-          ++n_q;
+        } else if (lane < 4 * np) {   // one box per (page, K or V, half), 2 KB each
+          const int q = lane >> 2, h = lane & 1, isv = (lane >> 1) & 1;
+          const int bq = q == 0 ? blk[0] : q == 1 ? blk[1] : q == 2 ? blk[2] : blk[3];
+          tma_5d((isv ? vd : kd) + h * 8192 + q * 2048, isv ? &a.vmap1 : &a.kmap1, 0, h, 0, it.g, bq, fb);
         }
+        if (lane >= 16 && lane < 16 + np) {   // cos/sin rows of the page starts, 512 B each
+          const int q = lane - 16;
+          const int pq = q == 0 ? pos[0] : q == 1 ? pos[1] : q == 2 ? pos[2] : pos[3];
+          tma_2d(csd + q * 512, &a.csmap, 0, pq, fb);
+        }
+        ++n_ld;
       }
     }
     if (!ok) s_abort = 1;
     // every copy this CTA issued has landed before its shared memory is given up (on the
     // normal path these waits return at once: the consumers have seen every phase)
-    if (lane == 0) {
-      for (int rs = 0; rs < NRS; ++rs) {
-        const uint32_t n = (n_raw + NRS - 1 - rs) / NRS;
-        if (n) mbar_wait(bar(B_RAWFULL + rs), (n - 1) & 1);
+    if (lane == 0)
+      for (int s = 0; s < NST; ++s) {
+        const uint32_t n = (n_ld + NST - 1 - s) / NST;
+        if (n) mbar_wait(bar(B_FULL + s), (n - 1) & 1);
       }
-      if (n_q) mbar_wait(bar(B_QFULL), (n_q - 1) & 1);
-    }
   }
   __syncwarp();
   fence_before();
@@ -771,28 +806,33 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 bool tc_attention_supported(int dtype, int D_, int rep) { return dtype == PIC_BF16 && D_ == D && rep == REP; }
 
-bool attn_q_map(CUtensorMap* m, const void* q16, int T, int H) {
-  auto enc = encode_fn();
-  if (!enc || T < 1 || H < 1) return false;
-  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)T};
-  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2};
-  cuuint32_t box[3] = {64, 1, RB};
-  cuuint32_t estr[3] = {1, 1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(q16), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// [rows][128] bf16 viewed as [rows][2 halves][64]: one box = one page (16 rows x both halves)
-bool attn_kv_map(CUtensorMap* m, const void* layer, int pool_blocks, int G) {
+// One layer of a pool, [blocks][G][16 rows][128] bf16, viewed as (64 dims, 2 halves, 16 rows, G,
+// blocks): a box is one 64-dim half of the 16 rows of one KV head's page in 4 consecutive blocks
+// (m4) or in one block (m1), landing as [pages][16 rows][128 B] -- one half of the K-major (K)
+// or MN-major (V) operand of 64 keys.
+bool attn_kv_map(CUtensorMap* m4, CUtensorMap* m1, const void* layer, int pool_blocks, int G) {
   auto enc = encode_fn();
   if (!enc || pool_blocks < 1 || G < 1) return false;
-  cuuint64_t dims[3] = {64, 2, (cuuint64_t)pool_blocks * G * kBlock};
-  cuuint64_t strides[2] = {128, (cuuint64_t)D * 2};
-  cuuint32_t box[3] = {64, 2, kBlock};
-  cuuint32_t estr[3] = {1, 1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(layer), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+  cuuint64_t dims[5] = {64, 2, (cuuint64_t)kBlock, (cuuint64_t)G, (cuuint64_t)pool_blocks};
+  cuuint64_t strides[4] = {128, (cuuint64_t)D * 2, (cuuint64_t)kBlock * D * 2, (cuuint64_t)G * kBlock * D * 2};
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  cuuint32_t box4[5] = {64, 1, kBlock, 1, 4}, box1[5] = {64, 1, kBlock, 1, 1};
+  auto make = [&](CUtensorMap* m, cuuint32_t* box) {
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(layer), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  };
+  return make(m4, box4) && make(m1, box1);
+}
+
+bool attn_cs_map(CUtensorMap* m, const float2* rope_cs, int n_pos) {
+  auto enc = encode_fn();
+  if (!enc || n_pos < 1) return false;
+  cuuint64_t dims[2] = {D, (cuuint64_t)n_pos};   // D floats = D/2 (cos, sin) pairs per position
+  cuuint64_t strides[1] = {(cuuint64_t)D * 4};
+  cuuint32_t box[2] = {D, 1}, estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float2*>(rope_cs), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 

@@ -154,7 +154,7 @@ pic_status pic_op_attention_noalloc(int32_t dtype, int32_t T, int32_t n_heads, i
   a.combines = (const AttnCombine*)(di + o_combs);
   a.n_combines = (int)combs.size();
   if (in.persistent) {
-    s = attention_prepare_tc(a, T, pool_blocks, (__half*)((char*)scratch + o_q16), st);
+    s = attention_prepare_tc(a, T, pool_blocks, rope_positions, (__half*)((char*)scratch + o_q16), st);
     if (s != PIC_OK) return s;
   }
   launch_attention(a, st);

@@ -154,7 +154,7 @@ pic_status pic_op_attention(int32_t dtype, int32_t T, int32_t n_heads, int32_t n
   a.combines = (const AttnCombine*)(di + o_combs);
   a.n_combines = (int)combs.size();
   if (in.persistent) {
-    pic_status e = attention_prepare_tc(a, T, pool_blocks, (__half*)((char*)scratch + L.q16_off), st);
+    pic_status e = attention_prepare_tc(a, T, pool_blocks, rope_positions, (__half*)((char*)scratch + L.q16_off), st);
     if (e != PIC_OK) return e;
   }
   launch_attention(a, st);
