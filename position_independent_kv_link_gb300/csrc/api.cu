@@ -141,8 +141,17 @@ struct pic_store {
   void* attn = nullptr;
   void* act = nullptr;
   void* lm_x = nullptr;
-  float* qkv_acc = nullptr;  // [max_rows][(H+2G)D] fp32, zeroed before each QKV GEMM
-  float* gu_acc = nullptr;   // [max_rows][2F] fp32, zeroed before each gate/up GEMM
+  float* qkv_acc = nullptr;  // [max_rows][(H+2G)D] fp32, the QKV GEMM's result
+  float* gu_acc = nullptr;   // [max_rows][2F] fp32, the gate/up GEMM's result
+  // tcgen05 GEMMs that start their output at zero themselves publish each zeroed tile here as
+  // the launch's epoch (device ints, zero at creation; epochs start at 1)
+  int* tile_ready = nullptr;
+  size_t tile_ready_cap = 0;
+  uint32_t gemm_epoch = 0;
+  uint32_t next_epoch() {
+    if (++gemm_epoch == 0) ++gemm_epoch;
+    return gemm_epoch;
+  }
   float* att_o = nullptr;
   float* att_ml = nullptr;
   int att_parts_cap = 0;
@@ -260,10 +269,18 @@ namespace {
 
 int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
-// Y[T][N] += X . W^T (fp32 Y accumulated in place); Wp: the packed copy of W, if any
-pic_status gemm(const pic_store* s, const void* W, const void* Wp, const void* X, float* Y, int N, int K, int T,
-                cudaStream_t st) {
-  if (Wp) return tc_gemm_run_packed(Wp, X, Y, N, K, T, st, true);   // model weights: fixed since creation
+// Y[T][N] += X . W^T (fp32 Y accumulated in place), or Y = X . W^T when `overwrite`; Wp: the
+// packed copy of W, if any. A packed GEMM that overwrites zeroes Y's tiles itself; otherwise Y
+// is cleared by a kernel first.
+pic_status gemm(pic_store* s, const void* W, const void* Wp, const void* X, float* Y, int N, int K, int T,
+                cudaStream_t st, bool overwrite) {
+  if (Wp) {
+    if (overwrite && tc_gemm_tiles(N, T) <= s->tile_ready_cap)   // model weights: fixed since creation
+      return tc_gemm_run_packed(Wp, X, Y, N, K, T, st, true, s->tile_ready, s->next_epoch());
+    if (overwrite) launch_zero(Y, (size_t)T * N, st);
+    return tc_gemm_run_packed(Wp, X, Y, N, K, T, st, true);
+  }
+  if (overwrite) launch_zero(Y, (size_t)T * N, st);
   launch_gemm_simt(s->m->cfg.dtype, s->m->cfg.dtype == PIC_BF16, W, X, Y, N, K, T, 1, st);
   return PIC_OK;
 }
@@ -419,43 +436,30 @@ pic_status run_forward_impl(pic_store* s, const Batch& b, float* hidden_out, flo
 
   const int qkv = s->m->qkv_dim();
   auto gemm_bytes = [&](double N, double K, double rows) { return N * K * es + rows * K * es + rows * N * 4; };
-  auto run_gemm = [&](const void* W, const void* Wp, const void* X, float* Y, int N, int K, int rows,
-                      int cls = PIC_PROF_GEMM) {
-    Rec r(s, st, cls, gemm_bytes(N, K, rows), 2.0 * N * K * rows, 1);
-    return gemm(s, W, Wp, X, Y, N, K, rows, st);
-  };
-  // The QKV and gate/up GEMMs reduce into fp32 accumulators zeroed ahead of them (cheaper than
-  // clearing them behind the read: the epilogues only read them): both at the start, then
-  // qkv_acc again after each QKV epilogue and gu_acc after the next layer's (the last SwiGLU
-  // read it), where their traffic does not delay a GEMM. Every kernel of the forward is a
-  // programmatic dependent launch of the one before it.
-  auto zero_acc = [&](float* acc, size_t n, float* acc2 = nullptr, size_t n2 = 0) -> pic_status {
-    Rec r(s, st, PIC_PROF_COPY, (double)(n + n2) * 4, 0, 1);
-    launch_zero(acc, n, st, acc2, n2);
-    return PIC_OK;
-  };
+  // The QKV, gate/up and LM-head GEMMs write fresh results (a tcgen05 GEMM zeroes its output
+  // tiles itself before its split-K reduce-adds land; a SIMT GEMM's output is cleared by a kernel
+  // first); the O and down projections add straight into the residual stream h. Every kernel of
+  // the forward is a programmatic dependent launch of the one before it.
   auto pk = [&](const std::vector<const void*>& v, int l) -> const void* { return v.empty() ? nullptr : v[l]; };
-  // The O and down projections add straight into the residual stream h.
-  {
-    pic_status e;
-    if ((e = zero_acc(s->qkv_acc, (size_t)T * qkv, s->gu_acc, (size_t)T * 2 * F)) != PIC_OK) return e;
-    if (!b.compile && b.n_lg > 0 && (e = zero_acc(logits_out, (size_t)b.n_lg * c.vocab)) != PIC_OK) return e;
-  }
+  auto run_gemm = [&](const void* W, const void* Wp, const void* X, float* Y, int N, int K, int rows, bool overwrite,
+                      int cls = PIC_PROF_GEMM) {
+    const bool zero_kernel = overwrite && !(Wp && tc_gemm_tiles(N, rows) <= s->tile_ready_cap);
+    Rec r(s, st, cls, gemm_bytes(N, K, rows) + (overwrite ? (double)rows * N * 4 : 0), 2.0 * N * K * rows,
+          1 + (zero_kernel ? 1 : 0));
+    return gemm(s, W, Wp, X, Y, N, K, rows, st, overwrite);
+  };
   {
     Rec r(s, st, PIC_PROF_ROWWISE, dT * dd * (es + 4 + es) + dT * 4, 0, 1);
     launch_embed_norm(dt, T, d, s->m->embed, d_tok, s->m->attn_norm[0], c.rms_eps, s->h, s->x, st);
   }
   for (int l = 0; l < c.n_layers; ++l) {
     pic_status e;
-    if ((e = run_gemm(s->m->wqkv[l], pk(s->m->pqkv, l), s->x, s->qkv_acc, qkv, d, T)) != PIC_OK) return e;
+    if ((e = run_gemm(s->m->wqkv[l], pk(s->m->pqkv, l), s->x, s->qkv_acc, qkv, d, T, true)) != PIC_OK) return e;
     {
       Rec r(s, st, PIC_PROF_ROWWISE, dT * dQKV * (4 + es), 0, 1);
       launch_qkv_epilogue(dt, T, H, G, D, s->qkv_acc, s->q, d_slot, s->k_layer(l), s->v_layer(l), d_pos, s->rope_cs,
                           att_tc ? (__half*)s->q : nullptr, st);
     }
-    if ((e = zero_acc(s->qkv_acc, (size_t)T * qkv, l > 0 ? s->gu_acc : nullptr, l > 0 ? (size_t)T * 2 * F : 0)) !=
-        PIC_OK)
-      return e;
     // compile keeps only KV: the last layer's attention and MLP feed nothing stored
     if (b.compile && l == c.n_layers - 1) break;
     aa.k_layer = s->k_layer(l);
@@ -470,19 +474,19 @@ pic_status run_forward_impl(pic_store* s, const Batch& b, float* hidden_out, flo
       Rec r(s, st, PIC_PROF_ATTENTION, att_bytes, att_flops, att_launches);
       launch_attention(aa, st);
     }
-    if ((e = run_gemm(s->m->wo[l], pk(s->m->po, l), s->attn, s->h, d, H * D, T)) != PIC_OK) return e;
+    if ((e = run_gemm(s->m->wo[l], pk(s->m->po, l), s->attn, s->h, d, H * D, T, false)) != PIC_OK) return e;
     {
       Rec r(s, st, PIC_PROF_ROWWISE, dT * dd * (4 + es), 0, 1);
       launch_rmsnorm_rows(dt, T, d, s->h, s->m->mlp_norm[l], c.rms_eps, s->x, false, nullptr, nullptr, nullptr,
                           nullptr, st);
     }
-    if ((e = run_gemm(s->m->wgu[l], pk(s->m->pgu, l), s->x, s->gu_acc, 2 * F, d, T, PIC_PROF_GEMM_GATE_UP)) != PIC_OK)
+    if ((e = run_gemm(s->m->wgu[l], pk(s->m->pgu, l), s->x, s->gu_acc, 2 * F, d, T, true, PIC_PROF_GEMM_GATE_UP)) != PIC_OK)
       return e;
     {
       Rec r(s, st, PIC_PROF_ROWWISE, dT * 2 * dF * 4 + dT * dF * es, 0, 1);
       launch_swiglu(dt, T, F, s->gu_acc, s->act, st);
     }
-    if ((e = run_gemm(s->m->wdown[l], pk(s->m->pdown, l), s->act, s->h, d, F, T)) != PIC_OK) return e;
+    if ((e = run_gemm(s->m->wdown[l], pk(s->m->pdown, l), s->act, s->h, d, F, T, false)) != PIC_OK) return e;
     const bool last = l == c.n_layers - 1;
     {
       Rec r(s, st, PIC_PROF_ROWWISE, dT * dd * (4 + es), 0, 1);
@@ -490,26 +494,18 @@ pic_status run_forward_impl(pic_store* s, const Batch& b, float* hidden_out, flo
                           d_out, hidden_out, d_lg, s->lm_x, st);
     }
   }
-  if (!b.compile && b.n_lg > 0) {   // logits were zeroed at the start
+  if (!b.compile && b.n_lg > 0) {
     pic_status e;
-    if ((e = run_gemm(s->m->lm_head, s->m->plm, s->lm_x, logits_out, c.vocab, d, b.n_lg)) != PIC_OK) return e;
+    if ((e = run_gemm(s->m->lm_head, s->m->plm, s->lm_x, logits_out, c.vocab, d, b.n_lg, true)) != PIC_OK) return e;
   }
   PIC_CUDA(cudaGetLastError());
   return PIC_OK;
 }
 
 pic_status run_forward(pic_store* s, const Batch& b, float* hidden_out, float* logits_out, cudaStream_t st) {
-  const pic_status e = run_forward_impl(s, b, hidden_out, logits_out, st);
-  if (e != PIC_OK) {
-    // a forward stopped part-way may leave sums in the in-place accumulators: clear them
-    const std::string msg = pic_last_error();
-    const size_t R = s->cfg.max_rows;
-    cudaMemsetAsync(s->qkv_acc, 0, R * (size_t)s->m->qkv_dim() * 4, st);
-    cudaMemsetAsync(s->gu_acc, 0, R * 2 * (size_t)s->m->cfg.ffn_dim * 4, st);
-    (void)cudaGetLastError();
-    set_error(msg);
-  }
-  return e;
+  // every GEMM result the forward reads is written fresh by that forward, so a forward stopped
+  // part-way leaves nothing a later one depends on
+  return run_forward_impl(s, b, hidden_out, logits_out, st);
 }
 
 bool valid_tokens(const int32_t* t, int n, int vocab) {
@@ -652,6 +648,12 @@ pic_status pic_store_create(pic_model* m, const pic_store_config* cfg, void* k_p
                o_atto = carve((size_t)s->att_parts_cap * kAttnPartRows * rep * c.head_dim * 4),
                o_attml = carve((size_t)s->att_parts_cap * kAttnPartRows * rep * 2 * 4), o_meta = carve(s->meta_cap * 4),
                o_rope = carve((size_t)std::max(16, sc.max_positions) * (c.head_dim / 2) * sizeof(float2));
+  // ready flags of the self-zeroing GEMMs' output tiles: the most tiles any of them has
+  const int rows_max = std::max(R, (size_t)sc.max_logit_rows) > 0 ? (int)std::max(R, (size_t)sc.max_logit_rows) : 1;
+  s->tile_ready_cap = std::max({tc_gemm_tiles(std::max(128, m->qkv_dim() / 128 * 128), rows_max),
+                                tc_gemm_tiles(std::max(128, 2 * c.ffn_dim / 128 * 128), rows_max),
+                                tc_gemm_tiles(std::max(128, c.vocab / 128 * 128), std::max(1, sc.max_logit_rows))});
+  const size_t o_ready = carve(s->tile_ready_cap * 4);
   cudaError_t e = cudaMalloc(&s->ws, off);
   if (e != cudaSuccess) return fail(PIC_ERR_CUDA, std::string("workspace cudaMalloc: ") + cudaGetErrorString(e));
   s->h = (float*)(s->ws + o_h);
@@ -666,10 +668,11 @@ pic_status pic_store_create(pic_model* m, const pic_store_config* cfg, void* k_p
   s->att_ml = (float*)(s->ws + o_attml);
   s->meta_d = (int32_t*)(s->ws + o_meta);
   s->rope_cs = (float2*)(s->ws + o_rope);
-  // the accumulators start at zero (each forward also zeroes them before their GEMM), and so
-  // do the q rows that no forward has written yet
-  e = cudaMemset(s->ws + o_qkv, 0, o_gu + R * 2 * F * 4 - o_qkv);
-  if (e == cudaSuccess) e = cudaMemset(s->ws + o_q, 0, o_attn - o_q);
+  s->tile_ready = (int*)(s->ws + o_ready);
+  // the q rows that no forward has written yet start at zero (a 32-row box of the tensor-core
+  // attention may read them), and so do the GEMMs' tile-ready flags
+  e = cudaMemset(s->ws + o_q, 0, o_attn - o_q);
+  if (e == cudaSuccess) e = cudaMemset(s->tile_ready, 0, s->tile_ready_cap * 4);
   if (e != cudaSuccess) {
     cudaFree(s->ws);
     return fail(PIC_ERR_CUDA, std::string("workspace memset: ") + cudaGetErrorString(e));

@@ -183,6 +183,12 @@ struct TcParams {
   int total;         // tiles * nkb work units (< 2^31, checked on the host)
   uint32_t ab_fmt;   // operand format of both A and B: 1 = bf16, 0 = fp16
   uint32_t tmem_cols;
+  // Y starts at zero inside the kernel (no separate clearing pass): the CTA whose range holds a
+  // tile's first k-block zeroes the tile's part of Y and then sets tile_ready[tile] = epoch;
+  // every reduce-add into a tile waits for that. Null: Y is accumulated into as it is.
+  int* tile_ready;
+  uint32_t epoch;
+  float* Y;          // raw Y [T][N] (for the zeroing)
 };
 
 // Segment walk shared by the MMA issuer and the epilogue: [g, end) inside one tile.
@@ -366,6 +372,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool leader = (warp == 3 && lane == 0);
     float* stg = reinterpret_cast<float*>(epi);
     asm volatile("griddepcontrol.wait;" ::: "memory");   // Y is written by earlier kernels
+    if (p.tile_ready) {
+      // zero the tiles whose first k-block is in this CTA's range: 32 threads per row of 128
+      // columns (16-byte stores), 4 rows per pass; then publish them
+      const int ep = threadIdx.x - 3 * 32;   // 0..127
+      const int t_tiles_bn = p.BN;
+      for (int tile = (lo + p.nkb - 1) / p.nkb; tile * p.nkb < hi; ++tile) {
+        const int m0 = (tile % p.m_tiles) * BM, t0 = (tile / p.m_tiles) * t_tiles_bn;
+        const int rows = min(t_tiles_bn, p.T - t0);
+        for (int rr = ep >> 5; rr < rows; rr += 4)
+          reinterpret_cast<float4*>(p.Y + (size_t)(t0 + rr) * p.N + m0)[ep & 31] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      __threadfence();
+      epi_bar();
+      if (leader)
+        for (int tile = (lo + p.nkb - 1) / p.nkb; tile * p.nkb < hi; ++tile)
+          asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p.tile_ready + tile), "r"(p.epoch) : "memory");
+    }
     Seg sg{0, lo, 0};
     int s = 0, buf = 0;
     while (next_seg(sg, hi, p.nkb)) {
@@ -379,6 +402,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       asm volatile("tcgen05.fence::after_thread_sync;");
       const int m0 = (sg.tile % p.m_tiles) * BM, t0 = (sg.tile / p.m_tiles) * p.BN;
       const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + ab * p.BN;
+      if (p.tile_ready && leader) {
+        // the tile's zeroing (by the CTA holding its first k-block) has landed
+        const unsigned long long w0 = gtimer();
+        for (uint32_t i = 0;; ++i) {
+          uint32_t v;
+          asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p.tile_ready + sg.tile) : "memory");
+          if (v == p.epoch) break;
+          if ((i & 63) == 63 && (s_abort || gtimer() - w0 > kWaitLimitNs)) {
+            atomicExch(&g_tc_timeout, 1);
+            s_abort = 1;
+            break;
+          }
+        }
+        asm volatile("fence.proxy.async.global;" ::: "memory");   // the reduce-adds come after the zeroes
+      }
       for (int c = 0; c < p.BN; c += EPI_ROWS) {
         float v[16];
         tmem_ld16(taddr + c, v);
@@ -502,12 +540,15 @@ bool tc_gemm_supported(int N, int K, int T) { return N >= BM && N % BM == 0 && K
 namespace {
 
 pic_status tc_gemm_launch(const void* W, bool packed, const void* X, float* Y, int N, int K, int T, cudaStream_t st,
-                          bool early_weights) {
+                          bool early_weights, int* tile_ready, uint32_t epoch) {
   if (!tc_gemm_supported(N, K, T)) return fail(PIC_ERR_UNSUPPORTED, "tcgen05 gemm: unsupported shape");
   if (((uintptr_t)W | (uintptr_t)X | (uintptr_t)Y) % 16)
     return fail(PIC_ERR_INVALID_ARG, "tcgen05 gemm: operands not 16-byte aligned");
   TcParams p{};
   p.w_packed = packed ? static_cast<const uint8_t*>(W) : nullptr;
+  p.tile_ready = tile_ready;
+  p.epoch = epoch;
+  p.Y = Y;
   p.ab_fmt = packed ? 0u : 1u;   // the packed copy is fp16 (X too); the plain layout is bf16
   p.N = N;
   p.K = K;
@@ -561,13 +602,15 @@ pic_status tc_gemm_launch(const void* W, bool packed, const void* X, float* Y, i
 }  // namespace
 
 pic_status tc_gemm_run(const void* W, const void* X, float* Y, int N, int K, int T, cudaStream_t st) {
-  return tc_gemm_launch(W, false, X, Y, N, K, T, st, false);
+  return tc_gemm_launch(W, false, X, Y, N, K, T, st, false, nullptr, 0);
 }
 
 pic_status tc_gemm_run_packed(const void* Wp, const void* X, float* Y, int N, int K, int T, cudaStream_t st,
-                              bool early_weights) {
-  return tc_gemm_launch(Wp, true, X, Y, N, K, T, st, early_weights);
+                              bool early_weights, int* tile_ready, uint32_t epoch) {
+  return tc_gemm_launch(Wp, true, X, Y, N, K, T, st, early_weights, tile_ready, epoch);
 }
+
+size_t tc_gemm_tiles(int N, int T) { return (size_t)(N / BM) * ((T + pick_bn(T) - 1) / pick_bn(T)); }
 
 pic_status tc_pack_weight(const void* W, void* out, int N, int K, cudaStream_t st) {
   if (!tc_gemm_supported(N, K, 1)) return fail(PIC_ERR_UNSUPPORTED, "pack: N % 128 and K % 64 must be 0");

@@ -118,8 +118,12 @@ constexpr float kQ16Scale = 1.4426950408889634f * 0.08838834764831845f;
 // Same with fp16 weights in the tile layout written by tc_pack_weight and fp16 X.
 // early_weights: launch as a programmatic dependent of the previous kernel, streaming weight
 // tiles before that kernel completes -- only for weights no kernel in flight writes.
+// tile_ready (non-null): Y = X . W^T instead of Y += ...: the kernel zeroes Y's tiles itself,
+// publishing each in tile_ready[tile] (>= tc_gemm_tiles(N, T) ints, device) as `epoch`, which
+// must differ from the value any earlier launch left there.
 pic_status tc_gemm_run_packed(const void* Wp, const void* X, float* Y, int N, int K, int T, cudaStream_t st,
-                              bool early_weights = false);
+                              bool early_weights = false, int* tile_ready = nullptr, uint32_t epoch = 0);
+size_t tc_gemm_tiles(int N, int T);
 // [N][K] bf16 -> N*K*2 bytes of fp16 16 KB tiles (128 rows x 64 k, 128-byte swizzled image),
 // tile (mt, kb) at (mt * K/64 + kb) * 16 KB.
 pic_status tc_pack_weight(const void* W, void* out, int N, int K, cudaStream_t st);
