@@ -128,23 +128,66 @@ def brute_compile(m: BruteModel, chunk: Sequence[int], n_dummy: int = 0, dummy: 
     return [Kc[l][n_dummy:] for l in range(nl)], [Vc[l][n_dummy:] for l in range(nl)]
 
 
+def brute_scores(m: BruteModel, compiled: List[Tuple], chunks: Sequence[Sequence[int]],
+                 query: Sequence[int]) -> List[float]:
+    """Dynamic (attention-based) selection scores, one query token and one head at a time:
+    the prompt keeps its compiled layer-0 K; each query token at layer 0 attends causally
+    over the prompt and the query tokens up to itself, RoPE at absolute positions; a prompt
+    token scores the sum of its softmax weights over the query tokens and heads (the
+    reading of CacheBlend's attention-based selection; EPIC summary page)."""
+    sp = m.spec
+    H, G, D = sp.n_heads, sp.n_kv_heads, sp.head_dim
+    rep = H // G
+    W = m.L[0]
+    K0: List[List[List[float]]] = []          # per position: per KV head pre-RoPE vector
+    for (ck, _), c in zip(compiled, chunks):
+        K0 += [list(r) for r in ck[0]]
+    N = len(K0)
+    Q = []
+    for tok in query:
+        x = _norm(list(m.E[int(tok)]), W["attn_norm"], sp.rms_eps)
+        q, k = _mv(W["wq"], x), _mv(W["wk"], x)
+        Q.append([q[h * D:(h + 1) * D] for h in range(H)])
+        K0.append([k[g * D:(g + 1) * D] for g in range(G)])
+    score = [0.0] * N
+    for j in range(len(query)):
+        p = N + j
+        for hq in range(H):
+            qr = _turn(Q[j][hq], p, sp.rope_base)
+            s = []
+            for u in range(p + 1):
+                kr = _turn(K0[u][hq // rep], u, sp.rope_base)
+                acc = 0.0
+                for i in range(D):
+                    acc += qr[i] * kr[i]
+                s.append(acc / math.sqrt(D))
+            mx = max(s)
+            w = [math.exp(a - mx) for a in s]
+            tot = sum(w)
+            for u in range(N):
+                score[u] += w[u] / tot
+    return score
+
+
 def brute_link(m: BruteModel, compiled: List[Tuple], chunks: Sequence[Sequence[int]], query: Sequence[int],
-               k: int, decode: Sequence[int] = ()) -> Dict[str, object]:
+               k: int, decode: Sequence[int] = (), chosen: Sequence[Sequence[int]] = None) -> Dict[str, object]:
     """LegoLink-k for one request, one token at a time in position order.
 
     compiled[i] = (K rows per layer, V rows per layer) of chunk i as brute_compile returns.
     Returns hidden of the query rows, last-row logits and per-layer recomputed K/V rows;
     then the tokens of `decode` are generated one after another from the linked caches
-    (their hidden states, logits and per-layer K/V rows under "decode_*").
+    (their hidden states, logits and per-layer K/V rows under "decode_*"). With `chosen`
+    (per chunk the token indices to recompute) those rows are recomputed instead of the
+    first k of each chunk.
     """
     nl = m.spec.n_layers
     seq: List[int] = []
     Kc = [[] for _ in range(nl)]
     Vc = [[] for _ in range(nl)]
     selected: List[int] = []
-    for (ck, cv), c in zip(compiled, chunks):
+    for i, ((ck, cv), c) in enumerate(zip(compiled, chunks)):
         off = len(seq)
-        for t in range(min(k, len(c))):
+        for t in (range(min(k, len(c))) if chosen is None else sorted(chosen[i])):
             selected.append(off + t)
         seq += [int(t) for t in c]
         for l in range(nl):

@@ -240,6 +240,57 @@ def compile_chunks(model: OracleModel, chunks: Sequence[np.ndarray], n_dummy: in
     return [([k[n_dummy:] for k in r.k], [v[n_dummy:] for v in r.v]) for r in res]
 
 
+# --------------------------------------------------------------------------- dynamic selection
+
+def query_attention_scores(model: OracleModel, chunk_tokens: Sequence[np.ndarray], chunk_k0: Sequence[np.ndarray],
+                           query: np.ndarray) -> np.ndarray:
+    """Attention mass each prompt token receives from the query at layer 0 (dynamic selection).
+
+    The pages compare LegoLink's static choice of chunk-initial tokens with CacheBlend's
+    "dynamic attention-based selection" of the tokens to recompute (EPIC summary page:
+    problem statement; Measured effects table, CacheBlend-r rows and the static-vs-dynamic
+    row) without giving its formula. Reading: the prompt is linked with no recomputation
+    (every chunk's compiled layer-0 K, rotated at its absolute position); the query rows'
+    q and K are computed at layer 0; each query row and head attends causally over the
+    prompt and the query; a prompt token's score is the sum of the softmax weights it gets
+    over all query rows and heads. Returns scores [N] for the N prompt tokens.
+    """
+    sp = model.spec
+    H, G, D = sp.n_heads, sp.n_kv_heads, sp.head_dim
+    W = model.layer(0)
+    q_tok = np.asarray(query)
+    N = sum(len(t) for t in chunk_tokens)
+    Lq = len(q_tok)
+    x = rms_norm(model.embed(q_tok), W["attn_norm"], sp.rms_eps)
+    q = (x @ W["wq"].T).reshape(Lq, H, D)
+    kq = (x @ W["wk"].T).reshape(Lq, G, D)
+    K = np.concatenate([_f64(k) for k in chunk_k0] + [kq])              # pre-RoPE, positions 0..N+Lq-1
+    pos = np.arange(N + Lq)
+    qpos = pos[N:]
+    q_rot = rope(q, qpos, sp.rope_base)
+    k_rot = rope(K, pos, sp.rope_base)
+    allowed = pos[None, :] <= qpos[:, None]
+    scores = np.zeros(N)
+    rep = H // G
+    for h in range(H):
+        s = (q_rot[:, h, :] @ k_rot[:, h // rep, :].T) / np.sqrt(D)
+        s = np.where(allowed, s, -np.inf)
+        p = np.exp(s - s.max(axis=1, keepdims=True))
+        p /= p.sum(axis=1, keepdims=True)
+        scores += p[:, :N].sum(axis=0)
+    return scores
+
+
+def select_top(scores: np.ndarray, r_percent: int) -> np.ndarray:
+    """The floor(r * N / 100) prompt positions with the largest scores (equal scores: the
+    lower position first), in ascending position order (CacheBlend-r recomputes r % of the
+    tokens: EPIC summary page, Measured effects table)."""
+    N = len(scores)
+    n = (int(r_percent) * N) // 100
+    order = sorted(range(N), key=lambda u: (-scores[u], u))
+    return np.asarray(sorted(order[:n]), dtype=np.int64)
+
+
 # --------------------------------------------------------------------------- paged store
 
 class OutOfBlocks(Exception):
@@ -409,10 +460,87 @@ class OracleStore:
             metas.append(LinkMeta(i32(sel), i32(slots), i32(table), i32(ppos), i32(plen), i32(priv)))
         return metas
 
+    def plan_selected(self, requests: Sequence[Tuple[Sequence[int], int, Sequence[Sequence[int]]]]) -> List[LinkMeta]:
+        """Metadata of a link whose recomputed rows are given per chunk (dynamic selection).
+
+        requests: (chunk ids, query length, per chunk the ascending token indices to
+        recompute). Every block of a chunk that holds a recomputed token becomes the
+        request's own copy (MEPIC abstract: only request-specific blocks are private); a
+        request takes, per chunk in order, one new block per such chunk block in ascending
+        order, then its query blocks; lowest free id first, all or nothing.
+        """
+        blocks_of = lambda sel: sorted({t // BLOCK for t in sel})
+        need = 0
+        for cids, lq, sels in requests:
+            need += sum(len(blocks_of(sel)) for sel in sels) + (-(-lq // BLOCK))
+        if need > len(self.free):
+            raise OutOfBlocks("link")
+        metas = []
+        for cids, lq, sels in requests:
+            sel, slots, table, ppos, plen, priv = [], [], [], [], [], []
+            off = 0
+            for c, cs in zip(cids, sels):
+                ch = self.chunks[c]
+                L = len(ch.tokens)
+                mine = blocks_of(cs)
+                own = dict(zip(mine, self._take(len(mine))))
+                priv += [own[j] for j in mine]
+                for j in range(-(-L // BLOCK)):
+                    table.append(own.get(j, ch.blocks[j]))
+                    ppos.append(off + BLOCK * j)
+                    plen.append(min(BLOCK, L - BLOCK * j))
+                for t in cs:
+                    sel.append(off + t)
+                    slots.append(own[t // BLOCK] * BLOCK + t % BLOCK)
+                off += L
+            qb = self._take(-(-lq // BLOCK))
+            priv += qb
+            for j in range(len(qb)):
+                table.append(qb[j])
+                ppos.append(off + BLOCK * j)
+                plen.append(min(BLOCK, lq - BLOCK * j))
+            for t in range(lq):
+                sel.append(off + t)
+                slots.append(qb[t // BLOCK] * BLOCK + t % BLOCK)
+            i32 = lambda a: np.asarray(a, dtype=np.int32)
+            metas.append(LinkMeta(i32(sel), i32(slots), i32(table), i32(ppos), i32(plen), i32(priv)))
+        return metas
+
+    def link_selected(self, requests: Sequence[Tuple[Sequence[int], np.ndarray, Sequence[Sequence[int]]]],
+                      all_logits: bool = False) -> LinkOut:
+        """Link with the recomputed rows given per chunk: the same steps as `link` (a4-a10)
+        over those rows, metadata from `plan_selected`."""
+        metas = self.plan_selected([(cids, len(q), sels) for cids, q, sels in requests])
+        return self._run_link([(cids, q) for cids, q, _ in requests], metas, all_logits)
+
+    def link_dynamic(self, requests: Sequence[Tuple[Sequence[int], np.ndarray]], r_percent: int,
+                     all_logits: bool = False) -> Tuple[LinkOut, List[np.ndarray]]:
+        """CacheBlend-r: per request, score the prompt tokens by the query's attention
+        (`query_attention_scores`), recompute the top r % of them (`select_top`) and the
+        query. Returns the link and each request's scores."""
+        sels, scores = [], []
+        for cids, q in requests:
+            chs = [self.chunks[c] for c in cids]
+            sc = query_attention_scores(self.model, [c.tokens for c in chs], [c.k[0] for c in chs], q)
+            top = select_top(sc, r_percent)
+            per, off = [], 0
+            for c in chs:
+                L = len(c.tokens)
+                per.append([int(u - off) for u in top if off <= u < off + L])
+                off += L
+            sels.append(per)
+            scores.append(sc)
+        out = self.link_selected([(cids, q, sel) for (cids, q), sel in zip(requests, sels)], all_logits)
+        return out, scores
+
     def link(self, requests: Sequence[Tuple[Sequence[int], np.ndarray]], k: int,
              all_logits: bool = False) -> LinkOut:
         """LegoLink-k over a batch of requests (steps a1-a10), returning outputs and metadata."""
         metas = self.plan([(cids, len(q)) for cids, q in requests], k)
+        return self._run_link(requests, metas, all_logits)
+
+    def _run_link(self, requests, metas: List[LinkMeta], all_logits: bool) -> LinkOut:
+        """Steps a4-a10 of a link whose metadata (blocks taken, selected rows) is planned."""
         rids = []
         for (cids, _), meta in zip(requests, metas):
             rid = self._next_req

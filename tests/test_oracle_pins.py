@@ -514,3 +514,128 @@ def test_decode_opens_blocks_in_call_order(tiny):
     for rid, f in zip(out.rids, g["final"]):
         m = st.request_meta(rid)
         assert {k: getattr(m, k).tolist() for k in f} == f
+
+
+# ----------------------------------------------------------------------------- dynamic selection (CacheBlend-r)
+
+def test_dynamic_scores_match_bruteforce(micro):
+    """Layer-0 attention mass per prompt token: the vectorised oracle equals the per-token loop."""
+    spec, w, model = micro
+    lens = [5, 16, 19]
+    chunks = [pi.gen_tokens(L, spec.vocab, 31, i) for i, L in enumerate(lens)]
+    q = pi.gen_tokens(6, spec.vocab, 32)
+    bm = bf.BruteModel(spec, w)
+    comp = [bf.brute_compile(bm, c) for c in chunks]
+    got = po.query_attention_scores(model, chunks, [np.asarray(ck[0]) for ck, _ in comp], q)
+    ref = np.asarray(bf.brute_scores(bm, comp, chunks, q))
+    assert got.shape == (sum(lens),)
+    assert rel_err(got, ref) < 1e-12
+    # every query row's weights sum to one over the prompt and the query keys it sees
+    assert 0.0 < got.sum() < len(q) * spec.n_heads
+
+
+def test_dynamic_select_hand_example():
+    """Top r % of N by score, equal scores taking the lower position first, ascending output."""
+    sc = np.array([1.0, 3.0, 3.0, 2.0, 0.0])
+    assert po.select_top(sc, 0).tolist() == []
+    assert po.select_top(sc, 20).tolist() == [1]          # n = 1: of the tied 3.0s, position 1
+    assert po.select_top(sc, 40).tolist() == [1, 2]
+    assert po.select_top(sc, 60).tolist() == [1, 2, 3]
+    assert po.select_top(sc, 99).tolist() == [0, 1, 2, 3]  # n = floor(4.95) = 4
+    assert po.select_top(sc, 100).tolist() == [0, 1, 2, 3, 4]
+
+
+def test_dynamic_metadata_hand_example():
+    """Blocks of recomputed tokens inside a chunk become private copies (hand-worked ids)."""
+    g = json.load(open(os.path.join(GOLD, "tiny_dynamic_metadata.json")))
+    st = po.OracleStore(None, 64)
+    cids = [st._add_chunk(np.zeros(g["chunk_len"], dtype=np.int32), [], []) for _ in range(g["n_chunks"])]
+    m, = st.plan_selected([(cids, g["query_len"], g["chosen"])])
+    for key in ("private_blocks", "page_table", "page_pos", "page_len", "selected", "slots"):
+        assert getattr(m, key).tolist() == g[key], key
+
+
+def test_selected_first_k_equals_legolink_k(tiny):
+    """Choosing the first k tokens of every chunk reproduces LegoLink-k exactly (metadata and outputs)."""
+    spec, w, model = tiny
+    lens = [64, 37, 64, 5]
+    chunks = [pi.gen_tokens(L, spec.vocab, 33, i) for i, L in enumerate(lens)]
+    q = pi.gen_tokens(16, spec.vocab, 34)
+    for k in (2, 17):
+        st_a, cids_a, out_a = _link(spec, model, chunks, [q], k=k)
+        st_b = po.OracleStore(model, 256)
+        cids_b = st_b.compile_many(chunks)
+        out_b = st_b.link_selected([(cids_b, q, [list(range(min(k, L))) for L in lens])])
+        for key in ("selected", "slots", "page_table", "page_pos", "page_len", "private_blocks"):
+            assert np.array_equal(getattr(out_a.meta[0], key), getattr(out_b.meta[0], key)), key
+        assert rel_err(out_b.hidden[0], out_a.hidden[0]) < 1e-13
+        assert rel_err(out_b.logits[0], out_a.logits[0]) < 1e-13
+
+
+def test_selected_matches_bruteforce(micro):
+    """Recomputed rows chosen anywhere in a chunk: equal to the per-token loop recomputing them."""
+    spec, w, model = micro
+    lens = [5, 16, 19]
+    chosen = [[3], [0, 7, 15], [2, 18]]
+    chunks = [pi.gen_tokens(L, spec.vocab, 35, i) for i, L in enumerate(lens)]
+    q = pi.gen_tokens(5, spec.vocab, 36)
+    st = po.OracleStore(model, 256)
+    cids = st.compile_many(chunks)
+    out = st.link_selected([(cids, q, chosen)])
+    bm = bf.BruteModel(spec, w)
+    comp = [bf.brute_compile(bm, c) for c in chunks]
+    ref = bf.brute_link(bm, comp, chunks, q, 0, chosen=chosen)
+    assert list(out.meta[0].selected) == ref["selected"]
+    assert rel_err(out.hidden[0], np.array(ref["hidden"])) < 1e-12
+    assert rel_err(out.logits[0][0], np.array(ref["logits"])) < 1e-12
+    for l in range(spec.n_layers):
+        assert rel_err(out.k[0][l], np.array(ref["k"][l])) < 1e-12
+
+
+def test_dynamic_r100_is_full_recompute(tiny):
+    """r = 100 %: every prompt token is recomputed -- a plain prefill of the concatenated prompt."""
+    spec, w, model = tiny
+    chunks = [pi.gen_tokens(64, spec.vocab, 37, i) for i in range(3)]
+    q = pi.gen_tokens(16, spec.vocab, 38)
+    st = po.OracleStore(model, 256)
+    cids = st.compile_many(chunks)
+    out, scores = st.link_dynamic([(cids, q)], 100, all_logits=True)
+    assert out.meta[0].selected.tolist() == list(range(3 * 64 + 16))
+    fr = po.full_prefill(model, np.concatenate(chunks + [q]))
+    assert rel_err(out.hidden[0], fr.hidden[-16:]) < 1e-11
+    for l in range(spec.n_layers):
+        assert rel_err(out.k[0][l], fr.k[l]) < 1e-11
+
+
+def test_dynamic_r0_is_naive_reuse(micro):
+    """r = 0: nothing but the query is recomputed -- every chunk's compiled KV reused as it is
+    (the per-token loop with k = 0 and no dummy prefix)."""
+    spec, w, model = micro
+    lens = [5, 16, 19]
+    chunks = [pi.gen_tokens(L, spec.vocab, 39, i) for i, L in enumerate(lens)]
+    q = pi.gen_tokens(5, spec.vocab, 40)
+    st = po.OracleStore(model, 256)
+    cids = st.compile_many(chunks)
+    out, _ = st.link_dynamic([(cids, q)], 0)
+    bm = bf.BruteModel(spec, w)
+    comp = [bf.brute_compile(bm, c) for c in chunks]
+    ref = bf.brute_link(bm, comp, chunks, q, 0)
+    assert out.meta[0].selected.tolist() == ref["selected"] == list(range(40, 45))
+    assert rel_err(out.hidden[0], np.array(ref["hidden"])) < 1e-12
+
+
+def test_dynamic_selects_by_attention(micro):
+    """The chosen rows are the highest-scoring ones: each chosen token's score is at least every
+    unchosen one's (ties to the lower position), and their count is floor(r N / 100)."""
+    spec, w, model = micro
+    lens = [5, 16, 19]
+    chunks = [pi.gen_tokens(L, spec.vocab, 41, i) for i, L in enumerate(lens)]
+    q = pi.gen_tokens(5, spec.vocab, 42)
+    st = po.OracleStore(model, 256)
+    cids = st.compile_many(chunks)
+    out, (sc,) = st.link_dynamic([(cids, q)], 15)
+    N = sum(lens)
+    chosen = [u for u in out.meta[0].selected.tolist() if u < N]
+    assert len(chosen) == 15 * N // 100
+    rest = [u for u in range(N) if u not in chosen]
+    assert min(sc[chosen]) >= max(sc[rest])
