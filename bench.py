@@ -36,11 +36,12 @@ import pic_inputs as pi  # noqa: E402
 METRIC = "linked prompt tokens/sec (link step, 8B shape)"
 UNIT = "tokens/s"
 
-# ncu dram__bytes_read.sum + dram__bytes_write.sum of one launch of the tcgen05 GEMM at the
-# gate/up shape of the 8B link (28672 x 4096 weights, 224 rows), measured on the kernel
-# source whose sha256 prefix is recorded beside it (262.44 MB read + 8.57 MB written); it is
-# reported as null once that source changes.
-GEMM_TRAFFIC = {"src_sha256_12": "ff2fd5e81231", "bytes_per_launch": 271018240, "shape": "28672x4096x224"}
+# ncu dram__bytes_read.sum + dram__bytes_write.sum of the tcgen05 GEMM over all its launches of
+# one 8B link step (10 x 512 + 64 query, k = 16: 224 rows), per launch: measured on a 2-layer
+# model of the same width (every layer's four projections are the same launches), scaled to 32
+# layers + the LM head (32 x 475.07 MB + 1051.83 MB over 129 launches), on the kernel source
+# whose sha256 prefix is recorded beside it; reported as null once that source changes.
+GEMM_TRAFFIC = {"src_sha256_12": "8cdca38feea7", "bytes_per_launch": 126000987, "shape": "all launches of a c2 step"}
 
 
 def kernel_sha() -> str:
@@ -248,11 +249,13 @@ def run_reference(args):
 
 def make_store(model, wl, extra_positions=0):
     """A store sized for the workload: its chunks, one private block per chunk per request and
-    the query pages (with slack), every request's positions."""
+    the query pages (with slack), every request's positions, and rows for a compile call of 4
+    chunks behind their dummy prefix (LegoLink-0)."""
     from position_independent_kv_link_gb300 import PicStore
     n_pos = max(sum(len(wl.chunks[c]) for c in r.chunk_ids) + len(r.query) for r in wl.requests)
     n_blocks = sum(-(-len(c) // 16) for c in wl.chunks) + 4 * (wl.selected_rows // 16 + 2 * len(wl.requests) * 10)
-    return PicStore(model, num_blocks=n_blocks, max_rows=max(wl.selected_rows, 2048),
+    compile_rows = max(sum(len(c) + wl.n_dummy for c in wl.chunks[i:i + 4]) for i in range(0, len(wl.chunks), 4))
+    return PicStore(model, num_blocks=n_blocks, max_rows=max(wl.selected_rows, compile_rows, 2048),
                     max_requests=max(len(wl.requests), 64), max_positions=n_pos + 80 + extra_positions,
                     max_logit_rows=max(64, len(wl.requests)))
 
@@ -685,6 +688,45 @@ def run_decode(args):
     return 0
 
 
+def run_link_only(args):
+    """Link steps only (for launch lists and per-kernel captures): compile the workload's chunks,
+    then W warm-up and K timed pic_link calls; prints the event-timed step and the launches per
+    step. --layers sets the model depth of this run (the 8B width is kept), so that a capture of
+    every kernel of a step holds a few GB instead of 16."""
+    from position_independent_kv_link_gb300 import PicModel
+    torch.cuda.set_device(0)
+    spec = workload(args.config).spec
+    if args.layers:
+        spec = spec.with_layers(args.layers)
+    wl = pi.config_workloads(spec)[args.config]
+    model = PicModel(spec, pi.gen_weights(spec))
+    store = make_store(model, wl)
+    cids = compile_all(store, wl)
+    reqs = [([cids[c] for c in r.chunk_ids], r.query) for r in wl.requests]
+
+    def step():
+        res = store.link(reqs, wl.k)
+        for r in res.requests:
+            store.release_request(r)
+    for _ in range(max(1, args.warmup)):
+        step()
+    store.sync()
+    n0 = store.launch_count()
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    store.sync()
+    ms = e0.elapsed_time(e1) / args.steps
+    print(json.dumps({"kernel": "link", "workload": wl.name, "layers": spec.n_layers, "ms_per_step": ms,
+                      "launches_per_step": (store.launch_count() - n0) / args.steps, "steps": args.steps,
+                      "warmup": max(1, args.warmup)}), flush=True)
+    return 0
+
+
 def run_kernel(args):
     """Times one kernel-level call at its shape in the 8B link (for ncu captures and sweeps).
 
@@ -767,18 +809,21 @@ def main():
     ap.add_argument("--cpu-layers", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", action="store_true", help="skip the other configurations' link measurements")
-    ap.add_argument("--kernel", choices=["gemm", "attention", "decode", "compile"], default=None,
+    ap.add_argument("--kernel", choices=["gemm", "attention", "decode", "compile", "link"], default=None,
                     help="time one kernel-level call at its 8B link shape instead of the link step "
                          "(decode: decode steps after one link of --config; compile: calls of 4 x 512-token "
                          "chunks)")
     ap.add_argument("--shape", default=None, help="gemm N,K,T for --kernel gemm (default 28672,4096,224); "
                                                   "attention n_chunks,k,query_len of 512-token chunks (default 10,16,64)")
     ap.add_argument("--unpacked", action="store_true", help="--kernel gemm on the plain [N][K] layout")
+    ap.add_argument("--layers", type=int, default=0, help="--kernel link: model depth of the run (8B width kept)")
     args = ap.parse_args()
     if args.kernel == "decode":
         return run_decode(args)
     if args.kernel == "compile":
         return run_compile(args)
+    if args.kernel == "link":
+        return run_link_only(args)
     if args.kernel:
         return run_kernel(args)
     if args.impl == "reference":

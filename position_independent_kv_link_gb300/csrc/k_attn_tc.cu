@@ -307,7 +307,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
   fence_before();
   __syncthreads();
   fence_after();
-  pdl_enter();   // the setup above overlaps the previous kernel; everything below reads its outputs
+  // Programmatic dependent launch: the next kernel may launch now (it waits for this one's
+  // completion before reading its outputs). This kernel's own reads of the previous kernels'
+  // outputs (the rotated q, the K/V pages) come after griddepcontrol.wait in the roles that make
+  // them; the work plan, page tables and cos/sin table are written before the forward starts and
+  // are read earlier, overlapping the previous kernel's tail.
+  asm volatile("griddepcontrol.launch_dependents;");
   const uint32_t tmem = *tmem_slot;
 
   if (warp < kSoftmaxWarps) {
@@ -331,12 +336,21 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     };
     uint32_t gt = 0, ct = 0;   // key tiles of the CTA; key tiles of this MMA tile
     bool ok = true;
+    const int row = RB * t + r;
+    // the next item and this row's position in it are fetched an item ahead
+    AttnItem it_n{};
+    int qp_n = -1;
+    if (blockIdx.x < a.n_items) {
+      it_n = a.items[blockIdx.x];
+      qp_n = row < it_n.nrows ? a.q_pos[it_n.row0 + row] : -1;
+    }
+    asm volatile("griddepcontrol.wait;" ::: "memory");   // q16 is written by the previous kernel
     for (int ii = blockIdx.x; ii < a.n_items; ii += gridDim.x) {
-      const AttnItem it = a.items[ii];
+      const AttnItem it = it_n;
+      const int qp = qp_n;
+      if (ii + (int)gridDim.x < a.n_items) it_n = a.items[ii + gridDim.x];
       const int nt = item_tiles(it), na = item_tiles_of(it, t);
-      const int row = RB * t + r;
       const bool mine = row < it.nrows;
-      const int qp = mine ? a.q_pos[it.row0 + row] : -1;
       if (na > 0) {
         // this row's q (128 fp16, rotated and scaled) into the K-major, 128-byte-swizzled A
         // operand of the S products: MMA row m = hh * 32 + r, dims 8c..8c+7 of half h at
@@ -467,6 +481,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         ++ct;
       }
       if (!ok) break;
+      if (ii + (int)gridDim.x < a.n_items) qp_n = row < it_n.nrows ? a.q_pos[it_n.row0 + row] : -1;
       // ---- drain O_t: normalized output, or the unnormalized partial with its reference max and sum
       bool okd = true;
       if (na > 0) {
@@ -569,6 +584,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
             ok = false;
             break;
           }
+          __nanosleep(64);   // leave the issue slots of this sub-partition to the softmax and transform
         }
         for (int t = 0; t < MT; ++t)
           if (na[t] > 0) {
@@ -729,6 +745,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
           pos[q] = __shfl_sync(0xffffffffu, cpos, p0 - w0 + q);
           len[q] = q < np ? __shfl_sync(0xffffffffu, clen, p0 - w0 + q) : 0;
         }
+        if (gt == 0) asm volatile("griddepcontrol.wait;" ::: "memory");   // the pages are written by earlier kernels
         // stage s free once every PV of key tile gt - NST has retired
         if (lane == 0) ok = !s_abort && (kr == 0 || mbar_wait(bar(B_EMPTY + s), (kr - 1) & 1));
         ok = __shfl_sync(0xffffffffu, ok, 0);
