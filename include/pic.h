@@ -176,6 +176,35 @@ pic_status pic_chunk_import(pic_store* s, const int32_t* tokens, int32_t n_token
 pic_status pic_link(pic_store* s, const pic_link_request* reqs, int32_t n_reqs, int32_t k, int32_t all_logits,
                     float* hidden_out, float* logits_out, pic_stream_t stream, pic_request* out_requests);
 
+/* link with dynamic (attention-based) token selection -- the CacheBlend-r step the EPIC pages
+ * compare LegoLink's static choice against (EPIC summary page: problem statement; Measured
+ * effects table, CacheBlend-r rows and the static-vs-dynamic row). Per request, with N prompt
+ * tokens (the chunks' total length) and query_len query tokens:
+ *   1. score: the query rows' layer-0 q and k are computed (embedding, RMSNorm, QKV
+ *      projection); each query row and head attends causally, RoPE at absolute positions,
+ *      over the prompt's compiled layer-0 K (nothing recomputed) and the query's own k; a
+ *      prompt token's score is the sum of the softmax weights it receives over all query rows
+ *      and heads (fp32);
+ *   2. choose: the floor(r_percent * N / 100) tokens with the largest scores, equal scores
+ *      taken in ascending position order;
+ *   3. link: as pic_link, with the chosen tokens in place of each chunk's first k: every
+ *      chunk block holding a chosen token becomes a private copy (per request, per chunk in
+ *      order, ascending block order, lowest free ids first), then the query blocks; the
+ *      chosen rows and the query run through every layer.
+ * r_percent = 0 recomputes only the query (naive reuse); r_percent = 100 recomputes every
+ * token (full recompute). The chosen positions are the request's selected list
+ * (pic_request_get_info), followed by the query positions. Steps 1-2 run on the stream and
+ * the call waits for them (the plan of step 3 needs the choice); step 3 is asynchronous as
+ * in pic_link. Scoring is skipped when the choice does not depend on it (every request keeps
+ * none or all of its tokens) and scores_out is NULL.
+ * scores_out: NULL, or a device fp32 array of sum(N) that receives every request's token
+ * scores in order. Capacities as pic_link (sum of kept tokens + query rows <= max_rows);
+ * PIC_ERR_CAPACITY also when the scoring scratch (2 x query rows x n_heads + sum(N) floats,
+ * the latter only when scores_out is NULL) exceeds max_rows x 2 x ffn_dim floats. */
+pic_status pic_link_dynamic(pic_store* s, const pic_link_request* reqs, int32_t n_reqs, int32_t r_percent,
+                            int32_t all_logits, float* hidden_out, float* logits_out, float* scores_out,
+                            pic_stream_t stream, pic_request* out_requests);
+
 /* decode: one generated token per linked request, after its link -- the step that turns the
  * linked prompt into output tokens (time to first token ends at the link's logits; EPIC
  * summary page, Measured effects table). For each i, host token tokens[i] is appended to
@@ -269,7 +298,8 @@ enum {
   PIC_PROF_ROWWISE = 2,    /* embedding/norm, split-K epilogues, SwiGLU */
   PIC_PROF_COPY = 3,       /* request-private block copies, KV import, accumulator zeroing */
   PIC_PROF_GEMM_GATE_UP = 4, /* the MLP gate/up projection GEMM (the largest weight stream) */
-  PIC_PROF_CLASSES = 5
+  PIC_PROF_SELECT = 5,     /* dynamic selection: token scoring and top-r choice */
+  PIC_PROF_CLASSES = 6
 };
 typedef struct {
   int64_t launches[PIC_PROF_CLASSES];  /* kernel launches recorded while profiling */

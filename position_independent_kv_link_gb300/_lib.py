@@ -40,7 +40,7 @@ class RequestInfo(C.Structure):
                 ("private_blocks", C.POINTER(C.c_int32))]
 
 
-PROF_CLASSES = 5
+PROF_CLASSES = 6
 
 
 class CacheStats(C.Structure):
@@ -75,6 +75,7 @@ SIGNATURES = {
     "pic_store_evict": (I32, [P, I32, PI32]),
     "pic_chunk_import": (I32, [P, PI32, I32, P, P, P, PI32]),
     "pic_link": (I32, [P, C.POINTER(LinkRequest), I32, I32, I32, P, P, P, PI32]),
+    "pic_link_dynamic": (I32, [P, C.POINTER(LinkRequest), I32, I32, I32, P, P, P, P, PI32]),
     "pic_decode": (I32, [P, PI32, PI32, I32, P, P, P, PI32, PI32]),
     "pic_request_get_info": (I32, [P, I32, C.POINTER(RequestInfo)]),
     "pic_chunk_get_blocks": (I32, [P, I32, PI32, C.POINTER(PI32)]),

@@ -125,6 +125,7 @@ class PicStore:
                                           C.byref(h)))
         self.handle = h
         self.max_logit_rows = max_logit_rows
+        self._chunk_len = {}   # chunk handle -> tokens (sizes the optional scores output)
 
     # -- compile / import
     def compile(self, chunks: Sequence[np.ndarray], n_dummy: int = 0, stream=None) -> List[int]:
@@ -134,6 +135,7 @@ class PicStore:
         out = np.zeros(len(toks), dtype=np.int32)
         L.check(self.lib.pic_compile(self.handle, ptrs, _ptr_i32(lens), len(toks), n_dummy, _stream(stream),
                                      _ptr_i32(out)))
+        self._chunk_len.update(zip(out.tolist(), (len(t) for t in toks)))
         return out.tolist()
 
     def import_chunk(self, tokens: np.ndarray, k: torch.Tensor, v: torch.Tensor, stream=None) -> int:
@@ -144,12 +146,11 @@ class PicStore:
         out = np.zeros(1, dtype=np.int32)
         L.check(self.lib.pic_chunk_import(self.handle, _ptr_i32(t), len(t), k.data_ptr(), v.data_ptr(),
                                           _stream(stream), _ptr_i32(out)))
+        self._chunk_len[int(out[0])] = len(t)
         return int(out[0])
 
     # -- link
-    def link(self, requests: Sequence[Tuple[Sequence[int], np.ndarray]], k: int, all_logits: bool = False,
-             stream=None, hidden_out: Optional[torch.Tensor] = None,
-             logits_out: Optional[torch.Tensor] = None) -> LinkResult:
+    def _link_args(self, requests, all_logits, hidden_out, logits_out):
         cfg = self.model.cfg
         keep = []
         reqs = (L.LinkRequest * len(requests))()
@@ -167,9 +168,34 @@ class PicStore:
             logits_out = torch.empty((n_lg, cfg.vocab), dtype=torch.float32, device=dev)
         assert hidden_out.shape == (n_q, cfg.d_model) and hidden_out.dtype == torch.float32
         assert logits_out.shape == (n_lg, cfg.vocab) and logits_out.dtype == torch.float32
+        return reqs, keep, hidden_out, logits_out
+
+    def link(self, requests: Sequence[Tuple[Sequence[int], np.ndarray]], k: int, all_logits: bool = False,
+             stream=None, hidden_out: Optional[torch.Tensor] = None,
+             logits_out: Optional[torch.Tensor] = None) -> LinkResult:
+        """pic_link (LegoLink-k): the first k tokens of every chunk and the query recomputed."""
+        reqs, keep, hidden_out, logits_out = self._link_args(requests, all_logits, hidden_out, logits_out)
         out = np.zeros(len(requests), dtype=np.int32)
         L.check(self.lib.pic_link(self.handle, reqs, len(requests), k, int(all_logits), hidden_out.data_ptr(),
                                   logits_out.data_ptr(), _stream(stream), _ptr_i32(out)))
+        return LinkResult(hidden_out, logits_out, out.tolist())
+
+    def link_dynamic(self, requests: Sequence[Tuple[Sequence[int], np.ndarray]], r_percent: int,
+                     all_logits: bool = False, stream=None, hidden_out: Optional[torch.Tensor] = None,
+                     logits_out: Optional[torch.Tensor] = None, scores_out: Optional[torch.Tensor] = None
+                     ) -> LinkResult:
+        """pic_link_dynamic (CacheBlend-r): the r % prompt tokens the query attends to most at
+        layer 0, and the query, recomputed. scores_out: optional device fp32 [sum of prompt
+        lengths] receiving the token scores."""
+        reqs, keep, hidden_out, logits_out = self._link_args(requests, all_logits, hidden_out, logits_out)
+        if scores_out is not None:
+            n_tok = sum(self._chunk_len[c] for cids, _ in requests for c in cids)
+            assert scores_out.shape == (n_tok,) and scores_out.dtype == torch.float32 and scores_out.is_cuda
+        out = np.zeros(len(requests), dtype=np.int32)
+        L.check(self.lib.pic_link_dynamic(self.handle, reqs, len(requests), int(r_percent), int(all_logits),
+                                          hidden_out.data_ptr(), logits_out.data_ptr(),
+                                          scores_out.data_ptr() if scores_out is not None else None,
+                                          _stream(stream), _ptr_i32(out)))
         return LinkResult(hidden_out, logits_out, out.tolist())
 
     def compile_cached(self, chunks: Sequence[np.ndarray], n_dummy: int = 0, stream=None):
@@ -182,6 +208,7 @@ class PicStore:
         hits = np.zeros(len(toks), dtype=np.int32)
         L.check(self.lib.pic_compile_cached(self.handle, ptrs, _ptr_i32(lens), len(toks), n_dummy, _stream(stream),
                                             _ptr_i32(out), _ptr_i32(hits)))
+        self._chunk_len.update(zip(out.tolist(), (len(t) for t in toks)))
         return out.tolist(), hits.astype(bool).tolist()
 
     def cache_stats(self) -> Dict[str, int]:
@@ -248,7 +275,7 @@ class PicStore:
         """Per kernel class: launches, summed event ms, algorithmic bytes and FLOPs."""
         p = L.Profile()
         L.check(self.lib.pic_profile_end(self.handle, C.byref(p)))
-        names = ["gemm", "attention", "rowwise", "copy", "gemm_gate_up"]
+        names = ["gemm", "attention", "rowwise", "copy", "gemm_gate_up", "select"]
         out = {n: {"launches": int(p.launches[i]), "ms": p.ms[i], "bytes": p.bytes[i], "flops": p.flops[i]}
                for i, n in enumerate(names)}
         out["total_launches"] = int(p.total_launches)

@@ -514,6 +514,121 @@ bool valid_tokens(const int32_t* t, int n, int vocab) {
   return true;
 }
 
+// Per request, per chunk: the chunk-local indices of the tokens a link recomputes, ascending.
+using Selection = std::vector<std::vector<int32_t>>;
+
+// Handles alive, tokens in range, linked lengths within max_positions.
+pic_status check_link_requests(pic_store* s, const pic_link_request* reqs, int32_t n_reqs) {
+  const auto& c = s->m->cfg;
+  if (n_reqs > s->cfg.max_requests) return fail(PIC_ERR_CAPACITY, "requests exceed max_requests");
+  for (int r = 0; r < n_reqs; ++r) {
+    const auto& q = reqs[r];
+    if (q.n_chunks < 0 || (q.n_chunks > 0 && !q.chunks) || q.query_len < 1 || !q.query)
+      return fail(PIC_ERR_INVALID_ARG, "invalid request");
+    if (!valid_tokens(q.query, q.query_len, c.vocab)) return fail(PIC_ERR_INVALID_ARG, "query token out of range");
+    long long len = q.query_len;
+    for (int i = 0; i < q.n_chunks; ++i) {
+      const Chunk* ch = s->live_chunk(q.chunks[i]);
+      if (!ch) return fail(PIC_ERR_INVALID_ARG, "unknown chunk handle");
+      len += (long long)ch->tokens.size();
+    }
+    if (len > s->cfg.max_positions) return fail(PIC_ERR_CAPACITY, "linked sequence exceeds max_positions");
+  }
+  return PIC_OK;
+}
+
+// The link proper (requests already checked): per request, in order, each chunk takes one new
+// block per block holding a recomputed token (copies of those shared blocks, in ascending
+// block order, lowest free ids first), then the query blocks; the recomputed rows and the
+// query run through every layer, writing their K/V into those blocks.
+pic_status link_selected(pic_store* s, const pic_link_request* reqs, int32_t n_reqs, const std::vector<Selection>& sels,
+                         int32_t all_logits, float* hidden_out, float* logits_out, cudaStream_t st,
+                         pic_request* out_requests) {
+  int need = 0;
+  long long rows = 0, lg_rows = 0;
+  for (int r = 0; r < n_reqs; ++r) {
+    for (const auto& sel : sels[r]) {
+      for (size_t t = 0; t < sel.size(); ++t)
+        if (!t || sel[t] / kBlock != sel[t - 1] / kBlock) ++need;
+      rows += (long long)sel.size();
+    }
+    need += ceil_div(reqs[r].query_len, kBlock);
+    rows += reqs[r].query_len;
+    lg_rows += all_logits ? reqs[r].query_len : 1;
+  }
+  if (rows > s->cfg.max_rows) return fail(PIC_ERR_CAPACITY, "selected rows exceed max_rows");
+  if (lg_rows > s->cfg.max_logit_rows) return fail(PIC_ERR_CAPACITY, "logit rows exceed max_logit_rows");
+  if (!s->reserve(need)) return fail(PIC_ERR_OUT_OF_BLOCKS, "not enough free blocks for link");
+
+  Batch b;
+  std::vector<Request> made(n_reqs);
+  for (int r = 0; r < n_reqs; ++r) {
+    const auto& q = reqs[r];
+    Request& R = made[r];
+    b.begin_seq();
+    int off = 0;
+    for (int i = 0; i < q.n_chunks; ++i) {
+      const Chunk& ch = s->chunks[q.chunks[i]];
+      const std::vector<int32_t>& sel = sels[r][i];
+      const int L = (int)ch.tokens.size();
+      std::vector<int> mine, owner(ch.blocks.size(), -1);   // chunk blocks made private, their new copy
+      for (int32_t t : sel)
+        if (mine.empty() || mine.back() != t / kBlock) mine.push_back(t / kBlock);
+      std::vector<int32_t> own = s->take((int)mine.size());
+      for (size_t m = 0; m < mine.size(); ++m) {
+        owner[mine[m]] = (int)m;
+        b.copy_pairs.push_back(ch.blocks[mine[m]]);
+        b.copy_pairs.push_back(own[m]);
+      }
+      R.private_blocks.insert(R.private_blocks.end(), own.begin(), own.end());
+      for (int j = 0; j < (int)ch.blocks.size(); ++j) {
+        const int blk = owner[j] >= 0 ? own[owner[j]] : ch.blocks[j];
+        R.page_table.push_back(blk);
+        R.page_pos.push_back(off + kBlock * j);
+        R.page_len.push_back(std::min(kBlock, L - kBlock * j));
+        b.page(blk, off + kBlock * j, std::min(kBlock, L - kBlock * j));
+      }
+      for (int32_t t : sel) {
+        const int slot = own[owner[t / kBlock]] * kBlock + t % kBlock;
+        R.selected.push_back(off + t);
+        R.slots.push_back(slot);
+        b.row(ch.tokens[t], off + t, slot);
+      }
+      R.chunk_ids.push_back(q.chunks[i]);
+      off += L;
+    }
+    std::vector<int32_t> qb = s->take(ceil_div(q.query_len, kBlock));
+    R.private_blocks.insert(R.private_blocks.end(), qb.begin(), qb.end());
+    for (int j = 0; j < (int)qb.size(); ++j) {
+      R.page_table.push_back(qb[j]);
+      R.page_pos.push_back(off + kBlock * j);
+      R.page_len.push_back(std::min(kBlock, q.query_len - kBlock * j));
+      b.page(qb[j], off + kBlock * j, std::min(kBlock, q.query_len - kBlock * j));
+    }
+    for (int t = 0; t < q.query_len; ++t) {
+      const int slot = qb[t / kBlock] * kBlock + t % kBlock;
+      R.selected.push_back(off + t);
+      R.slots.push_back(slot);
+      b.row(q.query[t], off + t, slot);
+      b.out_row.back() = b.n_hidden++;
+      if (all_logits || t == q.query_len - 1) b.lg_row.back() = b.n_lg++;
+    }
+    b.end_seq();
+  }
+  pic_status e = run_forward(s, b, hidden_out, logits_out, st);
+  if (e != PIC_OK) {
+    for (auto& R : made) s->give(R.private_blocks);
+    return e;
+  }
+  for (int r = 0; r < n_reqs; ++r) {
+    for (int32_t cid : made[r].chunk_ids) s->chunks[cid].refs++;
+    const int id = s->next_request++;
+    s->requests[id] = std::move(made[r]);
+    out_requests[r] = id;
+  }
+  return PIC_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -887,96 +1002,159 @@ pic_status pic_link(pic_store* s, const pic_link_request* reqs, int32_t n_reqs, 
                     float* hidden_out, float* logits_out, pic_stream_t stream, pic_request* out_requests) {
   if (!s || !reqs || n_reqs < 1 || k < 0 || !hidden_out || !logits_out || !out_requests)
     return fail(PIC_ERR_INVALID_ARG, "invalid link arguments");
-  const auto& c = s->m->cfg;
-  if (n_reqs > s->cfg.max_requests) return fail(PIC_ERR_CAPACITY, "requests exceed max_requests");
-  // validate and count blocks (nothing is allocated before every check passes)
-  int need = 0;
-  long long rows = 0, lg_rows = 0;
-  for (int r = 0; r < n_reqs; ++r) {
-    const auto& q = reqs[r];
-    if (q.n_chunks < 0 || (q.n_chunks > 0 && !q.chunks) || q.query_len < 1 || !q.query)
-      return fail(PIC_ERR_INVALID_ARG, "invalid request");
-    if (!valid_tokens(q.query, q.query_len, c.vocab)) return fail(PIC_ERR_INVALID_ARG, "query token out of range");
-    long long len = q.query_len;
-    for (int i = 0; i < q.n_chunks; ++i) {
-      const Chunk* ch = s->live_chunk(q.chunks[i]);
-      if (!ch) return fail(PIC_ERR_INVALID_ARG, "unknown chunk handle");
-      const int L = (int)ch->tokens.size();
-      need += ceil_div(std::min(k, L), kBlock);
-      rows += std::min(k, L);
-      len += L;
+  pic_status e = check_link_requests(s, reqs, n_reqs);
+  if (e != PIC_OK) return e;
+  // LegoLink-k: the first min(k, L) tokens of every chunk
+  std::vector<Selection> sels(n_reqs);
+  for (int r = 0; r < n_reqs; ++r)
+    for (int i = 0; i < reqs[r].n_chunks; ++i) {
+      const int L = (int)s->chunks[reqs[r].chunks[i]].tokens.size();
+      std::vector<int32_t> first(std::min(k, L));
+      for (int t = 0; t < (int)first.size(); ++t) first[t] = t;
+      sels[r].push_back(std::move(first));
     }
-    if (len > s->cfg.max_positions) return fail(PIC_ERR_CAPACITY, "linked sequence exceeds max_positions");
-    need += ceil_div(q.query_len, kBlock);
-    rows += q.query_len;
-    lg_rows += all_logits ? q.query_len : 1;
-  }
-  if (rows > s->cfg.max_rows) return fail(PIC_ERR_CAPACITY, "selected rows exceed max_rows");
-  if (lg_rows > s->cfg.max_logit_rows) return fail(PIC_ERR_CAPACITY, "logit rows exceed max_logit_rows");
-  if (!s->reserve(need)) return fail(PIC_ERR_OUT_OF_BLOCKS, "not enough free blocks for link");
+  return link_selected(s, reqs, n_reqs, sels, all_logits, hidden_out, logits_out, (cudaStream_t)stream, out_requests);
+}
 
-  Batch b;
-  std::vector<Request> made(n_reqs);
+pic_status pic_link_dynamic(pic_store* s, const pic_link_request* reqs, int32_t n_reqs, int32_t r_percent,
+                            int32_t all_logits, float* hidden_out, float* logits_out, float* scores_out,
+                            pic_stream_t stream, pic_request* out_requests) {
+  if (!s || !reqs || n_reqs < 1 || r_percent < 0 || r_percent > 100 || !hidden_out || !logits_out || !out_requests)
+    return fail(PIC_ERR_INVALID_ARG, "invalid link arguments");
+  pic_status e = check_link_requests(s, reqs, n_reqs);
+  if (e != PIC_OK) return e;
+  const auto& c = s->m->cfg;
+  const int H = c.n_heads, G = c.n_kv_heads, D = c.head_dim;
+  cudaStream_t st = (cudaStream_t)stream;
+  // per request: prompt length, kept count floor(r N / 100), its query rows, pages and scores
+  std::vector<SelectReq> sr(n_reqs);
+  std::vector<int> tok, pblk, ppos, plen;
+  long long rows = 0;
+  bool partial = scores_out != nullptr;
   for (int r = 0; r < n_reqs; ++r) {
     const auto& q = reqs[r];
-    Request& R = made[r];
-    b.begin_seq();
-    int off = 0;
+    SelectReq& R = sr[r];
+    R.row0 = (int)tok.size();
+    R.lq = q.query_len;
+    R.page0 = (int)pblk.size();
+    R.tok0 = r ? sr[r - 1].tok0 + sr[r - 1].n_tok : 0;
+    R.out0 = r ? sr[r - 1].out0 + sr[r - 1].n_pick : 0;
+    int N = 0;
     for (int i = 0; i < q.n_chunks; ++i) {
       const Chunk& ch = s->chunks[q.chunks[i]];
-      const int L = (int)ch.tokens.size(), ki = std::min(k, L), mb = ceil_div(ki, kBlock);
-      std::vector<int32_t> own = s->take(mb);
-      R.private_blocks.insert(R.private_blocks.end(), own.begin(), own.end());
+      const int L = (int)ch.tokens.size();
       for (int j = 0; j < (int)ch.blocks.size(); ++j) {
-        const int blk = j < mb ? own[j] : ch.blocks[j];
-        R.page_table.push_back(blk);
-        R.page_pos.push_back(off + kBlock * j);
-        R.page_len.push_back(std::min(kBlock, L - kBlock * j));
-        b.page(blk, off + kBlock * j, std::min(kBlock, L - kBlock * j));
+        pblk.push_back(ch.blocks[j]);
+        ppos.push_back(N + kBlock * j);
+        plen.push_back(std::min(kBlock, L - kBlock * j));
       }
-      for (int j = 0; j < mb; ++j) {
-        b.copy_pairs.push_back(ch.blocks[j]);
-        b.copy_pairs.push_back(own[j]);
-      }
-      for (int t = 0; t < ki; ++t) {
-        const int slot = own[t / kBlock] * kBlock + t % kBlock;
-        R.selected.push_back(off + t);
-        R.slots.push_back(slot);
-        b.row(ch.tokens[t], off + t, slot);
-      }
-      R.chunk_ids.push_back(q.chunks[i]);
+      N += L;
+    }
+    R.n_tok = N;
+    R.n_pages = (int)pblk.size() - R.page0;
+    R.n_pick = (int)((long long)r_percent * N / 100);
+    partial |= R.n_pick > 0 && R.n_pick < N;
+    tok.insert(tok.end(), q.query, q.query + q.query_len);
+    rows += R.n_pick + q.query_len;
+  }
+  if (rows > s->cfg.max_rows) return fail(PIC_ERR_CAPACITY, "selected rows exceed max_rows");
+  const int n_rows = (int)tok.size();
+  const int n_tok = sr.back().tok0 + sr.back().n_tok, n_out = sr.back().out0 + sr.back().n_pick;
+
+  std::vector<Selection> sels(n_reqs);
+  auto split = [&](int r, const int32_t* chosen) {   // ascending prompt positions -> per chunk
+    int at = 0, off = 0;
+    for (int i = 0; i < reqs[r].n_chunks; ++i) {
+      const int L = (int)s->chunks[reqs[r].chunks[i]].tokens.size();
+      std::vector<int32_t> mine;
+      for (; at < sr[r].n_pick && chosen[at] < off + L; ++at) mine.push_back(chosen[at] - off);
+      sels[r].push_back(std::move(mine));
       off += L;
     }
-    std::vector<int32_t> qb = s->take(ceil_div(q.query_len, kBlock));
-    R.private_blocks.insert(R.private_blocks.end(), qb.begin(), qb.end());
-    for (int j = 0; j < (int)qb.size(); ++j) {
-      R.page_table.push_back(qb[j]);
-      R.page_pos.push_back(off + kBlock * j);
-      R.page_len.push_back(std::min(kBlock, q.query_len - kBlock * j));
-      b.page(qb[j], off + kBlock * j, std::min(kBlock, q.query_len - kBlock * j));
+  };
+  if (!partial) {
+    // nothing or everything kept: the choice needs no scores
+    for (int r = 0; r < n_reqs; ++r) {
+      std::vector<int32_t> all(sr[r].n_pick);
+      for (int u = 0; u < sr[r].n_pick; ++u) all[u] = u;
+      split(r, all.data());
     }
-    for (int t = 0; t < q.query_len; ++t) {
-      const int slot = qb[t / kBlock] * kBlock + t % kBlock;
-      R.selected.push_back(off + t);
-      R.slots.push_back(slot);
-      b.row(q.query[t], off + t, slot);
-      b.out_row.back() = b.n_hidden++;
-      if (all_logits || t == q.query_len - 1) b.lg_row.back() = b.n_lg++;
+  } else {
+    // the scoring pass: layer-0 q, k of the query rows, then every prompt token's score
+    const size_t qkv = s->m->qkv_dim();
+    const size_t ml_floats = (size_t)n_rows * H * 2, sc_floats = scores_out ? 0 : (size_t)n_tok;
+    if (ml_floats + sc_floats > (size_t)s->cfg.max_rows * 2 * c.ffn_dim)
+      return fail(PIC_ERR_CAPACITY, "prompt tokens exceed the scoring workspace");
+    const size_t n_int = tok.size() + 3 * pblk.size() + (size_t)kSelectReqInts * n_reqs + n_out;
+    if (n_int > s->meta_cap) return fail(PIC_ERR_CAPACITY, "metadata exceeds workspace");
+    if (s->meta_ev_pending) {
+      PIC_CUDA(cudaEventSynchronize(s->meta_ev));
+      s->meta_ev_pending = false;
     }
-    b.end_seq();
+    int32_t* hp = s->meta_h;
+    size_t o = 0;
+    auto put = [&](const void* src, size_t n) {
+      if (n) std::memcpy(hp + o, src, n * 4);
+      const size_t at = o;
+      o += n;
+      return s->meta_d + at;
+    };
+    const int* d_tok = put(tok.data(), tok.size());
+    const int* d_pblk = put(pblk.data(), pblk.size());
+    const int* d_ppos = put(ppos.data(), ppos.size());
+    const int* d_plen = put(plen.data(), plen.size());
+    const SelectReq* d_req = (const SelectReq*)put(sr.data(), (size_t)kSelectReqInts * n_reqs);
+    const size_t o_chosen = o;
+    PIC_CUDA(cudaMemcpyAsync(s->meta_d, hp, o * 4, cudaMemcpyHostToDevice, st));
+    const int es = (int)dtype_size(c.dtype);
+    {
+      Rec rc(s, st, PIC_PROF_ROWWISE, (double)n_rows * c.d_model * (es + 4 + es), 0, 1);
+      launch_embed_norm(c.dtype, n_rows, c.d_model, s->m->embed, d_tok, s->m->attn_norm[0], c.rms_eps, s->h, s->x,
+                        st);
+    }
+    {
+      const bool pk = !s->m->pqkv.empty();
+      const bool zero_kernel = !(pk && tc_gemm_tiles((int)qkv, n_rows) <= s->tile_ready_cap);
+      Rec rc(s, st, PIC_PROF_GEMM, (double)qkv * c.d_model * es + (double)n_rows * (c.d_model * es + qkv * 8),
+             2.0 * qkv * c.d_model * n_rows, 1 + (zero_kernel ? 1 : 0));
+      if ((e = gemm(s, s->m->wqkv[0], pk ? s->m->pqkv[0] : nullptr, s->x, s->qkv_acc, (int)qkv, c.d_model, n_rows, st,
+                    true)) != PIC_OK)
+        return e;
+    }
+    SelectArgs a{};
+    a.reqs = d_req;
+    a.n_reqs = n_reqs;
+    a.n_rows = n_rows;
+    a.n_tok = n_tok;
+    a.H = H;
+    a.G = G;
+    a.qkv = s->qkv_acc;
+    a.k_layer0 = s->k_layer(0);
+    a.page_block = d_pblk;
+    a.page_pos = d_ppos;
+    a.page_len = d_plen;
+    a.rope_cs = s->rope_cs;
+    a.qrot = s->q;
+    a.ml = s->gu_acc;
+    a.scores = scores_out ? scores_out : s->gu_acc + ml_floats;
+    a.chosen = s->meta_d + o_chosen;
+    {
+      double pairs = 0;   // (query row, key) pairs scored twice, once per pass
+      for (const SelectReq& R : sr) pairs += (double)R.lq * R.n_tok + (double)R.lq * (R.lq + 1) / 2;
+      Rec rc(s, st, PIC_PROF_SELECT, 2.0 * n_tok * G * D * es + (double)n_rows * H * D * 8, pairs * H * D * 4.0 * 2, 3);
+      if ((e = launch_select(a, D, c.dtype, st)) != PIC_OK) return e;
+    }
+    if (n_out) PIC_CUDA(cudaMemcpyAsync(hp + o_chosen, a.chosen, (size_t)n_out * 4, cudaMemcpyDeviceToHost, st));
+    PIC_CUDA(cudaStreamSynchronize(st));
+    for (int r = 0; r < n_reqs; ++r) {
+      const int32_t* ch = hp + o_chosen + sr[r].out0;
+      for (int i = 0; i < sr[r].n_pick; ++i)
+        if (ch[i] < 0 || ch[i] >= sr[r].n_tok || (i && ch[i] <= ch[i - 1]))
+          return fail(PIC_ERR_CUDA, "token selection returned an invalid position list");
+      split(r, ch);
+    }
   }
-  pic_status e = run_forward(s, b, hidden_out, logits_out, (cudaStream_t)stream);
-  if (e != PIC_OK) {
-    for (auto& R : made) s->give(R.private_blocks);
-    return e;
-  }
-  for (int r = 0; r < n_reqs; ++r) {
-    for (int32_t cid : made[r].chunk_ids) s->chunks[cid].refs++;
-    const int id = s->next_request++;
-    s->requests[id] = std::move(made[r]);
-    out_requests[r] = id;
-  }
-  return PIC_OK;
+  return link_selected(s, reqs, n_reqs, sels, all_logits, hidden_out, logits_out, st, out_requests);
 }
 
 pic_status pic_decode(pic_store* s, const pic_request* reqs, const int32_t* tokens, int32_t n_reqs,
