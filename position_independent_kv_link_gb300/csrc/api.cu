@@ -158,8 +158,11 @@ struct pic_store {
   int32_t* meta_d = nullptr;
   size_t meta_cap = 0;  // int32 elements
   float2* rope_cs = nullptr;
-  std::vector<CUtensorMap> kv_maps;  // per layer: K, V (4-block boxes), K, V (1-page boxes); built on first use
-  CUtensorMap cs_map;                // rows of the cos/sin table (with kv_maps)
+  std::vector<CUtensorMap> v_maps;   // per layer: V pool boxes of 4 blocks, of 1 block; built on first use
+  // rotated K of every page of a forward, one layer at a time (tensor-core attention): grown
+  // on first need to the largest page count seen
+  __half* krot = nullptr;
+  int krot_pages = 0;
   int32_t* meta_h = nullptr;  // pinned staging
   cudaEvent_t meta_ev = nullptr;
   bool meta_ev_pending = false;
@@ -395,24 +398,36 @@ pic_status run_forward_impl(pic_store* s, const Batch& b, float* hidden_out, flo
   const double att_bytes = att_kv_bytes + 2 * dT * dHD * es;
   const double att_flops = att_pairs * H * D * 4.0;
   const int att_launches = 1 + (combs.empty() ? 0 : 1);
+  // the K rotation of the tensor-core path: every page's K read, rotated K written
+  const double rot_bytes = 2.0 * (double)P * G * kBlock * D * 2;
 
   AttnArgs aa{};
   const bool att_tc = attention_persistent(dt, D, H / G);
+  const int n_pages = (int)P;
   if (att_tc) {
-    if (s->kv_maps.empty()) {
-      s->kv_maps.resize(4 * (size_t)c.n_layers);
+    if (s->v_maps.empty()) {
+      s->v_maps.resize(2 * (size_t)c.n_layers);
       for (int l = 0; l < c.n_layers; ++l)
-        if (!attn_kv_map(&s->kv_maps[4 * l], &s->kv_maps[4 * l + 2], s->k_layer(l), s->blocks_total(), G) ||
-            !attn_kv_map(&s->kv_maps[4 * l + 1], &s->kv_maps[4 * l + 3], s->v_layer(l), s->blocks_total(), G)) {
-          s->kv_maps.clear();
-          return fail(PIC_ERR_CUDA, "cuTensorMapEncodeTiled failed for the KV pools");
+        if (!attn_v_map(&s->v_maps[2 * l], &s->v_maps[2 * l + 1], s->v_layer(l), s->blocks_total(), G)) {
+          s->v_maps.clear();
+          return fail(PIC_ERR_CUDA, "cuTensorMapEncodeTiled failed for the V pools");
         }
-      if (!attn_cs_map(&s->cs_map, s->rope_cs, std::max(16, s->cfg.max_positions))) {
-        s->kv_maps.clear();
-        return fail(PIC_ERR_CUDA, "cuTensorMapEncodeTiled failed for the cos/sin table");
-      }
     }
-    aa.csmap = s->cs_map;
+    if (n_pages > s->krot_pages) {
+      // cudaFree waits for the kernels still reading the old scratch
+      const int want = std::max(n_pages, s->krot_pages + s->krot_pages / 4);
+      __half* fresh = nullptr;
+      PIC_CUDA(cudaFree(s->krot));
+      s->krot = nullptr;
+      s->krot_pages = 0;
+      PIC_CUDA(cudaMalloc(&fresh, attention_krot_bytes(want, G)));
+      s->krot = fresh;
+      s->krot_pages = want;
+    }
+    if (!attn_krot_map(&aa.kmap, s->krot, std::max(1, n_pages), G))
+      return fail(PIC_ERR_CUDA, "cuTensorMapEncodeTiled failed for the rotated-K scratch");
+    aa.krot = s->krot;
+    aa.n_pages = n_pages;
     aa.q16 = (const __half*)s->q;   // written rotated and scaled by the QKV epilogue
   }
   aa.dtype = dt;
@@ -465,10 +480,10 @@ pic_status run_forward_impl(pic_store* s, const Batch& b, float* hidden_out, flo
     aa.k_layer = s->k_layer(l);
     aa.v_layer = s->v_layer(l);
     if (att_tc) {
-      aa.kmap = s->kv_maps[4 * l];
-      aa.vmap = s->kv_maps[4 * l + 1];
-      aa.kmap1 = s->kv_maps[4 * l + 2];
-      aa.vmap1 = s->kv_maps[4 * l + 3];
+      aa.vmap = s->v_maps[2 * l];
+      aa.vmap1 = s->v_maps[2 * l + 1];
+      Rec r(s, st, PIC_PROF_ATTENTION, rot_bytes, 0, 1);
+      launch_rope_k(n_pages, G, d_pblk, d_ppos, d_plen, s->k_layer(l), s->rope_cs, s->krot, st);
     }
     {
       Rec r(s, st, PIC_PROF_ATTENTION, att_bytes, att_flops, att_launches);
@@ -818,6 +833,7 @@ pic_status pic_store_destroy(pic_store* s) {
     cudaEventDestroy(s->meta_ev);
   }
   cudaFree(s->ws);
+  cudaFree(s->krot);
   cudaFreeHost(s->meta_h);
   delete s;
   return PIC_OK;

@@ -1,45 +1,44 @@
 // tcgen05 paged attention with fused RoPE for bf16 KV, head_dim 128, 4 query heads per KV head.
 //
-// Persistent: CTA b walks the work items b, b + grid, b + 2 grid, ... (the planner deals them
-// in that order). An item is up to 64 consecutive query rows of one sequence x the 4 query
-// heads sharing KV head g x a run of pages. Its rows form two M = 128 MMA tiles: tile t holds
-// rows 32t..32t+31 of the item x the 4 heads (MMA row = head * 32 + row). Every 64-key tile
-// (4 pages) of K and V is loaded, rotated and converted ONCE and then feeds both MMA tiles,
-// which halves the per-row cost of the K rotation against items of 32 rows. Rows are in
-// ascending position order, so tile 0 sees no key beyond its own last row: it stops after the
-// key tiles holding pages [page0, page_mid) and the item's later key tiles run for tile 1
-// alone.
+// Two launches per layer. rope_k_kernel rotates the K of every page of the work by RoPE at each
+// row's absolute position (MEPIC abstract: K is kept without positional encoding and rotated at
+// attention time) into an fp16 scratch [pages][G][16][128] indexed by the work's page number,
+// rows beyond a page's length zero: each page is rotated once per layer however many work items
+// read it. attn_tc_kernel then reads the rotated K and the stored bf16 V straight into the MMA
+// operand layouts by TMA; nothing is converted on the way.
 //
-// Key tiles stream through a ring of 4 shared-memory stages. A stage holds K and V of 64 keys
-// exactly in the layout the MMAs read ([64-dim half][key][128 B], 128-byte swizzled): the load
-// warp fills each half with one TMA box over 4 consecutive pool blocks (pages of a chunk or a
-// query are allocated consecutively), or one box per page when they are not, plus the cos/sin
-// table rows of the page starts. The transform then rotates K and converts V to fp16 in place,
-// and the stage is free again once the PV products of its key tile have retired.
+// attn_tc_kernel is persistent: CTA b walks the work items b, b + grid, b + 2 grid, ... (the
+// planner deals them in that order). An item is up to 64 consecutive query rows of one sequence
+// x the 4 query heads sharing KV head g x a run of pages. Its rows form two M = 128 MMA tiles:
+// tile t holds rows 32t..32t+31 of the item x the 4 heads (MMA row = head * 32 + row). Every
+// 64-key tile (4 pages) of K and V feeds both MMA tiles. Rows are in ascending position order,
+// so tile 0 sees no key beyond its own last row: it stops after the key tiles holding pages
+// [page0, page_mid) and the item's later key tiles run for tile 1 alone.
 //
-//   warp 17     loads: K and V boxes and the cos/sin rows of each key tile (TMA), the page
-//               metadata (the warp's lanes hold a window of 32 pages, the next one prefetched).
-//   warps 8-15  transform, in place: K rotated by RoPE at each key's absolute position (MEPIC
-//               abstract: K is kept without positional encoding and RoPE is fused into
-//               attention) into fp16, V converted to fp16; rows without a key zeroed.
-//               cos/sin(p theta) is composed from the table row of the page start and that of
-//               the offset inside the page (the latter held in registers: each thread always
-//               rotates the same row offset and dims).
-//   warp 16     TMEM owner (all 512 columns: O_t at [128t, 128t + 128), two S buffers of tile t
+// Key tiles stream through a ring of 4 shared-memory stages, each K then V of 64 keys in the
+// layout the MMAs read ([64-dim half][key][128 B], 128-byte swizzled).
+//
+//   warp 9      loads: per key tile, rotated K as two boxes of 4 consecutive scratch pages (one per
+//               64-dim half) and V as two boxes over 4 consecutive pool blocks (pages of a chunk
+//               or a query are allocated consecutively), else one box per full page; a page with
+//               fewer than 16 rows is copied by the warp's lanes with its missing rows zeroed,
+//               and the V rows of pages past the item's end are zeroed (P is 0 there; V must be
+//               finite). The warp also writes each key's position (the causal mask) and holds the
+//               page metadata (its lanes hold a window of 32 pages, the next one prefetched).
+//   warp 8      TMEM owner (all 512 columns: O_t at [128t, 128t + 128), two S buffers of tile t
 //               at 256 + 128t + {0, 64}); one thread issues the S products S_t = Q_t K^T (M128
-//               N64 K128) of both MMA tiles, each as soon as its key tile is transformed and its
-//               S buffer free -- a key tile ahead of the softmax.
+//               N64 K128, fp16) of both MMA tiles, each as soon as its key tile has landed and
+//               its S buffer is free -- a key tile ahead of the softmax.
 //   warps 0-7   MMA tile t = warpgroup t, thread = one MMA row = one TMEM lane. The warpgroup
 //               writes the tile's Q rows into shared memory at the start of an item (the A
 //               operand of its S products); per key tile each thread reads its row of S, masks
 //               keys after its position (only on key tiles that need it), keeps a running
-//               reference maximum and writes P = 2^(S - ref) as fp16 pairs over the S columns,
-//               and the warpgroup's first thread then issues O_t += P_t V (M128 N128 K64, P_t
-//               from TMEM) at once. O in TMEM is rescaled only when the maximum grows by more
-//               than 2^8 (P stays <= 256, safe in fp16); the sum uses the same reference, so
-//               O / l is exact softmax. At the end of an item the warpgroup drains O_t
-//               (normalized output, or the unnormalized partial with its reference maximum and
-//               sum for the merge).
+//               reference maximum and writes P = 2^(S - ref) as bf16 pairs over the S columns,
+//               and the warpgroup's first thread then issues O_t += P_t V (M128 N128 K64, bf16,
+//               P_t from TMEM) at once. O in TMEM is rescaled only when the maximum grows by
+//               more than 2^8 (P stays <= 256); the sum uses the same reference, so O / l is
+//               exact softmax. At the end of an item the warpgroup drains O_t (normalized output,
+//               or the unnormalized partial with its reference maximum and sum for the merge).
 // Barrier phases run over the CTA's whole key-tile sequence (and per MMA tile over that tile's
 // own sequence), so the next item's loads overlap the current item's tail. Every wait is
 // bounded; on expiry the CTA raises the device timeout flag, stops issuing work, waits
@@ -65,9 +64,7 @@ constexpr int MT = 2;                     // MMA tiles per item (items of up to 
 constexpr int KT = 64;                    // keys per tile (4 pages)
 constexpr int NST = 4;                    // key-tile stages
 constexpr int kSoftmaxWarps = 4 * MT;
-constexpr int kTransformWarps = 8;
-constexpr int W_XF = kSoftmaxWarps;                 // first transform warp
-constexpr int W_MMA = W_XF + kTransformWarps, W_LOAD = W_MMA + 1;
+constexpr int W_MMA = kSoftmaxWarps, W_LOAD = W_MMA + 1;
 constexpr int kThreads = (W_LOAD + 1) * 32;
 constexpr float kRescale = 8.f;           // rescale O when the row max grows by more than 2^8
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
@@ -79,9 +76,7 @@ constexpr int Q_TILE = 32768;                     // one MMA tile of Q: 2 halves
 constexpr int ST_BYTES = 32768;                   // one key tile: K then V, each [2 halves][64 keys][128 B]
 constexpr int OFF_Q = 0;                          // [MT] Q tiles                              64 KB
 constexpr int OFF_ST = OFF_Q + MT * Q_TILE;       // [NST] key-tile stages                    128 KB
-constexpr int OFF_CS = OFF_ST + NST * ST_BYTES;   // [NST][4 pages][512 B] cos/sin rows         8 KB
-constexpr int OFF_TM = OFF_CS + NST * 2048;       // int [NST][4][2] page start, valid rows
-constexpr int OFF_POS = OFF_TM + NST * 32;        // int [NST][KT] key positions (INT_MAX = none)
+constexpr int OFF_POS = OFF_ST + NST * ST_BYTES;  // int [NST][KT] key positions (INT_MAX = none)
 constexpr int OFF_TILE = OFF_POS + NST * KT * 4;  // int [NST] last key position, INT_MAX if ragged
 constexpr int OFF_BAR = (OFF_TILE + NST * 4 + 7) / 8 * 8;
 constexpr int N_BARS = 32;
@@ -90,21 +85,21 @@ static_assert(SMEM_BYTES + 1024 <= 227 * 1024, "shared memory budget");
 
 // barrier slots ([t][b]: MMA tile t, S buffer b)
 constexpr int B_FULL = 0;                         // [NST] stage landed (TMA bytes + loader arrival)
-constexpr int B_XF = B_FULL + NST;                // [NST] stage transformed (transform warps)
-constexpr int B_EMPTY = B_XF + NST;               // [NST] both MMA tiles' PVs of the stage's key tile retired
+constexpr int B_EMPTY = B_FULL + NST;             // [NST] both MMA tiles' PVs of the stage's key tile retired
 constexpr int B_SFULL = B_EMPTY + NST;            // [2][2] S_t in buffer b computed (commit)
 constexpr int B_PVDONE = B_SFULL + 2 * MT;        // [2][2] O_t += P_t V of buffer b retired (commit)
 constexpr int B_QREADY = B_PVDONE + 2 * MT;       // [2] Q_t of the item written (warpgroup t)
 constexpr int B_DONE = B_QREADY + MT;             // [3] every MMA of an issuing thread retired
 static_assert(B_DONE + MT + 1 <= N_BARS, "barrier slots");
 // Every waiter must observe each phase of a barrier before the barrier can complete the next
-// one (a parity wait cannot tell phase n from n + 2). FULL has only the transform as waiter;
-// XF is waited on by the S issuer and both warpgroups, but a stage can only be refilled after
-// both warpgroups released it, i.e. after each has used that phase (a warpgroup releases a key
-// tile it takes no part in only after waiting for it, so its release never counts toward the
-// stage's previous use); EMPTY has only the loader. The S/PV/Q barriers of MMA tile t count
-// that tile's own key tiles and items: S_t into buffer b is issued only after the PV that read
-// buffer b's previous P retired, and the next item's first S_t only after Q_t was rewritten.
+// one (a parity wait cannot tell phase n from n + 2). FULL is waited on by the S issuer and
+// both warpgroups, but a stage can only be refilled after both warpgroups released it, i.e.
+// after each has used that phase (a warpgroup releases a key tile it takes no part in only
+// after waiting for it, so its release never counts toward the stage's previous use), and a
+// warpgroup uses a key tile only after the S issuer issued its S product; EMPTY has only the
+// loader. The S/PV/Q barriers of MMA tile t count that tile's own key tiles and items: S_t into
+// buffer b is issued only after the PV that read buffer b's previous P retired, and the next
+// item's first S_t only after Q_t was rewritten.
 
 __device__ int g_attn_timeout = 0;
 
@@ -250,17 +245,14 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
 }
-// bf16 pair -> fp16 pair (exact widening, one rounding)
-__device__ __forceinline__ uint32_t bf2_to_h2(uint32_t w) {
-  return pack_f16x2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
 }
-__device__ __forceinline__ void bf8_to_f32(const uint4& u, float* f) {
-  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    f[2 * e] = __uint_as_float(w[e] << 16);
-    f[2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
-  }
+// kind::f16 with A and B bf16, D fp32, M x N; A K-major (TMEM); B MN-major
+__device__ __forceinline__ constexpr uint32_t idesc_bf16_bmn(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
 // key tiles of an item, and those MMA tile t takes part in (tile 0: pages [page0, page_mid);
@@ -274,7 +266,6 @@ __device__ __forceinline__ int item_tiles_of(const AttnItem& it, int t) {
 __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_constant__ AttnArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  int* sTm = reinterpret_cast<int*>(sm + OFF_TM);   // [stage][page][start, valid rows]
   int* sPos = reinterpret_cast<int*>(sm + OFF_POS);
   int* sTile = reinterpret_cast<int*>(sm + OFF_TILE);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
@@ -288,7 +279,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     s_abort = 0;
     for (int i = 0; i < NST; ++i) {
       mbar_init(bar(B_FULL + i), 1);
-      mbar_init(bar(B_XF + i), kTransformWarps);
       mbar_init(bar(B_EMPTY + i), MT);   // one release per MMA tile
     }
     for (int i = 0; i < 2 * MT; ++i) {
@@ -322,7 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     const bool issuer = hh == 0 && lane == 0;
     const uint32_t trow = tmem + ((uint32_t)(hh * 32) << 16);   // this warp's TMEM lane quarter
     const uint32_t t_o = trow + TM_O + 128 * t, t_sb = trow + TM_S + 128 * t;
-    const uint32_t id_pv = idesc_f16(128, D, true);
+    const uint32_t id_pv = idesc_bf16_bmn(128, D);
     uint8_t* qs = sm + OFF_Q + t * Q_TILE;
     // every thread of the warpgroup takes part, so all of them take the same branch after it
     auto wg_all = [&](bool v) -> bool {
@@ -377,7 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
           // this MMA tile takes no part in the key tile: release its share of the stage once the
           // stage holds the tile (the release must not count toward the stage's previous use)
           if (issuer) {
-            if (!s_abort && mbar_wait(bar(B_XF + sl), (g / NST) & 1))
+            if (!s_abort && mbar_wait(bar(B_FULL + sl), (g / NST) & 1))
               umma_commit(bar(B_EMPTY + sl));
             else
               s_abort = 1;
@@ -387,7 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         const int b = ct & 1;
         const uint32_t t_s = t_sb + 64 * b;
         bool okw = !s_abort && mbar_wait(bar(B_SFULL + 2 * t + b), (ct >> 1) & 1) &&
-                   mbar_wait(bar(B_XF + sl), (g / NST) & 1);
+                   mbar_wait(bar(B_FULL + sl), (g / NST) & 1);
         okw = __all_sync(0xffffffffu, okw);
         if (okw) {
           fence_after();
@@ -426,7 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
           const float scale = (grow && mref != -INFINITY) ? ex2(mref - mnew) : 1.f;
           l *= scale;
           mref = mnew;
-          // P = 2^(S - ref) as fp16 pairs: keys 2c, 2c + 1 in column 32 + c of the S buffer
+          // P = 2^(S - ref) as bf16 pairs: keys 2c, 2c + 1 in column 32 + c of the S buffer
           const float mz = mref == -INFINITY ? 0.f : mref;   // fully masked so far: every s is -inf, p = 0
           float rs = 0.f;
           auto store_p = [&](int h) {
@@ -435,7 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
             for (int e = 0; e < 16; ++e) {
               const float p0 = ex2(s[2 * e] - mz), p1 = ex2(s[2 * e + 1] - mz);
               rs += p0 + p1;
-              pv[e] = pack_f16x2(p0, p1);
+              pv[e] = pack_bf16x2(p0, p1);
             }
             tmem_st16(t_s + 32 + 16 * h, pv);
           };
@@ -536,7 +526,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     }
   } else if (warp == W_MMA) {
     // =============================== S products of both MMA tiles, each as soon as its key tile
-    // is transformed, its S buffer free (the PV that read it retired) and, for an item's first,
+    // has landed, its S buffer is free (the PV that read it retired) and, for an item's first,
     // its Q tile written
     if (lane == 0) {
       const uint32_t id_s = idesc_f16(128, KT, false);
@@ -557,7 +547,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
             if (js[t] >= na[t]) continue;
             const uint32_t g = gt + js[t], c = ct[t] + js[t];
             const int b = c & 1, st = g % NST;
-            if (mbar_test(bar(B_XF + st), (g / NST) & 1) &&
+            if (mbar_test(bar(B_FULL + st), (g / NST) & 1) &&
                 (js[t] > 0 || mbar_test(bar(B_QREADY + t), ci[t] & 1)) &&
                 (c < 2 || mbar_test(bar(B_PVDONE + 2 * t + b), ((c - 2) >> 1) & 1))) {
               fence_after();
@@ -584,7 +574,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
             ok = false;
             break;
           }
-          __nanosleep(64);   // leave the issue slots of this sub-partition to the softmax and transform
+          __nanosleep(64);   // leave the issue slots of this sub-partition to the softmax
         }
         for (int t = 0; t < MT; ++t)
           if (na[t] > 0) {
@@ -597,122 +587,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       umma_commit(bar(B_DONE + MT));   // fires once every MMA of this thread has retired
       mbar_wait(bar(B_DONE + MT), 0);
     }
-  } else if (warp < W_MMA) {
-    // =============================== transform warps, in place in the stage
-    const int tt = tid - W_XF * 32, tw = warp - W_XF;
-    // K: row offset rr of pages pg0, pg0 + 1; dims 8cq..8cq+7 and 64 + 8cq..
-    const int rr = lane & 15, cq = 2 * (tw & 3) + (lane >> 4), pg0 = 2 * (tw >> 2);
-    float2 lo[8];   // (cos, sin)(rr theta_i) for this thread's 8 frequencies
-#pragma unroll
-    for (int e = 0; e < 8; ++e) lo[e] = a.rope_cs[rr * 64 + 8 * cq + e];
-    uint32_t gt = 0;
-    bool ok = true;
-    for (int ii = blockIdx.x; ii < a.n_items && ok; ii += gridDim.x) {
-      const int nt = item_tiles(a.items[ii]);
-      for (int j = 0; j < nt; ++j, ++gt) {
-        const int s = gt % NST;
-        ok = __all_sync(0xffffffffu, !s_abort && mbar_wait(bar(B_FULL + s), (gt / NST) & 1));
-        if (!ok) break;
-        // Every shared-memory input of the tile is read before the first store (the stores go
-        // to the same stage, so a load placed after them could not be moved ahead of them).
-        const int4 tmA = reinterpret_cast<const int4*>(sTm + s * 8)[0], tmB = reinterpret_cast<const int4*>(sTm + s * 8)[1];
-        const int st0 = pg0 ? tmB.x : tmA.x, ln0 = pg0 ? tmB.y : tmA.y, st1 = pg0 ? tmB.z : tmA.z,
-                  ln1 = pg0 ? tmB.w : tmA.w;
-        uint8_t* kst = sm + OFF_ST + s * ST_BYTES;
-        uint8_t* vst = kst + 16384;
-        // K, rows rr of pages pg0 and pg0 + 1: dims 8cq..8cq+7 (half 0) and 64 + 8cq.. (half 1)
-        uint4* kp[2][2];
-        uint4 kr[2][2];
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int key = (pg0 + u) * 16 + rr;
-          kp[u][0] = reinterpret_cast<uint4*>(kst + sw128(key, cq));
-          kp[u][1] = reinterpret_cast<uint4*>(kst + 8192 + sw128(key, cq));
-          kr[u][0] = *kp[u][0];
-          kr[u][1] = *kp[u][1];
-        }
-        // V: 4 chunks of 16 bytes of [half][key][8]
-        uint4 vr[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) vr[i] = reinterpret_cast<const uint4*>(vst)[tt + 32 * kTransformWarps * i];
-        // K rotated by RoPE at start + rr; rows without a key (ragged or missing pages) become 0
-        uint4 ky[2][2];
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int len = u ? ln1 : ln0;
-          ky[u][0] = ky[u][1] = make_uint4(0, 0, 0, 0);
-          if (rr < len) {
-            float v1[8], v2[8];
-            bf8_to_f32(kr[u][0], v1);
-            bf8_to_f32(kr[u][1], v2);
-            const float4* hrow = reinterpret_cast<const float4*>(sm + OFF_CS + (s * 4 + pg0 + u) * 512) + 4 * cq;
-            uint32_t o1[4], o2[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const float4 h4 = hrow[q];   // (cos, sin) of the page start for frequencies 8cq + 2q, + 1
-              const float2 hi[2] = {make_float2(h4.x, h4.y), make_float2(h4.z, h4.w)};
-              float y1e[2], y2e[2];
-#pragma unroll
-              for (int e = 0; e < 2; ++e) {
-                const int f = 2 * q + e;
-                const float cs = hi[e].x * lo[f].x - hi[e].y * lo[f].y;
-                const float sn = hi[e].y * lo[f].x + hi[e].x * lo[f].y;
-                y1e[e] = v1[f] * cs - v2[f] * sn;
-                y2e[e] = v2[f] * cs + v1[f] * sn;
-              }
-              o1[q] = pack_f16x2(y1e[0], y1e[1]);
-              o2[q] = pack_f16x2(y2e[0], y2e[1]);
-            }
-            ky[u][0] = make_uint4(o1[0], o1[1], o1[2], o1[3]);
-            ky[u][1] = make_uint4(o2[0], o2[1], o2[2], o2[3]);
-          }
-        }
-        // V bf16 -> fp16 in place ([half][key][128 B] is already the MN-major operand of
-        // O += P V); rows without a key become 0 (P is 0 there, V must be finite)
-        uint4 vy[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int key = ((tt + 32 * kTransformWarps * i) >> 3) & 63;
-          const uint4 w = vr[i];
-          const int pg = key >> 4, ln = pg == 0 ? tmA.y : pg == 1 ? tmA.w : pg == 2 ? tmB.y : tmB.w;
-          vy[i] = (key & 15) < ln
-                      ? make_uint4(bf2_to_h2(w.x), bf2_to_h2(w.y), bf2_to_h2(w.z), bf2_to_h2(w.w))
-                      : make_uint4(0, 0, 0, 0);
-        }
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          *kp[u][0] = ky[u][0];
-          *kp[u][1] = ky[u][1];
-        }
-#pragma unroll
-        for (int i = 0; i < 4; ++i) reinterpret_cast<uint4*>(vst)[tt + 32 * kTransformWarps * i] = vy[i];
-        if (cq == 0) {
-          sPos[s * KT + pg0 * 16 + rr] = rr < ln0 ? st0 + rr : INT_MAX;
-          sPos[s * KT + (pg0 + 1) * 16 + rr] = rr < ln1 ? st1 + rr : INT_MAX;
-        }
-        if (tt == 0) {   // last key position of the tile; INT_MAX when some slot holds no key
-          const int sts[4] = {tmA.x, tmA.z, tmB.x, tmB.z}, lns[4] = {tmA.y, tmA.w, tmB.y, tmB.w};
-          int kmax = -1;
-          bool full = true;
-#pragma unroll
-          for (int pg = 0; pg < 4; ++pg) {
-            if (lns[pg] > 0) kmax = sts[pg] + lns[pg] - 1;
-            if (lns[pg] < kBlock) full = false;
-          }
-          sTile[s] = full ? kmax : INT_MAX;
-        }
-        fence_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(B_XF + s));
-      }
-    }
-    if (!ok) s_abort = 1;
   } else if (warp == W_LOAD) {
     // =============================== loads (lanes issue the boxes; the warp holds page metadata)
     uint32_t n_ld = 0;   // key tiles issued
     bool ok = true;
     // lane i: metadata of page w0 + i (cur) and of page w0 + 32 + i (nxt, loaded one window ahead)
     int w0 = 0, cblk = 0, cpos = 0, clen = 0, nblk = 0, npos = 0, nlen = 0;
+    const __nv_bfloat16* vl = static_cast<const __nv_bfloat16*>(a.v_layer);
     for (int ii = blockIdx.x; ii < a.n_items && ok; ii += gridDim.x) {
       const AttnItem it = a.items[ii];
       const int nt = item_tiles(it);
@@ -750,33 +631,57 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         if (lane == 0) ok = !s_abort && (kr == 0 || mbar_wait(bar(B_EMPTY + s), (kr - 1) & 1));
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
-        const uint32_t fb = bar(B_FULL + s);
-        if (lane == 0) {
-          int* tm = sTm + s * 8;
+        // key positions of the tile (INT_MAX: no key), and its last position (INT_MAX when some
+        // slot holds no key: the tile then needs the mask whatever the row)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int key = 2 * lane + e, q = key >> 4, rr = key & 15;
+          const int lq = q == 0 ? len[0] : q == 1 ? len[1] : q == 2 ? len[2] : len[3];
+          const int pq = q == 0 ? pos[0] : q == 1 ? pos[1] : q == 2 ? pos[2] : pos[3];
+          sPos[s * KT + key] = rr < lq ? pq + rr : INT_MAX;
+        }
+        bool full[4];
+        int n_full = 0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          full[q] = len[q] == kBlock;
+          n_full += full[q];
+        }
+        if (lane == 0) sTile[s] = n_full == 4 ? pos[3] + kBlock - 1 : INT_MAX;
+        const uint32_t kd = smem_u32(sm + OFF_ST + s * ST_BYTES), vd = kd + 16384;
+        const bool run = n_full == 4 && blk[1] == blk[0] + 1 && blk[2] == blk[0] + 2 && blk[3] == blk[0] + 3;
+        if (n_full < 4) {
+          // V of the pages that are not full: rows with a key copied, the others zeroed
+          // (4 KB per page: 2 halves x 16 rows x 8 chunks of 16 bytes)
+#pragma unroll
           for (int q = 0; q < 4; ++q) {
-            tm[2 * q] = pos[q];
-            tm[2 * q + 1] = len[q];
+            if (full[q]) continue;
+            const __nv_bfloat16* src = vl + ((size_t)blk[q] * a.G + it.g) * kBlock * D;
+            for (int i = lane; i < 256; i += 32) {
+              const int h = i >> 7, rr = (i >> 3) & 15, c = i & 7;
+              const uint4 v = rr < len[q] ? *reinterpret_cast<const uint4*>(src + rr * D + h * 64 + c * 8)
+                                          : make_uint4(0, 0, 0, 0);
+              asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(vd + h * 8192 + sw128(q * 16 + rr, c)),
+                           "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                           : "memory");
+            }
           }
-          mbar_expect_tx(fb, (uint32_t)np * (8192 + 512));   // arrives too: the boxes complete the phase
+          fence_async_smem();   // the MMAs read these rows through the async proxy
         }
         __syncwarp();
-        const uint32_t kd = smem_u32(sm + OFF_ST + s * ST_BYTES), vd = kd + 16384;
-        const uint32_t csd = smem_u32(sm + OFF_CS + s * 2048);
-        const bool run = np == 4 && blk[1] == blk[0] + 1 && blk[2] == blk[0] + 2 && blk[3] == blk[0] + 3;
-        if (run) {   // 4 consecutive blocks: one box per (K or V, half), 8 KB each
-          if (lane < 4) {
-            const int h = lane & 1;
-            tma_5d((lane < 2 ? kd : vd) + h * 8192, lane < 2 ? &a.kmap : &a.vmap, 0, h, 0, it.g, blk[0], fb);
-          }
-        } else if (lane < 4 * np) {   // one box per (page, K or V, half), 2 KB each
-          const int q = lane >> 2, h = lane & 1, isv = (lane >> 1) & 1;
+        const uint32_t fb = bar(B_FULL + s);
+        // arrives too: the boxes complete the phase (K always 2 x 8 KB; V 2 x 2 KB per full page)
+        if (lane == 0) mbar_expect_tx(fb, 16384u + (uint32_t)n_full * 4096u);
+        __syncwarp();
+        if (lane < 2)   // rotated K: one box of 4 consecutive scratch pages per 64-dim half
+          tma_5d(kd + lane * 8192, &a.kmap, 0, lane, 0, it.g, p0, fb);
+        if (run) {   // V of 4 consecutive full blocks: one box per half, 8 KB each
+          if (lane == 2 || lane == 3) tma_5d(vd + (lane - 2) * 8192, &a.vmap, 0, lane - 2, 0, it.g, blk[0], fb);
+        } else if (lane >= 8 && lane < 16) {   // V of one full page per box, 2 KB each
+          const int q = (lane - 8) >> 1, h = lane & 1;
           const int bq = q == 0 ? blk[0] : q == 1 ? blk[1] : q == 2 ? blk[2] : blk[3];
-          tma_5d((isv ? vd : kd) + h * 8192 + q * 2048, isv ? &a.vmap1 : &a.kmap1, 0, h, 0, it.g, bq, fb);
-        }
-        if (lane >= 16 && lane < 16 + np) {   // cos/sin rows of the page starts, 512 B each
-          const int q = lane - 16;
-          const int pq = q == 0 ? pos[0] : q == 1 ? pos[1] : q == 2 ? pos[2] : pos[3];
-          tma_2d(csd + q * 512, &a.csmap, 0, pq, fb);
+          const bool fq = q == 0 ? full[0] : q == 1 ? full[1] : q == 2 ? full[2] : full[3];
+          if (fq) tma_5d(vd + h * 8192 + q * 2048, &a.vmap1, 0, h, 0, it.g, bq, fb);
         }
         ++n_ld;
       }
@@ -794,6 +699,41 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
   fence_before();
   __syncthreads();
   if (warp == W_MMA) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
+}
+
+// K of page p of the work, KV head g, rotated by RoPE at each row's absolute position, fp16, to
+// krot[p][g][16][128]; rows beyond the page's length zero. CTA (p, g), thread = (row r, dims
+// 8c..8c+7 and 64 + 8c..64 + 8c + 7).
+__global__ void __launch_bounds__(128) rope_k_kernel(int G, const int* __restrict__ page_block,
+                                                     const int* __restrict__ page_pos,
+                                                     const int* __restrict__ page_len,
+                                                     const __nv_bfloat16* __restrict__ k_layer,
+                                                     const float2* __restrict__ rope_cs, __half* __restrict__ krot) {
+  pdl_enter();
+  const int p = blockIdx.x, g = blockIdx.y, r = threadIdx.x >> 3, c = threadIdx.x & 7;
+  const int blk = page_block[p], len = page_len[p];
+  uint4 y1 = make_uint4(0, 0, 0, 0), y2 = y1;
+  if (r < len) {
+    const __nv_bfloat16* src = k_layer + (((size_t)blk * G + g) * kBlock + r) * D + 8 * c;
+    const uint4 u1 = *reinterpret_cast<const uint4*>(src), u2 = *reinterpret_cast<const uint4*>(src + 64);
+    const float4* row = reinterpret_cast<const float4*>(rope_cs + (size_t)(page_pos[p] + r) * (D / 2) + 8 * c);
+    const uint32_t w1[4] = {u1.x, u1.y, u1.z, u1.w}, w2[4] = {u2.x, u2.y, u2.z, u2.w};
+    uint32_t o1[4], o2[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float4 cs = row[e];   // (cos, sin) of frequencies 8c + 2e and 8c + 2e + 1
+      // bf16 pair -> two floats (exact), then the rotate-half pairs (i, i + 64)
+      const float a0 = __uint_as_float(w1[e] << 16), a1 = __uint_as_float(w1[e] & 0xffff0000u);
+      const float b0 = __uint_as_float(w2[e] << 16), b1 = __uint_as_float(w2[e] & 0xffff0000u);
+      o1[e] = pack_f16x2(a0 * cs.x - b0 * cs.y, a1 * cs.z - b1 * cs.w);
+      o2[e] = pack_f16x2(b0 * cs.x + a0 * cs.y, b1 * cs.z + a1 * cs.w);
+    }
+    y1 = make_uint4(o1[0], o1[1], o1[2], o1[3]);
+    y2 = make_uint4(o2[0], o2[1], o2[2], o2[3]);
+  }
+  __half* dst = krot + (((size_t)p * G + g) * kBlock + r) * D + 8 * c;
+  *reinterpret_cast<uint4*>(dst) = y1;
+  *reinterpret_cast<uint4*>(dst + 64) = y2;
 }
 
 int sm_count() {
@@ -823,34 +763,38 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 bool tc_attention_supported(int dtype, int D_, int rep) { return dtype == PIC_BF16 && D_ == D && rep == REP; }
 
-// One layer of a pool, [blocks][G][16 rows][128] bf16, viewed as (64 dims, 2 halves, 16 rows, G,
-// blocks): a box is one 64-dim half of the 16 rows of one KV head's page in 4 consecutive blocks
-// (m4) or in one block (m1), landing as [pages][16 rows][128 B] -- one half of the K-major (K)
-// or MN-major (V) operand of 64 keys.
-bool attn_kv_map(CUtensorMap* m4, CUtensorMap* m1, const void* layer, int pool_blocks, int G) {
+// A [n][G][16 rows][128] array of 16-bit elements (`type`: a pool layer of bf16 V, or the fp16
+// rotated-K scratch) viewed as (64 dims, 2 halves, 16 rows, G, n): a box is one 64-dim half of
+// the 16 rows of one KV head's page in `pages` consecutive entries, landing as [pages][16
+// rows][128 B] -- one half of the K-major (K) or MN-major (V) operand of 16 x pages keys.
+bool attn_page_map(CUtensorMap* m, CUtensorMapDataType type, const void* base, int n, int G, int pages) {
   auto enc = encode_fn();
-  if (!enc || pool_blocks < 1 || G < 1) return false;
-  cuuint64_t dims[5] = {64, 2, (cuuint64_t)kBlock, (cuuint64_t)G, (cuuint64_t)pool_blocks};
+  if (!enc || n < 1 || G < 1) return false;
+  cuuint64_t dims[5] = {64, 2, (cuuint64_t)kBlock, (cuuint64_t)G, (cuuint64_t)n};
   cuuint64_t strides[4] = {128, (cuuint64_t)D * 2, (cuuint64_t)kBlock * D * 2, (cuuint64_t)G * kBlock * D * 2};
   cuuint32_t estr[5] = {1, 1, 1, 1, 1};
-  cuuint32_t box4[5] = {64, 1, kBlock, 1, 4}, box1[5] = {64, 1, kBlock, 1, 1};
-  auto make = [&](CUtensorMap* m, cuuint32_t* box) {
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(layer), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-  };
-  return make(m4, box4) && make(m1, box1);
+  cuuint32_t box[5] = {64, 1, kBlock, 1, (cuuint32_t)pages};
+  return enc(m, type, 5, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
 }
 
-bool attn_cs_map(CUtensorMap* m, const float2* rope_cs, int n_pos) {
-  auto enc = encode_fn();
-  if (!enc || n_pos < 1) return false;
-  cuuint64_t dims[2] = {D, (cuuint64_t)n_pos};   // D floats = D/2 (cos, sin) pairs per position
-  cuuint64_t strides[1] = {(cuuint64_t)D * 4};
-  cuuint32_t box[2] = {D, 1}, estr[2] = {1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float2*>(rope_cs), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+bool attn_v_map(CUtensorMap* m4, CUtensorMap* m1, const void* v_layer, int pool_blocks, int G) {
+  return attn_page_map(m4, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, v_layer, pool_blocks, G, 4) &&
+         attn_page_map(m1, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, v_layer, pool_blocks, G, 1);
+}
+
+bool attn_krot_map(CUtensorMap* m, const __half* krot, int n_pages, int G) {
+  return attn_page_map(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, krot, n_pages, G, 4);
+}
+
+size_t attention_krot_bytes(int n_pages, int G) { return (size_t)n_pages * G * kBlock * D * sizeof(__half); }
+
+void launch_rope_k(int n_pages, int G, const int* page_block, const int* page_pos, const int* page_len,
+                   const void* k_layer, const float2* rope_cs, __half* krot, cudaStream_t st) {
+  if (n_pages > 0)
+    launch_dependent(rope_k_kernel, dim3(n_pages, G), dim3(128), 0, st, G, page_block, page_pos, page_len,
+                     static_cast<const __nv_bfloat16*>(k_layer), rope_cs, krot);
 }
 
 int attention_tc_rows_per_item() { return MT * RB; }

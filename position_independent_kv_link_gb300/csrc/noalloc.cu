@@ -100,13 +100,14 @@ pic_status pic_op_attention_noalloc(int32_t dtype, int32_t T, int32_t n_heads, i
   plan_attention(in, items, combs, n_parts);
 
   // exact footprint of this call: metadata ints, partial outputs and (max, sum) pairs, then
-  // the rotated fp16 q of the tensor-core path
+  // the rotated fp16 q and K of the tensor-core path
   const int rep = n_heads / n_kv_heads;
   const size_t n_ints = (size_t)T + 3 * (size_t)n_pages + kAttnItemInts * items.size() + 5 * combs.size();
   const size_t o_part = align256(n_ints * 4);
   const size_t o_ml = o_part + align256((size_t)n_parts * kAttnPartRows * rep * head_dim * 4);
   const size_t o_q16 = o_ml + align256((size_t)n_parts * kAttnPartRows * rep * 2 * 4);
-  const size_t need = o_q16 + (in.persistent ? align256((size_t)T * n_heads * head_dim * 2) : 0);
+  const size_t o_krot = o_q16 + (in.persistent ? align256((size_t)T * n_heads * head_dim * 2) : 0);
+  const size_t need = o_krot + (in.persistent ? align256(attention_krot_bytes(n_pages, n_kv_heads)) : 0);
   if (need > kNoAllocScratchBytes)
     return fail(PIC_ERR_CAPACITY, "attention needs " + std::to_string(need) + " bytes of scratch; the fixed area holds " +
                                       std::to_string(kNoAllocScratchBytes) + " (use pic_op_attention with a caller buffer)");
@@ -154,7 +155,9 @@ pic_status pic_op_attention_noalloc(int32_t dtype, int32_t T, int32_t n_heads, i
   a.combines = (const AttnCombine*)(di + o_combs);
   a.n_combines = (int)combs.size();
   if (in.persistent) {
-    s = attention_prepare_tc(a, T, pool_blocks, rope_positions, (__half*)((char*)scratch + o_q16), st);
+    a.n_pages = n_pages;
+    s = attention_prepare_tc(a, T, pool_blocks, (__half*)((char*)scratch + o_q16), (__half*)((char*)scratch + o_krot),
+                             st);
     if (s != PIC_OK) return s;
   }
   launch_attention(a, st);

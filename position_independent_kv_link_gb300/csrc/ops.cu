@@ -19,7 +19,7 @@ int current_sms() {
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
 struct AttnScratchLayout {
-  size_t ints_bytes, part_o_off, part_ml_off, q16_off, total;
+  size_t ints_bytes, part_o_off, part_ml_off, q16_off, krot_off, total;
   int max_parts, max_items;
 };
 
@@ -34,7 +34,9 @@ AttnScratchLayout attn_layout(int T, int n_heads, int n_kv_heads, int head_dim, 
   L.part_o_off = L.ints_bytes;
   L.part_ml_off = L.part_o_off + align256((size_t)L.max_parts * kAttnPartRows * rep * head_dim * 4);
   L.q16_off = L.part_ml_off + align256((size_t)L.max_parts * kAttnPartRows * rep * 2 * 4);
-  L.total = L.q16_off + align256((size_t)T * n_heads * head_dim * 2);   // rotated fp16 q (tensor-core path)
+  // tensor-core path: rotated fp16 q, then the rotated fp16 K of every page
+  L.krot_off = L.q16_off + align256((size_t)T * n_heads * head_dim * 2);
+  L.total = L.krot_off + align256((size_t)n_pages * n_kv_heads * kBlock * head_dim * 2);
   return L;
 }
 
@@ -154,7 +156,9 @@ pic_status pic_op_attention(int32_t dtype, int32_t T, int32_t n_heads, int32_t n
   a.combines = (const AttnCombine*)(di + o_combs);
   a.n_combines = (int)combs.size();
   if (in.persistent) {
-    pic_status e = attention_prepare_tc(a, T, pool_blocks, rope_positions, (__half*)((char*)scratch + L.q16_off), st);
+    a.n_pages = n_pages;
+    pic_status e = attention_prepare_tc(a, T, pool_blocks, (__half*)((char*)scratch + L.q16_off),
+                                        (__half*)((char*)scratch + L.krot_off), st);
     if (e != PIC_OK) return e;
   }
   launch_attention(a, st);

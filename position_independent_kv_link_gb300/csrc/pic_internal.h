@@ -156,11 +156,14 @@ struct AttnCombine {   // merge `nparts` partial results of rows [row0, row0+nro
   int row0, nrows, g, part0, nparts;
 };
 struct AttnArgs {
-  // tensor-core kernel only (attention_persistent shapes): K and V pools of the layer
-  // (attn_kv_map), boxes of one 64-dim half of 4 consecutive blocks' pages (kmap, vmap) or of
-  // one page (kmap1, vmap1); rows of the cos/sin table (attn_cs_map); q16: q as fp16 [T][H][D],
-  // rotated and scaled (the QKV epilogue's q16 output)
-  CUtensorMap kmap, vmap, kmap1, vmap1, csmap;
+  // tensor-core kernel only (attention_persistent shapes): kmap boxes 4 consecutive pages of the
+  // rotated-K scratch krot [n_pages][G][16][128] fp16 (attn_krot_map, written per layer by
+  // launch_rope_k); vmap / vmap1 box one 64-dim half of 4 consecutive blocks' / one block's page
+  // of the V pool layer (attn_v_map); q16: q as fp16 [T][H][D], rotated and scaled (the QKV
+  // epilogue's q16 output)
+  CUtensorMap kmap, vmap, vmap1;
+  __half* krot;
+  int n_pages;
   const __half* q16;
   int dtype, H, G, D;
   int rb;                   // rows per work item of this plan (16, 32 or 64)
@@ -200,19 +203,24 @@ int attention_tc_rows_per_item();   // k_attn_tc.cu
 // True when the shape runs the persistent tensor-core kernel: its CTA b takes items b, b + grid,
 // b + 2 grid, ... with grid = min(items, SMs), so the planner orders items for that walk.
 bool attention_persistent(int dtype, int D, int rep);
-// Tensor maps of the tensor-core attention: Q fp16 [T][H][128] (3-D, boxes of 64 dims x 1
-// head x 32 rows) and one layer of a KV pool [pool_blocks][G][16][128] bf16 viewed as 5-D
-// (64 dims, 2 halves, 16 rows, G, blocks): m4 boxes one half of the pages of 4 consecutive
-// blocks of one KV head (8 KB), m1 one half of one page (2 KB). All 128-byte swizzled. False
-// when encoding fails.
-bool attn_kv_map(CUtensorMap* m4, CUtensorMap* m1, const void* layer, int pool_blocks, int G);
-// The cos/sin table [n_pos][64] float2 as rows of 512 bytes (one box = one position's row).
-bool attn_cs_map(CUtensorMap* m, const float2* rope_cs, int n_pos);
+// Tensor maps of the tensor-core attention (k_attn_tc.cu): the V pool layer [pool_blocks][G][16]
+// [128] bf16 viewed as 5-D (64 dims, 2 halves, 16 rows, G, blocks) -- m4 boxes one half of the
+// pages of 4 consecutive blocks of one KV head (8 KB), m1 one half of one page (2 KB) -- and the
+// rotated-K scratch [n_pages][G][16][128] fp16 the same way with 4-page boxes. 128-byte
+// swizzled. False when encoding fails.
+bool attn_v_map(CUtensorMap* m4, CUtensorMap* m1, const void* v_layer, int pool_blocks, int G);
+bool attn_krot_map(CUtensorMap* m, const __half* krot, int n_pages, int G);
+// Bytes of the rotated-K scratch for n_pages pages.
+size_t attention_krot_bytes(int n_pages, int G);
+// krot[p][g] = fp16(RoPE(K[page_block[p]][g][r], page_pos[p] + r)) for r < page_len[p], 0 for the
+// other rows, for every page p of the work (one programmatic-dependent launch).
+void launch_rope_k(int n_pages, int G, const int* page_block, const int* page_pos, const int* page_len,
+                   const void* k_layer, const float2* rope_cs, __half* krot, cudaStream_t st);
 // For callers holding fp32 pre-RoPE a.q (kernel-level calls): writes the rotated fp16 copy
-// into q16 ([T][H][128], 16-byte aligned), sets a.q16 to it, and the K/V maps from a.k_layer /
-// a.v_layer (pools of pool_blocks blocks) and the cos/sin map from a.rope_cs (rope_positions rows).
-pic_status attention_prepare_tc(AttnArgs& a, int T, int pool_blocks, int rope_positions, __half* q16,
-                                cudaStream_t st);
+// into q16 ([T][H][128], 16-byte aligned) and the rotated K of the a.n_pages pages into krot
+// (attention_krot_bytes, 16-byte aligned), and sets a.q16, a.krot and the maps (V pool of
+// pool_blocks blocks).
+pic_status attention_prepare_tc(AttnArgs& a, int T, int pool_blocks, __half* q16, __half* krot, cudaStream_t st);
 void plan_attention(const AttnPlanInput& in, std::vector<AttnItem>& items, std::vector<AttnCombine>& combines,
                     int& n_parts);
 size_t attention_part_bytes(int n_parts, int rep, int D);

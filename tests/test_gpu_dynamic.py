@@ -132,25 +132,30 @@ def test_small_bf16_dynamic_batch_of_three():
 
 
 def test_r0_and_r100_match_static_link():
-    """r = 0: the query alone (pic_link, k = 0); r = 100: every token (k = longest chunk)."""
+    """r = 0: the query alone (pic_link, k = 0); r = 100: every token (k = longest chunk). Same
+    metadata as pic_link, and the same outputs as the oracle's static link."""
     spec = pi.SMALL_BF16
     wl = pi.make_workload("dyn ends", spec, 3, [48, 20, 37], 16, 0)
     w = pi.gen_weights(spec)
+    om = po.OracleModel(spec, w)
     model, store = _stores(spec, w)
     try:
         cids = store.compile(wl.chunks)
         reqs = [([cids[c] for c in r.chunk_ids], r.query) for r in wl.requests]
         for r, k in ((0, 0), (100, 48)):
             a = store.link_dynamic(reqs, r, all_logits=True)
+            store.sync()
             ia = store.request_info(a.requests[0])
-            ha, la = a.hidden.clone(), a.logits.clone()
+            ost = po.OracleStore(om, 512)
+            ocids = ost.compile_many(wl.chunks)
+            out = ost.link([([ocids[c] for c in q.chunk_ids], q.query) for q in wl.requests], k, all_logits=True)
+            compare_link(store, a, out, spec)
             store.release_request(a.requests[0])
             b = store.link(reqs, k, all_logits=True)
             store.sync()
             ib = store.request_info(b.requests[0])
             for key in ia:
                 assert np.array_equal(ia[key], ib[key]), (r, key)
-            assert rel_err(ha, b.hidden) <= 1e-3 and rel_err(la, b.logits) <= 1e-3
             store.release_request(b.requests[0])
     finally:
         store.close()

@@ -65,7 +65,7 @@ def test_noalloc_attention_matches_regular_entry_point():
         # the case's pages are split into runs whose partial results are merged, so the
         # partial-result regions of the fixed area are in use
         counts = np.zeros(3, dtype=np.int32)
-        items = np.zeros((4096, 6), dtype=np.int32)
+        items = np.zeros((4096, 7), dtype=np.int32)
         combs = np.zeros((4096, 5), dtype=np.int32)
         seq_rows, seq_pages = np.array([0, T], dtype=np.int32), np.array([0, n_pages], dtype=np.int32)
         L.check(lib.pic_op_attention_plan(L.PIC_BF16, 8, 2, 128, 1, P(seq_rows), P(seq_pages), P(qpos), P(ppos),
