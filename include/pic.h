@@ -144,7 +144,12 @@ pic_status pic_model_destroy(pic_model* m);
 
 /* Creates a paged store over caller-owned K/V pools (layout in the header comment).
  * Allocates the library-owned device workspace and the RoPE table (fp64 angles on
- * the host, stored fp32). */
+ * the host, stored fp32). bf16 models with head_dim 128 and 4 query heads per KV head
+ * (the tensor-core attention) also use a device scratch holding one layer's K of every
+ * page of a forward, rotated to each row's position (fp16, 4 KB per page and KV head):
+ * the store allocates it at the first compile, link or decode that needs it and grows it
+ * (a cudaFree + cudaMalloc, which synchronizes the device) when a later call has more
+ * pages; it is freed with the store. */
 pic_status pic_store_create(pic_model* m, const pic_store_config* cfg, void* k_pool, void* v_pool,
                             pic_store** out);
 pic_status pic_store_destroy(pic_store* s);
@@ -349,7 +354,10 @@ pic_status pic_op_gemm_packed(const void* W_packed, const void* X, float* Y, int
  * valid rows); k_layer/v_layer: one layer of the pools ([pool_blocks][G][16][D]); every
  * page block must be < pool_blocks. rope_cs: device float2 [rope_positions][D/2] (cos,
  * sin), e.g. from pic_op_rope_table; every position must be < rope_positions, and
- * rope_positions >= 16. Scratch as reported by pic_op_attention_scratch_bytes. */
+ * rope_positions >= 16. Scratch as reported by pic_op_attention_scratch_bytes (the work
+ * list, split partials, and for the tensor-core path -- bf16, head_dim 128, 4 query heads
+ * per KV head -- q and every page's K rotated to fp16). Rows beyond a page's length are
+ * never read. */
 size_t pic_op_attention_scratch_bytes(int32_t T, int32_t n_heads, int32_t n_kv_heads, int32_t head_dim,
                                       int32_t n_pages);
 pic_status pic_op_attention(int32_t dtype, int32_t T, int32_t n_heads, int32_t n_kv_heads, int32_t head_dim,
@@ -366,11 +374,11 @@ pic_status pic_op_attention(int32_t dtype, int32_t T, int32_t n_heads, int32_t n
  * those of pic_op_attention without the scratch buffer: the call uses a fixed 16 MiB
  * area inside the library (pic_op_attention_noalloc_max_scratch() bytes), held by every
  * GPU that loads the library until the process exits. It calls no cudaMalloc/cudaFree.
- *  - A shape whose exact work list and partial results exceed the area is rejected
- *    with PIC_ERR_CAPACITY before any GPU work.
+ *  - A shape whose exact work list, partial results and (tensor-core path) rotated q
+ *    and K exceed the area is rejected with PIC_ERR_CAPACITY before any GPU work.
  *  - The first call on a device looks up the area's device address (with that device
- *    current); make that first call before any stream capture. That look-up is guarded
- *    by a lock, so first calls from several host threads are safe.
+ *    current). That look-up is guarded by a lock, so first calls from several host
+ *    threads are safe.
  *  - Every call reuses the same area and leaves its contents behind; nothing in it has
  *    to start at zero (each word read is written earlier in the same call). Calls that
  *    overlap on the GPU (different streams, or different host threads) race on it:

@@ -64,7 +64,7 @@ constexpr int MT = 2;                     // MMA tiles per item (items of up to 
 constexpr int KT = 64;                    // keys per tile (4 pages)
 constexpr int NST = 4;                    // key-tile stages
 constexpr int kSoftmaxWarps = 4 * MT;
-constexpr int W_MMA = kSoftmaxWarps, W_LOAD = W_MMA + 1;
+constexpr int W_MMA = kSoftmaxWarps, W_LOAD = W_MMA + MT;   // one MMA-issuing warp per MMA tile
 constexpr int kThreads = (W_LOAD + 1) * 32;
 constexpr float kRescale = 8.f;           // rescale O when the row max grows by more than 2^8
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
@@ -88,9 +88,10 @@ constexpr int B_FULL = 0;                         // [NST] stage landed (TMA byt
 constexpr int B_EMPTY = B_FULL + NST;             // [NST] both MMA tiles' PVs of the stage's key tile retired
 constexpr int B_SFULL = B_EMPTY + NST;            // [2][2] S_t in buffer b computed (commit)
 constexpr int B_PVDONE = B_SFULL + 2 * MT;        // [2][2] O_t += P_t V of buffer b retired (commit)
-constexpr int B_QREADY = B_PVDONE + 2 * MT;       // [2] Q_t of the item written (warpgroup t)
-constexpr int B_DONE = B_QREADY + MT;             // [3] every MMA of an issuing thread retired
-static_assert(B_DONE + MT + 1 <= N_BARS, "barrier slots");
+constexpr int B_QREADY = B_PVDONE + 2 * MT;       // [2] Q_t of the item written (the 4 warps of warpgroup t)
+constexpr int B_PREADY = B_QREADY + MT;           // [2][2] P_t in buffer b written (the 4 warps of warpgroup t)
+constexpr int B_DONE = B_PREADY + 2 * MT;         // [2] every MMA of MMA tile t's issuing thread retired
+static_assert(B_DONE + MT <= N_BARS, "barrier slots");
 // Every waiter must observe each phase of a barrier before the barrier can complete the next
 // one (a parity wait cannot tell phase n from n + 2). FULL is waited on by the S issuer and
 // both warpgroups, but a stage can only be refilled after both warpgroups released it, i.e.
@@ -146,13 +147,6 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
       return false;
     }
   }
-}
-__device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
-          dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
-      : "memory");
 }
 __device__ __forceinline__ void tma_5d(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2, int c3, int c4,
                                        uint32_t bar) {
@@ -285,8 +279,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       mbar_init(bar(B_SFULL + i), 1);
       mbar_init(bar(B_PVDONE + i), 1);
     }
-    for (int t = 0; t < MT; ++t) mbar_init(bar(B_QREADY + t), 1);
-    for (int i = 0; i <= MT; ++i) mbar_init(bar(B_DONE + i), 1);
+    for (int t = 0; t < MT; ++t) mbar_init(bar(B_QREADY + t), 4);
+    for (int i = 0; i < 2 * MT; ++i) mbar_init(bar(B_PREADY + i), 4);
+    for (int t = 0; t < MT; ++t) mbar_init(bar(B_DONE + t), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == W_MMA) {
@@ -312,18 +307,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     const bool issuer = hh == 0 && lane == 0;
     const uint32_t trow = tmem + ((uint32_t)(hh * 32) << 16);   // this warp's TMEM lane quarter
     const uint32_t t_o = trow + TM_O + 128 * t, t_sb = trow + TM_S + 128 * t;
-    const uint32_t id_pv = idesc_bf16_bmn(128, D);
     uint8_t* qs = sm + OFF_Q + t * Q_TILE;
     // every thread of the warpgroup takes part, so all of them take the same branch after it
-    auto wg_all = [&](bool v) -> bool {
-      uint32_t res;
-      asm volatile(
-          "{\n .reg .pred p, q;\n setp.ne.u32 q, %1, 0;\n bar.red.and.pred p, %2, 128, q;\n selp.u32 %0, 1, 0, p;\n}\n"
-          : "=r"(res)
-          : "r"((uint32_t)v), "r"(1 + t)
-          : "memory");
-      return res != 0;
-    };
     uint32_t gt = 0, ct = 0;   // key tiles of the CTA; key tiles of this MMA tile
     bool ok = true;
     const int row = RB * t + r;
@@ -355,10 +340,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
           *reinterpret_cast<uint4*>(qs + (c >> 3) * 16384 + sw128(m, c & 7)) = x;
         }
         fence_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_QREADY + t));
       }
-      ok = wg_all(ok && !s_abort);
-      if (!ok) break;
-      if (na > 0 && issuer) mbar_arrive(bar(B_QREADY + t));
+      if (s_abort) {
+        ok = false;
+        break;
+      }
       float mref = -INFINITY, l = 0.f;
       for (int j = 0; j < nt; ++j) {
         const uint32_t g = gt + j;
@@ -379,37 +367,37 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         bool okw = !s_abort && mbar_wait(bar(B_SFULL + 2 * t + b), (ct >> 1) & 1) &&
                    mbar_wait(bar(B_FULL + sl), (g / NST) & 1);
         okw = __all_sync(0xffffffffu, okw);
-        if (okw) {
+        if (!okw) {
+          ok = false;
+          break;
+        }
+        {
           fence_after();
-          // Two halves of 32 keys keep the register footprint low: the low half is read for the
-          // maximum and again for P; P (64 fp16 = 32 columns) goes over the high half's columns,
-          // high keys first (their S is in registers by then), then the low keys.
+          // All 64 keys of the row in registers (one TMEM round trip); P (64 bf16 = 32 columns)
+          // goes over the S buffer's high half.
           const bool need_mask = __any_sync(0xffffffffu, sTile[sl] > qp);
-          const int* kpos = sPos + sl * KT;
-          auto load_half = [&](int h, float* v) {   // S of keys 32h..32h+31, masked by position
-            tmem_ld16(t_s + 32 * h, v);
-            tmem_ld16(t_s + 32 * h + 16, v + 16);
-            tmem_wait_ld();
-            if (need_mask) {
-              const int4* kp = reinterpret_cast<const int4*>(kpos + 32 * h);
+          float s[KT];
 #pragma unroll
-              for (int i = 0; i < 8; ++i) {
-                const int4 k4 = kp[i];
-                if (k4.x > qp) v[4 * i] = -INFINITY;
-                if (k4.y > qp) v[4 * i + 1] = -INFINITY;
-                if (k4.z > qp) v[4 * i + 2] = -INFINITY;
-                if (k4.w > qp) v[4 * i + 3] = -INFINITY;
-              }
+          for (int c = 0; c < KT; c += 16) tmem_ld16(t_s + c, s + c);
+          tmem_wait_ld();
+          if (need_mask) {
+            const int4* kp = reinterpret_cast<const int4*>(sPos + sl * KT);
+#pragma unroll
+            for (int i = 0; i < KT / 4; ++i) {
+              const int4 k4 = kp[i];
+              if (k4.x > qp) s[4 * i] = -INFINITY;
+              if (k4.y > qp) s[4 * i + 1] = -INFINITY;
+              if (k4.z > qp) s[4 * i + 2] = -INFINITY;
+              if (k4.w > qp) s[4 * i + 3] = -INFINITY;
             }
-          };
-          float s[32];
-          load_half(0, s);
-          float mx = s[0];
+          }
+          // maximum and sum as 8 independent chains (no long dependent latency chain)
+          float m8[8];
 #pragma unroll
-          for (int i = 1; i < 32; ++i) mx = fmaxf(mx, s[i]);
-          load_half(1, s);
+          for (int u = 0; u < 8; ++u) m8[u] = s[u];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) mx = fmaxf(mx, s[i]);
+          for (int i = 8; i < KT; ++i) m8[i & 7] = fmaxf(m8[i & 7], s[i]);
+          const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
           // new reference when the maximum grows by more than 2^8 (or for the first keys seen)
           const bool grow = mx > mref + kRescale;
           const float mnew = grow ? mx : mref;
@@ -418,20 +406,19 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
           mref = mnew;
           // P = 2^(S - ref) as bf16 pairs: keys 2c, 2c + 1 in column 32 + c of the S buffer
           const float mz = mref == -INFINITY ? 0.f : mref;   // fully masked so far: every s is -inf, p = 0
-          float rs = 0.f;
-          auto store_p = [&](int h) {
+          float r8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
             uint32_t pv[16];
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
-              const float p0 = ex2(s[2 * e] - mz), p1 = ex2(s[2 * e + 1] - mz);
-              rs += p0 + p1;
+              const float p0 = ex2(s[32 * h + 2 * e] - mz), p1 = ex2(s[32 * h + 2 * e + 1] - mz);
+              r8[e & 7] += p0 + p1;
               pv[e] = pack_bf16x2(p0, p1);
             }
             tmem_st16(t_s + 32 + 16 * h, pv);
-          };
-          store_p(1);
-          load_half(0, s);
-          store_p(0);
+          }
+          const float rs = ((r8[0] + r8[1]) + (r8[2] + r8[3])) + ((r8[4] + r8[5]) + (r8[6] + r8[7]));
           l += rs;
           if (__any_sync(0xffffffffu, scale != 1.f)) {
             // O holds the sums of this item's earlier key tiles: rescale it before this P is
@@ -449,25 +436,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
                 tmem_st16f(t_o + c, o);
               }
             } else {
-              okw = false;
+              ok = false;
             }
           }
           tmem_wait_st();
           fence_before();
         }
-        ok = wg_all(okw);   // P_t (and the rescaled O_t) of the whole tile written
         if (!ok) break;
-        // ---- O_t += P_t V at once; the stage's share is released when it retires
-        if (issuer) {
-          fence_after();
-          const uint32_t vb = smem_u32(sm + OFF_ST + sl * ST_BYTES + 16384);
-          const uint32_t pa = tmem + TM_S + 128 * t + 64 * b + 32;   // P over the S buffer's high half
-#pragma unroll
-          for (int k = 0; k < 4; ++k)   // K dimension 64 keys = 4 steps of 16 (8 TMEM columns of P each)
-            umma_ts(tmem + TM_O + 128 * t, pa + 8 * k, desc_mnmajor(vb + k * 2048, 8192), id_pv, (j | k) != 0);
-          umma_commit(bar(B_PVDONE + 2 * t + b));
-          umma_commit(bar(B_EMPTY + sl));
-        }
+        // this warp's rows of P_t (and of the rescaled O_t) are written: the MMA thread issues
+        // O_t += P_t V once all four warps of the warpgroup have arrived
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_PREADY + 2 * t + b));
         ++ct;
       }
       if (!ok) break;
@@ -513,23 +492,22 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
           const size_t pi = ((size_t)it.part * kAttnPartRows + row) * REP + hh;
           *reinterpret_cast<float2*>(a.part_ml + pi * 2) = make_float2(mref, l);
         }
-        fence_before();   // the next item's first PV overwrites O_t after the barrier at its start
+        fence_before();   // the next item's first PV overwrites O_t only after this warp's next P arrival
       }
       if (!okd) s_abort = 1;
       gt += nt;
     }
     if (!ok) s_abort = 1;
-    // every MMA this thread issued has retired before the TMEM is given up
-    if (issuer) {
-      umma_commit(bar(B_DONE + t));
-      mbar_wait(bar(B_DONE + t), 0);
-    }
-  } else if (warp == W_MMA) {
-    // =============================== S products of both MMA tiles, each as soon as its key tile
-    // has landed, its S buffer is free (the PV that read it retired) and, for an item's first,
-    // its Q tile written
+  } else if (warp < W_MMA + MT) {
+    // =============================== every MMA of the CTA, from one thread: per MMA tile, O_t +=
+    // P_t V of a key tile as soon as the warpgroup has written its P, and S_t of a key tile as soon
+    // as the tile has landed, its S buffer's previous P has been fed to its PV (issued earlier by
+    // this thread: the tensor pipe runs one thread's MMAs in issue order, so the S product cannot
+    // overwrite P before the PV has read it) and, for an item's first, its Q tile is written
+    const int tw = warp - W_MMA;   // the MMA tile this thread issues for
     if (lane == 0) {
       const uint32_t id_s = idesc_f16(128, KT, false);
+      const uint32_t id_pv = idesc_bf16_bmn(128, D);
       uint32_t gt = 0;
       uint32_t ct[MT] = {0, 0}, ci[MT] = {0, 0};   // per MMA tile: key tiles and items taken part in
       bool ok = true;
@@ -537,30 +515,47 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         const AttnItem it = a.items[ii];
         const int nt = item_tiles(it);
         const int na[MT] = {item_tiles_of(it, 0), item_tiles_of(it, 1)};
-        int js[MT] = {0, 0};
+        int js[MT] = {0, 0}, jp[MT] = {0, 0};   // next S, next PV (key tiles of the item)
         uint32_t idle = 0;
         unsigned long long t_idle = 0;
-        while (js[0] < na[0] || js[1] < na[1]) {
+        while (jp[tw] < na[tw]) {
           bool prog = false;
+          {
+            const int t = tw;
+            if (jp[t] < js[t]) {   // PV of key tile jp once its P is written
+              const uint32_t g = gt + jp[t], c = ct[t] + jp[t];
+              const int b = c & 1, st = g % NST;
+              if (mbar_test(bar(B_PREADY + 2 * t + b), (c >> 1) & 1)) {
+                fence_after();
+                const uint32_t vb = smem_u32(sm + OFF_ST + st * ST_BYTES + 16384);
+                const uint32_t pa = tmem + TM_S + 128 * t + 64 * b + 32;   // P over the S buffer's high half
 #pragma unroll
-          for (int t = 0; t < MT; ++t) {
-            if (js[t] >= na[t]) continue;
-            const uint32_t g = gt + js[t], c = ct[t] + js[t];
-            const int b = c & 1, st = g % NST;
-            if (mbar_test(bar(B_FULL + st), (g / NST) & 1) &&
-                (js[t] > 0 || mbar_test(bar(B_QREADY + t), ci[t] & 1)) &&
-                (c < 2 || mbar_test(bar(B_PVDONE + 2 * t + b), ((c - 2) >> 1) & 1))) {
-              fence_after();
-              const uint32_t qa = smem_u32(sm + OFF_Q + t * Q_TILE), kb = smem_u32(sm + OFF_ST + st * ST_BYTES);
-#pragma unroll
-              for (int k = 0; k < 8; ++k) {   // K dimension 128 = 2 halves x 4 steps of 16
-                const uint32_t off = (k & 3) * 32;
-                umma_ss(tmem + TM_S + 128 * t + 64 * b, desc_kmajor(qa + (k >> 2) * 16384 + off),
-                        desc_kmajor(kb + (k >> 2) * 8192 + off), id_s, k != 0);
+                for (int k = 0; k < 4; ++k)   // K dimension 64 keys = 4 steps of 16 (8 TMEM columns of P each)
+                  umma_ts(tmem + TM_O + 128 * t, pa + 8 * k, desc_mnmajor(vb + k * 2048, 8192), id_pv,
+                          (jp[t] | k) != 0);
+                umma_commit(bar(B_PVDONE + 2 * t + b));
+                umma_commit(bar(B_EMPTY + st));   // the stage's share is released when the PV retires
+                ++jp[t];
+                prog = true;
               }
-              umma_commit(bar(B_SFULL + 2 * t + b));
-              ++js[t];
-              prog = true;
+            }
+            if (js[t] < na[t] && js[t] < jp[t] + 2) {   // S of key tile js into a buffer whose PV is issued
+              const uint32_t g = gt + js[t], c = ct[t] + js[t];
+              const int b = c & 1, st = g % NST;
+              if (mbar_test(bar(B_FULL + st), (g / NST) & 1) &&
+                  (js[t] > 0 || mbar_test(bar(B_QREADY + t), ci[t] & 1))) {
+                fence_after();
+                const uint32_t qa = smem_u32(sm + OFF_Q + t * Q_TILE), kb = smem_u32(sm + OFF_ST + st * ST_BYTES);
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {   // K dimension 128 = 2 halves x 4 steps of 16
+                  const uint32_t off = (k & 3) * 32;
+                  umma_ss(tmem + TM_S + 128 * t + 64 * b, desc_kmajor(qa + (k >> 2) * 16384 + off),
+                          desc_kmajor(kb + (k >> 2) * 8192 + off), id_s, k != 0);
+                }
+                umma_commit(bar(B_SFULL + 2 * t + b));
+                ++js[t];
+                prog = true;
+              }
             }
           }
           if (prog) {
@@ -574,7 +569,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
             ok = false;
             break;
           }
-          __nanosleep(64);   // leave the issue slots of this sub-partition to the softmax
         }
         for (int t = 0; t < MT; ++t)
           if (na[t] > 0) {
@@ -584,8 +578,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         gt += nt;
       }
       if (!ok) s_abort = 1;
-      umma_commit(bar(B_DONE + MT));   // fires once every MMA of this thread has retired
-      mbar_wait(bar(B_DONE + MT), 0);
+      umma_commit(bar(B_DONE + tw));   // fires once every MMA of this thread has retired
+      mbar_wait(bar(B_DONE + tw), 0);
     }
   } else if (warp == W_LOAD) {
     // =============================== loads (lanes issue the boxes; the warp holds page metadata)
