@@ -18,27 +18,31 @@
 // Key tiles stream through a ring of 4 shared-memory stages, each K then V of 64 keys in the
 // layout the MMAs read ([64-dim half][key][128 B], 128-byte swizzled).
 //
-//   warp 9      loads: per key tile, rotated K as two boxes of 4 consecutive scratch pages (one per
+//   warp 10     loads: per key tile, rotated K as two boxes of 4 consecutive scratch pages (one per
 //               64-dim half) and V as two boxes over 4 consecutive pool blocks (pages of a chunk
 //               or a query are allocated consecutively), else one box per full page; a page with
 //               fewer than 16 rows is copied by the warp's lanes with its missing rows zeroed,
 //               and the V rows of pages past the item's end are zeroed (P is 0 there; V must be
 //               finite). The warp also writes each key's position (the causal mask) and holds the
 //               page metadata (its lanes hold a window of 32 pages, the next one prefetched).
-//   warp 8      TMEM owner (all 512 columns: O_t at [128t, 128t + 128), two S buffers of tile t
-//               at 256 + 128t + {0, 64}); one thread issues the S products S_t = Q_t K^T (M128
-//               N64 K128, fp16) of both MMA tiles, each as soon as its key tile has landed and
-//               its S buffer is free -- a key tile ahead of the softmax.
+//   warps 8, 9  one MMA-issuing thread per MMA tile t (warp 8 also owns the TMEM: all 512
+//               columns, O_t at [128t, 128t + 128), two S buffers of tile t at 256 + 128t +
+//               {0, 64}). Per key tile j of its tile, in this order: O_t += P_t(j) V(j) (M128 N128
+//               K64, bf16, P_t from TMEM) as soon as the warpgroup has written P_t(j), then
+//               S_t(j + 2) = Q_t K(j + 2)^T (M128 N64 K128, fp16) into the S buffer that held
+//               P_t(j) as soon as key tile j + 2 has landed. One thread's MMAs run in issue order,
+//               so that S product cannot overwrite P_t(j) before the PV has read it: no wait for
+//               the PV to retire, and the S products stay two key tiles ahead of the softmax.
 //   warps 0-7   MMA tile t = warpgroup t, thread = one MMA row = one TMEM lane. The warpgroup
 //               writes the tile's Q rows into shared memory at the start of an item (the A
-//               operand of its S products); per key tile each thread reads its row of S, masks
-//               keys after its position (only on key tiles that need it), keeps a running
-//               reference maximum and writes P = 2^(S - ref) as bf16 pairs over the S columns,
-//               and the warpgroup's first thread then issues O_t += P_t V (M128 N128 K64, bf16,
-//               P_t from TMEM) at once. O in TMEM is rescaled only when the maximum grows by
-//               more than 2^8 (P stays <= 256); the sum uses the same reference, so O / l is
-//               exact softmax. At the end of an item the warpgroup drains O_t (normalized output,
-//               or the unnormalized partial with its reference maximum and sum for the merge).
+//               operand of its S products); per key tile each thread reads its row of S (64
+//               keys, one TMEM round trip), masks keys after its position (only on key tiles
+//               that need it), keeps a running reference maximum and writes P = 2^(S - ref) as
+//               bf16 pairs over the S columns. O in TMEM is rescaled only when the maximum grows
+//               by more than 2^8 (P stays <= 256); the sum uses the same reference, so O / l is
+//               exact softmax. At the end of an item each warp drains its rows of O_t (normalized
+//               output, or the unnormalized partial with its reference maximum and sum for the
+//               merge).
 // Barrier phases run over the CTA's whole key-tile sequence (and per MMA tile over that tile's
 // own sequence), so the next item's loads overlap the current item's tail. Every wait is
 // bounded; on expiry the CTA raises the device timeout flag, stops issuing work, waits
@@ -93,14 +97,15 @@ constexpr int B_PREADY = B_QREADY + MT;           // [2][2] P_t in buffer b writ
 constexpr int B_DONE = B_PREADY + 2 * MT;         // [2] every MMA of MMA tile t's issuing thread retired
 static_assert(B_DONE + MT <= N_BARS, "barrier slots");
 // Every waiter must observe each phase of a barrier before the barrier can complete the next
-// one (a parity wait cannot tell phase n from n + 2). FULL is waited on by the S issuer and
-// both warpgroups, but a stage can only be refilled after both warpgroups released it, i.e.
-// after each has used that phase (a warpgroup releases a key tile it takes no part in only
-// after waiting for it, so its release never counts toward the stage's previous use), and a
-// warpgroup uses a key tile only after the S issuer issued its S product; EMPTY has only the
-// loader. The S/PV/Q barriers of MMA tile t count that tile's own key tiles and items: S_t into
-// buffer b is issued only after the PV that read buffer b's previous P retired, and the next
-// item's first S_t only after Q_t was rewritten.
+// one (a parity wait cannot tell phase n from n + 2). FULL is waited on by both MMA threads and
+// both warpgroups, but a stage can only be refilled after both MMA tiles released it (the PV
+// retired, or the key tile was waited for and skipped), i.e. after each has used that phase.
+// EMPTY has only the loader. SFULL_t(b) is waited on by the four warps of warpgroup t; the next
+// S product into buffer b follows the PV of P_t in b, which waits for all four warps' PREADY, so
+// every warp has seen the phase. PREADY_t(b) is waited on by MMA thread t only, and a warp
+// writes the next P into b only after that S product. PVDONE is waited on by the warpgroup
+// (rescale, drain) and completes once per PV, each after this warpgroup's P. QREADY_t is waited
+// on by MMA thread t before an item's first S product, and completes once per item.
 
 __device__ int g_attn_timeout = 0;
 
@@ -330,7 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         // this row's q (128 fp16, rotated and scaled) into the K-major, 128-byte-swizzled A
         // operand of the S products: MMA row m = hh * 32 + r, dims 8c..8c+7 of half h at
         // [h][m][chunk c]. Every S product of this tile's previous item has retired (this
-        // warpgroup consumed them), and the next is issued only after QREADY.
+        // warpgroup consumed them), and the next item's are issued only after QREADY.
         const uint4* src =
             reinterpret_cast<const uint4*>(a.q16 + ((size_t)(it.row0 + (mine ? row : 0)) * a.H + it.g * REP + hh) * D);
         const int m = hh * RB + r;
@@ -499,10 +504,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     }
     if (!ok) s_abort = 1;
   } else if (warp < W_MMA + MT) {
-    // =============================== every MMA of the CTA, from one thread: per MMA tile, O_t +=
-    // P_t V of a key tile as soon as the warpgroup has written its P, and S_t of a key tile as soon
-    // as the tile has landed, its S buffer's previous P has been fed to its PV (issued earlier by
-    // this thread: the tensor pipe runs one thread's MMAs in issue order, so the S product cannot
+    // =============================== every MMA of MMA tile tw, from one thread: O_t += P_t V of a
+    // key tile as soon as the warpgroup has written its P, and S_t of a key tile as soon as the
+    // tile has landed, its S buffer's previous P has been fed to its PV (issued earlier by this
+    // thread: the tensor pipe runs one thread's MMAs in issue order, so the S product cannot
     // overwrite P before the PV has read it) and, for an item's first, its Q tile is written
     const int tw = warp - W_MMA;   // the MMA tile this thread issues for
     if (lane == 0) {
