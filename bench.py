@@ -249,11 +249,14 @@ def run_reference(args):
 
 def make_store(model, wl, extra_positions=0):
     """A store sized for the workload: its chunks, one private block per chunk per request and
-    the query pages (with slack), every request's positions, and rows for a compile call of 4
-    chunks behind their dummy prefix (LegoLink-0)."""
+    the query pages (with slack), a private copy of every chunk block, every request's
+    positions, and rows for a compile call of 4 chunks behind their dummy prefix (LegoLink-0)."""
     from position_independent_kv_link_gb300 import PicStore
     n_pos = max(sum(len(wl.chunks[c]) for c in r.chunk_ids) + len(r.query) for r in wl.requests)
-    n_blocks = sum(-(-len(c) // 16) for c in wl.chunks) + 4 * (wl.selected_rows // 16 + 2 * len(wl.requests) * 10)
+    chunk_blocks = sum(-(-len(c) // 16) for c in wl.chunks)
+    # room for every chunk block made private once (a dynamic-selection link may choose a token
+    # in each of them), plus the static links' private and query blocks
+    n_blocks = 2 * chunk_blocks + 4 * (wl.selected_rows // 16 + 2 * len(wl.requests) * 10)
     compile_rows = max(sum(len(c) + wl.n_dummy for c in wl.chunks[i:i + 4]) for i in range(0, len(wl.chunks), 4))
     return PicStore(model, num_blocks=n_blocks, max_rows=max(wl.selected_rows, compile_rows, 2048),
                     max_requests=max(len(wl.requests), 64), max_positions=n_pos + 80 + extra_positions,
@@ -433,6 +436,7 @@ def run_ours(args):
     d2h = hid.numel() * 4 + lg.numel() * 4
 
     dec = time_decode(store, reqs, wl, 3, args.steps, stream, world, barrier)
+    dyn = time_dynamic(store, reqs, wl, 15, 3, args.steps, stream, world, barrier)
     cpool = time_compile_pool(model, spec, pk, world, barrier) if spec.n_layers == 32 else None
 
     rl = roofline_link(wl, pk)
@@ -475,6 +479,10 @@ def run_ours(args):
         "clocks": clk,
         "compile": {"tokens_per_s": compiled_tokens / compile_s, "ms": compile_s * 1e3, "chunks": len(wl.chunks)},
         "compile_pool": cpool,
+        "dynamic": {"what": "pic_link_dynamic at r = 15 % (CacheBlend-15, the pages' comparison point): layer-0 "
+                            "query attention scores for every prompt token, the top 15 % chosen on the GPU, the "
+                            "link over the chosen rows and the query; against the LegoLink-16 step above",
+                    **dyn, "static_ms_per_step": ms_step, "ratio_to_static": dyn["ms_per_step"] / ms_step},
         "decode": {"what": "pic_decode after the link: one generated token per request per step, attending to "
                            "the request's linked KV (RoPE at load)",
                    "requests": n_r, "steps": args.steps, "ms_per_step": dec_ms / args.steps,
@@ -557,6 +565,46 @@ def time_decode(store, reqs, wl, warmup, steps, stream, world, barrier):
                    "GBs": v["bytes"] / (v["ms"] / 1e3) / 1e9 if v["ms"] > 0 else None}
                for k, v in prof.items() if isinstance(v, dict)}
     return {"ms": ms, "requests": n_r, "launches": launches, "kernels": kernels}
+
+
+def time_dynamic(store, reqs, wl, r_percent, warmup, steps, stream, world, barrier):
+    """Times `steps` links of the workload's requests with dynamic (attention-based) token
+    selection at r % (pic_link_dynamic: the layer-0 scoring pass, the wait for its choice, then
+    the link over the chosen rows) after `warmup`, then the same steps under per-launch
+    profiling. Every request is released after its step."""
+    def step():
+        res = store.link_dynamic(reqs, r_percent)
+        for h in res.requests:
+            store.release_request(h)
+        return res
+    for _ in range(warmup):
+        step()
+    store.sync()
+    barrier()
+    n0 = store.launch_count()
+    t0 = time.perf_counter()
+    d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    d0.record(stream)
+    for _ in range(steps):
+        res = step()
+    d1.record(stream)
+    torch.cuda.synchronize()
+    wall = (time.perf_counter() - t0) * 1e3 / steps
+    store.sync()
+    barrier()
+    ms = slowest_rank(d0.elapsed_time(d1), world) / steps
+    launches = (store.launch_count() - n0) / steps
+    store.profile_begin()
+    for _ in range(steps):
+        step()
+    prof = store.profile_end()
+    store.sync()
+    rows = sum(int(r_percent * sum(len(wl.chunks[c]) for c in q.chunk_ids) // 100) + len(q.query)
+               for q in wl.requests)
+    kernels = {k: {"ms_per_step": v["ms"] / steps, "launches_per_step": v["launches"] / steps}
+               for k, v in prof.items() if isinstance(v, dict) and v["launches"] > 0}
+    return {"r_percent": r_percent, "ms_per_step": ms, "wall_ms_per_step": wall, "selected_rows": rows,
+            "gpu_launches_per_step": launches, "kernels": kernels}
 
 
 def compile_flops_per_token(spec, L: int) -> float:
@@ -673,7 +721,10 @@ def run_decode(args):
     spec = wl.spec
     model = PicModel(spec, pi.gen_weights(spec))
     n_pos = max(sum(len(wl.chunks[c]) for c in r.chunk_ids) + len(r.query) for r in wl.requests)
-    n_blocks = sum(-(-len(c) // 16) for c in wl.chunks) + 4 * (wl.selected_rows // 16 + 2 * len(wl.requests) * 10)
+    chunk_blocks = sum(-(-len(c) // 16) for c in wl.chunks)
+    # room for every chunk block made private once (a dynamic-selection link may choose a token
+    # in each of them), plus the static links' private and query blocks
+    n_blocks = 2 * chunk_blocks + 4 * (wl.selected_rows // 16 + 2 * len(wl.requests) * 10)
     store = PicStore(model, num_blocks=n_blocks, max_rows=max(wl.selected_rows, 2048),
                      max_requests=max(len(wl.requests), 64), max_positions=n_pos + 80 + 2 * args.steps + args.warmup,
                      max_logit_rows=max(64, len(wl.requests)))

@@ -47,7 +47,8 @@ constexpr int BK = 64;           // K per stage: 64 bf16 = one 128-byte swizzle 
 constexpr int UMMA_K = 16;       // K per tcgen05.mma (kind::f16)
 constexpr int A_STAGE = BM * BK * 2;   // 16 KB
 constexpr int EPI_ROWS = 16;     // token rows per reduce-add tile
-constexpr int EPI_BYTES = EPI_ROWS * BM * 4;  // 8 KB, double buffered
+constexpr int EPI_COLS = 32;     // weight rows per reduce-add tile: one epilogue warp's TMEM lane quarter
+constexpr int EPI_BYTES = EPI_ROWS * BM * 4;  // 8 KB: the four warps' tiles, double buffered
 constexpr int kWarps = 7;
 constexpr int kThreads = kWarps * 32;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
@@ -147,16 +148,21 @@ __device__ __forceinline__ void umma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
 
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
-  uint32_t r[16];
+// tcgen05.ld of 16 columns without waiting; tmem_wait16 on the same registers before using them
+// (the registers are operands of the wait, so no use can be scheduled ahead of it)
+__device__ __forceinline__ void tmem_ld16_async(uint32_t taddr, uint32_t* r) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
         "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
       : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_wait16(uint32_t* r) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
+               :
+               : "memory");
 }
 
 // named barrier of the four epilogue warps
@@ -368,7 +374,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp >= 3) {
     // ---------------- epilogue: TMEM -> [16 tokens][128 rows] fp32 tile -> bulk reduce-add into Y
     const int q = warp & 3;                    // TMEM lane quarter this warp may access
-    const int nl = q * 32 + lane;              // weight row within the tile
     const bool leader = (warp == 3 && lane == 0);
     float* stg = reinterpret_cast<float*>(epi);
     asm volatile("griddepcontrol.wait;" ::: "memory");   // Y is written by earlier kernels
@@ -402,7 +407,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       asm volatile("tcgen05.fence::after_thread_sync;");
       const int m0 = (sg.tile % p.m_tiles) * BM, t0 = (sg.tile / p.m_tiles) * p.BN;
       const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + ab * p.BN;
-      if (p.tile_ready && leader) {
+      if (p.tile_ready && lane == 0) {
         // the tile's zeroing (by the CTA holding its first k-block) has landed
         const unsigned long long w0 = gtimer();
         for (uint32_t i = 0;; ++i) {
@@ -417,26 +422,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         asm volatile("fence.proxy.async.global;" ::: "memory");   // the reduce-adds come after the zeroes
       }
+      // Each warp drains its own 32 weight rows on its own: 16 token columns per step from TMEM
+      // (the next step's load in flight while this one is staged) into its [16][32] fp32 tile,
+      // bulk reduce-added into Y by the warp's first lane, two tiles alternating.
+      float* W = stg + q * (2 * EPI_ROWS * EPI_COLS);
+      uint32_t cur[16], nxt[16];
+      tmem_ld16_async(taddr, cur);
+      tmem_wait16(cur);
       for (int c = 0; c < p.BN; c += EPI_ROWS) {
-        float v[16];
-        tmem_ld16(taddr + c, v);
-        float* S = stg + buf * (EPI_ROWS * BM);
+        if (c + EPI_ROWS < p.BN) tmem_ld16_async(taddr + c + EPI_ROWS, nxt);
+        float* S = W + buf * (EPI_ROWS * EPI_COLS);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) S[j * BM + nl] = v[j];
+        for (int j = 0; j < 16; ++j) S[j * EPI_COLS + lane] = __uint_as_float(cur[j]);
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        epi_bar();
-        if (leader) {
+        __syncwarp();
+        if (lane == 0) {
           if (t0 + c < p.T)
             asm volatile(
                 "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
                     reinterpret_cast<uint64_t>(&map_y)),
-                "r"(m0), "r"(t0 + c), "r"(smem_u32(S))
+                "r"(m0 + q * EPI_COLS), "r"(t0 + c), "r"(smem_u32(S))
                 : "memory");
           asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-          asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");  // the other buffer is free again
+          asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");  // the other tile is free again
         }
-        epi_bar();
+        __syncwarp();
         buf ^= 1;
+        if (c + EPI_ROWS < p.BN) {
+          tmem_wait16(nxt);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) cur[j] = nxt[j];
+        }
       }
       // the MMAs of the segment after next may overwrite this accumulator
       asm volatile("tcgen05.fence::before_thread_sync;");
@@ -444,7 +460,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(smem_u32(acc_empty + ab));
       ++s;
     }
-    if (leader) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+    if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
   }
   __syncwarp();
   asm volatile("tcgen05.fence::before_thread_sync;");
@@ -488,13 +504,13 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
   return fn;
 }
 
-// fp32 [rows][cols] destination of the bulk reduce-add; box = 128 columns x EPI_ROWS rows
+// fp32 [rows][cols] destination of the bulk reduce-add; box = EPI_COLS columns x EPI_ROWS rows
 bool make_map_f32(CUtensorMap* m, void* base, int rows, int cols) {
   auto enc = get_encode();
   if (!enc) return false;
   cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)cols * 4};
-  cuuint32_t box[2] = {(cuuint32_t)BM, (cuuint32_t)EPI_ROWS};
+  cuuint32_t box[2] = {(cuuint32_t)EPI_COLS, (cuuint32_t)EPI_ROWS};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                    CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
