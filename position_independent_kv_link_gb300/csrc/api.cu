@@ -163,6 +163,9 @@ struct pic_store {
   // on first need to the largest page count seen
   __half* krot = nullptr;
   int krot_pages = 0;
+  // query-key logits of a dynamic-selection pass: grown on first need to the largest pass seen
+  float* sel_logits = nullptr;
+  size_t sel_logits_cap = 0;
   int32_t* meta_h = nullptr;  // pinned staging
   cudaEvent_t meta_ev = nullptr;
   bool meta_ev_pending = false;
@@ -834,6 +837,7 @@ pic_status pic_store_destroy(pic_store* s) {
   }
   cudaFree(s->ws);
   cudaFree(s->krot);
+  cudaFree(s->sel_logits);
   cudaFreeHost(s->meta_h);
   delete s;
   return PIC_OK;
@@ -1055,6 +1059,8 @@ pic_status pic_link_dynamic(pic_store* s, const pic_link_request* reqs, int32_t 
     R.page0 = (int)pblk.size();
     R.tok0 = r ? sr[r - 1].tok0 + sr[r - 1].n_tok : 0;
     R.out0 = r ? sr[r - 1].out0 + sr[r - 1].n_pick : 0;
+    R.kb0 = r ? sr[r - 1].kb0 + ceil_div(sr[r - 1].n_tok + sr[r - 1].lq, kSelectKeyBlock) : 0;
+    R.pkb0 = r ? sr[r - 1].pkb0 + ceil_div(sr[r - 1].n_tok, kSelectKeyBlock) : 0;
     int N = 0;
     for (int i = 0; i < q.n_chunks; ++i) {
       const Chunk& ch = s->chunks[q.chunks[i]];
@@ -1101,6 +1107,22 @@ pic_status pic_link_dynamic(pic_store* s, const pic_link_request* reqs, int32_t 
     const size_t ml_floats = (size_t)n_rows * H * 2, sc_floats = scores_out ? 0 : (size_t)n_tok;
     if (ml_floats + sc_floats > (size_t)s->cfg.max_rows * 2 * c.ffn_dim)
       return fail(PIC_ERR_CAPACITY, "prompt tokens exceed the scoring workspace");
+    // every query row's logits against every key it may see, per request
+    size_t n_logits = 0;
+    for (SelectReq& R : sr) {
+      if (n_logits > (size_t)INT32_MAX) break;
+      R.lg0 = (int)n_logits;
+      n_logits += (size_t)R.lq * H * (R.n_tok + R.lq);
+    }
+    if (n_logits > (size_t)INT32_MAX) return fail(PIC_ERR_CAPACITY, "dynamic selection: too many query-key logits");
+    if (n_logits > s->sel_logits_cap) {
+      // cudaFree waits for the kernels still reading the old scratch
+      PIC_CUDA(cudaFree(s->sel_logits));
+      s->sel_logits = nullptr;
+      s->sel_logits_cap = 0;
+      PIC_CUDA(cudaMalloc(&s->sel_logits, n_logits * sizeof(float)));
+      s->sel_logits_cap = n_logits;
+    }
     const size_t n_int = tok.size() + 3 * pblk.size() + (size_t)kSelectReqInts * n_reqs + n_out;
     if (n_int > s->meta_cap) return fail(PIC_ERR_CAPACITY, "metadata exceeds workspace");
     if (s->meta_ev_pending) {
@@ -1151,13 +1173,17 @@ pic_status pic_link_dynamic(pic_store* s, const pic_link_request* reqs, int32_t 
     a.page_len = d_plen;
     a.rope_cs = s->rope_cs;
     a.qrot = s->q;
+    a.logits = s->sel_logits;
+    a.n_kb = sr.back().kb0 + ceil_div(sr.back().n_tok + sr.back().lq, kSelectKeyBlock);
+    a.n_pkb = sr.back().pkb0 + ceil_div(sr.back().n_tok, kSelectKeyBlock);
     a.ml = s->gu_acc;
     a.scores = scores_out ? scores_out : s->gu_acc + ml_floats;
     a.chosen = s->meta_d + o_chosen;
     {
-      double pairs = 0;   // (query row, key) pairs scored twice, once per pass
+      double pairs = 0;   // (query row, visible key) pairs: one logit each
       for (const SelectReq& R : sr) pairs += (double)R.lq * R.n_tok + (double)R.lq * (R.lq + 1) / 2;
-      Rec rc(s, st, PIC_PROF_SELECT, 2.0 * n_tok * G * D * es + (double)n_rows * H * D * 8, pairs * H * D * 4.0 * 2, 3);
+      Rec rc(s, st, PIC_PROF_SELECT, (double)n_tok * G * D * es + (double)n_rows * H * D * 8 + 3.0 * n_logits * 4,
+             pairs * H * D * 2.0, 5);
       if ((e = launch_select(a, D, c.dtype, st)) != PIC_OK) return e;
     }
     if (n_out) PIC_CUDA(cudaMemcpyAsync(hp + o_chosen, a.chosen, (size_t)n_out * 4, cudaMemcpyDeviceToHost, st));

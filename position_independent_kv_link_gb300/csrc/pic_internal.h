@@ -228,15 +228,19 @@ size_t attention_part_bytes(int n_parts, int rep, int D);
 // ------------------------------------------------------------------ dynamic selection (k_select.cu)
 // One request of a dynamic-selection pass: its query rows [row0, row0 + lq) of the pass's
 // layer-0 QKV rows, its n_tok prompt tokens (scores [tok0, tok0 + n_tok)), its prompt pages
-// [page0, page0 + n_pages) of the pass's page arrays, and the n_pick positions it keeps
-// (chosen[out0, out0 + n_pick), ascending).
+// [page0, page0 + n_pages) of the pass's page arrays, the n_pick positions it keeps
+// (chosen[out0, out0 + n_pick), ascending), its blocks of 64 keys over the prompt and the
+// query (from kb0) and over the prompt alone (from pkb0), and its logits [lq][H][n_tok + lq]
+// from float lg0 of the logits scratch.
 struct SelectReq {
-  int row0, lq, n_tok, tok0, page0, n_pages, n_pick, out0;
+  int row0, lq, n_tok, tok0, page0, n_pages, n_pick, out0, kb0, pkb0, lg0;
 };
 constexpr int kSelectReqInts = sizeof(SelectReq) / sizeof(int);
+constexpr int kSelectKeyBlock = 64;   // keys per block of the scoring kernels
 struct SelectArgs {
-  const SelectReq* reqs;    // device, ascending row0 and tok0
+  const SelectReq* reqs;    // device, ascending row0, tok0, kb0, pkb0
   int n_reqs, n_rows, n_tok, H, G;
+  int n_kb, n_pkb;          // key blocks over prompt + query keys, over prompt keys (all requests)
   const float* qkv;         // [n_rows][(H + 2G) D] fp32 layer-0 projections of the query rows
   const void* k_layer0;     // layer 0 of the K pool [blocks][G][16][D], model dtype, pre-RoPE
   const int* page_block;    // pages of every request's prompt, position order
@@ -244,11 +248,12 @@ struct SelectArgs {
   const int* page_len;
   const float2* rope_cs;    // [positions][D/2]
   float* qrot;              // scratch [n_rows][H][D]
-  float* ml;                // scratch [n_rows][H][2]
+  float* logits;            // scratch, the requests' logits (SelectReq::lg0)
+  float* ml;                // scratch [n_rows][H][2]: max, 1 / sum
   float* scores;            // [n_tok] out
   int* chosen;              // out
 };
-// Scores every prompt token and writes each request's chosen positions (3 launches).
+// Scores every prompt token and writes each request's chosen positions (5 launches).
 pic_status launch_select(const SelectArgs& a, int D, int dtype, cudaStream_t st);
 
 void rope_table_host(int n_pos, int D, double base, std::vector<float2>& out);
