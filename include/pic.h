@@ -205,7 +205,11 @@ pic_status pic_link(pic_store* s, const pic_link_request* reqs, int32_t n_reqs, 
  * scores_out: NULL, or a device fp32 array of sum(N) that receives every request's token
  * scores in order. Capacities as pic_link (sum of kept tokens + query rows <= max_rows);
  * PIC_ERR_CAPACITY also when the scoring scratch (2 x query rows x n_heads + sum(N) floats,
- * the latter only when scores_out is NULL) exceeds max_rows x 2 x ffn_dim floats. */
+ * the latter only when scores_out is NULL) exceeds max_rows x 2 x ffn_dim floats, or when
+ * the pass's logits (query_len x n_heads x (N + query_len) per request) exceed 2^31 floats.
+ * The logits live in a device scratch the store allocates at the first scoring pass and grows
+ * (cudaFree + cudaMalloc, which synchronize the device) when a later pass needs more; it is
+ * freed with the store. */
 pic_status pic_link_dynamic(pic_store* s, const pic_link_request* reqs, int32_t n_reqs, int32_t r_percent,
                             int32_t all_logits, float* hidden_out, float* logits_out, float* scores_out,
                             pic_stream_t stream, pic_request* out_requests);
