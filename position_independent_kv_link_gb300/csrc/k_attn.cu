@@ -129,21 +129,40 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(AttnArgs a) {
     if (s < c.nparts) {
       const float2 ml = *reinterpret_cast<const float2*>(a.part_ml + part(s) * 2);
       if (ml.y > 0.f) {
-        w = exp2f(ml.x - M);
-        L += w * ml.y;
+        // fp32 partials hold the part's unnormalized sum (reference max ml.x); fp16 partials
+        // hold it divided by the part's own sum ml.y
+        w = a.part_f16 ? exp2f(ml.x - M) * ml.y : exp2f(ml.x - M);
+        L += a.part_f16 ? w : w * ml.y;
       }
     }
     const int n = min(32, c.nparts - s0);
+    if (a.part_f16) {
 #pragma unroll 4
-    for (int k = 0; k < n; ++k) {
-      const float wk = __shfl_sync(0xffffffffu, w, k);
-      const float* src = a.part_o + part(s0 + k) * D + lane * NJ;
-      if constexpr (NJ == 4) {
-        const float4 x = *reinterpret_cast<const float4*>(src);
-        o[0] += wk * x.x, o[1] += wk * x.y, o[2] += wk * x.z, o[3] += wk * x.w;
-      } else {
-        const float2 x = *reinterpret_cast<const float2*>(src);
-        o[0] += wk * x.x, o[1] += wk * x.y;
+      for (int k = 0; k < n; ++k) {
+        const float wk = __shfl_sync(0xffffffffu, w, k);
+        const __half* src = reinterpret_cast<const __half*>(a.part_o) + part(s0 + k) * D + lane * NJ;
+        if constexpr (NJ == 4) {
+          const uint2 u = *reinterpret_cast<const uint2*>(src);
+          const float2 x0 = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
+          const float2 x1 = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+          o[0] += wk * x0.x, o[1] += wk * x0.y, o[2] += wk * x1.x, o[3] += wk * x1.y;
+        } else {
+          const float2 x = __half22float2(*reinterpret_cast<const __half2*>(src));
+          o[0] += wk * x.x, o[1] += wk * x.y;
+        }
+      }
+    } else {
+#pragma unroll 4
+      for (int k = 0; k < n; ++k) {
+        const float wk = __shfl_sync(0xffffffffu, w, k);
+        const float* src = a.part_o + part(s0 + k) * D + lane * NJ;
+        if constexpr (NJ == 4) {
+          const float4 x = *reinterpret_cast<const float4*>(src);
+          o[0] += wk * x.x, o[1] += wk * x.y, o[2] += wk * x.z, o[3] += wk * x.w;
+        } else {
+          const float2 x = *reinterpret_cast<const float2*>(src);
+          o[0] += wk * x.x, o[1] += wk * x.y;
+        }
       }
     }
   }
@@ -198,9 +217,10 @@ pic_status attention_prepare_tc(AttnArgs& a, int T, int pool_blocks, __half* q16
 
 void launch_attention(const AttnArgs& a, cudaStream_t st) {
   if (tc_attention_supported(a.dtype, a.D, a.H / a.G)) {
-    launch_attention_tc(a, st);
-    if (a.n_combines > 0) {
-      AttnArgs b = a;
+    AttnArgs b = a;
+    b.part_f16 = 1;
+    launch_attention_tc(b, st);
+    if (b.n_combines > 0) {
       b.n_items = 0;  // merge only
       launch_attention_simt(b, st);
     }

@@ -41,8 +41,8 @@
 //               bf16 pairs over the S columns. O in TMEM is rescaled only when the maximum grows
 //               by more than 2^8 (P stays <= 256); the sum uses the same reference, so O / l is
 //               exact softmax. At the end of an item each warp drains its rows of O_t (normalized
-//               output, or the unnormalized partial with its reference maximum and sum for the
-//               merge).
+//               output, or for a split item O / l in fp16 with its reference maximum and sum
+//               for the merge).
 // Barrier phases run over the CTA's whole key-tile sequence (and per MMA tile over that tile's
 // own sequence), so the next item's loads overlap the current item's tail. Every wait is
 // bounded; on expiry the CTA raises the device timeout flag, stops issuing work, waits
@@ -324,30 +324,36 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       it_n = a.items[blockIdx.x];
       qp_n = row < it_n.nrows ? a.q_pos[it_n.row0 + row] : -1;
     }
+    // this row's q of item itq (128 fp16, rotated and scaled) into the K-major, 128-byte-swizzled
+    // A operand of the S products: MMA row m = hh * 32 + r, dims 8c..8c+7 of half h at
+    // [h][m][chunk c]; every load is issued before the first store. Called once every S product
+    // of this tile's previous item has retired (this warp consumed the last one), so the next
+    // item's Q is in place while the current item's last PV and drain run; its S products are
+    // issued only after QREADY.
+    auto write_q = [&](const AttnItem& itq) {
+      if (item_tiles_of(itq, t) <= 0) return;
+      const bool mq = row < itq.nrows;
+      const uint4* src =
+          reinterpret_cast<const uint4*>(a.q16 + ((size_t)(itq.row0 + (mq ? row : 0)) * a.H + itq.g * REP + hh) * D);
+      uint4 x[16];
+#pragma unroll
+      for (int c = 0; c < 16; ++c) x[c] = mq ? src[c] : make_uint4(0, 0, 0, 0);
+      const int m = hh * RB + r;
+#pragma unroll
+      for (int c = 0; c < 16; ++c) *reinterpret_cast<uint4*>(qs + (c >> 3) * 16384 + sw128(m, c & 7)) = x[c];
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_QREADY + t));
+    };
     asm volatile("griddepcontrol.wait;" ::: "memory");   // q16 is written by the previous kernel
+    if (blockIdx.x < a.n_items) write_q(it_n);
     for (int ii = blockIdx.x; ii < a.n_items; ii += gridDim.x) {
       const AttnItem it = it_n;
       const int qp = qp_n;
-      if (ii + (int)gridDim.x < a.n_items) it_n = a.items[ii + gridDim.x];
+      const bool has_next = ii + (int)gridDim.x < a.n_items;
+      if (has_next) it_n = a.items[ii + gridDim.x];
       const int nt = item_tiles(it), na = item_tiles_of(it, t);
       const bool mine = row < it.nrows;
-      if (na > 0) {
-        // this row's q (128 fp16, rotated and scaled) into the K-major, 128-byte-swizzled A
-        // operand of the S products: MMA row m = hh * 32 + r, dims 8c..8c+7 of half h at
-        // [h][m][chunk c]. Every S product of this tile's previous item has retired (this
-        // warpgroup consumed them), and the next item's are issued only after QREADY.
-        const uint4* src =
-            reinterpret_cast<const uint4*>(a.q16 + ((size_t)(it.row0 + (mine ? row : 0)) * a.H + it.g * REP + hh) * D);
-        const int m = hh * RB + r;
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const uint4 x = mine ? src[c] : make_uint4(0, 0, 0, 0);
-          *reinterpret_cast<uint4*>(qs + (c >> 3) * 16384 + sw128(m, c & 7)) = x;
-        }
-        fence_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(B_QREADY + t));
-      }
       if (s_abort) {
         ok = false;
         break;
@@ -455,8 +461,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         ++ct;
       }
       if (!ok) break;
-      if (ii + (int)gridDim.x < a.n_items) qp_n = row < it_n.nrows ? a.q_pos[it_n.row0 + row] : -1;
-      // ---- drain O_t: normalized output, or the unnormalized partial with its reference max and sum
+      if (has_next) {
+        write_q(it_n);   // every S product of this item has been consumed by this warp
+        qp_n = row < it_n.nrows ? a.q_pos[it_n.row0 + row] : -1;
+      }
+      // ---- drain O_t: normalized output, or (split item) O / l in fp16 with its reference max and sum
       bool okd = true;
       if (na > 0) {
         okd = __all_sync(0xffffffffu, mbar_wait(bar(B_PVDONE + 2 * t + ((ct - 1) & 1)), ((ct - 1) >> 1) & 1));
@@ -486,11 +495,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
                                     pack_f16x2(o[8 * c + 4] * inv, o[8 * c + 5] * inv),
                                     pack_f16x2(o[8 * c + 6] * inv, o[8 * c + 7] * inv));
             }
-          } else if (mine) {
-            float4* dst =
-                reinterpret_cast<float4*>(a.part_o + (((size_t)it.part * kAttnPartRows + row) * REP + hh) * D + c0);
+          } else if (mine) {   // split partial: O / l in fp16 (within V's range), merged with (max, l)
+            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__half*>(a.part_o) +
+                                                  (((size_t)it.part * kAttnPartRows + row) * REP + hh) * D + c0);
 #pragma unroll
-            for (int e = 0; e < 16; ++e) dst[e] = make_float4(o[4 * e], o[4 * e + 1], o[4 * e + 2], o[4 * e + 3]);
+            for (int c = 0; c < 8; ++c)
+              dst[c] = make_uint4(pack_f16x2(o[8 * c] * inv, o[8 * c + 1] * inv),
+                                  pack_f16x2(o[8 * c + 2] * inv, o[8 * c + 3] * inv),
+                                  pack_f16x2(o[8 * c + 4] * inv, o[8 * c + 5] * inv),
+                                  pack_f16x2(o[8 * c + 6] * inv, o[8 * c + 7] * inv));
           }
         }
         if (it.part >= 0 && mine) {

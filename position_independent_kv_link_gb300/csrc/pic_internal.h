@@ -176,7 +176,8 @@ struct AttnArgs {
   const int* page_len;
   const float2* rope_cs;    // [max_pos][D/2]
   void* out;                // [T][H][D] activation type (fp16 for bf16 KV, fp32 for fp32 KV)
-  float* part_o;            // [parts][kAttnPartRows][rep][D]
+  float* part_o;            // [parts][kAttnPartRows][rep][D]: fp32 unnormalized sums, or (part_f16) fp16 O / l
+  int part_f16;             // the tensor-core kernel writes its split partials normalized, in fp16
   float* part_ml;           // [parts][kAttnPartRows][rep][2]
   const AttnItem* items;
   int n_items;
