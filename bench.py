@@ -8,7 +8,7 @@ and LM head. The chunks are compiled once before timing (compile is reported
 separately). Metric: linked prompt tokens per second (chunk + query tokens / link
 latency). Inputs (15 GB of weights, 0.68 GB of KV) are far larger than L2.
 
-  python bench.py [--gpus N --steps K --warmup W] [--impl reference] [--config c2]
+  python bench.py [--gpus N --steps K --warmup W] [--impl reference] [--config 8b_10x512]
 
 Under torchrun each rank runs an independent replica (requests are independent, so
 the link step shards by request with no collective); value = all ranks' tokens / the
@@ -41,7 +41,7 @@ UNIT = "tokens/s"
 # model of the same width (every layer's four projections are the same launches), scaled to 32
 # layers + the LM head (32 x 475.29 MB + 1051.71 MB over 129 launches), on the kernel source
 # whose sha256 prefix is recorded beside it; reported as null once that source changes.
-GEMM_TRAFFIC = {"src_sha256_12": "e57463c5f186", "bytes_per_launch": 126054682, "shape": "all launches of a c2 step"}
+GEMM_TRAFFIC = {"src_sha256_12": "e57463c5f186", "bytes_per_launch": 126054682, "shape": "all launches of an 8B 10x512 link step"}
 
 
 def kernel_sha() -> str:
@@ -450,7 +450,7 @@ def run_ours(args):
     g_ms, g_bytes, g_n = sum(v["ms"] for v in gl), sum(v["bytes"] for v in gl), sum(v["launches"] for v in gl)
     achieved = g_bytes / (g_ms / 1e3) / 1e9 if g_ms > 0 else None
     traffic = None
-    if GEMM_TRAFFIC["src_sha256_12"] == kernel_sha() and GEMM_TRAFFIC.get("shape") == "all launches of a c2 step":
+    if GEMM_TRAFFIC["src_sha256_12"] == kernel_sha() and GEMM_TRAFFIC.get("shape") == "all launches of an 8B 10x512 link step":
         traffic = GEMM_TRAFFIC["bytes_per_launch"]
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -493,15 +493,16 @@ def run_ours(args):
         "setup_s": {"weights_gen": t_gen},
     }
     # the other evaluated configurations on the same model (the 8B shape): link throughput, the
-    # link roofline and per-class kernel times; c5 at k = 16 is the headline workload itself
+    # link roofline and per-class kernel times; the k sweep at k = 16 is the headline workload itself
     if not args.no_configs and spec.n_layers == 32:
         cfgs = {}
-        for name, n in (("c3", 5), ("c4", 5), ("c5_k0", 10), ("c5_k2", 10), ("c5_k32", 10), ("c5_k512", 5)):
+        for name, n in (("8b_98x512", 5), ("8b_32req", 5), ("8b_10x512_k0", 10), ("8b_10x512_k2", 10),
+                        ("8b_10x512_k32", 10), ("8b_10x512_k512", 5)):
             try:
                 cfgs[name] = measure_config(model, name, pk, min(n, args.steps), 3)
             except Exception as e:   # reported in the line, never fatal to it
                 cfgs[name] = {"error": repr(e)[:300]}
-        cfgs["c5_k16"] = {"same_as": "the headline workload (c2)"}
+        cfgs["8b_10x512_k16"] = {"same_as": "the headline workload (8b_10x512)"}
         line["configs"] = cfgs
     if cpu_weights is not None:
         try:
@@ -623,7 +624,7 @@ def time_compile_pool(model, spec, pk, world, barrier):
     tokens), 4 chunks (2048 rows) per pic_compile call after one warm-up call; every chunk's KV
     stays resident until the end. CUDA events around the 16 timed calls."""
     from position_independent_kv_link_gb300 import PicStore
-    wl4 = pi.config_workloads(spec)["c4"]
+    wl4 = pi.config_workloads(spec)["8b_32req"]
     pool = wl4.chunks
     L = len(pool[0])
     per_call = 4
@@ -687,7 +688,7 @@ def run_compile(args):
     torch.cuda.set_device(0)
     spec = workload(args.config).spec
     model = PicModel(spec, pi.gen_weights(spec))
-    pool = pi.config_workloads(spec)["c4"].chunks
+    pool = pi.config_workloads(spec)["8b_32req"].chunks
     per_call, n_calls = 4, max(1, args.warmup) + args.steps
     batch = lambda i: [pool[(per_call * i + j) % len(pool)] for j in range(per_call)]
     st = PicStore(model, num_blocks=n_calls * sum(-(-len(c) // 16) for c in batch(0)) + 8,
@@ -856,7 +857,8 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--config", default="c2", help="tiny, c2, c3, c4, c5_k{0,2,16,32,512}")
+    ap.add_argument("--config", default="8b_10x512",
+                    help="tiny, 8b_10x512, 8b_98x512, 8b_32req, 8b_10x512_k{0,2,16,32,512}")
     ap.add_argument("--cpu-layers", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", action="store_true", help="skip the other configurations' link measurements")

@@ -258,15 +258,18 @@ def make_workload(name: str, spec: ModelSpec, n_chunks: int, chunk_len, query_le
 
 
 def config_workloads(spec_8b: ModelSpec = LLAMA3_8B) -> Dict[str, Workload]:
-    """The five evaluated configurations (keys: tiny, c2, c3, c4, c5_k{0,2,16,32,512})."""
+    """The evaluated workloads, keyed by shape: tiny (fp32, 4 x 64 + 16, k = 2), 8b_10x512 (10 x 512 +
+    64 query, k = 16), 8b_98x512 (98 x 512 + 64, k = 16), 8b_32req (32 requests x 8 Zipf chunks of
+    a 64-chunk pool + 32 query, k = 16) and the k sweep 8b_10x512_k{0,2,16,32,512} (k = 0 with
+    the LegoLink-0 dummy prefix)."""
     w = {
         "tiny": make_workload("tiny: 4x64 + 16 query, k=2", TINY, 4, 64, 16, 2),
-        "c2": make_workload("8B: 10x512 + 64 query, k=16", spec_8b, 10, 512, 64, 16),
-        "c3": make_workload("8B long: 98x512 + 64 query, k=16", spec_8b, 98, 512, 64, 16),
-        "c4": make_workload("8B batched: 32 req x (8x512 Zipf from 64) + 32 query, k=16",
+        "8b_10x512": make_workload("8B: 10x512 + 64 query, k=16", spec_8b, 10, 512, 64, 16),
+        "8b_98x512": make_workload("8B long: 98x512 + 64 query, k=16", spec_8b, 98, 512, 64, 16),
+        "8b_32req": make_workload("8B batched: 32 req x (8x512 Zipf from 64) + 32 query, k=16",
                             spec_8b, 64, 512, 32, 16, n_requests=32, pool=64, per_request=8),
     }
     for k in (0, 2, 16, 32, 512):
-        w[f"c5_k{k}"] = make_workload(f"8B ablation: 10x512 + 64 query, k={k}", spec_8b, 10, 512, 64, k,
+        w[f"8b_10x512_k{k}"] = make_workload(f"8B ablation: 10x512 + 64 query, k={k}", spec_8b, 10, 512, 64, k,
                                       n_dummy=N_DUMMY_LEGOLINK0 if k == 0 else 0)
     return w

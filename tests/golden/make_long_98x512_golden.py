@@ -1,5 +1,5 @@
 """Writes the fp64 oracle's outputs of the long-context link (8B shape, 98 x 512-token
-chunks + 64-token query, k = 16, all 32 layers) to tests/golden/c3_link_outputs.npz.
+chunks + 64-token query, k = 16, all 32 layers) to tests/golden/long_98x512_link_outputs.npz.
 
 Calls only the oracle (oracle/pic_oracle.py) and the seeded input generators (pic_inputs):
 the weights are the seeded random-init 8B weights, the compiled chunk KV is the seeded
@@ -8,7 +8,7 @@ chunk). Stored: the final-normed hidden states of the 64 query rows, the logits 
 query row, and the recomputed K/V of a sample of selected rows at a sample of layers, all as
 float32 (the comparison tolerance is 2e-2 relative, far above float32 rounding).
 
-Takes ~15-30 minutes and ~35 GB of host memory:  python tests/golden/make_c3_golden.py
+Takes ~15-30 minutes and ~35 GB of host memory:  python tests/golden/make_long_98x512_golden.py
 """
 import os
 import sys
@@ -22,7 +22,7 @@ sys.path.insert(0, ROOT)
 import pic_inputs as pi  # noqa: E402
 from oracle import pic_oracle as po  # noqa: E402
 
-OUT = os.path.join(os.path.dirname(os.path.abspath(__file__)), "c3_link_outputs.npz")
+OUT = os.path.join(os.path.dirname(os.path.abspath(__file__)), "long_98x512_link_outputs.npz")
 # recomputed rows and layers whose K/V are stored (rows index the selected list, ascending positions)
 KV_ROWS = [0, 15, 16, 800, 1551, 1552, 1567, 1568, 1600, 1631]
 KV_LAYERS = [0, 1, 15, 31]
@@ -31,7 +31,7 @@ KV_LAYERS = [0, 1, 15, 31]
 def main():
     t0 = time.time()
     spec = pi.LLAMA3_8B
-    wl = pi.config_workloads()["c3"]
+    wl = pi.config_workloads()["8b_98x512"]
     w = pi.gen_weights(spec)
     om = po.OracleModel(spec, w)
     ost = po.OracleStore(om, 1 << 13)

@@ -6,16 +6,16 @@ bounded time. Compiled chunk KV is a seeded stand-in imported into both stores (
 link's arithmetic does not depend on how the chunk KV was produced; compile itself is
 checked at the same width with fewer layers).
 
-  c2 / c5 (10 x 512 + 64 query, k in {0, 2, 16, 32}): every output, 32 layers; at k = 16
+  10 x 512 + 64 query, k in {0, 2, 16, 32}: every output, 32 layers; at k = 16
       also one decode step after the link (hidden, logits, the new K/V row of every layer).
-  c5 k = 512 (full recompute): recomputed K/V of chunks 1-2 at every layer (they depend
+  10 x 512 + 64, k = 512 (full recompute): recomputed K/V of chunks 1-2 at every layer (they depend
       only on those chunks), compared with a plain prefill of chunks 1-2.
-  c3 (98 x 512 + 64, k = 16): recomputed K/V of the first 4 chunks' rows at every layer
+  98 x 512 + 64, k = 16: recomputed K/V of the first 4 chunks' rows at every layer
       (prefix sample), plus a 2-layer model over the whole 50k-token prompt, every output.
-  c3 also against stored fp64 oracle outputs of the whole 32-layer link (the 64 query rows'
+  98 x 512 + 64 also against stored fp64 oracle outputs of the whole 32-layer link (the 64 query rows'
       hidden states, the last row's logits, sampled recomputed K/V rows at sampled layers),
-      written by tests/golden/make_c3_golden.py.
-  c4 (32 requests x 8 Zipf chunks + 32 query): requests 1, 2, 16 and 32 (the last) in full,
+      written by tests/golden/make_long_98x512_golden.py.
+  32 requests x 8 Zipf chunks + 32 query: requests 1, 2, 16 and 32 (the last) in full,
       out of the batch of 32.
 Page tables, slots and selected lists are compared bit-exactly for every request.
 """
@@ -96,12 +96,12 @@ def _check_kv(store, handle, ref_k, ref_v, layers, rows=None):
     return worst
 
 
-# ----------------------------------------------------------------------------- c2 and the c5 sweep
+# ----------------------------------------------------------------------------- 10 x 512 + 64 and the k sweep
 
 @pytest.mark.parametrize("k", [16, 0, 2, 32])
-def test_c2_c5_full_outputs(m8b, k):
+def test_10x512_k_sweep_full_outputs(m8b, k):
     spec, w, model, om = m8b
-    wl = pi.config_workloads()[f"c5_k{k}"]
+    wl = pi.config_workloads()[f"8b_10x512_k{k}"]
     store = _store(model, wl)
     ost = po.OracleStore(om, 1 << 14)
     order = list(range(len(wl.chunks)))
@@ -127,10 +127,10 @@ def test_c2_c5_full_outputs(m8b, k):
     store.close()
 
 
-def test_c5_full_recompute_prefix(m8b):
+def test_10x512_full_recompute_prefix(m8b):
     """k = 512 recomputes every row; rows of chunks 1-2 equal a plain prefill of those chunks."""
     spec, w, model, om = m8b
-    wl = pi.config_workloads()["c5_k512"]
+    wl = pi.config_workloads()["8b_10x512_k512"]
     store = _store(model, wl)
     order = list(range(len(wl.chunks)))
     g, _ = _import(store, spec, wl, order)
@@ -143,19 +143,19 @@ def test_c5_full_recompute_prefix(m8b):
     store.close()
 
 
-# ----------------------------------------------------------------------------- c3 (long context)
+# ----------------------------------------------------------------------------- 98 x 512 + 64 (long context)
 
-C3_GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "c3_link_outputs.npz")
+LONG_GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "long_98x512_link_outputs.npz")
 
 
-def test_c3_all_layers(m8b):
+def test_98x512_all_layers(m8b):
     """The 98-chunk, 50k-token link through all 32 layers. (1) The 64 query rows' final hidden
     states, the last row's logits and sampled recomputed K/V rows against the fp64 oracle's
-    outputs, computed once by tests/golden/make_c3_golden.py from the same seeded weights and
+    outputs, computed once by tests/golden/make_long_98x512_golden.py from the same seeded weights and
     chunk KV. (2) The recomputed K/V of the first 4 chunks' rows at every layer against an
     oracle link of those chunks (they depend on nothing later)."""
     spec, w, model, om = m8b
-    wl = pi.config_workloads()["c3"]
+    wl = pi.config_workloads()["8b_98x512"]
     store = _store(model, wl)
     order = list(range(len(wl.chunks)))
     g, _ = _import(store, spec, wl, order)
@@ -163,7 +163,7 @@ def test_c3_all_layers(m8b):
     res = store.link([([g[c] for c in r.chunk_ids], r.query)], wl.k)
     store.sync()
     _check_meta(store, res.requests, _meta_oracle(wl, order, wl.requests))
-    gold = np.load(C3_GOLDEN)
+    gold = np.load(LONG_GOLDEN)
     info = store.request_info(res.requests[0])
     assert np.array_equal(info["selected"], gold["selected"])
     assert rel_err(res.hidden, gold["hidden"]) <= TOL
@@ -187,14 +187,14 @@ class _NullStore:
         return None
 
 
-def test_c3_two_layer_full_outputs():
+def test_98x512_two_layer_full_outputs():
     """The whole 50k-token, 98-chunk link with a 2-layer model of the same width: every output."""
     from position_independent_kv_link_gb300 import PicModel
     spec = pi.LLAMA3_8B.with_layers(2)
     w = pi.gen_weights(spec)
     model = PicModel(spec, w)
     om = po.OracleModel(spec, w)
-    wl = pi.config_workloads(spec)["c3"]
+    wl = pi.config_workloads(spec)["8b_98x512"]
     store = _store(model, wl)
     ost = po.OracleStore(om, 1 << 13)
     g, o = _import(store, spec, wl, range(len(wl.chunks)), ost)
@@ -209,11 +209,11 @@ def test_c3_two_layer_full_outputs():
     model.close()
 
 
-# ----------------------------------------------------------------------------- c4 (batched, shared pool)
+# ----------------------------------------------------------------------------- 32 requests (batched, shared pool)
 
-def test_c4_batched_sampled_requests(m8b):
+def test_32req_batched_sampled_requests(m8b):
     spec, w, model, om = m8b
-    wl = pi.config_workloads()["c4"]
+    wl = pi.config_workloads()["8b_32req"]
     store = _store(model, wl)
     order = sorted({c for r in wl.requests for c in r.chunk_ids})
     g, _ = _import(store, spec, wl, order)

@@ -204,7 +204,7 @@ def test_8b_shape_dynamic_full_size():
     choice at r = 15 and r = 10, metadata, and the whole 32-layer link at r = 10."""
     from position_independent_kv_link_gb300 import PicModel, PicStore
     spec = pi.LLAMA3_8B
-    wl = pi.config_workloads()["c2"]
+    wl = pi.config_workloads()["8b_10x512"]
     w = pi.gen_weights(spec)
     om = po.OracleModel(spec, w)
     model = PicModel(spec, w)
