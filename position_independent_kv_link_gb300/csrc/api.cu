@@ -163,6 +163,10 @@ struct pic_store {
   // on first need to the largest page count seen
   __half* krot = nullptr;
   int krot_pages = 0;
+  // grid-barrier counter of the tensor-core attention (workspace, zero at creation) and the
+  // number of CTA arrivals every earlier launch adds to it
+  unsigned long long* att_sync = nullptr;
+  unsigned long long att_sync_total = 0;
   // query-key logits of a dynamic-selection pass: grown on first need to the largest pass seen
   float* sel_logits = nullptr;
   size_t sel_logits_cap = 0;
@@ -401,7 +405,7 @@ pic_status run_forward_impl(pic_store* s, const Batch& b, float* hidden_out, flo
   const double att_bytes = att_kv_bytes + 2 * dT * dHD * es;
   const double att_flops = att_pairs * H * D * 4.0;
   const int att_launches = 1 + (combs.empty() ? 0 : 1);
-  // the K rotation of the tensor-core path: every page's K read, rotated K written
+  // the K rotation inside the tensor-core attention: every page's K read, rotated K written
   const double rot_bytes = 2.0 * (double)P * G * kBlock * D * 2;
 
   AttnArgs aa{};
@@ -431,6 +435,7 @@ pic_status run_forward_impl(pic_store* s, const Batch& b, float* hidden_out, flo
       return fail(PIC_ERR_CUDA, "cuTensorMapEncodeTiled failed for the rotated-K scratch");
     aa.krot = s->krot;
     aa.n_pages = n_pages;
+    aa.grid_sync = s->att_sync;
     aa.q16 = (const __half*)s->q;   // written rotated and scaled by the QKV epilogue
   }
   aa.dtype = dt;
@@ -485,12 +490,16 @@ pic_status run_forward_impl(pic_store* s, const Batch& b, float* hidden_out, flo
     if (att_tc) {
       aa.vmap = s->v_maps[2 * l];
       aa.vmap1 = s->v_maps[2 * l + 1];
-      Rec r(s, st, PIC_PROF_ATTENTION, rot_bytes, 0, 1);
-      launch_rope_k(n_pages, G, d_pblk, d_ppos, d_plen, s->k_layer(l), s->rope_cs, s->krot, st);
+      aa.sync_base = s->att_sync_total;
     }
     {
-      Rec r(s, st, PIC_PROF_ATTENTION, att_bytes, att_flops, att_launches);
+      Rec r(s, st, PIC_PROF_ATTENTION, att_bytes + (att_tc ? rot_bytes : 0), att_flops, att_launches);
       launch_attention(aa, st);
+    }
+    if (att_tc) {
+      // the CTAs of this launch arrive at the grid-barrier counter once each
+      PIC_CUDA(cudaPeekAtLastError());
+      s->att_sync_total += (unsigned long long)attention_tc_grid((int)items.size());
     }
     if ((e = run_gemm(s->m->wo[l], pk(s->m->po, l), s->attn, s->h, d, H * D, T, false)) != PIC_OK) return e;
     {
@@ -787,6 +796,7 @@ pic_status pic_store_create(pic_model* m, const pic_store_config* cfg, void* k_p
                                 tc_gemm_tiles(std::max(128, 2 * c.ffn_dim / 128 * 128), rows_max),
                                 tc_gemm_tiles(std::max(128, c.vocab / 128 * 128), std::max(1, sc.max_logit_rows))});
   const size_t o_ready = carve(s->tile_ready_cap * 4);
+  const size_t o_sync = carve(sizeof(unsigned long long));   // the attention's grid-barrier counter
   cudaError_t e = cudaMalloc(&s->ws, off);
   if (e != cudaSuccess) return fail(PIC_ERR_CUDA, std::string("workspace cudaMalloc: ") + cudaGetErrorString(e));
   s->h = (float*)(s->ws + o_h);
@@ -802,10 +812,12 @@ pic_status pic_store_create(pic_model* m, const pic_store_config* cfg, void* k_p
   s->meta_d = (int32_t*)(s->ws + o_meta);
   s->rope_cs = (float2*)(s->ws + o_rope);
   s->tile_ready = (int*)(s->ws + o_ready);
+  s->att_sync = (unsigned long long*)(s->ws + o_sync);
   // the q rows that no forward has written yet start at zero (a 32-row box of the tensor-core
   // attention may read them), and so do the GEMMs' tile-ready flags
   e = cudaMemset(s->ws + o_q, 0, o_attn - o_q);
   if (e == cudaSuccess) e = cudaMemset(s->tile_ready, 0, s->tile_ready_cap * 4);
+  if (e == cudaSuccess) e = cudaMemset(s->att_sync, 0, sizeof(unsigned long long));
   if (e != cudaSuccess) {
     cudaFree(s->ws);
     return fail(PIC_ERR_CUDA, std::string("workspace memset: ") + cudaGetErrorString(e));

@@ -205,11 +205,14 @@ int attention_rows_per_block(int dtype, int D, int rep) {
 
 bool attention_persistent(int dtype, int D, int rep) { return tc_attention_supported(dtype, D, rep); }
 
-pic_status attention_prepare_tc(AttnArgs& a, int T, int pool_blocks, __half* q16, __half* krot, cudaStream_t st) {
+pic_status attention_prepare_tc(AttnArgs& a, int T, int pool_blocks, __half* q16, __half* krot,
+                                unsigned long long* sync, cudaStream_t st) {
   launch_rope_q16(T, a.H, a.q, a.q_pos, a.rope_cs, q16, st);
-  launch_rope_k(a.n_pages, a.G, a.page_block, a.page_pos, a.page_len, a.k_layer, a.rope_cs, krot, st);
+  PIC_CUDA(cudaMemsetAsync(sync, 0, sizeof(*sync), st));
   a.q16 = q16;
   a.krot = krot;
+  a.grid_sync = sync;
+  a.sync_base = 0;
   if (!attn_v_map(&a.vmap, &a.vmap1, a.v_layer, pool_blocks, a.G) || !attn_krot_map(&a.kmap, krot, a.n_pages, a.G))
     return fail(PIC_ERR_CUDA, "cuTensorMapEncodeTiled failed for the attention operands");
   return PIC_OK;

@@ -1,13 +1,13 @@
 // tcgen05 paged attention with fused RoPE for bf16 KV, head_dim 128, 4 query heads per KV head.
 //
-// Two launches per layer. rope_k_kernel rotates the K of every page of the work by RoPE at each
-// row's absolute position (MEPIC abstract: K is kept without positional encoding and rotated at
-// attention time) into an fp16 scratch [pages][G][16][128] indexed by the work's page number,
-// rows beyond a page's length zero: each page is rotated once per layer however many work items
-// read it. attn_tc_kernel then reads the rotated K and the stored bf16 V straight into the MMA
-// operand layouts by TMA; nothing is converted on the way.
+// One cooperative launch per layer, two phases. Phase 1: the CTAs rotate the K of every page of
+// the work by RoPE at each row's absolute position (MEPIC abstract: K is kept without positional
+// encoding and rotated inside attention) into an fp16 scratch [pages][G][16][128] indexed by the
+// work's page number, rows beyond a page's length zero: each page is rotated once per layer
+// however many work items read it. A grid barrier follows. Phase 2 reads the rotated K and the
+// stored bf16 V straight into the MMA operand layouts by TMA; nothing is converted on the way.
 //
-// attn_tc_kernel is persistent: CTA b walks the work items b, b + grid, b + 2 grid, ... (the
+// Phase 2 is persistent: CTA b walks the work items b, b + grid, b + 2 grid, ... (the
 // planner deals them in that order). An item is up to 64 consecutive query rows of one sequence
 // x the 4 query heads sharing KV head g x a run of pages. Its rows form two M = 128 MMA tiles:
 // tile t holds rows 32t..32t+31 of the item x the 4 heads (MMA row = head * 32 + row). Every
@@ -95,7 +95,8 @@ constexpr int B_PVDONE = B_SFULL + 2 * MT;        // [2][2] O_t += P_t V of buff
 constexpr int B_QREADY = B_PVDONE + 2 * MT;       // [2] Q_t of the item written (the 4 warps of warpgroup t)
 constexpr int B_PREADY = B_QREADY + MT;           // [2][2] P_t in buffer b written (the 4 warps of warpgroup t)
 constexpr int B_DONE = B_PREADY + 2 * MT;         // [2] every MMA of MMA tile t's issuing thread retired
-static_assert(B_DONE + MT <= N_BARS, "barrier slots");
+constexpr int B_ROT = B_DONE + MT;                // [2] a batch of phase 1 (K pages, cos/sin rows) landed in buffer i
+static_assert(B_ROT + 2 <= N_BARS, "barrier slots");
 // Every waiter must observe each phase of a barrier before the barrier can complete the next
 // one (a parity wait cannot tell phase n from n + 2). FULL is waited on by both MMA threads and
 // both warpgroups, but a stage can only be refilled after both MMA tiles released it (the PV
@@ -152,6 +153,12 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
       return false;
     }
   }
+}
+// plain bulk copy global -> shared (16-byte aligned addresses, size a multiple of 16)
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
 }
 __device__ __forceinline__ void tma_5d(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2, int c3, int c4,
                                        uint32_t bar) {
@@ -287,6 +294,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     for (int t = 0; t < MT; ++t) mbar_init(bar(B_QREADY + t), 4);
     for (int i = 0; i < 2 * MT; ++i) mbar_init(bar(B_PREADY + i), 4);
     for (int t = 0; t < MT; ++t) mbar_init(bar(B_DONE + t), 1);
+    mbar_init(bar(B_ROT), 1);
+    mbar_init(bar(B_ROT + 1), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == W_MMA) {
@@ -297,13 +306,118 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
   fence_before();
   __syncthreads();
   fence_after();
-  // Programmatic dependent launch: the next kernel may launch now (it waits for this one's
-  // completion before reading its outputs). This kernel's own reads of the previous kernels'
-  // outputs (the rotated q, the K/V pages) come after griddepcontrol.wait in the roles that make
-  // them; the work plan, page tables and cos/sin table are written before the forward starts and
-  // are read earlier, overlapping the previous kernel's tail.
+  // Programmatic dependent launch: the next kernel may launch once every CTA of this one has
+  // executed launch_dependents, i.e. once every CTA of this grid is resident (so the next
+  // kernel's CTAs can never hold an SM a CTA of this grid still needs for the grid barrier
+  // below); this kernel waits for the previous kernels (the K/V pages, the rotated q) before its
+  // first read of their outputs.
   asm volatile("griddepcontrol.launch_dependents;");
   const uint32_t tmem = *tmem_slot;
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+
+  // =============================== phase 1: RoPE. The CTAs rotate the K of every page of the work
+  // to each row's absolute position (MEPIC abstract: K is kept without positional encoding and
+  // rotated inside attention), each a share of the (page, KV head, row, 8-dim chunk) units, into
+  // the fp16 scratch krot[page][g][16][128] (rows beyond a page's length zero), so that a page is
+  // rotated once however many work items read it; then all CTAs meet at a grid barrier (the
+  // launch is cooperative: every CTA is resident), after which phase 2 reads the scratch by TMA.
+  {
+    // CTA b takes the (page, KV head) pairs [P b / grid, P (b + 1) / grid), page-major, in batches
+    // of up to 16 through two buffers (each: two key-tile stages for the pairs' K pages, 4 KB each,
+    // and one Q tile for the pages' cos/sin rows, 512 B per row; all idle until phase 2). The next
+    // batch's bulk copies are in flight while every thread rotates (row, 8-dim chunk) units of
+    // the current one from shared memory into the scratch.
+    constexpr int kRotPairs = 2 * ST_BYTES / 4096;   // 16 per buffer
+    constexpr int kRotPages = Q_TILE / 8192;         // 4 pages of cos/sin rows per buffer
+    const __nv_bfloat16* kl = static_cast<const __nv_bfloat16*>(a.k_layer);
+    const int P = a.n_pages * a.G;
+    const int pa = (int)((long long)P * blockIdx.x / gridDim.x), pb = (int)((long long)P * (blockIdx.x + 1) / gridDim.x);
+    // batch extent from b0: at most kRotPairs pairs over at most kRotPages pages
+    auto batch_n = [&](int b0) { return min(min(kRotPairs, pb - b0), (b0 / a.G + kRotPages) * a.G - b0); };
+    auto issue = [&](int b0, int buf) {   // warp 0: the batch's copies into buffer buf
+      const int n = batch_n(b0), p_lo = b0 / a.G, p_hi = (b0 + n - 1) / a.G;
+      uint8_t* ks = sm + OFF_ST + buf * 2 * ST_BYTES;
+      uint8_t* css = sm + OFF_Q + buf * Q_TILE;
+      uint32_t bytes = (uint32_t)n * 4096u;
+      for (int p = p_lo; p <= p_hi; ++p) bytes += (uint32_t)a.page_len[p] * 512u;
+      if (lane == 0) mbar_expect_tx(bar(B_ROT + buf), bytes);
+      __syncwarp();
+      for (int i = lane; i < n; i += 32) {   // K of pair b0 + i: [16 rows][128] bf16 = 4 KB
+        const int pg = b0 + i, p = pg / a.G, g = pg % a.G;
+        bulk_g2s(smem_u32(ks + i * 4096), kl + ((size_t)a.page_block[p] * a.G + g) * kBlock * D, 4096u, bar(B_ROT + buf));
+      }
+      for (int p = p_lo + lane; p <= p_hi; p += 32)   // cos/sin rows of the page's valid rows
+        bulk_g2s(smem_u32(css + (p - p_lo) * 8192), a.rope_cs + (size_t)a.page_pos[p] * (D / 2),
+                 (uint32_t)a.page_len[p] * 512u, bar(B_ROT + buf));
+    };
+    if (warp == 0 && pa < pb) issue(pa, 0);
+    uint32_t ph[2] = {0, 0};
+    for (int b0 = pa, k = 0; b0 < pb; b0 += batch_n(b0), ++k) {
+      const int buf = k & 1, n = batch_n(b0), nb = b0 + n;
+      // the other buffer was last read in the previous batch, which every thread has finished
+      if (warp == 0 && nb < pb) issue(nb, buf ^ 1);
+      const bool landed = __syncthreads_and(mbar_wait(bar(B_ROT + buf), ph[buf]));   // the same decision in every thread
+      ph[buf] ^= 1;
+      if (!landed) {
+        s_abort = 1;
+        break;
+      }
+      const int p_lo = b0 / a.G;
+      const uint8_t* ks = sm + OFF_ST + buf * 2 * ST_BYTES;
+      const uint8_t* css = sm + OFF_Q + buf * Q_TILE;
+      for (int u = tid; u < n * kBlock * 8; u += kThreads) {
+        const int c = u & 7, r = (u >> 3) & (kBlock - 1), i = u >> 7;
+        const int pg = b0 + i, p = pg / a.G;
+        uint4 y1 = make_uint4(0, 0, 0, 0), y2 = y1;
+        if (r < a.page_len[p]) {
+          const __nv_bfloat16* src = reinterpret_cast<const __nv_bfloat16*>(ks + i * 4096) + r * D + 8 * c;
+          const uint4 u1 = *reinterpret_cast<const uint4*>(src), u2 = *reinterpret_cast<const uint4*>(src + 64);
+          const float4* f4 = reinterpret_cast<const float4*>(css + (p - p_lo) * 8192 + r * 512) + 4 * c;
+          const uint32_t w1[4] = {u1.x, u1.y, u1.z, u1.w}, w2[4] = {u2.x, u2.y, u2.z, u2.w};
+          uint32_t o1[4], o2[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float4 f = f4[e];   // (cos, sin) of frequencies 8c + 2e and 8c + 2e + 1
+            // bf16 pair -> two floats (exact), then the rotate-half pairs (i, i + 64)
+            const float a0 = __uint_as_float(w1[e] << 16), a1 = __uint_as_float(w1[e] & 0xffff0000u);
+            const float b0v = __uint_as_float(w2[e] << 16), b1 = __uint_as_float(w2[e] & 0xffff0000u);
+            o1[e] = pack_f16x2(a0 * f.x - b0v * f.y, a1 * f.z - b1 * f.w);
+            o2[e] = pack_f16x2(b0v * f.x + a0 * f.y, b1 * f.z + a1 * f.w);
+          }
+          y1 = make_uint4(o1[0], o1[1], o1[2], o1[3]);
+          y2 = make_uint4(o2[0], o2[1], o2[2], o2[3]);
+        }
+        __half* dst = a.krot + ((size_t)pg * kBlock + r) * D + 8 * c;   // [page][g] pairs are consecutive
+        *reinterpret_cast<uint4*>(dst) = y1;
+        *reinterpret_cast<uint4*>(dst + 64) = y2;
+      }
+      fence_async_smem();   // these generic reads come before the async-proxy copies that reuse the buffer
+      __syncthreads();      // this buffer is read before the batch after next is copied into it
+    }
+    if (s_abort && warp == 0 && lane == 0)   // copies still in flight land before the memory is reused
+      for (int q = 0; q < 2; ++q) mbar_wait(bar(B_ROT + q), ph[q]);
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // phase 2's TMA loads rewrite these stages
+    asm volatile("fence.proxy.async.global;" ::: "memory");   // the TMA loads of phase 2 read these rows
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) {
+      const unsigned long long target = a.sync_base + gridDim.x;
+      atomicAdd(a.grid_sync, 1ull);
+      const unsigned long long t0 = gtimer();
+      for (uint32_t i = 0;; ++i) {
+        unsigned long long v;
+        asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(a.grid_sync) : "memory");
+        if (v >= target) break;
+        if ((i & 63) == 63 && gtimer() - t0 > kWaitLimitNs) {
+          atomicExch(&g_attn_timeout, 1);
+          s_abort = 1;
+          break;
+        }
+      }
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+    }
+    __syncthreads();
+  }
 
   if (warp < kSoftmaxWarps) {
     // =============================== MMA tile t: softmax warps (head hh, row r); the warpgroup's
@@ -345,7 +459,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_QREADY + t));
     };
-    asm volatile("griddepcontrol.wait;" ::: "memory");   // q16 is written by the previous kernel
     if (blockIdx.x < a.n_items) write_q(it_n);
     for (int ii = blockIdx.x; ii < a.n_items; ii += gridDim.x) {
       const AttnItem it = it_n;
@@ -638,7 +751,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
           pos[q] = __shfl_sync(0xffffffffu, cpos, p0 - w0 + q);
           len[q] = q < np ? __shfl_sync(0xffffffffu, clen, p0 - w0 + q) : 0;
         }
-        if (gt == 0) asm volatile("griddepcontrol.wait;" ::: "memory");   // the pages are written by earlier kernels
         // stage s free once every PV of key tile gt - NST has retired
         if (lane == 0) ok = !s_abort && (kr == 0 || mbar_wait(bar(B_EMPTY + s), (kr - 1) & 1));
         ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -713,41 +825,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
   if (warp == W_MMA) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
 }
 
-// K of page p of the work, KV head g, rotated by RoPE at each row's absolute position, fp16, to
-// krot[p][g][16][128]; rows beyond the page's length zero. CTA (p, g), thread = (row r, dims
-// 8c..8c+7 and 64 + 8c..64 + 8c + 7).
-__global__ void __launch_bounds__(128) rope_k_kernel(int G, const int* __restrict__ page_block,
-                                                     const int* __restrict__ page_pos,
-                                                     const int* __restrict__ page_len,
-                                                     const __nv_bfloat16* __restrict__ k_layer,
-                                                     const float2* __restrict__ rope_cs, __half* __restrict__ krot) {
-  pdl_enter();
-  const int p = blockIdx.x, g = blockIdx.y, r = threadIdx.x >> 3, c = threadIdx.x & 7;
-  const int blk = page_block[p], len = page_len[p];
-  uint4 y1 = make_uint4(0, 0, 0, 0), y2 = y1;
-  if (r < len) {
-    const __nv_bfloat16* src = k_layer + (((size_t)blk * G + g) * kBlock + r) * D + 8 * c;
-    const uint4 u1 = *reinterpret_cast<const uint4*>(src), u2 = *reinterpret_cast<const uint4*>(src + 64);
-    const float4* row = reinterpret_cast<const float4*>(rope_cs + (size_t)(page_pos[p] + r) * (D / 2) + 8 * c);
-    const uint32_t w1[4] = {u1.x, u1.y, u1.z, u1.w}, w2[4] = {u2.x, u2.y, u2.z, u2.w};
-    uint32_t o1[4], o2[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float4 cs = row[e];   // (cos, sin) of frequencies 8c + 2e and 8c + 2e + 1
-      // bf16 pair -> two floats (exact), then the rotate-half pairs (i, i + 64)
-      const float a0 = __uint_as_float(w1[e] << 16), a1 = __uint_as_float(w1[e] & 0xffff0000u);
-      const float b0 = __uint_as_float(w2[e] << 16), b1 = __uint_as_float(w2[e] & 0xffff0000u);
-      o1[e] = pack_f16x2(a0 * cs.x - b0 * cs.y, a1 * cs.z - b1 * cs.w);
-      o2[e] = pack_f16x2(b0 * cs.x + a0 * cs.y, b1 * cs.z + a1 * cs.w);
-    }
-    y1 = make_uint4(o1[0], o1[1], o1[2], o1[3]);
-    y2 = make_uint4(o2[0], o2[1], o2[2], o2[3]);
-  }
-  __half* dst = krot + (((size_t)p * G + g) * kBlock + r) * D + 8 * c;
-  *reinterpret_cast<uint4*>(dst) = y1;
-  *reinterpret_cast<uint4*>(dst + 64) = y2;
-}
-
 int sm_count() {
   static int n[64] = {};
   int dev = 0;
@@ -802,16 +879,13 @@ bool attn_krot_map(CUtensorMap* m, const __half* krot, int n_pages, int G) {
 
 size_t attention_krot_bytes(int n_pages, int G) { return (size_t)n_pages * G * kBlock * D * sizeof(__half); }
 
-void launch_rope_k(int n_pages, int G, const int* page_block, const int* page_pos, const int* page_len,
-                   const void* k_layer, const float2* rope_cs, __half* krot, cudaStream_t st) {
-  if (n_pages > 0)
-    launch_dependent(rope_k_kernel, dim3(n_pages, G), dim3(128), 0, st, G, page_block, page_pos, page_len,
-                     static_cast<const __nv_bfloat16*>(k_layer), rope_cs, krot);
-}
-
 int attention_tc_rows_per_item() { return MT * RB; }
 
-// Grid = min(items, SMs): the planner deals items for exactly this walk.
+int attention_tc_grid(int n_items) { return std::min(n_items, sm_count()); }
+
+// Grid = min(items, SMs): the planner deals items for exactly this walk. Cooperative (every CTA
+// resident: the kernel's grid barrier needs it; the launch fails otherwise) and a programmatic
+// dependent of the previous kernel.
 void launch_attention_tc(const AttnArgs& a, cudaStream_t st) {
   static bool attr[64] = {};
   int dev = 0;
@@ -821,7 +895,20 @@ void launch_attention_tc(const AttnArgs& a, cudaStream_t st) {
     cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (dev >= 0 && dev < 64) attr[dev] = true;
   }
-  if (a.n_items > 0) launch_dependent(attn_tc_kernel, dim3(std::min(a.n_items, sm_count())), dim3(kThreads), smem, st, a);
+  if (a.n_items <= 0) return;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(attention_tc_grid(a.n_items));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute at[2];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  at[1].id = cudaLaunchAttributeCooperative;
+  at[1].val.cooperative = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 2;
+  cudaLaunchKernelEx(&cfg, attn_tc_kernel, a);
 }
 
 void attn_raise_timeout() {

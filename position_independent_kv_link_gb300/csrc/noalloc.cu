@@ -107,7 +107,8 @@ pic_status pic_op_attention_noalloc(int32_t dtype, int32_t T, int32_t n_heads, i
   const size_t o_ml = o_part + align256((size_t)n_parts * kAttnPartRows * rep * head_dim * 4);
   const size_t o_q16 = o_ml + align256((size_t)n_parts * kAttnPartRows * rep * 2 * 4);
   const size_t o_krot = o_q16 + (in.persistent ? align256((size_t)T * n_heads * head_dim * 2) : 0);
-  const size_t need = o_krot + (in.persistent ? align256(attention_krot_bytes(n_pages, n_kv_heads)) : 0);
+  const size_t o_sync = o_krot + (in.persistent ? align256(attention_krot_bytes(n_pages, n_kv_heads)) : 0);
+  const size_t need = o_sync + (in.persistent ? 256 : 0);   // + the tensor-core kernel's grid-barrier counter
   if (need > kNoAllocScratchBytes)
     return fail(PIC_ERR_CAPACITY, "attention needs " + std::to_string(need) + " bytes of scratch; the fixed area holds " +
                                       std::to_string(kNoAllocScratchBytes) + " (use pic_op_attention with a caller buffer)");
@@ -157,7 +158,7 @@ pic_status pic_op_attention_noalloc(int32_t dtype, int32_t T, int32_t n_heads, i
   if (in.persistent) {
     a.n_pages = n_pages;
     s = attention_prepare_tc(a, T, pool_blocks, (__half*)((char*)scratch + o_q16), (__half*)((char*)scratch + o_krot),
-                             st);
+                             (unsigned long long*)((char*)scratch + o_sync), st);
     if (s != PIC_OK) return s;
   }
   launch_attention(a, st);

@@ -19,7 +19,7 @@ int current_sms() {
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
 struct AttnScratchLayout {
-  size_t ints_bytes, part_o_off, part_ml_off, q16_off, krot_off, total;
+  size_t ints_bytes, part_o_off, part_ml_off, q16_off, krot_off, sync_off, total;
   int max_parts, max_items;
 };
 
@@ -36,7 +36,8 @@ AttnScratchLayout attn_layout(int T, int n_heads, int n_kv_heads, int head_dim, 
   L.q16_off = L.part_ml_off + align256((size_t)L.max_parts * kAttnPartRows * rep * 2 * 4);
   // tensor-core path: rotated fp16 q, then the rotated fp16 K of every page
   L.krot_off = L.q16_off + align256((size_t)T * n_heads * head_dim * 2);
-  L.total = L.krot_off + align256((size_t)n_pages * n_kv_heads * kBlock * head_dim * 2);
+  L.sync_off = L.krot_off + align256((size_t)n_pages * n_kv_heads * kBlock * head_dim * 2);
+  L.total = L.sync_off + 256;   // the tensor-core kernel's grid-barrier counter
   return L;
 }
 
@@ -158,7 +159,8 @@ pic_status pic_op_attention(int32_t dtype, int32_t T, int32_t n_heads, int32_t n
   if (in.persistent) {
     a.n_pages = n_pages;
     pic_status e = attention_prepare_tc(a, T, pool_blocks, (__half*)((char*)scratch + L.q16_off),
-                                        (__half*)((char*)scratch + L.krot_off), st);
+                                        (__half*)((char*)scratch + L.krot_off),
+                                        (unsigned long long*)((char*)scratch + L.sync_off), st);
     if (e != PIC_OK) return e;
   }
   launch_attention(a, st);

@@ -156,14 +156,18 @@ struct AttnCombine {   // merge `nparts` partial results of rows [row0, row0+nro
   int row0, nrows, g, part0, nparts;
 };
 struct AttnArgs {
-  // tensor-core kernel only (attention_persistent shapes): kmap boxes 4 consecutive pages of the
-  // rotated-K scratch krot [n_pages][G][16][128] fp16 (attn_krot_map, written per layer by
-  // launch_rope_k); vmap / vmap1 box one 64-dim half of 4 consecutive blocks' / one block's page
-  // of the V pool layer (attn_v_map); q16: q as fp16 [T][H][D], rotated and scaled (the QKV
-  // epilogue's q16 output)
+  // tensor-core kernel only (attention_persistent shapes): the kernel first rotates the K of the
+  // n_pages pages into the scratch krot [n_pages][G][16][128] fp16, which kmap boxes 4
+  // consecutive pages of (attn_krot_map); vmap / vmap1 box one 64-dim half of 4 consecutive
+  // blocks' / one block's page of the V pool layer (attn_v_map); q16: q as fp16 [T][H][D],
+  // rotated and scaled (the QKV epilogue's q16 output). grid_sync: a device counter the CTAs
+  // add 1 to at the kernel's grid barrier, which opens once it reaches sync_base + the grid size
+  // (the caller adds attention_tc_grid(n_items) to sync_base after each launch).
   CUtensorMap kmap, vmap, vmap1;
   __half* krot;
   int n_pages;
+  unsigned long long* grid_sync;
+  unsigned long long sync_base;
   const __half* q16;
   int dtype, H, G, D;
   int rb;                   // rows per work item of this plan (16, 32 or 64)
@@ -213,15 +217,15 @@ bool attn_v_map(CUtensorMap* m4, CUtensorMap* m1, const void* v_layer, int pool_
 bool attn_krot_map(CUtensorMap* m, const __half* krot, int n_pages, int G);
 // Bytes of the rotated-K scratch for n_pages pages.
 size_t attention_krot_bytes(int n_pages, int G);
-// krot[p][g] = fp16(RoPE(K[page_block[p]][g][r], page_pos[p] + r)) for r < page_len[p], 0 for the
-// other rows, for every page p of the work (one programmatic-dependent launch).
-void launch_rope_k(int n_pages, int G, const int* page_block, const int* page_pos, const int* page_len,
-                   const void* k_layer, const float2* rope_cs, __half* krot, cudaStream_t st);
+// CTAs of the tensor-core attention for a plan of n_items items (the grid barrier's count).
+int attention_tc_grid(int n_items);
 // For callers holding fp32 pre-RoPE a.q (kernel-level calls): writes the rotated fp16 copy
-// into q16 ([T][H][128], 16-byte aligned) and the rotated K of the a.n_pages pages into krot
-// (attention_krot_bytes, 16-byte aligned), and sets a.q16, a.krot and the maps (V pool of
-// pool_blocks blocks).
-pic_status attention_prepare_tc(AttnArgs& a, int T, int pool_blocks, __half* q16, __half* krot, cudaStream_t st);
+// into q16 ([T][H][128], 16-byte aligned), zeroes the grid-barrier counter *sync (8 bytes of
+// device memory) and sets a.q16, a.krot (attention_krot_bytes of a.n_pages pages, 16-byte
+// aligned, filled by the attention kernel), the barrier and the maps (V pool of pool_blocks
+// blocks).
+pic_status attention_prepare_tc(AttnArgs& a, int T, int pool_blocks, __half* q16, __half* krot,
+                                unsigned long long* sync, cudaStream_t st);
 void plan_attention(const AttnPlanInput& in, std::vector<AttnItem>& items, std::vector<AttnCombine>& combines,
                     int& n_parts);
 size_t attention_part_bytes(int n_parts, int rep, int D);
