@@ -18,13 +18,15 @@
 // Key tiles stream through a ring of 4 shared-memory stages, each K then V of 64 keys in the
 // layout the MMAs read ([64-dim half][key][128 B], 128-byte swizzled).
 //
-//   warp 10     loads: per key tile, rotated K as two boxes of 4 consecutive scratch pages (one per
+//   warp 10     loads: it alone waits at the grid barrier (the other roles read nothing of
+//               what other CTAs wrote in phase 1), then per key tile, rotated K as two boxes of 4 consecutive scratch pages (one per
 //               64-dim half) and V as two boxes over 4 consecutive pool blocks (pages of a chunk
 //               or a query are allocated consecutively), else one box per full page; a page with
 //               fewer than 16 rows is copied by the warp's lanes with its missing rows zeroed,
 //               and the V rows of pages past the item's end are zeroed (P is 0 there; V must be
 //               finite). The warp also writes each key's position (the causal mask) and holds the
-//               page metadata (its lanes hold a window of 32 pages, the next one prefetched).
+//               page metadata (its lanes hold a window of 32 pages, the next one prefetched; the
+//               first item's is fetched before phase 1).
 //   warps 8, 9  one MMA-issuing thread per MMA tile t (warp 8 also owns the TMEM: all 512
 //               columns, O_t at [128t, 128t + 128), two S buffers of tile t at 256 + 128t +
 //               {0, 64}). Per key tile j of its tile, in this order: O_t += P_t(j) V(j) (M128 N128
@@ -35,7 +37,7 @@
 //               the PV to retire, and the S products stay two key tiles ahead of the softmax.
 //   warps 0-7   MMA tile t = warpgroup t, thread = one MMA row = one TMEM lane. The warpgroup
 //               writes the tile's Q rows into shared memory at the start of an item (the A
-//               operand of its S products); per key tile each thread reads its row of S (64
+//               operand of its S products; the first item's while the grid barrier is pending); per key tile each thread reads its row of S (64
 //               keys, one TMEM round trip), masks keys after its position (only on key tiles
 //               that need it), keeps a running reference maximum and writes P = 2^(S - ref) as
 //               bf16 pairs over the S columns. O in TMEM is rescaled only when the maximum grows
@@ -269,6 +271,15 @@ __device__ __forceinline__ int item_tiles_of(const AttnItem& it, int t) {
   return it.nrows > RB ? item_tiles(it) : 0;
 }
 
+// page metadata of page pg of an item ending at page1 (left as they are past the end)
+__device__ __forceinline__ void fetch_page(const AttnArgs& a, int page1, int pg, int& b, int& p, int& l) {
+  if (pg < page1) {
+    b = a.page_block[pg];
+    p = a.page_pos[pg];
+    l = a.page_len[pg];
+  }
+}
+
 __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_constant__ AttnArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -314,6 +325,24 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
   asm volatile("griddepcontrol.launch_dependents;");
   const uint32_t tmem = *tmem_slot;
   asm volatile("griddepcontrol.wait;" ::: "memory");
+
+  // The first item of each role and its page metadata are fetched now, so that their load
+  // latency passes during phase 1. Softmax warps: MMA tile t, head hh, row r of the item.
+  const int t = warp >> 2, hh = warp & 3, r = lane;
+  const int row = RB * t + r;
+  AttnItem it_n{};   // softmax warps: the next item; load warp: the first item
+  int qp_n = -1;
+  int cblk = 0, cpos = 0, clen = 0, nblk = 0, npos = 0, nlen = 0;   // load warp: lane i holds pages w0 + i, w0 + 32 + i
+  if (blockIdx.x < a.n_items) {
+    if (warp < kSoftmaxWarps) {
+      it_n = a.items[blockIdx.x];
+      qp_n = row < it_n.nrows ? a.q_pos[it_n.row0 + row] : -1;
+    } else if (warp == W_LOAD) {
+      it_n = a.items[blockIdx.x];
+      fetch_page(a, it_n.page1, it_n.page0 + lane, cblk, cpos, clen);
+      fetch_page(a, it_n.page1, it_n.page0 + 32 + lane, nblk, npos, nlen);
+    }
+  }
 
   // =============================== phase 1: RoPE. The CTAs rotate the K of every page of the work
   // to each row's absolute position (MEPIC abstract: K is kept without positional encoding and
@@ -400,29 +429,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     asm volatile("fence.proxy.async.global;" ::: "memory");   // the TMA loads of phase 2 read these rows
     __threadfence();
     __syncthreads();
-    if (tid == 0) {
-      const unsigned long long target = a.sync_base + gridDim.x;
-      atomicAdd(a.grid_sync, 1ull);
-      const unsigned long long t0 = gtimer();
-      for (uint32_t i = 0;; ++i) {
-        unsigned long long v;
-        asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(a.grid_sync) : "memory");
-        if (v >= target) break;
-        if ((i & 63) == 63 && gtimer() - t0 > kWaitLimitNs) {
-          atomicExch(&g_attn_timeout, 1);
-          s_abort = 1;
-          break;
-        }
-      }
-      asm volatile("fence.proxy.async.global;" ::: "memory");
-    }
-    __syncthreads();
   }
+  // From here the roles run on their own. Only the load warp reads what other CTAs wrote in
+  // phase 1, so only it waits at the grid barrier; the first item's Q is written meanwhile.
 
   if (warp < kSoftmaxWarps) {
     // =============================== MMA tile t: softmax warps (head hh, row r); the warpgroup's
     // first thread issues the tile's PV products
-    const int t = warp >> 2, hh = warp & 3, r = lane;   // MMA row hh * 32 + r = TMEM lane
     const bool issuer = hh == 0 && lane == 0;
     const uint32_t trow = tmem + ((uint32_t)(hh * 32) << 16);   // this warp's TMEM lane quarter
     const uint32_t t_o = trow + TM_O + 128 * t, t_sb = trow + TM_S + 128 * t;
@@ -430,14 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     // every thread of the warpgroup takes part, so all of them take the same branch after it
     uint32_t gt = 0, ct = 0;   // key tiles of the CTA; key tiles of this MMA tile
     bool ok = true;
-    const int row = RB * t + r;
     // the next item and this row's position in it are fetched an item ahead
-    AttnItem it_n{};
-    int qp_n = -1;
-    if (blockIdx.x < a.n_items) {
-      it_n = a.items[blockIdx.x];
-      qp_n = row < it_n.nrows ? a.q_pos[it_n.row0 + row] : -1;
-    }
     // this row's q of item itq (128 fp16, rotated and scaled) into the K-major, 128-byte-swizzled
     // A operand of the S products: MMA row m = hh * 32 + r, dims 8c..8c+7 of half h at
     // [h][m][chunk c]; every load is issued before the first store. Called once every S product
@@ -459,7 +465,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_QREADY + t));
     };
-    if (blockIdx.x < a.n_items) write_q(it_n);
+    if (blockIdx.x < a.n_items && !s_abort) write_q(it_n);
     for (int ii = blockIdx.x; ii < a.n_items; ii += gridDim.x) {
       const AttnItem it = it_n;
       const int qp = qp_n;
@@ -714,22 +720,34 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     }
   } else if (warp == W_LOAD) {
     // =============================== loads (lanes issue the boxes; the warp holds page metadata)
-    uint32_t n_ld = 0;   // key tiles issued
+    // the grid barrier: every CTA's phase 1 rows are written before the first K box is loaded
     bool ok = true;
+    if (lane == 0) {
+      const unsigned long long target = a.sync_base + gridDim.x;
+      atomicAdd(a.grid_sync, 1ull);
+      const unsigned long long t0 = gtimer();
+      for (uint32_t i = 0; !s_abort; ++i) {
+        unsigned long long v;
+        asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(a.grid_sync) : "memory");
+        if (v >= target) break;
+        if ((i & 63) == 63 && gtimer() - t0 > kWaitLimitNs) {
+          atomicExch(&g_attn_timeout, 1);
+          s_abort = 1;
+        }
+      }
+      ok = !s_abort;
+    }
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    asm volatile("fence.proxy.async.global;" ::: "memory");   // the TMA loads below read other CTAs' rows
+    uint32_t n_ld = 0;   // key tiles issued
     // lane i: metadata of page w0 + i (cur) and of page w0 + 32 + i (nxt, loaded one window ahead)
-    int w0 = 0, cblk = 0, cpos = 0, clen = 0, nblk = 0, npos = 0, nlen = 0;
+    int w0 = 0;
     const __nv_bfloat16* vl = static_cast<const __nv_bfloat16*>(a.v_layer);
     for (int ii = blockIdx.x; ii < a.n_items && ok; ii += gridDim.x) {
-      const AttnItem it = a.items[ii];
+      const bool first = ii == (int)blockIdx.x;
+      const AttnItem it = first ? it_n : a.items[ii];
       const int nt = item_tiles(it);
-      auto fetch = [&](int w, int& b, int& p, int& l) {
-        const int pg = w + lane;
-        if (pg < it.page1) {
-          b = a.page_block[pg];
-          p = a.page_pos[pg];
-          l = a.page_len[pg];
-        }
-      };
+      auto fetch = [&](int w, int& b, int& p, int& l) { fetch_page(a, it.page1, w + lane, b, p, l); };
       for (int j = 0; j < nt; ++j) {
         const uint32_t gt = n_ld;
         const int s = gt % NST;
@@ -737,8 +755,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         const int p0 = it.page0 + 4 * j, np = min(4, it.page1 - p0);
         if (j == 0) {
           w0 = p0;
-          fetch(w0, cblk, cpos, clen);
-          fetch(w0 + 32, nblk, npos, nlen);
+          if (!first) {   // the first item's window was fetched before phase 1
+            fetch(w0, cblk, cpos, clen);
+            fetch(w0 + 32, nblk, npos, nlen);
+          }
         } else if (p0 == w0 + 32) {   // windows are 8 key tiles: a tile never straddles two
           w0 = p0;
           cblk = nblk, cpos = npos, clen = nlen;
