@@ -792,9 +792,11 @@ pic_status pic_store_create(pic_model* m, const pic_store_config* cfg, void* k_p
                o_rope = carve((size_t)std::max(16, sc.max_positions) * (c.head_dim / 2) * sizeof(float2));
   // ready flags of the self-zeroing GEMMs' output tiles: the most tiles any of them has
   const int rows_max = std::max(R, (size_t)sc.max_logit_rows) > 0 ? (int)std::max(R, (size_t)sc.max_logit_rows) : 1;
-  s->tile_ready_cap = std::max({tc_gemm_tiles(std::max(128, m->qkv_dim() / 128 * 128), rows_max),
-                                tc_gemm_tiles(std::max(128, 2 * c.ffn_dim / 128 * 128), rows_max),
-                                tc_gemm_tiles(std::max(128, c.vocab / 128 * 128), std::max(1, sc.max_logit_rows))});
+  // (below 1024 rows the weight tiles have 128 rows, from there 256: both row counts are covered)
+  auto tiles_upto = [](int N, int T) { return std::max(tc_gemm_tiles(N, T), tc_gemm_tiles(N, std::min(T, 1023))); };
+  s->tile_ready_cap = std::max({tiles_upto(std::max(128, m->qkv_dim() / 128 * 128), rows_max),
+                                tiles_upto(std::max(128, 2 * c.ffn_dim / 128 * 128), rows_max),
+                                tiles_upto(std::max(128, c.vocab / 128 * 128), std::max(1, sc.max_logit_rows))});
   const size_t o_ready = carve(s->tile_ready_cap * 4);
   const size_t o_sync = carve(sizeof(unsigned long long));   // the attention's grid-barrier counter
   cudaError_t e = cudaMalloc(&s->ws, off);

@@ -4,21 +4,26 @@
 //
 // The link step multiplies a few hundred selected rows by large weight matrices: the
 // weights take the MMA's M side (128 rows per tile) and the token rows its N side (up
-// to 256 per tile), so each weight tile is streamed from HBM once per token tile.
+// to 256 per tile), so each weight tile is streamed from HBM once per token tile. Every
+// weight k-block (16 KB) brings the token tile's k-block (up to 32 KB, from L2) into the SM
+// with it; from 1024 token rows on (compute-bound, 4+ token tiles) the packed layout takes two
+// weight tiles per activation tile (256 weight rows: two M = 128 MMAs per K step into two
+// accumulators that fill the TMEM, one accumulator set).
 //
 // Persistent, stream-K, warp-specialized. The grid has one CTA per SM; the linear space
 // of (tile, 64-wide k-block) work is cut into equal contiguous ranges, one per CTA, so
 // every SM streams the same number of weight bytes. A CTA walks its range as segments
 // (maximal runs inside one tile). Each segment accumulates in one of two TMEM buffers
-// and is folded into Y by TMA bulk reduce-adds, so segments of the same tile that land
-// on different CTAs meet in Y with no fix-up pass, and the drain of one segment
-// overlaps the MMAs of the next.
+// (one set of two halves for 256-row tiles) and is folded into Y by TMA bulk reduce-adds,
+// so segments of the same tile that land on different CTAs meet in Y with no fix-up pass,
+// and (128-row tiles) the drain of one segment overlaps the MMAs of the next.
 //
-//   warp 0     TMA producer: weight tile + activation tile of each k-block into one stage
+//   warp 0     TMA producer: weight tile(s) + activation tile of each k-block into one stage
 //   warp 1     MMA issuer (one thread): tcgen05.mma kind::f16, fp32 accumulators in TMEM,
 //              one tcgen05.commit per k-block to free its stage
 //   warp 2     TMEM owner (alloc/dealloc)
-//   warps 3-6  epilogue: tcgen05.ld -> 16-row shared tile -> cp.reduce.async.bulk add
+//   warps 3-   epilogue, four warps per 128-row half: tcgen05.ld -> 16-row shared tile ->
+//              cp.reduce.async.bulk add
 //
 // For the model's fixed weights it is launched as a programmatic dependent of the previous
 // kernel in the stream: the producer fills the first pipeline stages with weight tiles (which
@@ -49,8 +54,16 @@ constexpr int A_STAGE = BM * BK * 2;   // 16 KB
 constexpr int EPI_ROWS = 16;     // token rows per reduce-add tile
 constexpr int EPI_COLS = 32;     // weight rows per reduce-add tile: one epilogue warp's TMEM lane quarter
 constexpr int EPI_BYTES = EPI_ROWS * BM * 4;  // 8 KB: the four warps' tiles, double buffered
-constexpr int kWarps = 7;
-constexpr int kThreads = kWarps * 32;
+// MW weight tiles of 128 rows share each k-block's activation tile (MW = 2: two M = 128 MMAs
+// per K step into two accumulators). Warps: producer, MMA issuer, TMEM owner, then four
+// epilogue warps per 128-row half. With MW = 2 the two accumulators of up to 256 columns fill
+// the TMEM, so there is one accumulator set instead of two alternating ones.
+template <int MW>
+struct Wide {
+  static constexpr int kWarps = 3 + 4 * MW;
+  static constexpr int kThreads = kWarps * 32;
+  static constexpr int kAcc = MW == 1 ? 2 : 1;   // accumulator sets
+};
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
 __device__ int g_tc_timeout = 0;
@@ -165,16 +178,20 @@ __device__ __forceinline__ void tmem_wait16(uint32_t* r) {
                : "memory");
 }
 
-// named barrier of the four epilogue warps
-__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// named barrier of the N epilogue threads
+template <int N>
+__device__ __forceinline__ void epi_bar() {
+  asm volatile("bar.sync 1, %0;" ::"n"(N) : "memory");
+}
 
-// same barrier with an AND over the 128 epilogue threads: all of them take the same branch
+// same barrier with an AND over the N epilogue threads: all of them take the same branch
+template <int N>
 __device__ __forceinline__ bool epi_all(bool v) {
   uint32_t r;
   asm volatile(
-      "{\n .reg .pred p, q;\n setp.ne.u32 q, %1, 0;\n bar.red.and.pred p, 1, 128, q;\n selp.u32 %0, 1, 0, p;\n}\n"
+      "{\n .reg .pred p, q;\n setp.ne.u32 q, %1, 0;\n bar.red.and.pred p, 1, %2, q;\n selp.u32 %0, 1, 0, p;\n}\n"
       : "=r"(r)
-      : "r"((uint32_t)v)
+      : "r"((uint32_t)v), "n"(N)
       : "memory");
   return r != 0;
 }
@@ -185,7 +202,7 @@ struct TcParams {
   int BN;            // token rows per tile (multiple of 16, <= 256)
   int S;             // pipeline stages (one k-block of weights + activations each)
   int nkb;           // k-blocks per tile
-  int m_tiles;       // weight-row tiles
+  int m_tiles;       // weight-row tiles (of 128 MW rows)
   int total;         // tiles * nkb work units (< 2^31, checked on the host)
   uint32_t ab_fmt;   // operand format of both A and B: 1 = bf16, 0 = fp16
   uint32_t tmem_cols;
@@ -212,17 +229,20 @@ __device__ __forceinline__ bool next_seg(Seg& s, int hi, int nkb) {
 
 // PACKED: weight tiles come from the pre-swizzled tile copy by one contiguous 16 KB bulk
 // copy each (sequential DRAM pages); otherwise by a 2-D tensor copy of the [N][K] matrix.
-template <bool PACKED>
-__global__ void __launch_bounds__(kThreads, 1)
+template <bool PACKED, int MW>
+__global__ void __launch_bounds__(Wide<MW>::kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_x,
                    const __grid_constant__ CUtensorMap map_y, const TcParams p) {
+  static_assert(PACKED || MW == 1, "wide tiles take the packed weights");
+  constexpr int kAcc = Wide<MW>::kAcc;
+  constexpr int kEpi = 128 * MW;   // epilogue threads
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int b_stage = p.BN * BK * 2;
-  const int stage = A_STAGE + b_stage;                        // one k-block: weight tile, then activation tile
+  const int stage = MW * A_STAGE + b_stage;                   // one k-block: MW weight tiles, then activation tile
   uint8_t* ring = smem;
-  uint8_t* epi = ring + p.S * stage;                          // [2][16][128] fp32
-  uint64_t* bars = reinterpret_cast<uint64_t*>(epi + 2 * EPI_BYTES);
+  uint8_t* epi = ring + p.S * stage;                          // [4 MW warps][2][16][32] fp32
+  uint64_t* bars = reinterpret_cast<uint64_t*>(epi + 2 * MW * EPI_BYTES);
   uint64_t* full = bars;
   uint64_t* empty = full + p.S;
   uint64_t* acc_full = empty + p.S;        // [2]
@@ -243,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(acc_full + i), 1);
-      mbar_init(smem_u32(acc_empty + i), 4);   // one arrival per epilogue warp
+      mbar_init(smem_u32(acc_empty + i), 4 * MW);   // one arrival per epilogue warp
     }
     mbar_init(smem_u32(mma_done), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -278,7 +298,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t fb = smem_u32(full + i), dst = smem_u32(ring + i * stage);
         mbar_expect_tx(fb, stage);
         if (PACKED)
-          bulk_load(dst, p.w_packed + ((size_t)m2 * p.nkb + k2) * A_STAGE, A_STAGE, fb, pol_w);
+#pragma unroll
+          for (int h = 0; h < MW; ++h)
+            bulk_load(dst + h * A_STAGE, p.w_packed + ((size_t)(m2 * MW + h) * p.nkb + k2) * A_STAGE, A_STAGE, fb,
+                      pol_w);
         else
           tma_load_2d(dst, &map_w, k2 * BK, m2 * BM, fb, pol_w);
         if (++k2 == p.nkb) {
@@ -290,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;");   // the next kernel may launch and wait for us
     for (int i = 0; i < pre; ++i) {
-      tma_load_2d(smem_u32(ring + i * stage) + A_STAGE, &map_x, kb * BK, tt * p.BN, smem_u32(full + i), pol_x);
+      tma_load_2d(smem_u32(ring + i * stage) + MW * A_STAGE, &map_x, kb * BK, tt * p.BN, smem_u32(full + i), pol_x);
       ++issued;
       if (++st == p.S) {
         st = 0;
@@ -313,10 +336,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t dst = smem_u32(ring + st * stage);
       mbar_expect_tx(fb, stage);
       if (PACKED)
-        bulk_load(dst, p.w_packed + ((size_t)mt * p.nkb + kb) * A_STAGE, A_STAGE, fb, pol_w);
+#pragma unroll
+        for (int h = 0; h < MW; ++h)
+          bulk_load(dst + h * A_STAGE, p.w_packed + ((size_t)(mt * MW + h) * p.nkb + kb) * A_STAGE, A_STAGE, fb, pol_w);
       else
         tma_load_2d(dst, &map_w, kb * BK, mt * BM, fb, pol_w);
-      tma_load_2d(dst + A_STAGE, &map_x, kb * BK, tt * p.BN, fb, pol_x);
+      tma_load_2d(dst + MW * A_STAGE, &map_x, kb * BK, tt * p.BN, fb, pol_x);
       ++issued;
       if (++st == p.S) {
         st = 0;
@@ -340,13 +365,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t ph = 0;
     bool stop = false;
     while (!stop && next_seg(sg, hi, p.nkb)) {
-      const int ab = s & 1;
-      if (s_abort || !mbar_wait(smem_u32(acc_empty + ab), (uint32_t)((s >> 1) & 1) ^ 1)) {
+      const int ab = kAcc == 2 ? (s & 1) : 0;
+      const uint32_t use = kAcc == 2 ? (uint32_t)(s >> 1) : (uint32_t)s;   // earlier uses of this accumulator set
+      if (s_abort || !mbar_wait(smem_u32(acc_empty + ab), (use & 1) ^ 1)) {
         s_abort = 1;
         break;
       }
       asm volatile("tcgen05.fence::after_thread_sync;");
-      const uint32_t d_tmem = tmem + ab * p.BN;
+      const uint32_t d_tmem = tmem + ab * MW * p.BN;   // half h at + h BN
       for (int g = sg.g; g < sg.end; ++g) {
         if (s_abort || !mbar_wait(smem_u32(full + st), ph)) {
           s_abort = 1;
@@ -355,11 +381,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         asm volatile("tcgen05.fence::after_thread_sync;");
         const uint32_t a_base = smem_u32(ring + st * stage);
-        const uint32_t b_base = a_base + A_STAGE;
+        const uint32_t b_base = a_base + MW * A_STAGE;
 #pragma unroll
-        for (int k = 0; k < BK / UMMA_K; ++k)
-          umma_bf16(d_tmem, smem_desc_sw128(a_base + k * UMMA_K * 2), smem_desc_sw128(b_base + k * UMMA_K * 2),
-                    idesc, (g != sg.g || k != 0) ? 1u : 0u);
+        for (int h = 0; h < MW; ++h)
+#pragma unroll
+          for (int k = 0; k < BK / UMMA_K; ++k)
+            umma_bf16(d_tmem + h * p.BN, smem_desc_sw128(a_base + h * A_STAGE + k * UMMA_K * 2),
+                      smem_desc_sw128(b_base + k * UMMA_K * 2), idesc, (g != sg.g || k != 0) ? 1u : 0u);
         umma_commit(smem_u32(empty + st));  // the stage is free once these MMAs retire
         if (++st == p.S) {
           st = 0;
@@ -372,24 +400,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     umma_commit(smem_u32(mma_done));          // fires once every MMA of this CTA has retired
     mbar_wait(smem_u32(mma_done), 0);
   } else if (warp >= 3) {
-    // ---------------- epilogue: TMEM -> [16 tokens][128 rows] fp32 tile -> bulk reduce-add into Y
+    // ---------------- epilogue: TMEM -> [16 tokens][32 rows] fp32 tiles -> bulk reduce-add into Y
+    const int e = warp - 3;                    // epilogue warp: 128-row half e / 4
+    const int hw = e >> 2;
     const int q = warp & 3;                    // TMEM lane quarter this warp may access
     const bool leader = (warp == 3 && lane == 0);
     float* stg = reinterpret_cast<float*>(epi);
     asm volatile("griddepcontrol.wait;" ::: "memory");   // Y is written by earlier kernels
     if (p.tile_ready) {
-      // zero the tiles whose first k-block is in this CTA's range: 32 threads per row of 128
+      // zero the tiles whose first k-block is in this CTA's range: 32 MW threads per row of 128 MW
       // columns (16-byte stores), 4 rows per pass; then publish them
-      const int ep = threadIdx.x - 3 * 32;   // 0..127
+      const int ep = threadIdx.x - 3 * 32;   // 0 .. 128 MW - 1
       const int t_tiles_bn = p.BN;
       for (int tile = (lo + p.nkb - 1) / p.nkb; tile * p.nkb < hi; ++tile) {
-        const int m0 = (tile % p.m_tiles) * BM, t0 = (tile / p.m_tiles) * t_tiles_bn;
+        const int m0 = (tile % p.m_tiles) * BM * MW, t0 = (tile / p.m_tiles) * t_tiles_bn;
         const int rows = min(t_tiles_bn, p.T - t0);
-        for (int rr = ep >> 5; rr < rows; rr += 4)
-          reinterpret_cast<float4*>(p.Y + (size_t)(t0 + rr) * p.N + m0)[ep & 31] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int rr = ep / (32 * MW); rr < rows; rr += 4)
+          reinterpret_cast<float4*>(p.Y + (size_t)(t0 + rr) * p.N + m0)[ep % (32 * MW)] = make_float4(0.f, 0.f, 0.f, 0.f);
       }
       __threadfence();
-      epi_bar();
+      epi_bar<kEpi>();
       if (leader)
         for (int tile = (lo + p.nkb - 1) / p.nkb; tile * p.nkb < hi; ++tile)
           asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p.tile_ready + tile), "r"(p.epoch) : "memory");
@@ -397,16 +427,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     Seg sg{0, lo, 0};
     int s = 0, buf = 0;
     while (next_seg(sg, hi, p.nkb)) {
-      const int ab = s & 1;
-      bool ok = !s_abort && mbar_wait(smem_u32(acc_full + ab), (uint32_t)((s >> 1) & 1));
-      ok = epi_all(ok);
+      const int ab = kAcc == 2 ? (s & 1) : 0;
+      const uint32_t use = kAcc == 2 ? (uint32_t)(s >> 1) : (uint32_t)s;
+      bool ok = !s_abort && mbar_wait(smem_u32(acc_full + ab), use & 1);
+      ok = epi_all<kEpi>(ok);
       if (!ok) {
         s_abort = 1;
         break;
       }
       asm volatile("tcgen05.fence::after_thread_sync;");
-      const int m0 = (sg.tile % p.m_tiles) * BM, t0 = (sg.tile / p.m_tiles) * p.BN;
-      const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + ab * p.BN;
+      const int m0 = (sg.tile % p.m_tiles) * BM * MW + hw * BM, t0 = (sg.tile / p.m_tiles) * p.BN;
+      const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + (ab * MW + hw) * p.BN;
       if (p.tile_ready && lane == 0) {
         // the tile's zeroing (by the CTA holding its first k-block) has landed
         const unsigned long long w0 = gtimer();
@@ -425,7 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Each warp drains its own 32 weight rows on its own: 16 token columns per step from TMEM
       // (the next step's load in flight while this one is staged) into its [16][32] fp32 tile,
       // bulk reduce-added into Y by the warp's first lane, two tiles alternating.
-      float* W = stg + q * (2 * EPI_ROWS * EPI_COLS);
+      float* W = stg + e * (2 * EPI_ROWS * EPI_COLS);
       uint32_t cur[16], nxt[16];
       tmem_ld16_async(taddr, cur);
       tmem_wait16(cur);
@@ -537,6 +568,14 @@ int pick_bn(int T) {
   return std::max(16, (T + 15) / 16 * 16);
 }
 
+// Weight tiles per activation tile: 2 (256 weight rows) for the packed layout from 1024 token
+// rows on, when N holds whole 256-row tiles. There the GEMM is compute-bound over 4 or more
+// token tiles, and each 16 KB weight k-block would bring a 32 KB activation k-block into the SM
+// with it: measured on the 8B link shapes, 5120-5184 rows run 6-9 % faster this way and 2048
+// rows (a compile call) 5 %, while 224 and 384 rows run 9 % and 6 % slower (their single
+// accumulator set serialises each drain with the next segment).
+int pick_mw(bool packed, int N, int T) { return packed && N % (2 * BM) == 0 && T >= 1024 ? 2 : 1; }
+
 int device_sms() {
   static int sms[64] = {};
   int dev = 0;
@@ -571,16 +610,17 @@ pic_status tc_gemm_launch(const void* W, bool packed, const void* X, float* Y, i
   p.T = T;
   p.BN = pick_bn(T);
   p.nkb = K / BK;
-  p.m_tiles = N / BM;
+  const int wide = pick_mw(packed, N, T);   // weight tiles per activation tile
+  p.m_tiles = N / (BM * wide);
   const long long tiles = (long long)p.m_tiles * ((T + p.BN - 1) / p.BN);
   if (tiles * p.nkb >= (1LL << 31)) return fail(PIC_ERR_UNSUPPORTED, "tcgen05 gemm: shape too large");
   p.total = (int)(tiles * p.nkb);
   const int b_stage = p.BN * BK * 2;
-  // shared memory: as many stages as fit next to the two epilogue tiles and the barriers
-  const int budget = 227 * 1024 - 1024 - 2 * EPI_BYTES - 512;
-  p.S = std::min(12, budget / (A_STAGE + b_stage));
+  // shared memory: as many stages as fit next to the epilogue tiles and the barriers
+  const int budget = 227 * 1024 - 1024 - 2 * wide * EPI_BYTES - 512;
+  p.S = std::min(12, budget / (wide * A_STAGE + b_stage));
   if (p.S < 2) return fail(PIC_ERR_UNSUPPORTED, "tcgen05 gemm: pipeline does not fit shared memory");
-  p.tmem_cols = 32;
+  p.tmem_cols = 32;   // two accumulator sets of one BN-column tile, or one set of two (wide = 2)
   while ((int)p.tmem_cols < 2 * p.BN) p.tmem_cols <<= 1;
   CUtensorMap mw, mx, my;
   std::memset(&mw, 0, sizeof(mw));
@@ -588,20 +628,22 @@ pic_status tc_gemm_launch(const void* W, bool packed, const void* X, float* Y, i
       !make_map_f32(&my, Y, T, N))
     return fail(PIC_ERR_CUDA, "cuTensorMapEncodeTiled failed");
   const size_t smem =
-      1024 + (size_t)p.S * (A_STAGE + b_stage) + 2 * EPI_BYTES + (2 * p.S + 6) * 8 + 16;
+      1024 + (size_t)p.S * (wide * A_STAGE + b_stage) + 2 * wide * EPI_BYTES + (2 * p.S + 6) * 8 + 16;
   int dev = 0;
   cudaGetDevice(&dev);
-  static size_t attr_smem[2][64] = {};
-  auto kern = packed ? tc_gemm_kernel<true> : tc_gemm_kernel<false>;
-  if (dev < 0 || dev >= 64 || attr_smem[packed][dev] < smem) {
+  static size_t attr_smem[3][64] = {};
+  const int variant = packed ? wide : 0;
+  auto kern = !packed ? tc_gemm_kernel<false, 1> : wide == 2 ? tc_gemm_kernel<true, 2> : tc_gemm_kernel<true, 1>;
+  const int threads = wide == 2 ? Wide<2>::kThreads : Wide<1>::kThreads;
+  if (dev < 0 || dev >= 64 || attr_smem[variant][dev] < smem) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return fail(PIC_ERR_CUDA, std::string("tcgen05 gemm attribute: ") + cudaGetErrorString(e));
-    if (dev >= 0 && dev < 64) attr_smem[packed][dev] = smem;
+    if (dev >= 0 && dev < 64) attr_smem[variant][dev] = smem;
   }
   const int grid = std::min(device_sms(), p.total);
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(threads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cudaLaunchAttribute at[1];
@@ -626,7 +668,9 @@ pic_status tc_gemm_run_packed(const void* Wp, const void* X, float* Y, int N, in
   return tc_gemm_launch(Wp, true, X, Y, N, K, T, st, early_weights, tile_ready, epoch);
 }
 
-size_t tc_gemm_tiles(int N, int T) { return (size_t)(N / BM) * ((T + pick_bn(T) - 1) / pick_bn(T)); }
+size_t tc_gemm_tiles(int N, int T) {   // of the packed layout's launch
+  return (size_t)(N / (BM * pick_mw(true, N, T))) * ((T + pick_bn(T) - 1) / pick_bn(T));
+}
 
 pic_status tc_pack_weight(const void* W, void* out, int N, int K, cudaStream_t st) {
   if (!tc_gemm_supported(N, K, 1)) return fail(PIC_ERR_UNSUPPORTED, "pack: N % 128 and K % 64 must be 0");
