@@ -563,9 +563,11 @@ bool make_map(CUtensorMap* m, const void* base, int rows, int K, int box_rows, b
   return r == CUDA_SUCCESS;
 }
 
+// Token rows per tile: the fewest tiles of at most 256 rows, of equal height rounded up to 16
+// (1632 rows: 7 tiles of 240 rather than 6 of 256 and one of 96, which would pad the MMAs by 10 %)
 int pick_bn(int T) {
-  if (T >= 256) return 256;
-  return std::max(16, (T + 15) / 16 * 16);
+  const int n = std::max(1, (T + 255) / 256);
+  return std::max(16, ((T + n - 1) / n + 15) / 16 * 16);
 }
 
 // Weight tiles per activation tile: 2 (256 weight rows) for the packed layout from 1024 token
