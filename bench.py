@@ -488,7 +488,7 @@ def run_ours(args):
                             "link over the chosen rows and the query; against the LegoLink-16 step above",
                     **dyn, "static_ms_per_step": ms_step, "ratio_to_static": dyn["ms_per_step"] / ms_step},
         "decode": {"what": "pic_decode after the link: one generated token per request per step, attending to "
-                           "the request's linked KV (RoPE at load)",
+                           "the request's linked KV (RoPE inside the attention)",
                    "requests": n_r, "steps": args.steps, "ms_per_step": dec_ms / args.steps,
                    "tokens_per_s": job_throughput(n_r * args.steps, world, dec_ms / 1e3),
                    "roofline_ms": dec_roof_ms, "frac": dec_roof_ms / (dec_ms / args.steps),

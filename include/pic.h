@@ -223,7 +223,7 @@ pic_status pic_link_dynamic(pic_store* s, const pic_link_request* reqs, int32_t 
  * free id, requests in call order; the block joins the request's private blocks and page
  * table); its query attends causally to every row of the request's pages -- the reused and
  * recomputed chunk rows, the query rows, earlier decoded rows -- and to itself, with RoPE
- * applied at load from each key's absolute position, as in link.
+ * applied inside the attention at each key's absolute position, as in link.
  * Requests must be distinct and alive. n_reqs <= max_requests, max_rows and max_logit_rows;
  * each request's new length <= max_positions (else PIC_ERR_CAPACITY). PIC_ERR_OUT_OF_BLOCKS
  * when the pool cannot give every request that needs one a new block; then nothing changes.
