@@ -297,10 +297,13 @@ void plan_attention(const AttnPlanInput& in, std::vector<AttnItem>& items, std::
   // Persistent kernel: CTA c of n = min(items, SMs) takes items c, c + n, c + 2n, ...; the sorted
   // items are dealt in snake order (round k runs over the CTAs backwards when k is odd). Parts are
   // whole 64-key tiles (4 pages). The part size is the one, among those giving about 1, 1.5, 2,
-  // 3 or 4 items per SM, whose deal has the smallest estimated makespan, then the fewest items.
-  // Estimated cost of an item: per 64-key tile one unit for loading and transforming it plus one
-  // per MMA tile that takes part (rows 0-31 up to page_mid, rows 32-63 throughout), and four
-  // units of fixed cost (Q load, O drain).
+  // 3 or 4 items per SM, with the smallest estimate, then the fewest items. The estimate is the
+  // deal's makespan plus the split merge: each part's fp16 partial is written by its item and
+  // read back by the merge kernel, which runs over all SMs, kMergeCost units per part per SM
+  // (one unit ~ one key tile's load). Estimated cost of an item: per 64-key tile one unit for
+  // loading it plus one per MMA tile that takes part (rows 0-31 up to page_mid, rows 32-63
+  // throughout), and four units of fixed cost (Q load, O drain).
+  constexpr long long kMergeCost = 5;
   auto cost = [](const AttnItem& it) -> long long {
     const int nt = (it.page1 - it.page0 + 3) / 4;
     const int n0 = std::max(0, (it.page_mid - it.page0 + 3) / 4), n1 = it.nrows > 32 ? nt : 0;
@@ -331,9 +334,9 @@ void plan_attention(const AttnPlanInput& in, std::vector<AttnItem>& items, std::
     std::vector<AttnCombine> cbs;
     int nparts = 0;
     build(P, its, cbs, nparts);
-    const long long span = deal(its);
-    if (best < 0 || span < best || (span == best && its.size() < items.size())) {
-      best = span;
+    const long long est = deal(its) * std::max(1, in.num_sms) + kMergeCost * nparts;
+    if (best < 0 || est < best || (est == best && its.size() < items.size())) {
+      best = est;
       best_P = P;
       items.swap(its);
       combines.swap(cbs);

@@ -5,7 +5,8 @@ attention is only right if every page a block can see is read exactly once and e
 run's partial result is merged exactly once; these invariants are checked on link, decode and
 compile-shaped batches, ragged and random, for each kernel family's shape. The part-size rule
 of the persistent kernel (a few candidate sizes, the one whose snake deal over the CTAs has
-the smallest estimated makespan) is restated here independently and compared item by item.
+the smallest estimated makespan plus merge cost) is restated here independently and compared
+item by item.
 """
 
 import numpy as np
@@ -182,7 +183,7 @@ def model_plan(seqs, G, rb, num_sms, persistent):
                     p0, p1 = pb + s * P, min(pe, pb + (s + 1) * P)
                     items.append((row0, n, g, p0, p1, parts + s, min(p1, max(p0, pe0))))
                 parts += ns
-        return sorted(items, key=lambda it: -(it[4] - it[3]))   # stable: heaviest first
+        return sorted(items, key=lambda it: -(it[4] - it[3])), parts   # stable: heaviest first
 
     def cost(it):
         """Per 64-key tile: 1 + the MMA tiles taking part (rows 0-31 up to page_mid, rows 32-63
@@ -194,7 +195,7 @@ def model_plan(seqs, G, rb, num_sms, persistent):
 
     if not persistent:
         target = max(1, (4 * num_sms) // G)
-        return build(max(4, -(-total // target)))
+        return build(max(4, -(-total // target)))[0]
 
     def snake(items):
         n = min(len(items), num_sms)
@@ -211,9 +212,11 @@ def model_plan(seqs, G, rb, num_sms, persistent):
     for per_sm in (1, 1.5, 2, 3, 4):
         want = max(1, int(per_sm * 2) * num_sms // 2)
         P = (max(8, -(-total * G // want)) + 3) // 4 * 4
-        dealt, span = snake(build(P))
-        if best is None or (span, len(dealt)) < (best[0], len(best[1])):
-            best = (span, dealt)
+        items, parts = build(P)
+        dealt, span = snake(items)
+        est = span * num_sms + 5 * parts   # makespan + 5 units per split part over the SMs (the merge)
+        if best is None or (est, len(dealt)) < (best[0], len(best[1])):
+            best = (est, dealt)
     return best[1]
 
 
@@ -250,8 +253,9 @@ def test_plan_rejects_bad_input_and_reports_sizes(lib):
     def call(sr, sp, r, p, num_sms=152):
         return lib.pic_op_attention_plan(L.PIC_BF16, 32, 8, 128, 1, P(sr), P(sp), P(r), P(p), num_sms,
                                          None, 0, None, 0, P(counts))
-    # output arrays too small: the sizes are reported for a second call
-    assert call(seq_rows, seq_pages, rp, pp) == L.PIC_ERR_CAPACITY and counts.tolist() == [296, 32, 296]
+    # output arrays too small: the sizes are reported for a second call (the c2 link: 4 blocks x 8
+    # KV heads in 52-page parts, 168 items, all of them split)
+    assert call(seq_rows, seq_pages, rp, pp) == L.PIC_ERR_CAPACITY and counts.tolist() == [168, 32, 168]
     bad = rp.copy()
     bad[5] = bad[4]                                            # row positions must ascend
     assert call(seq_rows, seq_pages, bad, pp) == L.PIC_ERR_INVALID_ARG
