@@ -296,18 +296,21 @@ void plan_attention(const AttnPlanInput& in, std::vector<AttnItem>& items, std::
   }
   // Persistent kernel: CTA c of n = min(items, SMs) takes items c, c + n, c + 2n, ...; the sorted
   // items are dealt in snake order (round k runs over the CTAs backwards when k is odd). Parts are
-  // whole 64-key tiles (4 pages). The part size is the one, among those giving about 1, 1.5, 2,
-  // 3 or 4 items per SM, with the smallest estimate, then the fewest items. The estimate is the
-  // deal's makespan plus the split merge: each part's fp16 partial is written by its item and
-  // read back by the merge kernel, which runs over all SMs, kMergeCost units per part per SM
-  // (one unit ~ one key tile's load). Estimated cost of an item: per 64-key tile one unit for
-  // loading it plus one per MMA tile that takes part (rows 0-31 up to page_mid, rows 32-63
-  // throughout), and four units of fixed cost (Q load, O drain).
-  constexpr long long kMergeCost = 5;
+  // whole 64-key tiles (4 pages). Candidate part sizes, for about 1, 1.5, 2, 3 and 4 items per
+  // SM: the size from the average page count, and the smallest size whose item count does not
+  // exceed the target (blocks seldom divide evenly: at the 8B 10 x 512 link the first gives 168
+  // items for 152 SMs, the second exactly 152). The candidate with the smallest estimate is
+  // taken (then the fewest items, then the smaller size). The estimate is the deal's makespan
+  // times the SM count plus kMergeCost per split part: each part's fp16 partial is written by its
+  // item and read back by the merge kernel, which runs over all SMs. An item's cost, in units of
+  // 0.01 us, is a fit of this kernel's per-CTA globaltimer traces on GB300: 26 per 64-key tile,
+  // 33 per MMA tile that takes part in it (rows 0-31 up to page_mid, rows 32-63 throughout), and
+  // 491 per item (Q load, pipeline fill, O drain).
+  constexpr long long kMergeCost = 150;
   auto cost = [](const AttnItem& it) -> long long {
     const int nt = (it.page1 - it.page0 + 3) / 4;
     const int n0 = std::max(0, (it.page_mid - it.page0 + 3) / 4), n1 = it.nrows > 32 ? nt : 0;
-    return nt + n0 + n1 + 4;
+    return 26LL * nt + 33LL * (n0 + n1) + 491;
   };
   auto deal = [&](std::vector<AttnItem>& its) -> long long {
     const int n = std::min<int>((int)its.size(), std::max(1, in.num_sms));
@@ -324,12 +327,25 @@ void plan_attention(const AttnPlanInput& in, std::vector<AttnItem>& items, std::
     its.swap(dealt);
     return *std::max_element(load.begin(), load.end());
   };
-  long long best = -1;
-  int best_P = 0;
+  int max_pages = 1;
+  for (const Blk& b : blks) max_pages = std::max(max_pages, b.pe - b.pb);
+  auto n_items_of = [&](int P) {
+    long long n = 0;
+    for (const Blk& b : blks) n += std::max(1, (b.pe - b.pb + P - 1) / P);
+    return n * G;
+  };
+  std::vector<int> cands;
   for (const int twice_per_sm : {2, 3, 4, 6, 8}) {
     const long long want = std::max<long long>(1, (long long)twice_per_sm * std::max(1, in.num_sms) / 2);
-    const int P = (int)((std::max<long long>(8, (total * G + want - 1) / want) + 3) / 4 * 4);
-    if (P == best_P) continue;
+    int P = (int)((std::max<long long>(8, (total * G + want - 1) / want) + 3) / 4 * 4);
+    cands.push_back(P);
+    while (n_items_of(P) > want && P < max_pages) P += 4;
+    cands.push_back(P);
+  }
+  std::sort(cands.begin(), cands.end());
+  cands.erase(std::unique(cands.begin(), cands.end()), cands.end());
+  long long best = -1;
+  for (const int P : cands) {
     std::vector<AttnItem> its;
     std::vector<AttnCombine> cbs;
     int nparts = 0;
@@ -337,7 +353,6 @@ void plan_attention(const AttnPlanInput& in, std::vector<AttnItem>& items, std::
     const long long est = deal(its) * std::max(1, in.num_sms) + kMergeCost * nparts;
     if (best < 0 || est < best || (est == best && its.size() < items.size())) {
       best = est;
-      best_P = P;
       items.swap(its);
       combines.swap(cbs);
       n_parts = nparts;

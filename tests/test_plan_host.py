@@ -186,12 +186,12 @@ def model_plan(seqs, G, rb, num_sms, persistent):
         return sorted(items, key=lambda it: -(it[4] - it[3])), parts   # stable: heaviest first
 
     def cost(it):
-        """Per 64-key tile: 1 + the MMA tiles taking part (rows 0-31 up to page_mid, rows 32-63
-        throughout), plus 4 per item."""
+        """In 0.01 us: 26 per 64-key tile, 33 per MMA tile taking part in it (rows 0-31 up to
+        page_mid, rows 32-63 throughout), 491 per item."""
         nt = (it[4] - it[3] + 3) // 4
         n0 = max(0, (it[6] - it[3] + 3) // 4)
         n1 = nt if it[1] > 32 else 0
-        return nt + n0 + n1 + 4
+        return 26 * nt + 33 * (n0 + n1) + 491
 
     if not persistent:
         target = max(1, (4 * num_sms) // G)
@@ -208,13 +208,24 @@ def model_plan(seqs, G, rb, num_sms, persistent):
                 load[c] += cost(it)
         return dealt, max(load)
 
-    best = None
+    max_pages = max([pe - pb for _, _, pb, pe, _ in blocks] + [1])
+
+    def n_items(P):
+        return G * sum(max(1, -(-(pe - pb) // P)) for _, _, pb, pe, _ in blocks)
+
+    cands = set()
     for per_sm in (1, 1.5, 2, 3, 4):
         want = max(1, int(per_sm * 2) * num_sms // 2)
-        P = (max(8, -(-total * G // want)) + 3) // 4 * 4
+        P = (max(8, -(-total * G // want)) + 3) // 4 * 4   # from the average page count
+        cands.add(P)
+        while n_items(P) > want and P < max_pages:           # the smallest size that fits the target
+            P += 4
+        cands.add(P)
+    best = None
+    for P in sorted(cands):
         items, parts = build(P)
         dealt, span = snake(items)
-        est = span * num_sms + 5 * parts   # makespan + 5 units per split part over the SMs (the merge)
+        est = span * num_sms + 150 * parts   # makespan + the merge (150 per split part, over the SMs)
         if best is None or (est, len(dealt)) < (best[0], len(best[1])):
             best = (est, dealt)
     return best[1]
@@ -254,8 +265,8 @@ def test_plan_rejects_bad_input_and_reports_sizes(lib):
         return lib.pic_op_attention_plan(L.PIC_BF16, 32, 8, 128, 1, P(sr), P(sp), P(r), P(p), num_sms,
                                          None, 0, None, 0, P(counts))
     # output arrays too small: the sizes are reported for a second call (the c2 link: 4 blocks x 8
-    # KV heads in 52-page parts, 168 items, all of them split)
-    assert call(seq_rows, seq_pages, rp, pp) == L.PIC_ERR_CAPACITY and counts.tolist() == [168, 32, 168]
+    # KV heads in 56-page parts, 152 items for 152 SMs, all of them split)
+    assert call(seq_rows, seq_pages, rp, pp) == L.PIC_ERR_CAPACITY and counts.tolist() == [152, 32, 152]
     bad = rp.copy()
     bad[5] = bad[4]                                            # row positions must ascend
     assert call(seq_rows, seq_pages, bad, pp) == L.PIC_ERR_INVALID_ARG
