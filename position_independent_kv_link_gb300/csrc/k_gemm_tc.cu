@@ -214,6 +214,30 @@ struct TcParams {
   float* Y;          // raw Y [T][N] (for the zeroing)
 };
 
+// The order a CTA walks its range [lo, hi). Every segment is drained (a full tile of reduce-adds)
+// whatever its length; with one accumulator set (256-row weight tiles) a drain holds up the next
+// segment's MMAs, and a range that ends with a segment shorter than the one it starts with would
+// finish with two drains back to back. Such a range is walked from the start m of its last
+// segment: [m, hi), then [lo, m), so the short segment's drain comes first, under the longer
+// segments' weight loads (measured: 32-request batch 80.0 -> 74.5 ms, full recompute 81.6 ->
+// 75.7 ms). With two accumulator sets the plain order is kept: there the reorder measured slower
+// (k = 32 7.07 -> 7.51 ms), as CTAs a token tile apart no longer reach a weight band together and
+// share it through L2. The producer, the MMA issuer and the epilogue walk the same order.
+struct Walk {
+  int a0, b0, a1, b1;   // units [a0, b0), then [a1, b1)
+};
+__device__ __forceinline__ Walk range_walk(int lo, int hi, int nkb, bool reorder) {
+  const int m = max(lo, (hi - 1) / nkb * nkb);          // first unit of the last segment
+  const int first_end = min(hi, (lo / nkb + 1) * nkb);  // end of the first segment
+  if (reorder && m > lo && hi - m < first_end - lo) return Walk{m, hi, lo, m};
+  return Walk{lo, hi, hi, hi};
+}
+// the i-th unit of the walk
+__device__ __forceinline__ int walk_unit(const Walk& w, int i) {
+  const int n0 = w.b0 - w.a0;
+  return i < n0 ? w.a0 + i : w.a1 + (i - n0);
+}
+
 // Segment walk shared by the MMA issuer and the epilogue: [g, end) inside one tile.
 struct Seg {
   int g, end;
@@ -254,6 +278,7 @@ __global__ void __launch_bounds__(Wide<MW>::kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int lo = (int)((long long)p.total * blockIdx.x / gridDim.x);
   const int hi = (int)((long long)p.total * (blockIdx.x + 1) / gridDim.x);
+  const Walk wk = range_walk(lo, hi, p.nkb, kAcc == 1);
 
   if (threadIdx.x == 0) {
     s_abort = 0;
@@ -281,53 +306,51 @@ __global__ void __launch_bounds__(Wide<MW>::kThreads, 1)
 
   if (warp == 0 && lane == 0) {
     // ---------------- TMA producer: weight tile (HBM stream, evicted first from L2) and
-    // activation tile (small, reused by every weight tile, kept in L2) of each k-block.
-    // Stage, phase and (tile, k-block) advance incrementally: no division in the loop.
+    // activation tile (small, reused by every weight tile, kept in L2) of each k-block, in the
+    // range's walk order.
     uint64_t pol_w, pol_x;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol_w));
     asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol_x));
     int st = 0, issued = 0;
     uint32_t ph = 0;
-    int tile = lo / p.nkb, kb = lo % p.nkb;
-    int mt = tile % p.m_tiles, tt = tile / p.m_tiles;
+    const int n_units = hi - lo;
     // weights of the first stages before the previous kernel has finished, then its outputs
-    const int pre = min(p.S, hi - lo);
-    {
-      int k2 = kb, m2 = mt;
-      for (int i = 0; i < pre; ++i) {
-        const uint32_t fb = smem_u32(full + i), dst = smem_u32(ring + i * stage);
-        mbar_expect_tx(fb, stage);
-        if (PACKED)
+    const int pre = min(p.S, n_units);
+    for (int i = 0; i < pre; ++i) {
+      const int u = walk_unit(wk, i), kb = u % p.nkb, mt = (u / p.nkb) % p.m_tiles;
+      const uint32_t fb = smem_u32(full + i), dst = smem_u32(ring + i * stage);
+      mbar_expect_tx(fb, stage);
+      if (PACKED)
 #pragma unroll
-          for (int h = 0; h < MW; ++h)
-            bulk_load(dst + h * A_STAGE, p.w_packed + ((size_t)(m2 * MW + h) * p.nkb + k2) * A_STAGE, A_STAGE, fb,
-                      pol_w);
-        else
-          tma_load_2d(dst, &map_w, k2 * BK, m2 * BM, fb, pol_w);
-        if (++k2 == p.nkb) {
-          k2 = 0;
-          if (++m2 == p.m_tiles) m2 = 0;
-        }
-      }
+        for (int h = 0; h < MW; ++h)
+          bulk_load(dst + h * A_STAGE, p.w_packed + ((size_t)(mt * MW + h) * p.nkb + kb) * A_STAGE, A_STAGE, fb,
+                    pol_w);
+      else
+        tma_load_2d(dst, &map_w, kb * BK, mt * BM, fb, pol_w);
     }
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;");   // the next kernel may launch and wait for us
     for (int i = 0; i < pre; ++i) {
+      const int u = walk_unit(wk, i), kb = u % p.nkb, tt = (u / p.nkb) / p.m_tiles;
       tma_load_2d(smem_u32(ring + i * stage) + MW * A_STAGE, &map_x, kb * BK, tt * p.BN, smem_u32(full + i), pol_x);
       ++issued;
       if (++st == p.S) {
         st = 0;
         ph ^= 1;
       }
-      if (++kb == p.nkb) {
-        kb = 0;
-        if (++mt == p.m_tiles) {
-          mt = 0;
-          ++tt;
-        }
-      }
     }
-    for (int g = lo + pre; g < hi; ++g) {
+    // (k-block, weight tile, token tile) of each unit advance incrementally: no division in the
+    // loop but at the walk's one jump between its two ranges
+    const int n0 = wk.b0 - wk.a0;
+    int kb = 0, mt = 0, tt = 0;
+    auto locate = [&](int u) {
+      kb = u % p.nkb;
+      const int tile = u / p.nkb;
+      mt = tile % p.m_tiles;
+      tt = tile / p.m_tiles;
+    };
+    if (pre < n_units) locate(walk_unit(wk, pre));
+    for (int i = pre; i < n_units; ++i) {
       if (s_abort || !mbar_wait(smem_u32(empty + st), ph ^ 1)) {
         s_abort = 1;
         break;
@@ -347,7 +370,9 @@ __global__ void __launch_bounds__(Wide<MW>::kThreads, 1)
         st = 0;
         ph ^= 1;
       }
-      if (++kb == p.nkb) {
+      if (i + 1 == n0) {
+        locate(wk.a1);
+      } else if (++kb == p.nkb) {
         kb = 0;
         if (++mt == p.m_tiles) {
           mt = 0;
@@ -360,11 +385,13 @@ __global__ void __launch_bounds__(Wide<MW>::kThreads, 1)
   } else if (warp == 1 && lane == 0) {
     // ---------------- MMA issuer: one commit per k-block releases its stage
     const uint32_t idesc = idesc_f16kind(BM, p.BN, p.ab_fmt);
-    Seg sg{0, lo, 0};
     int s = 0, st = 0;
     uint32_t ph = 0;
     bool stop = false;
-    while (!stop && next_seg(sg, hi, p.nkb)) {
+    for (int r = 0; r < 2 && !stop && !s_abort; ++r) {
+    Seg sg{0, r ? wk.a1 : wk.a0, 0};
+    const int seg_end = r ? wk.b1 : wk.b0;
+    while (!stop && next_seg(sg, seg_end, p.nkb)) {
       const int ab = kAcc == 2 ? (s & 1) : 0;
       const uint32_t use = kAcc == 2 ? (uint32_t)(s >> 1) : (uint32_t)s;   // earlier uses of this accumulator set
       if (s_abort || !mbar_wait(smem_u32(acc_empty + ab), (use & 1) ^ 1)) {
@@ -397,6 +424,7 @@ __global__ void __launch_bounds__(Wide<MW>::kThreads, 1)
       if (!stop) umma_commit(smem_u32(acc_full + ab));
       ++s;
     }
+    }
     umma_commit(smem_u32(mma_done));          // fires once every MMA of this CTA has retired
     mbar_wait(smem_u32(mma_done), 0);
   } else if (warp >= 3) {
@@ -424,15 +452,19 @@ __global__ void __launch_bounds__(Wide<MW>::kThreads, 1)
         for (int tile = (lo + p.nkb - 1) / p.nkb; tile * p.nkb < hi; ++tile)
           asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p.tile_ready + tile), "r"(p.epoch) : "memory");
     }
-    Seg sg{0, lo, 0};
     int s = 0, buf = 0;
-    while (next_seg(sg, hi, p.nkb)) {
+    bool quit = false;   // the same in all epilogue threads (set after epi_all)
+    for (int r = 0; r < 2 && !quit; ++r) {
+    Seg sg{0, r ? wk.a1 : wk.a0, 0};
+    const int seg_end = r ? wk.b1 : wk.b0;
+    while (next_seg(sg, seg_end, p.nkb)) {
       const int ab = kAcc == 2 ? (s & 1) : 0;
       const uint32_t use = kAcc == 2 ? (uint32_t)(s >> 1) : (uint32_t)s;
       bool ok = !s_abort && mbar_wait(smem_u32(acc_full + ab), use & 1);
       ok = epi_all<kEpi>(ok);
       if (!ok) {
         s_abort = 1;
+        quit = true;
         break;
       }
       asm volatile("tcgen05.fence::after_thread_sync;");
@@ -490,6 +522,7 @@ __global__ void __launch_bounds__(Wide<MW>::kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(acc_empty + ab));
       ++s;
+    }
     }
     if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
   }
