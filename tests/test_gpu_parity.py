@@ -42,13 +42,15 @@ def test_gemm_bf16_tcgen05(N, K, T):
 
 @pytest.mark.parametrize("N,K,T", [(128, 64, 1), (6144, 4096, 224), (384, 512, 300), (4096, 14336, 64),
                                    (1024, 256, 513), (256, 2048, 137), (512, 64, 129), (512, 256, 1100),
-                                   (256, 1024, 1024), (384, 128, 1500)])
+                                   (256, 1024, 1024), (384, 128, 1500), (1024, 4096, 1100)])
 def test_gemm_bf16_packed_weights(N, K, T):
     """The layout the model repacks its matrices into, through the packed tcgen05 path: (1024,
     256, 513) over three token tiles, (256, 2048, 137) two weight tiles split over 64 CTAs,
     (512, 64, 129) one k-block per tile; from 1024 token rows with 256-row weight tiles when N
     allows: (512, 256, 1100) over five token tiles (the last ragged), (256, 1024, 1024) one
-    weight tile; (384, 128, 1500) stays at 128 rows (N not a multiple of 256)."""
+    weight tile, (1024, 4096, 1100) ~8 k-blocks per CTA over 64-k-block tiles (ranges that end
+    with a shorter segment are walked from it); (384, 128, 1500) stays at 128 rows (N not a
+    multiple of 256)."""
     from position_independent_kv_link_gb300 import gemm_packed, pack_weight
     W = pi.randn((N, K), ("gemmWp", N, K), 0.05, torch.bfloat16)
     X = pi.randn((T, K), ("gemmXp", T, K), 1.0, torch.float16)
